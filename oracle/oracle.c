@@ -1,0 +1,304 @@
+/*
+ * oracle.c -- CPU oracle for the routed MoE SwiGLU feed-forward forward pass.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the tests, the smoke check and
+ * the benchmark's cpu_baseline / reference legs may load this library.  It
+ * shares no code with the CUDA path (no headers, tables or helpers).
+ *
+ * Everything here is deliberately plain: fp64 arithmetic, straight loops in
+ * the order the method states them, OpenMP only across independent tokens.
+ *
+ * Sources (page titles and sections):
+ *  - "Prime Flash MoE - Faster MoE Kernels optimized for Blackwell", sec. 1
+ *    "The computation": per routed (token, expert) pair, gate_up = W1[e] x_t
+ *    with W1 output-major, gate = first H outputs, up = last H outputs
+ *    (chunk(2)), act = silu(gate) * up, y = W2[e] act, and the routing weight
+ *    is applied to y before the top-k outputs are summed into out[t].
+ *  - same page, sec. 5 "The two epilogues": act is rounded to bf16 before the
+ *    down projection; sec. 7 "The MXFP8 variant", "The epilogue also
+ *    quantizes": in MXFP8 mode act is requantized to e4m3 with one e8m0
+ *    scale per 32 contiguous elements along H.
+ *  - "Porting Block-Scaled GEMM Kernels from Blackwell to Rubin", sec. 6.2:
+ *    on sm_100/sm_103 the scale byte is obtained by rounding amax/448 up to
+ *    a power of two (cvt.rp ... ue8m0), then values are multiplied by the
+ *    reciprocal scale and converted to e4m3 with round-to-nearest-even and
+ *    saturation.
+ *  - OCP Microscaling (MX) format: E4M3 is bias 7, no infinities, S.1111.111
+ *    is NaN, max finite 448, subnormal step 2^-9; E8M0 encodes 2^(s-127).
+ *
+ * Readings where the pages are silent are listed in the design notes; the ones
+ * that change arithmetic are repeated at the functions they affect.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------ */
+/* Number formats                                                           */
+/* ------------------------------------------------------------------------ */
+
+/* bf16 is the upper half of an IEEE binary32; widening is exact. */
+double oracle_bf16_to_f64(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* binary32 -> bf16, round to nearest, ties to even (NaN stays NaN). */
+uint16_t oracle_f32_to_bf16(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x0040u);
+    /* Add just under half an ulp of bf16, plus one if the kept lsb is odd. */
+    u += 0x7fffu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+/* OCP E4M3 (FN variant): s.eeee.mmm, bias 7, exponent field 0 = subnormal,
+ * 0x7f / 0xff = NaN, no infinities. */
+double oracle_e4m3_to_f64(uint8_t q) {
+    int s = q >> 7, ef = (q >> 3) & 0xf, m = q & 7;
+    double v;
+    if (ef == 0xf && m == 7) return NAN;
+    if (ef == 0) v = ldexp((double)m, -9);              /* m/8 * 2^(1-7) */
+    else         v = ldexp(1.0 + m / 8.0, ef - 7);
+    return s ? -v : v;
+}
+
+/* Real number -> E4M3, round to nearest even, saturating to +-448. */
+uint8_t oracle_f64_to_e4m3(double v) {
+    uint8_t sign = (v < 0 || (v == 0 && signbit(v))) ? 0x80 : 0x00;
+    double a = fabs(v);
+    if (isnan(v)) return 0x7f;
+    if (a >= 448.0) return sign | 0x7e;                 /* satfinite */
+    if (a < ldexp(1.0, -6)) {
+        /* Subnormal grid: multiples of 2^-9.  A result of 8 is 2^-6, which
+         * is exactly the encoding of the smallest normal (0x08). */
+        double n = nearbyint(ldexp(a, 9));
+        return sign | (uint8_t)n;
+    }
+    int ex;
+    double f = frexp(a, &ex);                           /* a = f 2^ex, f in [0.5,1) */
+    int e = ex - 1;                                     /* a = (2f) 2^e, 2f in [1,2) */
+    double mant = nearbyint((2.0 * f - 1.0) * 8.0);     /* 3 fraction bits, RNE */
+    if (mant == 8.0) { mant = 0.0; e += 1; }
+    if (e > 8 || (e == 8 && mant > 6.0)) return sign | 0x7e;
+    return sign | (uint8_t)(((e + 7) << 3) | (int)mant);
+}
+
+double oracle_e8m0_to_f64(uint8_t s) {
+    if (s == 0xff) return NAN;
+    return ldexp(1.0, (int)s - 127);
+}
+
+/*
+ * Scale exponent for one MX block: the smallest integer e with
+ * amax * 2^-e <= 448, i.e. e = ceil(log2(amax / 448)), which is what rounding
+ * amax/448 up to a power of two gives.  Written without logarithms: with
+ * amax = m 2^p, m in [1,2), and 448 = 1.75 2^8,
+ *   e = p - 8 + (m > 1.75).
+ * amax == 0 yields e = 0 (scale byte 127).
+ */
+int oracle_mx_scale_exponent(double amax) {
+    if (amax == 0.0) return 0;
+    int ex;
+    double f = frexp(amax, &ex);
+    double m = 2.0 * f;
+    int p = ex - 1;
+    return p - 8 + (m > 1.75 ? 1 : 0);
+}
+
+/*
+ * Quantize n values (n a multiple of 32) to MXFP8: per block of 32, the scale
+ * exponent above, scale byte e + 127, codes e4m3(a * 2^-e).  The values are
+ * first rounded to binary32, the precision in which the kernel holds act when
+ * it takes this decision (fp32 accumulators read from tensor memory).
+ * deq (optional) receives q * 2^e.
+ */
+void oracle_mx_quantize(const double* a, int n, uint8_t* q, uint8_t* sf, double* deq) {
+    for (int b = 0; b < n / 32; ++b) {
+        double amax = 0.0;
+        for (int i = 0; i < 32; ++i) {
+            double v = (double)(float)a[b * 32 + i];
+            if (fabs(v) > amax) amax = fabs(v);
+        }
+        int e = oracle_mx_scale_exponent(amax);
+        sf[b] = (uint8_t)(e + 127);
+        for (int i = 0; i < 32; ++i) {
+            double v = (double)(float)a[b * 32 + i];
+            uint8_t c = oracle_f64_to_e4m3(ldexp(v, -e));
+            q[b * 32 + i] = c;
+            if (deq) deq[b * 32 + i] = ldexp(oracle_e4m3_to_f64(c), e);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Routing permutation                                                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Counting sort of the routed pairs p = t*k + j by expert id.
+ *   counts[e]       number of pairs routed to expert e
+ *   offsets[0..E]   exclusive prefix sum of counts
+ *   slot_of_pair[p] offsets[e] + (number of earlier pairs p' < p with the
+ *                   same expert): the stable order within each expert.
+ * The padded variant gives every expert a segment rounded up to a multiple of
+ * `pad` rows (empty experts get none) and the slot of each pair in it.
+ * Returns 0, or -1 if an id lies outside [0, E).
+ */
+int oracle_route(int T, int E, int k, const int32_t* ids, int pad,
+                 int64_t* counts, int64_t* offsets, int64_t* slot_of_pair,
+                 int64_t* pad_offsets, int64_t* pad_slot_of_pair) {
+    int64_t P = (int64_t)T * k;
+    for (int64_t p = 0; p < P; ++p)
+        if (ids[p] < 0 || ids[p] >= E) return -1;
+    for (int e = 0; e < E; ++e) counts[e] = 0;
+    for (int64_t p = 0; p < P; ++p) counts[ids[p]] += 1;
+    offsets[0] = 0;
+    for (int e = 0; e < E; ++e) offsets[e + 1] = offsets[e] + counts[e];
+    if (pad_offsets) {
+        pad_offsets[0] = 0;
+        for (int e = 0; e < E; ++e)
+            pad_offsets[e + 1] = pad_offsets[e] + (counts[e] + pad - 1) / pad * pad;
+    }
+    int64_t* seen = (int64_t*)calloc((size_t)E, sizeof(int64_t));
+    if (!seen) return -2;
+    for (int64_t p = 0; p < P; ++p) {
+        int e = ids[p];
+        if (slot_of_pair) slot_of_pair[p] = offsets[e] + seen[e];
+        if (pad_slot_of_pair && pad_offsets) pad_slot_of_pair[p] = pad_offsets[e] + seen[e];
+        seen[e] += 1;
+    }
+    free(seen);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The forward pass                                                         */
+/* ------------------------------------------------------------------------ */
+
+enum { ORACLE_IN_BF16 = 0, ORACLE_IN_MXFP8 = 1 };
+enum { ORACLE_ACT_EXACT = 0, ORACLE_ACT_BF16 = 1, ORACLE_ACT_MXFP8 = 2 };
+
+/* Element i of a row-major operand, dequantized exactly to double.
+ * bf16: the value itself.  MXFP8: e4m3(q[i]) * 2^(sf[i/32] - 127), the scale
+ * blocks running along the last (contiguous, reduction) dimension. */
+static double elem(int in_mode, const void* v, const uint8_t* sf, int64_t i) {
+    if (in_mode == ORACLE_IN_BF16) return oracle_bf16_to_f64(((const uint16_t*)v)[i]);
+    return oracle_e4m3_to_f64(((const uint8_t*)v)[i]) * oracle_e8m0_to_f64(sf[i / 32]);
+}
+
+static double silu(double g) { return g / (1.0 + exp(-g)); }
+
+/*
+ * out[n][d] for each requested token t = tokens[n] (all T tokens when tokens
+ * is NULL):
+ *
+ *   acc = 0
+ *   for j = 0 .. k-1 (ascending):
+ *     e = ids[t][j], w = topk_w[t][j]
+ *     g[h] = sum_d W1[e][h][d]   x[t][d]        h < H   (gate rows 0..H-1)
+ *     u[h] = sum_d W1[e][H+h][d] x[t][d]                (up rows H..2H-1)
+ *     a[h] = silu(g[h]) * u[h]
+ *     a    = act_round(a)                               (see below)
+ *     y[d] = sum_h W2[e][d][h] a[h]
+ *     acc[d] += w * y[d]
+ *   out[n] = acc
+ *
+ * act_round: EXACT keeps fp64; BF16 rounds each a[h] to binary32 then to bf16
+ * (RNE); MXFP8 requantizes a to e4m3 with one scale per 32 consecutive h.
+ * Shapes: x[T][D], W1[E][2H][D], W2[E][D][H], ids/topk_w[T][k]; MXFP8 scale
+ * arrays have one byte per 32 elements of the last dimension.
+ * Returns 0, or -1 for an expert id outside [0, E) or a bad argument.
+ */
+int oracle_moe_ffn(int T, int E, int D, int H, int k, int in_mode,
+                   const void* x, const uint8_t* x_sf,
+                   const void* w1, const uint8_t* w1_sf,
+                   const void* w2, const uint8_t* w2_sf,
+                   const int32_t* ids, const float* topk_w,
+                   int act_mode, const int32_t* tokens, int n_tokens,
+                   double* out, int n_threads) {
+    if (T < 0 || E < 1 || D < 1 || H < 1 || k < 1) return -1;
+    if (act_mode == ORACLE_ACT_MXFP8 && H % 32) return -1;
+    if (in_mode == ORACLE_IN_MXFP8 && (D % 32 || H % 32)) return -1;
+    int n = tokens ? n_tokens : T;
+    for (int i = 0; i < n; ++i) {
+        int t = tokens ? tokens[i] : i;
+        if (t < 0 || t >= T) return -1;
+        for (int j = 0; j < k; ++j)
+            if (ids[(int64_t)t * k + j] < 0 || ids[(int64_t)t * k + j] >= E) return -1;
+    }
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+    int failed = 0;
+#pragma omp parallel
+    {
+        double* xd = (double*)malloc(sizeof(double) * (size_t)D);
+        double* g = (double*)malloc(sizeof(double) * (size_t)H);
+        double* u = (double*)malloc(sizeof(double) * (size_t)H);
+        double* a = (double*)malloc(sizeof(double) * (size_t)H);
+        uint8_t* aq = (uint8_t*)malloc((size_t)H);
+        uint8_t* asf = (uint8_t*)malloc((size_t)H / 32 + 1);
+        if (!xd || !g || !u || !a || !aq || !asf) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int i = 0; i < n; ++i) {
+                int t = tokens ? tokens[i] : i;
+                double* acc = out + (int64_t)i * D;
+                for (int d = 0; d < D; ++d) {
+                    acc[d] = 0.0;
+                    xd[d] = elem(in_mode, x, x_sf, (int64_t)t * D + d);
+                }
+                for (int j = 0; j < k; ++j) {
+                    int e = ids[(int64_t)t * k + j];
+                    double w = (double)topk_w[(int64_t)t * k + j];
+                    int64_t w1e = (int64_t)e * 2 * H * D;
+                    for (int h = 0; h < H; ++h) {
+                        double sg = 0.0, su = 0.0;
+                        int64_t rg = w1e + (int64_t)h * D, ru = w1e + (int64_t)(H + h) * D;
+                        for (int d = 0; d < D; ++d) {
+                            sg += elem(in_mode, w1, w1_sf, rg + d) * xd[d];
+                            su += elem(in_mode, w1, w1_sf, ru + d) * xd[d];
+                        }
+                        g[h] = sg;
+                        u[h] = su;
+                    }
+                    for (int h = 0; h < H; ++h) a[h] = silu(g[h]) * u[h];
+                    if (act_mode == ORACLE_ACT_BF16) {
+                        for (int h = 0; h < H; ++h) a[h] = oracle_bf16_to_f64(oracle_f32_to_bf16((float)a[h]));
+                    } else if (act_mode == ORACLE_ACT_MXFP8) {
+                        oracle_mx_quantize(a, H, aq, asf, a);
+                    }
+                    int64_t w2e = (int64_t)e * D * H;
+                    for (int d = 0; d < D; ++d) {
+                        double y = 0.0;
+                        int64_t r = w2e + (int64_t)d * H;
+                        for (int h = 0; h < H; ++h) y += elem(in_mode, w2, w2_sf, r + h) * a[h];
+                        acc[d] += w * y;
+                    }
+                }
+            }
+        }
+        free(xd); free(g); free(u); free(a); free(aq); free(asf);
+    }
+    return failed ? -2 : 0;
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
