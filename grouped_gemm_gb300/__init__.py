@@ -1,0 +1,157 @@
+"""Python binding of the GB300 MoE SwiGLU FFN library (libmoe_ffn.so).
+
+Argument marshalling only: every step of the forward pass runs in the CUDA
+kernels behind the C ABI declared in ``include/moe_ffn.h``.  The function names
+are the C names.  Tensors are torch tensors (device memory and streams come
+from PyTorch); their data pointers are passed through unchanged.  There is no
+CPU fallback: if the library cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "MOE_BF16", "MOE_MXFP8", "MOE_FUSED", "MOE_SPLIT", "MoeFFNError", "library_path", "lib",
+    "moe_ffn_workspace_size", "moe_ffn_workspace_init", "moe_ffn_forward", "moe_ffn_route",
+    "moe_ffn_sync_status", "moe_ffn_set_wait_limit_ns", "moe_ffn_profile_enable", "moe_ffn_profile_read", "moe_ffn_status_string", "alloc_workspace",
+]
+
+MOE_BF16, MOE_MXFP8 = 0, 1
+MOE_FUSED, MOE_SPLIT = 0, 1
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_MISALIGNED",
+                4: "MOE_ERR_BAD_ROUTING", 5: "MOE_ERR_WORKSPACE_TOO_SMALL", 6: "MOE_ERR_DEVICE_TIMEOUT",
+                7: "MOE_ERR_CUDA"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MoeFFNError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} ({moe_ffn_status_string(status)})")
+
+
+def library_path() -> str:
+    from . import build as _build
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmoe_ffn.so, building it first if the sources are newer."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            from . import build as _build
+            path = _build.build()
+            L = ctypes.CDLL(path)
+            c = ctypes
+            vp, i, sz = c.c_void_p, c.c_int, c.c_size_t
+            L.moe_ffn_workspace_size.argtypes = [i, i, i, i, i, i, i]
+            L.moe_ffn_workspace_size.restype = sz
+            L.moe_ffn_workspace_init.argtypes = [vp, sz, vp]
+            L.moe_ffn_workspace_init.restype = i
+            L.moe_ffn_forward.argtypes = [vp] * 9 + [i] * 7 + [vp, sz, vp]
+            L.moe_ffn_forward.restype = i
+            L.moe_ffn_route.argtypes = [vp, vp, i, i, i, vp, vp, vp, vp, sz, vp]
+            L.moe_ffn_route.restype = i
+            L.moe_ffn_sync_status.argtypes = [vp, vp]
+            L.moe_ffn_sync_status.restype = i
+            L.moe_ffn_set_wait_limit_ns.argtypes = [c.c_uint64]
+            L.moe_ffn_set_wait_limit_ns.restype = None
+            L.moe_ffn_profile_enable.argtypes = [i]
+            L.moe_ffn_profile_enable.restype = i
+            L.moe_ffn_profile_read.argtypes = [c.POINTER(c.c_float), i, c.POINTER(c.c_int)]
+            L.moe_ffn_profile_read.restype = i
+            L.moe_ffn_status_string.argtypes = [i]
+            L.moe_ffn_status_string.restype = c.c_char_p
+            _lib = L
+    return _lib
+
+
+def _p(t):
+    """Device (or host) pointer of a tensor, None for None, ints pass through."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str) -> int:
+    if status != 0:
+        raise MoeFFNError(status, where)
+    return status
+
+
+def moe_ffn_status_string(status: int) -> str:
+    return lib().moe_ffn_status_string(int(status)).decode()
+
+
+def moe_ffn_workspace_size(T, E, D, H, k, dtype=MOE_BF16, pipeline=MOE_SPLIT) -> int:
+    return int(lib().moe_ffn_workspace_size(T, E, D, H, k, dtype, pipeline))
+
+
+def moe_ffn_workspace_init(workspace, stream=None) -> int:
+    return _check(lib().moe_ffn_workspace_init(_p(workspace), workspace.numel() * workspace.element_size(),
+                                               _stream(stream)), "moe_ffn_workspace_init")
+
+
+def alloc_workspace(T, E, D, H, k, dtype=MOE_BF16, pipeline=MOE_SPLIT, device="cuda"):
+    """A caller-owned workspace tensor of the right size, status words zeroed."""
+    import torch
+    n = moe_ffn_workspace_size(T, E, D, H, k, dtype, pipeline)
+    if n == 0:
+        raise MoeFFNError(1, "moe_ffn_workspace_size")
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    moe_ffn_workspace_init(ws)
+    return ws
+
+
+def moe_ffn_forward(x, w1, w2, topk_ids, topk_w, out, *, E, D, H, k, workspace, dtype=MOE_BF16,
+                    pipeline=MOE_SPLIT, x_sf=None, w1_sf=None, w2_sf=None, T=None, stream=None,
+                    check=True) -> int:
+    T = x.shape[0] if T is None else T
+    st = lib().moe_ffn_forward(_p(x), _p(x_sf), _p(w1), _p(w1_sf), _p(w2), _p(w2_sf), _p(topk_ids), _p(topk_w),
+                               _p(out), T, E, D, H, k, dtype, pipeline, _p(workspace),
+                               workspace.numel() * workspace.element_size(), _stream(stream))
+    return _check(st, "moe_ffn_forward") if check else st
+
+
+def moe_ffn_route(topk_ids, topk_w, T, E, k, counts, offsets, slot_of_pair, workspace, stream=None,
+                  check=True) -> int:
+    st = lib().moe_ffn_route(_p(topk_ids), _p(topk_w), T, E, k, _p(counts), _p(offsets), _p(slot_of_pair),
+                             _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    return _check(st, "moe_ffn_route") if check else st
+
+
+def moe_ffn_sync_status(workspace, stream=None) -> int:
+    """Synchronize and return (and clear) the device-side status: 0, 4 or 6."""
+    return int(lib().moe_ffn_sync_status(_p(workspace), _stream(stream)))
+
+
+def moe_ffn_profile_enable(on: bool) -> int:
+    return _check(lib().moe_ffn_profile_enable(1 if on else 0), "moe_ffn_profile_enable")
+
+
+def moe_ffn_profile_read() -> list:
+    """Stage durations (ms) of the most recent profiled forward call."""
+    buf = (ctypes.c_float * 8)()
+    n = ctypes.c_int(0)
+    _check(lib().moe_ffn_profile_read(buf, 8, ctypes.byref(n)), "moe_ffn_profile_read")
+    return [float(buf[i]) for i in range(n.value)]
+
+
+def moe_ffn_set_wait_limit_ns(ns: int) -> None:
+    lib().moe_ffn_set_wait_limit_ns(int(ns))

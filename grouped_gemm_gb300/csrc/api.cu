@@ -1,0 +1,280 @@
+// api.cu -- the extern "C" entry points: argument checks, workspace layout,
+// tensor-map encoding and the launch sequence of each pipeline.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/moe_ffn.h"
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+std::atomic<unsigned long long> g_wait_limit_ns{2000ull * 1000 * 1000};
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool shape_ok(int T, int E, int D, int H, int k) {
+  return T >= 0 && E >= 1 && E <= kMaxExperts && k >= 1 && D >= 128 && H >= 128 && D % 128 == 0 && H % 128 == 0 &&
+         (int64_t)T * k < (int64_t)1 << 30;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Row-major bf16 matrix [rows, cols] read in boxes of [box_rows, 64] with the
+// 128-byte swizzle (64 bf16 = one 128-byte swizzle row).
+bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Optional per-stage timing (benchmarking aid).
+constexpr int kMaxProfileEvents = 8;
+struct Profile {
+  std::mutex mu;
+  bool on = false;
+  bool created = false;
+  cudaEvent_t ev[kMaxProfileEvents] = {};
+  int recorded = 0;  // events recorded by the last profiled call
+} g_prof;
+
+// Record the next stage boundary of the current call (no-op when disabled).
+void prof_mark(cudaStream_t st, int idx) {
+  if (!g_prof.on || !g_prof.created || idx >= kMaxProfileEvents) return;
+  cudaEventRecord(g_prof.ev[idx], st);
+  g_prof.recorded = idx + 1;
+}
+
+}  // namespace
+
+Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipeline) {
+  Workspace w{};
+  const int64_t P = (int64_t)T * k;
+  const int64_t live_experts = P < E ? P : E;
+  w.S_max = (int64_t)align_up((size_t)(P + live_experts * (kRowPad - 1)), kRowPad);
+  if (w.S_max == 0) w.S_max = kRowPad;
+  w.max_rb = (int)(w.S_max / kRowPad);
+  w.route_blocks = (T + kRouteTokPerBlock - 1) / kRouteTokPerBlock;
+  if (w.route_blocks == 0) w.route_blocks = 1;
+  uint8_t* b = static_cast<uint8_t*>(base);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    uint8_t* p = b ? b + off : nullptr;
+    off = align_up(off + bytes, 256);
+    return p;
+  };
+  w.err = reinterpret_cast<int*>(take(32));
+  w.meta = reinterpret_cast<int*>(take(32));
+  w.counts = reinterpret_cast<int*>(take(sizeof(int) * E));
+  w.offsets = reinterpret_cast<int*>(take(sizeof(int) * (E + 1)));
+  w.pad_offsets = reinterpret_cast<int*>(take(sizeof(int) * (E + 1)));
+  w.expert_of_rb = reinterpret_cast<int*>(take(sizeof(int) * w.max_rb));
+  w.row_tok = reinterpret_cast<int*>(take(sizeof(int) * w.S_max));
+  w.slot_w = reinterpret_cast<float*>(take(sizeof(float) * w.S_max));
+  w.slot_of_pair = reinterpret_cast<int*>(take(sizeof(int) * (P ? P : 1)));
+  w.blk_base = reinterpret_cast<int*>(take(sizeof(int) * (size_t)w.route_blocks * E));
+  if (pipeline == MOE_SPLIT) {
+    w.xg = take((size_t)w.S_max * D * 2);
+    w.act = take((size_t)w.S_max * H * 2);
+  }
+  w.bytes = off;
+  return w;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_ffn_workspace_size(int T, int E, int D, int H, int k, int dtype, int pipeline) {
+  if (!shape_ok(T, E, D, H, k) || (dtype != MOE_BF16 && dtype != MOE_MXFP8) ||
+      (pipeline != MOE_FUSED && pipeline != MOE_SPLIT))
+    return 0;
+  return plan_workspace(nullptr, T, E, D, H, k, pipeline).bytes;
+}
+
+moe_status_t moe_ffn_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
+  if (!workspace || workspace_bytes < 64) return MOE_ERR_INVALID_ARG;
+  return cuda_status(cudaMemsetAsync(workspace, 0, 64, static_cast<cudaStream_t>(stream)));
+}
+
+void moe_ffn_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1); }
+
+moe_status_t moe_ffn_route(const int32_t* topk_ids, const float* topk_w, int T, int E, int k, int32_t* counts,
+                           int32_t* offsets, int32_t* slot_of_pair, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  if (T < 0 || E < 1 || E > kMaxExperts || k < 1 || (int64_t)T * k >= ((int64_t)1 << 30)) return MOE_ERR_INVALID_ARG;
+  if (!workspace || (T > 0 && (!topk_ids || !topk_w))) return MOE_ERR_INVALID_ARG;
+  Workspace ws = plan_workspace(workspace, T, E, 128, 128, k, MOE_FUSED);
+  if (workspace_bytes < ws.bytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    if (counts) cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, st);
+    if (offsets) cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), st);
+    return cuda_status(cudaGetLastError());
+  }
+  cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (counts) e = cudaMemcpyAsync(counts, ws.counts, sizeof(int32_t) * E, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess && offsets)
+    e = cudaMemcpyAsync(offsets, ws.offsets, sizeof(int32_t) * (E + 1), cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess && slot_of_pair)
+    e = cudaMemcpyAsync(slot_of_pair, ws.slot_of_pair, sizeof(int32_t) * T * k, cudaMemcpyDeviceToDevice, st);
+  return cuda_status(e);
+}
+
+moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, const void* w1_sf, const void* w2,
+                             const void* w2_sf, const int32_t* topk_ids, const float* topk_w, void* out, int T, int E,
+                             int D, int H, int k, int dtype, int pipeline, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  if (!shape_ok(T, E, D, H, k)) return MOE_ERR_INVALID_ARG;
+  if (dtype != MOE_BF16 && dtype != MOE_MXFP8) return MOE_ERR_INVALID_ARG;
+  if (pipeline != MOE_FUSED && pipeline != MOE_SPLIT) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !w1 || !w2 || !topk_ids || !topk_w || !out || !workspace) return MOE_ERR_INVALID_ARG;
+  if (dtype == MOE_BF16 && (x_sf || w1_sf || w2_sf)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w1) || !aligned16(w2) || !aligned16(out) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(topk_ids) & 3u) || (reinterpret_cast<uintptr_t>(topk_w) & 3u))
+    return MOE_ERR_MISALIGNED;
+  if (dtype != MOE_BF16 || pipeline != MOE_SPLIT) return MOE_ERR_UNSUPPORTED;
+  if (D % kDownN != 0) return MOE_ERR_UNSUPPORTED;
+  Workspace ws = plan_workspace(workspace, T, E, D, H, k, pipeline);
+  if (workspace_bytes < ws.bytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = num_sms();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  CUtensorMap map_xg, map_w1, map_act, map_w2;
+  if (!make_map_bf16(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, kBM) ||
+      !make_map_bf16(&map_w1, w1, (uint64_t)E * 2 * H, (uint64_t)D, kUpFold) ||
+      !make_map_bf16(&map_act, ws.act, (uint64_t)ws.S_max, (uint64_t)H, kBM) ||
+      !make_map_bf16(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, kDownN))
+    return MOE_ERR_CUDA;
+
+  prof_mark(st, 0);
+  cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  prof_mark(st, 1);
+  e = launch_gather_zero(ws, x, D, out, (int64_t)T * D * 2, sms * 4, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  prof_mark(st, 2);
+
+  GemmArgs ga{};
+  ga.meta = ws.meta;
+  ga.expert_of_rb = ws.expert_of_rb;
+  ga.row_tok = ws.row_tok;
+  ga.slot_w = ws.slot_w;
+  ga.act = ws.act;
+  ga.out = out;
+  ga.err = ws.err;
+  ga.wait_limit_ns = g_wait_limit_ns.load();
+  ga.D = D;
+  ga.H = H;
+
+  GemmArgs up = ga;
+  up.n_col_tiles = H / kUpFold;
+  up.k_blocks = D / kBK;
+  const int up_grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * up.n_col_tiles);
+  e = launch_up_bf16(map_xg, map_w1, up, up_grid, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  prof_mark(st, 3);
+
+  GemmArgs dn = ga;
+  dn.n_col_tiles = D / kDownN;
+  dn.k_blocks = H / kBK;
+  const int dn_grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * dn.n_col_tiles);
+  e = launch_down_bf16(map_act, map_w2, dn, dn_grid, st, !g_prof.on);
+  prof_mark(st, 4);
+  return cuda_status(e);
+}
+
+moe_status_t moe_ffn_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (on && !g_prof.created) {
+    for (int i = 0; i < kMaxProfileEvents; ++i)
+      if (cudaEventCreate(&g_prof.ev[i]) != cudaSuccess) return MOE_ERR_CUDA;
+    g_prof.created = true;
+  }
+  g_prof.on = on != 0;
+  g_prof.recorded = 0;
+  return MOE_OK;
+}
+
+moe_status_t moe_ffn_profile_read(float* ms, int capacity, int* n_stages) {
+  if (!ms || !n_stages) return MOE_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  *n_stages = 0;
+  if (!g_prof.created || g_prof.recorded < 2) return MOE_OK;
+  if (cudaEventSynchronize(g_prof.ev[g_prof.recorded - 1]) != cudaSuccess) return MOE_ERR_CUDA;
+  int n = 0;
+  for (int i = 0; i + 1 < g_prof.recorded && n < capacity; ++i, ++n)
+    if (cudaEventElapsedTime(&ms[n], g_prof.ev[i], g_prof.ev[i + 1]) != cudaSuccess) return MOE_ERR_CUDA;
+  *n_stages = n;
+  return MOE_OK;
+}
+
+moe_status_t moe_ffn_sync_status(void* workspace, void* stream) {
+  if (!workspace) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  int words[2] = {0, 0};
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpy(words, workspace, sizeof words, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemset(workspace, 0, 64) != cudaSuccess) return MOE_ERR_CUDA;
+  if (words[0] & kErrTimeout) return MOE_ERR_DEVICE_TIMEOUT;
+  if (words[0] & kErrBadRouting) return MOE_ERR_BAD_ROUTING;
+  return MOE_OK;
+}
+
+const char* moe_ffn_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape, dtype or pipeline";
+    case MOE_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case MOE_ERR_BAD_ROUTING: return "expert id outside [0, E)";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_DEVICE_TIMEOUT: return "a device-side wait timed out; output is invalid";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,287 @@
+// gemm_bf16.cu -- persistent grouped GEMMs of the split pipeline on tcgen05.
+//
+// UP  (GEMM1 + SwiGLU): for each 128-row block rb of the sorted, padded token
+//     order (expert e = expert_of_rb[rb]) and each column tile j, the
+//     accumulator holds [gate rows j*G .. +G | up rows H + j*G .. +G] of
+//     W1[e] times the 128 gathered rows, so both halves of every SwiGLU pair
+//     sit in the same TMEM accumulator ("Prime Flash MoE", sec. 2 "Trick 1":
+//     gate and up interleaved per 128-row block; here the interleave is two
+//     TMA boxes into adjacent shared-memory rows).  The epilogue computes
+//     act = silu(gate) * up in fp32, rounds to bf16 and stores act[slot, j*G..]
+//     (sec. 5 "SwiGLU", sec. 6: the split pipeline writes act once).
+// DOWN (GEMM2 + weighted reduce): for each row block and 256-column tile of
+//     D, acc = act[rb rows, :] * W2[e][cols, :]^T over all of H (sec. 6 "The
+//     down-projection kernel": C = 1, no split-K); the epilogue scales row r
+//     by its routing weight in fp32, rounds to bf16 and reduces into
+//     out[row_tok[r], cols] with 16-byte red.global.add.noftz.v4.bf16x2
+//     (sec. 5 "The same three jobs without the staging buffer"): one
+//     instruction does the top-k sum and the scatter back to token order.
+//
+// Warp roles (192 threads, one CTA per SM, persistent over a static tile list):
+//   warp 0      TMA producer (one lane): A and B tiles into a STAGES-deep ring
+//   warp 1      TMEM allocator; one lane issues tcgen05.mma (M=128, K=16)
+//   warps 2..5  epilogue: tcgen05.ld of the warp's 32 TMEM lanes (= rows)
+// The accumulator is double-buffered in TMEM (2 x N columns) so the epilogue
+// of tile i overlaps the main loop of tile i+1.  Every wait is bounded.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+enum { kModeUp = 0, kModeDown = 1 };
+
+template <int MODE, int N, int STAGES>
+struct GemmCfg {
+  static constexpr int kABytes = kBM * kBK * 2;             // 16 KB
+  static constexpr int kBBytes = N * kBK * 2;               // N rows of 128 B
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * N;                   // double-buffered accumulator
+  static constexpr int kSmemBytes = 1024 /*align slack*/ + STAGES * kStageBytes + 256 /*barriers*/;
+  static_assert(N % 32 == 0 && N >= 32 && N <= 256, "MMA N");
+  static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns: power of two <= 512");
+  static_assert(kSmemBytes <= 232448, "shared memory");
+};
+
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;  // 200 ms
+
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+
+__device__ __forceinline__ float swiglu(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+
+template <int MODE, int N, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                             const GemmArgs args) {
+  using Cfg = GemmCfg<MODE, N, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * Cfg::kABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * Cfg::kStageBytes);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WaitCtl wc{abort_flag, args.err, args.wait_limit_ns};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], kEpiThreads);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&map_a);
+    prefetch_tmap(&map_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  if (MODE == kModeUp && threadIdx.x == 0) griddep_launch_dependents();
+
+  const int num_rb = args.meta[0];
+  const int n_tiles = num_rb * args.n_col_tiles;
+  const int KB = args.k_blocks;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    if (MODE == kModeDown) griddep_wait();  // act is written by the previous grid
+    int s = 0;
+    uint32_t ph = 0;
+    int issued_phase[STAGES];
+#pragma unroll
+    for (int i = 0; i < STAGES; ++i) issued_phase[i] = -1;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
+      const int rb = tile / args.n_col_tiles, j = tile % args.n_col_tiles;
+      const int e = args.expert_of_rb[rb];
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait(&empty[s], ph ^ 1u, wc, 1)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
+        tma_load_2d(sA + s * Cfg::kABytes, &map_a, &full[s], kb * kBK, rb * kBM);
+        if (MODE == kModeUp) {
+          constexpr int G = N / 2;
+          const int row0 = e * 2 * args.H + j * G;
+          tma_load_2d(sB + s * Cfg::kBBytes, &map_b, &full[s], kb * kBK, row0);
+          tma_load_2d(sB + s * Cfg::kBBytes + G * kBK * 2, &map_b, &full[s], kb * kBK, row0 + args.H);
+        } else {
+          tma_load_2d(sB + s * Cfg::kBBytes, &map_b, &full[s], kb * kBK, e * args.D + j * N);
+        }
+        issued_phase[s] = (int)ph;
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+    if (!ok) {  // let every copy already in flight land before the CTA exits
+      for (int i = 0; i < STAGES; ++i)
+        if (issued_phase[i] >= 0) mbar_wait_drain(&full[i], (uint32_t)issued_phase[i], kDrainNs);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, N);
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    int it = 0;
+    for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+      if (!mbar_wait(&tempty[acc], aph ^ 1u, wc, 2)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * N;
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!mbar_wait(&full[s], ph, wc, 3)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t adesc = sdesc_sw128(smem_addr(sA + s * Cfg::kABytes));
+        const uint64_t bdesc = sdesc_sw128(smem_addr(sB + s * Cfg::kBBytes));
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          // +32 bytes per K step of 16 bf16 = +2 in the descriptor's address field
+          umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+        }
+        umma_commit(&empty[s]);  // frees the smem stage once these MMAs are done
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok) break;
+      umma_commit(&tfull[acc]);  // accumulator ready for the epilogue
+    }
+    if (!ok) {  // wait for every MMA already issued before TMEM is released
+      umma_commit(drain);
+      mbar_wait_drain(drain, 0, kDrainNs);
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;  // TMEM lanes this warp may access
+    const int row = quad * 32 + lane;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
+    int it = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t aph = (uint32_t)(it >> 1) & 1u;
+      if (!mbar_wait(&tfull[acc], aph, wc, 4)) break;
+      tc_fence_after();
+      const int rb = tile / args.n_col_tiles, j = tile % args.n_col_tiles;
+      const int64_t slot = (int64_t)rb * kBM + row;
+      const int tok = args.row_tok[slot];
+      const uint32_t tacc = lane_base + acc * N;
+      if (MODE == kModeUp) {
+        constexpr int G = N / 2;
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(args.act) + slot * args.H + j * G;
+#pragma unroll 1
+        for (int c = 0; c < G / 32; ++c) {
+          uint32_t g[32], u[32];
+          tmem_ld_x32_pair(tacc + c * 32, tacc + G + c * 32, g, u);
+          if (tok >= 0) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_bf16x2(swiglu(u2f(g[2 * i]), u2f(u[2 * i])), swiglu(u2f(g[2 * i + 1]), u2f(u[2 * i + 1])));
+#pragma unroll
+            for (int q = 0; q < 4; ++q) st_global_v4(dst + c * 32 + q * 8, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
+        }
+      } else {
+        const float w = args.slot_w[slot];
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(args.out) + (int64_t)(tok < 0 ? 0 : tok) * args.D + j * N;
+#pragma unroll 1
+        for (int c = 0; c < N / 32; c += 2) {
+          uint32_t v0[32], v1[32];
+          tmem_ld_x32_pair(tacc + c * 32, tacc + (c + 1) * 32, v0, v1);
+          if (tok >= 0) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              red_add_bf16x8(dst + c * 32 + q * 8, pack_bf16x2(w * u2f(v0[8 * q + 0]), w * u2f(v0[8 * q + 1])),
+                             pack_bf16x2(w * u2f(v0[8 * q + 2]), w * u2f(v0[8 * q + 3])),
+                             pack_bf16x2(w * u2f(v0[8 * q + 4]), w * u2f(v0[8 * q + 5])),
+                             pack_bf16x2(w * u2f(v0[8 * q + 6]), w * u2f(v0[8 * q + 7])));
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              red_add_bf16x8(dst + (c + 1) * 32 + q * 8, pack_bf16x2(w * u2f(v1[8 * q + 0]), w * u2f(v1[8 * q + 1])),
+                             pack_bf16x2(w * u2f(v1[8 * q + 2]), w * u2f(v1[8 * q + 3])),
+                             pack_bf16x2(w * u2f(v1[8 * q + 4]), w * u2f(v1[8 * q + 5])),
+                             pack_bf16x2(w * u2f(v1[8 * q + 6]), w * u2f(v1[8 * q + 7])));
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+template <int MODE, int N, int STAGES>
+cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args, int grid,
+                        cudaStream_t stream, bool pdl) {
+  using Cfg = GemmCfg<MODE, N, STAGES>;
+  auto kern = grouped_gemm_bf16_kernel<MODE, N, STAGES>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a, b, args);
+}
+
+}  // namespace
+
+cudaError_t launch_up_bf16(const CUtensorMap& map_a, const CUtensorMap& map_w1, const GemmArgs& args, int grid,
+                           cudaStream_t stream) {
+  return launch_gemm<kModeUp, 2 * kUpFold, kUpStages>(map_a, map_w1, args, grid, stream, false);
+}
+
+cudaError_t launch_down_bf16(const CUtensorMap& map_act, const CUtensorMap& map_w2, const GemmArgs& args, int grid,
+                             cudaStream_t stream, bool pdl) {
+  return launch_gemm<kModeDown, kDownN, kDownStages>(map_act, map_w2, args, grid, stream, pdl);
+}
+
+}  // namespace moe

@@ -1,0 +1,72 @@
+// internal.h -- shared host/device declarations of the MoE FFN library:
+// workspace layout, kernel parameter blocks and launch helpers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+constexpr int kBM = 128;          // rows per tile = tcgen05 MMA M
+constexpr int kBK = 64;           // K elements per pipeline stage (128 B of bf16)
+constexpr int kRowPad = 128;      // per-expert row segments are padded to this
+constexpr int kMaxExperts = 1024;
+constexpr int kRouteTokPerBlock = 256;  // tokens per routing block
+
+// Device-side view of the caller's workspace.  Every region starts on a
+// 256-byte boundary; sizes depend only on (T, E, D, H, k, pipeline).
+struct Workspace {
+  int* err;            // [8]   err[0] error bits, err[1] timeout site
+  int* meta;           // [8]   meta[0] = number of 128-row blocks
+  int* counts;         // [E]
+  int* offsets;        // [E+1] unpadded exclusive scan of counts
+  int* pad_offsets;    // [E+1] exclusive scan of counts rounded up to 128
+  int* expert_of_rb;   // [max_rb]
+  int* row_tok;        // [S_max] token of each padded slot, -1 for padding
+  float* slot_w;       // [S_max] routing weight of each padded slot, 0 for padding
+  int* slot_of_pair;   // [P]   unpadded slot of pair p = t*k + j
+  int* blk_base;       // [NB*E] per routing block: rank base within each expert
+  void* xg;            // [S_max, D] bf16 gathered rows (split pipeline)
+  void* act;           // [S_max, H] bf16 activation (split pipeline)
+  size_t bytes;        // total bytes required
+  int64_t S_max;       // padded slot capacity (multiple of 128)
+  int max_rb;
+  int route_blocks;
+};
+
+Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipeline);
+
+// ----------------------------------------------------------------- kernels
+struct GemmArgs {
+  const int* meta;          // meta[0] = number of row blocks
+  const int* expert_of_rb;
+  const int* row_tok;
+  const float* slot_w;
+  void* act;                // up: bf16 [S_max, H] output
+  void* out;                // down: bf16 [T, D] reduction target
+  int* err;
+  unsigned long long wait_limit_ns;
+  int D, H;
+  int n_col_tiles;          // column tiles per row block
+  int k_blocks;             // reduction length / kBK
+};
+
+cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const float* topk_w, int T, int E, int k,
+                         cudaStream_t stream);
+// xg = x[row_tok] for live slots, and (when out != nullptr) out[0 .. out_bytes) = 0.
+cudaError_t launch_gather_zero(const Workspace& ws, const void* x, int D, void* out, int64_t out_bytes, int grid,
+                               cudaStream_t stream);
+cudaError_t launch_up_bf16(const CUtensorMap& map_a, const CUtensorMap& map_w1, const GemmArgs& args, int grid,
+                           cudaStream_t stream);
+cudaError_t launch_down_bf16(const CUtensorMap& map_act, const CUtensorMap& map_w2, const GemmArgs& args, int grid,
+                             cudaStream_t stream, bool pdl);
+
+// tile shapes of the bf16 GEMMs (host and device agree on these)
+constexpr int kUpFold = 128;      // gate rows + up rows per tile: N = 2 * kUpFold
+constexpr int kUpStages = 4;
+constexpr int kDownN = 256;
+constexpr int kDownStages = 4;
+
+}  // namespace moe

@@ -1,0 +1,241 @@
+// route.cu -- the routing permutation and the row gather.
+//
+// Routing ("Prime Flash MoE", sec. 3 "For the tokens: TMA gathers them too"
+// and sec. 6 "The down-projection kernel": tokens are processed in sorted,
+// per-expert order with each expert's segment padded to 128 rows):
+//   counts[e]      = #pairs p = t*k + j with topk_ids[p] == e
+//   offsets        = exclusive scan of counts               (E+1 entries)
+//   pad_offsets    = exclusive scan of counts rounded up to 128
+//   slot_of_pair[p]= offsets[e] + #{p' < p : topk_ids[p'] == e}  (stable)
+//   row_tok[s], slot_w[s] for the padded slot s = pad_offsets[e] + rank,
+//   -1 / 0 for padding rows; expert_of_rb[rb] for each 128-row block.
+// Three kernels, all deterministic (no order-dependent atomics on results):
+//   1. per-block histograms,
+//   2. one block: scans over blocks and over experts, padding, block->expert,
+//   3. per-block stable scatter using warp match + per-warp prefix counts.
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kScatterWarps = 8;
+
+__global__ void __launch_bounds__(256) route_count_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int k,
+                                                          int* __restrict__ blk_counts, int* __restrict__ err) {
+  extern __shared__ int hist[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int64_t p0 = (int64_t)blockIdx.x * kRouteTokPerBlock * k;
+  const int64_t p1 = min(P, p0 + (int64_t)kRouteTokPerBlock * k);
+  bool bad = false;
+  for (int64_t p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
+    const int e = ids[p];
+    if ((unsigned)e < (unsigned)E) atomicAdd(&hist[e], 1);
+    else bad = true;
+  }
+  if (bad) atomicOr(err, kErrBadRouting);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) blk_counts[(int64_t)blockIdx.x * E + e] = hist[e];
+}
+
+// Exclusive scan of one int per thread over a 1024-thread block; *total gets the sum.
+__device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int s = warp_sums[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    warp_sums[lane] = s;
+  }
+  __syncthreads();
+  const int base = warp ? warp_sums[warp - 1] : 0;
+  *total = warp_sums[31];
+  __syncthreads();
+  return base + x - v;
+}
+
+__global__ void __launch_bounds__(1024) route_scan_kernel(int NB, int E, int* __restrict__ blk, int* counts,
+                                                          int* offsets, int* pad_offsets, int* meta,
+                                                          int* expert_of_rb, int* row_tok, float* slot_w) {
+  __shared__ int seg_sum[1024];
+  __shared__ int cnt_s[kMaxExperts];
+  __shared__ int warp_sums[32];
+  const int tid = threadIdx.x;
+  int Ep = 1;
+  while (Ep < E) Ep <<= 1;
+  const int nseg = 1024 / Ep;
+  const int e = tid % Ep, seg = tid / Ep;
+  const int per = (NB + nseg - 1) / nseg;
+  const int b0 = min(NB, seg * per), b1 = min(NB, b0 + per);
+  // pass 1: per-segment sums of the block histograms
+  int run = 0;
+  if (e < E) {
+#pragma unroll 8
+    for (int b = b0; b < b1; ++b) run += blk[(int64_t)b * E + e];
+  }
+  seg_sum[tid] = run;
+  __syncthreads();
+  if (seg == 0 && e < E) {
+    int acc = 0;
+    for (int s = 0; s < nseg; ++s) {
+      const int v = seg_sum[s * Ep + e];
+      seg_sum[s * Ep + e] = acc;
+      acc += v;
+    }
+    cnt_s[e] = acc;
+  }
+  __syncthreads();
+  // pass 2: per-block rank bases (exclusive scan over blocks, per expert)
+  if (e < E) {
+    int acc = seg_sum[tid];
+#pragma unroll 8
+    for (int b = b0; b < b1; ++b) {
+      const int c = blk[(int64_t)b * E + e];
+      blk[(int64_t)b * E + e] = acc;
+      acc += c;
+    }
+  }
+  // scans over experts
+  const int cnt = tid < E ? cnt_s[tid] : 0;
+  const int padc = (cnt + kRowPad - 1) / kRowPad * kRowPad;
+  int tot, ptot;
+  const int off = block_exclusive_scan(cnt, warp_sums, &tot);
+  const int poff = block_exclusive_scan(padc, warp_sums, &ptot);
+  if (tid < E) {
+    counts[tid] = cnt;
+    offsets[tid] = off;
+    pad_offsets[tid] = poff;
+    for (int rb = poff / kRowPad; rb < (poff + padc) / kRowPad; ++rb) expert_of_rb[rb] = tid;
+    for (int s = poff + cnt; s < poff + padc; ++s) {
+      row_tok[s] = -1;
+      slot_w[s] = 0.f;
+    }
+  }
+  if (tid == 0) {
+    offsets[E] = tot;
+    pad_offsets[E] = ptot;
+    meta[0] = ptot / kRowPad;
+  }
+}
+
+__global__ void __launch_bounds__(kScatterWarps * 32)
+    route_scatter_kernel(const int32_t* __restrict__ ids, const float* __restrict__ topk_w, int64_t P, int E, int k,
+                         const int* __restrict__ blk_base, const int* __restrict__ offsets,
+                         const int* __restrict__ pad_offsets, int* __restrict__ row_tok, float* __restrict__ slot_w,
+                         int* __restrict__ slot_of_pair) {
+  extern __shared__ int wcnt[];  // [kScatterWarps][E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t p0 = (int64_t)blockIdx.x * kRouteTokPerBlock * k;
+  const int64_t p1 = min(P, p0 + (int64_t)kRouteTokPerBlock * k);
+  const int64_t sub = (p1 - p0 + kScatterWarps - 1) / kScatterWarps;
+  const int64_t q0 = min(p1, p0 + warp * sub), q1 = min(p1, q0 + sub);
+  for (int i = threadIdx.x; i < kScatterWarps * E; i += blockDim.x) wcnt[i] = 0;
+  __syncthreads();
+  for (int64_t p = q0 + lane; p < q1; p += 32) {
+    const int e = ids[p];
+    if ((unsigned)e < (unsigned)E) atomicAdd(&wcnt[warp * E + e], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int acc = blk_base[(int64_t)blockIdx.x * E + e];
+    for (int w = 0; w < kScatterWarps; ++w) {
+      const int c = wcnt[w * E + e];
+      wcnt[w * E + e] = acc;
+      acc += c;
+    }
+  }
+  __syncthreads();
+  int* mine = wcnt + warp * E;
+  for (int64_t base = q0; base < q1; base += 32) {
+    const int64_t p = base + lane;
+    const bool in = p < q1;
+    const int e = in ? ids[p] : -1;
+    const bool valid = in && (unsigned)e < (unsigned)E;
+    const int key = valid ? e : E + lane;  // invalid lanes never match anyone
+    const unsigned peers = __match_any_sync(0xffffffffu, key);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const int r = valid ? mine[e] + rank : 0;
+    __syncwarp();
+    if (valid && rank == 0) mine[e] += __popc(peers);
+    __syncwarp();
+    if (valid) {
+      const int ps = pad_offsets[e] + r;
+      row_tok[ps] = (int)(p / k);
+      slot_w[ps] = topk_w[p];
+      slot_of_pair[p] = offsets[e] + r;
+    } else if (in) {
+      slot_of_pair[p] = -1;
+    }
+  }
+}
+
+// xg[s, :] = x[row_tok[s], :] for live slots (16-byte vector copies, one warp
+// per row); padding rows are skipped -- each GEMM output row depends only on
+// its own input row and padding rows are dropped by the reductions.  The same
+// launch zero-fills `out` (the down projection reduces into it).
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, const int* __restrict__ row_tok,
+                                                          const int* __restrict__ meta, uint4* __restrict__ xg,
+                                                          int vec_per_row, uint4* __restrict__ out,
+                                                          int64_t out_vecs) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t S = (int64_t)meta[0] * kRowPad;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp; row < S; row += nwarps) {
+    const int tok = row_tok[row];
+    if (tok < 0) continue;
+    const uint4* src = x + (int64_t)tok * vec_per_row;
+    uint4* dst = xg + row * vec_per_row;
+    int i = lane;
+    for (; i + 96 < vec_per_row; i += 128) {
+      const uint4 a = __ldg(src + i), b = __ldg(src + i + 32), c = __ldg(src + i + 64), d = __ldg(src + i + 96);
+      dst[i] = a;
+      dst[i + 32] = b;
+      dst[i + 64] = c;
+      dst[i + 96] = d;
+    }
+    for (; i < vec_per_row; i += 32) dst[i] = __ldg(src + i);
+  }
+  if (out) {
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < out_vecs; i += (int64_t)gridDim.x * blockDim.x)
+      out[i] = z;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const float* topk_w, int T, int E, int k,
+                         cudaStream_t stream) {
+  const int64_t P = (int64_t)T * k;
+  const int NB = ws.route_blocks;
+  route_count_kernel<<<NB, 256, E * sizeof(int), stream>>>(topk_ids, P, E, k, ws.blk_base, ws.err);
+  route_scan_kernel<<<1, 1024, 0, stream>>>(NB, E, ws.blk_base, ws.counts, ws.offsets, ws.pad_offsets, ws.meta,
+                                            ws.expert_of_rb, ws.row_tok, ws.slot_w);
+  route_scatter_kernel<<<NB, kScatterWarps * 32, kScatterWarps * E * sizeof(int), stream>>>(
+      topk_ids, topk_w, P, E, k, ws.blk_base, ws.offsets, ws.pad_offsets, ws.row_tok, ws.slot_w, ws.slot_of_pair);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_zero(const Workspace& ws, const void* x, int D, void* out, int64_t out_bytes, int grid,
+                               cudaStream_t stream) {
+  gather_rows_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), ws.row_tok, ws.meta,
+                                               static_cast<uint4*>(ws.xg), D / 8, static_cast<uint4*>(out),
+                                               out_bytes / 16);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

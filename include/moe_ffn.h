@@ -1,0 +1,119 @@
+/*
+ * moe_ffn.h -- C ABI of the GB300 (sm_103a) routed Mixture-of-Experts SwiGLU
+ * feed-forward forward pass.
+ *
+ * What it computes ("Prime Flash MoE - Faster MoE Kernels optimized for
+ * Blackwell", sec. 1 "The computation"): for every token t and each of its k
+ * routed experts e = topk_ids[t][j] with routing weight w = topk_w[t][j],
+ *
+ *     gate = W1[e][0:H]  x_t        up = W1[e][H:2H] x_t       (W1 output-major)
+ *     act  = silu(gate) * up        (fp32, rounded to bf16 before the next GEMM)
+ *     y    = W2[e] act
+ *     out[t] = sum_j w * y          (the weight is applied before the sum)
+ *
+ * Layouts (all row-major, contiguous, device memory):
+ *     x         [T, D]        bf16
+ *     w1        [E, 2H, D]    bf16, rows 0..H-1 of each expert = gate, H..2H-1 = up
+ *     w2        [E, D, H]     bf16
+ *     topk_ids  [T, k]        int32, each in [0, E); repeats within a token allowed
+ *     topk_w    [T, k]        float32
+ *     out       [T, D]        bf16, OVERWRITTEN (the library zero-fills it)
+ * Requirements: T >= 0 (T == 0 is a no-op), 1 <= k, 1 <= E <= 1024,
+ * D % 128 == 0, H % 128 == 0, every pointer 16-byte aligned.
+ *
+ * Ownership: the caller owns every buffer, including the workspace; the
+ * library allocates no device memory.  Calls are asynchronous on `stream` (a
+ * cudaStream_t passed as void*, NULL = legacy default stream) and may be
+ * captured in CUDA graphs.  Host-detectable errors are returned immediately;
+ * errors found on the device (an expert id out of range, a bounded wait that
+ * ran out) are recorded in the workspace's status words, are sticky, and are
+ * returned and cleared by moe_ffn_sync_status().  No C++ exception crosses
+ * this interface.
+ */
+#ifndef MOE_FFN_H_
+#define MOE_FFN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,         /* null pointer, negative size, k < 1 ... */
+  MOE_ERR_UNSUPPORTED = 2,         /* shape or dtype/pipeline combination not built */
+  MOE_ERR_MISALIGNED = 3,          /* a pointer is not 16-byte aligned */
+  MOE_ERR_BAD_ROUTING = 4,         /* device saw an expert id outside [0, E) */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 5,
+  MOE_ERR_DEVICE_TIMEOUT = 6,      /* a bounded device wait ran out; output invalid */
+  MOE_ERR_CUDA = 7                 /* a CUDA runtime call failed */
+} moe_status_t;
+
+typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_dtype_t;
+
+/* MOE_FUSED: one GEMM kernel per call, the activation never leaves the SM
+ *            ("Prime Flash MoE" sec. 2 "Trick 2", sec. 4).
+ * MOE_SPLIT: gather, up-projection + SwiGLU writing the activation once, then
+ *            the down projection with C = 1 ("Prime Flash MoE" sec. 6). */
+typedef enum { MOE_FUSED = 0, MOE_SPLIT = 1 } moe_pipeline_t;
+
+/* Bytes of workspace moe_ffn_forward needs for this problem.  Returns 0 for
+ * an invalid shape.  The first 64 bytes are the status words: zero them once
+ * before first use (moe_ffn_workspace_init does so). */
+size_t moe_ffn_workspace_size(int T, int E, int D, int H, int k, int dtype, int pipeline);
+
+/* Zero the workspace's status words (asynchronous on stream). */
+moe_status_t moe_ffn_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
+
+/* The forward pass described above.  x_sf, w1_sf, w2_sf are the MXFP8 scale
+ * arrays and must be NULL for MOE_BF16. */
+moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, const void* w1_sf, const void* w2,
+                             const void* w2_sf, const int32_t* topk_ids, const float* topk_w, void* out, int T, int E,
+                             int D, int H, int k, int dtype, int pipeline, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* The routing permutation alone ("Prime Flash MoE" sec. 3 and 6: tokens are
+ * processed in per-expert sorted order).  Writes, into caller device arrays:
+ *   counts[E]         pairs routed to each expert
+ *   offsets[E+1]      exclusive prefix sum of counts
+ *   slot_of_pair[T*k] offsets[e] + number of earlier pairs (p' < p, p = t*k+j)
+ *                     routed to the same expert: a stable counting sort.
+ * Any output pointer may be NULL.  Bit-exact by construction (no
+ * order-dependent atomics).  Uses the same workspace as moe_ffn_forward. */
+moe_status_t moe_ffn_route(const int32_t* topk_ids, const float* topk_w, int T, int E, int k, int32_t* counts,
+                           int32_t* offsets, int32_t* slot_of_pair, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/* Synchronize `stream`, then return (and clear) the device status recorded in
+ * the workspace since the last call: MOE_OK, MOE_ERR_BAD_ROUTING or
+ * MOE_ERR_DEVICE_TIMEOUT.  MOE_ERR_CUDA if synchronization itself failed. */
+moe_status_t moe_ffn_sync_status(void* workspace, void* stream);
+
+/* Upper bound, in nanoseconds, of every wait inside the kernels (default 2 s).
+ * Process-wide; affects launches made after the call. */
+void moe_ffn_set_wait_limit_ns(uint64_t ns);
+
+/* Per-stage timing of later moe_ffn_forward calls (a benchmarking aid, off by
+ * default).  While enabled, each call records CUDA events on its stream
+ * between its stages; the split pipeline's stages are
+ *   0 routing (three kernels), 1 gather + zero-fill of out,
+ *   2 up-projection + SwiGLU, 3 down-projection + weighted reduction.
+ * Events are created lazily on the current device.  Recording events between
+ * the up and down kernels stops them overlapping, so time the step itself
+ * with profiling off. */
+moe_status_t moe_ffn_profile_enable(int on);
+
+/* Synchronize on the most recent profiled call and write its stage durations
+ * in milliseconds to ms[0 .. *n_stages) (at most `capacity`). */
+moe_status_t moe_ffn_profile_read(float* ms, int capacity, int* n_stages);
+
+/* Static description of a status code. */
+const char* moe_ffn_status_string(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FFN_H_ */

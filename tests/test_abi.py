@@ -1,0 +1,73 @@
+"""The C-ABI library loads on a machine without a GPU, exports every entry
+point include/moe_ffn.h declares, and rejects bad arguments on the host."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import grouped_gemm_gb300 as moe
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe_ffn.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(moe_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for n in ("moe_ffn_forward", "moe_ffn_workspace_size", "moe_ffn_route", "moe_ffn_sync_status",
+              "moe_ffn_status_string", "moe_ffn_workspace_init", "moe_ffn_set_wait_limit_ns"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(moe.library_path() if os.path.exists(moe.library_path()) else moe.lib()._name)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings():
+    for s in range(8):
+        assert moe.moe_ffn_status_string(s) and moe.moe_ffn_status_string(s) != "unknown status"
+
+
+def test_workspace_size_rules():
+    ok = moe.moe_ffn_workspace_size(64, 8, 256, 128, 2)
+    assert ok > 0
+    assert moe.moe_ffn_workspace_size(64, 8, 200, 128, 2) == 0      # D % 128
+    assert moe.moe_ffn_workspace_size(64, 8, 256, 100, 2) == 0      # H % 128
+    assert moe.moe_ffn_workspace_size(64, 0, 256, 128, 2) == 0      # E >= 1
+    assert moe.moe_ffn_workspace_size(64, 2000, 256, 128, 2) == 0   # E <= 1024
+    assert moe.moe_ffn_workspace_size(64, 8, 256, 128, 0) == 0      # k >= 1
+    assert moe.moe_ffn_workspace_size(-1, 8, 256, 128, 2) == 0
+    # the split pipeline holds the gathered rows and the activation
+    big = moe.moe_ffn_workspace_size(4096, 128, 2048, 768, 8, moe.MOE_BF16, moe.MOE_SPLIT)
+    P = 4096 * 8
+    s_max = (P + 128 * 127 + 127) // 128 * 128
+    assert big >= s_max * (2048 + 768) * 2
+
+
+def test_forward_rejects_bad_arguments_on_host():
+    L = moe.lib()
+    A = 1 << 20  # a fake, 16-byte aligned address: never dereferenced
+    ws = 10 ** 9
+    call = lambda *a: L.moe_ffn_forward(*a)
+    base = [A, None, A, None, A, None, A, A, A, 64, 8, 256, 128, 2, 0, 1, A, ws, None]
+    a = list(base); a[0] = None
+    assert call(*a) == 1                                   # null x
+    a = list(base); a[0] = A + 2
+    assert call(*a) == 3                                   # misaligned x
+    a = list(base); a[11] = 200
+    assert call(*a) == 1                                   # D % 128
+    a = list(base); a[14] = 5
+    assert call(*a) == 1                                   # bad dtype
+    a = list(base); a[1] = A
+    assert call(*a) == 1                                   # scales given for bf16
+    a = list(base); a[9] = 0
+    assert call(*a) == 0                                   # T == 0: no-op
+    a = list(base); a[17] = 16
+    assert call(*a) in (5, 7)                              # workspace too small (or no device here)
