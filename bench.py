@@ -1,0 +1,413 @@
+#!/usr/bin/env python
+"""Benchmark of the routed MoE SwiGLU FFN forward pass on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode]
+                    [--pipeline split] [--impl ours|reference]
+
+One step = one full forward pass (routing, gather + zero-fill, up-projection
+with SwiGLU, down-projection with the weighted reduction) over one batch of
+seeded synthetic inputs already resident in HBM.  Prints ONE JSON line on
+rank 0.  Under torchrun each rank runs its own token batch against its own
+copy of the weights (the path shards by tokens, no collective on the data
+path): weak scaling, value = all ranks' FLOPs / max-over-ranks time.
+
+--impl reference times the CPU oracle (fp64, OpenMP) on the host cores, on a
+bounded sample of tokens per step, with the same metric and workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE FFN fwd TFLOP/s & tokens/s on 1×GB300; % of roofline (tensor or HBM)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+STAGES = ["route", "gather_zero", "up_swiglu", "down_reduce"]
+KERNELS_PER_STEP = {"split": 6}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--pipeline", choices=["split", "fused"], default="split")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic(w, ids):
+    """Compulsory bytes and FLOPs of the whole step and of each GEMM kernel."""
+    import numpy as np
+    P = w.T * w.k
+    live = int(np.unique(ids).size)
+    eb = 2 if w.dtype == "bf16" else 1
+    sfb = 0 if w.dtype == "bf16" else 1.0 / 32
+    elem = eb + sfb
+    step_bytes = (w.T * w.D * elem + live * 3 * w.H * w.D * elem + P * 8 + w.T * w.D * 2)
+    up_bytes = live * 2 * w.H * w.D * elem + P * w.D * elem + P * w.H * elem
+    down_bytes = live * w.D * w.H * elem + P * w.H * elem + w.T * w.D * 2
+    return {
+        "step_flops": 6.0 * P * w.D * w.H, "step_bytes": float(step_bytes),
+        "up_swiglu": {"flops": 4.0 * P * w.D * w.H, "bytes": float(up_bytes)},
+        "down_reduce": {"flops": 2.0 * P * w.D * w.H, "bytes": float(down_bytes)},
+        "live_experts": live,
+    }
+
+
+def source_digest(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "up_swiglu": ["grouped_gemm_gb300/csrc/gemm_bf16.cu", "grouped_gemm_gb300/csrc/ptx.cuh",
+                  "grouped_gemm_gb300/csrc/internal.h"],
+    "down_reduce": ["grouped_gemm_gb300/csrc/gemm_bf16.cu", "grouped_gemm_gb300/csrc/ptx.cuh",
+                    "grouped_gemm_gb300/csrc/internal.h"],
+}
+
+
+def traffic_from_profiles(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
+    sources are unchanged since the capture; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    d = re.search(r"source_digest:\s*([0-9a-f]+)", text)
+    if not m or not d or d.group(1) != source_digest(KERNEL_SOURCES.get(kernel, [])):
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, gpu_index):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                self.samples.append((time.time(), float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                pass
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not inside:
+            return None
+        sm = [s[1] for s in inside]
+        reasons = sorted({self.NAMES[i] for s in inside for i, v in enumerate(s[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(s[2] for s in inside), "reasons": reasons,
+                "samples": len(inside)}
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import grouped_gemm_gb300 as moe
+    from grouped_gemm_gb300 import workloads as wl
+
+    torch.cuda.set_device(local_rank)
+    inp = wl.make_inputs(args.workload, seed=rank)
+    w = inp["workload"]
+    if w.dtype != "bf16" or args.pipeline != "split":
+        raise SystemExit(f"workload {args.workload} / pipeline {args.pipeline} not built yet")
+    dev = {k: torch.from_numpy(inp[k].view(np.int16)).cuda() for k in ("x", "w1", "w2")}
+    ids = torch.from_numpy(inp["topk_ids"]).cuda()
+    tw = torch.from_numpy(inp["topk_w"]).cuda()
+    out = torch.empty(w.T, w.D, dtype=torch.bfloat16, device="cuda")
+    pipeline = moe.MOE_SPLIT
+    ws = moe.alloc_workspace(w.T, w.E, w.D, w.H, w.k, moe.MOE_BF16, pipeline)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        moe.moe_ffn_forward(dev["x"], dev["w1"], dev["w2"], ids, tw, out, E=w.E, D=w.D, H=w.H, k=w.k,
+                            workspace=ws, dtype=moe.MOE_BF16, pipeline=pipeline, stream=stream)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    st = moe.moe_ffn_sync_status(ws)
+    if st != 0:
+        raise SystemExit(f"device status after warm-up: {moe.moe_ffn_status_string(st)}")
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    ev1.synchronize()
+    t_host1 = time.time()
+    torch.cuda.synchronize()
+    barrier()
+    ms_total = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms_total], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms = ms_total / args.steps
+    # keep the same step running so the clock sampler sees load for >= 1.5 s
+    t_sus0 = time.time()
+    while time.time() - t_sus0 < 1.5:
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize()
+    t_sus1 = time.time()
+    if sampler:
+        time.sleep(0.2)
+        sampler.stop()
+    st = moe.moe_ffn_sync_status(ws)
+    if st != 0:
+        raise SystemExit(f"device status after timing: {moe.moe_ffn_status_string(st)}")
+
+    alg = algorithmic(w, inp["topk_ids"])
+    flops_all = alg["step_flops"] * world
+    value = flops_all / (ms * 1e-3) / 1e12
+    tokens_per_s = w.T * world / (ms * 1e-3)
+
+    # per-stage durations from library-recorded CUDA events on the same stream
+    moe.moe_ffn_profile_enable(True)
+    per = []
+    for _ in range(min(args.steps, 30)):
+        step()
+        per.append(moe.moe_ffn_profile_read())
+    moe.moe_ffn_profile_enable(False)
+    stage_ms = {name: statistics.median(p[i] for p in per) for i, name in enumerate(STAGES) if len(per[0]) > i}
+
+    peaks, peak_src = load_peaks()
+    dom = max(("up_swiglu", "down_reduce"), key=lambda s: stage_ms.get(s, 0.0))
+    kd = alg[dom]
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    tensor_bound = kd["flops"] / kd["bytes"] > ridge
+    t_dom = stage_ms[dom] * 1e-3
+    if tensor_bound:
+        achieved, peak, unit = kd["flops"] / t_dom / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved, peak, unit = kd["bytes"] / t_dom / 1e9, peaks["hbm_gbs"], "GB/s"
+    roofline = {"bound": "tensor" if tensor_bound else "hbm", "kernel": dom, "achieved": round(achieved, 1),
+                "peak": peak, "peak_source": peak_src, "unit": unit, "frac": round(achieved / peak, 4),
+                "traffic": traffic_from_profiles(dom, args.workload),
+                "algorithmic_per_launch": kd["flops"] if tensor_bound else kd["bytes"],
+                "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()}}
+    step_bound = max(alg["step_flops"] / (peaks["bf16_tflops"] * 1e12), alg["step_bytes"] / (peaks["hbm_gbs"] * 1e9))
+
+    # end to end: host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        xh = torch.from_numpy(inp["x"].view(np.int16)).pin_memory()
+        idh = torch.from_numpy(inp["topk_ids"]).pin_memory()
+        twh = torch.from_numpy(inp["topk_w"]).pin_memory()
+        outh = torch.empty(w.T, w.D, dtype=torch.bfloat16).pin_memory()
+
+        def e2e_step():
+            dev["x"].copy_(xh, non_blocking=True)
+            ids.copy_(idh, non_blocking=True)
+            tw.copy_(twh, non_blocking=True)
+            step()
+            outh.copy_(out, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        n_e2e = max(1, min(args.steps, 100))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        e1.synchronize()
+        e_ms = e0.elapsed_time(e1) / n_e2e
+        if world > 1:
+            t = torch.tensor([e_ms], device="cuda")
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": round(flops_all / (e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(xh.numel() * 2 + idh.numel() * 4 + twh.numel() * 4),
+               "d2h_bytes_per_step": int(outh.numel() * 2), "ms_per_step": round(e_ms, 4),
+               "resident": "expert weights stay in HBM (model parameters)"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp, w, budget_s=12.0)
+
+    if rank != 0:
+        return None
+    clocks = sampler.summary(t_host0, t_host1) if sampler else None
+    if clocks is None and sampler:
+        clocks = sampler.summary(t_sus0, t_sus1)
+        if clocks is not None:
+            clocks["window"] = "the same step run for 1.5 s right after the timed region"
+    return {
+        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "tokens_per_s": round(tokens_per_s, 1),
+        "roofline_step_frac": round(step_bound / (ms * 1e-3), 4),
+        "config": {"workload": w.name, "T": w.T, "D": w.D, "H": w.H, "E": w.E, "k": w.k, "routing": w.routing,
+                   "pipeline": args.pipeline, "seed": "rank", "parallelism": f"token-sharded x{world}",
+                   "l2": (f"inputs larger than L2: {alg['step_bytes'] / 1e9:.2f} GB compulsory per step "
+                          f"(129 MB L2), no flush needed")},
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": KERNELS_PER_STEP["split"] * args.steps, "clocks": clocks,
+    }
+
+
+def cpu_baseline(inp, w, budget_s=12.0):
+    """The oracle, as it stands, on the host cores over a bounded token sample."""
+    import numpy as np
+
+    import oracle
+    per_tok = 6.0 * w.k * w.D * w.H
+    n = 1
+    t0 = time.time()
+    oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], inp["topk_ids"], inp["topk_w"], act=oracle.ACT_BF16,
+                   tokens=np.arange(n, dtype=np.int32))
+    t1 = max(time.time() - t0, 1e-3)
+    cores = oracle.max_threads()
+    n = int(min(w.T, max(cores, budget_s / t1 * 0.9)))
+    n = max(1, n // cores * cores) if n >= cores else n
+    toks = np.sort(np.random.default_rng(123).choice(w.T, n, replace=False)).astype(np.int32)
+    t0 = time.time()
+    oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], inp["topk_ids"], inp["topk_w"], act=oracle.ACT_BF16,
+                   tokens=toks)
+    dt = time.time() - t0
+    return {"value": round(per_tok * n / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {w.T} tokens of the {w.name} workload (all k={w.k} experts each), {dt:.1f} s",
+            "tokens_per_s": round(n / dt, 3)}
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, rank):
+    if rank != 0:
+        return None
+    import numpy as np
+
+    import oracle
+    from grouped_gemm_gb300 import workloads as wl
+    inp = wl.make_inputs(args.workload, seed=0)
+    w = inp["workload"]
+    cores = oracle.max_threads()
+    per_tok = 6.0 * w.k * w.D * w.H
+    # tokens per step: about one second of CPU work
+    t0 = time.time()
+    oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], inp["topk_ids"], inp["topk_w"], act=oracle.ACT_BF16,
+                   tokens=np.arange(min(cores, w.T), dtype=np.int32))
+    t_one = max(time.time() - t0, 1e-3)
+    n = int(max(1, min(w.T, min(cores, w.T) * max(1.0, 1.0 / t_one))))
+    order = np.random.default_rng(7).permutation(w.T).astype(np.int32)
+
+    def step(i):
+        toks = np.sort(np.take(order, np.arange(i * n, (i + 1) * n) % w.T))
+        oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], inp["topk_ids"], inp["topk_w"], act=oracle.ACT_BF16,
+                       tokens=toks)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.time()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = time.time() - t0
+    ms = dt * 1e3 / args.steps
+    value = per_tok * n / (ms * 1e-3) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "D": w.D, "H": w.H, "E": w.E, "k": w.k, "routing": w.routing,
+                   "pipeline": args.pipeline, "seed": 0, "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} tokens of the {w.name} workload per step (all k={w.k} experts each)"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank)
+    else:
+        if world > 1:
+            import torch
+            torch.cuda.set_device(local_rank)
+            torch.distributed.init_process_group(backend="nccl", device_id=torch.device("cuda", local_rank))
+        line = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+    if line is not None and rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()
