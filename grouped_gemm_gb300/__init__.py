@@ -14,7 +14,7 @@ import threading
 
 __all__ = [
     "MOE_BF16", "MOE_MXFP8", "MOE_FUSED", "MOE_SPLIT", "MoeFFNError", "library_path", "lib",
-    "moe_ffn_workspace_size", "moe_ffn_workspace_init", "moe_ffn_forward", "moe_ffn_route",
+    "moe_ffn_workspace_size", "moe_ffn_workspace_init", "moe_ffn_forward", "moe_ffn_route", "moe_ffn_route_noalloc",
     "moe_ffn_sync_status", "moe_ffn_set_wait_limit_ns", "moe_ffn_profile_enable", "moe_ffn_profile_read", "moe_ffn_status_string", "alloc_workspace",
 ]
 
@@ -57,6 +57,8 @@ def lib() -> ctypes.CDLL:
             L.moe_ffn_forward.restype = i
             L.moe_ffn_route.argtypes = [vp, vp, i, i, i, vp, vp, vp, vp, sz, vp]
             L.moe_ffn_route.restype = i
+            L.moe_ffn_route_noalloc.argtypes = [vp, vp, i, i, i, vp, vp, vp, vp, vp]
+            L.moe_ffn_route_noalloc.restype = i
             L.moe_ffn_sync_status.argtypes = [vp, vp]
             L.moe_ffn_sync_status.restype = i
             L.moe_ffn_set_wait_limit_ns.argtypes = [c.c_uint64]
@@ -134,6 +136,16 @@ def moe_ffn_route(topk_ids, topk_w, T, E, k, counts, offsets, slot_of_pair, work
     st = lib().moe_ffn_route(_p(topk_ids), _p(topk_w), T, E, k, _p(counts), _p(offsets), _p(slot_of_pair),
                              _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     return _check(st, "moe_ffn_route") if check else st
+
+
+def moe_ffn_route_noalloc(topk_ids, topk_w, T, E, k, counts, offsets, slot_of_pair, status_bits=None, stream=None,
+                          check=True) -> int:
+    """Routing permutation without a caller workspace, for callers that
+    cannot allocate device memory (scratch is a fixed array inside the
+    library; T*k <= 131072).  Calls on one device must not overlap."""
+    st = lib().moe_ffn_route_noalloc(_p(topk_ids), _p(topk_w), T, E, k, _p(counts), _p(offsets),
+                                     _p(slot_of_pair), _p(status_bits), _stream(stream))
+    return _check(st, "moe_ffn_route_noalloc") if check else st
 
 
 def moe_ffn_sync_status(workspace, stream=None) -> int:

@@ -86,6 +86,28 @@ moe_status_t moe_ffn_route(const int32_t* topk_ids, const float* topk_w, int T, 
                            int32_t* offsets, int32_t* slot_of_pair, void* workspace, size_t workspace_bytes,
                            void* stream);
 
+/* The routing permutation, for callers that cannot allocate device memory.
+ * The paper has no counterpart to this entry point.
+ *
+ * Same results as moe_ffn_route, but the scratch lives in a fixed 6 MiB
+ * device array inside this library instead of a caller workspace, for callers
+ * that cannot call cudaMalloc or hand over a buffer of their own (graph
+ * capture under an allocator that forbids new allocations, runtimes whose
+ * device memory is planned ahead of time).  Inputs and the output arrays are
+ * still the caller's.  Limits: T*k <= 131072 pairs and E <= 1024; larger
+ * problems return MOE_ERR_WORKSPACE_TOO_SMALL without launching anything.
+ * status_bits (optional, device int32) receives the call's device error bits:
+ * 0, or bit 0 set when an expert id was outside [0, E).
+ * The first call on each device looks up the array's device address (setup
+ * done once per device, with that device current); make that first call
+ * before any stream capture.  The call allocates nothing.  All calls on a
+ * device share the array and it keeps the last call's contents: calls that
+ * overlap on the GPU (several streams or host threads at once) race and give
+ * wrong results. */
+moe_status_t moe_ffn_route_noalloc(const int32_t* topk_ids, const float* topk_w, int T, int E, int k,
+                                   int32_t* counts, int32_t* offsets, int32_t* slot_of_pair, int32_t* status_bits,
+                                   void* stream);
+
 /* Synchronize `stream`, then return (and clear) the device status recorded in
  * the workspace since the last call: MOE_OK, MOE_ERR_BAD_ROUTING or
  * MOE_ERR_DEVICE_TIMEOUT.  MOE_ERR_CUDA if synchronization itself failed. */
