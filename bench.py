@@ -32,8 +32,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE FFN fwd TFLOP/s & tokens/s on 1×GB300; % of roofline (tensor or HBM)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-STAGES = ["route", "gather_zero", "up_swiglu", "down_reduce"]
-KERNELS_PER_STEP = {"split": 6}
+STAGES = {"split": ["route", "gather_zero", "up_swiglu", "down_reduce"],
+          "fused": ["route", "gather_zero", "fused_gemm", "to_bf16"]}
+KERNELS_PER_STEP = {"split": 6, "fused": 6}
 
 
 def parse_args():
@@ -167,13 +168,13 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     inp = wl.make_inputs(args.workload, seed=rank)
     w = inp["workload"]
-    if w.dtype != "bf16" or args.pipeline != "split":
-        raise SystemExit(f"workload {args.workload} / pipeline {args.pipeline} not built yet")
+    if w.dtype != "bf16":
+        raise SystemExit(f"workload {args.workload} ({w.dtype}) not built yet")
     dev = {k: torch.from_numpy(inp[k].view(np.int16)).cuda() for k in ("x", "w1", "w2")}
     ids = torch.from_numpy(inp["topk_ids"]).cuda()
     tw = torch.from_numpy(inp["topk_w"]).cuda()
     out = torch.empty(w.T, w.D, dtype=torch.bfloat16, device="cuda")
-    pipeline = moe.MOE_SPLIT
+    pipeline = moe.MOE_SPLIT if args.pipeline == "split" else moe.MOE_FUSED
     ws = moe.alloc_workspace(w.T, w.E, w.D, w.H, w.k, moe.MOE_BF16, pipeline)
     stream = torch.cuda.current_stream()
 
@@ -238,11 +239,17 @@ def run_ours(args, rank, world, local_rank):
         step()
         per.append(moe.moe_ffn_profile_read())
     moe.moe_ffn_profile_enable(False)
-    stage_ms = {name: statistics.median(p[i] for p in per) for i, name in enumerate(STAGES) if len(per[0]) > i}
+    names = STAGES[args.pipeline]
+    stage_ms = {name: statistics.median(p[i] for p in per) for i, name in enumerate(names) if len(per[0]) > i}
 
     peaks, peak_src = load_peaks()
-    dom = max(("up_swiglu", "down_reduce"), key=lambda s: stage_ms.get(s, 0.0))
-    kd = alg[dom]
+    if args.pipeline == "split":
+        dom = max(("up_swiglu", "down_reduce"), key=lambda s: stage_ms.get(s, 0.0))
+        kd = alg[dom]
+    else:
+        dom = "fused_gemm"
+        kd = {"flops": alg["up_swiglu"]["flops"] + alg["down_reduce"]["flops"],
+              "bytes": alg["step_bytes"]}
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     tensor_bound = kd["flops"] / kd["bytes"] > ridge
     t_dom = stage_ms[dom] * 1e-3
@@ -315,7 +322,7 @@ def run_ours(args, rank, world, local_rank):
                    "l2": (f"inputs larger than L2: {alg['step_bytes'] / 1e9:.2f} GB compulsory per step "
                           f"(129 MB L2), no flush needed")},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": KERNELS_PER_STEP["split"] * args.steps, "clocks": clocks,
+        "gpu_launches": KERNELS_PER_STEP[args.pipeline] * args.steps, "clocks": clocks,
     }
 
 

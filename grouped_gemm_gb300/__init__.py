@@ -15,7 +15,7 @@ import threading
 __all__ = [
     "MOE_BF16", "MOE_MXFP8", "MOE_FUSED", "MOE_SPLIT", "MoeFFNError", "library_path", "lib",
     "moe_ffn_workspace_size", "moe_ffn_workspace_init", "moe_ffn_forward", "moe_ffn_route", "moe_ffn_route_noalloc",
-    "moe_ffn_sync_status", "moe_ffn_set_wait_limit_ns", "moe_ffn_profile_enable", "moe_ffn_profile_read", "moe_ffn_status_string", "alloc_workspace",
+    "moe_ffn_sync_status", "moe_ffn_set_wait_limit_ns", "moe_ffn_profile_enable", "moe_ffn_profile_read", "moe_ffn_set_option", "MOE_OPT_GATHER", "moe_ffn_status_string", "alloc_workspace",
 ]
 
 MOE_BF16, MOE_MXFP8 = 0, 1
@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
             L.moe_ffn_sync_status.restype = i
             L.moe_ffn_set_wait_limit_ns.argtypes = [c.c_uint64]
             L.moe_ffn_set_wait_limit_ns.restype = None
+            L.moe_ffn_set_option.argtypes = [i, c.c_longlong]
+            L.moe_ffn_set_option.restype = i
             L.moe_ffn_profile_enable.argtypes = [i]
             L.moe_ffn_profile_enable.restype = i
             L.moe_ffn_profile_read.argtypes = [c.POINTER(c.c_float), i, c.POINTER(c.c_int)]
@@ -151,6 +153,14 @@ def moe_ffn_route_noalloc(topk_ids, topk_w, T, E, k, counts, offsets, slot_of_pa
 def moe_ffn_sync_status(workspace, stream=None) -> int:
     """Synchronize and return (and clear) the device-side status: 0, 4 or 6."""
     return int(lib().moe_ffn_sync_status(_p(workspace), _stream(stream)))
+
+
+MOE_OPT_GATHER = 0
+MOE_OPT_L2_PREFETCH = 1
+
+
+def moe_ffn_set_option(option: int, value: int) -> int:
+    return _check(lib().moe_ffn_set_option(int(option), int(value)), "moe_ffn_set_option")
 
 
 def moe_ffn_profile_enable(on: bool) -> int:

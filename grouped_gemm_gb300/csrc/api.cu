@@ -17,6 +17,8 @@ namespace moe {
 namespace {
 
 std::atomic<unsigned long long> g_wait_limit_ns{2000ull * 1000 * 1000};
+std::atomic<int> g_gather_mode{0};  // MOE_OPT_GATHER: 0 gather kernel, 1 in-GEMM gather4
+std::atomic<int> g_prefetch{0};     // MOE_OPT_L2_PREFETCH (measured slower on GB300: off)
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -42,7 +44,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // Row-major bf16 matrix [rows, cols] read in boxes of [box_rows, 64] with the
-// 128-byte swizzle (64 bf16 = one 128-byte swizzle row).
+// 128-byte swizzle (64 bf16 = one 128-byte swizzle row).  box_rows == 1 is the
+// one-row box tile::gather4 requires.
 bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
@@ -113,11 +116,54 @@ Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipe
   if (pipeline == MOE_SPLIT) {
     w.xg = take((size_t)w.S_max * D * 2);
     w.act = take((size_t)w.S_max * H * 2);
+  } else {
+    w.xg = take((size_t)w.S_max * D * 2);
+    w.acc_f32 = take((size_t)T * D * 4);
   }
   w.bytes = off;
   return w;
 }
 
+namespace {
+
+// Fused pipeline: routing, gather (+ zero-fill of the fp32 accumulator), one
+// GEMM kernel that keeps act on chip, rounding of the accumulator to bf16.
+moe_status_t forward_fused_bf16(const Workspace& ws, const void* x, const void* w1, const void* w2,
+                                const int32_t* topk_ids, const float* topk_w, void* out, int T, int E, int D, int H,
+                                int k, int sms, cudaStream_t st) {
+  CUtensorMap map_xg, map_w1, map_w2;
+  if (!make_map_bf16(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, kBM) ||
+      !make_map_bf16(&map_w1, w1, (uint64_t)E * 2 * H, (uint64_t)D, kUpFold) ||
+      !make_map_bf16(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, kDownN))
+    return MOE_ERR_CUDA;
+  prof_mark(st, 0);
+  cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  prof_mark(st, 1);
+  e = launch_gather_zero(ws, x, D, ws.acc_f32, (int64_t)T * D * 4, sms * 4, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  prof_mark(st, 2);
+  FusedArgs fa{};
+  fa.meta = ws.meta;
+  fa.expert_of_rb = ws.expert_of_rb;
+  fa.row_tok = ws.row_tok;
+  fa.slot_w = ws.slot_w;
+  fa.out_f32 = ws.acc_f32;
+  fa.err = ws.err;
+  fa.wait_limit_ns = g_wait_limit_ns.load();
+  fa.D = D;
+  fa.H = H;
+  fa.n_slices = H / 128;
+  const int grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * fa.n_slices);
+  e = launch_fused_bf16(map_xg, map_w1, map_w2, fa, grid, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  prof_mark(st, 3);
+  e = launch_f32_to_bf16(ws.acc_f32, out, (int64_t)T * D, sms * 4, st);
+  prof_mark(st, 4);
+  return cuda_status(e);
+}
+
+}  // namespace
 }  // namespace moe
 
 using namespace moe;
@@ -137,6 +183,20 @@ moe_status_t moe_ffn_workspace_init(void* workspace, size_t workspace_bytes, voi
 }
 
 void moe_ffn_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1); }
+
+moe_status_t moe_ffn_set_option(int option, long long value) {
+  switch (option) {
+    case MOE_OPT_GATHER:
+      if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
+      g_gather_mode.store((int)value);
+      return MOE_OK;
+    case MOE_OPT_L2_PREFETCH:
+      if (value < 0 || value > 64) return MOE_ERR_INVALID_ARG;
+      g_prefetch.store((int)value);
+      return MOE_OK;
+  }
+  return MOE_ERR_INVALID_ARG;
+}
 
 moe_status_t moe_ffn_route(const int32_t* topk_ids, const float* topk_w, int T, int E, int k, int32_t* counts,
                            int32_t* offsets, int32_t* slot_of_pair, void* workspace, size_t workspace_bytes,
@@ -174,27 +234,36 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   if (!aligned16(x) || !aligned16(w1) || !aligned16(w2) || !aligned16(out) || !aligned16(workspace) ||
       (reinterpret_cast<uintptr_t>(topk_ids) & 3u) || (reinterpret_cast<uintptr_t>(topk_w) & 3u))
     return MOE_ERR_MISALIGNED;
-  if (dtype != MOE_BF16 || pipeline != MOE_SPLIT) return MOE_ERR_UNSUPPORTED;
+  if (dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if (D % kDownN != 0) return MOE_ERR_UNSUPPORTED;
   Workspace ws = plan_workspace(workspace, T, E, D, H, k, pipeline);
   if (workspace_bytes < ws.bytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
   const int sms = num_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (pipeline == MOE_FUSED) return forward_fused_bf16(ws, x, w1, w2, topk_ids, topk_w, out, T, E, D, H, k, sms, st);
 
+  const bool gather4 = g_gather_mode.load() == 1;
   CUtensorMap map_xg, map_w1, map_act, map_w2;
-  if (!make_map_bf16(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, kBM) ||
+  const bool map_a_ok = gather4 ? make_map_bf16(&map_xg, x, (uint64_t)T, (uint64_t)D, 1)
+                                : make_map_bf16(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, kBM);
+  if (!map_a_ok ||
       !make_map_bf16(&map_w1, w1, (uint64_t)E * 2 * H, (uint64_t)D, kUpFold) ||
       !make_map_bf16(&map_act, ws.act, (uint64_t)ws.S_max, (uint64_t)H, kBM) ||
       !make_map_bf16(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, kDownN))
     return MOE_ERR_CUDA;
 
   prof_mark(st, 0);
-  cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st);
+  // With the in-GEMM gather the routing launch also zero-fills out;
+  // otherwise the gather kernel does.
+  cudaError_t e = gather4 ? launch_route(ws, topk_ids, topk_w, T, E, k, st, out, (int64_t)T * D * 2, sms * 2)
+                          : launch_route(ws, topk_ids, topk_w, T, E, k, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 1);
-  e = launch_gather_zero(ws, x, D, out, (int64_t)T * D * 2, sms * 4, st);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (!gather4) {
+    e = launch_gather_zero(ws, x, D, out, (int64_t)T * D * 2, sms * 4, st);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
   prof_mark(st, 2);
 
   GemmArgs ga{};
@@ -208,12 +277,13 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   ga.wait_limit_ns = g_wait_limit_ns.load();
   ga.D = D;
   ga.H = H;
+  ga.prefetch = g_prefetch.load();
 
   GemmArgs up = ga;
   up.n_col_tiles = H / kUpFold;
   up.k_blocks = D / kBK;
   const int up_grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * up.n_col_tiles);
-  e = launch_up_bf16(map_xg, map_w1, up, up_grid, st);
+  e = launch_up_bf16(map_xg, map_w1, up, up_grid, st, gather4);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 3);
 

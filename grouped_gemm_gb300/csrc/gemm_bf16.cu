@@ -3,22 +3,25 @@
 // UP  (GEMM1 + SwiGLU): for each 128-row block rb of the sorted, padded token
 //     order (expert e = expert_of_rb[rb]) and each column tile j, the
 //     accumulator holds [gate rows j*G .. +G | up rows H + j*G .. +G] of
-//     W1[e] times the 128 gathered rows, so both halves of every SwiGLU pair
-//     sit in the same TMEM accumulator ("Prime Flash MoE", sec. 2 "Trick 1":
-//     gate and up interleaved per 128-row block; here the interleave is two
-//     TMA boxes into adjacent shared-memory rows).  The epilogue computes
-//     act = silu(gate) * up in fp32, rounds to bf16 and stores act[slot, j*G..]
-//     (sec. 5 "SwiGLU", sec. 6: the split pipeline writes act once).
+//     W1[e] times the 128 routed rows, so both halves of every SwiGLU pair sit
+//     in the same TMEM accumulator ("Prime Flash MoE", sec. 2 "Trick 1": gate
+//     and up interleaved per 128-row block; here the interleave is two TMA
+//     boxes into adjacent shared-memory rows).  The 128 token rows arrive
+//     either with tile::gather4 straight from x (four rows per instruction,
+//     sec. 3 "For the tokens: TMA gathers them too") or as a plain tile of the
+//     pre-gathered xg (sec. 6).  The epilogue computes act = silu(gate) * up
+//     in fp32, rounds to bf16 and stores act[slot, j*G..] (sec. 5 "SwiGLU",
+//     sec. 6: the split pipeline writes act once).
 // DOWN (GEMM2 + weighted reduce): for each row block and 256-column tile of
 //     D, acc = act[rb rows, :] * W2[e][cols, :]^T over all of H (sec. 6 "The
-//     down-projection kernel": C = 1, no split-K); the epilogue scales row r
-//     by its routing weight in fp32, rounds to bf16 and reduces into
-//     out[row_tok[r], cols] with 16-byte red.global.add.noftz.v4.bf16x2
-//     (sec. 5 "The same three jobs without the staging buffer"): one
-//     instruction does the top-k sum and the scatter back to token order.
+//     down-projection kernel": C = 1, no split-K).  The epilogue scales row r
+//     by its routing weight in fp32, rounds to bf16 into a padded shared
+//     staging row and reduces the whole 512-byte row into out[row_tok[r]] with
+//     one cp.reduce.async.bulk .add.bf16 (sec. 5 "Three jobs - one
+//     instruction": the top-k sum and the scatter back to token order).
 //
 // Warp roles (192 threads, one CTA per SM, persistent over a static tile list):
-//   warp 0      TMA producer (one lane): A and B tiles into a STAGES-deep ring
+//   warp 0      TMA producer: A and B tiles into a STAGES-deep ring
 //   warp 1      TMEM allocator; one lane issues tcgen05.mma (M=128, K=16)
 //   warps 2..5  epilogue: tcgen05.ld of the warp's 32 TMEM lanes (= rows)
 // The accumulator is double-buffered in TMEM (2 x N columns) so the epilogue
@@ -40,10 +43,16 @@ struct GemmCfg {
   static constexpr int kBBytes = N * kBK * 2;               // N rows of 128 B
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * N;                   // double-buffered accumulator
-  static constexpr int kSmemBytes = 1024 /*align slack*/ + STAGES * kStageBytes + 256 /*barriers*/;
+  // DOWN stages each output row (N bf16) in shared memory for the bulk
+  // reduction; +16 B per row keeps the 32 rows of a warp on distinct banks.
+  static constexpr int kStageRowBytes = N * 2 + 16;
+  static constexpr int kStagingBytes = MODE == kModeDown ? kBM * kStageRowBytes : 0;
+  static constexpr int kBarrierBytes = 256;
+  static constexpr int kSmemBytes = 1024 /*align slack*/ + STAGES * kStageBytes + kStagingBytes + kBarrierBytes;
   static_assert(N % 32 == 0 && N >= 32 && N <= 256, "MMA N");
   static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns: power of two <= 512");
   static_assert(kSmemBytes <= 232448, "shared memory");
+  static_assert((2 * STAGES + 5) * 8 + 8 <= kBarrierBytes, "barrier area");
 };
 
 constexpr int kThreads = 192;
@@ -54,7 +63,7 @@ __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 
 __device__ __forceinline__ float swiglu(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
 
-template <int MODE, int N, int STAGES>
+template <int MODE, int N, int STAGES, bool GATHER>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                              const GemmArgs args) {
@@ -63,7 +72,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * Cfg::kABytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * Cfg::kStageBytes);
+  uint8_t* sStage = smem + STAGES * Cfg::kStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + Cfg::kStagingBytes);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -103,41 +113,86 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = num_rb * args.n_col_tiles;
   const int KB = args.k_blocks;
 
-  if (warp == 0 && lane == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (MODE == kModeDown) griddep_wait();  // act is written by the previous grid
+    if (MODE == kModeDown && lane == 0) griddep_wait();  // act is written by the previous grid
+    __syncwarp();
     int s = 0;
     uint32_t ph = 0;
     int issued_phase[STAGES];
 #pragma unroll
     for (int i = 0; i < STAGES; ++i) issued_phase[i] = -1;
     bool ok = true;
+    // L2 prefetch cursor: runs args.prefetch k-blocks ahead of the loads
+    // (across tile boundaries) so that tiles land in L2 before the ring needs
+    // them -- more bytes in flight than the shared-memory ring can hold.
+    int pf_tile = blockIdx.x, pf_kb = 0, pf_e = pf_tile < n_tiles ? args.expert_of_rb[pf_tile / args.n_col_tiles] : 0;
+    auto prefetch_one = [&]() {
+      if (pf_tile >= n_tiles) return;
+      const int prb = pf_tile / args.n_col_tiles, pj = pf_tile % args.n_col_tiles;
+      if (!GATHER) tma_prefetch_2d(&map_a, pf_kb * kBK, prb * kBM);
+      if (MODE == kModeUp) {
+        constexpr int G = N / 2;
+        const int row0 = pf_e * 2 * args.H + pj * G;
+        tma_prefetch_2d(&map_b, pf_kb * kBK, row0);
+        tma_prefetch_2d(&map_b, pf_kb * kBK, row0 + args.H);
+      } else {
+        tma_prefetch_2d(&map_b, pf_kb * kBK, pf_e * args.D + pj * N);
+      }
+      if (++pf_kb == KB) {
+        pf_kb = 0;
+        pf_tile += gridDim.x;
+        if (pf_tile < n_tiles) pf_e = args.expert_of_rb[pf_tile / args.n_col_tiles];
+      }
+    };
+    if (lane == 0)
+      for (int i = 0; i < args.prefetch; ++i) prefetch_one();
     for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
       const int rb = tile / args.n_col_tiles, j = tile % args.n_col_tiles;
       const int e = args.expert_of_rb[rb];
+      int g0 = 0, g1 = 0, g2 = 0, g3 = 0;
+      if (GATHER) {  // lane l fetches tile rows 4l..4l+3; padding rows read row 0
+        const int* rt = args.row_tok + (int64_t)rb * kBM + lane * 4;
+        g0 = max(rt[0], 0);
+        g1 = max(rt[1], 0);
+        g2 = max(rt[2], 0);
+        g3 = max(rt[3], 0);
+      }
       for (int kb = 0; kb < KB; ++kb) {
-        if (!mbar_wait(&empty[s], ph ^ 1u, wc, 1)) {
+        int got = 1;
+        if (lane == 0) {
+          got = mbar_wait(&empty[s], ph ^ 1u, wc, 1) ? 1 : 0;
+          if (got) mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
+        }
+        got = __shfl_sync(0xffffffffu, got, 0);
+        if (!got) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
-        tma_load_2d(sA + s * Cfg::kABytes, &map_a, &full[s], kb * kBK, rb * kBM);
-        if (MODE == kModeUp) {
-          constexpr int G = N / 2;
-          const int row0 = e * 2 * args.H + j * G;
-          tma_load_2d(sB + s * Cfg::kBBytes, &map_b, &full[s], kb * kBK, row0);
-          tma_load_2d(sB + s * Cfg::kBBytes + G * kBK * 2, &map_b, &full[s], kb * kBK, row0 + args.H);
-        } else {
-          tma_load_2d(sB + s * Cfg::kBBytes, &map_b, &full[s], kb * kBK, e * args.D + j * N);
+        if (GATHER) {
+          tma_gather4(sA + s * Cfg::kABytes + lane * 4 * kBK * 2, &map_a, &full[s], kb * kBK, g0, g1, g2, g3);
+        } else if (lane == 0) {
+          tma_load_2d(sA + s * Cfg::kABytes, &map_a, &full[s], kb * kBK, rb * kBM);
         }
-        issued_phase[s] = (int)ph;
+        if (lane == 0) {
+          if (args.prefetch > 0) prefetch_one();
+          if (MODE == kModeUp) {
+            constexpr int G = N / 2;
+            const int row0 = e * 2 * args.H + j * G;
+            tma_load_2d(sB + s * Cfg::kBBytes, &map_b, &full[s], kb * kBK, row0);
+            tma_load_2d(sB + s * Cfg::kBBytes + G * kBK * 2, &map_b, &full[s], kb * kBK, row0 + args.H);
+          } else {
+            tma_load_2d(sB + s * Cfg::kBBytes, &map_b, &full[s], kb * kBK, e * args.D + j * N);
+          }
+          issued_phase[s] = (int)ph;
+        }
         if (++s == STAGES) {
           s = 0;
           ph ^= 1u;
         }
       }
     }
-    if (!ok) {  // let every copy already in flight land before the CTA exits
+    if (!ok && lane == 0) {  // let every copy already in flight land before the CTA exits
       for (int i = 0; i < STAGES; ++i)
         if (issued_phase[i] >= 0) mbar_wait_drain(&full[i], (uint32_t)issued_phase[i], kDrainNs);
     }
@@ -188,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;  // TMEM lanes this warp may access
     const int row = quad * 32 + lane;
     const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
+    uint8_t* my_stage = sStage + row * Cfg::kStageRowBytes;
     int it = 0;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
       const int acc = it & 1;
@@ -216,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         const float w = args.slot_w[slot];
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(args.out) + (int64_t)(tok < 0 ? 0 : tok) * args.D + j * N;
+        bulk_wait_read_all();  // the previous tile's reduction has left the staging row
 #pragma unroll 1
         for (int c = 0; c < N / 32; c += 2) {
           uint32_t v0[32], v1[32];
@@ -224,22 +280,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (tok >= 0) {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              red_add_bf16x8(dst + c * 32 + q * 8, pack_bf16x2(w * u2f(v0[8 * q + 0]), w * u2f(v0[8 * q + 1])),
-                             pack_bf16x2(w * u2f(v0[8 * q + 2]), w * u2f(v0[8 * q + 3])),
-                             pack_bf16x2(w * u2f(v0[8 * q + 4]), w * u2f(v0[8 * q + 5])),
-                             pack_bf16x2(w * u2f(v0[8 * q + 6]), w * u2f(v0[8 * q + 7])));
+              st_shared_v4(my_stage + c * 64 + q * 16, pack_bf16x2(w * u2f(v0[8 * q + 0]), w * u2f(v0[8 * q + 1])),
+                           pack_bf16x2(w * u2f(v0[8 * q + 2]), w * u2f(v0[8 * q + 3])),
+                           pack_bf16x2(w * u2f(v0[8 * q + 4]), w * u2f(v0[8 * q + 5])),
+                           pack_bf16x2(w * u2f(v0[8 * q + 6]), w * u2f(v0[8 * q + 7])));
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              red_add_bf16x8(dst + (c + 1) * 32 + q * 8, pack_bf16x2(w * u2f(v1[8 * q + 0]), w * u2f(v1[8 * q + 1])),
-                             pack_bf16x2(w * u2f(v1[8 * q + 2]), w * u2f(v1[8 * q + 3])),
-                             pack_bf16x2(w * u2f(v1[8 * q + 4]), w * u2f(v1[8 * q + 5])),
-                             pack_bf16x2(w * u2f(v1[8 * q + 6]), w * u2f(v1[8 * q + 7])));
+              st_shared_v4(my_stage + (c + 1) * 64 + q * 16,
+                           pack_bf16x2(w * u2f(v1[8 * q + 0]), w * u2f(v1[8 * q + 1])),
+                           pack_bf16x2(w * u2f(v1[8 * q + 2]), w * u2f(v1[8 * q + 3])),
+                           pack_bf16x2(w * u2f(v1[8 * q + 4]), w * u2f(v1[8 * q + 5])),
+                           pack_bf16x2(w * u2f(v1[8 * q + 6]), w * u2f(v1[8 * q + 7])));
           }
+        }
+        if (tok >= 0) {
+          fence_proxy_async_smem();
+          bulk_reduce_add_bf16(static_cast<__nv_bfloat16*>(args.out) + (int64_t)tok * args.D + j * N, my_stage,
+                               N * 2);
+          bulk_commit();
         }
       }
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
     }
+    if (MODE == kModeDown) bulk_wait_all();  // reductions complete before the CTA exits
   }
 
   // ------------------------------------------------------------ teardown
@@ -252,11 +316,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int MODE, int N, int STAGES>
+template <int MODE, int N, int STAGES, bool GATHER>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args, int grid,
                         cudaStream_t stream, bool pdl) {
   using Cfg = GemmCfg<MODE, N, STAGES>;
-  auto kern = grouped_gemm_bf16_kernel<MODE, N, STAGES>;
+  auto kern = grouped_gemm_bf16_kernel<MODE, N, STAGES, GATHER>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
@@ -275,13 +339,14 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmAr
 }  // namespace
 
 cudaError_t launch_up_bf16(const CUtensorMap& map_a, const CUtensorMap& map_w1, const GemmArgs& args, int grid,
-                           cudaStream_t stream) {
-  return launch_gemm<kModeUp, 2 * kUpFold, kUpStages>(map_a, map_w1, args, grid, stream, false);
+                           cudaStream_t stream, bool gather4) {
+  if (gather4) return launch_gemm<kModeUp, 2 * kUpFold, kUpStages, true>(map_a, map_w1, args, grid, stream, false);
+  return launch_gemm<kModeUp, 2 * kUpFold, kUpStages, false>(map_a, map_w1, args, grid, stream, false);
 }
 
 cudaError_t launch_down_bf16(const CUtensorMap& map_act, const CUtensorMap& map_w2, const GemmArgs& args, int grid,
                              cudaStream_t stream, bool pdl) {
-  return launch_gemm<kModeDown, kDownN, kDownStages>(map_act, map_w2, args, grid, stream, pdl);
+  return launch_gemm<kModeDown, kDownN, kDownStages, false>(map_act, map_w2, args, grid, stream, pdl);
 }
 
 }  // namespace moe

@@ -30,6 +30,7 @@ struct Workspace {
   int* blk_base;       // [NB*E] per routing block: rank base within each expert
   void* xg;            // [S_max, D] bf16 gathered rows (split pipeline)
   void* act;           // [S_max, H] bf16 activation (split pipeline)
+  void* acc_f32;       // [T, D] fp32 reduction target (fused pipeline)
   size_t bytes;        // total bytes required
   int64_t S_max;       // padded slot capacity (multiple of 128)
   int max_rb;
@@ -51,22 +52,43 @@ struct GemmArgs {
   int D, H;
   int n_col_tiles;          // column tiles per row block
   int k_blocks;             // reduction length / kBK
+  int prefetch;             // k-blocks of L2 prefetch ahead of the smem ring (0 = off)
 };
 
+// Routing; when zero_out != nullptr the first launch also zero-fills
+// zero_out[0 .. zero_bytes) (the reduction target of the GEMMs).
 cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const float* topk_w, int T, int E, int k,
-                         cudaStream_t stream);
+                         cudaStream_t stream, void* zero_out = nullptr, int64_t zero_bytes = 0, int zero_grid = 0);
 // xg = x[row_tok] for live slots, and (when out != nullptr) out[0 .. out_bytes) = 0.
 cudaError_t launch_gather_zero(const Workspace& ws, const void* x, int D, void* out, int64_t out_bytes, int grid,
                                cudaStream_t stream);
+// gather4: map_a is x [T, D] with one-row boxes and the kernel gathers the
+// token rows itself; otherwise map_a is the pre-gathered xg [S_max, D].
 cudaError_t launch_up_bf16(const CUtensorMap& map_a, const CUtensorMap& map_w1, const GemmArgs& args, int grid,
-                           cudaStream_t stream);
+                           cudaStream_t stream, bool gather4);
 cudaError_t launch_down_bf16(const CUtensorMap& map_act, const CUtensorMap& map_w2, const GemmArgs& args, int grid,
                              cudaStream_t stream, bool pdl);
+
+struct FusedArgs {
+  const int* meta;
+  const int* expert_of_rb;
+  const int* row_tok;
+  const float* slot_w;
+  void* out_f32;            // fp32 [T, D], zeroed before the launch
+  int* err;
+  unsigned long long wait_limit_ns;
+  int D, H;
+  int n_slices;             // H / 128
+};
+
+cudaError_t launch_fused_bf16(const CUtensorMap& map_xg, const CUtensorMap& map_w1, const CUtensorMap& map_w2,
+                              const FusedArgs& args, int grid, cudaStream_t stream);
+cudaError_t launch_f32_to_bf16(const void* acc, void* out, int64_t n, int grid, cudaStream_t stream);
 
 // tile shapes of the bf16 GEMMs (host and device agree on these)
 constexpr int kUpFold = 128;      // gate rows + up rows per tile: N = 2 * kUpFold
 constexpr int kUpStages = 4;
 constexpr int kDownN = 256;
-constexpr int kDownStages = 4;
+constexpr int kDownStages = 3;
 
 }  // namespace moe

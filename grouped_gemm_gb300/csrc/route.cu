@@ -24,8 +24,16 @@ namespace {
 constexpr int kScatterWarps = 8;
 
 __global__ void __launch_bounds__(256) route_count_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int k,
-                                                          int* __restrict__ blk_counts, int* __restrict__ err) {
+                                                          int NB, int* __restrict__ blk_counts, int* __restrict__ err,
+                                                          uint4* __restrict__ zero_out, int64_t zero_vecs) {
   extern __shared__ int hist[];
+  if (zero_out) {  // every block of the (possibly wider) grid helps zero-fill the reduction target
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < zero_vecs;
+         i += (int64_t)gridDim.x * blockDim.x)
+      zero_out[i] = z;
+  }
+  if ((int)blockIdx.x >= NB) return;
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
   const int64_t p0 = (int64_t)blockIdx.x * kRouteTokPerBlock * k;
@@ -219,10 +227,12 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
 }  // namespace
 
 cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const float* topk_w, int T, int E, int k,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, void* zero_out, int64_t zero_bytes, int zero_grid) {
   const int64_t P = (int64_t)T * k;
   const int NB = ws.route_blocks;
-  route_count_kernel<<<NB, 256, E * sizeof(int), stream>>>(topk_ids, P, E, k, ws.blk_base, ws.err);
+  const int grid = zero_out ? (NB > zero_grid ? NB : zero_grid) : NB;
+  route_count_kernel<<<grid, 256, E * sizeof(int), stream>>>(topk_ids, P, E, k, NB, ws.blk_base, ws.err,
+                                                             static_cast<uint4*>(zero_out), zero_bytes / 16);
   route_scan_kernel<<<1, 1024, 0, stream>>>(NB, E, ws.blk_base, ws.counts, ws.offsets, ws.pad_offsets, ws.meta,
                                             ws.expert_of_rb, ws.row_tok, ws.slot_w);
   route_scatter_kernel<<<NB, kScatterWarps * 32, kScatterWarps * E * sizeof(int), stream>>>(

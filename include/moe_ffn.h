@@ -117,6 +117,21 @@ moe_status_t moe_ffn_sync_status(void* workspace, void* stream);
  * Process-wide; affects launches made after the call. */
 void moe_ffn_set_wait_limit_ns(uint64_t ns);
 
+/* Process-wide tuning options (affect calls made afterwards).
+ *   MOE_OPT_GATHER  0 (default): a gather kernel first materializes x in
+ *                   sorted order (16-byte vector copies) and the up kernel
+ *                   reads plain 128-row tiles of it ("Prime Flash MoE" sec. 6);
+ *                   1: the up-projection kernel fetches its token rows itself
+ *                   with TMA tile::gather4, four rows per instruction (sec. 3
+ *                   "For the tokens: TMA gathers them too").  Measured on
+ *                   GB300, option 1 makes the up kernel 2-3.5x slower.
+ *   MOE_OPT_L2_PREFETCH  0..64 (default 0): how many K-blocks ahead of the
+ *                   shared-memory ring the GEMM producers prefetch operand
+ *                   tiles into L2 (cp.async.bulk.prefetch.tensor); 0 = off.
+ *                   Measured on GB300, prefetching slowed every workload. */
+typedef enum { MOE_OPT_GATHER = 0, MOE_OPT_L2_PREFETCH = 1 } moe_option_t;
+moe_status_t moe_ffn_set_option(int option, long long value);
+
 /* Per-stage timing of later moe_ffn_forward calls (a benchmarking aid, off by
  * default).  While enabled, each call records CUDA events on its stream
  * between its stages; the split pipeline's stages are

@@ -18,7 +18,19 @@ from helpers import assert_close, run_forward, to_dev
 
 pytestmark = pytest.mark.gpu
 
-PIPELINES = [moe.MOE_SPLIT]
+# (pipeline, gather option): the split pipeline with the materializing gather
+# kernel (default) and with the in-kernel TMA gather4
+MODES = {"split": (moe.MOE_SPLIT, 0), "split_gather4": (moe.MOE_SPLIT, 1), "fused": (moe.MOE_FUSED, 0)}
+PIPELINES = list(MODES)
+
+
+def run_mode(inp, dev, mode, **kw):
+    pipeline, gather = MODES[mode]
+    moe.moe_ffn_set_option(moe.MOE_OPT_GATHER, gather)
+    try:
+        return run_forward(inp, dev, pipeline=pipeline, **kw)
+    finally:
+        moe.moe_ffn_set_option(moe.MOE_OPT_GATHER, 0)
 
 
 def oracle_out(inp, tokens=None):
@@ -37,14 +49,15 @@ def oracle_out(inp, tokens=None):
 ])
 def test_forward_small(T, D, H, E, k, routing, pipeline):
     inp = wl.make_custom(T, D, H, E, k, seed=T + D, routing=routing)
-    out, _ = run_forward(inp, to_dev(inp), pipeline=pipeline)
-    assert_close(out, oracle_out(inp), label=f"T={T} D={D} H={H} E={E} k={k}")
+    out, _ = run_mode(inp, to_dev(inp), pipeline)
+    r = assert_close(out, oracle_out(inp), label=f"T={T} D={D} H={H} E={E} k={k}")
+    print(f"{pipeline} T={T} D={D} H={H} E={E} k={k}: max_rel={r[0]:.2e} mean_rel={r[1]:.2e} cos={r[2]:.6f}")
 
 
 @pytest.mark.parametrize("pipeline", PIPELINES)
 def test_forward_tiny_workload(pipeline):
     inp = wl.make_inputs("tiny", seed=0)
-    out, _ = run_forward(inp, to_dev(inp), pipeline=pipeline)
+    out, _ = run_mode(inp, to_dev(inp), pipeline)
     assert_close(out, oracle_out(inp), label="tiny")
 
 
@@ -53,7 +66,7 @@ def test_forward_all_tokens_one_expert(pipeline):
     inp = wl.make_custom(600, 256, 256, 8, 2, seed=5, routing="uniform")
     inp["topk_ids"][:, 0] = 3
     inp["topk_ids"][:, 1] = 3          # the same expert twice per token
-    out, _ = run_forward(inp, to_dev(inp), pipeline=pipeline)
+    out, _ = run_mode(inp, to_dev(inp), pipeline)
     assert_close(out, oracle_out(inp), label="one expert")
 
 
@@ -61,8 +74,8 @@ def test_forward_all_tokens_one_expert(pipeline):
 def test_forward_repeat_calls_and_reused_workspace(pipeline):
     inp = wl.make_custom(100, 256, 128, 8, 2, seed=11)
     dev = to_dev(inp)
-    out1, ws = run_forward(inp, dev, pipeline=pipeline)
-    out2, _ = run_forward(inp, dev, pipeline=pipeline, workspace=ws, out=torch.ones_like(out1))
+    out1, ws = run_mode(inp, dev, pipeline)
+    out2, _ = run_mode(inp, dev, pipeline, workspace=ws, out=torch.ones_like(out1))
     ref = oracle_out(inp)
     assert_close(out1, ref, label="first")
     assert_close(out2, ref, label="second (out overwritten, not accumulated)")
@@ -79,10 +92,11 @@ def test_unsupported_combinations_rejected():
 @pytest.mark.parametrize("pipeline", PIPELINES)
 def test_forward_full_workload_sampled(name, n_sample, pipeline):
     inp = wl.make_inputs(name, seed=0)
-    out, _ = run_forward(inp, to_dev(inp), pipeline=pipeline)
+    out, _ = run_mode(inp, to_dev(inp), pipeline)
     T = inp["workload"].T
     tokens = None if n_sample is None else np.sort(np.random.default_rng(1).choice(T, n_sample, replace=False))
     ref = oracle_out(inp, tokens=None if tokens is None else tokens.astype(np.int32))
     got = out if tokens is None else out[torch.from_numpy(tokens).cuda()]
-    assert_close(got, ref, label=name)
+    r = assert_close(got, ref, label=name)
+    print(f"{pipeline} {name}: max_rel={r[0]:.2e} mean_rel={r[1]:.2e} cos={r[2]:.6f}")
     assert torch.isfinite(out.float()).all()
