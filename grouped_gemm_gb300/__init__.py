@@ -15,7 +15,7 @@ import threading
 __all__ = [
     "MOE_BF16", "MOE_MXFP8", "MOE_FUSED", "MOE_SPLIT", "MoeFFNError", "library_path", "lib",
     "moe_ffn_workspace_size", "moe_ffn_workspace_init", "moe_ffn_forward", "moe_ffn_route", "moe_ffn_route_noalloc",
-    "moe_ffn_sync_status", "moe_ffn_set_wait_limit_ns", "moe_ffn_profile_enable", "moe_ffn_profile_read", "moe_ffn_set_option", "MOE_OPT_GATHER", "moe_ffn_status_string", "alloc_workspace",
+    "moe_ffn_sync_status", "moe_ffn_set_wait_limit_ns", "moe_ffn_profile_enable", "moe_ffn_profile_read", "moe_ffn_set_option", "MOE_OPT_GATHER", "moe_ffn_prepare_mxfp8_weights", "moe_ffn_debug_mx_quantize", "moe_ffn_status_string", "alloc_workspace",
 ]
 
 MOE_BF16, MOE_MXFP8 = 0, 1
@@ -59,6 +59,10 @@ def lib() -> ctypes.CDLL:
             L.moe_ffn_route.restype = i
             L.moe_ffn_route_noalloc.argtypes = [vp, vp, i, i, i, vp, vp, vp, vp, vp]
             L.moe_ffn_route_noalloc.restype = i
+            L.moe_ffn_prepare_mxfp8_weights.argtypes = [vp, vp, vp, vp, i, i, i, vp]
+            L.moe_ffn_prepare_mxfp8_weights.restype = i
+            L.moe_ffn_debug_mx_quantize.argtypes = [vp, c.c_int64, vp, vp, vp]
+            L.moe_ffn_debug_mx_quantize.restype = i
             L.moe_ffn_sync_status.argtypes = [vp, vp]
             L.moe_ffn_sync_status.restype = i
             L.moe_ffn_set_wait_limit_ns.argtypes = [c.c_uint64]
@@ -148,6 +152,16 @@ def moe_ffn_route_noalloc(topk_ids, topk_w, T, E, k, counts, offsets, slot_of_pa
     st = lib().moe_ffn_route_noalloc(_p(topk_ids), _p(topk_w), T, E, k, _p(counts), _p(offsets),
                                      _p(slot_of_pair), _p(status_bits), _stream(stream))
     return _check(st, "moe_ffn_route_noalloc") if check else st
+
+
+def moe_ffn_prepare_mxfp8_weights(w1_sf, w2_sf, w1_sf_packed, w2_sf_packed, E, D, H, stream=None) -> int:
+    return _check(lib().moe_ffn_prepare_mxfp8_weights(_p(w1_sf), _p(w2_sf), _p(w1_sf_packed), _p(w2_sf_packed), E, D,
+                                                       H, _stream(stream)), "moe_ffn_prepare_mxfp8_weights")
+
+
+def moe_ffn_debug_mx_quantize(x, q, sf, stream=None) -> int:
+    return _check(lib().moe_ffn_debug_mx_quantize(_p(x), x.numel(), _p(q), _p(sf), _stream(stream)),
+                  "moe_ffn_debug_mx_quantize")
 
 
 def moe_ffn_sync_status(workspace, stream=None) -> int:

@@ -46,17 +46,24 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // Row-major bf16 matrix [rows, cols] read in boxes of [box_rows, 64] with the
 // 128-byte swizzle (64 bf16 = one 128-byte swizzle row).  box_rows == 1 is the
 // one-row box tile::gather4 requires.
-bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+bool make_map_2d(CUtensorMap* m, CUtensorMapDataType type, int elem_bytes, const void* base, uint64_t rows,
+                 uint64_t cols, uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+  cuuint64_t strides[1] = {cols * elem_bytes};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / elem_bytes), box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(m, type, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, rows, cols, box_rows);
+}
+// e4m3 bytes [rows, cols] in boxes of [box_rows, 128] (one 128-byte swizzle row).
+bool make_map_fp8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, rows, cols, box_rows);
 }
 
 int num_sms() {
@@ -87,7 +94,7 @@ void prof_mark(cudaStream_t st, int idx) {
 
 }  // namespace
 
-Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipeline) {
+Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipeline, int dtype) {
   Workspace w{};
   const int64_t P = (int64_t)T * k;
   const int64_t live_experts = P < E ? P : E;
@@ -113,7 +120,12 @@ Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipe
   w.slot_w = reinterpret_cast<float*>(take(sizeof(float) * w.S_max));
   w.slot_of_pair = reinterpret_cast<int*>(take(sizeof(int) * (P ? P : 1)));
   w.blk_base = reinterpret_cast<int*>(take(sizeof(int) * (size_t)w.route_blocks * E));
-  if (pipeline == MOE_SPLIT) {
+  if (dtype == MOE_MXFP8) {
+    w.xg = take((size_t)w.S_max * D);
+    w.xg_sf = take((size_t)w.S_max * D / 32);
+    w.act = take((size_t)w.S_max * H);
+    w.act_sf = take((size_t)w.S_max * H / 32);
+  } else if (pipeline == MOE_SPLIT) {
     w.xg = take((size_t)w.S_max * D * 2);
     w.act = take((size_t)w.S_max * H * 2);
   } else {
@@ -163,6 +175,57 @@ moe_status_t forward_fused_bf16(const Workspace& ws, const void* x, const void* 
   return cuda_status(e);
 }
 
+// MXFP8 split pipeline: routing, gather of e4m3 rows and their scales (+ zero
+// of out), block-scaled up-projection with SwiGLU and requantization,
+// block-scaled down-projection with the weighted reduction.
+moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void* x_sf, const void* w1,
+                                 const void* w1_sf, const void* w2, const void* w2_sf, const int32_t* topk_ids,
+                                 const float* topk_w, void* out, int T, int E, int D, int H, int k, int sms,
+                                 cudaStream_t st) {
+  CUtensorMap map_xg, map_w1, map_act, map_w2;
+  if (!make_map_fp8(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, kBM) ||
+      !make_map_fp8(&map_w1, w1, (uint64_t)E * 2 * H, (uint64_t)D, 128) ||
+      !make_map_fp8(&map_act, ws.act, (uint64_t)ws.S_max, (uint64_t)H, kBM) ||
+      !make_map_fp8(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, 256))
+    return MOE_ERR_CUDA;
+  prof_mark(st, 0);
+  cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  prof_mark(st, 1);
+  e = launch_gather_mx(ws, x, x_sf, D, out, (int64_t)T * D * 2, sms * 4, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  prof_mark(st, 2);
+  MxArgs ma{};
+  ma.meta = ws.meta;
+  ma.expert_of_rb = ws.expert_of_rb;
+  ma.row_tok = ws.row_tok;
+  ma.slot_w = ws.slot_w;
+  ma.act = ws.act;
+  ma.act_sf = ws.act_sf;
+  ma.out = out;
+  ma.err = ws.err;
+  ma.wait_limit_ns = g_wait_limit_ns.load();
+  ma.D = D;
+  ma.H = H;
+  MxArgs up = ma;
+  up.sf_a = ws.xg_sf;
+  up.sf_b = w1_sf;
+  up.n_col_tiles = H / 128;
+  up.k_blocks = D / 128;
+  e = launch_up_mxfp8(map_xg, map_w1, up, (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * up.n_col_tiles), st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  prof_mark(st, 3);
+  MxArgs dn = ma;
+  dn.sf_a = ws.act_sf;
+  dn.sf_b = w2_sf;
+  dn.n_col_tiles = D / 256;
+  dn.k_blocks = H / 128;
+  e = launch_down_mxfp8(map_act, map_w2, dn, (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * dn.n_col_tiles), st,
+                        !g_prof.on);
+  prof_mark(st, 4);
+  return cuda_status(e);
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -174,7 +237,7 @@ size_t moe_ffn_workspace_size(int T, int E, int D, int H, int k, int dtype, int 
   if (!shape_ok(T, E, D, H, k) || (dtype != MOE_BF16 && dtype != MOE_MXFP8) ||
       (pipeline != MOE_FUSED && pipeline != MOE_SPLIT))
     return 0;
-  return plan_workspace(nullptr, T, E, D, H, k, pipeline).bytes;
+  return plan_workspace(nullptr, T, E, D, H, k, pipeline, dtype).bytes;
 }
 
 moe_status_t moe_ffn_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
@@ -231,16 +294,21 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   if (T == 0) return MOE_OK;
   if (!x || !w1 || !w2 || !topk_ids || !topk_w || !out || !workspace) return MOE_ERR_INVALID_ARG;
   if (dtype == MOE_BF16 && (x_sf || w1_sf || w2_sf)) return MOE_ERR_INVALID_ARG;
+  if (dtype == MOE_MXFP8 && (!x_sf || !w1_sf || !w2_sf)) return MOE_ERR_INVALID_ARG;
+  if (dtype == MOE_MXFP8 && ((reinterpret_cast<uintptr_t>(x_sf) & 3u) || !aligned16(w1_sf) || !aligned16(w2_sf)))
+    return MOE_ERR_MISALIGNED;
   if (!aligned16(x) || !aligned16(w1) || !aligned16(w2) || !aligned16(out) || !aligned16(workspace) ||
       (reinterpret_cast<uintptr_t>(topk_ids) & 3u) || (reinterpret_cast<uintptr_t>(topk_w) & 3u))
     return MOE_ERR_MISALIGNED;
-  if (dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (dtype == MOE_MXFP8 && pipeline != MOE_SPLIT) return MOE_ERR_UNSUPPORTED;
   if (D % kDownN != 0) return MOE_ERR_UNSUPPORTED;
-  Workspace ws = plan_workspace(workspace, T, E, D, H, k, pipeline);
+  Workspace ws = plan_workspace(workspace, T, E, D, H, k, pipeline, dtype);
   if (workspace_bytes < ws.bytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
   const int sms = num_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == MOE_MXFP8)
+    return forward_split_mxfp8(ws, x, x_sf, w1, w1_sf, w2, w2_sf, topk_ids, topk_w, out, T, E, D, H, k, sms, st);
   if (pipeline == MOE_FUSED) return forward_fused_bf16(ws, x, w1, w2, topk_ids, topk_w, out, T, E, D, H, k, sms, st);
 
   const bool gather4 = g_gather_mode.load() == 1;
@@ -319,6 +387,27 @@ moe_status_t moe_ffn_profile_read(float* ms, int capacity, int* n_stages) {
     if (cudaEventElapsedTime(&ms[n], g_prof.ev[i], g_prof.ev[i + 1]) != cudaSuccess) return MOE_ERR_CUDA;
   *n_stages = n;
   return MOE_OK;
+}
+
+moe_status_t moe_ffn_prepare_mxfp8_weights(const void* w1_sf, const void* w2_sf, void* w1_sf_packed,
+                                           void* w2_sf_packed, int E, int D, int H, void* stream) {
+  if (E < 1 || D < 128 || H < 128 || D % 128 || H % 128) return MOE_ERR_INVALID_ARG;
+  if (!w1_sf || !w2_sf || !w1_sf_packed || !w2_sf_packed) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(w1_sf) & 3u) || (reinterpret_cast<uintptr_t>(w2_sf) & 3u) ||
+      !aligned16(w1_sf_packed) || !aligned16(w2_sf_packed))
+    return MOE_ERR_MISALIGNED;
+  const int sms = num_sms();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_pack_sf(w1_sf, w1_sf_packed, (int64_t)E * 2 * H, D, sms * 4, st);
+  if (e == cudaSuccess) e = launch_pack_sf(w2_sf, w2_sf_packed, (int64_t)E * D, H, sms * 4, st);
+  return cuda_status(e);
+}
+
+moe_status_t moe_ffn_debug_mx_quantize(const float* in, int64_t n, uint8_t* q, uint8_t* sf, void* stream) {
+  if (n < 0 || n % 32 || (n > 0 && (!in || !q || !sf))) return MOE_ERR_INVALID_ARG;
+  if (n == 0) return MOE_OK;
+  return cuda_status(launch_mx_quantize(in, n, q, sf, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_ffn_sync_status(void* workspace, void* stream) {

@@ -1,0 +1,374 @@
+// gemm_mxfp8.cu -- the MXFP8 variant of the split pipeline ("Prime Flash MoE"
+// sec. 7 "The MXFP8 variant"): e4m3 data with one ue8m0 scale per 32 elements
+// along K, tcgen05.mma kind::mxf8f6f4 block_scale, scales copied from shared
+// memory into tensor memory with tcgen05.cp before the MMAs that read them.
+//
+// UP:   acc[128 x 256] = (xg * s_x) . ([W1 gate j | W1 up j] * s_w1)^T over K=D,
+//       act = silu(gate) * up in fp32, requantized per 32 along H to e4m3 +
+//       ue8m0 (sec. 7 "The epilogue also quantizes"), stored with its scale
+//       tiles in the blocked layout the down kernel's tcgen05.cp expects
+//       (sec. 7 "The split variant, in MXFP8").
+// DOWN: acc[128 x 256] = (act * s_act) . (W2[e][n] * s_w2)^T over K=H, weighted
+//       by the routing weight in fp32, rounded to bf16 and reduced into out
+//       with one bulk reduction per row.
+// A stage holds K = 128 (four MMAs of K = 32, one UTCCP group: sec. 7 "this is
+// also the reason the MXFP8 kernel uses BK = 128").  The accumulator takes 256
+// TMEM columns, so it is single-buffered and the scale sets sit behind it at
+// columns 256 + 16 * stage_slot (sec. 7: the scale columns rotate so in-flight
+// stages never overwrite each other's scales).  The epilogue frees the
+// accumulator as soon as it has read it.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "mx.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+enum { kMxUp = 0, kMxDown = 1 };
+constexpr int kMxBK = 128;                  // fp8 elements (bytes) per stage row
+constexpr int kMxN = 256;
+constexpr int kMxThreads = 192;
+constexpr int kMxEpi = 128;
+constexpr uint64_t kMxDrainNs = 200ull * 1000 * 1000;
+
+template <int MODE, int STAGES>
+struct MxCfg {
+  static constexpr int kA = kBM * kMxBK;          // 16 KB
+  static constexpr int kB = kMxN * kMxBK;         // 32 KB
+  static constexpr int kSF = 512 * 3;             // SFA tile + two SFB tiles
+  static constexpr int kTx = kA + kB + kSF;
+  static constexpr int kStageRowBytes = kMxN * 2 + 16;
+  static constexpr int kStaging = MODE == kMxDown ? kBM * kStageRowBytes : 0;
+  static constexpr int kBarrierBytes = 256;
+  static constexpr int kSmem = 1024 + STAGES * (kA + kB + kSF) + kStaging + kBarrierBytes;
+  static_assert(kSmem <= 232448, "shared memory");
+  static_assert(256 + 16 * STAGES <= 512, "TMEM columns");
+};
+
+__device__ __forceinline__ float mx_u2f(uint32_t u) { return __uint_as_float(u); }
+__device__ __forceinline__ float mx_swiglu(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+
+template <int MODE, int STAGES>
+__global__ void __launch_bounds__(kMxThreads, 1)
+    grouped_gemm_mxfp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                              const MxArgs args) {
+  using Cfg = MxCfg<MODE, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + STAGES * Cfg::kA;
+  uint8_t* sSF = sB + STAGES * Cfg::kB;
+  uint8_t* sStage = sSF + STAGES * Cfg::kSF;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + Cfg::kStaging);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 1;
+  uint64_t* drain = tempty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WaitCtl wc{abort_flag, args.err, args.wait_limit_ns};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(tfull, 1);
+    mbar_init(tempty, kMxEpi);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&map_a);
+    prefetch_tmap(&map_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  if (MODE == kMxUp && threadIdx.x == 0) griddep_launch_dependents();
+
+  const int num_rb = args.meta[0];
+  const int n_tiles = num_rb * args.n_col_tiles;
+  const int KB = args.k_blocks;             // K / 128
+  const uint8_t* sf_a = static_cast<const uint8_t*>(args.sf_a);
+  const uint8_t* sf_b = static_cast<const uint8_t*>(args.sf_b);
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    if (MODE == kMxDown) griddep_wait();
+    int s = 0;
+    uint32_t ph = 0;
+    int issued_phase[STAGES];
+#pragma unroll
+    for (int i = 0; i < STAGES; ++i) issued_phase[i] = -1;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
+      const int rb = tile / args.n_col_tiles, j = tile % args.n_col_tiles;
+      const int e = args.expert_of_rb[rb];
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!(ok = mbar_wait(&empty[s], ph ^ 1u, wc, 21))) break;
+        mbar_arrive_expect_tx(&full[s], Cfg::kTx);
+        issued_phase[s] = (int)ph;
+        uint8_t* a = sA + s * Cfg::kA;
+        uint8_t* b = sB + s * Cfg::kB;
+        uint8_t* sf = sSF + s * Cfg::kSF;
+        tma_load_2d(a, &map_a, &full[s], kb * kMxBK, rb * kBM);
+        bulk_load(sf, sf_a + sf_tile_offset(rb, kb, KB), 512, &full[s]);
+        if (MODE == kMxUp) {
+          const int rt_gate = e * (2 * args.H / 128) + j;   // 128-row tiles of W1 [E*2H, D]
+          const int rt_up = rt_gate + args.H / 128;
+          tma_load_2d(b, &map_b, &full[s], kb * kMxBK, rt_gate * 128);
+          tma_load_2d(b + 128 * kMxBK, &map_b, &full[s], kb * kMxBK, rt_up * 128);
+          bulk_load(sf + 512, sf_b + sf_tile_offset(rt_gate, kb, KB), 512, &full[s]);
+          bulk_load(sf + 1024, sf_b + sf_tile_offset(rt_up, kb, KB), 512, &full[s]);
+        } else {
+          const int rt0 = e * (args.D / 128) + j * 2;       // 128-row tiles of W2 [E*D, H]
+          tma_load_2d(b, &map_b, &full[s], kb * kMxBK, rt0 * 128);
+          bulk_load(sf + 512, sf_b + sf_tile_offset(rt0, kb, KB), 512, &full[s]);
+          bulk_load(sf + 1024, sf_b + sf_tile_offset(rt0 + 1, kb, KB), 512, &full[s]);
+        }
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+    if (!ok) {
+      for (int i = 0; i < STAGES; ++i)
+        if (issued_phase[i] >= 0) mbar_wait_drain(&full[i], (uint32_t)issued_phase[i], kMxDrainNs);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t idesc = idesc_mxf8(kBM, kMxN);
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    int it = 0;
+    for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x, ++it) {
+      if (!(ok = mbar_wait(tempty, ((uint32_t)it & 1u) ^ 1u, wc, 22))) break;
+      tc_fence_after();
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!(ok = mbar_wait(&full[s], ph, wc, 23))) break;
+        tc_fence_after();
+        // scale tiles of this stage -> TMEM columns reserved for this ring slot
+        const uint32_t sfa_col = tmem_base + 256 + 16 * s, sfb_col = sfa_col + 4;
+        const uint32_t sf_smem = smem_addr(sSF + s * Cfg::kSF);
+        utccp_sf(sfa_col, sdesc_sf_tile(sf_smem));
+        utccp_sf(sfb_col, sdesc_sf_tile(sf_smem + 512));
+        utccp_sf(sfb_col + 4, sdesc_sf_tile(sf_smem + 1024));
+        const uint64_t ad = sdesc_sw128(smem_addr(sA + s * Cfg::kA));
+        const uint64_t bd = sdesc_sw128(smem_addr(sB + s * Cfg::kB));
+#pragma unroll
+        for (int kk = 0; kk < kMxBK / 32; ++kk)
+          umma_mxf8(tmem_base, ad + 2 * kk, bd + 2 * kk, idesc_with_sf_id(idesc, kk), sfa_col, sfb_col,
+                    (kb | kk) != 0);
+        umma_commit(&empty[s]);
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok) break;
+      umma_commit(tfull);
+    }
+    if (!ok) {
+      umma_commit(drain);
+      mbar_wait_drain(drain, 0, kMxDrainNs);
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
+    uint8_t* my_stage = sStage + row * Cfg::kStageRowBytes;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+      if (!mbar_wait(tfull, (uint32_t)it & 1u, wc, 24)) break;
+      tc_fence_after();
+      const int rb = tile / args.n_col_tiles, j = tile % args.n_col_tiles;
+      const int64_t slot = (int64_t)rb * kBM + row;
+      const int tok = args.row_tok[slot];
+      if (MODE == kMxUp) {
+        float act[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t g[32], u[32];
+          tmem_ld_x32_pair(lane_base + c * 32, lane_base + 128 + c * 32, g, u);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) act[c * 32 + i] = mx_swiglu(mx_u2f(g[i]), mx_u2f(u[i]));
+        }
+        tc_fence_before();
+        mbar_arrive(tempty);  // the accumulator is free for the next tile
+        if (tok >= 0) {
+          uint8_t* dst = static_cast<uint8_t*>(args.act) + slot * args.H + j * 128;
+          uint32_t sfw = 0;
+#pragma unroll
+          for (int blk = 0; blk < 4; ++blk) {
+            uint32_t q[8];
+            const uint32_t sfb = mx_quantize32(act + blk * 32, q);
+            sfw |= sfb << (8 * blk);
+            st_global_v4(dst + blk * 32, q[0], q[1], q[2], q[3]);
+            st_global_v4(dst + blk * 32 + 16, q[4], q[5], q[6], q[7]);
+          }
+          uint8_t* sfdst = static_cast<uint8_t*>(args.act_sf) + sf_tile_offset(rb, j, args.H / 128) + sf_in_tile(row);
+          *reinterpret_cast<uint32_t*>(sfdst) = sfw;
+        }
+      } else {
+        const float w = args.slot_w[slot];
+        bulk_wait_read_all();
+#pragma unroll 1
+        for (int c = 0; c < kMxN / 32; c += 2) {
+          uint32_t v0[32], v1[32];
+          tmem_ld_x32_pair(lane_base + c * 32, lane_base + (c + 1) * 32, v0, v1);
+          if (tok >= 0) {
+#pragma unroll
+            for (int qd = 0; qd < 4; ++qd)
+              st_shared_v4(my_stage + c * 64 + qd * 16, pack_bf16x2(w * mx_u2f(v0[8 * qd]), w * mx_u2f(v0[8 * qd + 1])),
+                           pack_bf16x2(w * mx_u2f(v0[8 * qd + 2]), w * mx_u2f(v0[8 * qd + 3])),
+                           pack_bf16x2(w * mx_u2f(v0[8 * qd + 4]), w * mx_u2f(v0[8 * qd + 5])),
+                           pack_bf16x2(w * mx_u2f(v0[8 * qd + 6]), w * mx_u2f(v0[8 * qd + 7])));
+#pragma unroll
+            for (int qd = 0; qd < 4; ++qd)
+              st_shared_v4(my_stage + (c + 1) * 64 + qd * 16,
+                           pack_bf16x2(w * mx_u2f(v1[8 * qd]), w * mx_u2f(v1[8 * qd + 1])),
+                           pack_bf16x2(w * mx_u2f(v1[8 * qd + 2]), w * mx_u2f(v1[8 * qd + 3])),
+                           pack_bf16x2(w * mx_u2f(v1[8 * qd + 4]), w * mx_u2f(v1[8 * qd + 5])),
+                           pack_bf16x2(w * mx_u2f(v1[8 * qd + 6]), w * mx_u2f(v1[8 * qd + 7])));
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(tempty);
+        if (tok >= 0) {
+          fence_proxy_async_smem();
+          bulk_reduce_add_bf16(static_cast<__nv_bfloat16*>(args.out) + (int64_t)tok * args.D + j * kMxN, my_stage,
+                               kMxN * 2);
+          bulk_commit();
+        }
+      }
+    }
+    if (MODE == kMxDown) bulk_wait_all();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+template <int MODE, int STAGES>
+cudaError_t launch_mx(const CUtensorMap& a, const CUtensorMap& b, const MxArgs& args, int grid, cudaStream_t stream,
+                      bool pdl) {
+  using Cfg = MxCfg<MODE, STAGES>;
+  auto kern = grouped_gemm_mxfp8_kernel<MODE, STAGES>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kMxThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a, b, args);
+}
+
+// xg[s] = x[row_tok[s]] (D bytes of e4m3 per row) and the row's scales moved
+// from row-major x_sf[T, D/32] into the blocked tile layout of xg_sf; live
+// slots only.  The same launch zero-fills out.
+__global__ void __launch_bounds__(256) gather_rows_mx_kernel(const uint4* __restrict__ x, const uint32_t* __restrict__ x_sf,
+                                                             const int* __restrict__ row_tok, const int* __restrict__ meta,
+                                                             uint4* __restrict__ xg, uint8_t* __restrict__ xg_sf, int D,
+                                                             uint4* __restrict__ out, int64_t out_vecs) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t S = (int64_t)meta[0] * kRowPad;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int vec_per_row = D / 16, kt_per_row = D / 128;
+  for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp; row < S; row += nwarps) {
+    const int tok = row_tok[row];
+    if (tok < 0) continue;
+    const uint4* src = x + (int64_t)tok * vec_per_row;
+    uint4* dst = xg + row * vec_per_row;
+    for (int i = lane; i < vec_per_row; i += 32) dst[i] = __ldg(src + i);
+    const int r = (int)(row % kRowPad);
+    const int64_t rt = row / kRowPad;
+    for (int kt = lane; kt < kt_per_row; kt += 32)
+      *reinterpret_cast<uint32_t*>(xg_sf + sf_tile_offset(rt, kt, kt_per_row) + sf_in_tile(r)) =
+          __ldg(x_sf + (int64_t)tok * (D / 128) + kt);
+  }
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < out_vecs; i += (int64_t)gridDim.x * blockDim.x)
+    out[i] = z;
+}
+
+// Row-major scales sf[rows, K/32] -> blocked tiles (rows % 128 == 0).
+__global__ void __launch_bounds__(256) pack_sf_kernel(const uint32_t* __restrict__ sf, uint8_t* __restrict__ packed,
+                                                      int64_t rows, int K) {
+  const int kt_per_row = K / 128;
+  const int64_t n = rows * kt_per_row;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = i / kt_per_row;
+    const int kt = (int)(i % kt_per_row);
+    *reinterpret_cast<uint32_t*>(packed + sf_tile_offset(row / 128, kt, kt_per_row) + sf_in_tile((int)(row % 128))) =
+        sf[i];
+  }
+}
+
+// Test hook: the epilogue's requantization applied to n fp32 values.
+__global__ void mx_quantize_kernel(const float* __restrict__ in, int64_t n_blocks, uint8_t* __restrict__ q,
+                                   uint8_t* __restrict__ sf) {
+  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < n_blocks; b += (int64_t)gridDim.x * blockDim.x) {
+    float a[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) a[i] = in[b * 32 + i];
+    uint32_t qq[8];
+    sf[b] = (uint8_t)mx_quantize32(a, qq);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) reinterpret_cast<uint32_t*>(q + b * 32)[i] = qq[i];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_up_mxfp8(const CUtensorMap& a, const CUtensorMap& w1, const MxArgs& args, int grid,
+                            cudaStream_t stream) {
+  return launch_mx<kMxUp, 4>(a, w1, args, grid, stream, false);
+}
+cudaError_t launch_down_mxfp8(const CUtensorMap& act, const CUtensorMap& w2, const MxArgs& args, int grid,
+                              cudaStream_t stream, bool pdl) {
+  return launch_mx<kMxDown, 3>(act, w2, args, grid, stream, pdl);
+}
+cudaError_t launch_gather_mx(const Workspace& ws, const void* x, const void* x_sf, int D, void* out, int64_t out_bytes,
+                             int grid, cudaStream_t stream) {
+  gather_rows_mx_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), static_cast<const uint32_t*>(x_sf),
+                                                  ws.row_tok, ws.meta, static_cast<uint4*>(ws.xg),
+                                                  static_cast<uint8_t*>(ws.xg_sf), D, static_cast<uint4*>(out),
+                                                  out_bytes / 16);
+  return cudaGetLastError();
+}
+cudaError_t launch_pack_sf(const void* sf, void* packed, int64_t rows, int K, int grid, cudaStream_t stream) {
+  pack_sf_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint32_t*>(sf), static_cast<uint8_t*>(packed), rows, K);
+  return cudaGetLastError();
+}
+cudaError_t launch_mx_quantize(const float* in, int64_t n, uint8_t* q, uint8_t* sf, cudaStream_t stream) {
+  const int64_t nb = n / 32;
+  const int grid = (int)std::min<int64_t>((nb + 127) / 128, 4096);
+  mx_quantize_kernel<<<grid > 0 ? grid : 1, 128, 0, stream>>>(in, nb, q, sf);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -31,13 +31,15 @@ struct Workspace {
   void* xg;            // [S_max, D] bf16 gathered rows (split pipeline)
   void* act;           // [S_max, H] bf16 activation (split pipeline)
   void* acc_f32;       // [T, D] fp32 reduction target (fused pipeline)
+  void* xg_sf;         // MXFP8: scales of xg in blocked 512-byte tiles (S_max * D/32 bytes)
+  void* act_sf;        // MXFP8: scales of act in blocked tiles (S_max * H/32 bytes)
   size_t bytes;        // total bytes required
   int64_t S_max;       // padded slot capacity (multiple of 128)
   int max_rb;
   int route_blocks;
 };
 
-Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipeline);
+Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipeline, int dtype = 0);
 
 // ----------------------------------------------------------------- kernels
 struct GemmArgs {
@@ -84,6 +86,32 @@ struct FusedArgs {
 cudaError_t launch_fused_bf16(const CUtensorMap& map_xg, const CUtensorMap& map_w1, const CUtensorMap& map_w2,
                               const FusedArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_f32_to_bf16(const void* acc, void* out, int64_t n, int grid, cudaStream_t stream);
+
+struct MxArgs {
+  const int* meta;
+  const int* expert_of_rb;
+  const int* row_tok;
+  const float* slot_w;
+  void* act;                // up: e4m3 [S_max, H] output
+  void* act_sf;             // up: blocked scale tiles of act
+  void* out;                // down: bf16 [T, D] reduction target
+  const void* sf_a;         // blocked scale tiles of the A operand
+  const void* sf_b;         // blocked scale tiles of the weights
+  int* err;
+  unsigned long long wait_limit_ns;
+  int D, H;
+  int n_col_tiles;
+  int k_blocks;             // K / 128
+};
+
+cudaError_t launch_up_mxfp8(const CUtensorMap& a, const CUtensorMap& w1, const MxArgs& args, int grid,
+                            cudaStream_t stream);
+cudaError_t launch_down_mxfp8(const CUtensorMap& act, const CUtensorMap& w2, const MxArgs& args, int grid,
+                              cudaStream_t stream, bool pdl);
+cudaError_t launch_gather_mx(const Workspace& ws, const void* x, const void* x_sf, int D, void* out, int64_t out_bytes,
+                             int grid, cudaStream_t stream);
+cudaError_t launch_pack_sf(const void* sf, void* packed, int64_t rows, int K, int grid, cudaStream_t stream);
+cudaError_t launch_mx_quantize(const float* in, int64_t n, uint8_t* q, uint8_t* sf, cudaStream_t stream);
 
 // tile shapes of the bf16 GEMMs (host and device agree on these)
 constexpr int kUpFold = 128;      // gate rows + up rows per tile: N = 2 * kUpFold

@@ -68,11 +68,34 @@ size_t moe_ffn_workspace_size(int T, int E, int D, int H, int k, int dtype, int 
 moe_status_t moe_ffn_workspace_init(void* workspace, size_t workspace_bytes, void* stream);
 
 /* The forward pass described above.  x_sf, w1_sf, w2_sf are the MXFP8 scale
- * arrays and must be NULL for MOE_BF16. */
+ * arrays and must be NULL for MOE_BF16.
+ *
+ * MOE_MXFP8 ("Prime Flash MoE" sec. 7; MOE_SPLIT only): x, w1, w2 hold OCP
+ * e4m3 codes (one byte per element, same shapes as above); every 32
+ * consecutive elements along the contiguous (reduction) dimension share one
+ * ue8m0 scale byte s (value 2^(s-127)).  x_sf is row-major [T, D/32] (4-byte
+ * aligned); w1_sf and w2_sf are the weight scales already repacked by
+ * moe_ffn_prepare_mxfp8_weights.  The activation is requantized to MXFP8
+ * (per 32 along H) between the two GEMMs; out stays bf16. */
 moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, const void* w1_sf, const void* w2,
                              const void* w2_sf, const int32_t* topk_ids, const float* topk_w, void* out, int T, int E,
                              int D, int H, int k, int dtype, int pipeline, void* workspace, size_t workspace_bytes,
                              void* stream);
+
+/* One-time repacking of MXFP8 weight scales into the 512-byte tile layout the
+ * kernels copy into tensor memory ("Prime Flash MoE" sec. 7 "Scales are
+ * piped through tensor memory"; 128 rows x 4 K-scales per tile).
+ *   w1_sf [E, 2H, D/32] and w2_sf [E, D, H/32] row-major ue8m0 (4-byte aligned);
+ *   w1_sf_packed (E*2H*D/32 bytes) and w2_sf_packed (E*D*H/32 bytes) are
+ *   caller buffers, 16-byte aligned, written asynchronously on stream. */
+moe_status_t moe_ffn_prepare_mxfp8_weights(const void* w1_sf, const void* w2_sf, void* w1_sf_packed,
+                                           void* w2_sf_packed, int E, int D, int H, void* stream);
+
+/* Test hook: the MXFP8 requantization the up-projection epilogue applies to
+ * act, run on n fp32 values (n % 32 == 0): per 32 values, scale exponent
+ * e = ceil(log2(amax/448)) (0 for amax == 0, at least -127), scale byte
+ * sf = e + 127, codes q = e4m3_rne_satfinite(v * 2^-e).  Device pointers. */
+moe_status_t moe_ffn_debug_mx_quantize(const float* in, int64_t n, uint8_t* q, uint8_t* sf, void* stream);
 
 /* The routing permutation alone ("Prime Flash MoE" sec. 3 and 6: tokens are
  * processed in per-expert sorted order).  Writes, into caller device arrays:
