@@ -88,11 +88,15 @@ def source_digest(files):
     return h.hexdigest()[:16]
 
 
+_BF16_SRC = ["grouped_gemm_gb300/csrc/gemm_bf16.cu", "grouped_gemm_gb300/csrc/ptx.cuh",
+             "grouped_gemm_gb300/csrc/internal.h"]
+_MX_SRC = ["grouped_gemm_gb300/csrc/gemm_mxfp8.cu", "grouped_gemm_gb300/csrc/mx.cuh", "grouped_gemm_gb300/csrc/ptx.cuh",
+           "grouped_gemm_gb300/csrc/internal.h"]
 KERNEL_SOURCES = {
-    "up_swiglu": ["grouped_gemm_gb300/csrc/gemm_bf16.cu", "grouped_gemm_gb300/csrc/ptx.cuh",
-                  "grouped_gemm_gb300/csrc/internal.h"],
-    "down_reduce": ["grouped_gemm_gb300/csrc/gemm_bf16.cu", "grouped_gemm_gb300/csrc/ptx.cuh",
-                    "grouped_gemm_gb300/csrc/internal.h"],
+    "up_swiglu": _BF16_SRC, "down_reduce": _BF16_SRC,
+    "up_swiglu_mxfp8": _MX_SRC, "down_reduce_mxfp8": _MX_SRC,
+    "fused_gemm": ["grouped_gemm_gb300/csrc/gemm_fused.cu", "grouped_gemm_gb300/csrc/ptx.cuh",
+                   "grouped_gemm_gb300/csrc/internal.h"],
 }
 
 
@@ -157,6 +161,21 @@ class ClockSampler:
                 "samples": len(inside)}
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of every rank's x (the slowest rank sets the step time)."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_tflops(flops_per_rank: float, ms_max: float, world: int) -> float:
+    """Whole-job throughput: every rank's FLOPs over the slowest rank's time."""
+    return flops_per_rank * world / (ms_max * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args, rank, world, local_rank):
     import numpy as np
@@ -168,19 +187,28 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     inp = wl.make_inputs(args.workload, seed=rank)
     w = inp["workload"]
-    if w.dtype != "bf16":
-        raise SystemExit(f"workload {args.workload} ({w.dtype}) not built yet")
-    dev = {k: torch.from_numpy(inp[k].view(np.int16)).cuda() for k in ("x", "w1", "w2")}
+    mx = w.dtype == "mxfp8"
+    dtype = moe.MOE_MXFP8 if mx else moe.MOE_BF16
+    if mx and args.pipeline != "split":
+        raise SystemExit("the MXFP8 path is built for the split pipeline")
+    dev = {k: torch.from_numpy(inp[k] if mx else inp[k].view(np.int16)).cuda() for k in ("x", "w1", "w2")}
+    if mx:  # weight scales are repacked once, like the weights themselves
+        dev["x_sf"] = torch.from_numpy(inp["x_sf"]).cuda()
+        dev["w1_sf"] = torch.empty(inp["w1_sf"].size, dtype=torch.uint8, device="cuda")
+        dev["w2_sf"] = torch.empty(inp["w2_sf"].size, dtype=torch.uint8, device="cuda")
+        moe.moe_ffn_prepare_mxfp8_weights(torch.from_numpy(inp["w1_sf"]).cuda(), torch.from_numpy(inp["w2_sf"]).cuda(),
+                                          dev["w1_sf"], dev["w2_sf"], w.E, w.D, w.H)
     ids = torch.from_numpy(inp["topk_ids"]).cuda()
     tw = torch.from_numpy(inp["topk_w"]).cuda()
     out = torch.empty(w.T, w.D, dtype=torch.bfloat16, device="cuda")
     pipeline = moe.MOE_SPLIT if args.pipeline == "split" else moe.MOE_FUSED
-    ws = moe.alloc_workspace(w.T, w.E, w.D, w.H, w.k, moe.MOE_BF16, pipeline)
+    ws = moe.alloc_workspace(w.T, w.E, w.D, w.H, w.k, dtype, pipeline)
     stream = torch.cuda.current_stream()
 
     def step():
         moe.moe_ffn_forward(dev["x"], dev["w1"], dev["w2"], ids, tw, out, E=w.E, D=w.D, H=w.H, k=w.k,
-                            workspace=ws, dtype=moe.MOE_BF16, pipeline=pipeline, stream=stream)
+                            workspace=ws, dtype=dtype, pipeline=pipeline, stream=stream, x_sf=dev.get("x_sf"),
+                            w1_sf=dev.get("w1_sf"), w2_sf=dev.get("w2_sf"))
 
     def barrier():
         if world > 1:
@@ -207,11 +235,7 @@ def run_ours(args, rank, world, local_rank):
     t_host1 = time.time()
     torch.cuda.synchronize()
     barrier()
-    ms_total = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms_total], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), world, device="cuda")
     ms = ms_total / args.steps
     # keep the same step running so the clock sampler sees load for >= 1.5 s
     t_sus0 = time.time()
@@ -229,7 +253,7 @@ def run_ours(args, rank, world, local_rank):
 
     alg = algorithmic(w, inp["topk_ids"])
     flops_all = alg["step_flops"] * world
-    value = flops_all / (ms * 1e-3) / 1e12
+    value = weak_scaling_tflops(alg["step_flops"], ms, world)
     tokens_per_s = w.T * world / (ms * 1e-3)
 
     # per-stage durations from library-recorded CUDA events on the same stream
@@ -243,6 +267,10 @@ def run_ours(args, rank, world, local_rank):
     stage_ms = {name: statistics.median(p[i] for p in per) for i, name in enumerate(names) if len(per[0]) > i}
 
     peaks, peak_src = load_peaks()
+    if mx:  # e4m3 contraction: the measured bf16 peak times the nominal fp8/bf16 ratio (4.5 / 2.25)
+        peaks = dict(peaks)
+        peaks["bf16_tflops"] = peaks["bf16_tflops"] * 2.0
+        peak_src += " bf16 x nominal fp8/bf16 ratio 2"
     if args.pipeline == "split":
         dom = max(("up_swiglu", "down_reduce"), key=lambda s: stage_ms.get(s, 0.0))
         kd = alg[dom]
@@ -259,7 +287,7 @@ def run_ours(args, rank, world, local_rank):
         achieved, peak, unit = kd["bytes"] / t_dom / 1e9, peaks["hbm_gbs"], "GB/s"
     roofline = {"bound": "tensor" if tensor_bound else "hbm", "kernel": dom, "achieved": round(achieved, 1),
                 "peak": peak, "peak_source": peak_src, "unit": unit, "frac": round(achieved / peak, 4),
-                "traffic": traffic_from_profiles(dom, args.workload),
+                "traffic": traffic_from_profiles(dom + ("_mxfp8" if mx and dom != "fused_gemm" else ""), args.workload),
                 "algorithmic_per_launch": kd["flops"] if tensor_bound else kd["bytes"],
                 "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()}}
     step_bound = max(alg["step_flops"] / (peaks["bf16_tflops"] * 1e12), alg["step_bytes"] / (peaks["hbm_gbs"] * 1e9))
@@ -267,13 +295,16 @@ def run_ours(args, rank, world, local_rank):
     # end to end: host buffers, copies inside the timed region
     e2e = None
     if not args.no_e2e:
-        xh = torch.from_numpy(inp["x"].view(np.int16)).pin_memory()
+        xh = torch.from_numpy(inp["x"] if mx else inp["x"].view(np.int16)).pin_memory()
+        xsfh = torch.from_numpy(inp["x_sf"]).pin_memory() if mx else None
         idh = torch.from_numpy(inp["topk_ids"]).pin_memory()
         twh = torch.from_numpy(inp["topk_w"]).pin_memory()
         outh = torch.empty(w.T, w.D, dtype=torch.bfloat16).pin_memory()
 
         def e2e_step():
             dev["x"].copy_(xh, non_blocking=True)
+            if mx:
+                dev["x_sf"].copy_(xsfh, non_blocking=True)
             ids.copy_(idh, non_blocking=True)
             tw.copy_(twh, non_blocking=True)
             step()
@@ -290,13 +321,10 @@ def run_ours(args, rank, world, local_rank):
             e2e_step()
         e1.record(stream)
         e1.synchronize()
-        e_ms = e0.elapsed_time(e1) / n_e2e
-        if world > 1:
-            t = torch.tensor([e_ms], device="cuda")
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world, device="cuda")
         e2e = {"value": round(flops_all / (e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": int(xh.numel() * 2 + idh.numel() * 4 + twh.numel() * 4),
+               "h2d_bytes_per_step": int(xh.numel() * xh.element_size() + (xsfh.numel() if mx else 0) +
+                                         idh.numel() * 4 + twh.numel() * 4),
                "d2h_bytes_per_step": int(outh.numel() * 2), "ms_per_step": round(e_ms, 4),
                "resident": "expert weights stay in HBM (model parameters)"}
 
@@ -314,7 +342,7 @@ def run_ours(args, rank, world, local_rank):
     return {
         "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "e4m3 (MXFP8)" if mx else "bf16", "data": "synthetic",
         "tokens_per_s": round(tokens_per_s, 1),
         "roofline_step_frac": round(step_bound / (ms * 1e-3), 4),
         "config": {"workload": w.name, "T": w.T, "D": w.D, "H": w.H, "E": w.E, "k": w.k, "routing": w.routing,
@@ -326,6 +354,14 @@ def run_ours(args, rank, world, local_rank):
     }
 
 
+def oracle_call(inp, tokens):
+    import oracle
+    mx = inp["workload"].dtype == "mxfp8"
+    return oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], inp["topk_ids"], inp["topk_w"],
+                          act=oracle.ACT_MXFP8 if mx else oracle.ACT_BF16, tokens=tokens,
+                          x_sf=inp.get("x_sf"), w1_sf=inp.get("w1_sf"), w2_sf=inp.get("w2_sf"))
+
+
 def cpu_baseline(inp, w, budget_s=12.0):
     """The oracle, as it stands, on the host cores over a bounded token sample."""
     import numpy as np
@@ -334,16 +370,14 @@ def cpu_baseline(inp, w, budget_s=12.0):
     per_tok = 6.0 * w.k * w.D * w.H
     n = 1
     t0 = time.time()
-    oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], inp["topk_ids"], inp["topk_w"], act=oracle.ACT_BF16,
-                   tokens=np.arange(n, dtype=np.int32))
+    oracle_call(inp, np.arange(n, dtype=np.int32))
     t1 = max(time.time() - t0, 1e-3)
     cores = oracle.max_threads()
     n = int(min(w.T, max(cores, budget_s / t1 * 0.9)))
     n = max(1, n // cores * cores) if n >= cores else n
     toks = np.sort(np.random.default_rng(123).choice(w.T, n, replace=False)).astype(np.int32)
     t0 = time.time()
-    oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], inp["topk_ids"], inp["topk_w"], act=oracle.ACT_BF16,
-                   tokens=toks)
+    oracle_call(inp, toks)
     dt = time.time() - t0
     return {"value": round(per_tok * n / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{n} of {w.T} tokens of the {w.name} workload (all k={w.k} experts each), {dt:.1f} s",
@@ -364,16 +398,14 @@ def run_reference(args, rank):
     per_tok = 6.0 * w.k * w.D * w.H
     # tokens per step: about one second of CPU work
     t0 = time.time()
-    oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], inp["topk_ids"], inp["topk_w"], act=oracle.ACT_BF16,
-                   tokens=np.arange(min(cores, w.T), dtype=np.int32))
+    oracle_call(inp, np.arange(min(cores, w.T), dtype=np.int32))
     t_one = max(time.time() - t0, 1e-3)
     n = int(max(1, min(w.T, min(cores, w.T) * max(1.0, 1.0 / t_one))))
     order = np.random.default_rng(7).permutation(w.T).astype(np.int32)
 
     def step(i):
         toks = np.sort(np.take(order, np.arange(i * n, (i + 1) * n) % w.T))
-        oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], inp["topk_ids"], inp["topk_w"], act=oracle.ACT_BF16,
-                       tokens=toks)
+        oracle_call(inp, toks)
 
     for i in range(args.warmup):
         step(i)

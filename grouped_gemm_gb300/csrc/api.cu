@@ -19,6 +19,7 @@ namespace {
 std::atomic<unsigned long long> g_wait_limit_ns{2000ull * 1000 * 1000};
 std::atomic<int> g_gather_mode{0};  // MOE_OPT_GATHER: 0 gather kernel, 1 in-GEMM gather4
 std::atomic<int> g_prefetch{0};     // MOE_OPT_L2_PREFETCH (measured slower on GB300: off)
+std::atomic<int> g_stall_test{0};   // MOE_OPT_TEST_STALL
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -120,7 +121,9 @@ Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipe
   w.slot_w = reinterpret_cast<float*>(take(sizeof(float) * w.S_max));
   w.slot_of_pair = reinterpret_cast<int*>(take(sizeof(int) * (P ? P : 1)));
   w.blk_base = reinterpret_cast<int*>(take(sizeof(int) * (size_t)w.route_blocks * E));
-  if (dtype == MOE_MXFP8) {
+  if (pipeline == kRouteOnly) {
+    // routing regions only
+  } else if (dtype == MOE_MXFP8) {
     w.xg = take((size_t)w.S_max * D);
     w.xg_sf = take((size_t)w.S_max * D / 32);
     w.act = take((size_t)w.S_max * H);
@@ -166,6 +169,7 @@ moe_status_t forward_fused_bf16(const Workspace& ws, const void* x, const void* 
   fa.D = D;
   fa.H = H;
   fa.n_slices = H / 128;
+  fa.stall_test = g_stall_test.load();
   const int grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * fa.n_slices);
   e = launch_fused_bf16(map_xg, map_w1, map_w2, fa, grid, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -207,6 +211,7 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
   ma.wait_limit_ns = g_wait_limit_ns.load();
   ma.D = D;
   ma.H = H;
+  ma.stall_test = g_stall_test.load();
   MxArgs up = ma;
   up.sf_a = ws.xg_sf;
   up.sf_b = w1_sf;
@@ -253,6 +258,10 @@ moe_status_t moe_ffn_set_option(int option, long long value) {
       if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
       g_gather_mode.store((int)value);
       return MOE_OK;
+    case MOE_OPT_TEST_STALL:
+      if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
+      g_stall_test.store((int)value);
+      return MOE_OK;
     case MOE_OPT_L2_PREFETCH:
       if (value < 0 || value > 64) return MOE_ERR_INVALID_ARG;
       g_prefetch.store((int)value);
@@ -266,7 +275,7 @@ moe_status_t moe_ffn_route(const int32_t* topk_ids, const float* topk_w, int T, 
                            void* stream) {
   if (T < 0 || E < 1 || E > kMaxExperts || k < 1 || (int64_t)T * k >= ((int64_t)1 << 30)) return MOE_ERR_INVALID_ARG;
   if (!workspace || (T > 0 && (!topk_ids || !topk_w))) return MOE_ERR_INVALID_ARG;
-  Workspace ws = plan_workspace(workspace, T, E, 128, 128, k, MOE_FUSED);
+  Workspace ws = plan_workspace(workspace, T, E, 128, 128, k, kRouteOnly);
   if (workspace_bytes < ws.bytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (T == 0) {
@@ -346,6 +355,7 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   ga.D = D;
   ga.H = H;
   ga.prefetch = g_prefetch.load();
+  ga.stall_test = g_stall_test.load();
 
   GemmArgs up = ga;
   up.n_col_tiles = H / kUpFold;

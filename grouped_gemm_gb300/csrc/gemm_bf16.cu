@@ -52,7 +52,7 @@ struct GemmCfg {
   static_assert(N % 32 == 0 && N >= 32 && N <= 256, "MMA N");
   static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns: power of two <= 512");
   static_assert(kSmemBytes <= 232448, "shared memory");
-  static_assert((2 * STAGES + 5) * 8 + 8 <= kBarrierBytes, "barrier area");
+  static_assert((2 * STAGES + 6) * 8 + 8 <= kBarrierBytes, "barrier area");
 };
 
 constexpr int kThreads = 192;
@@ -78,7 +78,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* never = drain + 1;  // no thread ever arrives here (failure-path test hook)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -94,6 +95,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tempty[a], kEpiThreads);
     }
     mbar_init(drain, 1);
+    mbar_init(never, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&map_a);
@@ -202,6 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
+    if (args.stall_test) ok = mbar_wait(never, 0, wc, 90);  // runs out after the wait limit
     int it = 0;
     for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x, ++it) {
       const int acc = it & 1;

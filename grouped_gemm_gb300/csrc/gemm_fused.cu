@@ -47,7 +47,7 @@ constexpr int kRedBytes = kBM * kRedRowBytes;
 constexpr int kFBarrierBytes = 256;
 constexpr int kFSmem = 1024 + kFStages * kFStage + kActBytes + kRedBytes + kFBarrierBytes;
 static_assert(kFSmem <= 232448, "shared memory");
-static_assert((2 * kFStages + 6) * 8 + 8 <= kFBarrierBytes, "barrier area");
+static_assert((2 * kFStages + 7) * 8 + 8 <= kFBarrierBytes, "barrier area");
 constexpr uint64_t kFDrainNs = 200ull * 1000 * 1000;
 
 __device__ __forceinline__ float f_u2f(uint32_t u) { return __uint_as_float(u); }
@@ -67,7 +67,8 @@ __global__ void __launch_bounds__(kFThreads, 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* act_full = tempty + 2;
   uint64_t* drain = act_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* never = drain + 1;  // no thread ever arrives here (failure-path test hook)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -84,6 +85,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     }
     mbar_init(act_full, kFEpiThreads);
     mbar_init(drain, 1);
+    mbar_init(never, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&map_xg);
@@ -154,6 +156,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
     uint32_t ph = 0;
     uint32_t q = 0;  // accumulator job counter
     bool ok = true;
+    if (args.stall_test) ok = mbar_wait(never, 0, wc, 91);  // runs out after the wait limit
     int it = 0;
     const uint32_t act_addr = smem_addr(act);
     for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x, ++it) {

@@ -67,7 +67,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 1;
   uint64_t* drain = tempty + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* never = drain + 1;  // no thread ever arrives here (failure-path test hook)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -81,6 +82,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     mbar_init(tfull, 1);
     mbar_init(tempty, kMxEpi);
     mbar_init(drain, 1);
+    mbar_init(never, 1);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&map_a);
@@ -152,6 +154,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
+    if (args.stall_test) ok = mbar_wait(never, 0, wc, 92);  // runs out after the wait limit
     int it = 0;
     for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x, ++it) {
       if (!(ok = mbar_wait(tempty, ((uint32_t)it & 1u) ^ 1u, wc, 22))) break;

@@ -39,6 +39,9 @@ struct Workspace {
   int route_blocks;
 };
 
+// pipeline = kRouteOnly plans only the routing regions (the common prefix of
+// every layout).
+constexpr int kRouteOnly = -1;
 Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipeline, int dtype = 0);
 
 // ----------------------------------------------------------------- kernels
@@ -55,6 +58,7 @@ struct GemmArgs {
   int n_col_tiles;          // column tiles per row block
   int k_blocks;             // reduction length / kBK
   int prefetch;             // k-blocks of L2 prefetch ahead of the smem ring (0 = off)
+  int stall_test;           // test hook: the MMA issuer first waits on a barrier nothing arrives on
 };
 
 // Routing; when zero_out != nullptr the first launch also zero-fills
@@ -81,6 +85,7 @@ struct FusedArgs {
   unsigned long long wait_limit_ns;
   int D, H;
   int n_slices;             // H / 128
+  int stall_test;           // test hook (see GemmArgs)
 };
 
 cudaError_t launch_fused_bf16(const CUtensorMap& map_xg, const CUtensorMap& map_w1, const CUtensorMap& map_w2,
@@ -102,6 +107,7 @@ struct MxArgs {
   int D, H;
   int n_col_tiles;
   int k_blocks;             // K / 128
+  int stall_test;           // test hook (see GemmArgs)
 };
 
 cudaError_t launch_up_mxfp8(const CUtensorMap& a, const CUtensorMap& w1, const MxArgs& args, int grid,

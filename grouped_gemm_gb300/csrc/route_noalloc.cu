@@ -64,12 +64,12 @@ extern "C" moe_status_t moe_ffn_route_noalloc(const int32_t* topk_ids, const flo
   if (T < 0 || E < 1 || E > kMaxExperts || k < 1) return MOE_ERR_INVALID_ARG;
   if ((int64_t)T * k > kNoAllocMaxPairs) return MOE_ERR_WORKSPACE_TOO_SMALL;
   if (T > 0 && (!topk_ids || !topk_w)) return MOE_ERR_INVALID_ARG;
-  const Workspace probe = plan_workspace(nullptr, T, E, 128, 128, k, MOE_FUSED);
+  const Workspace probe = plan_workspace(nullptr, T, E, 128, 128, k, kRouteOnly);
   if (probe.bytes > kNoAllocScratchBytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const Workspace ws = plan_workspace(scratch, T, E, 128, 128, k, MOE_FUSED);
+  const Workspace ws = plan_workspace(scratch, T, E, 128, 128, k, kRouteOnly);
   // The status words accumulate error bits: they must start at zero.
   cudaError_t e = cudaMemsetAsync(ws.err, 0, 32, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;

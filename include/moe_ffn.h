@@ -151,8 +151,14 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *   MOE_OPT_L2_PREFETCH  0..64 (default 0): how many K-blocks ahead of the
  *                   shared-memory ring the GEMM producers prefetch operand
  *                   tiles into L2 (cp.async.bulk.prefetch.tensor); 0 = off.
- *                   Measured on GB300, prefetching slowed every workload. */
-typedef enum { MOE_OPT_GATHER = 0, MOE_OPT_L2_PREFETCH = 1 } moe_option_t;
+ *                   Measured on GB300, prefetching slowed every workload.
+ *   MOE_OPT_TEST_STALL  0 (default) or 1: test hook for failure detection.
+ *                   With 1, each GEMM kernel's MMA issuer first waits on a
+ *                   barrier that nothing ever arrives on; the wait runs out
+ *                   after the wait limit, the kernel records
+ *                   MOE_ERR_DEVICE_TIMEOUT and exits cleanly (no fault, no
+ *                   hang), so the status path can be tested on a GPU. */
+typedef enum { MOE_OPT_GATHER = 0, MOE_OPT_L2_PREFETCH = 1, MOE_OPT_TEST_STALL = 2 } moe_option_t;
 moe_status_t moe_ffn_set_option(int option, long long value);
 
 /* Per-stage timing of later moe_ffn_forward calls (a benchmarking aid, off by

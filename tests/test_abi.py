@@ -71,3 +71,25 @@ def test_forward_rejects_bad_arguments_on_host():
     assert call(*a) == 0                                   # T == 0: no-op
     a = list(base); a[17] = 16
     assert call(*a) in (5, 7)                              # workspace too small (or no device here)
+
+
+def test_header_compiles_as_c_and_cpp():
+    import subprocess
+    for lang, std in (("c", "c99"), ("c++", "c++17")):
+        subprocess.run(["gcc", "-x", lang, f"-std={std}", "-Wall", "-Werror", "-fsyntax-only", HEADER], check=True)
+
+
+def test_noalloc_route_size_limits_on_host():
+    """The allocation-free routing call accepts problems up to T*k = 131072 with
+    E = 1024 (its scratch layout fits the fixed array) and rejects larger ones
+    before touching the device.  Without a GPU an accepted call stops at the
+    device lookup (MOE_ERR_CUDA); a rejected one returns
+    MOE_ERR_WORKSPACE_TOO_SMALL."""
+    import torch
+    L = moe.lib()
+    A = 1 << 20
+    if torch.cuda.is_available():
+        pytest.skip("host-only check")
+    assert L.moe_ffn_route_noalloc(A, A, 131072, 1024, 1, A, A, A, None, None) == 7
+    assert L.moe_ffn_route_noalloc(A, A, 16384, 1024, 8, A, A, A, None, None) == 7
+    assert L.moe_ffn_route_noalloc(A, A, 16385, 1024, 8, A, A, A, None, None) == 5

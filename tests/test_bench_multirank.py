@@ -1,0 +1,57 @@
+"""Host-side logic of bench.py's multi-rank (token-sharded, weak-scaling) path
+on CPU with the gloo backend, world size 2: the step time is the slowest
+rank's, the value aggregates every rank's work, and the reference arm runs on
+rank 0 only."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, results):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        ms_local = [2.0, 5.0][rank]
+        ms = bench.max_over_ranks(ms_local, world)
+        value = bench.weak_scaling_tflops(1e12, ms, world)
+        dist.barrier()
+        results[rank] = (ms, value)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_weak_scaling_gloo():
+    world = 2
+    mgr = mp.get_context("spawn").Manager()
+    results = mgr.dict()
+    mp.start_processes(_worker, args=(world, _free_port(), results), nprocs=world, start_method="spawn", join=True)
+    for r in range(world):
+        ms, value = results[r]
+        assert ms == 5.0
+        assert value == pytest.approx(1e12 * 2 / 5e-3 / 1e12)
+
+
+def test_single_rank_helpers():
+    assert bench.max_over_ranks(3.0, 1) == 3.0
+    assert bench.weak_scaling_tflops(2e12, 1.0, 1) == pytest.approx(2000.0)
+
+
+def test_reference_arm_only_on_rank0():
+    class A:
+        workload, steps, warmup, gpus, pipeline = "tiny", 1, 0, 2, "split"
+    assert bench.run_reference(A(), rank=1) is None
