@@ -17,9 +17,10 @@ namespace moe {
 namespace {
 
 std::atomic<unsigned long long> g_wait_limit_ns{2000ull * 1000 * 1000};
-std::atomic<int> g_gather_mode{0};  // MOE_OPT_GATHER: 0 gather kernel, 1 in-GEMM gather4
+std::atomic<int> g_gather_mode{0};  // MOE_OPT_GATHER: 0 gather kernel, 1 in-GEMM gather4, 2 in-GEMM cp.async
 std::atomic<int> g_prefetch{0};     // MOE_OPT_L2_PREFETCH (measured slower on GB300: off)
 std::atomic<int> g_stall_test{0};   // MOE_OPT_TEST_STALL
+std::atomic<int> g_up_pairs{0};     // MOE_OPT_UP_PAIRS (measured slower on GB300: off)
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -117,6 +118,7 @@ Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipe
   w.offsets = reinterpret_cast<int*>(take(sizeof(int) * (E + 1)));
   w.pad_offsets = reinterpret_cast<int*>(take(sizeof(int) * (E + 1)));
   w.expert_of_rb = reinterpret_cast<int*>(take(sizeof(int) * w.max_rb));
+  w.pair_info = reinterpret_cast<int*>(take(sizeof(int) * w.max_rb));
   w.row_tok = reinterpret_cast<int*>(take(sizeof(int) * w.S_max));
   w.slot_w = reinterpret_cast<float*>(take(sizeof(float) * w.S_max));
   w.slot_of_pair = reinterpret_cast<int*>(take(sizeof(int) * (P ? P : 1)));
@@ -255,12 +257,16 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns) { g_wait_limit_ns.store(ns ? ns : 1)
 moe_status_t moe_ffn_set_option(int option, long long value) {
   switch (option) {
     case MOE_OPT_GATHER:
-      if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
+      if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
       g_gather_mode.store((int)value);
       return MOE_OK;
     case MOE_OPT_TEST_STALL:
       if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
       g_stall_test.store((int)value);
+      return MOE_OK;
+    case MOE_OPT_UP_PAIRS:
+      if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
+      g_up_pairs.store((int)value);
       return MOE_OK;
     case MOE_OPT_L2_PREFETCH:
       if (value < 0 || value > 64) return MOE_ERR_INVALID_ARG;
@@ -320,10 +326,11 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
     return forward_split_mxfp8(ws, x, x_sf, w1, w1_sf, w2, w2_sf, topk_ids, topk_w, out, T, E, D, H, k, sms, st);
   if (pipeline == MOE_FUSED) return forward_fused_bf16(ws, x, w1, w2, topk_ids, topk_w, out, T, E, D, H, k, sms, st);
 
-  const bool gather4 = g_gather_mode.load() == 1;
+  const int gather = g_gather_mode.load();
+  const bool in_gemm_gather = gather != 0;
   CUtensorMap map_xg, map_w1, map_act, map_w2;
-  const bool map_a_ok = gather4 ? make_map_bf16(&map_xg, x, (uint64_t)T, (uint64_t)D, 1)
-                                : make_map_bf16(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, kBM);
+  const bool map_a_ok = in_gemm_gather ? make_map_bf16(&map_xg, x, (uint64_t)T, (uint64_t)D, 1)
+                                       : make_map_bf16(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, kBM);
   if (!map_a_ok ||
       !make_map_bf16(&map_w1, w1, (uint64_t)E * 2 * H, (uint64_t)D, kUpFold) ||
       !make_map_bf16(&map_act, ws.act, (uint64_t)ws.S_max, (uint64_t)H, kBM) ||
@@ -333,11 +340,12 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   prof_mark(st, 0);
   // With the in-GEMM gather the routing launch also zero-fills out;
   // otherwise the gather kernel does.
-  cudaError_t e = gather4 ? launch_route(ws, topk_ids, topk_w, T, E, k, st, out, (int64_t)T * D * 2, sms * 2)
-                          : launch_route(ws, topk_ids, topk_w, T, E, k, st);
+  cudaError_t e = in_gemm_gather
+                      ? launch_route(ws, topk_ids, topk_w, T, E, k, st, out, (int64_t)T * D * 2, sms * 2)
+                      : launch_route(ws, topk_ids, topk_w, T, E, k, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 1);
-  if (!gather4) {
+  if (!in_gemm_gather) {
     e = launch_gather_zero(ws, x, D, out, (int64_t)T * D * 2, sms * 4, st);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
@@ -346,6 +354,7 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   GemmArgs ga{};
   ga.meta = ws.meta;
   ga.expert_of_rb = ws.expert_of_rb;
+  ga.pair_info = ws.pair_info;
   ga.row_tok = ws.row_tok;
   ga.slot_w = ws.slot_w;
   ga.act = ws.act;
@@ -361,7 +370,9 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   up.n_col_tiles = H / kUpFold;
   up.k_blocks = D / kBK;
   const int up_grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * up.n_col_tiles);
-  e = launch_up_bf16(map_xg, map_w1, up, up_grid, st, gather4);
+  up.x = x;
+  e = (gather == 0 && g_up_pairs.load()) ? launch_up_pair_bf16(map_xg, map_w1, up, up_grid, st)
+                                         : launch_up_bf16(map_xg, map_w1, up, up_grid, st, gather);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 3);
 
@@ -427,6 +438,7 @@ moe_status_t moe_ffn_sync_status(void* workspace, void* stream) {
   if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemcpy(words, workspace, sizeof words, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaMemset(workspace, 0, 64) != cudaSuccess) return MOE_ERR_CUDA;
+  if (words[0] & kErrLaunch) return MOE_ERR_CUDA;
   if (words[0] & kErrTimeout) return MOE_ERR_DEVICE_TIMEOUT;
   if (words[0] & kErrBadRouting) return MOE_ERR_BAD_ROUTING;
   return MOE_OK;

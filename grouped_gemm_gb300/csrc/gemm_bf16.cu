@@ -43,12 +43,15 @@ struct GemmCfg {
   static constexpr int kBBytes = N * kBK * 2;               // N rows of 128 B
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * N;                   // double-buffered accumulator
-  // DOWN stages each output row (N bf16) in shared memory for the bulk
-  // reduction; +16 B per row keeps the 32 rows of a warp on distinct banks.
-  static constexpr int kStageRowBytes = N * 2 + 16;
+  // DOWN stages half an output row (N/2 bf16) at a time in shared memory for
+  // the bulk reduction; +16 B per row keeps the 32 rows of a warp on distinct
+  // banks.  Half rows leave room for a 4-stage ring.
+  static constexpr int kStageRowBytes = N + 16;
   static constexpr int kStagingBytes = MODE == kModeDown ? kBM * kStageRowBytes : 0;
-  static constexpr int kBarrierBytes = 256;
-  static constexpr int kSmemBytes = 1024 /*align slack*/ + STAGES * kStageBytes + kStagingBytes + kBarrierBytes;
+  static constexpr int kBarrierBytes = 128;
+  // No alignment slack: dynamic shared memory starts 1024-byte aligned (the
+  // kernel checks and reports an error otherwise).
+  static constexpr int kSmemBytes = STAGES * kStageBytes + kStagingBytes + kBarrierBytes;
   static_assert(N % 32 == 0 && N >= 32 && N <= 256, "MMA N");
   static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns: power of two <= 512");
   static_assert(kSmemBytes <= 232448, "shared memory");
@@ -57,19 +60,29 @@ struct GemmCfg {
 
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
+constexpr int kGatherThreads = 128;   // extra producer warps 6..9 of the cp.async gather
+enum { kGatherTile = 0, kGatherTma4 = 1, kGatherCpAsync = 2 };
+template <int GATHER>
+constexpr int threads_for() { return GATHER == kGatherCpAsync ? kThreads + kGatherThreads : kThreads; }
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;  // 200 ms
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 
-__device__ __forceinline__ float swiglu(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+// silu(g) * u = g / (1 + e^-g) * u; fast reciprocal division (the result is
+// rounded to bf16 right after).
+__device__ __forceinline__ float swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
-template <int MODE, int N, int STAGES, bool GATHER>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int MODE, int N, int STAGES, int GATHER>
+__global__ void __launch_bounds__(threads_for<GATHER>(), 1)
     grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                              const GemmArgs args) {
   using Cfg = GemmCfg<MODE, N, STAGES>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_addr(smem_raw) & 1023u) {  // SW128 tiles need 1024-byte alignment
+    if (threadIdx.x == 0) atomicOr(args.err, kErrLaunch);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * Cfg::kABytes;
   uint8_t* sStage = smem + STAGES * Cfg::kStageBytes;
@@ -87,7 +100,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
+      // with the cp.async gather, each of its threads also arrives once per stage
+      mbar_init(&full[s], GATHER == kGatherCpAsync ? 1 + kGatherThreads : 1);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -132,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto prefetch_one = [&]() {
       if (pf_tile >= n_tiles) return;
       const int prb = pf_tile / args.n_col_tiles, pj = pf_tile % args.n_col_tiles;
-      if (!GATHER) tma_prefetch_2d(&map_a, pf_kb * kBK, prb * kBM);
+      if (GATHER == kGatherTile) tma_prefetch_2d(&map_a, pf_kb * kBK, prb * kBM);
       if (MODE == kModeUp) {
         constexpr int G = N / 2;
         const int row0 = pf_e * 2 * args.H + pj * G;
@@ -153,7 +167,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rb = tile / args.n_col_tiles, j = tile % args.n_col_tiles;
       const int e = args.expert_of_rb[rb];
       int g0 = 0, g1 = 0, g2 = 0, g3 = 0;
-      if (GATHER) {  // lane l fetches tile rows 4l..4l+3; padding rows read row 0
+      if (GATHER == kGatherTma4) {  // lane l fetches tile rows 4l..4l+3; padding rows read row 0
         const int* rt = args.row_tok + (int64_t)rb * kBM + lane * 4;
         g0 = max(rt[0], 0);
         g1 = max(rt[1], 0);
@@ -164,16 +178,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         int got = 1;
         if (lane == 0) {
           got = mbar_wait(&empty[s], ph ^ 1u, wc, 1) ? 1 : 0;
-          if (got) mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
+          if (got)
+            mbar_arrive_expect_tx(&full[s], GATHER == kGatherCpAsync ? Cfg::kBBytes : Cfg::kStageBytes);
         }
         got = __shfl_sync(0xffffffffu, got, 0);
         if (!got) {
           ok = false;
           break;
         }
-        if (GATHER) {
+        if (GATHER == kGatherTma4) {
           tma_gather4(sA + s * Cfg::kABytes + lane * 4 * kBK * 2, &map_a, &full[s], kb * kBK, g0, g1, g2, g3);
-        } else if (lane == 0) {
+        } else if (GATHER == kGatherTile && lane == 0) {
           tma_load_2d(sA + s * Cfg::kABytes, &map_a, &full[s], kb * kBK, rb * kBM);
         }
         if (lane == 0) {
@@ -241,7 +256,55 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit(drain);
       mbar_wait_drain(drain, 0, kDrainNs);
     }
-  } else if (warp >= 2) {
+  } else if (GATHER == kGatherCpAsync && warp >= 6) {
+    // ------------------------------------------------------------ row gather
+    // 128 threads copy the tile's 128 token rows straight from x: thread t
+    // moves 16-byte chunk t%8 of rows t/8 + 16i (i < 8), written at its
+    // 128-byte-swizzle position, so each warp instruction covers four whole
+    // 128-byte row segments.  A stage is released to the MMA issuer
+    // (fence.proxy.async, then an arrive on full[]) kLag stages after it was
+    // issued, when cp.async.wait_group shows its copies have landed.
+    constexpr int kLag = STAGES - 1;
+    const int gt = threadIdx.x - kThreads;
+    const int chunk = gt & 7, r0 = gt >> 3;
+    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(args.x);
+    int s = 0;
+    uint32_t ph = 0;
+    int issued = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
+      const int rb = tile / args.n_col_tiles;
+      const __nv_bfloat16* src[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        src[i] = x + (int64_t)max(args.row_tok[(int64_t)rb * kBM + r0 + 16 * i], 0) * args.D + chunk * 8;
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!(ok = mbar_wait(&empty[s], ph ^ 1u, wc, 5))) break;
+        uint8_t* a = sA + s * Cfg::kABytes;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int r = r0 + 16 * i;
+          cp_async_16(a + r * 128 + ((chunk ^ (r & 7)) << 4), src[i] + kb * kBK);
+        }
+        cp_async_commit();
+        if (issued >= kLag) {
+          cp_async_wait_group<kLag>();
+          fence_proxy_async_smem();
+          mbar_arrive(&full[(issued - kLag) % STAGES]);
+        }
+        ++issued;
+        if (++s == STAGES) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+    cp_async_wait_group<0>();
+    if (ok) {  // release the last stages
+      fence_proxy_async_smem();
+      for (int n = max(issued - kLag, 0); n < issued; ++n) mbar_arrive(&full[n % STAGES]);
+    }
+  } else if (warp >= 2 && warp < 6) {
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;  // TMEM lanes this warp may access
     const int row = quad * 32 + lane;
@@ -275,32 +338,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         const float w = args.slot_w[slot];
-        bulk_wait_read_all();  // the previous tile's reduction has left the staging row
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(args.out) + (int64_t)(tok < 0 ? 0 : tok) * args.D + j * N;
 #pragma unroll 1
-        for (int c = 0; c < N / 32; c += 2) {
-          uint32_t v0[32], v1[32];
-          tmem_ld_x32_pair(tacc + c * 32, tacc + (c + 1) * 32, v0, v1);
-          if (tok >= 0) {
+        for (int h = 0; h < 2; ++h) {     // two half rows of N/2 columns
+          bulk_wait_read_all();          // the previous reduction has left the staging row
+#pragma unroll 1
+          for (int c = h * (N / 64); c < (h + 1) * (N / 64); c += 2) {
+            uint32_t v0[32], v1[32];
+            tmem_ld_x32_pair(tacc + c * 32, tacc + (c + 1) * 32, v0, v1);
+            if (tok >= 0) {
+              uint8_t* st0 = my_stage + (c - h * (N / 64)) * 64;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              st_shared_v4(my_stage + c * 64 + q * 16, pack_bf16x2(w * u2f(v0[8 * q + 0]), w * u2f(v0[8 * q + 1])),
-                           pack_bf16x2(w * u2f(v0[8 * q + 2]), w * u2f(v0[8 * q + 3])),
-                           pack_bf16x2(w * u2f(v0[8 * q + 4]), w * u2f(v0[8 * q + 5])),
-                           pack_bf16x2(w * u2f(v0[8 * q + 6]), w * u2f(v0[8 * q + 7])));
+              for (int q = 0; q < 4; ++q)
+                st_shared_v4(st0 + q * 16, pack_bf16x2(w * u2f(v0[8 * q + 0]), w * u2f(v0[8 * q + 1])),
+                             pack_bf16x2(w * u2f(v0[8 * q + 2]), w * u2f(v0[8 * q + 3])),
+                             pack_bf16x2(w * u2f(v0[8 * q + 4]), w * u2f(v0[8 * q + 5])),
+                             pack_bf16x2(w * u2f(v0[8 * q + 6]), w * u2f(v0[8 * q + 7])));
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              st_shared_v4(my_stage + (c + 1) * 64 + q * 16,
-                           pack_bf16x2(w * u2f(v1[8 * q + 0]), w * u2f(v1[8 * q + 1])),
-                           pack_bf16x2(w * u2f(v1[8 * q + 2]), w * u2f(v1[8 * q + 3])),
-                           pack_bf16x2(w * u2f(v1[8 * q + 4]), w * u2f(v1[8 * q + 5])),
-                           pack_bf16x2(w * u2f(v1[8 * q + 6]), w * u2f(v1[8 * q + 7])));
+              for (int q = 0; q < 4; ++q)
+                st_shared_v4(st0 + 64 + q * 16, pack_bf16x2(w * u2f(v1[8 * q + 0]), w * u2f(v1[8 * q + 1])),
+                             pack_bf16x2(w * u2f(v1[8 * q + 2]), w * u2f(v1[8 * q + 3])),
+                             pack_bf16x2(w * u2f(v1[8 * q + 4]), w * u2f(v1[8 * q + 5])),
+                             pack_bf16x2(w * u2f(v1[8 * q + 6]), w * u2f(v1[8 * q + 7])));
+            }
           }
-        }
-        if (tok >= 0) {
-          fence_proxy_async_smem();
-          bulk_reduce_add_bf16(static_cast<__nv_bfloat16*>(args.out) + (int64_t)tok * args.D + j * N, my_stage,
-                               N * 2);
-          bulk_commit();
+          if (tok >= 0) {
+            fence_proxy_async_smem();
+            bulk_reduce_add_bf16(orow + h * (N / 2), my_stage, N);
+            bulk_commit();
+          }
         }
       }
       tc_fence_before();
@@ -319,16 +385,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int MODE, int N, int STAGES, bool GATHER>
+template <int MODE, int N, int STAGES, int GATHER>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args, int grid,
                         cudaStream_t stream, bool pdl) {
   using Cfg = GemmCfg<MODE, N, STAGES>;
   auto kern = grouped_gemm_bf16_kernel<MODE, N, STAGES, GATHER>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
-  if (err != cudaSuccess) return err;
+  // once per device: not a stream operation, so it stays out of graph capture
+  static bool smem_set[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!smem_set[dev]) {
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+    if (err != cudaSuccess) return err;
+    smem_set[dev] = true;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads_for<GATHER>());
   cfg.dynamicSmemBytes = Cfg::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -342,14 +415,17 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmAr
 }  // namespace
 
 cudaError_t launch_up_bf16(const CUtensorMap& map_a, const CUtensorMap& map_w1, const GemmArgs& args, int grid,
-                           cudaStream_t stream, bool gather4) {
-  if (gather4) return launch_gemm<kModeUp, 2 * kUpFold, kUpStages, true>(map_a, map_w1, args, grid, stream, false);
-  return launch_gemm<kModeUp, 2 * kUpFold, kUpStages, false>(map_a, map_w1, args, grid, stream, false);
+                           cudaStream_t stream, int gather) {
+  if (gather == kGatherTma4)
+    return launch_gemm<kModeUp, 2 * kUpFold, kUpStages, kGatherTma4>(map_a, map_w1, args, grid, stream, false);
+  if (gather == kGatherCpAsync)
+    return launch_gemm<kModeUp, 2 * kUpFold, kUpStages, kGatherCpAsync>(map_a, map_w1, args, grid, stream, false);
+  return launch_gemm<kModeUp, 2 * kUpFold, kUpStages, kGatherTile>(map_a, map_w1, args, grid, stream, false);
 }
 
 cudaError_t launch_down_bf16(const CUtensorMap& map_act, const CUtensorMap& map_w2, const GemmArgs& args, int grid,
                              cudaStream_t stream, bool pdl) {
-  return launch_gemm<kModeDown, kDownN, kDownStages, false>(map_act, map_w2, args, grid, stream, pdl);
+  return launch_gemm<kModeDown, kDownN, kDownStages, kGatherTile>(map_act, map_w2, args, grid, stream, pdl);
 }
 
 }  // namespace moe

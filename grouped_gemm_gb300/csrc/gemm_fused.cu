@@ -51,7 +51,7 @@ static_assert((2 * kFStages + 7) * 8 + 8 <= kFBarrierBytes, "barrier area");
 constexpr uint64_t kFDrainNs = 200ull * 1000 * 1000;
 
 __device__ __forceinline__ float f_u2f(uint32_t u) { return __uint_as_float(u); }
-__device__ __forceinline__ float f_swiglu(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+__device__ __forceinline__ float f_swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
 __global__ void __launch_bounds__(kFThreads, 1)
     fused_moe_bf16_kernel(const __grid_constant__ CUtensorMap map_xg, const __grid_constant__ CUtensorMap map_w1,
@@ -313,8 +313,15 @@ __global__ void __launch_bounds__(256) f32_to_bf16_kernel(const float4* __restri
 
 cudaError_t launch_fused_bf16(const CUtensorMap& map_xg, const CUtensorMap& map_w1, const CUtensorMap& map_w2,
                               const FusedArgs& args, int grid, cudaStream_t stream) {
-  cudaError_t err = cudaFuncSetAttribute(fused_moe_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmem);
-  if (err != cudaSuccess) return err;
+  // once per device: not a stream operation, so it stays out of graph capture
+  static bool smem_set[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!smem_set[dev]) {
+    cudaError_t err = cudaFuncSetAttribute(fused_moe_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFSmem);
+    if (err != cudaSuccess) return err;
+    smem_set[dev] = true;
+  }
   fused_moe_bf16_kernel<<<grid, kFThreads, kFSmem, stream>>>(map_xg, map_w1, map_w2, args);
   return cudaGetLastError();
 }

@@ -49,7 +49,7 @@ struct MxCfg {
 };
 
 __device__ __forceinline__ float mx_u2f(uint32_t u) { return __uint_as_float(u); }
-__device__ __forceinline__ float mx_swiglu(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+__device__ __forceinline__ float mx_swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
 template <int MODE, int STAGES>
 __global__ void __launch_bounds__(kMxThreads, 1)
@@ -275,8 +275,15 @@ cudaError_t launch_mx(const CUtensorMap& a, const CUtensorMap& b, const MxArgs& 
                       bool pdl) {
   using Cfg = MxCfg<MODE, STAGES>;
   auto kern = grouped_gemm_mxfp8_kernel<MODE, STAGES>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
-  if (err != cudaSuccess) return err;
+  // once per device: not a stream operation, so it stays out of graph capture
+  static bool smem_set[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!smem_set[dev]) {
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    if (err != cudaSuccess) return err;
+    smem_set[dev] = true;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kMxThreads);

@@ -19,11 +19,12 @@ constexpr int kRouteTokPerBlock = 256;  // tokens per routing block
 // 256-byte boundary; sizes depend only on (T, E, D, H, k, pipeline).
 struct Workspace {
   int* err;            // [8]   err[0] error bits, err[1] timeout site
-  int* meta;           // [8]   meta[0] = number of 128-row blocks
+  int* meta;           // [8]   meta[0] = number of 128-row blocks, meta[1] = number of block pairs
   int* counts;         // [E]
   int* offsets;        // [E+1] unpadded exclusive scan of counts
   int* pad_offsets;    // [E+1] exclusive scan of counts rounded up to 128
   int* expert_of_rb;   // [max_rb]
+  int* pair_info;      // [max_rb] (first row block << 1) | (second block of the same expert exists)
   int* row_tok;        // [S_max] token of each padded slot, -1 for padding
   float* slot_w;       // [S_max] routing weight of each padded slot, 0 for padding
   int* slot_of_pair;   // [P]   unpadded slot of pair p = t*k + j
@@ -46,8 +47,9 @@ Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipe
 
 // ----------------------------------------------------------------- kernels
 struct GemmArgs {
-  const int* meta;          // meta[0] = number of row blocks
+  const int* meta;          // meta[0] = number of row blocks, meta[1] = number of block pairs
   const int* expert_of_rb;
+  const int* pair_info;     // pairs of row blocks of one expert (see Workspace)
   const int* row_tok;
   const float* slot_w;
   void* act;                // up: bf16 [S_max, H] output
@@ -59,6 +61,7 @@ struct GemmArgs {
   int k_blocks;             // reduction length / kBK
   int prefetch;             // k-blocks of L2 prefetch ahead of the smem ring (0 = off)
   int stall_test;           // test hook: the MMA issuer first waits on a barrier nothing arrives on
+  const void* x;            // up with the cp.async gather: the token rows [T, D]
 };
 
 // Routing; when zero_out != nullptr the first launch also zero-fills
@@ -68,10 +71,15 @@ cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const flo
 // xg = x[row_tok] for live slots, and (when out != nullptr) out[0 .. out_bytes) = 0.
 cudaError_t launch_gather_zero(const Workspace& ws, const void* x, int D, void* out, int64_t out_bytes, int grid,
                                cudaStream_t stream);
-// gather4: map_a is x [T, D] with one-row boxes and the kernel gathers the
-// token rows itself; otherwise map_a is the pre-gathered xg [S_max, D].
+// gather: 0 = map_a is the pre-gathered xg [S_max, D]; 1 = map_a is x [T, D]
+// with one-row boxes and the kernel gathers with TMA gather4; 2 = the kernel's
+// cp.async warps gather rows of args.x (map_a unused).
 cudaError_t launch_up_bf16(const CUtensorMap& map_a, const CUtensorMap& map_w1, const GemmArgs& args, int grid,
-                           cudaStream_t stream, bool gather4);
+                           cudaStream_t stream, int gather);
+// Up-projection with two row blocks of one expert per tile sharing each W1
+// tile (tiles = block pairs x column tiles).
+cudaError_t launch_up_pair_bf16(const CUtensorMap& map_a, const CUtensorMap& map_w1, const GemmArgs& args, int grid,
+                                cudaStream_t stream);
 cudaError_t launch_down_bf16(const CUtensorMap& map_act, const CUtensorMap& map_w2, const GemmArgs& args, int grid,
                              cudaStream_t stream, bool pdl);
 
@@ -123,6 +131,6 @@ cudaError_t launch_mx_quantize(const float* in, int64_t n, uint8_t* q, uint8_t* 
 constexpr int kUpFold = 128;      // gate rows + up rows per tile: N = 2 * kUpFold
 constexpr int kUpStages = 4;
 constexpr int kDownN = 256;
-constexpr int kDownStages = 3;
+constexpr int kDownStages = 4;
 
 }  // namespace moe

@@ -16,6 +16,7 @@ namespace moe {
 // Bits of the device error word (workspace word 0).
 constexpr int kErrBadRouting = 1;   // an expert id outside [0, E)
 constexpr int kErrTimeout = 2;      // a bounded wait ran out
+constexpr int kErrLaunch = 4;       // a kernel found its launch environment unusable
 
 struct WaitCtl {
   volatile int* abort;       // CTA-local abort flag (shared memory)
@@ -135,6 +136,16 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, u
       " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_addr(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
       : "memory");
+}
+
+// 16-byte global -> shared copy through L2 only (cp.async, tracked by groups).
+__device__ __forceinline__ void cp_async_16(void* sdst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(sdst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Make this thread's generic-proxy shared-memory writes visible to the async

@@ -76,9 +76,18 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
   return base + x - v;
 }
 
+// Pairs of consecutive row blocks of one expert: expert e with nrb blocks owns
+// ceil(nrb/2) pairs; pair_info = (first block << 1) | (1 if the pair is full).
+__device__ void fill_pairs(int e, int lane, int po, int pc, int pair_off, int* pair_info) {
+  const int rb0 = po / kRowPad, nrb = pc / kRowPad;
+  for (int q = lane; q < (nrb + 1) / 2; q += 32)
+    pair_info[pair_off + q] = ((rb0 + 2 * q) << 1) | (2 * q + 1 < nrb ? 1 : 0);
+}
+
 __global__ void __launch_bounds__(1024) route_scan_kernel(int NB, int E, int* __restrict__ blk, int* counts,
                                                           int* offsets, int* pad_offsets, int* meta,
-                                                          int* expert_of_rb, int* row_tok, float* slot_w) {
+                                                          int* expert_of_rb, int* pair_info, int* row_tok,
+                                                          float* slot_w) {
   __shared__ int seg_sum[1024];
   __shared__ int cnt_s[kMaxExperts];
   __shared__ int warp_sums[32];
@@ -120,23 +129,81 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int NB, int E, int* __
   // scans over experts
   const int cnt = tid < E ? cnt_s[tid] : 0;
   const int padc = (cnt + kRowPad - 1) / kRowPad * kRowPad;
-  int tot, ptot;
+  int tot, ptot, qtot;
   const int off = block_exclusive_scan(cnt, warp_sums, &tot);
   const int poff = block_exclusive_scan(padc, warp_sums, &ptot);
+  const int qoff = block_exclusive_scan((padc / kRowPad + 1) / 2, warp_sums, &qtot);
+  __shared__ int pair_off_s[kMaxExperts];
   if (tid < E) {
     counts[tid] = cnt;
     offsets[tid] = off;
     pad_offsets[tid] = poff;
-    for (int rb = poff / kRowPad; rb < (poff + padc) / kRowPad; ++rb) expert_of_rb[rb] = tid;
-    for (int s = poff + cnt; s < poff + padc; ++s) {
-      row_tok[s] = -1;
-      slot_w[s] = 0.f;
-    }
+    seg_sum[tid] = poff;  // reuse: padded offset of each expert
+    pair_off_s[tid] = qoff;
   }
   if (tid == 0) {
     offsets[E] = tot;
     pad_offsets[E] = ptot;
     meta[0] = ptot / kRowPad;
+    meta[1] = qtot;
+  }
+  __syncthreads();
+  // padding rows and block -> expert, one warp per expert
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int e = warp; e < E; e += 32) {
+    const int c = cnt_s[e], po = seg_sum[e];
+    const int pc = (c + kRowPad - 1) / kRowPad * kRowPad;
+    for (int s2 = po + c + lane; s2 < po + pc; s2 += 32) {
+      row_tok[s2] = -1;
+      slot_w[s2] = 0.f;
+    }
+    for (int rb = po / kRowPad + lane; rb < (po + pc) / kRowPad; rb += 32) expert_of_rb[rb] = e;
+    fill_pairs(e, lane, po, pc, pair_off_s[e], pair_info);
+  }
+}
+
+// Stable scatter of one warp's contiguous pair range [q0, q1): 32 pairs per
+// step, ranks from __match_any_sync, the running per-expert base in `mine`.
+// ids and weights are fetched eight steps at a time so the loop is not a chain
+// of dependent global loads.
+__device__ __forceinline__ void scatter_range(const int32_t* __restrict__ ids, const float* __restrict__ topk_w,
+                                              int64_t q0, int64_t q1, int E, int k, int* mine, const int* s_off,
+                                              const int* s_poff, int* __restrict__ row_tok,
+                                              float* __restrict__ slot_w, int* __restrict__ slot_of_pair) {
+  const int lane = threadIdx.x & 31;
+  constexpr int kBatch = 8;
+  for (int64_t b0 = q0; b0 < q1; b0 += 32 * kBatch) {
+    int ev[kBatch];
+    float wv[kBatch];
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int64_t p = b0 + i * 32 + lane;
+      ev[i] = p < q1 ? ids[p] : -1;
+      wv[i] = p < q1 ? topk_w[p] : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int64_t p = b0 + i * 32 + lane;
+      if (b0 + i * 32 >= q1) break;  // warp-uniform
+      const bool in = p < q1;
+      const int e = ev[i];
+      const bool valid = in && (unsigned)e < (unsigned)E;
+      const int key = valid ? e : E + lane;  // invalid lanes never match anyone
+      const unsigned peers = __match_any_sync(0xffffffffu, key);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      const int r = valid ? mine[e] + rank : 0;
+      __syncwarp();
+      if (valid && rank == 0) mine[e] += __popc(peers);
+      __syncwarp();
+      if (valid) {
+        const int ps = s_poff[e] + r;
+        row_tok[ps] = (int)(p / k);
+        slot_w[ps] = wv[i];
+        slot_of_pair[p] = s_off[e] + r;
+      } else if (in) {
+        slot_of_pair[p] = -1;
+      }
+    }
   }
 }
 
@@ -145,13 +212,19 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
                          const int* __restrict__ blk_base, const int* __restrict__ offsets,
                          const int* __restrict__ pad_offsets, int* __restrict__ row_tok, float* __restrict__ slot_w,
                          int* __restrict__ slot_of_pair) {
-  extern __shared__ int wcnt[];  // [kScatterWarps][E]
+  extern __shared__ int wcnt[];  // [kScatterWarps][E], then offsets[E], pad_offsets[E]
+  int* s_off = wcnt + kScatterWarps * E;
+  int* s_poff = s_off + E;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t p0 = (int64_t)blockIdx.x * kRouteTokPerBlock * k;
   const int64_t p1 = min(P, p0 + (int64_t)kRouteTokPerBlock * k);
   const int64_t sub = (p1 - p0 + kScatterWarps - 1) / kScatterWarps;
   const int64_t q0 = min(p1, p0 + warp * sub), q1 = min(p1, q0 + sub);
   for (int i = threadIdx.x; i < kScatterWarps * E; i += blockDim.x) wcnt[i] = 0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    s_off[e] = offsets[e];
+    s_poff[e] = pad_offsets[e];
+  }
   __syncthreads();
   for (int64_t p = q0 + lane; p < q1; p += 32) {
     const int e = ids[p];
@@ -167,28 +240,85 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
     }
   }
   __syncthreads();
-  int* mine = wcnt + warp * E;
-  for (int64_t base = q0; base < q1; base += 32) {
-    const int64_t p = base + lane;
-    const bool in = p < q1;
-    const int e = in ? ids[p] : -1;
-    const bool valid = in && (unsigned)e < (unsigned)E;
-    const int key = valid ? e : E + lane;  // invalid lanes never match anyone
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    const int r = valid ? mine[e] + rank : 0;
-    __syncwarp();
-    if (valid && rank == 0) mine[e] += __popc(peers);
-    __syncwarp();
-    if (valid) {
-      const int ps = pad_offsets[e] + r;
-      row_tok[ps] = (int)(p / k);
-      slot_w[ps] = topk_w[p];
-      slot_of_pair[p] = offsets[e] + r;
-    } else if (in) {
-      slot_of_pair[p] = -1;
+  scatter_range(ids, topk_w, q0, q1, E, k, wcnt + warp * E, s_off, s_poff, row_tok, slot_w, slot_of_pair);
+}
+
+// The whole routing permutation in one 1024-thread block, for small problems
+// (P <= kRouteSmallMaxPairs, E <= kRouteSmallMaxExperts): per-warp histograms
+// of 32 contiguous pair ranges, scans over warps and experts, padding and
+// block->expert tables, then the same stable warp-match scatter as above.
+constexpr int kRouteSmallWarps = 32;
+constexpr int kRouteSmallMaxExperts = 256;
+constexpr int64_t kRouteSmallMaxPairs = 8192;
+
+__global__ void __launch_bounds__(1024)
+    route_small_kernel(const int32_t* __restrict__ ids, const float* __restrict__ topk_w, int P, int E, int k,
+                       int* __restrict__ err, int* __restrict__ counts, int* __restrict__ offsets,
+                       int* __restrict__ pad_offsets, int* __restrict__ meta, int* __restrict__ expert_of_rb,
+                       int* __restrict__ pair_info, int* __restrict__ row_tok, float* __restrict__ slot_w,
+                       int* __restrict__ slot_of_pair) {
+  __shared__ int wcnt[kRouteSmallWarps * kRouteSmallMaxExperts];
+  __shared__ int s_off[kRouteSmallMaxExperts], s_poff[kRouteSmallMaxExperts], s_cnt[kRouteSmallMaxExperts];
+  __shared__ int s_qoff[kRouteSmallMaxExperts];
+  __shared__ int warp_sums[32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sub = (P + kRouteSmallWarps - 1) / kRouteSmallWarps;
+  const int q0 = min(P, warp * sub), q1 = min(P, q0 + sub);
+  for (int i = threadIdx.x; i < kRouteSmallWarps * E; i += blockDim.x) wcnt[i] = 0;
+  __syncthreads();
+  bool bad = false;
+  for (int p = q0 + lane; p < q1; p += 32) {
+    const int e = ids[p];
+    if ((unsigned)e < (unsigned)E) atomicAdd(&wcnt[warp * E + e], 1);
+    else bad = true;
+  }
+  if (bad) atomicOr(err, kErrBadRouting);
+  __syncthreads();
+  // exclusive prefix over warps, per expert; totals = counts
+  int cnt = 0;
+  if (threadIdx.x < E) {
+    const int e = threadIdx.x;
+    for (int w = 0; w < kRouteSmallWarps; ++w) {
+      const int c = wcnt[w * E + e];
+      wcnt[w * E + e] = cnt;
+      cnt += c;
     }
   }
+  const int padc = (cnt + kRowPad - 1) / kRowPad * kRowPad;
+  int tot, ptot, qtot;
+  const int off = block_exclusive_scan(cnt, warp_sums, &tot);
+  const int poff = block_exclusive_scan(padc, warp_sums, &ptot);
+  const int qoff = block_exclusive_scan((padc / kRowPad + 1) / 2, warp_sums, &qtot);
+  if (threadIdx.x < E) {
+    const int e = threadIdx.x;
+    counts[e] = cnt;
+    offsets[e] = off;
+    pad_offsets[e] = poff;
+    s_off[e] = off;
+    s_poff[e] = poff;
+    s_cnt[e] = cnt;
+    s_qoff[e] = qoff;
+  }
+  if (threadIdx.x == 0) {
+    offsets[E] = tot;
+    pad_offsets[E] = ptot;
+    meta[0] = ptot / kRowPad;
+    meta[1] = qtot;
+  }
+  __syncthreads();
+  // padding rows and block -> expert, one warp per expert
+  for (int e = warp; e < E; e += kRouteSmallWarps) {
+    const int c = s_cnt[e], po = s_poff[e];
+    const int pc = (c + kRowPad - 1) / kRowPad * kRowPad;
+    for (int s2 = po + c + lane; s2 < po + pc; s2 += 32) {
+      row_tok[s2] = -1;
+      slot_w[s2] = 0.f;
+    }
+    for (int rb = po / kRowPad + lane; rb < (po + pc) / kRowPad; rb += 32) expert_of_rb[rb] = e;
+    fill_pairs(e, lane, po, pc, s_qoff[e], pair_info);
+  }
+  // stable scatter
+  scatter_range(ids, topk_w, q0, q1, E, k, wcnt + warp * E, s_off, s_poff, row_tok, slot_w, slot_of_pair);
 }
 
 // xg[s, :] = x[row_tok[s], :] for live slots (16-byte vector copies, one warp
@@ -229,13 +359,19 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
 cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const float* topk_w, int T, int E, int k,
                          cudaStream_t stream, void* zero_out, int64_t zero_bytes, int zero_grid) {
   const int64_t P = (int64_t)T * k;
+  if (!zero_out && P <= kRouteSmallMaxPairs && E <= kRouteSmallMaxExperts) {
+    route_small_kernel<<<1, 1024, 0, stream>>>(topk_ids, topk_w, (int)P, E, k, ws.err, ws.counts, ws.offsets,
+                                               ws.pad_offsets, ws.meta, ws.expert_of_rb, ws.pair_info, ws.row_tok,
+                                               ws.slot_w, ws.slot_of_pair);
+    return cudaGetLastError();
+  }
   const int NB = ws.route_blocks;
   const int grid = zero_out ? (NB > zero_grid ? NB : zero_grid) : NB;
   route_count_kernel<<<grid, 256, E * sizeof(int), stream>>>(topk_ids, P, E, k, NB, ws.blk_base, ws.err,
                                                              static_cast<uint4*>(zero_out), zero_bytes / 16);
   route_scan_kernel<<<1, 1024, 0, stream>>>(NB, E, ws.blk_base, ws.counts, ws.offsets, ws.pad_offsets, ws.meta,
-                                            ws.expert_of_rb, ws.row_tok, ws.slot_w);
-  route_scatter_kernel<<<NB, kScatterWarps * 32, kScatterWarps * E * sizeof(int), stream>>>(
+                                            ws.expert_of_rb, ws.pair_info, ws.row_tok, ws.slot_w);
+  route_scatter_kernel<<<NB, kScatterWarps * 32, (kScatterWarps + 2) * E * sizeof(int), stream>>>(
       topk_ids, topk_w, P, E, k, ws.blk_base, ws.offsets, ws.pad_offsets, ws.row_tok, ws.slot_w, ws.slot_of_pair);
   return cudaGetLastError();
 }

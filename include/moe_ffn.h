@@ -148,6 +148,9 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   with TMA tile::gather4, four rows per instruction (sec. 3
  *                   "For the tokens: TMA gathers them too").  Measured on
  *                   GB300, option 1 makes the up kernel 2-3.5x slower.
+ *                   2: four extra warps of the up-projection kernel copy the
+ *                   token rows from x with 16-byte cp.async into the
+ *                   swizzled operand tile (no gathered copy of x in HBM).
  *   MOE_OPT_L2_PREFETCH  0..64 (default 0): how many K-blocks ahead of the
  *                   shared-memory ring the GEMM producers prefetch operand
  *                   tiles into L2 (cp.async.bulk.prefetch.tensor); 0 = off.
@@ -157,8 +160,19 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   barrier that nothing ever arrives on; the wait runs out
  *                   after the wait limit, the kernel records
  *                   MOE_ERR_DEVICE_TIMEOUT and exits cleanly (no fault, no
- *                   hang), so the status path can be tested on a GPU. */
-typedef enum { MOE_OPT_GATHER = 0, MOE_OPT_L2_PREFETCH = 1, MOE_OPT_TEST_STALL = 2 } moe_option_t;
+ *                   hang), so the status path can be tested on a GPU.
+ *   MOE_OPT_UP_PAIRS  0 (default) or 1: with 1 (and MOE_OPT_GATHER 0) each
+ *                   tile of the bf16 up-projection takes two row blocks of
+ *                   one expert against one weight tile ("Prime Flash MoE"
+ *                   sec. 5 "BPC and CPC").  Measured on GB300 it is 7-17%
+ *                   slower (its accumulators fill TMEM, so the epilogue no
+ *                   longer overlaps the next tile's MMAs). */
+typedef enum {
+  MOE_OPT_GATHER = 0,
+  MOE_OPT_L2_PREFETCH = 1,
+  MOE_OPT_TEST_STALL = 2,
+  MOE_OPT_UP_PAIRS = 3
+} moe_option_t;
 moe_status_t moe_ffn_set_option(int option, long long value);
 
 /* Per-stage timing of later moe_ffn_forward calls (a benchmarking aid, off by

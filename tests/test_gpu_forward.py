@@ -20,17 +20,21 @@ pytestmark = pytest.mark.gpu
 
 # (pipeline, gather option): the split pipeline with the materializing gather
 # kernel (default) and with the in-kernel TMA gather4
-MODES = {"split": (moe.MOE_SPLIT, 0), "split_gather4": (moe.MOE_SPLIT, 1), "fused": (moe.MOE_FUSED, 0)}
+MODES = {"split": (moe.MOE_SPLIT, 0, 0), "split_pairs": (moe.MOE_SPLIT, 0, 1),
+         "split_gather4": (moe.MOE_SPLIT, 1, 0), "split_cpasync": (moe.MOE_SPLIT, 2, 0),
+         "fused": (moe.MOE_FUSED, 0, 0)}
 PIPELINES = list(MODES)
 
 
 def run_mode(inp, dev, mode, **kw):
-    pipeline, gather = MODES[mode]
+    pipeline, gather, pairs = MODES[mode]
     moe.moe_ffn_set_option(moe.MOE_OPT_GATHER, gather)
+    moe.moe_ffn_set_option(moe.MOE_OPT_UP_PAIRS, pairs)
     try:
         return run_forward(inp, dev, pipeline=pipeline, **kw)
     finally:
         moe.moe_ffn_set_option(moe.MOE_OPT_GATHER, 0)
+        moe.moe_ffn_set_option(moe.MOE_OPT_UP_PAIRS, 0)
 
 
 def oracle_out(inp, tokens=None):

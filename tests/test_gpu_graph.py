@@ -1,0 +1,50 @@
+"""The forward pass can be captured in a CUDA graph (the pages time graph
+replays) and replays give the same result as eager calls."""
+import numpy as np
+import pytest
+import torch
+
+import grouped_gemm_gb300 as moe
+import oracle
+from grouped_gemm_gb300 import workloads as wl
+
+from helpers import assert_close, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("pipeline", [moe.MOE_SPLIT, moe.MOE_FUSED])
+def test_graph_replay_matches_oracle(pipeline):
+    inp = wl.make_custom(300, 512, 256, 16, 4, seed=21)
+    w = inp["workload"]
+    dev = to_dev(inp)
+    out = torch.empty(w.T, w.D, dtype=torch.bfloat16, device="cuda")
+    ws = moe.alloc_workspace(w.T, w.E, w.D, w.H, w.k, moe.MOE_BF16, pipeline)
+
+    def step():
+        moe.moe_ffn_forward(dev["x"], dev["w1"], dev["w2"], dev["topk_ids"], dev["topk_w"], out, E=w.E, D=w.D,
+                            H=w.H, k=w.k, workspace=ws, pipeline=pipeline)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    ref = oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], inp["topk_ids"], inp["topk_w"], act=oracle.ACT_BF16)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert moe.moe_ffn_sync_status(ws) == 0
+        assert_close(out, ref, label="graph replay")
+    # new routing written into the same input buffers is picked up by the replay
+    inp2 = wl.make_custom(300, 512, 256, 16, 4, seed=22)
+    dev["topk_ids"].copy_(torch.from_numpy(inp2["topk_ids"]))
+    dev["topk_w"].copy_(torch.from_numpy(inp2["topk_w"]))
+    g.replay()
+    torch.cuda.synchronize()
+    ref2 = oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], inp2["topk_ids"], inp2["topk_w"], act=oracle.ACT_BF16)
+    assert_close(out, ref2, label="graph replay, new routing")
