@@ -21,6 +21,7 @@ std::atomic<int> g_gather_mode{0};  // MOE_OPT_GATHER: 0 gather kernel, 1 in-GEM
 std::atomic<int> g_prefetch{0};     // MOE_OPT_L2_PREFETCH (measured slower on GB300: off)
 std::atomic<int> g_stall_test{0};   // MOE_OPT_TEST_STALL
 std::atomic<int> g_up_pairs{0};     // MOE_OPT_UP_PAIRS (measured slower on GB300: off)
+std::atomic<int> g_dynamic_tiles{0};  // MOE_OPT_DYNAMIC_TILES (measured: +2% decode, -3..5% prefill/large: off)
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -264,6 +265,10 @@ moe_status_t moe_ffn_set_option(int option, long long value) {
       if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
       g_stall_test.store((int)value);
       return MOE_OK;
+    case MOE_OPT_DYNAMIC_TILES:
+      if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
+      g_dynamic_tiles.store((int)value);
+      return MOE_OK;
     case MOE_OPT_UP_PAIRS:
       if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
       g_up_pairs.store((int)value);
@@ -366,7 +371,9 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   ga.prefetch = g_prefetch.load();
   ga.stall_test = g_stall_test.load();
 
+  const bool dyn = g_dynamic_tiles.load() != 0;
   GemmArgs up = ga;
+  up.tile_counter = dyn ? ws.meta + 2 : nullptr;
   up.n_col_tiles = H / kUpFold;
   up.k_blocks = D / kBK;
   const int up_grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * up.n_col_tiles);
@@ -377,6 +384,7 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   prof_mark(st, 3);
 
   GemmArgs dn = ga;
+  dn.tile_counter = dyn ? ws.meta + 3 : nullptr;
   dn.n_col_tiles = D / kDownN;
   dn.k_blocks = H / kBK;
   const int dn_grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * dn.n_col_tiles);

@@ -36,6 +36,7 @@ namespace moe {
 namespace {
 
 enum { kModeUp = 0, kModeDown = 1 };
+constexpr int kTileSlots = 4;   // depth of the producer -> consumers tile-index ring
 
 template <int MODE, int N, int STAGES>
 struct GemmCfg {
@@ -48,14 +49,14 @@ struct GemmCfg {
   // banks.  Half rows leave room for a 4-stage ring.
   static constexpr int kStageRowBytes = N + 16;
   static constexpr int kStagingBytes = MODE == kModeDown ? kBM * kStageRowBytes : 0;
-  static constexpr int kBarrierBytes = 128;
+  static constexpr int kBarrierBytes = 256;
   // No alignment slack: dynamic shared memory starts 1024-byte aligned (the
   // kernel checks and reports an error otherwise).
   static constexpr int kSmemBytes = STAGES * kStageBytes + kStagingBytes + kBarrierBytes;
   static_assert(N % 32 == 0 && N >= 32 && N <= 256, "MMA N");
   static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns: power of two <= 512");
   static_assert(kSmemBytes <= 232448, "shared memory");
-  static_assert((2 * STAGES + 6) * 8 + 8 <= kBarrierBytes, "barrier area");
+  static_assert((2 * STAGES + 6 + 2 * kTileSlots) * 8 + 8 + 4 * kTileSlots <= kBarrierBytes, "barrier area");
 };
 
 constexpr int kThreads = 192;
@@ -92,11 +93,20 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint64_t* never = drain + 1;  // no thread ever arrives here (failure-path test hook)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
+  uint64_t* tile_full = never + 1;
+  uint64_t* tile_empty = tile_full + kTileSlots;
+  volatile int* tile_ring = reinterpret_cast<volatile int*>(tile_empty + kTileSlots);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(tile_ring) + kTileSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const WaitCtl wc{abort_flag, args.err, args.wait_limit_ns};
+  // Tile sequence: warp 0 draws tile indices (from a global atomic counter
+  // when args.tile_counter is set -- CTAs that finish early take more tiles --
+  // else the static round-robin blockIdx.x + i * gridDim.x) and publishes them
+  // through a small ring; the MMA issuer, the epilogue and the gather warps
+  // read the same sequence.  An index >= n_tiles ends the sequence.
+  constexpr int kTileReaders = 1 + kEpiThreads + (GATHER == kGatherCpAsync ? kGatherThreads : 0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -110,6 +120,10 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
     }
     mbar_init(drain, 1);
     mbar_init(never, 1);
+    for (int i = 0; i < kTileSlots; ++i) {
+      mbar_init(&tile_full[i], 1);
+      mbar_init(&tile_empty[i], kTileReaders);
+    }
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&map_a);
@@ -128,6 +142,20 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
   const int num_rb = args.meta[0];
   const int n_tiles = num_rb * args.n_col_tiles;
   const int KB = args.k_blocks;
+
+  // consumer side of the tile ring: the next tile index, or -1 if aborting
+  int t_slot = 0;
+  uint32_t t_phase = 0;
+  auto take_tile = [&](int site) -> int {
+    if (!mbar_wait(&tile_full[t_slot], t_phase, wc, site)) return -1;
+    const int t = tile_ring[t_slot];
+    mbar_arrive(&tile_empty[t_slot]);
+    if (++t_slot == kTileSlots) {
+      t_slot = 0;
+      t_phase ^= 1u;
+    }
+    return t;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -163,7 +191,31 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
     };
     if (lane == 0)
       for (int i = 0; i < args.prefetch; ++i) prefetch_one();
-    for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
+    int tile = -1;
+    while (ok) {
+      // publish the next tile index to the other roles (warp 0, lane 0)
+      int next = 0;
+      if (lane == 0) {
+        if (!mbar_wait(&tile_empty[t_slot], t_phase ^ 1u, wc, 6)) {
+          next = -1;
+        } else {
+          next = args.tile_counter ? atomicAdd(args.tile_counter, 1)
+                                   : (tile < 0 ? (int)blockIdx.x : tile + (int)gridDim.x);
+          tile_ring[t_slot] = next;
+          mbar_arrive(&tile_full[t_slot]);
+        }
+      }
+      next = __shfl_sync(0xffffffffu, next, 0);
+      if (++t_slot == kTileSlots) {
+        t_slot = 0;
+        t_phase ^= 1u;
+      }
+      if (next < 0) {
+        ok = false;
+        break;
+      }
+      if (next >= n_tiles) break;
+      tile = next;
       const int rb = tile / args.n_col_tiles, j = tile % args.n_col_tiles;
       const int e = args.expert_of_rb[rb];
       int g0 = 0, g1 = 0, g2 = 0, g3 = 0;
@@ -221,7 +273,13 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
     bool ok = true;
     if (args.stall_test) ok = mbar_wait(never, 0, wc, 90);  // runs out after the wait limit
     int it = 0;
-    for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x, ++it) {
+    for (; ok; ++it) {
+      const int tile = take_tile(7);
+      if (tile < 0) {
+        ok = false;
+        break;
+      }
+      if (tile >= n_tiles) break;
       const int acc = it & 1;
       const uint32_t aph = (uint32_t)(it >> 1) & 1u;
       if (!mbar_wait(&tempty[acc], aph ^ 1u, wc, 2)) {
@@ -272,7 +330,13 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
     uint32_t ph = 0;
     int issued = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
+    while (ok) {
+      const int tile = take_tile(8);
+      if (tile < 0) {
+        ok = false;
+        break;
+      }
+      if (tile >= n_tiles) break;
       const int rb = tile / args.n_col_tiles;
       const __nv_bfloat16* src[8];
 #pragma unroll
@@ -311,7 +375,9 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
     const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
     uint8_t* my_stage = sStage + row * Cfg::kStageRowBytes;
     int it = 0;
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
+    for (;; ++it) {
+      const int tile = take_tile(9);
+      if (tile < 0 || tile >= n_tiles) break;
       const int acc = it & 1;
       const uint32_t aph = (uint32_t)(it >> 1) & 1u;
       if (!mbar_wait(&tfull[acc], aph, wc, 4)) break;

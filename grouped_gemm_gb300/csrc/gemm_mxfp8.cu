@@ -16,7 +16,8 @@
 // TMEM columns, so it is single-buffered and the scale sets sit behind it at
 // columns 256 + 16 * stage_slot (sec. 7: the scale columns rotate so in-flight
 // stages never overwrite each other's scales).  The epilogue frees the
-// accumulator as soon as it has read it.
+// accumulator as soon as it has read it; eight epilogue warps (two per TMEM
+// lane quadrant, each taking half of the columns) keep that window short.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -30,8 +31,8 @@ namespace {
 enum { kMxUp = 0, kMxDown = 1 };
 constexpr int kMxBK = 128;                  // fp8 elements (bytes) per stage row
 constexpr int kMxN = 256;
-constexpr int kMxThreads = 192;
-constexpr int kMxEpi = 128;
+constexpr int kMxThreads = 64 + 256;   // producer warp, MMA warp, 8 epilogue warps
+constexpr int kMxEpi = 256;            // two warps per TMEM lane quadrant, one per column half
 constexpr uint64_t kMxDrainNs = 200ull * 1000 * 1000;
 
 template <int MODE, int STAGES>
@@ -40,8 +41,10 @@ struct MxCfg {
   static constexpr int kB = kMxN * kMxBK;         // 32 KB
   static constexpr int kSF = 512 * 3;             // SFA tile + two SFB tiles
   static constexpr int kTx = kA + kB + kSF;
-  static constexpr int kStageRowBytes = kMxN * 2 + 16;
-  static constexpr int kStaging = MODE == kMxDown ? kBM * kStageRowBytes : 0;
+  // DOWN: each epilogue thread stages half an output row (128 bf16, +16 B so
+  // a warp's rows fall on distinct banks) for its bulk reduction.
+  static constexpr int kStageRowBytes = kMxN + 16;
+  static constexpr int kStaging = MODE == kMxDown ? kMxEpi * kStageRowBytes : 0;
   static constexpr int kBarrierBytes = 256;
   static constexpr int kSmem = 1024 + STAGES * (kA + kB + kSF) + kStaging + kBarrierBytes;
   static_assert(kSmem <= 232448, "shared memory");
@@ -190,9 +193,10 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;      // which half of the accumulator columns
     const int row = quad * 32 + lane;
     const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
-    uint8_t* my_stage = sStage + row * Cfg::kStageRowBytes;
+    uint8_t* my_stage = sStage + (half * kBM + row) * Cfg::kStageRowBytes;
     int it = 0;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
       if (!mbar_wait(tfull, (uint32_t)it & 1u, wc, 24)) break;
@@ -201,37 +205,41 @@ __global__ void __launch_bounds__(kMxThreads, 1)
       const int64_t slot = (int64_t)rb * kBM + row;
       const int tok = args.row_tok[slot];
       if (MODE == kMxUp) {
-        float act[128];
+        // columns [64 half, 64 half + 64) of gate (0..127) and of up (128..255)
+        float act[64];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t g[32], u[32];
-          tmem_ld_x32_pair(lane_base + c * 32, lane_base + 128 + c * 32, g, u);
+          const int col = half * 64 + c * 32;
+          tmem_ld_x32_pair(lane_base + col, lane_base + 128 + col, g, u);
 #pragma unroll
           for (int i = 0; i < 32; ++i) act[c * 32 + i] = mx_swiglu(mx_u2f(g[i]), mx_u2f(u[i]));
         }
         tc_fence_before();
-        mbar_arrive(tempty);  // the accumulator is free for the next tile
+        mbar_arrive(tempty);  // the accumulator is free once all 256 threads have read it
         if (tok >= 0) {
-          uint8_t* dst = static_cast<uint8_t*>(args.act) + slot * args.H + j * 128;
+          uint8_t* dst = static_cast<uint8_t*>(args.act) + slot * args.H + j * 128 + half * 64;
           uint32_t sfw = 0;
 #pragma unroll
-          for (int blk = 0; blk < 4; ++blk) {
+          for (int blk = 0; blk < 2; ++blk) {
             uint32_t q[8];
             const uint32_t sfb = mx_quantize32(act + blk * 32, q);
             sfw |= sfb << (8 * blk);
             st_global_v4(dst + blk * 32, q[0], q[1], q[2], q[3]);
             st_global_v4(dst + blk * 32 + 16, q[4], q[5], q[6], q[7]);
           }
-          uint8_t* sfdst = static_cast<uint8_t*>(args.act_sf) + sf_tile_offset(rb, j, args.H / 128) + sf_in_tile(row);
-          *reinterpret_cast<uint32_t*>(sfdst) = sfw;
+          uint8_t* sfdst = static_cast<uint8_t*>(args.act_sf) + sf_tile_offset(rb, j, args.H / 128) + sf_in_tile(row) +
+                           half * 2;
+          *reinterpret_cast<uint16_t*>(sfdst) = (uint16_t)sfw;
         }
       } else {
         const float w = args.slot_w[slot];
         bulk_wait_read_all();
 #pragma unroll 1
-        for (int c = 0; c < kMxN / 32; c += 2) {
+        for (int c = 0; c < 4; c += 2) {   // 4 chunks of 32 columns = this thread's half
           uint32_t v0[32], v1[32];
-          tmem_ld_x32_pair(lane_base + c * 32, lane_base + (c + 1) * 32, v0, v1);
+          const int col = half * 128 + c * 32;
+          tmem_ld_x32_pair(lane_base + col, lane_base + col + 32, v0, v1);
           if (tok >= 0) {
 #pragma unroll
             for (int qd = 0; qd < 4; ++qd)
@@ -252,8 +260,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         mbar_arrive(tempty);
         if (tok >= 0) {
           fence_proxy_async_smem();
-          bulk_reduce_add_bf16(static_cast<__nv_bfloat16*>(args.out) + (int64_t)tok * args.D + j * kMxN, my_stage,
-                               kMxN * 2);
+          bulk_reduce_add_bf16(static_cast<__nv_bfloat16*>(args.out) + (int64_t)tok * args.D + j * kMxN + half * 128,
+                               my_stage, kMxN);
           bulk_commit();
         }
       }
@@ -297,28 +305,48 @@ cudaError_t launch_mx(const CUtensorMap& a, const CUtensorMap& b, const MxArgs& 
   return cudaLaunchKernelEx(&cfg, kern, a, b, args);
 }
 
-// xg[s] = x[row_tok[s]] (D bytes of e4m3 per row) and the row's scales moved
-// from row-major x_sf[T, D/32] into the blocked tile layout of xg_sf; live
-// slots only.  The same launch zero-fills out.
+// xg[s] = x[row_tok[s]] (D bytes of e4m3 per row, one warp per row, live slots
+// only), then the scales of every row block moved from row-major x_sf[T, D/32]
+// into the blocked 512-byte tiles of xg_sf: one warp per (row block, K tile),
+// lane l gathering the 4-byte scale words of rows l, l+32, l+64, l+96 and
+// writing them as one 16-byte store (the tile's row l).  The same launch
+// zero-fills out.
 __global__ void __launch_bounds__(256) gather_rows_mx_kernel(const uint4* __restrict__ x, const uint32_t* __restrict__ x_sf,
                                                              const int* __restrict__ row_tok, const int* __restrict__ meta,
                                                              uint4* __restrict__ xg, uint8_t* __restrict__ xg_sf, int D,
                                                              uint4* __restrict__ out, int64_t out_vecs) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t S = (int64_t)meta[0] * kRowPad;
+  const int n_rb = meta[0];
+  const int64_t S = (int64_t)n_rb * kRowPad;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t gwarp = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;
   const int vec_per_row = D / 16, kt_per_row = D / 128;
-  for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp; row < S; row += nwarps) {
+  for (int64_t row = gwarp; row < S; row += nwarps) {
     const int tok = row_tok[row];
     if (tok < 0) continue;
     const uint4* src = x + (int64_t)tok * vec_per_row;
     uint4* dst = xg + row * vec_per_row;
-    for (int i = lane; i < vec_per_row; i += 32) dst[i] = __ldg(src + i);
-    const int r = (int)(row % kRowPad);
-    const int64_t rt = row / kRowPad;
-    for (int kt = lane; kt < kt_per_row; kt += 32)
-      *reinterpret_cast<uint32_t*>(xg_sf + sf_tile_offset(rt, kt, kt_per_row) + sf_in_tile(r)) =
-          __ldg(x_sf + (int64_t)tok * (D / 128) + kt);
+    int i = lane;
+    for (; i + 96 < vec_per_row; i += 128) {
+      const uint4 a = __ldg(src + i), b = __ldg(src + i + 32), c = __ldg(src + i + 64), d = __ldg(src + i + 96);
+      dst[i] = a;
+      dst[i + 32] = b;
+      dst[i + 64] = c;
+      dst[i + 96] = d;
+    }
+    for (; i < vec_per_row; i += 32) dst[i] = __ldg(src + i);
+  }
+  const int64_t n_sf_tiles = (int64_t)n_rb * kt_per_row;
+  for (int64_t t = gwarp; t < n_sf_tiles; t += nwarps) {
+    const int64_t rb = t / kt_per_row;
+    const int kt = (int)(t % kt_per_row);
+    uint32_t w[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const int tok = row_tok[rb * kRowPad + g * 32 + lane];
+      w[g] = tok >= 0 ? __ldg(x_sf + (int64_t)tok * kt_per_row + kt) : 0x7f7f7f7fu;  // padding: scale 1
+    }
+    *reinterpret_cast<uint4*>(xg_sf + sf_tile_offset(rb, kt, kt_per_row) + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
   }
   const uint4 z = make_uint4(0, 0, 0, 0);
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < out_vecs; i += (int64_t)gridDim.x * blockDim.x)

@@ -19,7 +19,8 @@ constexpr int kRouteTokPerBlock = 256;  // tokens per routing block
 // 256-byte boundary; sizes depend only on (T, E, D, H, k, pipeline).
 struct Workspace {
   int* err;            // [8]   err[0] error bits, err[1] timeout site
-  int* meta;           // [8]   meta[0] = number of 128-row blocks, meta[1] = number of block pairs
+  int* meta;           // [8]   meta[0] = number of 128-row blocks, meta[1] = number of block pairs,
+                       //       meta[2], meta[3] = tile counters of the up and down kernels
   int* counts;         // [E]
   int* offsets;        // [E+1] unpadded exclusive scan of counts
   int* pad_offsets;    // [E+1] exclusive scan of counts rounded up to 128
@@ -62,6 +63,7 @@ struct GemmArgs {
   int prefetch;             // k-blocks of L2 prefetch ahead of the smem ring (0 = off)
   int stall_test;           // test hook: the MMA issuer first waits on a barrier nothing arrives on
   const void* x;            // up with the cp.async gather: the token rows [T, D]
+  int* tile_counter;        // dynamic tile scheduling: zeroed before the launch; nullptr = static
 };
 
 // Routing; when zero_out != nullptr the first launch also zero-fills

@@ -146,6 +146,8 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int NB, int E, int* __
     pad_offsets[E] = ptot;
     meta[0] = ptot / kRowPad;
     meta[1] = qtot;
+    meta[2] = 0;  // tile counters of the GEMM kernels that follow
+    meta[3] = 0;
   }
   __syncthreads();
   // padding rows and block -> expert, one warp per expert
@@ -304,6 +306,8 @@ __global__ void __launch_bounds__(1024)
     pad_offsets[E] = ptot;
     meta[0] = ptot / kRowPad;
     meta[1] = qtot;
+    meta[2] = 0;  // tile counters of the GEMM kernels that follow
+    meta[3] = 0;
   }
   __syncthreads();
   // padding rows and block -> expert, one warp per expert

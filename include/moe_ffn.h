@@ -166,12 +166,20 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   one expert against one weight tile ("Prime Flash MoE"
  *                   sec. 5 "BPC and CPC").  Measured on GB300 it is 7-17%
  *                   slower (its accumulators fill TMEM, so the epilogue no
- *                   longer overlaps the next tile's MMAs). */
+ *                   longer overlaps the next tile's MMAs).
+ *   MOE_OPT_DYNAMIC_TILES  0 (default) or 1: with 1 the split pipeline's
+ *                   bf16 GEMM kernels take their tiles from a global atomic
+ *                   counter (CTAs that finish early take more work; "Porting
+ *                   Block-Scaled GEMM Kernels" sec. 7 hands out work ids from
+ *                   an atomic counter); 0 = static round-robin.  Measured on
+ *                   GB300: 2% faster at decode, 3-5% slower at prefill and
+ *                   large_skewed. */
 typedef enum {
   MOE_OPT_GATHER = 0,
   MOE_OPT_L2_PREFETCH = 1,
   MOE_OPT_TEST_STALL = 2,
-  MOE_OPT_UP_PAIRS = 3
+  MOE_OPT_UP_PAIRS = 3,
+  MOE_OPT_DYNAMIC_TILES = 4
 } moe_option_t;
 moe_status_t moe_ffn_set_option(int option, long long value);
 
