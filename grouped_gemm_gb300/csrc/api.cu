@@ -21,7 +21,7 @@ std::atomic<int> g_gather_mode{0};  // MOE_OPT_GATHER: 0 gather kernel, 1 in-GEM
 std::atomic<int> g_prefetch{0};     // MOE_OPT_L2_PREFETCH (measured slower on GB300: off)
 std::atomic<int> g_stall_test{0};   // MOE_OPT_TEST_STALL
 std::atomic<int> g_up_pairs{0};     // MOE_OPT_UP_PAIRS (measured slower on GB300: off)
-std::atomic<int> g_dynamic_tiles{0};  // MOE_OPT_DYNAMIC_TILES (measured: +2% decode, -3..5% prefill/large: off)
+std::atomic<int> g_dynamic_tiles{2};  // MOE_OPT_DYNAMIC_TILES: 0 off, 1 on, 2 small problems only
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -266,7 +266,7 @@ moe_status_t moe_ffn_set_option(int option, long long value) {
       g_stall_test.store((int)value);
       return MOE_OK;
     case MOE_OPT_DYNAMIC_TILES:
-      if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
+      if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
       g_dynamic_tiles.store((int)value);
       return MOE_OK;
     case MOE_OPT_UP_PAIRS:
@@ -333,11 +333,17 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
 
   const int gather = g_gather_mode.load();
   const bool in_gemm_gather = gather != 0;
+  // Narrow up tiles when the 256-wide tiles would not fill the GPU several
+  // times over (decode-sized problems): the last wave of equal tiles leaves
+  // SMs idle, and narrower tiles make the waves finer.
+  const int fold = (!in_gemm_gather && !g_up_pairs.load() && (int64_t)ws.max_rb * (H / kUpFold) < 8LL * sms)
+                       ? kUpFoldNarrow
+                       : kUpFold;  // same test as small_problem below
   CUtensorMap map_xg, map_w1, map_act, map_w2;
   const bool map_a_ok = in_gemm_gather ? make_map_bf16(&map_xg, x, (uint64_t)T, (uint64_t)D, 1)
                                        : make_map_bf16(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, kBM);
   if (!map_a_ok ||
-      !make_map_bf16(&map_w1, w1, (uint64_t)E * 2 * H, (uint64_t)D, kUpFold) ||
+      !make_map_bf16(&map_w1, w1, (uint64_t)E * 2 * H, (uint64_t)D, fold) ||
       !make_map_bf16(&map_act, ws.act, (uint64_t)ws.S_max, (uint64_t)H, kBM) ||
       !make_map_bf16(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, kDownN))
     return MOE_ERR_CUDA;
@@ -371,15 +377,17 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   ga.prefetch = g_prefetch.load();
   ga.stall_test = g_stall_test.load();
 
-  const bool dyn = g_dynamic_tiles.load() != 0;
+  const int dyn_opt = g_dynamic_tiles.load();
+  const bool small_problem = (int64_t)ws.max_rb * (H / kUpFold) < 8LL * sms;
+  const bool dyn = dyn_opt == 1 || (dyn_opt == 2 && small_problem);
   GemmArgs up = ga;
   up.tile_counter = dyn ? ws.meta + 2 : nullptr;
-  up.n_col_tiles = H / kUpFold;
+  up.n_col_tiles = H / fold;
   up.k_blocks = D / kBK;
   const int up_grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * up.n_col_tiles);
   up.x = x;
   e = (gather == 0 && g_up_pairs.load()) ? launch_up_pair_bf16(map_xg, map_w1, up, up_grid, st)
-                                         : launch_up_bf16(map_xg, map_w1, up, up_grid, st, gather);
+                                         : launch_up_bf16(map_xg, map_w1, up, up_grid, st, gather, fold);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 3);
 

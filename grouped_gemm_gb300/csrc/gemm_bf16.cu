@@ -47,8 +47,10 @@ struct GemmCfg {
   // DOWN stages half an output row (N/2 bf16) at a time in shared memory for
   // the bulk reduction; +16 B per row keeps the 32 rows of a warp on distinct
   // banks.  Half rows leave room for a 4-stage ring.
+  // UP stages its row of N/2 act values the same way and writes it with one
+  // bulk copy.
   static constexpr int kStageRowBytes = N + 16;
-  static constexpr int kStagingBytes = MODE == kModeDown ? kBM * kStageRowBytes : 0;
+  static constexpr int kStagingBytes = kBM * kStageRowBytes;
   static constexpr int kBarrierBytes = 256;
   // No alignment slack: dynamic shared memory starts 1024-byte aligned (the
   // kernel checks and reports an error otherwise).
@@ -388,7 +390,7 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
       const uint32_t tacc = lane_base + acc * N;
       if (MODE == kModeUp) {
         constexpr int G = N / 2;
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(args.act) + slot * args.H + j * G;
+        if (tok >= 0) bulk_wait_read_all();  // the previous tile's store has left the staging row
 #pragma unroll 1
         for (int c = 0; c < G / 32; ++c) {
           uint32_t g[32], u[32];
@@ -399,8 +401,14 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
             for (int i = 0; i < 16; ++i)
               pk[i] = pack_bf16x2(swiglu(u2f(g[2 * i]), u2f(u[2 * i])), swiglu(u2f(g[2 * i + 1]), u2f(u[2 * i + 1])));
 #pragma unroll
-            for (int q = 0; q < 4; ++q) st_global_v4(dst + c * 32 + q * 8, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            for (int q = 0; q < 4; ++q)
+              st_shared_v4(my_stage + c * 64 + q * 16, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
           }
+        }
+        if (tok >= 0) {  // act[slot, j*G .. +G): one 2G-byte bulk copy of the staged row
+          fence_proxy_async_smem();
+          bulk_store(static_cast<__nv_bfloat16*>(args.act) + slot * args.H + j * G, my_stage, G * 2);
+          bulk_commit();
         }
       } else {
         const float w = args.slot_w[slot];
@@ -438,7 +446,7 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
     }
-    if (MODE == kModeDown) bulk_wait_all();  // reductions complete before the CTA exits
+    bulk_wait_all();  // bulk stores / reductions complete before the CTA exits
   }
 
   // ------------------------------------------------------------ teardown
@@ -481,7 +489,10 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmAr
 }  // namespace
 
 cudaError_t launch_up_bf16(const CUtensorMap& map_a, const CUtensorMap& map_w1, const GemmArgs& args, int grid,
-                           cudaStream_t stream, int gather) {
+                           cudaStream_t stream, int gather, int fold) {
+  if (fold == kUpFoldNarrow)  // 64 gate + 64 up rows per tile, 6-stage ring
+    return launch_gemm<kModeUp, 2 * kUpFoldNarrow, kUpStagesNarrow, kGatherTile>(map_a, map_w1, args, grid, stream,
+                                                                                false);
   if (gather == kGatherTma4)
     return launch_gemm<kModeUp, 2 * kUpFold, kUpStages, kGatherTma4>(map_a, map_w1, args, grid, stream, false);
   if (gather == kGatherCpAsync)

@@ -76,8 +76,10 @@ cudaError_t launch_gather_zero(const Workspace& ws, const void* x, int D, void* 
 // gather: 0 = map_a is the pre-gathered xg [S_max, D]; 1 = map_a is x [T, D]
 // with one-row boxes and the kernel gathers with TMA gather4; 2 = the kernel's
 // cp.async warps gather rows of args.x (map_a unused).
+// fold = gate (and up) rows per tile: kUpFold (N = 256) or kUpFoldNarrow (N =
+// 128, gather 0 only); map_w1's boxes must be `fold` rows.
 cudaError_t launch_up_bf16(const CUtensorMap& map_a, const CUtensorMap& map_w1, const GemmArgs& args, int grid,
-                           cudaStream_t stream, int gather);
+                           cudaStream_t stream, int gather, int fold);
 // Up-projection with two row blocks of one expert per tile sharing each W1
 // tile (tiles = block pairs x column tiles).
 cudaError_t launch_up_pair_bf16(const CUtensorMap& map_a, const CUtensorMap& map_w1, const GemmArgs& args, int grid,
@@ -132,6 +134,8 @@ cudaError_t launch_mx_quantize(const float* in, int64_t n, uint8_t* q, uint8_t* 
 // tile shapes of the bf16 GEMMs (host and device agree on these)
 constexpr int kUpFold = 128;      // gate rows + up rows per tile: N = 2 * kUpFold
 constexpr int kUpStages = 4;
+constexpr int kUpFoldNarrow = 64;    // narrow up tiles (N = 128) for problems with few row blocks
+constexpr int kUpStagesNarrow = 6;
 constexpr int kDownN = 256;
 constexpr int kDownStages = 4;
 

@@ -166,6 +166,13 @@ __device__ __forceinline__ void bulk_reduce_add_f32(void* gdst, const void* ssrc
                "r"(smem_addr(ssrc)), "r"(bytes)
                : "memory");
 }
+// global[0 .. bytes) = smem[0 .. bytes), performed by the TMA engine, tracked
+// by this thread's bulk-async group.
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_addr(ssrc)),
+               "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // All of this thread's bulk groups have finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }

@@ -167,13 +167,14 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   sec. 5 "BPC and CPC").  Measured on GB300 it is 7-17%
  *                   slower (its accumulators fill TMEM, so the epilogue no
  *                   longer overlaps the next tile's MMAs).
- *   MOE_OPT_DYNAMIC_TILES  0 (default) or 1: with 1 the split pipeline's
+ *   MOE_OPT_DYNAMIC_TILES  0, 1 or 2 (default): with 1 the split pipeline's
  *                   bf16 GEMM kernels take their tiles from a global atomic
  *                   counter (CTAs that finish early take more work; "Porting
  *                   Block-Scaled GEMM Kernels" sec. 7 hands out work ids from
- *                   an atomic counter); 0 = static round-robin.  Measured on
- *                   GB300: 2% faster at decode, 3-5% slower at prefill and
- *                   large_skewed. */
+ *                   an atomic counter); 0 = static round-robin; 2 = dynamic
+ *                   only when the problem has fewer than about eight waves of
+ *                   up-projection tiles.  Measured on GB300: 2% faster at
+ *                   decode, 3-5% slower at prefill and large_skewed. */
 typedef enum {
   MOE_OPT_GATHER = 0,
   MOE_OPT_L2_PREFETCH = 1,
