@@ -321,7 +321,9 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
       (reinterpret_cast<uintptr_t>(topk_ids) & 3u) || (reinterpret_cast<uintptr_t>(topk_w) & 3u))
     return MOE_ERR_MISALIGNED;
   if (dtype == MOE_MXFP8 && pipeline != MOE_SPLIT) return MOE_ERR_UNSUPPORTED;
-  if (D % kDownN != 0) return MOE_ERR_UNSUPPORTED;
+  // fused and MXFP8 kernels write 256-column output tiles; the bf16 split
+  // pipeline falls back to 128-column tiles
+  if (D % kDownN != 0 && (dtype != MOE_BF16 || pipeline != MOE_SPLIT)) return MOE_ERR_UNSUPPORTED;
   Workspace ws = plan_workspace(workspace, T, E, D, H, k, pipeline, dtype);
   if (workspace_bytes < ws.bytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
   const int sms = num_sms();
@@ -336,6 +338,7 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   // Narrow up tiles when the 256-wide tiles would not fill the GPU several
   // times over (decode-sized problems): the last wave of equal tiles leaves
   // SMs idle, and narrower tiles make the waves finer.
+  const int down_n = D % kDownN == 0 ? kDownN : kDownNNarrow;
   const int fold = (!in_gemm_gather && !g_up_pairs.load() && (int64_t)ws.max_rb * (H / kUpFold) < 8LL * sms)
                        ? kUpFoldNarrow
                        : kUpFold;  // same test as small_problem below
@@ -345,7 +348,7 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   if (!map_a_ok ||
       !make_map_bf16(&map_w1, w1, (uint64_t)E * 2 * H, (uint64_t)D, fold) ||
       !make_map_bf16(&map_act, ws.act, (uint64_t)ws.S_max, (uint64_t)H, kBM) ||
-      !make_map_bf16(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, kDownN))
+      !make_map_bf16(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, down_n))
     return MOE_ERR_CUDA;
 
   prof_mark(st, 0);
@@ -393,10 +396,10 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
 
   GemmArgs dn = ga;
   dn.tile_counter = dyn ? ws.meta + 3 : nullptr;
-  dn.n_col_tiles = D / kDownN;
+  dn.n_col_tiles = D / down_n;
   dn.k_blocks = H / kBK;
   const int dn_grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * dn.n_col_tiles);
-  e = launch_down_bf16(map_act, map_w2, dn, dn_grid, st, !g_prof.on);
+  e = launch_down_bf16(map_act, map_w2, dn, dn_grid, st, !g_prof.on, down_n);
   prof_mark(st, 4);
   return cuda_status(e);
 }

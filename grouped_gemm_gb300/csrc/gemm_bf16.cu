@@ -501,7 +501,10 @@ cudaError_t launch_up_bf16(const CUtensorMap& map_a, const CUtensorMap& map_w1, 
 }
 
 cudaError_t launch_down_bf16(const CUtensorMap& map_act, const CUtensorMap& map_w2, const GemmArgs& args, int grid,
-                             cudaStream_t stream, bool pdl) {
+                             cudaStream_t stream, bool pdl, int n) {
+  if (n == kDownNNarrow)  // D % 256 != 0: 128-column output tiles
+    return launch_gemm<kModeDown, kDownNNarrow, kDownStagesNarrow, kGatherTile>(map_act, map_w2, args, grid, stream,
+                                                                              pdl);
   return launch_gemm<kModeDown, kDownN, kDownStages, kGatherTile>(map_act, map_w2, args, grid, stream, pdl);
 }
 

@@ -84,8 +84,10 @@ cudaError_t launch_up_bf16(const CUtensorMap& map_a, const CUtensorMap& map_w1, 
 // tile (tiles = block pairs x column tiles).
 cudaError_t launch_up_pair_bf16(const CUtensorMap& map_a, const CUtensorMap& map_w1, const GemmArgs& args, int grid,
                                 cudaStream_t stream);
+// n = output columns per tile: kDownN, or kDownNNarrow when D % 256 != 0;
+// map_w2's boxes must be n rows.
 cudaError_t launch_down_bf16(const CUtensorMap& map_act, const CUtensorMap& map_w2, const GemmArgs& args, int grid,
-                             cudaStream_t stream, bool pdl);
+                             cudaStream_t stream, bool pdl, int n);
 
 struct FusedArgs {
   const int* meta;
@@ -138,5 +140,7 @@ constexpr int kUpFoldNarrow = 64;    // narrow up tiles (N = 128) for problems w
 constexpr int kUpStagesNarrow = 6;
 constexpr int kDownN = 256;
 constexpr int kDownStages = 4;
+constexpr int kDownNNarrow = 128;
+constexpr int kDownStagesNarrow = 6;
 
 }  // namespace moe

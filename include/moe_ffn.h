@@ -19,7 +19,8 @@
  *     topk_w    [T, k]        float32
  *     out       [T, D]        bf16, OVERWRITTEN (the library zero-fills it)
  * Requirements: T >= 0 (T == 0 is a no-op), 1 <= k, 1 <= E <= 1024,
- * D % 128 == 0, H % 128 == 0, every pointer 16-byte aligned.
+ * D % 128 == 0, H % 128 == 0, every pointer 16-byte aligned; the fused
+ * pipeline and MXFP8 also need D % 256 == 0 (else MOE_ERR_UNSUPPORTED).
  *
  * Ownership: the caller owns every buffer, including the workspace; the
  * library allocates no device memory.  Calls are asynchronous on `stream` (a

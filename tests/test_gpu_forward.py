@@ -50,8 +50,12 @@ def oracle_out(inp, tokens=None):
     (200, 256, 384, 3, 1, "uniform"),         # top-1, H not a multiple of 256
     (129, 768, 256, 40, 8, "zipf"),           # several experts empty
     (512, 2048, 768, 128, 8, "topk_logits"),  # prefill dims, 512 tokens
+    (96, 384, 128, 6, 3, "uniform"),          # D % 256 != 0 (split only: 128-column down tiles)
+    (200, 256, 128, 1024, 4, "uniform"),      # the largest expert count
 ])
 def test_forward_small(T, D, H, E, k, routing, pipeline):
+    if D % 256 and MODES[pipeline][0] != moe.MOE_SPLIT:
+        pytest.skip("fused pipeline needs D % 256 == 0")
     inp = wl.make_custom(T, D, H, E, k, seed=T + D, routing=routing)
     out, _ = run_mode(inp, to_dev(inp), pipeline)
     r = assert_close(out, oracle_out(inp), label=f"T={T} D={D} H={H} E={E} k={k}")
@@ -85,6 +89,16 @@ def test_forward_repeat_calls_and_reused_workspace(pipeline):
     assert_close(out2, ref, label="second (out overwritten, not accumulated)")
 
 
+def test_zero_tokens_is_a_noop():
+    inp = wl.make_custom(4, 256, 128, 4, 2, seed=2)
+    dev = to_dev(inp)
+    out = torch.zeros(1, 256, dtype=torch.bfloat16, device="cuda")
+    ws = moe.alloc_workspace(4, 4, 256, 128, 2)
+    assert moe.moe_ffn_forward(dev["x"], dev["w1"], dev["w2"], dev["topk_ids"], dev["topk_w"], out, E=4, D=256, H=128,
+                               k=2, workspace=ws, T=0) == 0
+    assert moe.moe_ffn_sync_status(ws) == 0
+
+
 def test_unsupported_combinations_rejected():
     # MXFP8 is built for the split pipeline only
     inp = wl.make_custom(8, 256, 128, 4, 2, seed=1)
@@ -93,9 +107,11 @@ def test_unsupported_combinations_rejected():
         run_forward(inp, dev, pipeline=moe.MOE_SPLIT, dtype=moe.MOE_MXFP8, check_status=False)
 
 
-@pytest.mark.parametrize("name,n_sample", [("decode", None), ("prefill", 96)])
+@pytest.mark.parametrize("name,n_sample", [("decode", None), ("prefill", 96), ("large_skewed", 40)])
 @pytest.mark.parametrize("pipeline", PIPELINES)
 def test_forward_full_workload_sampled(name, n_sample, pipeline):
+    if name == "large_skewed" and pipeline not in ("split", "fused"):
+        pytest.skip("option variants are covered at the smaller sizes")
     inp = wl.make_inputs(name, seed=0)
     out, _ = run_mode(inp, to_dev(inp), pipeline)
     T = inp["workload"].T
