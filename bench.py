@@ -190,8 +190,6 @@ def run_ours(args, rank, world, local_rank):
     w = inp["workload"]
     mx = w.dtype == "mxfp8"
     dtype = moe.MOE_MXFP8 if mx else moe.MOE_BF16
-    if mx and args.pipeline != "split":
-        raise SystemExit("the MXFP8 path is built for the split pipeline")
     dev = {k: torch.from_numpy(inp[k] if mx else inp[k].view(np.int16)).cuda() for k in ("x", "w1", "w2")}
     if mx:  # weight scales are repacked once, like the weights themselves
         dev["x_sf"] = torch.from_numpy(inp["x_sf"]).cuda()

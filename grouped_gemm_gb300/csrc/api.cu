@@ -129,8 +129,12 @@ Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipe
   } else if (dtype == MOE_MXFP8) {
     w.xg = take((size_t)w.S_max * D);
     w.xg_sf = take((size_t)w.S_max * D / 32);
-    w.act = take((size_t)w.S_max * H);
-    w.act_sf = take((size_t)w.S_max * H / 32);
+    if (pipeline == MOE_SPLIT) {
+      w.act = take((size_t)w.S_max * H);
+      w.act_sf = take((size_t)w.S_max * H / 32);
+    } else {
+      w.acc_f32 = take((size_t)T * D * 4);
+    }
   } else if (pipeline == MOE_SPLIT) {
     w.xg = take((size_t)w.S_max * D * 2);
     w.act = take((size_t)w.S_max * H * 2);
@@ -234,6 +238,48 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
   return cuda_status(e);
 }
 
+// MXFP8 fused pipeline: routing, gather of e4m3 rows and scales (+ zero of the
+// fp32 accumulator), one block-scaled GEMM kernel that keeps the requantized
+// act on chip, rounding of the accumulator to bf16.
+moe_status_t forward_fused_mxfp8(const Workspace& ws, const void* x, const void* x_sf, const void* w1,
+                                 const void* w1_sf, const void* w2, const void* w2_sf, const int32_t* topk_ids,
+                                 const float* topk_w, void* out, int T, int E, int D, int H, int k, int sms,
+                                 cudaStream_t st) {
+  CUtensorMap map_xg, map_w1, map_w2;
+  if (!make_map_fp8(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, kBM) ||
+      !make_map_fp8(&map_w1, w1, (uint64_t)E * 2 * H, (uint64_t)D, 128) ||
+      !make_map_fp8(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, 256))
+    return MOE_ERR_CUDA;
+  prof_mark(st, 0);
+  cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  prof_mark(st, 1);
+  e = launch_gather_mx(ws, x, x_sf, D, ws.acc_f32, (int64_t)T * D * 4, sms * 4, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  prof_mark(st, 2);
+  FusedMxArgs fa{};
+  fa.meta = ws.meta;
+  fa.expert_of_rb = ws.expert_of_rb;
+  fa.row_tok = ws.row_tok;
+  fa.slot_w = ws.slot_w;
+  fa.out_f32 = ws.acc_f32;
+  fa.xg_sf = ws.xg_sf;
+  fa.w1_sf = w1_sf;
+  fa.w2_sf = w2_sf;
+  fa.err = ws.err;
+  fa.wait_limit_ns = g_wait_limit_ns.load();
+  fa.D = D;
+  fa.H = H;
+  fa.stall_test = g_stall_test.load();
+  const int grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * (H / 128));
+  e = launch_fused_mxfp8(map_xg, map_w1, map_w2, fa, grid, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  prof_mark(st, 3);
+  e = launch_f32_to_bf16(ws.acc_f32, out, (int64_t)T * D, sms * 4, st);
+  prof_mark(st, 4);
+  return cuda_status(e);
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -320,7 +366,6 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   if (!aligned16(x) || !aligned16(w1) || !aligned16(w2) || !aligned16(out) || !aligned16(workspace) ||
       (reinterpret_cast<uintptr_t>(topk_ids) & 3u) || (reinterpret_cast<uintptr_t>(topk_w) & 3u))
     return MOE_ERR_MISALIGNED;
-  if (dtype == MOE_MXFP8 && pipeline != MOE_SPLIT) return MOE_ERR_UNSUPPORTED;
   // fused and MXFP8 kernels write 256-column output tiles; the bf16 split
   // pipeline falls back to 128-column tiles
   if (D % kDownN != 0 && (dtype != MOE_BF16 || pipeline != MOE_SPLIT)) return MOE_ERR_UNSUPPORTED;
@@ -329,6 +374,8 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   const int sms = num_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == MOE_MXFP8 && pipeline == MOE_FUSED)
+    return forward_fused_mxfp8(ws, x, x_sf, w1, w1_sf, w2, w2_sf, topk_ids, topk_w, out, T, E, D, H, k, sms, st);
   if (dtype == MOE_MXFP8)
     return forward_split_mxfp8(ws, x, x_sf, w1, w1_sf, w2, w2_sf, topk_ids, topk_w, out, T, E, D, H, k, sms, st);
   if (pipeline == MOE_FUSED) return forward_fused_bf16(ws, x, w1, w2, topk_ids, topk_w, out, T, E, D, H, k, sms, st);

@@ -133,6 +133,23 @@ cudaError_t launch_gather_mx(const Workspace& ws, const void* x, const void* x_s
 cudaError_t launch_pack_sf(const void* sf, void* packed, int64_t rows, int K, int grid, cudaStream_t stream);
 cudaError_t launch_mx_quantize(const float* in, int64_t n, uint8_t* q, uint8_t* sf, cudaStream_t stream);
 
+struct FusedMxArgs {
+  const int* meta;
+  const int* expert_of_rb;
+  const int* row_tok;
+  const float* slot_w;
+  void* out_f32;            // fp32 [T, D], zeroed before the launch
+  const void* xg_sf;        // blocked scale tiles of xg
+  const void* w1_sf;        // packed W1 scales
+  const void* w2_sf;        // packed W2 scales
+  int* err;
+  unsigned long long wait_limit_ns;
+  int D, H;
+  int stall_test;
+};
+cudaError_t launch_fused_mxfp8(const CUtensorMap& map_xg, const CUtensorMap& map_w1, const CUtensorMap& map_w2,
+                               const FusedMxArgs& args, int grid, cudaStream_t stream);
+
 // tile shapes of the bf16 GEMMs (host and device agree on these)
 constexpr int kUpFold = 128;      // gate rows + up rows per tile: N = 2 * kUpFold
 constexpr int kUpStages = 4;

@@ -71,7 +71,7 @@ moe_status_t moe_ffn_workspace_init(void* workspace, size_t workspace_bytes, voi
 /* The forward pass described above.  x_sf, w1_sf, w2_sf are the MXFP8 scale
  * arrays and must be NULL for MOE_BF16.
  *
- * MOE_MXFP8 ("Prime Flash MoE" sec. 7; MOE_SPLIT only): x, w1, w2 hold OCP
+ * MOE_MXFP8 ("Prime Flash MoE" sec. 7; both pipelines): x, w1, w2 hold OCP
  * e4m3 codes (one byte per element, same shapes as above); every 32
  * consecutive elements along the contiguous (reduction) dimension share one
  * ue8m0 scale byte s (value 2^(s-127)).  x_sf is row-major [T, D/32] (4-byte

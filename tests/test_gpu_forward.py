@@ -100,11 +100,13 @@ def test_zero_tokens_is_a_noop():
 
 
 def test_unsupported_combinations_rejected():
-    # MXFP8 is built for the split pipeline only
     inp = wl.make_custom(8, 256, 128, 4, 2, seed=1)
     dev = to_dev(inp)
-    with pytest.raises(moe.MoeFFNError):
+    with pytest.raises(moe.MoeFFNError):  # MXFP8 without scale arrays
         run_forward(inp, dev, pipeline=moe.MOE_SPLIT, dtype=moe.MOE_MXFP8, check_status=False)
+    inp = wl.make_custom(8, 384, 128, 4, 2, seed=1)
+    with pytest.raises(moe.MoeFFNError):  # fused needs D % 256 == 0
+        run_forward(inp, to_dev(inp), pipeline=moe.MOE_FUSED, check_status=False)
 
 
 @pytest.mark.parametrize("name,n_sample", [("decode", None), ("prefill", 96), ("large_skewed", 40)])

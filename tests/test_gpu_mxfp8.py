@@ -77,7 +77,7 @@ def test_weight_scale_repacking_layout():
     assert np.array_equal(p2.cpu().numpy(), expected(w2_sf))
 
 
-def run_mx(inp):
+def run_mx(inp, pipeline=moe.MOE_SPLIT):
     w = inp["workload"]
     dev = {k: torch.from_numpy(inp[k]).cuda() for k in ("x", "x_sf", "w1", "w2")}
     w1p = torch.empty(inp["w1_sf"].size, dtype=torch.uint8, device="cuda")
@@ -87,9 +87,9 @@ def run_mx(inp):
     ids = torch.from_numpy(inp["topk_ids"]).cuda()
     tw = torch.from_numpy(inp["topk_w"]).cuda()
     out = torch.full((w.T, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
-    ws = moe.alloc_workspace(w.T, w.E, w.D, w.H, w.k, moe.MOE_MXFP8, moe.MOE_SPLIT)
+    ws = moe.alloc_workspace(w.T, w.E, w.D, w.H, w.k, moe.MOE_MXFP8, pipeline)
     moe.moe_ffn_forward(dev["x"], dev["w1"], dev["w2"], ids, tw, out, E=w.E, D=w.D, H=w.H, k=w.k, workspace=ws,
-                        dtype=moe.MOE_MXFP8, pipeline=moe.MOE_SPLIT, x_sf=dev["x_sf"], w1_sf=w1p, w2_sf=w2p)
+                        dtype=moe.MOE_MXFP8, pipeline=pipeline, x_sf=dev["x_sf"], w1_sf=w1p, w2_sf=w2p)
     st = moe.moe_ffn_sync_status(ws)
     assert st == 0, moe.moe_ffn_status_string(st)
     return out
@@ -100,6 +100,10 @@ def oracle_mx(inp, tokens=None):
                           x_sf=inp["x_sf"], w1_sf=inp["w1_sf"], w2_sf=inp["w2_sf"], tokens=tokens)
 
 
+PIPES = {"split": moe.MOE_SPLIT, "fused": moe.MOE_FUSED}
+
+
+@pytest.mark.parametrize("pipe", list(PIPES))
 @pytest.mark.parametrize("T,D,H,E,k,routing", [
     (64, 256, 128, 8, 2, "topk_logits"),
     (300, 512, 256, 16, 4, "uniform"),
@@ -107,16 +111,17 @@ def oracle_mx(inp, tokens=None):
     (129, 768, 256, 40, 8, "zipf"),
     (512, 1024, 512, 16, 8, "uniform"),
 ])
-def test_mxfp8_forward_small(T, D, H, E, k, routing):
+def test_mxfp8_forward_small(T, D, H, E, k, routing, pipe):
     inp = wl.make_custom(T, D, H, E, k, seed=T + H, routing=routing, dtype="mxfp8")
-    out = run_mx(inp)
-    r = assert_close(out, oracle_mx(inp), dtype="mxfp8", label=f"mxfp8 T={T} D={D} H={H}")
-    print(f"mxfp8 T={T} D={D} H={H} E={E} k={k}: max_rel={r[0]:.2e} mean_rel={r[1]:.2e} cos={r[2]:.6f}")
+    out = run_mx(inp, PIPES[pipe])
+    r = assert_close(out, oracle_mx(inp), dtype="mxfp8", label=f"mxfp8 {pipe} T={T} D={D} H={H}")
+    print(f"mxfp8 {pipe} T={T} D={D} H={H} E={E} k={k}: max_rel={r[0]:.2e} mean_rel={r[1]:.2e} cos={r[2]:.6f}")
 
 
-def test_mxfp8_full_workload_sampled():
+@pytest.mark.parametrize("pipe", list(PIPES))
+def test_mxfp8_full_workload_sampled(pipe):
     inp = wl.make_inputs("mxfp8", seed=0)
-    out = run_mx(inp)
+    out = run_mx(inp, PIPES[pipe])
     tokens = np.sort(np.random.default_rng(2).choice(inp["workload"].T, 48, replace=False)).astype(np.int32)
     r = assert_close(out[torch.from_numpy(tokens.astype(np.int64)).cuda()], oracle_mx(inp, tokens), dtype="mxfp8",
                      label="mxfp8 workload")
