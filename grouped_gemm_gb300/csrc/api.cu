@@ -22,6 +22,7 @@ std::atomic<int> g_prefetch{0};     // MOE_OPT_L2_PREFETCH (measured slower on G
 std::atomic<int> g_stall_test{0};   // MOE_OPT_TEST_STALL
 std::atomic<int> g_up_pairs{0};     // MOE_OPT_UP_PAIRS (measured slower on GB300: off)
 std::atomic<int> g_dynamic_tiles{2};  // MOE_OPT_DYNAMIC_TILES: 0 off, 1 on, 2 small problems only
+std::atomic<int> g_tile_cols{0};      // MOE_OPT_TILE_COLS: 0 auto, 128 or 256 (bf16 split GEMM tile width)
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -311,6 +312,10 @@ moe_status_t moe_ffn_set_option(int option, long long value) {
       if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
       g_stall_test.store((int)value);
       return MOE_OK;
+    case MOE_OPT_TILE_COLS:
+      if (value != 0 && value != 128 && value != 256) return MOE_ERR_INVALID_ARG;
+      g_tile_cols.store((int)value);
+      return MOE_OK;
     case MOE_OPT_DYNAMIC_TILES:
       if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
       g_dynamic_tiles.store((int)value);
@@ -385,10 +390,12 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   // Narrow up tiles when the 256-wide tiles would not fill the GPU several
   // times over (decode-sized problems): the last wave of equal tiles leaves
   // SMs idle, and narrower tiles make the waves finer.
-  const int down_n = D % kDownN == 0 ? kDownN : kDownNNarrow;
-  const int fold = (!in_gemm_gather && !g_up_pairs.load() && (int64_t)ws.max_rb * (H / kUpFold) < 8LL * sms)
+  const int cols = g_tile_cols.load();
+  const int down_n = (D % kDownN != 0 || cols == 128) ? kDownNNarrow : kDownN;
+  const bool narrow_ok = !in_gemm_gather && !g_up_pairs.load();
+  const int fold = (narrow_ok && (cols == 128 || (cols == 0 && (int64_t)ws.max_rb * (H / kUpFold) < 8LL * sms)))
                        ? kUpFoldNarrow
-                       : kUpFold;  // same test as small_problem below
+                       : kUpFold;  // auto: narrow when the wide tiles make fewer than ~8 waves
   CUtensorMap map_xg, map_w1, map_act, map_w2;
   const bool map_a_ok = in_gemm_gather ? make_map_bf16(&map_xg, x, (uint64_t)T, (uint64_t)D, 1)
                                        : make_map_bf16(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, kBM);

@@ -175,13 +175,20 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   an atomic counter); 0 = static round-robin; 2 = dynamic
  *                   only when the problem has fewer than about eight waves of
  *                   up-projection tiles.  Measured on GB300: 2% faster at
- *                   decode, 3-5% slower at prefill and large_skewed. */
+ *                   decode, 3-5% slower at prefill and large_skewed.
+ *   MOE_OPT_TILE_COLS  0 (default: automatic), 128 or 256: output columns per
+ *                   tile of the bf16 split GEMMs (up: 64+64 or 128+128 gate/up
+ *                   rows; down: 128 or 256 columns of D).  Automatic picks
+ *                   128-wide up tiles when the 256-wide ones would fill the
+ *                   GPU fewer than about eight times, and 256-wide down tiles
+ *                   whenever D % 256 == 0. */
 typedef enum {
   MOE_OPT_GATHER = 0,
   MOE_OPT_L2_PREFETCH = 1,
   MOE_OPT_TEST_STALL = 2,
   MOE_OPT_UP_PAIRS = 3,
-  MOE_OPT_DYNAMIC_TILES = 4
+  MOE_OPT_DYNAMIC_TILES = 4,
+  MOE_OPT_TILE_COLS = 5
 } moe_option_t;
 moe_status_t moe_ffn_set_option(int option, long long value);
 
