@@ -23,6 +23,7 @@ std::atomic<int> g_stall_test{0};   // MOE_OPT_TEST_STALL
 std::atomic<int> g_up_pairs{0};     // MOE_OPT_UP_PAIRS (measured slower on GB300: off)
 std::atomic<int> g_dynamic_tiles{2};  // MOE_OPT_DYNAMIC_TILES: 0 off, 1 on, 2 small problems only
 std::atomic<int> g_tile_cols{0};      // MOE_OPT_TILE_COLS: 0 auto, 128 or 256 (bf16 split GEMM tile width)
+std::atomic<int> g_swap_ab{0};        // MOE_OPT_SWAP_AB: swap-AB tail tiles (measured slower on GB300: off)
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -160,10 +161,10 @@ moe_status_t forward_fused_bf16(const Workspace& ws, const void* x, const void* 
       !make_map_bf16(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, kDownN))
     return MOE_ERR_CUDA;
   prof_mark(st, 0);
-  cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st);
+  cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st, nullptr, 0, 0, !g_prof.on);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 1);
-  e = launch_gather_zero(ws, x, D, ws.acc_f32, (int64_t)T * D * 4, sms * 4, st);
+  e = launch_gather_zero(ws, x, topk_ids, T, E, k, D, ws.acc_f32, (int64_t)T * D * 4, sms * 4, st, !g_prof.on);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 2);
   FusedArgs fa{};
@@ -201,7 +202,7 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
       !make_map_fp8(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, 256))
     return MOE_ERR_CUDA;
   prof_mark(st, 0);
-  cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st);
+  cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st, nullptr, 0, 0, !g_prof.on);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 1);
   e = launch_gather_mx(ws, x, x_sf, D, out, (int64_t)T * D * 2, sms * 4, st);
@@ -252,7 +253,7 @@ moe_status_t forward_fused_mxfp8(const Workspace& ws, const void* x, const void*
       !make_map_fp8(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, 256))
     return MOE_ERR_CUDA;
   prof_mark(st, 0);
-  cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st);
+  cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st, nullptr, 0, 0, !g_prof.on);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 1);
   e = launch_gather_mx(ws, x, x_sf, D, ws.acc_f32, (int64_t)T * D * 4, sms * 4, st);
@@ -311,6 +312,10 @@ moe_status_t moe_ffn_set_option(int option, long long value) {
     case MOE_OPT_TEST_STALL:
       if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
       g_stall_test.store((int)value);
+      return MOE_OK;
+    case MOE_OPT_SWAP_AB:
+      if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
+      g_swap_ab.store((int)value);
       return MOE_OK;
     case MOE_OPT_TILE_COLS:
       if (value != 0 && value != 128 && value != 256) return MOE_ERR_INVALID_ARG;
@@ -409,12 +414,12 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   // With the in-GEMM gather the routing launch also zero-fills out;
   // otherwise the gather kernel does.
   cudaError_t e = in_gemm_gather
-                      ? launch_route(ws, topk_ids, topk_w, T, E, k, st, out, (int64_t)T * D * 2, sms * 2)
-                      : launch_route(ws, topk_ids, topk_w, T, E, k, st);
+                      ? launch_route(ws, topk_ids, topk_w, T, E, k, st, out, (int64_t)T * D * 2, sms * 2, !g_prof.on)
+                      : launch_route(ws, topk_ids, topk_w, T, E, k, st, nullptr, 0, 0, !g_prof.on);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 1);
   if (!in_gemm_gather) {
-    e = launch_gather_zero(ws, x, D, out, (int64_t)T * D * 2, sms * 4, st);
+    e = launch_gather_zero(ws, x, topk_ids, T, E, k, D, out, (int64_t)T * D * 2, sms * 4, st, !g_prof.on);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   prof_mark(st, 2);
@@ -433,6 +438,9 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   ga.H = H;
   ga.prefetch = g_prefetch.load();
   ga.stall_test = g_stall_test.load();
+  ga.counts = ws.counts;
+  ga.pad_offsets = ws.pad_offsets;
+  ga.swap_ab = g_swap_ab.load();
 
   const int dyn_opt = g_dynamic_tiles.load();
   const bool small_problem = (int64_t)ws.max_rb * (H / kUpFold) < 8LL * sms;
@@ -444,7 +452,7 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   const int up_grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * up.n_col_tiles);
   up.x = x;
   e = (gather == 0 && g_up_pairs.load()) ? launch_up_pair_bf16(map_xg, map_w1, up, up_grid, st)
-                                         : launch_up_bf16(map_xg, map_w1, up, up_grid, st, gather, fold);
+                                         : launch_up_bf16(map_xg, map_w1, up, up_grid, st, gather, fold, !g_prof.on);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 3);
 

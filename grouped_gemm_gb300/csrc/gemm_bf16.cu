@@ -58,7 +58,7 @@ struct GemmCfg {
   static_assert(N % 32 == 0 && N >= 32 && N <= 256, "MMA N");
   static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns: power of two <= 512");
   static_assert(kSmemBytes <= 232448, "shared memory");
-  static_assert((2 * STAGES + 6 + 2 * kTileSlots) * 8 + 8 + 4 * kTileSlots <= kBarrierBytes, "barrier area");
+  static_assert((2 * STAGES + 7 + 2 * kTileSlots) * 8 + 8 + 8 * kTileSlots <= kBarrierBytes, "barrier area");
 };
 
 constexpr int kThreads = 192;
@@ -68,6 +68,22 @@ enum { kGatherTile = 0, kGatherTma4 = 1, kGatherCpAsync = 2 };
 template <int GATHER>
 constexpr int threads_for() { return GATHER == kGatherCpAsync ? kThreads + kGatherThreads : kThreads; }
 constexpr uint64_t kDrainNs = 200ull * 1000 * 1000;  // 200 ms
+
+// Swap-AB tail tiles.  The last row block of an expert holds v < 128 routed
+// rows; with M fixed at 128 rows a normal tile spends (128 - v) / 128 of its
+// MMA work on padding.  With the operands swapped the weight tile is the
+// M = 128 side and the routed rows are N = ns = v rounded up to 16: two MMAs
+// (weight rows 0..127 and 128..255 of the stage) accumulate transposed
+// results into TMEM columns [0, ns) and [128, 128 + ns), for 256 * ns instead
+// of 128 * 256 multiply-adds per K step ("Prime Flash MoE" and Pearl
+// "Optimizing Grouped GEMM for MoE on Blackwell": swap-AB for small
+// per-expert M).  Only the 256-row B stages (N = 256) have two 128-row halves.
+constexpr int kSwapMaxN = 112;
+
+// Rows of row block rb (of expert e) that hold routed pairs; the rest is padding.
+__device__ __forceinline__ int rb_rows(const GemmArgs& a, int rb, int e) {
+  return min(kBM, a.counts[e] - (rb * kBM - a.pad_offsets[e]));
+}
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 
@@ -95,10 +111,12 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint64_t* never = drain + 1;  // no thread ever arrives here (failure-path test hook)
-  uint64_t* tile_full = never + 1;
+  uint64_t* epi_bar = never + 1;  // the epilogue warps' barrier around the swap-AB staging tile
+  uint64_t* tile_full = epi_bar + 1;
   uint64_t* tile_empty = tile_full + kTileSlots;
   volatile int* tile_ring = reinterpret_cast<volatile int*>(tile_empty + kTileSlots);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(tile_ring) + kTileSlots);
+  volatile int* tile_ns = tile_ring + kTileSlots;  // swap-AB width of each published tile, 0 = normal
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(const_cast<int*>(tile_ns) + kTileSlots);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -122,6 +140,7 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
     }
     mbar_init(drain, 1);
     mbar_init(never, 1);
+    mbar_init(epi_bar, kEpiThreads);
     for (int i = 0; i < kTileSlots; ++i) {
       mbar_init(&tile_full[i], 1);
       mbar_init(&tile_empty[i], kTileReaders);
@@ -139,18 +158,25 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  if (MODE == kModeUp && threadIdx.x == 0) griddep_launch_dependents();
+  // Launched as a programmatic dependent, the prologue above overlaps the
+  // previous grid; everything below reads its outputs (xg or act, and the
+  // routing tables, complete before that grid began).
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
 
   const int num_rb = args.meta[0];
   const int n_tiles = num_rb * args.n_col_tiles;
   const int KB = args.k_blocks;
 
-  // consumer side of the tile ring: the next tile index, or -1 if aborting
+  // consumer side of the tile ring: the next tile index, or -1 if aborting;
+  // t_ns gets the tile's swap-AB width (0 = normal tile)
   int t_slot = 0;
   uint32_t t_phase = 0;
+  int t_ns = 0;
   auto take_tile = [&](int site) -> int {
     if (!mbar_wait(&tile_full[t_slot], t_phase, wc, site)) return -1;
     const int t = tile_ring[t_slot];
+    t_ns = tile_ns[t_slot];
     mbar_arrive(&tile_empty[t_slot]);
     if (++t_slot == kTileSlots) {
       t_slot = 0;
@@ -161,8 +187,6 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (MODE == kModeDown && lane == 0) griddep_wait();  // act is written by the previous grid
-    __syncwarp();
     int s = 0;
     uint32_t ph = 0;
     int issued_phase[STAGES];
@@ -203,7 +227,14 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
         } else {
           next = args.tile_counter ? atomicAdd(args.tile_counter, 1)
                                    : (tile < 0 ? (int)blockIdx.x : tile + (int)gridDim.x);
+          int ns = 0;
+          if (N == 256 && args.swap_ab && next < n_tiles) {
+            const int nrb = next / args.n_col_tiles;
+            const int v = rb_rows(args, nrb, args.expert_of_rb[nrb]);
+            if (v < kBM && ((v + 15) & ~15) <= kSwapMaxN) ns = (v + 15) & ~15;
+          }
           tile_ring[t_slot] = next;
+          tile_ns[t_slot] = ns;
           mbar_arrive(&tile_full[t_slot]);
         }
       }
@@ -290,6 +321,8 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
       }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * N;
+      const int ns = t_ns;
+      const uint32_t idesc_swap = idesc_bf16_f32(kBM, ns > 0 ? ns : 16);
       for (int kb = 0; kb < KB; ++kb) {
         if (!mbar_wait(&full[s], ph, wc, 3)) {
           ok = false;
@@ -298,10 +331,20 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
         tc_fence_after();
         const uint64_t adesc = sdesc_sw128(smem_addr(sA + s * Cfg::kABytes));
         const uint64_t bdesc = sdesc_sw128(smem_addr(sB + s * Cfg::kBBytes));
+        if (N == 256 && ns > 0) {
+          // swap-AB: weight rows are M, the tile's routed rows are N
+          const uint64_t bdesc_hi = sdesc_sw128(smem_addr(sB + s * Cfg::kBBytes + kBM * kBK * 2));
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          // +32 bytes per K step of 16 bf16 = +2 in the descriptor's address field
-          umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            umma_bf16(d_tmem, bdesc + 2 * kk, adesc + 2 * kk, idesc_swap, (kb | kk) != 0);
+            umma_bf16(d_tmem + kBM, bdesc_hi + 2 * kk, adesc + 2 * kk, idesc_swap, (kb | kk) != 0);
+          }
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // +32 bytes per K step of 16 bf16 = +2 in the descriptor's address field
+            umma_bf16(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+          }
         }
         umma_commit(&empty[s]);  // frees the smem stage once these MMAs are done
         if (++s == STAGES) {
@@ -376,6 +419,14 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
     const int row = quad * 32 + lane;
     const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
     uint8_t* my_stage = sStage + row * Cfg::kStageRowBytes;
+    // barrier of the 128 epilogue threads (bounded, unlike bar.sync)
+    uint32_t epi_ph = 0;
+    auto epi_sync = [&](int site) -> bool {
+      mbar_arrive(epi_bar);
+      const bool got = mbar_wait(epi_bar, epi_ph, wc, site);
+      epi_ph ^= 1u;
+      return got;
+    };
     int it = 0;
     for (;; ++it) {
       const int tile = take_tile(9);
@@ -388,7 +439,70 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
       const int64_t slot = (int64_t)rb * kBM + row;
       const int tok = args.row_tok[slot];
       const uint32_t tacc = lane_base + acc * N;
-      if (MODE == kModeUp) {
+      const int ns = t_ns;
+      if (N == 256 && ns > 0) {
+        // Swap-AB tile: this thread's TMEM lane is weight row `row` of each
+        // 128-row half and the columns are the tile's rows c < ns.  The values
+        // go transposed into the staging tile (staging row c = tile row c),
+        // then thread c moves staging row c with one bulk operation, as in a
+        // normal tile.  Staging rows of padding slots are written, not moved.
+        bool failed = false;
+        if (MODE == kModeUp) {
+          constexpr int G = N / 2;
+          bulk_wait_read_all();  // this thread's last store has left the staging tile
+          if (!epi_sync(12)) break;
+#pragma unroll 1
+          for (int c0 = 0; c0 < ns; c0 += 32) {
+            uint32_t g[32], u[32];
+            tmem_ld_x32_pair(tacc + c0, tacc + kBM + c0, g, u);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              st_shared_b16(sStage + (c0 + i) * Cfg::kStageRowBytes + row * 2, swiglu(u2f(g[i]), u2f(u[i])));
+          }
+          fence_proxy_async_smem();
+          if (!epi_sync(13)) break;
+          if (tok >= 0) {
+            bulk_store(static_cast<__nv_bfloat16*>(args.act) + slot * args.H + j * G, my_stage, G * 2);
+            bulk_commit();
+          }
+        } else {
+          const float* wrow = args.slot_w + (int64_t)rb * kBM;
+          __nv_bfloat16* orow =
+              static_cast<__nv_bfloat16*>(args.out) + (int64_t)(tok < 0 ? 0 : tok) * args.D + j * N;
+#pragma unroll 1
+          for (int hh = 0; hh < 2; ++hh) {  // D columns j*N + hh*128 .. +128
+            bulk_wait_read_all();
+            if (!epi_sync(12)) {
+              failed = true;
+              break;
+            }
+#pragma unroll 1
+            for (int c0 = 0; c0 < ns; c0 += 64) {
+              uint32_t a0[32], a1[32];
+              tmem_ld_x32_pair(tacc + hh * kBM + c0, tacc + hh * kBM + c0 + 32, a0, a1);
+              const float w0 = wrow[c0 + lane], w1 = wrow[c0 + 32 + lane];
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                st_shared_b16(sStage + (c0 + i) * Cfg::kStageRowBytes + row * 2,
+                              __shfl_sync(0xffffffffu, w0, i) * u2f(a0[i]));
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                st_shared_b16(sStage + (c0 + 32 + i) * Cfg::kStageRowBytes + row * 2,
+                              __shfl_sync(0xffffffffu, w1, i) * u2f(a1[i]));
+            }
+            fence_proxy_async_smem();
+            if (!epi_sync(13)) {
+              failed = true;
+              break;
+            }
+            if (tok >= 0) {
+              bulk_reduce_add_bf16(orow + hh * kBM, my_stage, kBM * 2);
+              bulk_commit();
+            }
+          }
+        }
+        if (failed) break;
+      } else if (MODE == kModeUp) {
         constexpr int G = N / 2;
         if (tok >= 0) bulk_wait_read_all();  // the previous tile's store has left the staging row
 #pragma unroll 1
@@ -489,15 +603,15 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmAr
 }  // namespace
 
 cudaError_t launch_up_bf16(const CUtensorMap& map_a, const CUtensorMap& map_w1, const GemmArgs& args, int grid,
-                           cudaStream_t stream, int gather, int fold) {
+                           cudaStream_t stream, int gather, int fold, bool pdl) {
   if (fold == kUpFoldNarrow)  // 64 gate + 64 up rows per tile, 6-stage ring
     return launch_gemm<kModeUp, 2 * kUpFoldNarrow, kUpStagesNarrow, kGatherTile>(map_a, map_w1, args, grid, stream,
-                                                                                false);
+                                                                                pdl);
   if (gather == kGatherTma4)
-    return launch_gemm<kModeUp, 2 * kUpFold, kUpStages, kGatherTma4>(map_a, map_w1, args, grid, stream, false);
+    return launch_gemm<kModeUp, 2 * kUpFold, kUpStages, kGatherTma4>(map_a, map_w1, args, grid, stream, pdl);
   if (gather == kGatherCpAsync)
-    return launch_gemm<kModeUp, 2 * kUpFold, kUpStages, kGatherCpAsync>(map_a, map_w1, args, grid, stream, false);
-  return launch_gemm<kModeUp, 2 * kUpFold, kUpStages, kGatherTile>(map_a, map_w1, args, grid, stream, false);
+    return launch_gemm<kModeUp, 2 * kUpFold, kUpStages, kGatherCpAsync>(map_a, map_w1, args, grid, stream, pdl);
+  return launch_gemm<kModeUp, 2 * kUpFold, kUpStages, kGatherTile>(map_a, map_w1, args, grid, stream, pdl);
 }
 
 cudaError_t launch_down_bf16(const CUtensorMap& map_act, const CUtensorMap& map_w2, const GemmArgs& args, int grid,

@@ -64,22 +64,29 @@ struct GemmArgs {
   int stall_test;           // test hook: the MMA issuer first waits on a barrier nothing arrives on
   const void* x;            // up with the cp.async gather: the token rows [T, D]
   int* tile_counter;        // dynamic tile scheduling: zeroed before the launch; nullptr = static
+  const int* counts;        // routed rows per expert and padded segment starts: the
+  const int* pad_offsets;   //   row count of each row block (swap-AB tail tiles)
+  int swap_ab;              // 1: tail row blocks of <= 112 rows run as swap-AB tiles
 };
 
 // Routing; when zero_out != nullptr the first launch also zero-fills
 // zero_out[0 .. zero_bytes) (the reduction target of the GEMMs).
+// pdl: the second and third routing launches start as programmatic dependents.
 cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const float* topk_w, int T, int E, int k,
-                         cudaStream_t stream, void* zero_out = nullptr, int64_t zero_bytes = 0, int zero_grid = 0);
-// xg = x[row_tok] for live slots, and (when out != nullptr) out[0 .. out_bytes) = 0.
-cudaError_t launch_gather_zero(const Workspace& ws, const void* x, int D, void* out, int64_t out_bytes, int grid,
-                               cudaStream_t stream);
+                         cudaStream_t stream, void* zero_out = nullptr, int64_t zero_bytes = 0, int zero_grid = 0,
+                         bool pdl = false);
+// xg[padded slot of pair p] = x[p / k] for every routed pair, and (when
+// out != nullptr) out[0 .. out_bytes) = 0, out_bytes a multiple of 16 * T.
+// pdl: launched as a programmatic dependent of the routing launch.
+cudaError_t launch_gather_zero(const Workspace& ws, const void* x, const int32_t* topk_ids, int T, int E, int k,
+                               int D, void* out, int64_t out_bytes, int grid, cudaStream_t stream, bool pdl);
 // gather: 0 = map_a is the pre-gathered xg [S_max, D]; 1 = map_a is x [T, D]
 // with one-row boxes and the kernel gathers with TMA gather4; 2 = the kernel's
 // cp.async warps gather rows of args.x (map_a unused).
 // fold = gate (and up) rows per tile: kUpFold (N = 256) or kUpFoldNarrow (N =
 // 128, gather 0 only); map_w1's boxes must be `fold` rows.
 cudaError_t launch_up_bf16(const CUtensorMap& map_a, const CUtensorMap& map_w1, const GemmArgs& args, int grid,
-                           cudaStream_t stream, int gather, int fold);
+                           cudaStream_t stream, int gather, int fold, bool pdl);
 // Up-projection with two row blocks of one expert per tile sharing each W1
 // tile (tiles = block pairs x column tiles).
 cudaError_t launch_up_pair_bf16(const CUtensorMap& map_a, const CUtensorMap& map_w1, const GemmArgs& args, int grid,

@@ -288,6 +288,11 @@ __device__ __forceinline__ void red_add_bf16x8(void* gptr, uint32_t p0, uint32_t
                : "memory");
 }
 
+__device__ __forceinline__ void st_shared_b16(void* sptr, float v) {
+  const uint16_t bits = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  asm volatile("st.shared.b16 [%0], %1;" ::"r"(smem_addr(sptr)), "h"(bits) : "memory");
+}
+
 __device__ __forceinline__ void st_global_v4(void* gptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(gptr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }

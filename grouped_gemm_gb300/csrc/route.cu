@@ -91,6 +91,8 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int NB, int E, int* __
   __shared__ int seg_sum[1024];
   __shared__ int cnt_s[kMaxExperts];
   __shared__ int warp_sums[32];
+  griddep_wait();  // programmatic dependent of the histogram launch
+  griddep_launch_dependents();
   const int tid = threadIdx.x;
   int Ep = 1;
   while (Ep < E) Ep <<= 1;
@@ -217,6 +219,8 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
   extern __shared__ int wcnt[];  // [kScatterWarps][E], then offsets[E], pad_offsets[E]
   int* s_off = wcnt + kScatterWarps * E;
   int* s_poff = s_off + E;
+  griddep_wait();  // programmatic dependent of the scan launch
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t p0 = (int64_t)blockIdx.x * kRouteTokPerBlock * k;
   const int64_t p1 = min(P, p0 + (int64_t)kRouteTokPerBlock * k);
@@ -269,10 +273,19 @@ __global__ void __launch_bounds__(1024)
   for (int i = threadIdx.x; i < kRouteSmallWarps * E; i += blockDim.x) wcnt[i] = 0;
   __syncthreads();
   bool bad = false;
-  for (int p = q0 + lane; p < q1; p += 32) {
-    const int e = ids[p];
-    if ((unsigned)e < (unsigned)E) atomicAdd(&wcnt[warp * E + e], 1);
-    else bad = true;
+  for (int b0 = q0; b0 < q1; b0 += 32 * 8) {  // eight independent loads in flight per lane
+    int ev[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int p = b0 + i * 32 + lane;
+      ev[i] = p < q1 ? ids[p] : 0;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (b0 + i * 32 + lane >= q1) continue;
+      if ((unsigned)ev[i] < (unsigned)E) atomicAdd(&wcnt[warp * E + ev[i]], 1);
+      else bad = true;
+    }
   }
   if (bad) atomicOr(err, kErrBadRouting);
   __syncthreads();
@@ -325,43 +338,69 @@ __global__ void __launch_bounds__(1024)
   scatter_range(ids, topk_w, q0, q1, E, k, wcnt + warp * E, s_off, s_poff, row_tok, slot_w, slot_of_pair);
 }
 
-// xg[s, :] = x[row_tok[s], :] for live slots (16-byte vector copies, one warp
-// per row); padding rows are skipped -- each GEMM output row depends only on
-// its own input row and padding rows are dropped by the reductions.  The same
-// launch zero-fills `out` (the down projection reduces into it).
-__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ x, const int* __restrict__ row_tok,
-                                                          const int* __restrict__ meta, uint4* __restrict__ xg,
-                                                          int vec_per_row, uint4* __restrict__ out,
-                                                          int64_t out_vecs) {
+// Token-major gather: xg[padded slot of pair p, :] = x[t, :] for the k pairs
+// p = t*k + j of every token t.  One warp per (token, 4 KB chunk of its row):
+// the chunk is read once into registers (16-byte vector loads, eight per lane)
+// and written to each of the token's k slots, so x is read once rather than k
+// times.  The padded slot is slot_of_pair[p] - offsets[e] + pad_offsets[e].
+// Padding rows of xg are never written: each GEMM output row depends only on
+// its own input row, and padding rows are dropped by the epilogues.  The same
+// warp zero-fills its share of the token's row of `out` (the reduction target
+// of the down projection).  Launched as a programmatic dependent of the
+// routing: it waits for the routing grid before reading its tables.
+constexpr int kGatherChunkVecs = 256;  // 4 KB per warp work item
+
+__global__ void __launch_bounds__(256)
+    gather_tokens_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ ids,
+                         const int* __restrict__ slot_of_pair, const int* __restrict__ offsets,
+                         const int* __restrict__ pad_offsets, int T, int E, int k, int vec_per_row,
+                         uint4* __restrict__ xg, uint4* __restrict__ out, int out_vecs_per_row) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t S = (int64_t)meta[0] * kRowPad;
+  const int n_chunks = (vec_per_row + kGatherChunkVecs - 1) / kGatherChunkVecs;
+  const int zero_per = (out_vecs_per_row + n_chunks - 1) / n_chunks;
+  const int64_t items = (int64_t)T * n_chunks;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp; row < S; row += nwarps) {
-    const int tok = row_tok[row];
-    if (tok < 0) continue;
-    const uint4* src = x + (int64_t)tok * vec_per_row;
-    uint4* dst = xg + row * vec_per_row;
-    int i = lane;
-    for (; i + 96 < vec_per_row; i += 128) {
-      const uint4 a = __ldg(src + i), b = __ldg(src + i + 32), c = __ldg(src + i + 64), d = __ldg(src + i + 96);
-      dst[i] = a;
-      dst[i + 32] = b;
-      dst[i + 64] = c;
-      dst[i + 96] = d;
+  for (int64_t it = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp; it < items; it += nwarps) {
+    const int t = (int)(it / n_chunks), c = (int)(it % n_chunks);
+    const int v0 = c * kGatherChunkVecs;
+    const uint4* src = x + (int64_t)t * vec_per_row + v0;
+    uint4 v[kGatherChunkVecs / 32];
+#pragma unroll
+    for (int i = 0; i < kGatherChunkVecs / 32; ++i)
+      if (v0 + i * 32 + lane < vec_per_row) v[i] = __ldg(src + i * 32 + lane);
+    for (int j0 = 0; j0 < k; j0 += 32) {
+      // lane l resolves the padded slot of pair j0 + l
+      int ps = -1;
+      if (j0 + lane < k) {
+        const int64_t p = (int64_t)t * k + j0 + lane;
+        const int e = ids[p], s = slot_of_pair[p];
+        if (s >= 0 && (unsigned)e < (unsigned)E) ps = s - offsets[e] + pad_offsets[e];
+      }
+      const int nj = min(32, k - j0);
+      for (int jj = 0; jj < nj; ++jj) {
+        const int slot = __shfl_sync(0xffffffffu, ps, jj);
+        if (slot < 0) continue;
+        uint4* dst = xg + (int64_t)slot * vec_per_row + v0;
+#pragma unroll
+        for (int i = 0; i < kGatherChunkVecs / 32; ++i)
+          if (v0 + i * 32 + lane < vec_per_row) dst[i * 32 + lane] = v[i];
+      }
     }
-    for (; i < vec_per_row; i += 32) dst[i] = __ldg(src + i);
-  }
-  if (out) {
-    const uint4 z = make_uint4(0, 0, 0, 0);
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < out_vecs; i += (int64_t)gridDim.x * blockDim.x)
-      out[i] = z;
+    if (out) {
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      uint4* orow = out + (int64_t)t * out_vecs_per_row;
+      const int z1 = min(out_vecs_per_row, (c + 1) * zero_per);
+      for (int i = c * zero_per + lane; i < z1; i += 32) orow[i] = z;
+    }
   }
 }
 
 }  // namespace
 
 cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const float* topk_w, int T, int E, int k,
-                         cudaStream_t stream, void* zero_out, int64_t zero_bytes, int zero_grid) {
+                         cudaStream_t stream, void* zero_out, int64_t zero_bytes, int zero_grid, bool pdl) {
   const int64_t P = (int64_t)T * k;
   if (!zero_out && P <= kRouteSmallMaxPairs && E <= kRouteSmallMaxExperts) {
     route_small_kernel<<<1, 1024, 0, stream>>>(topk_ids, topk_w, (int)P, E, k, ws.err, ws.counts, ws.offsets,
@@ -373,19 +412,46 @@ cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const flo
   const int grid = zero_out ? (NB > zero_grid ? NB : zero_grid) : NB;
   route_count_kernel<<<grid, 256, E * sizeof(int), stream>>>(topk_ids, P, E, k, NB, ws.blk_base, ws.err,
                                                              static_cast<uint4*>(zero_out), zero_bytes / 16);
-  route_scan_kernel<<<1, 1024, 0, stream>>>(NB, E, ws.blk_base, ws.counts, ws.offsets, ws.pad_offsets, ws.meta,
-                                            ws.expert_of_rb, ws.pair_info, ws.row_tok, ws.slot_w);
-  route_scatter_kernel<<<NB, kScatterWarps * 32, (kScatterWarps + 2) * E * sizeof(int), stream>>>(
-      topk_ids, topk_w, P, E, k, ws.blk_base, ws.offsets, ws.pad_offsets, ws.row_tok, ws.slot_w, ws.slot_of_pair);
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // the scan and the scatter start as programmatic dependents (their launch
+  // overlaps the previous kernel; each waits for it before reading)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.gridDim = dim3(1);
+  cfg.blockDim = dim3(1024);
+  e = cudaLaunchKernelEx(&cfg, route_scan_kernel, NB, E, ws.blk_base, ws.counts, ws.offsets, ws.pad_offsets, ws.meta,
+                         ws.expert_of_rb, ws.pair_info, ws.row_tok, ws.slot_w);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3(NB);
+  cfg.blockDim = dim3(kScatterWarps * 32);
+  cfg.dynamicSmemBytes = (kScatterWarps + 2) * E * sizeof(int);
+  return cudaLaunchKernelEx(&cfg, route_scatter_kernel, static_cast<const int32_t*>(topk_ids), topk_w, P, E, k,
+                            static_cast<const int*>(ws.blk_base), static_cast<const int*>(ws.offsets),
+                            static_cast<const int*>(ws.pad_offsets), ws.row_tok, ws.slot_w, ws.slot_of_pair);
 }
 
-cudaError_t launch_gather_zero(const Workspace& ws, const void* x, int D, void* out, int64_t out_bytes, int grid,
-                               cudaStream_t stream) {
-  gather_rows_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), ws.row_tok, ws.meta,
-                                               static_cast<uint4*>(ws.xg), D / 8, static_cast<uint4*>(out),
-                                               out_bytes / 16);
-  return cudaGetLastError();
+cudaError_t launch_gather_zero(const Workspace& ws, const void* x, const int32_t* topk_ids, int T, int E, int k,
+                               int D, void* out, int64_t out_bytes, int grid, cudaStream_t stream, bool pdl) {
+  if (T == 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gather_tokens_kernel, static_cast<const uint4*>(x), topk_ids,
+                            static_cast<const int*>(ws.slot_of_pair), static_cast<const int*>(ws.offsets),
+                            static_cast<const int*>(ws.pad_offsets), T, E, k, D / 8, static_cast<uint4*>(ws.xg),
+                            static_cast<uint4*>(out), out ? (int)(out_bytes / 16 / T) : 0);
 }
 
 }  // namespace moe

@@ -181,14 +181,23 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   rows; down: 128 or 256 columns of D).  Automatic picks
  *                   128-wide up tiles when the 256-wide ones would fill the
  *                   GPU fewer than about eight times, and 256-wide down tiles
- *                   whenever D % 256 == 0. */
+ *                   whenever D % 256 == 0.
+ *   MOE_OPT_SWAP_AB  0 (default) or 1: with 1 the bf16 split GEMMs with
+ *                   256-row weight tiles run the last row block of an expert
+ *                   as a swap-AB tile when it holds at most 112 routed rows:
+ *                   the weight rows become the MMA's M = 128 side and the
+ *                   routed rows its N (rounded up to 16), so padding rows
+ *                   cost no tensor-core work.  Measured on GB300: 1-3% slower
+ *                   at prefill, large_skewed and decode (those GEMMs are
+ *                   bound by operand traffic, not by tensor-core work). */
 typedef enum {
   MOE_OPT_GATHER = 0,
   MOE_OPT_L2_PREFETCH = 1,
   MOE_OPT_TEST_STALL = 2,
   MOE_OPT_UP_PAIRS = 3,
   MOE_OPT_DYNAMIC_TILES = 4,
-  MOE_OPT_TILE_COLS = 5
+  MOE_OPT_TILE_COLS = 5,
+  MOE_OPT_SWAP_AB = 6
 } moe_option_t;
 moe_status_t moe_ffn_set_option(int option, long long value);
 

@@ -18,23 +18,27 @@ from helpers import assert_close, run_forward, to_dev
 
 pytestmark = pytest.mark.gpu
 
-# (pipeline, gather option): the split pipeline with the materializing gather
-# kernel (default) and with the in-kernel TMA gather4
-MODES = {"split": (moe.MOE_SPLIT, 0, 0), "split_pairs": (moe.MOE_SPLIT, 0, 1),
-         "split_gather4": (moe.MOE_SPLIT, 1, 0), "split_cpasync": (moe.MOE_SPLIT, 2, 0),
-         "fused": (moe.MOE_FUSED, 0, 0)}
+# (pipeline, gather option, block pairs, swap-AB tail tiles): the split
+# pipeline with the materializing gather kernel (default), with in-kernel
+# gathers, with two row blocks per up tile and with the tail row blocks run as
+# swap-AB tiles
+MODES = {"split": (moe.MOE_SPLIT, 0, 0, 0), "split_pairs": (moe.MOE_SPLIT, 0, 1, 0),
+         "split_gather4": (moe.MOE_SPLIT, 1, 0, 0), "split_cpasync": (moe.MOE_SPLIT, 2, 0, 0),
+         "split_swap": (moe.MOE_SPLIT, 0, 0, 1), "fused": (moe.MOE_FUSED, 0, 0, 0)}
 PIPELINES = list(MODES)
 
 
 def run_mode(inp, dev, mode, **kw):
-    pipeline, gather, pairs = MODES[mode]
+    pipeline, gather, pairs, swap = MODES[mode]
     moe.moe_ffn_set_option(moe.MOE_OPT_GATHER, gather)
     moe.moe_ffn_set_option(moe.MOE_OPT_UP_PAIRS, pairs)
+    moe.moe_ffn_set_option(moe.MOE_OPT_SWAP_AB, swap)
     try:
         return run_forward(inp, dev, pipeline=pipeline, **kw)
     finally:
         moe.moe_ffn_set_option(moe.MOE_OPT_GATHER, 0)
         moe.moe_ffn_set_option(moe.MOE_OPT_UP_PAIRS, 0)
+        moe.moe_ffn_set_option(moe.MOE_OPT_SWAP_AB, 0)
 
 
 def oracle_out(inp, tokens=None):
