@@ -23,6 +23,7 @@ std::atomic<int> g_stall_test{0};   // MOE_OPT_TEST_STALL
 std::atomic<int> g_up_pairs{0};     // MOE_OPT_UP_PAIRS (measured slower on GB300: off)
 std::atomic<int> g_dynamic_tiles{2};  // MOE_OPT_DYNAMIC_TILES: 0 off, 1 on, 2 small problems only
 std::atomic<int> g_tile_cols{0};      // MOE_OPT_TILE_COLS: 0 auto, 128 or 256 (bf16 split GEMM tile width)
+std::atomic<int> g_fused_cluster{1};  // MOE_OPT_FUSED_CLUSTER: 0 off, 1 automatic size, 2/4/8 that size
 std::atomic<int> g_swap_ab{0};        // MOE_OPT_SWAP_AB: swap-AB tail tiles (measured slower on GB300: off)
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -143,6 +144,12 @@ Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipe
   } else {
     w.xg = take((size_t)w.S_max * D * 2);
     w.acc_f32 = take((size_t)T * D * 4);
+    if (fused_cluster_ok(D, H)) {  // capacity for the smallest cluster size that applies
+      int cmin = 0;
+      for (int C : {8, 4, 2, 1})
+        if (fused_cluster_h1(D, H, C)) cmin = C;
+      w.ring = take((size_t)(kFusedClusterMaxCtas / cmin) * 2 * kBM * H * 2);
+    }
   }
   w.bytes = off;
   return w;
@@ -150,11 +157,90 @@ Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipe
 
 namespace {
 
+// Cluster size for the fused kernel: the one with the shortest estimated run,
+// waves of row blocks over the co-resident clusters times the work of one row
+// block per CTA (1/C of it; more when GEMM1's sub-chunks are narrower than 128
+// act columns, i.e. more operand bytes per FLOP, and for single-CTA clusters,
+// which measured slower on GB300 than their share).  The row-block count is
+// estimated from the routed pairs (half a padded block per live expert).
+int choose_cluster_size(int D, int H, int64_t pairs, int E, int max_rb) {
+  const int64_t live = std::min<int64_t>(pairs, E);
+  const int64_t est_rb = std::min<int64_t>(max_rb, std::max<int64_t>(live, (pairs + kBM - 1) / kBM + live / 2));
+  int best = 0;
+  double best_cost = 0;
+  for (int C : {1, 2, 4, 8}) {
+    const int h1 = fused_cluster_h1(D, H, C);
+    if (!h1) continue;
+    const int ncl = std::min(fused_cluster_max_clusters(C), kFusedClusterMaxCtas / C);
+    if (ncl <= 0) continue;
+    const double waves = (double)((est_rb + ncl - 1) / ncl);
+    const double narrow = h1 == 128 ? 1.0 : h1 == 96 ? 1.1 : h1 == 64 ? 1.25 : 1.6;
+    const double cost = waves * narrow * (C == 1 ? 1.3 : 1.0) / C;
+    if (!best || cost < best_cost) {
+      best = C;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
+// Fused pipeline on clusters: routing, gather (+ zero-fill of out), one GEMM
+// kernel in which clusters of D/256 CTAs exchange act through an L2-resident
+// ring and reduce finished rows into out.
+moe_status_t forward_fused_cluster_bf16(const Workspace& ws, const void* x, const void* w1, const void* w2,
+                                        const int32_t* topk_ids, const float* topk_w, void* out, int T, int E, int D,
+                                        int H, int k, int sms, int C, cudaStream_t st) {
+  const int h1 = fused_cluster_h1(D, H, C);
+  const int ncl_cap = kFusedClusterMaxCtas / C;
+  const int ncl = std::min(std::min(fused_cluster_max_clusters(C), ncl_cap), ws.max_rb);
+  if (ncl <= 0 || !h1) return MOE_ERR_CUDA;
+  CUtensorMap map_xg, map_w1, map_w2, map_ring;
+  if (!make_map_bf16(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, kBM) ||
+      !make_map_bf16(&map_w1, w1, (uint64_t)E * 2 * H, (uint64_t)D, (uint32_t)h1) ||
+      !make_map_bf16(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, kFusedClusterN) ||
+      !make_map_bf16(&map_ring, ws.ring, (uint64_t)ncl_cap * 2 * kBM, (uint64_t)H, kBM))
+    return MOE_ERR_CUDA;
+  prof_mark(st, 0);
+  cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st, nullptr, 0, 0, !g_prof.on);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  prof_mark(st, 1);
+  e = launch_gather_zero(ws, x, topk_ids, T, E, k, D, out, (int64_t)T * D * 2, sms * 4, st, !g_prof.on);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  prof_mark(st, 2);
+  FusedClusterArgs fa{};
+  fa.meta = ws.meta;
+  fa.expert_of_rb = ws.expert_of_rb;
+  fa.row_tok = ws.row_tok;
+  fa.slot_w = ws.slot_w;
+  fa.out = out;
+  fa.ring = ws.ring;
+  fa.err = ws.err;
+  fa.wait_limit_ns = g_wait_limit_ns.load();
+  fa.D = D;
+  fa.H = H;
+  fa.csize = C;
+  fa.h1 = h1;
+  fa.s1 = H / C / h1;
+  fa.s2 = D / C / kFusedClusterN;
+  fa.stall_test = g_stall_test.load();
+  e = launch_fused_cluster_bf16(map_xg, map_w1, map_w2, map_ring, fa, ncl, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  prof_mark(st, 3);
+  prof_mark(st, 4);  // no rounding pass: out is reduced in bf16 directly
+  return MOE_OK;
+}
+
 // Fused pipeline: routing, gather (+ zero-fill of the fp32 accumulator), one
 // GEMM kernel that keeps act on chip, rounding of the accumulator to bf16.
 moe_status_t forward_fused_bf16(const Workspace& ws, const void* x, const void* w1, const void* w2,
                                 const int32_t* topk_ids, const float* topk_w, void* out, int T, int E, int D, int H,
                                 int k, int sms, cudaStream_t st) {
+  const int opt = g_fused_cluster.load();
+  if (opt && fused_cluster_ok(D, H)) {
+    int C = (opt > 1 && fused_cluster_h1(D, H, opt)) ? opt : 0;
+    if (!C) C = choose_cluster_size(D, H, (int64_t)T * k, E, ws.max_rb);
+    if (C) return forward_fused_cluster_bf16(ws, x, w1, w2, topk_ids, topk_w, out, T, E, D, H, k, sms, C, st);
+  }
   CUtensorMap map_xg, map_w1, map_w2;
   if (!make_map_bf16(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, kBM) ||
       !make_map_bf16(&map_w1, w1, (uint64_t)E * 2 * H, (uint64_t)D, kUpFold) ||
@@ -312,6 +398,10 @@ moe_status_t moe_ffn_set_option(int option, long long value) {
     case MOE_OPT_TEST_STALL:
       if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
       g_stall_test.store((int)value);
+      return MOE_OK;
+    case MOE_OPT_FUSED_CLUSTER:
+      if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8) return MOE_ERR_INVALID_ARG;
+      g_fused_cluster.store((int)value);
       return MOE_OK;
     case MOE_OPT_SWAP_AB:
       if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;

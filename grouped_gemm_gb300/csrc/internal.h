@@ -33,6 +33,7 @@ struct Workspace {
   void* xg;            // [S_max, D] bf16 gathered rows (split pipeline)
   void* act;           // [S_max, H] bf16 activation (split pipeline)
   void* acc_f32;       // [T, D] fp32 reduction target (fused pipeline)
+  void* ring;          // fused pipeline on clusters: bf16 act exchange ring
   void* xg_sf;         // MXFP8: scales of xg in blocked 512-byte tiles (S_max * D/32 bytes)
   void* act_sf;        // MXFP8: scales of act in blocked tiles (S_max * H/32 bytes)
   size_t bytes;        // total bytes required
@@ -112,6 +113,47 @@ struct FusedArgs {
 cudaError_t launch_fused_bf16(const CUtensorMap& map_xg, const CUtensorMap& map_w1, const CUtensorMap& map_w2,
                               const FusedArgs& args, int grid, cudaStream_t stream);
 cudaError_t launch_f32_to_bf16(const void* acc, void* out, int64_t n, int grid, cudaStream_t stream);
+
+// Fused pipeline on clusters of C CTAs (one 128-row block per cluster at a
+// time, the activation exchanged through an L2-resident ring).
+constexpr int kFusedClusterN = 256;       // GEMM2 output columns per sub-chunk
+constexpr int kFusedClusterMaxCtas = 160; // ring capacity: clusters <= this / C
+struct FusedClusterArgs {
+  const int* meta;
+  const int* expert_of_rb;
+  const int* row_tok;
+  const float* slot_w;
+  void* out;                // bf16 [T, D], zeroed before the launch
+  void* ring;               // bf16 [n_clusters * 2 * 128, H]
+  int* err;
+  unsigned long long wait_limit_ns;
+  int D, H;
+  int csize;                // CTAs per cluster C (1, 2, 4 or 8)
+  int h1;                   // act columns per GEMM1 sub-chunk (32, 64, 96 or 128)
+  int s1;                   // GEMM1 sub-chunks per CTA: h1 * s1 = H / C
+  int s2;                   // GEMM2 sub-chunks per CTA: 256 * s2 = D / C
+  int stall_test;           // test hook (see GemmArgs)
+};
+// Act columns per GEMM1 sub-chunk for cluster size C, or 0 if (D, H) cannot
+// run on clusters of C.
+inline int fused_cluster_h1(int D, int H, int C) {
+  if (C != 1 && C != 2 && C != 4 && C != 8) return 0;
+  if (D % (kFusedClusterN * C) || H % C) return 0;
+  const int h = H / C;
+  for (int h1 : {128, 96, 64, 32})
+    if (h % h1 == 0) return h1;
+  return 0;
+}
+inline bool fused_cluster_ok(int D, int H) {
+  for (int C : {1, 2, 4, 8})
+    if (fused_cluster_h1(D, H, C)) return true;
+  return false;
+}
+// Co-resident clusters of size csize on the current device (0 on failure).
+int fused_cluster_max_clusters(int csize);
+cudaError_t launch_fused_cluster_bf16(const CUtensorMap& map_xg, const CUtensorMap& map_w1, const CUtensorMap& map_w2,
+                                      const CUtensorMap& map_ring, const FusedClusterArgs& args, int n_clusters,
+                                      cudaStream_t stream);
 
 struct MxArgs {
   const int* meta;

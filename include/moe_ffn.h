@@ -189,7 +189,18 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   routed rows its N (rounded up to 16), so padding rows
  *                   cost no tensor-core work.  Measured on GB300: 1-3% slower
  *                   at prefill, large_skewed and decode (those GEMMs are
- *                   bound by operand traffic, not by tensor-core work). */
+ *                   bound by operand traffic, not by tensor-core work).
+ *   MOE_OPT_FUSED_CLUSTER  1 (default: automatic size), 2, 4, 8 or 0: the
+ *                   bf16 fused pipeline runs on thread-block clusters of C
+ *                   CTAs (D % (256 C) == 0, H/C a multiple of 32): each CTA
+ *                   computes H/C columns of act for the cluster's row block,
+ *                   the slices meet in an L2-resident ring, and each CTA
+ *                   reduces D/C finished output columns into out in bf16.
+ *                   1 picks C from the shape and the number of clusters that
+ *                   fit on the device; 2, 4 or 8 request that size (automatic
+ *                   when it does not apply).  With 0 (or a shape no C fits)
+ *                   the fused pipeline splits H over CTAs and sums partial
+ *                   rows in an fp32 buffer. */
 typedef enum {
   MOE_OPT_GATHER = 0,
   MOE_OPT_L2_PREFETCH = 1,
@@ -197,7 +208,8 @@ typedef enum {
   MOE_OPT_UP_PAIRS = 3,
   MOE_OPT_DYNAMIC_TILES = 4,
   MOE_OPT_TILE_COLS = 5,
-  MOE_OPT_SWAP_AB = 6
+  MOE_OPT_SWAP_AB = 6,
+  MOE_OPT_FUSED_CLUSTER = 7
 } moe_option_t;
 moe_status_t moe_ffn_set_option(int option, long long value);
 

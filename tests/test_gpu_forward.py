@@ -18,27 +18,33 @@ from helpers import assert_close, run_forward, to_dev
 
 pytestmark = pytest.mark.gpu
 
-# (pipeline, gather option, block pairs, swap-AB tail tiles): the split
-# pipeline with the materializing gather kernel (default), with in-kernel
-# gathers, with two row blocks per up tile and with the tail row blocks run as
-# swap-AB tiles
-MODES = {"split": (moe.MOE_SPLIT, 0, 0, 0), "split_pairs": (moe.MOE_SPLIT, 0, 1, 0),
-         "split_gather4": (moe.MOE_SPLIT, 1, 0, 0), "split_cpasync": (moe.MOE_SPLIT, 2, 0, 0),
-         "split_swap": (moe.MOE_SPLIT, 0, 0, 1), "fused": (moe.MOE_FUSED, 0, 0, 0)}
+# Pipeline and option settings under test: the split pipeline with the
+# materializing gather kernel (default), with in-kernel gathers, with two row
+# blocks per up tile and with the tail row blocks run as swap-AB tiles; the
+# fused pipeline on clusters (default where the shape allows) and with the
+# H-split fp32 partial sums.
+MODES = {
+    "split": (moe.MOE_SPLIT, {}),
+    "split_pairs": (moe.MOE_SPLIT, {moe.MOE_OPT_UP_PAIRS: 1}),
+    "split_gather4": (moe.MOE_SPLIT, {moe.MOE_OPT_GATHER: 1}),
+    "split_cpasync": (moe.MOE_SPLIT, {moe.MOE_OPT_GATHER: 2}),
+    "split_swap": (moe.MOE_SPLIT, {moe.MOE_OPT_SWAP_AB: 1}),
+    "fused": (moe.MOE_FUSED, {}),
+    "fused_splitk": (moe.MOE_FUSED, {moe.MOE_OPT_FUSED_CLUSTER: 0}),
+}
+DEFAULTS = {moe.MOE_OPT_UP_PAIRS: 0, moe.MOE_OPT_GATHER: 0, moe.MOE_OPT_SWAP_AB: 0, moe.MOE_OPT_FUSED_CLUSTER: 1}
 PIPELINES = list(MODES)
 
 
 def run_mode(inp, dev, mode, **kw):
-    pipeline, gather, pairs, swap = MODES[mode]
-    moe.moe_ffn_set_option(moe.MOE_OPT_GATHER, gather)
-    moe.moe_ffn_set_option(moe.MOE_OPT_UP_PAIRS, pairs)
-    moe.moe_ffn_set_option(moe.MOE_OPT_SWAP_AB, swap)
+    pipeline, opts = MODES[mode]
+    for o, v in opts.items():
+        moe.moe_ffn_set_option(o, v)
     try:
         return run_forward(inp, dev, pipeline=pipeline, **kw)
     finally:
-        moe.moe_ffn_set_option(moe.MOE_OPT_GATHER, 0)
-        moe.moe_ffn_set_option(moe.MOE_OPT_UP_PAIRS, 0)
-        moe.moe_ffn_set_option(moe.MOE_OPT_SWAP_AB, 0)
+        for o in opts:
+            moe.moe_ffn_set_option(o, DEFAULTS[o])
 
 
 def oracle_out(inp, tokens=None):
@@ -64,6 +70,26 @@ def test_forward_small(T, D, H, E, k, routing, pipeline):
     out, _ = run_mode(inp, to_dev(inp), pipeline)
     r = assert_close(out, oracle_out(inp), label=f"T={T} D={D} H={H} E={E} k={k}")
     print(f"{pipeline} T={T} D={D} H={H} E={E} k={k}: max_rel={r[0]:.2e} mean_rel={r[1]:.2e} cos={r[2]:.6f}")
+
+
+@pytest.mark.parametrize("csize", [1, 2, 4, 8])   # 1: automatic
+@pytest.mark.parametrize("T,D,H,E,k", [
+    (150, 512, 128, 8, 2),      # 64 or 128 act columns per CTA
+    (300, 1024, 512, 16, 4),    # several GEMM1 and GEMM2 sub-chunks per CTA
+    (200, 2048, 256, 32, 8),    # 32 act columns per CTA with clusters of 8
+    (1000, 2048, 768, 8, 8),    # prefill dims, ~8 row blocks per expert: each ring buffer reused
+])
+def test_fused_cluster_shapes(T, D, H, E, k, csize):
+    if csize > 1 and (D % (256 * csize) or (H // csize) % 32):
+        pytest.skip("cluster size does not apply to this shape")
+    inp = wl.make_custom(T, D, H, E, k, seed=T + H, routing="uniform")
+    moe.moe_ffn_set_option(moe.MOE_OPT_FUSED_CLUSTER, csize)
+    try:
+        out, _ = run_forward(inp, to_dev(inp), pipeline=moe.MOE_FUSED)
+    finally:
+        moe.moe_ffn_set_option(moe.MOE_OPT_FUSED_CLUSTER, 1)
+    r = assert_close(out, oracle_out(inp), label=f"fused C={csize} T={T} D={D} H={H} E={E} k={k}")
+    print(f"fused C={csize} T={T} D={D} H={H} E={E} k={k}: max_rel={r[0]:.2e} mean_rel={r[1]:.2e} cos={r[2]:.6f}")
 
 
 @pytest.mark.parametrize("pipeline", PIPELINES)
@@ -116,7 +142,7 @@ def test_unsupported_combinations_rejected():
 @pytest.mark.parametrize("name,n_sample", [("decode", None), ("prefill", 96), ("large_skewed", 40)])
 @pytest.mark.parametrize("pipeline", PIPELINES)
 def test_forward_full_workload_sampled(name, n_sample, pipeline):
-    if name == "large_skewed" and pipeline not in ("split", "fused"):
+    if name == "large_skewed" and pipeline not in ("split", "fused", "fused_splitk"):
         pytest.skip("option variants are covered at the smaller sizes")
     inp = wl.make_inputs(name, seed=0)
     out, _ = run_mode(inp, to_dev(inp), pipeline)
