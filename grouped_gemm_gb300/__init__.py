@@ -177,6 +177,7 @@ MOE_OPT_DYNAMIC_TILES = 4
 MOE_OPT_TILE_COLS = 5
 MOE_OPT_SWAP_AB = 6
 MOE_OPT_FUSED_CLUSTER = 7
+MOE_OPT_PAIR_MMA = 8
 
 
 def moe_ffn_set_option(option: int, value: int) -> int:

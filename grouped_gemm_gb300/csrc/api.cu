@@ -24,6 +24,7 @@ std::atomic<int> g_up_pairs{0};     // MOE_OPT_UP_PAIRS (measured slower on GB30
 std::atomic<int> g_dynamic_tiles{2};  // MOE_OPT_DYNAMIC_TILES: 0 off, 1 on, 2 small problems only
 std::atomic<int> g_tile_cols{0};      // MOE_OPT_TILE_COLS: 0 auto, 128 or 256 (bf16 split GEMM tile width)
 std::atomic<int> g_fused_cluster{1};  // MOE_OPT_FUSED_CLUSTER: 0 off, 1 automatic size, 2/4/8 that size
+std::atomic<int> g_pair_mma{2};       // MOE_OPT_PAIR_MMA: 0 off, 1 on, 2 automatic (not for small problems)
 std::atomic<int> g_swap_ab{0};        // MOE_OPT_SWAP_AB: swap-AB tail tiles (measured slower on GB300: off)
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -137,6 +138,14 @@ Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipe
       w.act_sf = take((size_t)w.S_max * H / 32);
     } else {
       w.acc_f32 = take((size_t)T * D * 4);
+      int cmin = 0;  // ring capacity for the smallest cluster size that applies
+      for (int C : {8, 4, 2, 1})
+        if (fused_cluster_mx_fits(D, H, C)) cmin = C;
+      if (cmin) {
+        const size_t bufs = (size_t)(kFusedClusterMaxCtas / cmin) * 2;
+        w.ring = take(bufs * kBM * H);
+        w.ring_sf = take(bufs * (H / 128) * 512);
+      }
     }
   } else if (pipeline == MOE_SPLIT) {
     w.xg = take((size_t)w.S_max * D * 2);
@@ -326,6 +335,75 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
   return cuda_status(e);
 }
 
+// Cluster size for the MXFP8 fused kernel (same estimate as the bf16 one; the
+// act slices are always 128 columns wide).
+int choose_cluster_size_mx(int D, int H, int64_t pairs, int E, int max_rb) {
+  const int64_t live = std::min<int64_t>(pairs, E);
+  const int64_t est_rb = std::min<int64_t>(max_rb, std::max<int64_t>(live, (pairs + kBM - 1) / kBM + live / 2));
+  int best = 0;
+  double best_cost = 0;
+  for (int C : {1, 2, 4, 8}) {
+    if (!fused_cluster_mx_fits(D, H, C)) continue;
+    const int ncl = std::min(fused_cluster_mx_max_clusters(C), kFusedClusterMaxCtas / C);
+    if (ncl <= 0) continue;
+    const double cost = (double)((est_rb + ncl - 1) / ncl) * (C == 1 ? 1.3 : 1.0) / C;
+    if (!best || cost < best_cost) {
+      best = C;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
+// MXFP8 fused pipeline on clusters: routing, gather of e4m3 rows and scales (+
+// zero of out), one block-scaled GEMM kernel whose clusters exchange the
+// requantized act through an L2-resident ring.
+moe_status_t forward_fused_cluster_mxfp8(const Workspace& ws, const void* x, const void* x_sf, const void* w1,
+                                         const void* w1_sf, const void* w2, const void* w2_sf,
+                                         const int32_t* topk_ids, const float* topk_w, void* out, int T, int E, int D,
+                                         int H, int k, int sms, int C, cudaStream_t st) {
+  const int ncl_cap = kFusedClusterMaxCtas / C;
+  const int ncl = std::min(std::min(fused_cluster_mx_max_clusters(C), ncl_cap), ws.max_rb);
+  if (ncl <= 0) return MOE_ERR_CUDA;
+  CUtensorMap map_xg, map_w1, map_w2, map_ring;
+  if (!make_map_fp8(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, kBM) ||
+      !make_map_fp8(&map_w1, w1, (uint64_t)E * 2 * H, (uint64_t)D, 128) ||
+      !make_map_fp8(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, 256) ||
+      !make_map_fp8(&map_ring, ws.ring, (uint64_t)ncl_cap * 2 * kBM, (uint64_t)H, kBM))
+    return MOE_ERR_CUDA;
+  prof_mark(st, 0);
+  cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st, nullptr, 0, 0, !g_prof.on);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  prof_mark(st, 1);
+  e = launch_gather_mx(ws, x, x_sf, D, out, (int64_t)T * D * 2, sms * 4, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  prof_mark(st, 2);
+  FusedClusterMxArgs fa{};
+  fa.meta = ws.meta;
+  fa.expert_of_rb = ws.expert_of_rb;
+  fa.row_tok = ws.row_tok;
+  fa.slot_w = ws.slot_w;
+  fa.out = out;
+  fa.ring = ws.ring;
+  fa.ring_sf = ws.ring_sf;
+  fa.xg_sf = ws.xg_sf;
+  fa.w1_sf = w1_sf;
+  fa.w2_sf = w2_sf;
+  fa.err = ws.err;
+  fa.wait_limit_ns = g_wait_limit_ns.load();
+  fa.D = D;
+  fa.H = H;
+  fa.csize = C;
+  fa.s1 = H / C / 128;
+  fa.s2 = D / C / 256;
+  fa.stall_test = g_stall_test.load();
+  e = launch_fused_cluster_mxfp8(map_xg, map_w1, map_w2, map_ring, fa, ncl, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  prof_mark(st, 3);
+  prof_mark(st, 4);  // no rounding pass: out is reduced in bf16 directly
+  return MOE_OK;
+}
+
 // MXFP8 fused pipeline: routing, gather of e4m3 rows and scales (+ zero of the
 // fp32 accumulator), one block-scaled GEMM kernel that keeps the requantized
 // act on chip, rounding of the accumulator to bf16.
@@ -333,6 +411,14 @@ moe_status_t forward_fused_mxfp8(const Workspace& ws, const void* x, const void*
                                  const void* w1_sf, const void* w2, const void* w2_sf, const int32_t* topk_ids,
                                  const float* topk_w, void* out, int T, int E, int D, int H, int k, int sms,
                                  cudaStream_t st) {
+  const int opt = g_fused_cluster.load();
+  if (opt && ws.ring) {
+    int C = (opt > 1 && fused_cluster_mx_fits(D, H, opt)) ? opt : 0;
+    if (!C) C = choose_cluster_size_mx(D, H, (int64_t)T * k, E, ws.max_rb);
+    if (C)
+      return forward_fused_cluster_mxfp8(ws, x, x_sf, w1, w1_sf, w2, w2_sf, topk_ids, topk_w, out, T, E, D, H, k,
+                                         sms, C, st);
+  }
   CUtensorMap map_xg, map_w1, map_w2;
   if (!make_map_fp8(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, kBM) ||
       !make_map_fp8(&map_w1, w1, (uint64_t)E * 2 * H, (uint64_t)D, 128) ||
@@ -402,6 +488,10 @@ moe_status_t moe_ffn_set_option(int option, long long value) {
     case MOE_OPT_FUSED_CLUSTER:
       if (value != 0 && value != 1 && value != 2 && value != 4 && value != 8) return MOE_ERR_INVALID_ARG;
       g_fused_cluster.store((int)value);
+      return MOE_OK;
+    case MOE_OPT_PAIR_MMA:
+      if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
+      g_pair_mma.store((int)value);
       return MOE_OK;
     case MOE_OPT_SWAP_AB:
       if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
@@ -488,16 +578,24 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   const int cols = g_tile_cols.load();
   const int down_n = (D % kDownN != 0 || cols == 128) ? kDownNNarrow : kDownN;
   const bool narrow_ok = !in_gemm_gather && !g_up_pairs.load();
-  const int fold = (narrow_ok && (cols == 128 || (cols == 0 && (int64_t)ws.max_rb * (H / kUpFold) < 8LL * sms)))
-                       ? kUpFoldNarrow
-                       : kUpFold;  // auto: narrow when the wide tiles make fewer than ~8 waves
+  // CTA pairs unless the problem is small (decode-sized: its GEMMs stream
+  // weights, and the narrow single-CTA tiles fill the GPU better)
+  const int pair_opt = g_pair_mma.load();
+  const bool small_up = (int64_t)ws.max_rb * (H / kUpFold) < 8LL * sms;
+  const bool pair_mma =
+      (pair_opt == 1 || (pair_opt == 2 && !small_up)) && !in_gemm_gather && !g_up_pairs.load() && cols != 128;
+  const int fold =
+      (!pair_mma && narrow_ok && (cols == 128 || (cols == 0 && (int64_t)ws.max_rb * (H / kUpFold) < 8LL * sms)))
+          ? kUpFoldNarrow
+          : kUpFold;  // auto: narrow when the wide tiles make fewer than ~8 waves
+  const bool pair_down = pair_mma && down_n == kDownN;
   CUtensorMap map_xg, map_w1, map_act, map_w2;
   const bool map_a_ok = in_gemm_gather ? make_map_bf16(&map_xg, x, (uint64_t)T, (uint64_t)D, 1)
                                        : make_map_bf16(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, kBM);
   if (!map_a_ok ||
       !make_map_bf16(&map_w1, w1, (uint64_t)E * 2 * H, (uint64_t)D, fold) ||
       !make_map_bf16(&map_act, ws.act, (uint64_t)ws.S_max, (uint64_t)H, kBM) ||
-      !make_map_bf16(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, down_n))
+      !make_map_bf16(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, pair_down ? 128 : down_n))
     return MOE_ERR_CUDA;
 
   prof_mark(st, 0);
@@ -541,8 +639,15 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   up.k_blocks = D / kBK;
   const int up_grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * up.n_col_tiles);
   up.x = x;
-  e = (gather == 0 && g_up_pairs.load()) ? launch_up_pair_bf16(map_xg, map_w1, up, up_grid, st)
-                                         : launch_up_bf16(map_xg, map_w1, up, up_grid, st, gather, fold, !g_prof.on);
+  const int pair_slots = pair_mma ? pair_cluster_slots() : 0;
+  if (pair_mma && pair_slots <= 0) return MOE_ERR_CUDA;
+  if (pair_mma)
+    e = launch_up_pair2_bf16(map_xg, map_w1, up,
+                             (int)std::min<int64_t>(pair_slots, (int64_t)ws.max_rb * up.n_col_tiles), st, !g_prof.on);
+  else if (gather == 0 && g_up_pairs.load())
+    e = launch_up_pair_bf16(map_xg, map_w1, up, up_grid, st);
+  else
+    e = launch_up_bf16(map_xg, map_w1, up, up_grid, st, gather, fold, !g_prof.on);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 3);
 
@@ -551,7 +656,12 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   dn.n_col_tiles = D / down_n;
   dn.k_blocks = H / kBK;
   const int dn_grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * dn.n_col_tiles);
-  e = launch_down_bf16(map_act, map_w2, dn, dn_grid, st, !g_prof.on, down_n);
+  if (pair_down)
+    e = launch_down_pair2_bf16(map_act, map_w2, dn,
+                               (int)std::min<int64_t>(pair_slots, (int64_t)ws.max_rb * dn.n_col_tiles), st,
+                               !g_prof.on);
+  else
+    e = launch_down_bf16(map_act, map_w2, dn, dn_grid, st, !g_prof.on, down_n);
   prof_mark(st, 4);
   return cuda_status(e);
 }

@@ -1,0 +1,348 @@
+// gemm_pair2.cu -- the split pipeline's GEMMs on CTA pairs (tcgen05
+// cta_group::2): one MMA of M = 256 rows (two row blocks of one expert) by
+// N = 256 columns is issued by the even CTA of a two-CTA cluster; each CTA
+// holds its own 128 rows of A and half (128 rows) of the B tile in shared
+// memory and receives its 128 rows of the accumulator in its own tensor
+// memory.  Per K step a CTA brings in 32 KB (16 KB of A, 16 KB of B) for the
+// same 128 x 256 block of output as the single-CTA kernel's 48 KB: a third
+// fewer bytes per FLOP, six stages in the same shared memory, one and a half
+// times the work in flight per SM (Pearl "Optimizing Grouped GEMM for MoE on
+// Blackwell": 2-CTA 256-row tiles at large batch; "Prime Flash MoE" sec. 5
+// "BPC and CPC": two row tiles against the same weight tile).
+//
+// UP  (GEMM1 + SwiGLU): B = [W1 gate rows j*128 .. +128 (even CTA) | up rows
+//     H + j*128 .. +128 (odd CTA)], so each CTA's accumulator holds gate in
+//     columns [0, 128) and up in [128, 256) for its row block; the epilogue
+//     is the single-CTA kernel's (act row staged, one bulk store).
+// DOWN (GEMM2 + weighted reduce): B = W2[e] rows j*256 + 128 * rank .. +128;
+//     the epilogue scales by the routing weight and reduces half rows into out
+//     with bulk .add.bf16.
+// Tiles are (block pair, column tile j); a pair whose second block does not
+// exist (an expert with an odd number of row blocks) still runs both CTAs: the
+// odd CTA loads the first block's rows again and stores nothing.
+//
+// Synchronization: both CTAs' TMA loads complete on the even CTA's full[]
+// barrier (which expects the pair's bytes); the MMA commits arrive on empty[]
+// and tfull[] of both CTAs (multicast); each CTA's epilogue warps arrive on the
+// even CTA's tempty[] (release, cluster scope).  Every wait is bounded; both
+// CTAs meet at a cluster barrier before the pair releases tensor memory.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+enum { kPairUp = 0, kPairDown = 1 };
+constexpr int kQStages = 6;
+constexpr int kQThreads = 192;
+constexpr int kQA = kBM * kBK * 2;          // 16 KB: this CTA's 128 rows of A
+constexpr int kQB = 128 * kBK * 2;          // 16 KB: this CTA's half of the 256-row B tile
+constexpr int kQStage = kQA + kQB;
+constexpr int kQStageRow = 256 + 16;        // epilogue staging row (+16 B: a warp's rows on distinct banks)
+constexpr int kQStaging = kBM * kQStageRow;
+constexpr int kQBarrierBytes = 256;
+constexpr int kQSmem = kQStages * kQStage + kQStaging + kQBarrierBytes;
+static_assert(kQSmem <= 232448, "shared memory");
+static_assert((2 * kQStages + 6) * 8 + 8 <= kQBarrierBytes, "barrier area");
+constexpr uint64_t kQDrainNs = 200ull * 1000 * 1000;
+constexpr uint64_t kQSettleNs = 2ull * 1000 * 1000;  // abort path: copies in flight land well within this
+
+__device__ __forceinline__ float q_u2f(uint32_t u) { return __uint_as_float(u); }
+__device__ __forceinline__ float q_swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
+
+template <int MODE>
+__global__ void __launch_bounds__(kQThreads, 1)
+    gemm_pair2_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                      const GemmArgs args) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_addr(smem_raw) & 1023u) {  // the same in every CTA: all of them return here
+    if (threadIdx.x == 0) atomicOr(args.err, kErrLaunch);
+    return;
+  }
+  uint8_t* sA = smem_raw;
+  uint8_t* sB = sA + kQStages * kQA;
+  uint8_t* sStage = sB + kQStages * kQB;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + kQStaging);
+  uint64_t* empty = full + kQStages;
+  uint64_t* tfull = empty + kQStages;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint64_t* never = drain + 1;  // no thread ever arrives here (failure-path test hook)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const WaitCtl wc{abort_flag, args.err, args.wait_limit_ns};
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair_slot = (int)blockIdx.x >> 1, n_pair_slots = (int)gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kQStages; ++s) {
+      mbar_init(&full[s], 1);   // even CTA: its producer's arrive + both CTAs' bytes
+      mbar_init(&empty[s], 1);  // the pair MMA's commit
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 8);  // even CTA: four epilogue warps of each CTA
+    }
+    mbar_init(drain, 1);
+    mbar_init(never, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&map_a);
+    prefetch_tmap(&map_b);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, 512);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync_all();  // both CTAs' barriers and tensor memory exist
+  const uint32_t tmem_base = *tmem_slot;
+  // launched as a programmatic dependent: the prologue above overlapped the
+  // previous grid; everything below reads its outputs
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
+
+  const int NJ = args.n_col_tiles;
+  const int n_tiles = args.meta[1] * NJ;  // (block pair, column tile)
+  const int KB = args.k_blocks;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    int s = 0;
+    uint32_t ph = 0;
+    int issued_phase[kQStages];
+#pragma unroll
+    for (int i = 0; i < kQStages; ++i) issued_phase[i] = -1;
+    bool ok = true;
+    for (int tile = pair_slot; ok && tile < n_tiles; tile += n_pair_slots) {
+      const int info = args.pair_info[tile / NJ], j = tile % NJ;
+      const int rb0 = info >> 1, two = info & 1;
+      const int my_rb = rb0 + (int)(rank & (uint32_t)two);  // the odd CTA of a half pair reloads rb0
+      const int e = args.expert_of_rb[rb0];
+      const int brow = MODE == kPairUp ? e * 2 * args.H + (int)rank * args.H + j * 128
+                                       : e * args.D + j * 256 + (int)rank * 128;
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!(ok = mbar_wait(&empty[s], ph ^ 1u, wc, 61))) break;
+        if (leader) mbar_arrive_expect_tx(&full[s], 2 * kQStage);
+        const uint32_t fb = mapa_shared(smem_addr(&full[s]), 0);
+        tma_load_2d_pair(sA + s * kQA, &map_a, fb, kb * kBK, my_rb * kBM);
+        tma_load_2d_pair(sB + s * kQB, &map_b, fb, kb * kBK, brow);
+        issued_phase[s] = (int)ph;
+        if (++s == kQStages) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+    if (!ok) {  // let every copy already in flight land before the CTA exits
+      if (leader) {
+        for (int i = 0; i < kQStages; ++i)
+          if (issued_phase[i] >= 0) mbar_wait_drain(&full[i], (uint32_t)issued_phase[i], kQDrainNs);
+      } else {
+        spin_ns(kQSettleNs);  // this CTA's loads complete on the even CTA's barriers
+      }
+    }
+  } else if (warp == 1 && lane == 0 && leader) {
+    // ------------------------------------------------------------ MMA issuer (even CTA)
+    constexpr uint32_t idesc = idesc_bf16_f32(2 * kBM, 256);
+    int s = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    if (args.stall_test) ok = mbar_wait(never, 0, wc, 97);  // runs out after the wait limit
+    int it = 0;
+    for (int tile = pair_slot; ok && tile < n_tiles; tile += n_pair_slots, ++it) {
+      const int acc = it & 1;
+      if (!(ok = mbar_wait_cluster(&tempty[acc], ((uint32_t)(it >> 1) & 1u) ^ 1u, wc, 62))) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * 256;
+      for (int kb = 0; kb < KB; ++kb) {
+        if (!(ok = mbar_wait(&full[s], ph, wc, 63))) break;
+        tc_fence_after();
+        const uint64_t adesc = sdesc_sw128(smem_addr(sA + s * kQA));
+        const uint64_t bdesc = sdesc_sw128(smem_addr(sB + s * kQB));
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          umma_bf16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+        umma_commit_pair(&empty[s], 0x3);  // frees this stage in both CTAs
+        if (++s == kQStages) {
+          s = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok) break;
+      umma_commit_pair(&tfull[acc], 0x3);  // both CTAs' accumulators ready
+    }
+    if (!ok) {  // wait for every MMA already issued before tensor memory is released
+      umma_commit_pair(drain, 0x1);
+      mbar_wait_drain(drain, 0, kQDrainNs);
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int quad = warp & 3;  // TMEM lanes this warp may access
+    const int row = quad * 32 + lane;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
+    uint8_t* my_stage = sStage + row * kQStageRow;
+    const uint32_t tempty_leader0 = mapa_shared(smem_addr(&tempty[0]), 0);
+    int it = 0;
+    for (int tile = pair_slot; tile < n_tiles; tile += n_pair_slots, ++it) {
+      const int acc = it & 1;
+      if (!mbar_wait(&tfull[acc], (uint32_t)(it >> 1) & 1u, wc, 64)) break;
+      tc_fence_after();
+      const int info = args.pair_info[tile / NJ], j = tile % NJ;
+      const bool valid = rank == 0 || (info & 1);
+      const int64_t slot = (int64_t)((info >> 1) + (int)rank) * kBM + row;
+      const int tok = valid ? args.row_tok[slot] : -1;
+      const uint32_t tacc = lane_base + acc * 256;
+      if (MODE == kPairUp) {
+        if (tok >= 0) bulk_wait_read_all();  // the previous tile's store has left the staging row
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t g[32], u[32];
+          tmem_ld_x32_pair(tacc + c * 32, tacc + 128 + c * 32, g, u);
+          if (tok >= 0) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack_bf16x2(q_swiglu(q_u2f(g[2 * i]), q_u2f(u[2 * i])),
+                                  q_swiglu(q_u2f(g[2 * i + 1]), q_u2f(u[2 * i + 1])));
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              st_shared_v4(my_stage + c * 64 + q * 16, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
+        }
+        if (tok >= 0) {  // act[slot, j*128 .. +128): one 256-byte bulk copy of the staged row
+          fence_proxy_async_smem();
+          bulk_store(static_cast<__nv_bfloat16*>(args.act) + slot * args.H + j * 128, my_stage, 256);
+          bulk_commit();
+        }
+      } else {
+        const float w = valid ? args.slot_w[slot] : 0.f;
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(args.out) + (int64_t)(tok < 0 ? 0 : tok) * args.D + j * 256;
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {  // two half rows of 128 columns
+          bulk_wait_read_all();        // the previous reduction has left the staging row
+#pragma unroll 1
+          for (int c = h * 4; c < h * 4 + 4; c += 2) {
+            uint32_t v0[32], v1[32];
+            tmem_ld_x32_pair(tacc + c * 32, tacc + (c + 1) * 32, v0, v1);
+            if (tok >= 0) {
+              uint8_t* st0 = my_stage + (c - h * 4) * 64;
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                st_shared_v4(st0 + q * 16, pack_bf16x2(w * q_u2f(v0[8 * q + 0]), w * q_u2f(v0[8 * q + 1])),
+                             pack_bf16x2(w * q_u2f(v0[8 * q + 2]), w * q_u2f(v0[8 * q + 3])),
+                             pack_bf16x2(w * q_u2f(v0[8 * q + 4]), w * q_u2f(v0[8 * q + 5])),
+                             pack_bf16x2(w * q_u2f(v0[8 * q + 6]), w * q_u2f(v0[8 * q + 7])));
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                st_shared_v4(st0 + 64 + q * 16, pack_bf16x2(w * q_u2f(v1[8 * q + 0]), w * q_u2f(v1[8 * q + 1])),
+                             pack_bf16x2(w * q_u2f(v1[8 * q + 2]), w * q_u2f(v1[8 * q + 3])),
+                             pack_bf16x2(w * q_u2f(v1[8 * q + 4]), w * q_u2f(v1[8 * q + 5])),
+                             pack_bf16x2(w * q_u2f(v1[8 * q + 6]), w * q_u2f(v1[8 * q + 7])));
+            }
+          }
+          if (tok >= 0) {
+            fence_proxy_async_smem();
+            bulk_reduce_add_bf16(orow + h * 128, my_stage, 256);
+            bulk_commit();
+          }
+        }
+      }
+      // this warp has read the accumulator: tell the even CTA's MMA issuer
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty_leader0 + acc * 8);
+    }
+    bulk_wait_all();  // bulk stores / reductions complete before the CTA exits
+  }
+
+  // ------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // neither CTA leaves while the other may still use its barriers or shared memory
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, 512);
+  }
+}
+
+template <int MODE>
+cudaError_t launch_pair2(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args, int n_pairs,
+                         cudaStream_t stream, bool pdl) {
+  auto kern = gemm_pair2_kernel<MODE>;
+  // once per device: not a stream operation, so it stays out of graph capture
+  static bool smem_set[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!smem_set[dev]) {
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem);
+    if (err != cudaSuccess) return err;
+    smem_set[dev] = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * n_pairs);
+  cfg.blockDim = dim3(kQThreads);
+  cfg.dynamicSmemBytes = kQSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, kern, a, b, args);
+}
+
+}  // namespace
+
+int pair_cluster_slots() {
+  // once per device: not a stream operation
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cache[dev]) return cache[dev];
+  auto kern = gemm_pair2_kernel<kPairUp>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kQThreads);
+  cfg.dynamicSmemBytes = kQSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cache[dev] = n;
+  return n;
+}
+
+cudaError_t launch_up_pair2_bf16(const CUtensorMap& map_xg, const CUtensorMap& map_w1, const GemmArgs& args,
+                                 int n_pairs, cudaStream_t stream, bool pdl) {
+  return launch_pair2<kPairUp>(map_xg, map_w1, args, n_pairs, stream, pdl);
+}
+
+cudaError_t launch_down_pair2_bf16(const CUtensorMap& map_act, const CUtensorMap& map_w2, const GemmArgs& args,
+                                   int n_pairs, cudaStream_t stream, bool pdl) {
+  return launch_pair2<kPairDown>(map_act, map_w2, args, n_pairs, stream, pdl);
+}
+
+}  // namespace moe

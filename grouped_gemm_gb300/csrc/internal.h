@@ -33,7 +33,8 @@ struct Workspace {
   void* xg;            // [S_max, D] bf16 gathered rows (split pipeline)
   void* act;           // [S_max, H] bf16 activation (split pipeline)
   void* acc_f32;       // [T, D] fp32 reduction target (fused pipeline)
-  void* ring;          // fused pipeline on clusters: bf16 act exchange ring
+  void* ring;          // fused pipeline on clusters: act exchange ring (bf16, or e4m3)
+  void* ring_sf;       // MXFP8 fused pipeline on clusters: scale tiles of the ring
   void* xg_sf;         // MXFP8: scales of xg in blocked 512-byte tiles (S_max * D/32 bytes)
   void* act_sf;        // MXFP8: scales of act in blocked tiles (S_max * H/32 bytes)
   size_t bytes;        // total bytes required
@@ -92,6 +93,16 @@ cudaError_t launch_up_bf16(const CUtensorMap& map_a, const CUtensorMap& map_w1, 
 // tile (tiles = block pairs x column tiles).
 cudaError_t launch_up_pair_bf16(const CUtensorMap& map_a, const CUtensorMap& map_w1, const GemmArgs& args, int grid,
                                 cudaStream_t stream);
+// The split GEMMs on CTA pairs (cta_group::2): tiles are (block pair, column
+// tile); n_pairs pairs of CTAs are launched as two-CTA clusters.  Up: fold
+// 128, map_w1 boxes of 128 rows.  Down: 256-column tiles, map_w2 boxes of 128
+// rows.
+cudaError_t launch_up_pair2_bf16(const CUtensorMap& map_xg, const CUtensorMap& map_w1, const GemmArgs& args,
+                                 int n_pairs, cudaStream_t stream, bool pdl);
+cudaError_t launch_down_pair2_bf16(const CUtensorMap& map_act, const CUtensorMap& map_w2, const GemmArgs& args,
+                                   int n_pairs, cudaStream_t stream, bool pdl);
+// Co-resident two-CTA clusters of the pair kernels on the current device.
+int pair_cluster_slots();
 // n = output columns per tile: kDownN, or kDownNNarrow when D % 256 != 0;
 // map_w2's boxes must be n rows.
 cudaError_t launch_down_bf16(const CUtensorMap& map_act, const CUtensorMap& map_w2, const GemmArgs& args, int grid,
@@ -149,6 +160,35 @@ inline bool fused_cluster_ok(int D, int H) {
     if (fused_cluster_h1(D, H, C)) return true;
   return false;
 }
+// MXFP8 fused pipeline on clusters: act slices of 128 columns (one scale tile
+// of K), GEMM2 sub-chunks of 256 output columns.
+struct FusedClusterMxArgs {
+  const int* meta;
+  const int* expert_of_rb;
+  const int* row_tok;
+  const float* slot_w;
+  void* out;                // bf16 [T, D], zeroed before the launch
+  void* ring;               // e4m3 [n_clusters * 2 * 128, H]
+  void* ring_sf;            // blocked scale tiles of the ring: [n_clusters * 2][H / 128] x 512 B
+  const void* xg_sf;        // blocked scale tiles of xg
+  const void* w1_sf;        // packed W1 scales
+  const void* w2_sf;        // packed W2 scales
+  int* err;
+  unsigned long long wait_limit_ns;
+  int D, H;
+  int csize;                // CTAs per cluster C (1, 2, 4 or 8)
+  int s1;                   // GEMM1 sub-chunks per CTA: 128 * s1 = H / C
+  int s2;                   // GEMM2 sub-chunks per CTA: 256 * s2 = D / C
+  int stall_test;           // test hook (see GemmArgs)
+};
+inline bool fused_cluster_mx_fits(int D, int H, int C) {
+  return (C == 1 || C == 2 || C == 4 || C == 8) && D % (256 * C) == 0 && H % (128 * C) == 0;
+}
+int fused_cluster_mx_max_clusters(int csize);
+cudaError_t launch_fused_cluster_mxfp8(const CUtensorMap& map_xg, const CUtensorMap& map_w1,
+                                       const CUtensorMap& map_w2, const CUtensorMap& map_ring,
+                                       const FusedClusterMxArgs& args, int n_clusters, cudaStream_t stream);
+
 // Co-resident clusters of size csize on the current device (0 on failure).
 int fused_cluster_max_clusters(int csize);
 cudaError_t launch_fused_cluster_bf16(const CUtensorMap& map_xg, const CUtensorMap& map_w1, const CUtensorMap& map_w2,

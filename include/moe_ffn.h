@@ -200,7 +200,17 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   fit on the device; 2, 4 or 8 request that size (automatic
  *                   when it does not apply).  With 0 (or a shape no C fits)
  *                   the fused pipeline splits H over CTAs and sums partial
- *                   rows in an fp32 buffer. */
+ *                   rows in an fp32 buffer.
+ *   MOE_OPT_PAIR_MMA  2 (default: automatic), 1 or 0: with 1 the bf16 split
+ *                   pipeline's up and down GEMMs run on CTA pairs (two-CTA
+ *                   clusters sharing one tcgen05 MMA of 256 rows,
+ *                   cta_group::2): each CTA loads half of every weight tile, a
+ *                   third fewer operand bytes per FLOP.  Two row blocks of one
+ *                   expert form a tile; an expert with an odd number of row
+ *                   blocks pays one idle half.  2 uses pairs unless the
+ *                   problem is decode-sized (fewer than about eight waves of
+ *                   up tiles).  Measured on GB300: prefill 0.360 -> 0.335 ms,
+ *                   large_skewed 7.47 -> 6.83 ms, decode unchanged. */
 typedef enum {
   MOE_OPT_GATHER = 0,
   MOE_OPT_L2_PREFETCH = 1,
@@ -209,7 +219,8 @@ typedef enum {
   MOE_OPT_DYNAMIC_TILES = 4,
   MOE_OPT_TILE_COLS = 5,
   MOE_OPT_SWAP_AB = 6,
-  MOE_OPT_FUSED_CLUSTER = 7
+  MOE_OPT_FUSED_CLUSTER = 7,
+  MOE_OPT_PAIR_MMA = 8
 } moe_option_t;
 moe_status_t moe_ffn_set_option(int option, long long value);
 

@@ -21,21 +21,25 @@ def oracle_out(inp):
     return oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], inp["topk_ids"], inp["topk_w"], act=oracle.ACT_BF16)
 
 
-# (pipeline, MOE_OPT_FUSED_CLUSTER): split; fused on clusters of two CTAs
-# (D = 512); fused with H-split fp32 partial sums
-@pytest.mark.parametrize("pipeline,cluster", [(moe.MOE_SPLIT, 1), (moe.MOE_FUSED, 1), (moe.MOE_FUSED, 0)])
-def test_wait_timeout_is_reported_and_context_survives(pipeline, cluster):
+# (pipeline, MOE_OPT_FUSED_CLUSTER, MOE_OPT_PAIR_MMA): split on single CTAs and
+# on CTA pairs; fused on clusters of two CTAs (D = 512); fused with H-split
+# fp32 partial sums
+@pytest.mark.parametrize("pipeline,cluster,pair", [(moe.MOE_SPLIT, 1, 0), (moe.MOE_SPLIT, 1, 1),
+                                                   (moe.MOE_FUSED, 1, 2), (moe.MOE_FUSED, 0, 2)])
+def test_wait_timeout_is_reported_and_context_survives(pipeline, cluster, pair):
     inp = wl.make_custom(300, 512, 256, 16, 4, seed=3)
     dev = to_dev(inp)
     moe.moe_ffn_set_wait_limit_ns(1_000_000)
     moe.moe_ffn_set_option(moe.MOE_OPT_TEST_STALL, 1)
     moe.moe_ffn_set_option(moe.MOE_OPT_FUSED_CLUSTER, cluster)
+    moe.moe_ffn_set_option(moe.MOE_OPT_PAIR_MMA, pair)
     try:
         _, ws = run_forward(inp, dev, pipeline=pipeline, check_status=False)
         st = moe.moe_ffn_sync_status(ws)
     finally:
         moe.moe_ffn_set_option(moe.MOE_OPT_TEST_STALL, 0)
         moe.moe_ffn_set_option(moe.MOE_OPT_FUSED_CLUSTER, 1)
+        moe.moe_ffn_set_option(moe.MOE_OPT_PAIR_MMA, 2)
         moe.moe_ffn_set_wait_limit_ns(2_000_000_000)
     assert st == 6, moe.moe_ffn_status_string(st)
     assert moe.moe_ffn_sync_status(ws) == 0          # status words cleared by the read

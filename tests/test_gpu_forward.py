@@ -20,19 +20,22 @@ pytestmark = pytest.mark.gpu
 
 # Pipeline and option settings under test: the split pipeline with the
 # materializing gather kernel (default), with in-kernel gathers, with two row
-# blocks per up tile and with the tail row blocks run as swap-AB tiles; the
+# blocks per up tile, with the tail row blocks run as swap-AB tiles and with
+# both GEMMs on CTA pairs; the
 # fused pipeline on clusters (default where the shape allows) and with the
 # H-split fp32 partial sums.
 MODES = {
-    "split": (moe.MOE_SPLIT, {}),
+    "split": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 0}),
     "split_pairs": (moe.MOE_SPLIT, {moe.MOE_OPT_UP_PAIRS: 1}),
     "split_gather4": (moe.MOE_SPLIT, {moe.MOE_OPT_GATHER: 1}),
     "split_cpasync": (moe.MOE_SPLIT, {moe.MOE_OPT_GATHER: 2}),
     "split_swap": (moe.MOE_SPLIT, {moe.MOE_OPT_SWAP_AB: 1}),
+    "split_pair2": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 1}),
     "fused": (moe.MOE_FUSED, {}),
     "fused_splitk": (moe.MOE_FUSED, {moe.MOE_OPT_FUSED_CLUSTER: 0}),
 }
-DEFAULTS = {moe.MOE_OPT_UP_PAIRS: 0, moe.MOE_OPT_GATHER: 0, moe.MOE_OPT_SWAP_AB: 0, moe.MOE_OPT_FUSED_CLUSTER: 1}
+DEFAULTS = {moe.MOE_OPT_UP_PAIRS: 0, moe.MOE_OPT_GATHER: 0, moe.MOE_OPT_SWAP_AB: 0, moe.MOE_OPT_FUSED_CLUSTER: 1,
+            moe.MOE_OPT_PAIR_MMA: 2}
 PIPELINES = list(MODES)
 
 
@@ -142,7 +145,7 @@ def test_unsupported_combinations_rejected():
 @pytest.mark.parametrize("name,n_sample", [("decode", None), ("prefill", 96), ("large_skewed", 40)])
 @pytest.mark.parametrize("pipeline", PIPELINES)
 def test_forward_full_workload_sampled(name, n_sample, pipeline):
-    if name == "large_skewed" and pipeline not in ("split", "fused", "fused_splitk"):
+    if name == "large_skewed" and pipeline not in ("split", "fused", "fused_splitk", "split_pair2"):
         pytest.skip("option variants are covered at the smaller sizes")
     inp = wl.make_inputs(name, seed=0)
     out, _ = run_mode(inp, to_dev(inp), pipeline)

@@ -77,7 +77,9 @@ def test_weight_scale_repacking_layout():
     assert np.array_equal(p2.cpu().numpy(), expected(w2_sf))
 
 
-def run_mx(inp, pipeline=moe.MOE_SPLIT):
+def run_mx(inp, pipeline=moe.MOE_SPLIT, cluster=1):
+    """cluster: MOE_OPT_FUSED_CLUSTER for the call (1 automatic, 2/4/8 that
+    size, 0 the fused kernel with fp32 partial sums)."""
     w = inp["workload"]
     dev = {k: torch.from_numpy(inp[k]).cuda() for k in ("x", "x_sf", "w1", "w2")}
     w1p = torch.empty(inp["w1_sf"].size, dtype=torch.uint8, device="cuda")
@@ -88,8 +90,12 @@ def run_mx(inp, pipeline=moe.MOE_SPLIT):
     tw = torch.from_numpy(inp["topk_w"]).cuda()
     out = torch.full((w.T, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
     ws = moe.alloc_workspace(w.T, w.E, w.D, w.H, w.k, moe.MOE_MXFP8, pipeline)
-    moe.moe_ffn_forward(dev["x"], dev["w1"], dev["w2"], ids, tw, out, E=w.E, D=w.D, H=w.H, k=w.k, workspace=ws,
-                        dtype=moe.MOE_MXFP8, pipeline=pipeline, x_sf=dev["x_sf"], w1_sf=w1p, w2_sf=w2p)
+    moe.moe_ffn_set_option(moe.MOE_OPT_FUSED_CLUSTER, cluster)
+    try:
+        moe.moe_ffn_forward(dev["x"], dev["w1"], dev["w2"], ids, tw, out, E=w.E, D=w.D, H=w.H, k=w.k, workspace=ws,
+                            dtype=moe.MOE_MXFP8, pipeline=pipeline, x_sf=dev["x_sf"], w1_sf=w1p, w2_sf=w2p)
+    finally:
+        moe.moe_ffn_set_option(moe.MOE_OPT_FUSED_CLUSTER, 1)
     st = moe.moe_ffn_sync_status(ws)
     assert st == 0, moe.moe_ffn_status_string(st)
     return out
@@ -100,7 +106,8 @@ def oracle_mx(inp, tokens=None):
                           x_sf=inp["x_sf"], w1_sf=inp["w1_sf"], w2_sf=inp["w2_sf"], tokens=tokens)
 
 
-PIPES = {"split": moe.MOE_SPLIT, "fused": moe.MOE_FUSED}
+# fused: on clusters (automatic size); fused_splitk: H split over CTAs with fp32 partial sums
+PIPES = {"split": (moe.MOE_SPLIT, 1), "fused": (moe.MOE_FUSED, 1), "fused_splitk": (moe.MOE_FUSED, 0)}
 
 
 @pytest.mark.parametrize("pipe", list(PIPES))
@@ -113,7 +120,7 @@ PIPES = {"split": moe.MOE_SPLIT, "fused": moe.MOE_FUSED}
 ])
 def test_mxfp8_forward_small(T, D, H, E, k, routing, pipe):
     inp = wl.make_custom(T, D, H, E, k, seed=T + H, routing=routing, dtype="mxfp8")
-    out = run_mx(inp, PIPES[pipe])
+    out = run_mx(inp, *PIPES[pipe])
     r = assert_close(out, oracle_mx(inp), dtype="mxfp8", label=f"mxfp8 {pipe} T={T} D={D} H={H}")
     print(f"mxfp8 {pipe} T={T} D={D} H={H} E={E} k={k}: max_rel={r[0]:.2e} mean_rel={r[1]:.2e} cos={r[2]:.6f}")
 
@@ -121,9 +128,23 @@ def test_mxfp8_forward_small(T, D, H, E, k, routing, pipe):
 @pytest.mark.parametrize("pipe", list(PIPES))
 def test_mxfp8_full_workload_sampled(pipe):
     inp = wl.make_inputs("mxfp8", seed=0)
-    out = run_mx(inp, PIPES[pipe])
+    out = run_mx(inp, *PIPES[pipe])
     tokens = np.sort(np.random.default_rng(2).choice(inp["workload"].T, 48, replace=False)).astype(np.int32)
     r = assert_close(out[torch.from_numpy(tokens.astype(np.int64)).cuda()], oracle_mx(inp, tokens), dtype="mxfp8",
                      label="mxfp8 workload")
     print(f"mxfp8 workload: max_rel={r[0]:.2e} mean_rel={r[1]:.2e} cos={r[2]:.6f}")
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("csize", [2, 4, 8])
+@pytest.mark.parametrize("T,D,H,E,k", [
+    (512, 1024, 512, 16, 8),     # several GEMM1 and GEMM2 sub-chunks per CTA
+    (1000, 2048, 1024, 8, 8),    # ~8 row blocks per expert: each ring buffer reused
+])
+def test_mxfp8_fused_cluster_sizes(T, D, H, E, k, csize):
+    if D % (256 * csize) or H % (128 * csize):
+        pytest.skip("cluster size does not apply to this shape")
+    inp = wl.make_custom(T, D, H, E, k, seed=T + D, routing="uniform", dtype="mxfp8")
+    out = run_mx(inp, moe.MOE_FUSED, cluster=csize)
+    r = assert_close(out, oracle_mx(inp), dtype="mxfp8", label=f"mxfp8 fused C={csize} T={T} D={D} H={H}")
+    print(f"mxfp8 fused C={csize} T={T} D={D} H={H} E={E} k={k}: max_rel={r[0]:.2e} mean_rel={r[1]:.2e}")
