@@ -47,7 +47,12 @@ def parse_args():
     ap.add_argument("--pipeline", choices=["split", "fused"], default="split")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--from-logits", action="store_true",
+                    help="start each step from router logits [T, E] (moe_ffn_forward_logits: top-k and softmax "
+                         "fused into the routing launch) instead of given top-k ids and weights")
     ap.add_argument("--no-graph", action="store_true", help="launch each step eagerly instead of replaying a CUDA graph")
+    ap.add_argument("--option", action="append", default=[], metavar="NAME=VALUE",
+                    help="library tuning option, e.g. PAIR_TAILS=0 (moe_ffn_set_option; repeatable)")
     return ap.parse_args()
 
 
@@ -89,15 +94,21 @@ def source_digest(files):
     return h.hexdigest()[:16]
 
 
-_BF16_SRC = ["grouped_gemm_gb300/csrc/gemm_bf16.cu", "grouped_gemm_gb300/csrc/ptx.cuh",
-             "grouped_gemm_gb300/csrc/internal.h"]
-_MX_SRC = ["grouped_gemm_gb300/csrc/gemm_mxfp8.cu", "grouped_gemm_gb300/csrc/mx.cuh", "grouped_gemm_gb300/csrc/ptx.cuh",
-           "grouped_gemm_gb300/csrc/internal.h"]
+_PTX = ["grouped_gemm_gb300/csrc/ptx.cuh", "grouped_gemm_gb300/csrc/internal.h"]
+_MXH = ["grouped_gemm_gb300/csrc/mx.cuh"]
+# kernel name (moe_ffn_profile_stage_kernel) -> the sources it is built from
 KERNEL_SOURCES = {
-    "up_swiglu": _BF16_SRC, "down_reduce": _BF16_SRC,
-    "up_swiglu_mxfp8": _MX_SRC, "down_reduce_mxfp8": _MX_SRC,
-    "fused_gemm": ["grouped_gemm_gb300/csrc/gemm_fused.cu", "grouped_gemm_gb300/csrc/ptx.cuh",
-                   "grouped_gemm_gb300/csrc/internal.h"],
+    "up_swiglu_bf16": ["grouped_gemm_gb300/csrc/gemm_bf16.cu"] + _PTX,
+    "down_reduce_bf16": ["grouped_gemm_gb300/csrc/gemm_bf16.cu"] + _PTX,
+    "up_swiglu_pair2": ["grouped_gemm_gb300/csrc/gemm_pair2.cu"] + _PTX,
+    "down_reduce_pair2": ["grouped_gemm_gb300/csrc/gemm_pair2.cu"] + _PTX,
+    "up_pair_bf16": ["grouped_gemm_gb300/csrc/gemm_pair.cu"] + _PTX,
+    "up_swiglu_mxfp8": ["grouped_gemm_gb300/csrc/gemm_mxfp8.cu"] + _MXH + _PTX,
+    "down_reduce_mxfp8": ["grouped_gemm_gb300/csrc/gemm_mxfp8.cu"] + _MXH + _PTX,
+    "fused_cluster_bf16": ["grouped_gemm_gb300/csrc/gemm_fused_cluster.cu"] + _PTX,
+    "fused_moe_bf16": ["grouped_gemm_gb300/csrc/gemm_fused.cu"] + _PTX,
+    "fused_cluster_mxfp8": ["grouped_gemm_gb300/csrc/gemm_fused_cluster_mx.cu"] + _MXH + _PTX,
+    "fused_moe_mxfp8": ["grouped_gemm_gb300/csrc/gemm_fused_mx.cu"] + _MXH + _PTX,
 }
 
 
@@ -186,6 +197,9 @@ def run_ours(args, rank, world, local_rank):
     from grouped_gemm_gb300 import workloads as wl
 
     torch.cuda.set_device(local_rank)
+    for opt in args.option:
+        name, val = opt.split("=")
+        moe.moe_ffn_set_option(getattr(moe, "MOE_OPT_" + name.upper()), int(val))
     inp = wl.make_inputs(args.workload, seed=rank)
     w = inp["workload"]
     mx = w.dtype == "mxfp8"
@@ -199,12 +213,21 @@ def run_ours(args, rank, world, local_rank):
                                           dev["w1_sf"], dev["w2_sf"], w.E, w.D, w.H)
     ids = torch.from_numpy(inp["topk_ids"]).cuda()
     tw = torch.from_numpy(inp["topk_w"]).cuda()
+    logits = None
+    if args.from_logits:  # the router's input; ids and weights become the call's outputs
+        logits_np = wl.router_logits(w.T, w.E, seed=1000 + rank)
+        logits = torch.from_numpy(logits_np).cuda()
     out = torch.empty(w.T, w.D, dtype=torch.bfloat16, device="cuda")
     pipeline = moe.MOE_SPLIT if args.pipeline == "split" else moe.MOE_FUSED
     ws = moe.alloc_workspace(w.T, w.E, w.D, w.H, w.k, dtype, pipeline)
     stream = torch.cuda.current_stream()
 
     def step():  # one forward pass on the current stream
+        if logits is not None:
+            moe.moe_ffn_forward_logits(dev["x"], dev["w1"], dev["w2"], logits, ids, tw, out, E=w.E, D=w.D, H=w.H,
+                                       k=w.k, workspace=ws, dtype=dtype, pipeline=pipeline, x_sf=dev.get("x_sf"),
+                                       w1_sf=dev.get("w1_sf"), w2_sf=dev.get("w2_sf"))
+            return
         moe.moe_ffn_forward(dev["x"], dev["w1"], dev["w2"], ids, tw, out, E=w.E, D=w.D, H=w.H, k=w.k,
                             workspace=ws, dtype=dtype, pipeline=pipeline, x_sf=dev.get("x_sf"),
                             w1_sf=dev.get("w1_sf"), w2_sf=dev.get("w2_sf"))
@@ -233,6 +256,8 @@ def run_ours(args, rank, world, local_rank):
     st = moe.moe_ffn_sync_status(ws)
     if st != 0:
         raise SystemExit(f"device status after warm-up: {moe.moe_ffn_status_string(st)}")
+    if logits is not None:  # the experts the router picked set the algorithmic bytes
+        inp["topk_ids"] = ids.cpu().numpy()
 
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     time.sleep(0.3)
@@ -275,8 +300,9 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(min(args.steps, 30)):
         step()
         per.append(moe.moe_ffn_profile_read())
-    moe.moe_ffn_profile_enable(False)
     names = STAGES[args.pipeline]
+    stage_kernels = {name: moe.moe_ffn_profile_stage_kernel(i) for i, name in enumerate(names)}
+    moe.moe_ffn_profile_enable(False)
     stage_ms = {name: statistics.median(p[i] for p in per) for i, name in enumerate(names) if len(per[0]) > i}
 
     peaks, peak_src = load_peaks()
@@ -298,11 +324,12 @@ def run_ours(args, rank, world, local_rank):
         achieved, peak, unit = kd["flops"] / t_dom / 1e12, peaks["bf16_tflops"], "TFLOP/s"
     else:
         achieved, peak, unit = kd["bytes"] / t_dom / 1e9, peaks["hbm_gbs"], "GB/s"
-    roofline = {"bound": "tensor" if tensor_bound else "hbm", "kernel": dom, "achieved": round(achieved, 1),
+    kname = stage_kernels[dom]
+    roofline = {"bound": "tensor" if tensor_bound else "hbm", "kernel": kname, "achieved": round(achieved, 1),
                 "peak": peak, "peak_source": peak_src, "unit": unit, "frac": round(achieved / peak, 4),
-                "traffic": traffic_from_profiles(dom + ("_mxfp8" if mx and dom != "fused_gemm" else ""), args.workload),
+                "traffic": traffic_from_profiles(kname, args.workload),
                 "algorithmic_per_launch": kd["flops"] if tensor_bound else kd["bytes"],
-                "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()}}
+                "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()}, "stage_kernels": stage_kernels}
     step_bound = max(alg["step_flops"] / (peaks["bf16_tflops"] * 1e12), alg["step_bytes"] / (peaks["hbm_gbs"] * 1e9))
 
     # end to end: host buffers, copies inside the timed region
@@ -312,14 +339,18 @@ def run_ours(args, rank, world, local_rank):
         xsfh = torch.from_numpy(inp["x_sf"]).pin_memory() if mx else None
         idh = torch.from_numpy(inp["topk_ids"]).pin_memory()
         twh = torch.from_numpy(inp["topk_w"]).pin_memory()
+        lgh = torch.from_numpy(logits_np).pin_memory() if logits is not None else None
         outh = torch.empty(w.T, w.D, dtype=torch.bfloat16).pin_memory()
 
         def e2e_step():
             dev["x"].copy_(xh, non_blocking=True)
             if mx:
                 dev["x_sf"].copy_(xsfh, non_blocking=True)
-            ids.copy_(idh, non_blocking=True)
-            tw.copy_(twh, non_blocking=True)
+            if logits is not None:
+                logits.copy_(lgh, non_blocking=True)
+            else:
+                ids.copy_(idh, non_blocking=True)
+                tw.copy_(twh, non_blocking=True)
             step()
             outh.copy_(out, non_blocking=True)
 
@@ -337,7 +368,7 @@ def run_ours(args, rank, world, local_rank):
         e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world, device="cuda")
         e2e = {"value": round(flops_all / (e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(xh.numel() * xh.element_size() + (xsfh.numel() if mx else 0) +
-                                         idh.numel() * 4 + twh.numel() * 4),
+                                         (lgh.numel() * 4 if logits is not None else idh.numel() * 4 + twh.numel() * 4)),
                "d2h_bytes_per_step": int(outh.numel() * 2), "ms_per_step": round(e_ms, 4),
                "resident": "expert weights stay in HBM (model parameters)"}
 
@@ -360,6 +391,8 @@ def run_ours(args, rank, world, local_rank):
         "roofline_step_frac": round(step_bound / (ms * 1e-3), 4),
         "config": {"workload": w.name, "T": w.T, "D": w.D, "H": w.H, "E": w.E, "k": w.k, "routing": w.routing,
                    "pipeline": args.pipeline, "seed": "rank", "parallelism": f"token-sharded x{world}",
+                   "options": args.option,
+                   "routing_input": "router logits [T, E] fp32" if args.from_logits else "top-k ids and weights",
                    "launch": "eager" if graph is None else "CUDA graph replay of one step",
                    "l2": (f"inputs larger than L2: {alg['step_bytes'] / 1e9:.2f} GB compulsory per step "
                           f"(129 MB L2), no flush needed")},

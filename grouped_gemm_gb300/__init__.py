@@ -14,8 +14,8 @@ import threading
 
 __all__ = [
     "MOE_BF16", "MOE_MXFP8", "MOE_FUSED", "MOE_SPLIT", "MoeFFNError", "library_path", "lib",
-    "moe_ffn_workspace_size", "moe_ffn_workspace_init", "moe_ffn_forward", "moe_ffn_route", "moe_ffn_route_noalloc",
-    "moe_ffn_sync_status", "moe_ffn_set_wait_limit_ns", "moe_ffn_profile_enable", "moe_ffn_profile_read", "moe_ffn_set_option", "MOE_OPT_GATHER", "moe_ffn_prepare_mxfp8_weights", "moe_ffn_debug_mx_quantize", "moe_ffn_status_string", "alloc_workspace",
+    "moe_ffn_workspace_size", "moe_ffn_workspace_init", "moe_ffn_forward", "moe_ffn_forward_logits", "moe_ffn_router_topk", "moe_ffn_route", "moe_ffn_route_noalloc",
+    "moe_ffn_sync_status", "moe_ffn_set_wait_limit_ns", "moe_ffn_profile_enable", "moe_ffn_profile_read", "moe_ffn_profile_stage_kernel", "moe_ffn_set_option", "MOE_OPT_GATHER", "moe_ffn_prepare_mxfp8_weights", "moe_ffn_debug_mx_quantize", "moe_ffn_status_string", "alloc_workspace",
 ]
 
 MOE_BF16, MOE_MXFP8 = 0, 1
@@ -55,6 +55,10 @@ def lib() -> ctypes.CDLL:
             L.moe_ffn_workspace_init.restype = i
             L.moe_ffn_forward.argtypes = [vp] * 9 + [i] * 7 + [vp, sz, vp]
             L.moe_ffn_forward.restype = i
+            L.moe_ffn_router_topk.argtypes = [vp, i, i, i, vp, vp, vp]
+            L.moe_ffn_router_topk.restype = i
+            L.moe_ffn_forward_logits.argtypes = [vp] * 10 + [i] * 7 + [vp, sz, vp]
+            L.moe_ffn_forward_logits.restype = i
             L.moe_ffn_route.argtypes = [vp, vp, i, i, i, vp, vp, vp, vp, sz, vp]
             L.moe_ffn_route.restype = i
             L.moe_ffn_route_noalloc.argtypes = [vp, vp, i, i, i, vp, vp, vp, vp, vp]
@@ -73,6 +77,8 @@ def lib() -> ctypes.CDLL:
             L.moe_ffn_profile_enable.restype = i
             L.moe_ffn_profile_read.argtypes = [c.POINTER(c.c_float), i, c.POINTER(c.c_int)]
             L.moe_ffn_profile_read.restype = i
+            L.moe_ffn_profile_stage_kernel.argtypes = [i]
+            L.moe_ffn_profile_stage_kernel.restype = c.c_char_p
             L.moe_ffn_status_string.argtypes = [i]
             L.moe_ffn_status_string.restype = c.c_char_p
             _lib = L
@@ -137,6 +143,26 @@ def moe_ffn_forward(x, w1, w2, topk_ids, topk_w, out, *, E, D, H, k, workspace, 
     return _check(st, "moe_ffn_forward") if check else st
 
 
+def moe_ffn_forward_logits(x, w1, w2, router_logits, topk_ids, topk_w, out, *, E, D, H, k, workspace,
+                           dtype=MOE_BF16, pipeline=MOE_SPLIT, x_sf=None, w1_sf=None, w2_sf=None, T=None,
+                           stream=None, check=True) -> int:
+    """moe_ffn_forward from router logits [T, E] fp32; topk_ids / topk_w [T, k]
+    are written by the call."""
+    T = x.shape[0] if T is None else T
+    st = lib().moe_ffn_forward_logits(_p(x), _p(x_sf), _p(w1), _p(w1_sf), _p(w2), _p(w2_sf), _p(router_logits),
+                                      _p(topk_ids), _p(topk_w), _p(out), T, E, D, H, k, dtype, pipeline,
+                                      _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    return _check(st, "moe_ffn_forward_logits") if check else st
+
+
+def moe_ffn_router_topk(logits, k, topk_ids, topk_w, T=None, E=None, stream=None, check=True) -> int:
+    """Top-k experts and softmax-renormalized weights of router logits [T, E]."""
+    T = logits.shape[0] if T is None else T
+    E = logits.shape[1] if E is None else E
+    st = lib().moe_ffn_router_topk(_p(logits), T, E, k, _p(topk_ids), _p(topk_w), _stream(stream))
+    return _check(st, "moe_ffn_router_topk") if check else st
+
+
 def moe_ffn_route(topk_ids, topk_w, T, E, k, counts, offsets, slot_of_pair, workspace, stream=None,
                   check=True) -> int:
     st = lib().moe_ffn_route(_p(topk_ids), _p(topk_w), T, E, k, _p(counts), _p(offsets), _p(slot_of_pair),
@@ -194,6 +220,12 @@ def moe_ffn_profile_read() -> list:
     n = ctypes.c_int(0)
     _check(lib().moe_ffn_profile_read(buf, 8, ctypes.byref(n)), "moe_ffn_profile_read")
     return [float(buf[i]) for i in range(n.value)]
+
+
+def moe_ffn_profile_stage_kernel(stage: int):
+    """Main kernel of one stage of the most recent profiled call (None if absent)."""
+    r = lib().moe_ffn_profile_stage_kernel(int(stage))
+    return None if r is None else r.decode()
 
 
 def moe_ffn_set_wait_limit_ns(ns: int) -> None:

@@ -90,6 +90,7 @@ struct Profile {
   bool created = false;
   cudaEvent_t ev[kMaxProfileEvents] = {};
   int recorded = 0;  // events recorded by the last profiled call
+  const char* kernel[kMaxProfileEvents] = {};  // main kernel of each stage of the last profiled call
 } g_prof;
 
 // Record the next stage boundary of the current call (no-op when disabled).
@@ -97,6 +98,18 @@ void prof_mark(cudaStream_t st, int idx) {
   if (!g_prof.on || !g_prof.created || idx >= kMaxProfileEvents) return;
   cudaEventRecord(g_prof.ev[idx], st);
   g_prof.recorded = idx + 1;
+}
+
+// Name the main kernel of a stage of the current call (no-op when disabled).
+void prof_kernel(int stage, const char* name) {
+  if (!g_prof.on || stage < 0 || stage >= kMaxProfileEvents) return;
+  g_prof.kernel[stage] = name;
+}
+
+// The routing and gather stages, common to every pipeline.
+void prof_front(bool mx) {
+  prof_kernel(0, "route");
+  prof_kernel(1, mx ? "gather_rows_mx" : "gather_tokens");
 }
 
 }  // namespace
@@ -232,6 +245,9 @@ moe_status_t forward_fused_cluster_bf16(const Workspace& ws, const void* x, cons
   fa.s1 = H / C / h1;
   fa.s2 = D / C / kFusedClusterN;
   fa.stall_test = g_stall_test.load();
+  prof_front(false);
+  prof_kernel(2, "fused_cluster_bf16");
+  prof_kernel(3, "none");
   e = launch_fused_cluster_bf16(map_xg, map_w1, map_w2, map_ring, fa, ncl, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 3);
@@ -275,6 +291,9 @@ moe_status_t forward_fused_bf16(const Workspace& ws, const void* x, const void* 
   fa.n_slices = H / 128;
   fa.stall_test = g_stall_test.load();
   const int grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * fa.n_slices);
+  prof_front(false);
+  prof_kernel(2, "fused_moe_bf16");
+  prof_kernel(3, "f32_to_bf16");
   e = launch_fused_bf16(map_xg, map_w1, map_w2, fa, grid, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 3);
@@ -321,6 +340,9 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
   up.sf_b = w1_sf;
   up.n_col_tiles = H / 128;
   up.k_blocks = D / 128;
+  prof_front(true);
+  prof_kernel(2, "up_swiglu_mxfp8");
+  prof_kernel(3, "down_reduce_mxfp8");
   e = launch_up_mxfp8(map_xg, map_w1, up, (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * up.n_col_tiles), st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 3);
@@ -397,6 +419,9 @@ moe_status_t forward_fused_cluster_mxfp8(const Workspace& ws, const void* x, con
   fa.s1 = H / C / 128;
   fa.s2 = D / C / 256;
   fa.stall_test = g_stall_test.load();
+  prof_front(true);
+  prof_kernel(2, "fused_cluster_mxfp8");
+  prof_kernel(3, "none");
   e = launch_fused_cluster_mxfp8(map_xg, map_w1, map_w2, map_ring, fa, ncl, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 3);
@@ -446,6 +471,9 @@ moe_status_t forward_fused_mxfp8(const Workspace& ws, const void* x, const void*
   fa.H = H;
   fa.stall_test = g_stall_test.load();
   const int grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * (H / 128));
+  prof_front(true);
+  prof_kernel(2, "fused_moe_mxfp8");
+  prof_kernel(3, "f32_to_bf16");
   e = launch_fused_mxfp8(map_xg, map_w1, map_w2, fa, grid, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 3);
@@ -497,6 +525,7 @@ moe_status_t moe_ffn_set_option(int option, long long value) {
       if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
       g_swap_ab.store((int)value);
       return MOE_OK;
+
     case MOE_OPT_TILE_COLS:
       if (value != 0 && value != 128 && value != 256) return MOE_ERR_INVALID_ARG;
       g_tile_cols.store((int)value);
@@ -540,10 +569,12 @@ moe_status_t moe_ffn_route(const int32_t* topk_ids, const float* topk_w, int T, 
   return cuda_status(e);
 }
 
-moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, const void* w1_sf, const void* w2,
-                             const void* w2_sf, const int32_t* topk_ids, const float* topk_w, void* out, int T, int E,
-                             int D, int H, int k, int dtype, int pipeline, void* workspace, size_t workspace_bytes,
-                             void* stream) {
+// The forward pass from top-k ids and weights, or (router_logits != nullptr)
+// from router logits, the routing launch writing topk_ids / topk_w first.
+static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w1, const void* w1_sf, const void* w2,
+                                  const void* w2_sf, const int32_t* topk_ids, const float* topk_w, void* out, int T,
+                                  int E, int D, int H, int k, int dtype, int pipeline, void* workspace,
+                                  size_t workspace_bytes, void* stream, const float* router_logits) {
   if (!shape_ok(T, E, D, H, k)) return MOE_ERR_INVALID_ARG;
   if (dtype != MOE_BF16 && dtype != MOE_MXFP8) return MOE_ERR_INVALID_ARG;
   if (pipeline != MOE_FUSED && pipeline != MOE_SPLIT) return MOE_ERR_INVALID_ARG;
@@ -561,6 +592,7 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   if (D % kDownN != 0 && (dtype != MOE_BF16 || pipeline != MOE_SPLIT)) return MOE_ERR_UNSUPPORTED;
   Workspace ws = plan_workspace(workspace, T, E, D, H, k, pipeline, dtype);
   if (workspace_bytes < ws.bytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  ws.router_logits = router_logits;
   const int sms = num_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -641,6 +673,9 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   up.x = x;
   const int pair_slots = pair_mma ? pair_cluster_slots() : 0;
   if (pair_mma && pair_slots <= 0) return MOE_ERR_CUDA;
+  prof_front(false);
+  prof_kernel(2, pair_mma ? "up_swiglu_pair2" : (gather == 0 && g_up_pairs.load()) ? "up_pair_bf16" : "up_swiglu_bf16");
+  prof_kernel(3, pair_down ? "down_reduce_pair2" : "down_reduce_bf16");
   if (pair_mma)
     e = launch_up_pair2_bf16(map_xg, map_w1, up,
                              (int)std::min<int64_t>(pair_slots, (int64_t)ws.max_rb * up.n_col_tiles), st, !g_prof.on);
@@ -666,6 +701,36 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
   return cuda_status(e);
 }
 
+moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, const void* w1_sf, const void* w2,
+                             const void* w2_sf, const int32_t* topk_ids, const float* topk_w, void* out, int T, int E,
+                             int D, int H, int k, int dtype, int pipeline, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  return forward_entry(x, x_sf, w1, w1_sf, w2, w2_sf, topk_ids, topk_w, out, T, E, D, H, k, dtype, pipeline,
+                       workspace, workspace_bytes, stream, nullptr);
+}
+
+moe_status_t moe_ffn_forward_logits(const void* x, const void* x_sf, const void* w1, const void* w1_sf,
+                                    const void* w2, const void* w2_sf, const float* router_logits,
+                                    int32_t* topk_ids, float* topk_w, void* out, int T, int E, int D, int H, int k,
+                                    int dtype, int pipeline, void* workspace, size_t workspace_bytes, void* stream) {
+  if (k > E) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && !router_logits) return MOE_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(router_logits) & 3u) return MOE_ERR_MISALIGNED;
+  return forward_entry(x, x_sf, w1, w1_sf, w2, w2_sf, topk_ids, topk_w, out, T, E, D, H, k, dtype, pipeline,
+                       workspace, workspace_bytes, stream, router_logits);
+}
+
+moe_status_t moe_ffn_router_topk(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w,
+                                 void* stream) {
+  if (T < 0 || E < 1 || E > kMaxExperts || k < 1 || k > E) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(logits) & 3u) || (reinterpret_cast<uintptr_t>(topk_ids) & 3u) ||
+      (reinterpret_cast<uintptr_t>(topk_w) & 3u))
+    return MOE_ERR_MISALIGNED;
+  return cuda_status(launch_router_topk(logits, T, E, k, topk_ids, topk_w, static_cast<cudaStream_t>(stream)));
+}
+
 moe_status_t moe_ffn_profile_enable(int on) {
   std::lock_guard<std::mutex> lk(g_prof.mu);
   if (on && !g_prof.created) {
@@ -689,6 +754,12 @@ moe_status_t moe_ffn_profile_read(float* ms, int capacity, int* n_stages) {
     if (cudaEventElapsedTime(&ms[n], g_prof.ev[i], g_prof.ev[i + 1]) != cudaSuccess) return MOE_ERR_CUDA;
   *n_stages = n;
   return MOE_OK;
+}
+
+const char* moe_ffn_profile_stage_kernel(int stage) {
+  std::lock_guard<std::mutex> lk(g_prof.mu);
+  if (stage < 0 || stage + 1 >= g_prof.recorded) return nullptr;
+  return g_prof.kernel[stage];
 }
 
 moe_status_t moe_ffn_prepare_mxfp8_weights(const void* w1_sf, const void* w2_sf, void* w1_sf_packed,

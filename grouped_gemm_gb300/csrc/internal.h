@@ -41,6 +41,9 @@ struct Workspace {
   int64_t S_max;       // padded slot capacity (multiple of 128)
   int max_rb;
   int route_blocks;
+  // Not a region of the workspace: the call's router logits [T, E] fp32 when
+  // the call starts from them (moe_ffn_forward_logits), else nullptr.
+  const float* router_logits;
 };
 
 // pipeline = kRouteOnly plans only the routing regions (the common prefix of
@@ -74,9 +77,15 @@ struct GemmArgs {
 // Routing; when zero_out != nullptr the first launch also zero-fills
 // zero_out[0 .. zero_bytes) (the reduction target of the GEMMs).
 // pdl: the second and third routing launches start as programmatic dependents.
+// With ws.router_logits set, the routing launch first runs the router over
+// those [T, E] logits and writes topk_ids / topk_w (then caller outputs).
 cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const float* topk_w, int T, int E, int k,
                          cudaStream_t stream, void* zero_out = nullptr, int64_t zero_bytes = 0, int zero_grid = 0,
                          bool pdl = false);
+// The router alone: top-k ids (decreasing logit, ties to the lower id) and the
+// softmax of the selected logits, for each of T tokens of logits [T, E].
+cudaError_t launch_router_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                               cudaStream_t stream);
 // xg[padded slot of pair p] = x[p / k] for every routed pair, and (when
 // out != nullptr) out[0 .. out_bytes) = 0, out_bytes a multiple of 16 * T.
 // pdl: launched as a programmatic dependent of the routing launch.

@@ -15,6 +15,9 @@
 //   3. per-block stable scatter using warp match + per-warp prefix counts.
 #include <cuda_runtime.h>
 
+#include <climits>
+#include <cmath>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -23,9 +26,129 @@ namespace {
 
 constexpr int kScatterWarps = 8;
 
+// ---------------------------------------------------------------- router
+// Top-k of one token's router logits by one warp, and the softmax of the
+// selected logits (the step that produces the path's inputs: "Prime Flash
+// MoE" sec. 1, a router selects the top-k experts of each token together with
+// normalized routing weights; the workloads take the top k of per-(token,
+// expert) logits and renormalize a softmax over the selected k).
+//   order: decreasing logit, ties to the lower expert id, NaN read as -inf;
+//   w[j] = exp(l_j - l_0) / sum_i exp(l_i - l_0) in fp32 (l_0 the largest);
+//   every weight is 1/k when l_0 is -inf.
+// Lane l holds experts l, l + 32, ... (EPL of them); the expert selected
+// j-th is kept by lane j % 32 in slot j / 32.  `count(e)` is called once per
+// selected expert by the lane that keeps it.
+template <int EPL, typename Count>
+__device__ __forceinline__ void router_warp_topk(const float* __restrict__ lrow, int E, int k, int32_t* ids,
+                                                 float* w, Count count) {
+  const int lane = threadIdx.x & 31;
+  float v[EPL];
+  uint32_t avail = 0;  // bit i: expert lane + 32 i exists and is not taken yet
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    const float x = e < E ? lrow[e] : -INFINITY;
+    v[i] = x != x ? -INFINITY : x;
+    if (e < E) avail |= 1u << i;
+  }
+  float selv[EPL];
+  int seli[EPL];
+#pragma unroll
+  for (int q = 0; q < EPL; ++q) {
+    selv[q] = -INFINITY;
+    seli[q] = 0;
+  }
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = INT_MAX;  // none yet: loses to any expert, even one at -inf
+#pragma unroll
+    for (int i = 0; i < EPL; ++i)  // ascending ids: strict > keeps the lower id on ties
+      if (((avail >> i) & 1u) && (bi == INT_MAX || v[i] > bv)) {
+        bv = v[i];
+        bi = lane + 32 * i;
+      }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    if ((bi & 31) == lane) avail &= ~(1u << (bi >> 5));
+    if ((j & 31) == lane) {
+#pragma unroll
+      for (int q = 0; q < EPL; ++q)
+        if (q == (j >> 5)) {
+          selv[q] = bv;
+          seli[q] = bi;
+        }
+    }
+  }
+  const float m = __shfl_sync(0xffffffffu, selv[0], 0);
+  const bool flat = m == -INFINITY;
+  float s = 0.f;
+#pragma unroll
+  for (int q = 0; q < EPL; ++q)
+    if (q * 32 + lane < k) s += flat ? 1.f : expf(selv[q] - m);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+#pragma unroll
+  for (int q = 0; q < EPL; ++q) {
+    const int j = q * 32 + lane;
+    if (j < k) {
+      ids[j] = seli[q];
+      w[j] = (flat ? 1.f : expf(selv[q] - m)) / s;
+      count(seli[q]);
+    }
+  }
+}
+
+// Experts per lane for E experts (a power of two, E <= 32 * result).
+__host__ __device__ constexpr int router_epl(int E) {
+  return E <= 32 ? 1 : E <= 64 ? 2 : E <= 128 ? 4 : E <= 256 ? 8 : E <= 512 ? 16 : 32;
+}
+
+// Tokens [t0, t1) by the block's warps: top-k ids and weights written to
+// ids/w [T, k], each selected expert counted in the shared histogram.
+template <int EPL>
+__device__ void router_tokens(const float* __restrict__ logits, int E, int k, int t0, int t1, int32_t* ids,
+                              float* w, int* hist) {
+  const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  for (int t = t0 + warp; t < t1; t += nw)
+    router_warp_topk<EPL>(logits + (int64_t)t * E, E, k, ids + (int64_t)t * k, w + (int64_t)t * k,
+                          [&](int e) { if (hist) atomicAdd(&hist[e], 1); });
+}
+
+__device__ void router_tokens_any(const float* __restrict__ logits, int E, int k, int t0, int t1, int32_t* ids,
+                                  float* w, int* hist) {
+  switch (router_epl(E)) {
+    case 1: router_tokens<1>(logits, E, k, t0, t1, ids, w, hist); break;
+    case 2: router_tokens<2>(logits, E, k, t0, t1, ids, w, hist); break;
+    case 4: router_tokens<4>(logits, E, k, t0, t1, ids, w, hist); break;
+    case 8: router_tokens<8>(logits, E, k, t0, t1, ids, w, hist); break;
+    case 16: router_tokens<16>(logits, E, k, t0, t1, ids, w, hist); break;
+    default: router_tokens<32>(logits, E, k, t0, t1, ids, w, hist); break;
+  }
+}
+
+// The router alone: one warp per token.
+__global__ void __launch_bounds__(256) router_topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                          int32_t* __restrict__ ids, float* __restrict__ w) {
+  const int per_block = blockDim.x >> 5;
+  const int t0 = blockIdx.x * per_block;
+  router_tokens_any(logits, E, k, t0, min(T, t0 + per_block), ids, w, nullptr);
+}
+
+// Per-block histograms of the routed pairs.  With logits != nullptr the block
+// first runs the router over its tokens, writing ids_out / w_out, and counts
+// the selected experts as it goes (ids is then unused).
 __global__ void __launch_bounds__(256) route_count_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int k,
                                                           int NB, int* __restrict__ blk_counts, int* __restrict__ err,
-                                                          uint4* __restrict__ zero_out, int64_t zero_vecs) {
+                                                          uint4* __restrict__ zero_out, int64_t zero_vecs,
+                                                          const float* __restrict__ logits, int32_t* ids_out,
+                                                          float* w_out) {
   extern __shared__ int hist[];
   if (zero_out) {  // every block of the (possibly wider) grid helps zero-fill the reduction target
     const uint4 z = make_uint4(0, 0, 0, 0);
@@ -36,15 +159,20 @@ __global__ void __launch_bounds__(256) route_count_kernel(const int32_t* __restr
   if ((int)blockIdx.x >= NB) return;
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
-  const int64_t p0 = (int64_t)blockIdx.x * kRouteTokPerBlock * k;
-  const int64_t p1 = min(P, p0 + (int64_t)kRouteTokPerBlock * k);
-  bool bad = false;
-  for (int64_t p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
-    const int e = ids[p];
-    if ((unsigned)e < (unsigned)E) atomicAdd(&hist[e], 1);
-    else bad = true;
+  if (logits) {
+    const int T = (int)(P / k), t0 = (int)blockIdx.x * kRouteTokPerBlock;
+    router_tokens_any(logits, E, k, t0, min(T, t0 + kRouteTokPerBlock), ids_out, w_out, hist);
+  } else {
+    const int64_t p0 = (int64_t)blockIdx.x * kRouteTokPerBlock * k;
+    const int64_t p1 = min(P, p0 + (int64_t)kRouteTokPerBlock * k);
+    bool bad = false;
+    for (int64_t p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
+      const int e = ids[p];
+      if ((unsigned)e < (unsigned)E) atomicAdd(&hist[e], 1);
+      else bad = true;
+    }
+    if (bad) atomicOr(err, kErrBadRouting);
   }
-  if (bad) atomicOr(err, kErrBadRouting);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) blk_counts[(int64_t)blockIdx.x * E + e] = hist[e];
 }
@@ -170,7 +298,22 @@ __global__ void __launch_bounds__(1024) route_scan_kernel(int NB, int E, int* __
 // step, ranks from __match_any_sync, the running per-expert base in `mine`.
 // ids and weights are fetched eight steps at a time so the loop is not a chain
 // of dependent global loads.
-__device__ __forceinline__ void scatter_range(const int32_t* __restrict__ ids, const float* __restrict__ topk_w,
+// kFresh: ids and weights were written earlier in the same launch (the router
+// runs first in the block), so they are read with volatile loads from L2,
+// never through the read-only path.
+template <bool kFresh = false>
+__device__ __forceinline__ int load_i32(const int32_t* p) {
+  if constexpr (kFresh) return *reinterpret_cast<const volatile int32_t*>(p);
+  else return *p;
+}
+template <bool kFresh = false>
+__device__ __forceinline__ float load_f32(const float* p) {
+  if constexpr (kFresh) return *reinterpret_cast<const volatile float*>(p);
+  else return *p;
+}
+
+template <bool kFresh = false>
+__device__ __forceinline__ void scatter_range(const int32_t* ids, const float* topk_w,
                                               int64_t q0, int64_t q1, int E, int k, int* mine, const int* s_off,
                                               const int* s_poff, int* __restrict__ row_tok,
                                               float* __restrict__ slot_w, int* __restrict__ slot_of_pair) {
@@ -182,8 +325,8 @@ __device__ __forceinline__ void scatter_range(const int32_t* __restrict__ ids, c
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
       const int64_t p = b0 + i * 32 + lane;
-      ev[i] = p < q1 ? ids[p] : -1;
-      wv[i] = p < q1 ? topk_w[p] : 0.f;
+      ev[i] = p < q1 ? load_i32<kFresh>(ids + p) : -1;
+      wv[i] = p < q1 ? load_f32<kFresh>(topk_w + p) : 0.f;
     }
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
@@ -257,12 +400,16 @@ constexpr int kRouteSmallWarps = 32;
 constexpr int kRouteSmallMaxExperts = 256;
 constexpr int64_t kRouteSmallMaxPairs = 8192;
 
+// kRouter: the block first runs the router over all T tokens (logits [T, E]),
+// writing ids / topk_w, and then routes what it wrote.
+template <bool kRouter>
 __global__ void __launch_bounds__(1024)
-    route_small_kernel(const int32_t* __restrict__ ids, const float* __restrict__ topk_w, int P, int E, int k,
+    route_small_kernel(const int32_t* ids, const float* topk_w, int P, int E, int k,
                        int* __restrict__ err, int* __restrict__ counts, int* __restrict__ offsets,
                        int* __restrict__ pad_offsets, int* __restrict__ meta, int* __restrict__ expert_of_rb,
                        int* __restrict__ pair_info, int* __restrict__ row_tok, float* __restrict__ slot_w,
-                       int* __restrict__ slot_of_pair) {
+                       int* __restrict__ slot_of_pair, const float* __restrict__ logits, int32_t* ids_out,
+                       float* w_out) {
   __shared__ int wcnt[kRouteSmallWarps * kRouteSmallMaxExperts];
   __shared__ int s_off[kRouteSmallMaxExperts], s_poff[kRouteSmallMaxExperts], s_cnt[kRouteSmallMaxExperts];
   __shared__ int s_qoff[kRouteSmallMaxExperts];
@@ -271,14 +418,19 @@ __global__ void __launch_bounds__(1024)
   const int sub = (P + kRouteSmallWarps - 1) / kRouteSmallWarps;
   const int q0 = min(P, warp * sub), q1 = min(P, q0 + sub);
   for (int i = threadIdx.x; i < kRouteSmallWarps * E; i += blockDim.x) wcnt[i] = 0;
-  __syncthreads();
+  if constexpr (kRouter) {
+    router_tokens_any(logits, E, k, 0, P / k, ids_out, w_out, nullptr);
+    ids = ids_out;
+    topk_w = w_out;
+  }
+  __syncthreads();  // also orders the router's global writes before the reads below
   bool bad = false;
   for (int b0 = q0; b0 < q1; b0 += 32 * 8) {  // eight independent loads in flight per lane
     int ev[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int p = b0 + i * 32 + lane;
-      ev[i] = p < q1 ? ids[p] : 0;
+      ev[i] = p < q1 ? load_i32<kRouter>(ids + p) : 0;
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
@@ -335,7 +487,7 @@ __global__ void __launch_bounds__(1024)
     fill_pairs(e, lane, po, pc, s_qoff[e], pair_info);
   }
   // stable scatter
-  scatter_range(ids, topk_w, q0, q1, E, k, wcnt + warp * E, s_off, s_poff, row_tok, slot_w, slot_of_pair);
+  scatter_range<kRouter>(ids, topk_w, q0, q1, E, k, wcnt + warp * E, s_off, s_poff, row_tok, slot_w, slot_of_pair);
 }
 
 // Token-major gather: xg[padded slot of pair p, :] = x[t, :] for the k pairs
@@ -402,16 +554,26 @@ __global__ void __launch_bounds__(256)
 cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const float* topk_w, int T, int E, int k,
                          cudaStream_t stream, void* zero_out, int64_t zero_bytes, int zero_grid, bool pdl) {
   const int64_t P = (int64_t)T * k;
+  const float* logits = ws.router_logits;
+  // with the router, topk_ids / topk_w are the caller's output arrays
+  int32_t* ids_out = logits ? const_cast<int32_t*>(topk_ids) : nullptr;
+  float* w_out = logits ? const_cast<float*>(topk_w) : nullptr;
   if (!zero_out && P <= kRouteSmallMaxPairs && E <= kRouteSmallMaxExperts) {
-    route_small_kernel<<<1, 1024, 0, stream>>>(topk_ids, topk_w, (int)P, E, k, ws.err, ws.counts, ws.offsets,
-                                               ws.pad_offsets, ws.meta, ws.expert_of_rb, ws.pair_info, ws.row_tok,
-                                               ws.slot_w, ws.slot_of_pair);
+    if (logits)
+      route_small_kernel<true><<<1, 1024, 0, stream>>>(
+          topk_ids, topk_w, (int)P, E, k, ws.err, ws.counts, ws.offsets, ws.pad_offsets, ws.meta, ws.expert_of_rb,
+          ws.pair_info, ws.row_tok, ws.slot_w, ws.slot_of_pair, logits, ids_out, w_out);
+    else
+      route_small_kernel<false><<<1, 1024, 0, stream>>>(
+          topk_ids, topk_w, (int)P, E, k, ws.err, ws.counts, ws.offsets, ws.pad_offsets, ws.meta, ws.expert_of_rb,
+          ws.pair_info, ws.row_tok, ws.slot_w, ws.slot_of_pair, nullptr, nullptr, nullptr);
     return cudaGetLastError();
   }
   const int NB = ws.route_blocks;
   const int grid = zero_out ? (NB > zero_grid ? NB : zero_grid) : NB;
   route_count_kernel<<<grid, 256, E * sizeof(int), stream>>>(topk_ids, P, E, k, NB, ws.blk_base, ws.err,
-                                                             static_cast<uint4*>(zero_out), zero_bytes / 16);
+                                                             static_cast<uint4*>(zero_out), zero_bytes / 16, logits,
+                                                             ids_out, w_out);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // the scan and the scatter start as programmatic dependents (their launch
@@ -434,6 +596,14 @@ cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const flo
   return cudaLaunchKernelEx(&cfg, route_scatter_kernel, static_cast<const int32_t*>(topk_ids), topk_w, P, E, k,
                             static_cast<const int*>(ws.blk_base), static_cast<const int*>(ws.offsets),
                             static_cast<const int*>(ws.pad_offsets), ws.row_tok, ws.slot_w, ws.slot_of_pair);
+}
+
+cudaError_t launch_router_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
+                               cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  constexpr int kWarps = 8;
+  router_topk_kernel<<<(T + kWarps - 1) / kWarps, kWarps * 32, 0, stream>>>(logits, T, E, k, ids, w);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_gather_zero(const Workspace& ws, const void* x, const int32_t* topk_ids, int T, int E, int k,

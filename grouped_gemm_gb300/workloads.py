@@ -113,6 +113,11 @@ def draw_routing(rng: np.random.Generator, T: int, E: int, k: int, kind: str):
     raise ValueError(kind)
 
 
+def router_logits(T: int, E: int, seed: int = 0) -> np.ndarray:
+    """float32 router logits [T, E] ~ N(0, 1), one per (token, expert)."""
+    return np.random.default_rng(seed).standard_normal(size=(T, E), dtype=np.float32)
+
+
 def mx_encode_rows(a: np.ndarray):
     """Encode float32 rows (last dim a multiple of 32) as e4m3 codes + e8m0 scales.
 

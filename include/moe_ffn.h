@@ -83,6 +83,33 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
                              int D, int H, int k, int dtype, int pipeline, void* workspace, size_t workspace_bytes,
                              void* stream);
 
+/* The router step that produces the path's inputs ("Prime Flash MoE" sec. 1:
+ * a router selects the top-k experts of each token together with normalized
+ * routing weights; the workloads' routers take the top k of per-(token,
+ * expert) logits and renormalize a softmax over the selected k).
+ *   logits    [T, E] float32 (4-byte aligned; a NaN logit is read as -inf)
+ *   topk_ids  [T, k] int32 output: the k experts with the largest logits, in
+ *             order of decreasing logit, ties going to the lower expert id
+ *   topk_w    [T, k] float32 output: w_j = exp(l_j - l_0) / sum_i exp(l_i - l_0)
+ *             over the selected logits (l_0 the largest), computed in fp32;
+ *             every weight is 1/k when l_0 is -inf
+ * Requires 1 <= k <= E <= 1024.  Device pointers, asynchronous on stream.
+ * The ids are a deterministic function of the logits (no atomics). */
+moe_status_t moe_ffn_router_topk(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w,
+                                 void* stream);
+
+/* moe_ffn_forward starting from router logits: the routing launch runs the
+ * router of moe_ffn_router_topk over each token first (fused with the
+ * per-expert histogram, no extra launch), writes topk_ids / topk_w (caller
+ * arrays [T, k], outputs here), then the forward pass proceeds exactly as
+ * moe_ffn_forward with those ids and weights.  Same workspace, requirements
+ * and errors as moe_ffn_forward, plus k <= E and router_logits [T, E] float32
+ * (4-byte aligned). */
+moe_status_t moe_ffn_forward_logits(const void* x, const void* x_sf, const void* w1, const void* w1_sf,
+                                    const void* w2, const void* w2_sf, const float* router_logits,
+                                    int32_t* topk_ids, float* topk_w, void* out, int T, int E, int D, int H, int k,
+                                    int dtype, int pipeline, void* workspace, size_t workspace_bytes, void* stream);
+
 /* One-time repacking of MXFP8 weight scales into the 512-byte tile layout the
  * kernels copy into tensor memory ("Prime Flash MoE" sec. 7 "Scales are
  * piped through tensor memory"; 128 rows x 4 K-scales per tile).
@@ -237,6 +264,12 @@ moe_status_t moe_ffn_profile_enable(int on);
 /* Synchronize on the most recent profiled call and write its stage durations
  * in milliseconds to ms[0 .. *n_stages) (at most `capacity`). */
 moe_status_t moe_ffn_profile_read(float* ms, int capacity, int* n_stages);
+
+/* Name of the main kernel that ran in stage `stage` of the most recent
+ * profiled call (for example "up_swiglu_pair2", "fused_cluster_bf16",
+ * "none" for a stage that launches nothing), or NULL when that call recorded
+ * no such stage.  The string is static; the caller does not free it. */
+const char* moe_ffn_profile_stage_kernel(int stage);
 
 /* Static description of a status code. */
 const char* moe_ffn_status_string(moe_status_t status);

@@ -64,6 +64,8 @@ def _load():
             lib.oracle_route.argtypes = [c.c_int, c.c_int, c.c_int, c.c_void_p, c.c_int,
                                          c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p]
             lib.oracle_route.restype = c.c_int
+            lib.oracle_router_topk.argtypes = [c.c_int, c.c_int, c.c_int, c.c_void_p, c.c_void_p, c.c_void_p]
+            lib.oracle_router_topk.restype = c.c_int
             lib.oracle_moe_ffn.argtypes = [c.c_int] * 6 + [c.c_void_p] * 8 + [c.c_int, c.c_void_p, c.c_int,
                                                                                c.c_void_p, c.c_int]
             lib.oracle_moe_ffn.restype = c.c_int
@@ -132,6 +134,20 @@ def route(topk_ids: np.ndarray, E: int, pad: int = 128):
     if rc != 0:
         raise ValueError("expert id out of range")
     return out
+
+
+# ---------------------------------------------------------------- router
+def router_topk(logits: np.ndarray, k: int):
+    """Top-k experts per token (decreasing logit, ties to the lower id) and the
+    softmax of their logits in fp64.  ``logits`` is float32 [T, E].  Returns
+    (ids int32 [T, k], weights float64 [T, k])."""
+    lg = np.ascontiguousarray(logits, np.float32)
+    T, E = lg.shape
+    ids = np.zeros((T, k), np.int32)
+    w = np.zeros((T, k), np.float64)
+    if _load().oracle_router_topk(T, E, int(k), _ptr(lg), _ptr(ids), _ptr(w)) != 0:
+        raise ValueError("router_topk: k must lie in [1, E]")
+    return ids, w
 
 
 # ---------------------------------------------------------------- forward

@@ -180,6 +180,61 @@ int oracle_route(int T, int E, int k, const int32_t* ids, int pad,
 }
 
 /* ------------------------------------------------------------------------ */
+/* The router step before the path                                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Top-k selection with normalized weights, the step that produces the path's
+ * inputs ("Prime Flash MoE" sec. 1: "a router has already selected the top-k
+ * experts for each token, together with normalized routing weights"; the
+ * workloads' routers take the top k of per-(token, expert) logits and a
+ * softmax renormalized over the selected k).
+ *
+ * For each token t, with l[e] = logits[t][e] (a NaN logit is read as -inf):
+ *   ids[t][0..k-1]: the k experts with the largest l[e], in order of
+ *                   decreasing l, ties going to the lower expert id; found
+ *                   by k passes, each taking the best expert not yet taken.
+ *   w[t][j] = exp(l[ids[t][j]] - m) / sum_i exp(l[ids[t][i]] - m), with
+ *             m = l[ids[t][0]] (the largest), in double.  If m is -inf
+ *             (every selected logit is -inf) each weight is 1/k.
+ * Returns 0, or -1 for a bad argument (k outside [1, E]).
+ */
+int oracle_router_topk(int T, int E, int k, const float* logits, int32_t* ids, double* w) {
+    if (T < 0 || E < 1 || k < 1 || k > E) return -1;
+    char* taken = (char*)malloc((size_t)E);
+    if (!taken) return -2;
+    for (int t = 0; t < T; ++t) {
+        const float* l = logits + (int64_t)t * E;
+        memset(taken, 0, (size_t)E);
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            double bv = 0.0;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                double v = isnan(l[e]) ? -INFINITY : (double)l[e];
+                if (best < 0 || v > bv) {  /* strict: an equal later id never wins */
+                    best = e;
+                    bv = v;
+                }
+            }
+            taken[best] = 1;
+            ids[(int64_t)t * k + j] = best;
+        }
+        double m = isnan(l[ids[(int64_t)t * k]]) ? -INFINITY : (double)l[ids[(int64_t)t * k]];
+        double sum = 0.0;
+        for (int j = 0; j < k; ++j) {
+            double v = isnan(l[ids[(int64_t)t * k + j]]) ? -INFINITY : (double)l[ids[(int64_t)t * k + j]];
+            double p = (m == -INFINITY) ? 1.0 : exp(v - m);
+            w[(int64_t)t * k + j] = p;
+            sum += p;
+        }
+        for (int j = 0; j < k; ++j) w[(int64_t)t * k + j] /= sum;
+    }
+    free(taken);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* The forward pass                                                         */
 /* ------------------------------------------------------------------------ */
 
