@@ -204,6 +204,7 @@ MOE_OPT_TILE_COLS = 5
 MOE_OPT_SWAP_AB = 6
 MOE_OPT_FUSED_CLUSTER = 7
 MOE_OPT_PAIR_MMA = 8
+MOE_OPT_PAIR_SWAP = 9
 
 
 def moe_ffn_set_option(option: int, value: int) -> int:

@@ -26,6 +26,7 @@ std::atomic<int> g_tile_cols{0};      // MOE_OPT_TILE_COLS: 0 auto, 128 or 256 (
 std::atomic<int> g_fused_cluster{1};  // MOE_OPT_FUSED_CLUSTER: 0 off, 1 automatic size, 2/4/8 that size
 std::atomic<int> g_pair_mma{2};       // MOE_OPT_PAIR_MMA: 0 off, 1 on, 2 automatic (not for small problems)
 std::atomic<int> g_swap_ab{0};        // MOE_OPT_SWAP_AB: swap-AB tail tiles (measured slower on GB300: off)
+std::atomic<int> g_pair_swap{0};      // MOE_OPT_PAIR_SWAP: max routed rows of a swap-AB pair tile (measured slower: off)
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -525,6 +526,10 @@ moe_status_t moe_ffn_set_option(int option, long long value) {
       if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
       g_swap_ab.store((int)value);
       return MOE_OK;
+    case MOE_OPT_PAIR_SWAP:
+      if (value < 0 || value > 256) return MOE_ERR_INVALID_ARG;
+      g_pair_swap.store((int)value);
+      return MOE_OK;
 
     case MOE_OPT_TILE_COLS:
       if (value != 0 && value != 128 && value != 256) return MOE_ERR_INVALID_ARG;
@@ -661,6 +666,7 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
   ga.counts = ws.counts;
   ga.pad_offsets = ws.pad_offsets;
   ga.swap_ab = g_swap_ab.load();
+  ga.pair_swap_max = g_pair_swap.load();
 
   const int dyn_opt = g_dynamic_tiles.load();
   const bool small_problem = (int64_t)ws.max_rb * (H / kUpFold) < 8LL * sms;

@@ -21,6 +21,17 @@
 // exist (an expert with an odd number of row blocks) still runs both CTAs: the
 // odd CTA loads the first block's rows again and stores nothing.
 //
+// Swap-AB pair tiles (DOWN, args.pair_swap_max > 0): a pair whose blocks hold
+// at most pair_swap_max routed rows -- typically a half pair, an expert's odd
+// last block -- runs with the operands swapped: the 256 W2 rows are the MMA's
+// M side (each CTA its own 128, the rows it loads anyway) and the pair's
+// routed rows its N = ns (rounded up to 16, half of them in each CTA), so the
+// tensor cores do 256 x ns instead of 256 x 256 multiply-adds per K step and
+// an idle half pair costs almost nothing ("Porting Block-Scaled GEMM Kernels"
+// sec. 5.1 and Pearl: swap-AB for small per-expert M).  The epilogue reads the
+// transposed accumulator (lane = output column, column = routed row) into the
+// staging tile row by row and reduces each staged row into out as usual.
+//
 // Synchronization: both CTAs' TMA loads complete on the even CTA's full[]
 // barrier (which expects the pair's bytes); the MMA commits arrive on empty[]
 // and tfull[] of both CTAs (multicast); each CTA's epilogue warps arrive on the
@@ -46,12 +57,21 @@ constexpr int kQStaging = kBM * kQStageRow;
 constexpr int kQBarrierBytes = 256;
 constexpr int kQSmem = kQStages * kQStage + kQStaging + kQBarrierBytes;
 static_assert(kQSmem <= 232448, "shared memory");
-static_assert((2 * kQStages + 6) * 8 + 8 <= kQBarrierBytes, "barrier area");
+static_assert((2 * kQStages + 7) * 8 + 8 <= kQBarrierBytes, "barrier area");
 constexpr uint64_t kQDrainNs = 200ull * 1000 * 1000;
 constexpr uint64_t kQSettleNs = 2ull * 1000 * 1000;  // abort path: copies in flight land well within this
 
 __device__ __forceinline__ float q_u2f(uint32_t u) { return __uint_as_float(u); }
 __device__ __forceinline__ float q_swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
+
+// N of a swap-AB pair tile (routed rows of the pair rounded up to 16), or 0
+// for a normal tile.  Every role of both CTAs derives it from the same tables.
+__device__ __forceinline__ int pair_swap_ns(const GemmArgs& a, int info) {
+  if (a.pair_swap_max <= 0) return 0;
+  const int rb0 = info >> 1, e = a.expert_of_rb[rb0];
+  const int rows = min(2 * kBM, a.counts[e] - (rb0 * kBM - a.pad_offsets[e]));
+  return rows <= a.pair_swap_max ? (rows + 15) & ~15 : 0;
+}
 
 template <int MODE>
 __global__ void __launch_bounds__(kQThreads, 1)
@@ -71,7 +91,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
   uint64_t* never = drain + 1;  // no thread ever arrives here (failure-path test hook)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(never + 1);
+  uint64_t* epi_bar = never + 1;  // this CTA's four epilogue warps (swap-AB staging)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -91,6 +112,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     }
     mbar_init(drain, 1);
     mbar_init(never, 1);
+    mbar_init(epi_bar, 128);
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&map_a);
@@ -129,11 +151,15 @@ __global__ void __launch_bounds__(kQThreads, 1)
       const int e = args.expert_of_rb[rb0];
       const int brow = MODE == kPairUp ? e * 2 * args.H + (int)rank * args.H + j * 128
                                        : e * args.D + j * 256 + (int)rank * 128;
+      // swap-AB: this CTA's half of the ns routed rows (the TMA box still moves
+      // 128 rows; the MMA reads the first ns / 2)
+      const int ns = MODE == kPairDown ? pair_swap_ns(args, info) : 0;
+      const int arow = ns ? rb0 * kBM + (int)rank * (ns >> 1) : my_rb * kBM;
       for (int kb = 0; kb < KB; ++kb) {
         if (!(ok = mbar_wait(&empty[s], ph ^ 1u, wc, 61))) break;
         if (leader) mbar_arrive_expect_tx(&full[s], 2 * kQStage);
         const uint32_t fb = mapa_shared(smem_addr(&full[s]), 0);
-        tma_load_2d_pair(sA + s * kQA, &map_a, fb, kb * kBK, my_rb * kBM);
+        tma_load_2d_pair(sA + s * kQA, &map_a, fb, kb * kBK, arow);
         tma_load_2d_pair(sB + s * kQB, &map_b, fb, kb * kBK, brow);
         issued_phase[s] = (int)ph;
         if (++s == kQStages) {
@@ -163,14 +189,22 @@ __global__ void __launch_bounds__(kQThreads, 1)
       if (!(ok = mbar_wait_cluster(&tempty[acc], ((uint32_t)(it >> 1) & 1u) ^ 1u, wc, 62))) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * 256;
+      const int ns = MODE == kPairDown ? pair_swap_ns(args, args.pair_info[tile / NJ]) : 0;
+      const uint32_t idesc_swap = idesc_bf16_f32(2 * kBM, ns ? ns : 16);
       for (int kb = 0; kb < KB; ++kb) {
         if (!(ok = mbar_wait(&full[s], ph, wc, 63))) break;
         tc_fence_after();
         const uint64_t adesc = sdesc_sw128(smem_addr(sA + s * kQA));
         const uint64_t bdesc = sdesc_sw128(smem_addr(sB + s * kQB));
+        if (ns) {  // swap-AB: weight rows are M, the routed rows are N
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk)
-          umma_bf16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_bf16_pair(d_tmem, bdesc + 2 * kk, adesc + 2 * kk, idesc_swap, (kb | kk) != 0);
+        } else {
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_bf16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc, (kb | kk) != 0);
+        }
         umma_commit_pair(&empty[s], 0x3);  // frees this stage in both CTAs
         if (++s == kQStages) {
           s = 0;
@@ -191,6 +225,14 @@ __global__ void __launch_bounds__(kQThreads, 1)
     const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
     uint8_t* my_stage = sStage + row * kQStageRow;
     const uint32_t tempty_leader0 = mapa_shared(smem_addr(&tempty[0]), 0);
+    // barrier of this CTA's 128 epilogue threads (bounded, unlike bar.sync)
+    uint32_t epi_ph = 0;
+    auto epi_sync = [&](int site) -> bool {
+      mbar_arrive(epi_bar);
+      const bool got = mbar_wait(epi_bar, epi_ph, wc, site);
+      epi_ph ^= 1u;
+      return got;
+    };
     int it = 0;
     for (int tile = pair_slot; tile < n_tiles; tile += n_pair_slots, ++it) {
       const int acc = it & 1;
@@ -201,7 +243,54 @@ __global__ void __launch_bounds__(kQThreads, 1)
       const int64_t slot = (int64_t)((info >> 1) + (int)rank) * kBM + row;
       const int tok = valid ? args.row_tok[slot] : -1;
       const uint32_t tacc = lane_base + acc * 256;
-      if (MODE == kPairUp) {
+      const int ns = MODE == kPairDown ? pair_swap_ns(args, info) : 0;
+      if (MODE == kPairDown && ns > 0) {
+        // Swap-AB tile: TMEM lane `row` is output column j*256 + 128*rank + row,
+        // column c is routed row c of the pair (slot (info >> 1) * 128 + c).
+        // 128 routed rows at a time go transposed into the staging tile (staging
+        // row c = routed row c); thread c then reduces staging row c into out.
+        const int64_t slot0 = (int64_t)(info >> 1) * kBM;
+        const int col = j * 256 + (int)rank * 128;
+        bool failed = false;
+#pragma unroll 1
+        for (int h0 = 0; h0 < ns; h0 += kBM) {
+          const int cn = min(ns - h0, kBM);
+          bulk_wait_read_all();  // this thread's last reduction has left its staging row
+          if (!epi_sync(67)) {
+            failed = true;
+            break;
+          }
+#pragma unroll 1
+          for (int c0 = 0; c0 < cn; c0 += 64) {
+            uint32_t a0[32], a1[32];
+            tmem_ld_x32_pair(tacc + h0 + c0, tacc + h0 + c0 + 32, a0, a1);
+            const int ci = h0 + c0 + lane;
+            const float w0 = ci < ns ? args.slot_w[slot0 + ci] : 0.f;
+            const float w1 = ci + 32 < ns ? args.slot_w[slot0 + ci + 32] : 0.f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              st_shared_b16(sStage + (c0 + i) * kQStageRow + row * 2, __shfl_sync(0xffffffffu, w0, i) * q_u2f(a0[i]));
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              st_shared_b16(sStage + (c0 + 32 + i) * kQStageRow + row * 2,
+                            __shfl_sync(0xffffffffu, w1, i) * q_u2f(a1[i]));
+          }
+          fence_proxy_async_smem();
+          if (!epi_sync(68)) {
+            failed = true;
+            break;
+          }
+          if (row < cn) {
+            const int tok = args.row_tok[slot0 + h0 + row];
+            if (tok >= 0) {
+              bulk_reduce_add_bf16(static_cast<__nv_bfloat16*>(args.out) + (int64_t)tok * args.D + col,
+                                   sStage + row * kQStageRow, 256);
+              bulk_commit();
+            }
+          }
+        }
+        if (failed) break;
+      } else if (MODE == kPairUp) {
         if (tok >= 0) bulk_wait_read_all();  // the previous tile's store has left the staging row
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {

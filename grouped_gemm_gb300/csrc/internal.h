@@ -72,6 +72,8 @@ struct GemmArgs {
   const int* counts;        // routed rows per expert and padded segment starts: the
   const int* pad_offsets;   //   row count of each row block (swap-AB tail tiles)
   int swap_ab;              // 1: tail row blocks of <= 112 rows run as swap-AB tiles
+  int pair_swap_max;        // CTA-pair down kernel: pairs with at most this many routed rows
+                            //   run as swap-AB tiles (0 = never)
 };
 
 // Routing; when zero_out != nullptr the first launch also zero-fills

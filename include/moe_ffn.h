@@ -237,7 +237,17 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   blocks pays one idle half.  2 uses pairs unless the
  *                   problem is decode-sized (fewer than about eight waves of
  *                   up tiles).  Measured on GB300: prefill 0.360 -> 0.335 ms,
- *                   large_skewed 7.47 -> 6.83 ms, decode unchanged. */
+ *                   large_skewed 7.47 -> 6.83 ms, decode unchanged.
+ *   MOE_OPT_PAIR_SWAP  0 (default) .. 256: with CTA pairs, a down-
+ *                   projection tile whose two row blocks hold at most this
+ *                   many routed rows (an expert's odd last block, or a small
+ *                   expert) runs swap-AB: the 256 weight rows are the MMA's M
+ *                   side and the routed rows, rounded up to 16, its N, so the
+ *                   idle or padded rows of the pair cost no tensor-core work.
+ *                   Measured on GB300 at prefill: down kernel 0.115 ms with
+ *                   0, 0.121 with 128, 0.141 with 256 (the transposing
+ *                   epilogue costs more than the MMA work saved; the kernel
+ *                   is bound by streaming the weights). */
 typedef enum {
   MOE_OPT_GATHER = 0,
   MOE_OPT_L2_PREFETCH = 1,
@@ -247,7 +257,8 @@ typedef enum {
   MOE_OPT_TILE_COLS = 5,
   MOE_OPT_SWAP_AB = 6,
   MOE_OPT_FUSED_CLUSTER = 7,
-  MOE_OPT_PAIR_MMA = 8
+  MOE_OPT_PAIR_MMA = 8,
+  MOE_OPT_PAIR_SWAP = 9
 } moe_option_t;
 moe_status_t moe_ffn_set_option(int option, long long value);
 

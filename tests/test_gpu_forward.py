@@ -21,7 +21,8 @@ pytestmark = pytest.mark.gpu
 # Pipeline and option settings under test: the split pipeline with the
 # materializing gather kernel (default), with in-kernel gathers, with two row
 # blocks per up tile, with the tail row blocks run as swap-AB tiles and with
-# both GEMMs on CTA pairs; the
+# both GEMMs on CTA pairs (down tiles never swap-AB by default, or swap-AB for
+# small pairs, or always); the
 # fused pipeline on clusters (default where the shape allows) and with the
 # H-split fp32 partial sums.
 MODES = {
@@ -31,11 +32,13 @@ MODES = {
     "split_cpasync": (moe.MOE_SPLIT, {moe.MOE_OPT_GATHER: 2}),
     "split_swap": (moe.MOE_SPLIT, {moe.MOE_OPT_SWAP_AB: 1}),
     "split_pair2": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 1}),
+    "split_pair2_swap": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 1, moe.MOE_OPT_PAIR_SWAP: 128}),
+    "split_pair2_allswap": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 1, moe.MOE_OPT_PAIR_SWAP: 256}),
     "fused": (moe.MOE_FUSED, {}),
     "fused_splitk": (moe.MOE_FUSED, {moe.MOE_OPT_FUSED_CLUSTER: 0}),
 }
 DEFAULTS = {moe.MOE_OPT_UP_PAIRS: 0, moe.MOE_OPT_GATHER: 0, moe.MOE_OPT_SWAP_AB: 0, moe.MOE_OPT_FUSED_CLUSTER: 1,
-            moe.MOE_OPT_PAIR_MMA: 2}
+            moe.MOE_OPT_PAIR_MMA: 2, moe.MOE_OPT_PAIR_SWAP: 0}
 PIPELINES = list(MODES)
 
 
