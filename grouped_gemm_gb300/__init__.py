@@ -205,6 +205,9 @@ MOE_OPT_SWAP_AB = 6
 MOE_OPT_FUSED_CLUSTER = 7
 MOE_OPT_PAIR_MMA = 8
 MOE_OPT_PAIR_SWAP = 9
+MOE_OPT_ROUTE_COOP = 10
+MOE_OPT_OUT_L2_HINT = 11
+MOE_OPT_GATHER_BLOCKS = 12
 
 
 def moe_ffn_set_option(option: int, value: int) -> int:

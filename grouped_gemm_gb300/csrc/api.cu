@@ -26,9 +26,20 @@ std::atomic<int> g_tile_cols{0};      // MOE_OPT_TILE_COLS: 0 auto, 128 or 256 (
 std::atomic<int> g_fused_cluster{1};  // MOE_OPT_FUSED_CLUSTER: 0 off, 1 automatic size, 2/4/8 that size
 std::atomic<int> g_pair_mma{2};       // MOE_OPT_PAIR_MMA: 0 off, 1 on, 2 automatic (not for small problems)
 std::atomic<int> g_swap_ab{0};        // MOE_OPT_SWAP_AB: swap-AB tail tiles (measured slower on GB300: off)
+std::atomic<int> g_out_hint{0};       // MOE_OPT_OUT_L2_HINT: 0 off (measured no gain), 1 automatic, 2 always
+std::atomic<int> g_gather_blocks{4};  // MOE_OPT_GATHER_BLOCKS: gather blocks per SM
 std::atomic<int> g_pair_swap{0};      // MOE_OPT_PAIR_SWAP: max routed rows of a swap-AB pair tile (measured slower: off)
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Whether the reductions into out carry an L2 evict_last hint: automatic when
+// out is no larger than about the L2 (it can then stay resident while the
+// weights stream past; a much larger out would only push weights out).
+constexpr int64_t kOutHintMaxBytes = 160ll << 20;
+int out_hint_for(int64_t out_bytes) {
+  const int opt = g_out_hint.load();
+  return opt == 2 || (opt == 1 && out_bytes <= kOutHintMaxBytes) ? 1 : 0;
+}
 
 bool shape_ok(int T, int E, int D, int H, int k) {
   return T >= 0 && E >= 1 && E <= kMaxExperts && k >= 1 && D >= 128 && H >= 128 && D % 128 == 0 && H % 128 == 0 &&
@@ -115,8 +126,11 @@ void prof_front(bool mx) {
 
 }  // namespace
 
+std::atomic<int> g_route_coop{1};
+
 Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipeline, int dtype) {
   Workspace w{};
+  w.wait_limit_ns = g_wait_limit_ns.load();
   const int64_t P = (int64_t)T * k;
   const int64_t live_experts = P < E ? P : E;
   w.S_max = (int64_t)align_up((size_t)(P + live_experts * (kRowPad - 1)), kRowPad);
@@ -227,7 +241,7 @@ moe_status_t forward_fused_cluster_bf16(const Workspace& ws, const void* x, cons
   cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st, nullptr, 0, 0, !g_prof.on);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 1);
-  e = launch_gather_zero(ws, x, topk_ids, T, E, k, D, out, (int64_t)T * D * 2, sms * 4, st, !g_prof.on);
+  e = launch_gather_zero(ws, x, topk_ids, T, E, k, D, out, (int64_t)T * D * 2, sms * g_gather_blocks.load(), st, !g_prof.on);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 2);
   FusedClusterArgs fa{};
@@ -242,6 +256,7 @@ moe_status_t forward_fused_cluster_bf16(const Workspace& ws, const void* x, cons
   fa.D = D;
   fa.H = H;
   fa.csize = C;
+  fa.out_hint = out_hint_for((int64_t)T * D * 2);
   fa.h1 = h1;
   fa.s1 = H / C / h1;
   fa.s2 = D / C / kFusedClusterN;
@@ -276,7 +291,7 @@ moe_status_t forward_fused_bf16(const Workspace& ws, const void* x, const void* 
   cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st, nullptr, 0, 0, !g_prof.on);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 1);
-  e = launch_gather_zero(ws, x, topk_ids, T, E, k, D, ws.acc_f32, (int64_t)T * D * 4, sms * 4, st, !g_prof.on);
+  e = launch_gather_zero(ws, x, topk_ids, T, E, k, D, ws.acc_f32, (int64_t)T * D * 4, sms * g_gather_blocks.load(), st, !g_prof.on);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 2);
   FusedArgs fa{};
@@ -320,7 +335,7 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
   cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st, nullptr, 0, 0, !g_prof.on);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 1);
-  e = launch_gather_mx(ws, x, x_sf, D, out, (int64_t)T * D * 2, sms * 4, st);
+  e = launch_gather_mx(ws, x, x_sf, topk_ids, T, E, k, D, out, (int64_t)T * D * 2, sms * g_gather_blocks.load(), st, !g_prof.on);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 2);
   MxArgs ma{};
@@ -336,6 +351,7 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
   ma.D = D;
   ma.H = H;
   ma.stall_test = g_stall_test.load();
+  ma.out_hint = out_hint_for((int64_t)T * D * 2);
   MxArgs up = ma;
   up.sf_a = ws.xg_sf;
   up.sf_b = w1_sf;
@@ -398,7 +414,7 @@ moe_status_t forward_fused_cluster_mxfp8(const Workspace& ws, const void* x, con
   cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st, nullptr, 0, 0, !g_prof.on);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 1);
-  e = launch_gather_mx(ws, x, x_sf, D, out, (int64_t)T * D * 2, sms * 4, st);
+  e = launch_gather_mx(ws, x, x_sf, topk_ids, T, E, k, D, out, (int64_t)T * D * 2, sms * g_gather_blocks.load(), st, !g_prof.on);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 2);
   FusedClusterMxArgs fa{};
@@ -417,6 +433,7 @@ moe_status_t forward_fused_cluster_mxfp8(const Workspace& ws, const void* x, con
   fa.D = D;
   fa.H = H;
   fa.csize = C;
+  fa.out_hint = out_hint_for((int64_t)T * D * 2);
   fa.s1 = H / C / 128;
   fa.s2 = D / C / 256;
   fa.stall_test = g_stall_test.load();
@@ -454,7 +471,8 @@ moe_status_t forward_fused_mxfp8(const Workspace& ws, const void* x, const void*
   cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st, nullptr, 0, 0, !g_prof.on);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 1);
-  e = launch_gather_mx(ws, x, x_sf, D, ws.acc_f32, (int64_t)T * D * 4, sms * 4, st);
+  e = launch_gather_mx(ws, x, x_sf, topk_ids, T, E, k, D, ws.acc_f32, (int64_t)T * D * 4, sms * g_gather_blocks.load(), st,
+                       !g_prof.on);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 2);
   FusedMxArgs fa{};
@@ -525,6 +543,18 @@ moe_status_t moe_ffn_set_option(int option, long long value) {
     case MOE_OPT_SWAP_AB:
       if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
       g_swap_ab.store((int)value);
+      return MOE_OK;
+    case MOE_OPT_ROUTE_COOP:
+      if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
+      g_route_coop.store((int)value);
+      return MOE_OK;
+    case MOE_OPT_OUT_L2_HINT:
+      if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
+      g_out_hint.store((int)value);
+      return MOE_OK;
+    case MOE_OPT_GATHER_BLOCKS:
+      if (value < 1 || value > 16) return MOE_ERR_INVALID_ARG;
+      g_gather_blocks.store((int)value);
       return MOE_OK;
     case MOE_OPT_PAIR_SWAP:
       if (value < 0 || value > 256) return MOE_ERR_INVALID_ARG;
@@ -644,7 +674,7 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 1);
   if (!in_gemm_gather) {
-    e = launch_gather_zero(ws, x, topk_ids, T, E, k, D, out, (int64_t)T * D * 2, sms * 4, st, !g_prof.on);
+    e = launch_gather_zero(ws, x, topk_ids, T, E, k, D, out, (int64_t)T * D * 2, sms * g_gather_blocks.load(), st, !g_prof.on);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   prof_mark(st, 2);
@@ -667,6 +697,7 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
   ga.pad_offsets = ws.pad_offsets;
   ga.swap_ab = g_swap_ab.load();
   ga.pair_swap_max = g_pair_swap.load();
+  ga.out_hint = out_hint_for((int64_t)T * D * 2);
 
   const int dyn_opt = g_dynamic_tiles.load();
   const bool small_problem = (int64_t)ws.max_rb * (H / kUpFold) < 8LL * sms;

@@ -89,7 +89,13 @@ __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 
 // silu(g) * u = g / (1 + e^-g) * u; fast reciprocal division (the result is
 // rounded to bf16 right after).
-__device__ __forceinline__ float swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
+// silu(g) * u with the optional clamp (lim = +inf when off): g <= lim,
+// -lim <= u <= lim.
+__device__ __forceinline__ float swiglu(float g, float u, float lim) {
+  g = fminf(g, lim);
+  u = fminf(fmaxf(u, -lim), lim);
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
 
 template <int MODE, int N, int STAGES, int GATHER>
 __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
@@ -120,6 +126,7 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float swiglu_lim = args.swiglu_limit > 0.f ? args.swiglu_limit : __int_as_float(0x7f800000);
   const WaitCtl wc{abort_flag, args.err, args.wait_limit_ns};
   // Tile sequence: warp 0 draws tile indices (from a global atomic counter
   // when args.tile_counter is set -- CTAs that finish early take more tiles --
@@ -457,7 +464,7 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
             tmem_ld_x32_pair(tacc + c0, tacc + kBM + c0, g, u);
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-              st_shared_b16(sStage + (c0 + i) * Cfg::kStageRowBytes + row * 2, swiglu(u2f(g[i]), u2f(u[i])));
+              st_shared_b16(sStage + (c0 + i) * Cfg::kStageRowBytes + row * 2, swiglu(u2f(g[i]), u2f(u[i]), swiglu_lim));
           }
           fence_proxy_async_smem();
           if (!epi_sync(13)) break;
@@ -496,7 +503,7 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
               break;
             }
             if (tok >= 0) {
-              bulk_reduce_add_bf16(orow + hh * kBM, my_stage, kBM * 2);
+              bulk_reduce_add_bf16_hint(orow + hh * kBM, my_stage, kBM * 2, args.out_hint != 0, l2_policy_evict_last());
               bulk_commit();
             }
           }
@@ -513,7 +520,7 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              pk[i] = pack_bf16x2(swiglu(u2f(g[2 * i]), u2f(u[2 * i])), swiglu(u2f(g[2 * i + 1]), u2f(u[2 * i + 1])));
+              pk[i] = pack_bf16x2(swiglu(u2f(g[2 * i]), u2f(u[2 * i]), swiglu_lim), swiglu(u2f(g[2 * i + 1]), u2f(u[2 * i + 1]), swiglu_lim));
 #pragma unroll
             for (int q = 0; q < 4; ++q)
               st_shared_v4(my_stage + c * 64 + q * 16, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
@@ -552,7 +559,7 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
           }
           if (tok >= 0) {
             fence_proxy_async_smem();
-            bulk_reduce_add_bf16(orow + h * (N / 2), my_stage, N);
+            bulk_reduce_add_bf16_hint(orow + h * (N / 2), my_stage, N, args.out_hint != 0, l2_policy_evict_last());
             bulk_commit();
           }
         }

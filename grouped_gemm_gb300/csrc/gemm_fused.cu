@@ -51,7 +51,13 @@ static_assert((2 * kFStages + 7) * 8 + 8 <= kFBarrierBytes, "barrier area");
 constexpr uint64_t kFDrainNs = 200ull * 1000 * 1000;
 
 __device__ __forceinline__ float f_u2f(uint32_t u) { return __uint_as_float(u); }
-__device__ __forceinline__ float f_swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
+// silu(g) * u with the optional clamp (lim = +inf when off): g <= lim,
+// -lim <= u <= lim.
+__device__ __forceinline__ float f_swiglu(float g, float u, float lim) {
+  g = fminf(g, lim);
+  u = fminf(fmaxf(u, -lim), lim);
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
 
 __global__ void __launch_bounds__(kFThreads, 1)
     fused_moe_bf16_kernel(const __grid_constant__ CUtensorMap map_xg, const __grid_constant__ CUtensorMap map_w1,
@@ -72,6 +78,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float swiglu_lim = args.swiglu_limit > 0.f ? args.swiglu_limit : __int_as_float(0x7f800000);
   const WaitCtl wc{abort_flag, args.err, args.wait_limit_ns};
 
   if (threadIdx.x == 0) {
@@ -245,7 +252,7 @@ __global__ void __launch_bounds__(kFThreads, 1)
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
               const int v = i * 8 + m * 2;
-              p[m] = pack_bf16x2(f_swiglu(f_u2f(g[v]), f_u2f(u[v])), f_swiglu(f_u2f(g[v + 1]), f_u2f(u[v + 1])));
+              p[m] = pack_bf16x2(f_swiglu(f_u2f(g[v]), f_u2f(u[v]), swiglu_lim), f_swiglu(f_u2f(g[v + 1]), f_u2f(u[v + 1]), swiglu_lim));
             }
             const int chunk = (c & 1) * 4 + i;  // 16-byte chunk within the 128-byte row
             st_shared_v4(kblk + ((chunk ^ (row & 7)) << 4), p[0], p[1], p[2], p[3]);

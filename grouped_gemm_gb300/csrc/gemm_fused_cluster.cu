@@ -58,7 +58,13 @@ constexpr uint32_t kAcc2Col = 256;
 constexpr uint64_t kCDrainNs = 200ull * 1000 * 1000;
 
 __device__ __forceinline__ float c_u2f(uint32_t u) { return __uint_as_float(u); }
-__device__ __forceinline__ float c_swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
+// silu(g) * u with the optional clamp (lim = +inf when off): g <= lim,
+// -lim <= u <= lim.
+__device__ __forceinline__ float c_swiglu(float g, float u, float lim) {
+  g = fminf(g, lim);
+  u = fminf(fmaxf(u, -lim), lim);
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
 
 // Job j of round r (row blocks 0 .. n-1; r in 0 .. n): GEMM1 sub-chunks of row
 // block r and GEMM2 sub-chunks of row block r - 1, alternating while both
@@ -106,6 +112,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float swiglu_lim = args.swiglu_limit > 0.f ? args.swiglu_limit : __int_as_float(0x7f800000);
   const WaitCtl wc{abort_flag, args.err, args.wait_limit_ns};
   const int C = args.csize;
   const int crank = (int)blockIdx.x % C, cid = (int)blockIdx.x / C, ncl = (int)gridDim.x / C;
@@ -288,8 +295,8 @@ __global__ void __launch_bounds__(kCThreads, 1)
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              pk[i] = pack_bf16x2(c_swiglu(c_u2f(g[2 * i]), c_u2f(u[2 * i])),
-                                  c_swiglu(c_u2f(g[2 * i + 1]), c_u2f(u[2 * i + 1])));
+              pk[i] = pack_bf16x2(c_swiglu(c_u2f(g[2 * i]), c_u2f(u[2 * i]), swiglu_lim),
+                                  c_swiglu(c_u2f(g[2 * i + 1]), c_u2f(u[2 * i + 1]), swiglu_lim));
 #pragma unroll
             for (int v = 0; v < 4; ++v)
               st_global_v4(dst + c + v * 8, pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
@@ -338,7 +345,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
           }
           if (tok >= 0) {
             fence_proxy_async_smem();
-            bulk_reduce_add_bf16(orow + hh * (kFusedClusterN / 2), my_stage, kFusedClusterN);
+            bulk_reduce_add_bf16_hint(orow + hh * (kFusedClusterN / 2), my_stage, kFusedClusterN, args.out_hint != 0, l2_policy_evict_last());
             bulk_commit();
           }
         }

@@ -54,7 +54,13 @@ static_assert(kMSfCol + 16 * kMStages <= 512, "TMEM columns");
 constexpr uint64_t kMDrainNs = 200ull * 1000 * 1000;
 
 __device__ __forceinline__ float m_u2f(uint32_t u) { return __uint_as_float(u); }
-__device__ __forceinline__ float m_swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
+// silu(g) * u with the optional clamp (lim = +inf when off): g <= lim,
+// -lim <= u <= lim.
+__device__ __forceinline__ float m_swiglu(float g, float u, float lim) {
+  g = fminf(g, lim);
+  u = fminf(fmaxf(u, -lim), lim);
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
 
 // Rounds as in the bf16 cluster kernel: round r interleaves the GEMM1 jobs of
 // row block r with the GEMM2 jobs of row block r - 1.
@@ -101,6 +107,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float swiglu_lim = args.swiglu_limit > 0.f ? args.swiglu_limit : __int_as_float(0x7f800000);
   const WaitCtl wc{abort_flag, args.err, args.wait_limit_ns};
   const int C = args.csize;
   const int crank = (int)blockIdx.x % C, cid = (int)blockIdx.x / C, ncl = (int)gridDim.x / C;
@@ -293,7 +300,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
           const int col = half * 64 + c * 32;
           tmem_ld_x32_pair(lane_base + col, lane_base + 128 + col, g, u);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) a[c * 32 + i] = m_swiglu(m_u2f(g[i]), m_u2f(u[i]));
+          for (int i = 0; i < 32; ++i) a[c * 32 + i] = m_swiglu(m_u2f(g[i]), m_u2f(u[i]), swiglu_lim);
         }
         tc_fence_before();
         mbar_arrive(tempty);  // the accumulator is free once all 256 threads have read it
@@ -342,7 +349,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
                            pack_bf16x2(w * m_u2f(v[c][8 * qd + 6]), w * m_u2f(v[c][8 * qd + 7])));
           }
           fence_proxy_async_smem();
-          bulk_reduce_add_bf16(orow, my_stage, kMStageCols * 2);
+          bulk_reduce_add_bf16_hint(orow, my_stage, kMStageCols * 2, args.out_hint != 0, l2_policy_evict_last());
           bulk_commit();
         }
       }

@@ -45,7 +45,13 @@ static_assert(256 + 16 * kXStages <= 512, "TMEM columns");
 constexpr uint64_t kXDrainNs = 200ull * 1000 * 1000;
 
 __device__ __forceinline__ float x_u2f(uint32_t u) { return __uint_as_float(u); }
-__device__ __forceinline__ float x_swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
+// silu(g) * u with the optional clamp (lim = +inf when off): g <= lim,
+// -lim <= u <= lim.
+__device__ __forceinline__ float x_swiglu(float g, float u, float lim) {
+  g = fminf(g, lim);
+  u = fminf(fmaxf(u, -lim), lim);
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
 
 __global__ void __launch_bounds__(kXThreads, 1)
     fused_moe_mxfp8_kernel(const __grid_constant__ CUtensorMap map_xg, const __grid_constant__ CUtensorMap map_w1,
@@ -69,6 +75,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float swiglu_lim = args.swiglu_limit > 0.f ? args.swiglu_limit : __int_as_float(0x7f800000);
   const WaitCtl wc{abort_flag, args.err, args.wait_limit_ns};
 
   if (threadIdx.x == 0) {
@@ -232,7 +239,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
         tmem_ld_x32_pair(lane_base + blk * 32, lane_base + 128 + blk * 32, g, u);
         float a[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) a[i] = x_swiglu(x_u2f(g[i]), x_u2f(u[i]));
+        for (int i = 0; i < 32; ++i) a[i] = x_swiglu(x_u2f(g[i]), x_u2f(u[i]), swiglu_lim);
         uint32_t qv[8];
         sfw |= mx_quantize32(a, qv) << (8 * blk);
         // 32 codes = 16-byte chunks 2*blk and 2*blk+1 of the 128-byte row, swizzled

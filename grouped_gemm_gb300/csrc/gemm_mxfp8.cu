@@ -52,7 +52,13 @@ struct MxCfg {
 };
 
 __device__ __forceinline__ float mx_u2f(uint32_t u) { return __uint_as_float(u); }
-__device__ __forceinline__ float mx_swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
+// silu(g) * u with the optional clamp (lim = +inf when off): g <= lim,
+// -lim <= u <= lim.
+__device__ __forceinline__ float mx_swiglu(float g, float u, float lim) {
+  g = fminf(g, lim);
+  u = fminf(fmaxf(u, -lim), lim);
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
 
 template <int MODE, int STAGES>
 __global__ void __launch_bounds__(kMxThreads, 1)
@@ -75,6 +81,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float swiglu_lim = args.swiglu_limit > 0.f ? args.swiglu_limit : __int_as_float(0x7f800000);
   const WaitCtl wc{abort_flag, args.err, args.wait_limit_ns};
 
   if (threadIdx.x == 0) {
@@ -213,7 +220,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
           const int col = half * 64 + c * 32;
           tmem_ld_x32_pair(lane_base + col, lane_base + 128 + col, g, u);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) act[c * 32 + i] = mx_swiglu(mx_u2f(g[i]), mx_u2f(u[i]));
+          for (int i = 0; i < 32; ++i) act[c * 32 + i] = mx_swiglu(mx_u2f(g[i]), mx_u2f(u[i]), swiglu_lim);
         }
         tc_fence_before();
         mbar_arrive(tempty);  // the accumulator is free once all 256 threads have read it
@@ -260,8 +267,8 @@ __global__ void __launch_bounds__(kMxThreads, 1)
         mbar_arrive(tempty);
         if (tok >= 0) {
           fence_proxy_async_smem();
-          bulk_reduce_add_bf16(static_cast<__nv_bfloat16*>(args.out) + (int64_t)tok * args.D + j * kMxN + half * 128,
-                               my_stage, kMxN);
+          bulk_reduce_add_bf16_hint(static_cast<__nv_bfloat16*>(args.out) + (int64_t)tok * args.D + j * kMxN + half * 128,
+                               my_stage, kMxN, args.out_hint != 0, l2_policy_evict_last());
           bulk_commit();
         }
       }
@@ -305,52 +312,80 @@ cudaError_t launch_mx(const CUtensorMap& a, const CUtensorMap& b, const MxArgs& 
   return cudaLaunchKernelEx(&cfg, kern, a, b, args);
 }
 
-// xg[s] = x[row_tok[s]] (D bytes of e4m3 per row, one warp per row, live slots
-// only), then the scales of every row block moved from row-major x_sf[T, D/32]
-// into the blocked 512-byte tiles of xg_sf: one warp per (row block, K tile),
-// lane l gathering the 4-byte scale words of rows l, l+32, l+64, l+96 and
-// writing them as one 16-byte store (the tile's row l).  The same launch
-// zero-fills out.
-__global__ void __launch_bounds__(256) gather_rows_mx_kernel(const uint4* __restrict__ x, const uint32_t* __restrict__ x_sf,
-                                                             const int* __restrict__ row_tok, const int* __restrict__ meta,
-                                                             uint4* __restrict__ xg, uint8_t* __restrict__ xg_sf, int D,
-                                                             uint4* __restrict__ out, int64_t out_vecs) {
+// Token-major gather of e4m3 rows: one warp per (token, 4 KB chunk of its code
+// row); the chunk is read once (16-byte loads, eight per lane) and written to
+// each of the token's k padded slots, so x is read once rather than k times.
+// The same warps zero-fill the token's row of `out` (the reduction target).
+// Then the scales: row-major x_sf[T, D/32] into the blocked 512-byte tiles of
+// xg_sf, slot by slot (padding rows get scale 1.0; their codes are never
+// written: each GEMM output row depends only on its own input row and padding
+// rows are dropped by the epilogues).  Launched as a programmatic dependent of
+// the routing.
+constexpr int kMxGatherChunkVecs = 256;
+
+__global__ void __launch_bounds__(256)
+    gather_tokens_mx_kernel(const uint4* __restrict__ x, const uint32_t* __restrict__ x_sf,
+                            const int32_t* __restrict__ ids, const int* __restrict__ slot_of_pair,
+                            const int* __restrict__ offsets, const int* __restrict__ pad_offsets,
+                            const int* __restrict__ row_tok, const int* __restrict__ meta, int T, int E, int k,
+                            int vec_per_row, int kt_per_row, uint4* __restrict__ xg, uint8_t* __restrict__ xg_sf,
+                            uint4* __restrict__ out, int out_vecs_per_row) {
+  griddep_wait();
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_rb = meta[0];
-  const int64_t S = (int64_t)n_rb * kRowPad;
+  const int n_chunks = (vec_per_row + kMxGatherChunkVecs - 1) / kMxGatherChunkVecs;
+  const int zero_per = (out_vecs_per_row + n_chunks - 1) / n_chunks;
+  const int64_t items = (int64_t)T * n_chunks;
   const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t gwarp = (int64_t)blockIdx.x * (blockDim.x >> 5) + warp;
-  const int vec_per_row = D / 16, kt_per_row = D / 128;
-  for (int64_t row = gwarp; row < S; row += nwarps) {
-    const int tok = row_tok[row];
-    if (tok < 0) continue;
-    const uint4* src = x + (int64_t)tok * vec_per_row;
-    uint4* dst = xg + row * vec_per_row;
-    int i = lane;
-    for (; i + 96 < vec_per_row; i += 128) {
-      const uint4 a = __ldg(src + i), b = __ldg(src + i + 32), c = __ldg(src + i + 64), d = __ldg(src + i + 96);
-      dst[i] = a;
-      dst[i + 32] = b;
-      dst[i + 64] = c;
-      dst[i + 96] = d;
+  for (int64_t it = gwarp; it < items; it += nwarps) {
+    const int t = (int)(it / n_chunks), c = (int)(it % n_chunks);
+    const int v0 = c * kMxGatherChunkVecs;
+    const uint4* src = x + (int64_t)t * vec_per_row + v0;
+    uint4 v[kMxGatherChunkVecs / 32];
+#pragma unroll
+    for (int i = 0; i < kMxGatherChunkVecs / 32; ++i)
+      if (v0 + i * 32 + lane < vec_per_row) v[i] = __ldg(src + i * 32 + lane);
+    for (int j0 = 0; j0 < k; j0 += 32) {
+      int ps = -1;  // lane l resolves the padded slot of pair j0 + l
+      if (j0 + lane < k) {
+        const int64_t p = (int64_t)t * k + j0 + lane;
+        const int e = ids[p], s = slot_of_pair[p];
+        if (s >= 0 && (unsigned)e < (unsigned)E) ps = s - offsets[e] + pad_offsets[e];
+      }
+      const int nj = min(32, k - j0);
+      for (int jj = 0; jj < nj; ++jj) {
+        const int slot = __shfl_sync(0xffffffffu, ps, jj);
+        if (slot < 0) continue;
+        uint4* dst = xg + (int64_t)slot * vec_per_row + v0;
+#pragma unroll
+        for (int i = 0; i < kMxGatherChunkVecs / 32; ++i)
+          if (v0 + i * 32 + lane < vec_per_row) dst[i * 32 + lane] = v[i];
+      }
     }
-    for (; i < vec_per_row; i += 32) dst[i] = __ldg(src + i);
+    if (out) {
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      uint4* orow = out + (int64_t)t * out_vecs_per_row;
+      const int z1 = min(out_vecs_per_row, (c + 1) * zero_per);
+      for (int i = c * zero_per + lane; i < z1; i += 32) orow[i] = z;
+    }
   }
-  const int64_t n_sf_tiles = (int64_t)n_rb * kt_per_row;
-  for (int64_t t = gwarp; t < n_sf_tiles; t += nwarps) {
-    const int64_t rb = t / kt_per_row;
-    const int kt = (int)(t % kt_per_row);
-    uint32_t w[4];
+  // scales: one warp per (row block, K tile) writes the blocked 512-byte tile
+  // with coalesced 16-byte stores, lane l gathering the 4-byte scale words of
+  // rows l, l + 32, l + 64, l + 96 (padding rows: scale 1.0, e8m0 127)
+  const int64_t n_sf_tiles = (int64_t)meta[0] * kt_per_row;
+  for (int64_t q = gwarp; q < n_sf_tiles; q += nwarps) {
+    const int64_t rb = q / kt_per_row;
+    const int kt = (int)(q % kt_per_row);
+    uint32_t wv[4];
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       const int tok = row_tok[rb * kRowPad + g * 32 + lane];
-      w[g] = tok >= 0 ? __ldg(x_sf + (int64_t)tok * kt_per_row + kt) : 0x7f7f7f7fu;  // padding: scale 1
+      wv[g] = tok >= 0 ? __ldg(x_sf + (int64_t)tok * kt_per_row + kt) : 0x7f7f7f7fu;
     }
-    *reinterpret_cast<uint4*>(xg_sf + sf_tile_offset(rb, kt, kt_per_row) + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(xg_sf + sf_tile_offset(rb, kt, kt_per_row) + lane * 16) =
+        make_uint4(wv[0], wv[1], wv[2], wv[3]);
   }
-  const uint4 z = make_uint4(0, 0, 0, 0);
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < out_vecs; i += (int64_t)gridDim.x * blockDim.x)
-    out[i] = z;
 }
 
 // Row-major scales sf[rows, K/32] -> blocked tiles (rows % 128 == 0).
@@ -390,13 +425,25 @@ cudaError_t launch_down_mxfp8(const CUtensorMap& act, const CUtensorMap& w2, con
                               cudaStream_t stream, bool pdl) {
   return launch_mx<kMxDown, 3>(act, w2, args, grid, stream, pdl);
 }
-cudaError_t launch_gather_mx(const Workspace& ws, const void* x, const void* x_sf, int D, void* out, int64_t out_bytes,
-                             int grid, cudaStream_t stream) {
-  gather_rows_mx_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x), static_cast<const uint32_t*>(x_sf),
-                                                  ws.row_tok, ws.meta, static_cast<uint4*>(ws.xg),
-                                                  static_cast<uint8_t*>(ws.xg_sf), D, static_cast<uint4*>(out),
-                                                  out_bytes / 16);
-  return cudaGetLastError();
+cudaError_t launch_gather_mx(const Workspace& ws, const void* x, const void* x_sf, const int32_t* topk_ids, int T,
+                             int E, int k, int D, void* out, int64_t out_bytes, int grid, cudaStream_t stream,
+                             bool pdl) {
+  if (T == 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gather_tokens_mx_kernel, static_cast<const uint4*>(x),
+                            static_cast<const uint32_t*>(x_sf), topk_ids, static_cast<const int*>(ws.slot_of_pair),
+                            static_cast<const int*>(ws.offsets), static_cast<const int*>(ws.pad_offsets),
+                            static_cast<const int*>(ws.row_tok), static_cast<const int*>(ws.meta), T, E, k, D / 16,
+                            D / 128, static_cast<uint4*>(ws.xg), static_cast<uint8_t*>(ws.xg_sf),
+                            static_cast<uint4*>(out), out ? (int)(out_bytes / 16 / T) : 0);
 }
 cudaError_t launch_pack_sf(const void* sf, void* packed, int64_t rows, int K, int grid, cudaStream_t stream) {
   pack_sf_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint32_t*>(sf), static_cast<uint8_t*>(packed), rows, K);

@@ -32,7 +32,13 @@ static_assert(kPSmem <= 232448, "shared memory");
 constexpr uint64_t kPDrainNs = 200ull * 1000 * 1000;
 
 __device__ __forceinline__ float p_u2f(uint32_t u) { return __uint_as_float(u); }
-__device__ __forceinline__ float p_swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
+// silu(g) * u with the optional clamp (lim = +inf when off): g <= lim,
+// -lim <= u <= lim.
+__device__ __forceinline__ float p_swiglu(float g, float u, float lim) {
+  g = fminf(g, lim);
+  u = fminf(fmaxf(u, -lim), lim);
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
 
 __global__ void __launch_bounds__(kPThreads, 1)
     up_pair_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
@@ -49,6 +55,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float swiglu_lim = args.swiglu_limit > 0.f ? args.swiglu_limit : __int_as_float(0x7f800000);
   const WaitCtl wc{abort_flag, args.err, args.wait_limit_ns};
 
   if (threadIdx.x == 0) {
@@ -168,8 +175,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              pk[i] = pack_bf16x2(p_swiglu(p_u2f(g[2 * i]), p_u2f(u[2 * i])),
-                                  p_swiglu(p_u2f(g[2 * i + 1]), p_u2f(u[2 * i + 1])));
+              pk[i] = pack_bf16x2(p_swiglu(p_u2f(g[2 * i]), p_u2f(u[2 * i]), swiglu_lim),
+                                  p_swiglu(p_u2f(g[2 * i + 1]), p_u2f(u[2 * i + 1]), swiglu_lim));
 #pragma unroll
             for (int q = 0; q < 4; ++q)
               st_global_v4(dst + c * 32 + q * 8, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);

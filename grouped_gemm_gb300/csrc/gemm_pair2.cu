@@ -62,7 +62,13 @@ constexpr uint64_t kQDrainNs = 200ull * 1000 * 1000;
 constexpr uint64_t kQSettleNs = 2ull * 1000 * 1000;  // abort path: copies in flight land well within this
 
 __device__ __forceinline__ float q_u2f(uint32_t u) { return __uint_as_float(u); }
-__device__ __forceinline__ float q_swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
+// silu(g) * u with the optional clamp (lim = +inf when off): g <= lim,
+// -lim <= u <= lim.
+__device__ __forceinline__ float q_swiglu(float g, float u, float lim) {
+  g = fminf(g, lim);
+  u = fminf(fmaxf(u, -lim), lim);
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
 
 // N of a swap-AB pair tile (routed rows of the pair rounded up to 16), or 0
 // for a normal tile.  Every role of both CTAs derives it from the same tables.
@@ -96,6 +102,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float swiglu_lim = args.swiglu_limit > 0.f ? args.swiglu_limit : __int_as_float(0x7f800000);
   const WaitCtl wc{abort_flag, args.err, args.wait_limit_ns};
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
@@ -283,8 +290,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
           if (row < cn) {
             const int tok = args.row_tok[slot0 + h0 + row];
             if (tok >= 0) {
-              bulk_reduce_add_bf16(static_cast<__nv_bfloat16*>(args.out) + (int64_t)tok * args.D + col,
-                                   sStage + row * kQStageRow, 256);
+              bulk_reduce_add_bf16_hint(static_cast<__nv_bfloat16*>(args.out) + (int64_t)tok * args.D + col,
+                                   sStage + row * kQStageRow, 256, args.out_hint != 0, l2_policy_evict_last());
               bulk_commit();
             }
           }
@@ -300,8 +307,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-              pk[i] = pack_bf16x2(q_swiglu(q_u2f(g[2 * i]), q_u2f(u[2 * i])),
-                                  q_swiglu(q_u2f(g[2 * i + 1]), q_u2f(u[2 * i + 1])));
+              pk[i] = pack_bf16x2(q_swiglu(q_u2f(g[2 * i]), q_u2f(u[2 * i]), swiglu_lim),
+                                  q_swiglu(q_u2f(g[2 * i + 1]), q_u2f(u[2 * i + 1]), swiglu_lim));
 #pragma unroll
             for (int q = 0; q < 4; ++q)
               st_shared_v4(my_stage + c * 64 + q * 16, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
@@ -340,7 +347,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
           }
           if (tok >= 0) {
             fence_proxy_async_smem();
-            bulk_reduce_add_bf16(orow + h * 128, my_stage, 256);
+            bulk_reduce_add_bf16_hint(orow + h * 128, my_stage, 256, args.out_hint != 0, l2_policy_evict_last());
             bulk_commit();
           }
         }

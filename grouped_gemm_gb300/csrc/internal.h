@@ -7,6 +7,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 namespace moe {
 
 constexpr int kBM = 128;          // rows per tile = tcgen05 MMA M
@@ -44,7 +46,12 @@ struct Workspace {
   // Not a region of the workspace: the call's router logits [T, E] fp32 when
   // the call starts from them (moe_ffn_forward_logits), else nullptr.
   const float* router_logits;
+  unsigned long long wait_limit_ns;  // bound of every device wait of the call
 };
+
+// MOE_OPT_ROUTE_COOP: 1 (default) routes problems too large for the
+// single-block kernel in one cooperative launch; 0 uses three launches.
+extern std::atomic<int> g_route_coop;
 
 // pipeline = kRouteOnly plans only the routing regions (the common prefix of
 // every layout).
@@ -74,6 +81,8 @@ struct GemmArgs {
   int swap_ab;              // 1: tail row blocks of <= 112 rows run as swap-AB tiles
   int pair_swap_max;        // CTA-pair down kernel: pairs with at most this many routed rows
                             //   run as swap-AB tiles (0 = never)
+  int out_hint;             // 1: reductions into out carry an L2 evict_last hint
+  float swiglu_limit;       // > 0: gate clamped to <= limit, up to [-limit, limit] before SwiGLU
 };
 
 // Routing; when zero_out != nullptr the first launch also zero-fills
@@ -130,6 +139,7 @@ struct FusedArgs {
   int D, H;
   int n_slices;             // H / 128
   int stall_test;           // test hook (see GemmArgs)
+  float swiglu_limit;       // > 0: gate clamped to <= limit, up to [-limit, limit] before SwiGLU
 };
 
 cudaError_t launch_fused_bf16(const CUtensorMap& map_xg, const CUtensorMap& map_w1, const CUtensorMap& map_w2,
@@ -155,6 +165,8 @@ struct FusedClusterArgs {
   int s1;                   // GEMM1 sub-chunks per CTA: h1 * s1 = H / C
   int s2;                   // GEMM2 sub-chunks per CTA: 256 * s2 = D / C
   int stall_test;           // test hook (see GemmArgs)
+  int out_hint;             // 1: reductions into out carry an L2 evict_last hint
+  float swiglu_limit;       // > 0: gate clamped to <= limit, up to [-limit, limit] before SwiGLU
 };
 // Act columns per GEMM1 sub-chunk for cluster size C, or 0 if (D, H) cannot
 // run on clusters of C.
@@ -191,6 +203,8 @@ struct FusedClusterMxArgs {
   int s1;                   // GEMM1 sub-chunks per CTA: 128 * s1 = H / C
   int s2;                   // GEMM2 sub-chunks per CTA: 256 * s2 = D / C
   int stall_test;           // test hook (see GemmArgs)
+  int out_hint;             // 1: reductions into out carry an L2 evict_last hint
+  float swiglu_limit;       // > 0: gate clamped to <= limit, up to [-limit, limit] before SwiGLU
 };
 inline bool fused_cluster_mx_fits(int D, int H, int C) {
   return (C == 1 || C == 2 || C == 4 || C == 8) && D % (256 * C) == 0 && H % (128 * C) == 0;
@@ -222,14 +236,17 @@ struct MxArgs {
   int n_col_tiles;
   int k_blocks;             // K / 128
   int stall_test;           // test hook (see GemmArgs)
+  int out_hint;             // 1: reductions into out carry an L2 evict_last hint
+  float swiglu_limit;       // > 0: gate clamped to <= limit, up to [-limit, limit] before SwiGLU
 };
 
 cudaError_t launch_up_mxfp8(const CUtensorMap& a, const CUtensorMap& w1, const MxArgs& args, int grid,
                             cudaStream_t stream);
 cudaError_t launch_down_mxfp8(const CUtensorMap& act, const CUtensorMap& w2, const MxArgs& args, int grid,
                               cudaStream_t stream, bool pdl);
-cudaError_t launch_gather_mx(const Workspace& ws, const void* x, const void* x_sf, int D, void* out, int64_t out_bytes,
-                             int grid, cudaStream_t stream);
+cudaError_t launch_gather_mx(const Workspace& ws, const void* x, const void* x_sf, const int32_t* topk_ids, int T,
+                             int E, int k, int D, void* out, int64_t out_bytes, int grid, cudaStream_t stream,
+                             bool pdl);
 cudaError_t launch_pack_sf(const void* sf, void* packed, int64_t rows, int K, int grid, cudaStream_t stream);
 cudaError_t launch_mx_quantize(const float* in, int64_t n, uint8_t* q, uint8_t* sf, cudaStream_t stream);
 
@@ -246,6 +263,7 @@ struct FusedMxArgs {
   unsigned long long wait_limit_ns;
   int D, H;
   int stall_test;
+  float swiglu_limit;       // > 0: gate clamped to <= limit, up to [-limit, limit] before SwiGLU
 };
 cudaError_t launch_fused_mxfp8(const CUtensorMap& map_xg, const CUtensorMap& map_w1, const CUtensorMap& map_w2,
                                const FusedMxArgs& args, int grid, cudaStream_t stream);

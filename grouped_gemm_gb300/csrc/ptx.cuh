@@ -214,6 +214,21 @@ __device__ __forceinline__ void bulk_reduce_add_bf16(void* gdst, const void* ssr
                "r"(smem_addr(ssrc)), "r"(bytes)
                : "memory");
 }
+// bulk_reduce_add_bf16 with an L2 eviction-priority hint when `hint` is set
+// (policy from createpolicy, e.g. evict_last to keep a reduction target that
+// about fits in L2 resident while operand tiles stream past it).
+__device__ __forceinline__ void bulk_reduce_add_bf16_hint(void* gdst, const void* ssrc, uint32_t bytes, bool hint,
+                                                          uint64_t policy) {
+  if (!hint) {
+    bulk_reduce_add_bf16(gdst, ssrc, bytes);
+    return;
+  }
+  asm volatile(
+      "cp.reduce.async.bulk.global.shared::cta.bulk_group.L2::cache_hint.add.noftz.bf16 [%0], [%1], %2, %3;" ::"l"(
+          gdst),
+      "r"(smem_addr(ssrc)), "r"(bytes), "l"(policy)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_reduce_add_f32(void* gdst, const void* ssrc, uint32_t bytes) {
   asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst),
                "r"(smem_addr(ssrc)), "r"(bytes)

@@ -17,6 +17,8 @@
 
 #include <climits>
 #include <cmath>
+#include <map>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -490,6 +492,261 @@ __global__ void __launch_bounds__(1024)
   scatter_range<kRouter>(ids, topk_w, q0, q1, E, k, wcnt + warp * E, s_off, s_poff, row_tok, slot_w, slot_of_pair);
 }
 
+// ---------------------------------------------------------------- one launch
+// The whole routing permutation in ONE cooperative launch of NB = route_blocks
+// blocks (all co-resident), for problems too large for the single-block
+// kernel: the three phases of the three-kernel path separated by two grid
+// barriers instead of two kernel boundaries.
+//   A. per-warp histograms of contiguous pair ranges (the router first, when
+//      logits are given); block totals to blk[b][e].  Block 0 sets meta to
+//      "no row blocks" and every block marks its pairs' slots and its share
+//      of the padded slots -1, so that if a barrier ever runs out the GEMMs
+//      that follow find nothing to do rather than stale tables.
+//   B. each expert's column is scanned (by one warp when NB <= 64, else by
+//      one block): blk[.][e] becomes the exclusive prefix over blocks,
+//      counts[e] the total.
+//   C. every block scans counts over experts (offsets, padded offsets);
+//      block 0 writes the expert tables (offsets, pad_offsets, expert_of_rb,
+//      pair_info, padding rows, meta); every block scatters its own pairs with
+//      the stable warp-match scatter.
+// Grid barrier: err[4] counts arrivals, err[5] is the generation; both are
+// zero at rest (status words, cleared with them).  Waits are bounded.
+constexpr int kCoopWarps = 8;
+
+struct CoopRouteArgs {
+  const int32_t* ids;
+  const float* topk_w;
+  const float* logits;   // router mode when set: ids / topk_w are written first
+  int32_t* ids_out;
+  float* w_out;
+  int64_t P;
+  int E, k, NB;
+  int* err;
+  unsigned long long wait_limit_ns;
+  int* blk;
+  int* counts;
+  int* offsets;
+  int* pad_offsets;
+  int* meta;
+  int* expert_of_rb;
+  int* pair_info;
+  int* row_tok;
+  float* slot_w;
+  int* slot_of_pair;
+  int64_t S_max;
+};
+
+__device__ bool coop_grid_sync(const CoopRouteArgs& a, int site) {
+  __syncthreads();
+  int ok = 1;
+  if (threadIdx.x == 0) {
+    volatile int* gen = a.err + 5;
+    const int g = *gen;
+    __threadfence();
+    if (atomicAdd(a.err + 4, 1) == a.NB - 1) {
+      atomicExch(a.err + 4, 0);
+      __threadfence();
+      atomicAdd(a.err + 5, 1);
+    } else {
+      const uint64_t t0 = globaltimer_ns();
+      for (uint32_t it = 1; *gen == g; ++it) {
+        if ((it & 63) == 0 && globaltimer_ns() - t0 > a.wait_limit_ns) {
+          atomicOr(a.err, kErrTimeout);
+          atomicCAS(a.err + 1, 0, site);
+          ok = 0;
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  return __syncthreads_and(ok) != 0;
+}
+
+template <bool kRouter>
+__global__ void __launch_bounds__(kCoopWarps * 32) route_coop_kernel(const CoopRouteArgs a) {
+  extern __shared__ int sm[];
+  int* wcnt = sm;                       // [kCoopWarps][E] per-warp counts, then bases
+  int* s_off = wcnt + kCoopWarps * a.E;  // [E]
+  int* s_poff = s_off + a.E;            // [E]
+  int* s_cnt = s_poff + a.E;            // [E]
+  int* s_qoff = s_cnt + a.E;            // [E]
+  __shared__ int warp_sums[32];
+  const int E = a.E, k = a.k, b = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t p0 = (int64_t)b * kRouteTokPerBlock * k;
+  const int64_t p1 = min(a.P, p0 + (int64_t)kRouteTokPerBlock * k);
+  const int64_t sub = (p1 - p0 + kCoopWarps - 1) / kCoopWarps;
+  const int64_t q0 = min(p1, p0 + warp * sub), q1 = min(p1, q0 + sub);
+  const int32_t* ids = a.ids;
+  const float* tw = a.topk_w;
+
+  // ---- A
+  if (b == 0 && threadIdx.x == 0) {
+    a.meta[0] = 0;
+    a.meta[1] = 0;
+  }
+  for (int64_t p = p0 + threadIdx.x; p < p1; p += blockDim.x) a.slot_of_pair[p] = -1;
+  for (int64_t r = (int64_t)b * blockDim.x + threadIdx.x; r < a.S_max; r += (int64_t)a.NB * blockDim.x)
+    a.row_tok[r] = -1;
+  for (int i = threadIdx.x; i < kCoopWarps * E; i += blockDim.x) wcnt[i] = 0;
+  if constexpr (kRouter) {
+    const int t0 = b * kRouteTokPerBlock;
+    router_tokens_any(a.logits, E, k, t0, t0 + (int)((p1 - p0) / k), a.ids_out, a.w_out, nullptr);
+    ids = a.ids_out;
+    tw = a.w_out;
+  }
+  __syncthreads();
+  bool bad = false;
+  for (int64_t p = q0 + lane; p < q1; p += 32) {
+    const int e = load_i32<kRouter>(ids + p);
+    if ((unsigned)e < (unsigned)E) atomicAdd(&wcnt[warp * E + e], 1);
+    else bad = true;
+  }
+  if (bad) atomicOr(a.err, kErrBadRouting);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int t = 0;
+    for (int w = 0; w < kCoopWarps; ++w) t += wcnt[w * E + e];
+    a.blk[(int64_t)b * E + e] = t;
+  }
+  if (!coop_grid_sync(a, 80)) return;
+
+  // ---- B: exclusive prefix over blocks of each expert's column: one warp per
+  // expert (warps of all blocks share the experts) when the column is short,
+  // else one block per expert, 256 blocks per step
+  if (a.NB <= 64) {
+    for (int e = b * kCoopWarps + warp; e < E; e += a.NB * kCoopWarps) {
+      int carry = 0;
+      for (int c0 = 0; c0 < a.NB; c0 += 32) {
+        const int bb = c0 + lane;
+        const int v = bb < a.NB ? a.blk[(int64_t)bb * E + e] : 0;
+        int x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        if (bb < a.NB) a.blk[(int64_t)bb * E + e] = carry + x - v;
+        carry += __shfl_sync(0xffffffffu, x, 31);
+      }
+      if (lane == 0) a.counts[e] = carry;
+    }
+  } else {
+    for (int e = b; e < E; e += a.NB) {
+      int carry = 0;
+      for (int c0 = 0; c0 < a.NB; c0 += blockDim.x) {
+        const int bb = c0 + threadIdx.x;
+        const int v = bb < a.NB ? a.blk[(int64_t)bb * E + e] : 0;
+        int x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_sums[warp] = x;
+        __syncthreads();
+        int wbase = 0, tot = 0;
+        for (int w = 0; w < kCoopWarps; ++w) {
+          const int sw = warp_sums[w];
+          if (w < warp) wbase += sw;
+          tot += sw;
+        }
+        if (bb < a.NB) a.blk[(int64_t)bb * E + e] = carry + wbase + x - v;
+        carry += tot;
+        __syncthreads();
+      }
+      if (threadIdx.x == 0) a.counts[e] = carry;
+    }
+  }
+  if (!coop_grid_sync(a, 81)) return;
+
+  // ---- C: scans over experts (every block), tables (block 0), scatter (all)
+  int warp_tot[3];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = a.counts[e];
+  __syncthreads();
+  // serial-in-thread chunks: thread i owns experts [i*per, (i+1)*per)
+  const int per = (E + blockDim.x - 1) / blockDim.x;
+  int c_sum = 0, pc_sum = 0, q_sum = 0;
+  const int e0 = threadIdx.x * per;
+  for (int e = e0; e < min(E, e0 + per); ++e) {
+    const int c = s_cnt[e], pc = (c + kRowPad - 1) / kRowPad * kRowPad;
+    c_sum += c;
+    pc_sum += pc;
+    q_sum += (pc / kRowPad + 1) / 2;
+  }
+  // block-wide exclusive scans of the three per-thread sums
+  int vals[3] = {c_sum, pc_sum, q_sum}, excl[3];
+#pragma unroll
+  for (int q = 0; q < 3; ++q) {
+    int x = vals[q];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    int wbase = 0, tot = 0;
+    for (int w = 0; w < kCoopWarps; ++w) {
+      const int sw = warp_sums[w];
+      if (w < warp) wbase += sw;
+      tot += sw;
+    }
+    excl[q] = wbase + x - vals[q];
+    warp_tot[q] = tot;
+    __syncthreads();
+  }
+  {
+    int off = excl[0], poff = excl[1], qoff = excl[2];
+    for (int e = e0; e < min(E, e0 + per); ++e) {
+      const int c = s_cnt[e], pc = (c + kRowPad - 1) / kRowPad * kRowPad;
+      s_off[e] = off;
+      s_poff[e] = poff;
+      s_qoff[e] = qoff;
+      if (b == 0) {
+        a.offsets[e] = off;
+        a.pad_offsets[e] = poff;
+      }
+      off += c;
+      poff += pc;
+      qoff += (pc / kRowPad + 1) / 2;
+    }
+  }
+  __syncthreads();
+  if (b == 0) {
+    // padding rows, block -> expert and pairs of every expert, one warp per expert
+    for (int e = warp; e < E; e += kCoopWarps) {
+      const int c = s_cnt[e], po = s_poff[e];
+      const int pc = (c + kRowPad - 1) / kRowPad * kRowPad;
+      for (int s2 = po + c + lane; s2 < po + pc; s2 += 32) a.slot_w[s2] = 0.f;  // row_tok is -1 already
+      for (int rb = po / kRowPad + lane; rb < (po + pc) / kRowPad; rb += 32) a.expert_of_rb[rb] = e;
+      fill_pairs(e, lane, po, pc, s_qoff[e], a.pair_info);
+    }
+    if (threadIdx.x == 0) {
+      a.offsets[E] = warp_tot[0];
+      a.pad_offsets[E] = warp_tot[1];
+      a.meta[2] = 0;  // tile counters of the GEMM kernels that follow
+      a.meta[3] = 0;
+      a.meta[1] = warp_tot[2];
+      __threadfence();
+      a.meta[0] = warp_tot[1] / kRowPad;
+    }
+  }
+  // this block's per-warp bases: blk[b][e] (prefix over blocks) + earlier warps
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int acc = a.blk[(int64_t)b * E + e];
+    for (int w = 0; w < kCoopWarps; ++w) {
+      const int c = wcnt[w * E + e];
+      wcnt[w * E + e] = acc;
+      acc += c;
+    }
+  }
+  __syncthreads();
+  scatter_range<kRouter>(ids, tw, q0, q1, E, k, wcnt + warp * E, s_off, s_poff, a.row_tok, a.slot_w,
+                         a.slot_of_pair);
+}
+
 // Token-major gather: xg[padded slot of pair p, :] = x[t, :] for the k pairs
 // p = t*k + j of every token t.  One warp per (token, 4 KB chunk of its row):
 // the chunk is read once into registers (16-byte vector loads, eight per lane)
@@ -551,6 +808,46 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace
 
+namespace {
+
+size_t route_coop_smem(int E) { return sizeof(int) * (size_t)(kCoopWarps + 4) * E; }
+
+// Whether NB routing blocks can all be resident at once (checked once per
+// device and expert count; a cooperative launch also refuses otherwise).
+bool route_coop_fits(int NB, int E) {
+  if (g_route_coop.load() == 0) return false;
+  static std::mutex mu;
+  static std::map<std::pair<int, int>, int> cap;  // (device, E) -> resident blocks
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lk(mu);
+  auto key = std::make_pair(dev, E);
+  auto it = cap.find(key);
+  if (it == cap.end()) {
+    int per_sm = 0, sms = 0, coop = 0;
+    const size_t smem = route_coop_smem(E);
+    if (smem > 48 * 1024 &&
+        cudaFuncSetAttribute(route_coop_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    if (smem > 48 * 1024)
+      cudaFuncSetAttribute(route_coop_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_coop_kernel<true>, kCoopWarps * 32, smem) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    it = cap.emplace(key, coop ? per_sm * sms : 0).first;
+  }
+  return NB >= 2 && NB <= it->second;
+}
+
+}  // namespace
+
 cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const float* topk_w, int T, int E, int k,
                          cudaStream_t stream, void* zero_out, int64_t zero_bytes, int zero_grid, bool pdl) {
   const int64_t P = (int64_t)T * k;
@@ -570,6 +867,43 @@ cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const flo
     return cudaGetLastError();
   }
   const int NB = ws.route_blocks;
+  if (!zero_out && route_coop_fits(NB, E)) {
+    CoopRouteArgs ca{};
+    ca.ids = topk_ids;
+    ca.topk_w = topk_w;
+    ca.logits = logits;
+    ca.ids_out = ids_out;
+    ca.w_out = w_out;
+    ca.P = P;
+    ca.E = E;
+    ca.k = k;
+    ca.NB = NB;
+    ca.err = ws.err;
+    ca.wait_limit_ns = ws.wait_limit_ns;
+    ca.blk = ws.blk_base;
+    ca.counts = ws.counts;
+    ca.offsets = ws.offsets;
+    ca.pad_offsets = ws.pad_offsets;
+    ca.meta = ws.meta;
+    ca.expert_of_rb = ws.expert_of_rb;
+    ca.pair_info = ws.pair_info;
+    ca.row_tok = ws.row_tok;
+    ca.slot_w = ws.slot_w;
+    ca.slot_of_pair = ws.slot_of_pair;
+    ca.S_max = ws.S_max;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(NB);
+    cfg.blockDim = dim3(kCoopWarps * 32);
+    cfg.dynamicSmemBytes = route_coop_smem(E);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return logits ? cudaLaunchKernelEx(&cfg, route_coop_kernel<true>, ca)
+                  : cudaLaunchKernelEx(&cfg, route_coop_kernel<false>, ca);
+  }
   const int grid = zero_out ? (NB > zero_grid ? NB : zero_grid) : NB;
   route_count_kernel<<<grid, 256, E * sizeof(int), stream>>>(topk_ids, P, E, k, NB, ws.blk_base, ws.err,
                                                              static_cast<uint4*>(zero_out), zero_bytes / 16, logits,

@@ -247,7 +247,24 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   Measured on GB300 at prefill: down kernel 0.115 ms with
  *                   0, 0.121 with 128, 0.141 with 256 (the transposing
  *                   epilogue costs more than the MMA work saved; the kernel
- *                   is bound by streaming the weights). */
+ *                   is bound by streaming the weights).
+ *   MOE_OPT_ROUTE_COOP  1 (default) or 0: routing of problems too large for
+ *                   the single-block kernel (more than 8192 pairs or 256
+ *                   experts) runs as ONE cooperative launch whose blocks meet
+ *                   at two bounded grid barriers (the workspace's status
+ *                   words hold the barrier state), when all its blocks fit on
+ *                   the device at once; 0 (or too many blocks) uses three
+ *                   launches (histograms, scans, scatter).
+ *   MOE_OPT_OUT_L2_HINT  0 (default), 1 or 2: the bulk reductions into out
+ *                   carry an L2 evict_last hint, so that an out of about the
+ *                   L2's size may stay resident while the weights stream past
+ *                   it instead of being read and written back for each of a
+ *                   token's k contributions.  1 applies it when out is at
+ *                   most 160 MiB, 2 always, 0 never.  Measured on GB300 at
+ *                   mxfp8 (out 134 MB): split 2.12 -> 2.10 ms, fused 2.28 ->
+ *                   2.34 ms; large_skewed unchanged.
+ *   MOE_OPT_GATHER_BLOCKS  1..16 (default 4): blocks per SM of the row-gather
+ *                   kernels (bytes in flight against HBM latency). */
 typedef enum {
   MOE_OPT_GATHER = 0,
   MOE_OPT_L2_PREFETCH = 1,
@@ -258,7 +275,10 @@ typedef enum {
   MOE_OPT_SWAP_AB = 6,
   MOE_OPT_FUSED_CLUSTER = 7,
   MOE_OPT_PAIR_MMA = 8,
-  MOE_OPT_PAIR_SWAP = 9
+  MOE_OPT_PAIR_SWAP = 9,
+  MOE_OPT_ROUTE_COOP = 10,
+  MOE_OPT_OUT_L2_HINT = 11,
+  MOE_OPT_GATHER_BLOCKS = 12
 } moe_option_t;
 moe_status_t moe_ffn_set_option(int option, long long value);
 

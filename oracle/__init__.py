@@ -67,7 +67,7 @@ def _load():
             lib.oracle_router_topk.argtypes = [c.c_int, c.c_int, c.c_int, c.c_void_p, c.c_void_p, c.c_void_p]
             lib.oracle_router_topk.restype = c.c_int
             lib.oracle_moe_ffn.argtypes = [c.c_int] * 6 + [c.c_void_p] * 8 + [c.c_int, c.c_void_p, c.c_int,
-                                                                               c.c_void_p, c.c_int]
+                                                                               c.c_void_p, c.c_int, c.c_double]
             lib.oracle_moe_ffn.restype = c.c_int
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = c.c_int
@@ -152,12 +152,13 @@ def router_topk(logits: np.ndarray, k: int):
 
 # ---------------------------------------------------------------- forward
 def moe_ffn(x, w1, w2, topk_ids, topk_w, *, act=ACT_BF16, x_sf=None, w1_sf=None, w2_sf=None,
-            tokens=None, threads: int = 0) -> np.ndarray:
+            tokens=None, threads: int = 0, swiglu_limit: float = 0.0) -> np.ndarray:
     """fp64 forward pass.
 
     bf16 inputs are uint16 bit patterns; MXFP8 inputs are uint8 e4m3 codes with
     uint8 e8m0 scale arrays (one per 32 along the last dimension).  Returns
-    float64 out[n_tokens, D] for ``tokens`` (or all T tokens).
+    float64 out[n_tokens, D] for ``tokens`` (or all T tokens).  ``swiglu_limit``
+    > 0 selects the clamped SwiGLU (gate <= limit, |up| <= limit).
     """
     mx = x_sf is not None
     x = np.ascontiguousarray(x)
@@ -180,7 +181,8 @@ def moe_ffn(x, w1, w2, topk_ids, topk_w, *, act=ACT_BF16, x_sf=None, w1_sf=None,
     out = np.zeros((n, D), np.float64)
     rc = _load().oracle_moe_ffn(T, E, D, H, k, IN_MXFP8 if mx else IN_BF16,
                                 _ptr(x), _ptr(x_sf), _ptr(w1), _ptr(w1_sf), _ptr(w2), _ptr(w2_sf),
-                                _ptr(ids), _ptr(tw), act, _ptr(tok), n, _ptr(out), int(threads))
+                                _ptr(ids), _ptr(tw), act, _ptr(tok), n, _ptr(out), int(threads),
+                                float(swiglu_limit))
     if rc != 0:
         raise ValueError(f"oracle_moe_ffn failed ({rc})")
     return out

@@ -260,6 +260,10 @@ static double silu(double g) { return g / (1.0 + exp(-g)); }
  *     e = ids[t][j], w = topk_w[t][j]
  *     g[h] = sum_d W1[e][h][d]   x[t][d]        h < H   (gate rows 0..H-1)
  *     u[h] = sum_d W1[e][H+h][d] x[t][d]                (up rows H..2H-1)
+ *     (clamped variant, swiglu_limit L > 0: g[h] = min(g[h], L),
+ *      u[h] = min(max(u[h], -L), L) first -- the gate from above only, the up
+ *      projection on both sides, as "Porting Block-Scaled GEMM Kernels from
+ *      Blackwell to Rubin" sec. 5.3 describes the gpt-oss-style activation)
  *     a[h] = silu(g[h]) * u[h]
  *     a    = act_round(a)                               (see below)
  *     y[d] = sum_h W2[e][d][h] a[h]
@@ -278,7 +282,7 @@ int oracle_moe_ffn(int T, int E, int D, int H, int k, int in_mode,
                    const void* w2, const uint8_t* w2_sf,
                    const int32_t* ids, const float* topk_w,
                    int act_mode, const int32_t* tokens, int n_tokens,
-                   double* out, int n_threads) {
+                   double* out, int n_threads, double swiglu_limit) {
     if (T < 0 || E < 1 || D < 1 || H < 1 || k < 1) return -1;
     if (act_mode == ORACLE_ACT_MXFP8 && H % 32) return -1;
     if (in_mode == ORACLE_IN_MXFP8 && (D % 32 || H % 32)) return -1;
@@ -328,6 +332,13 @@ int oracle_moe_ffn(int T, int E, int D, int H, int k, int in_mode,
                         }
                         g[h] = sg;
                         u[h] = su;
+                    }
+                    if (swiglu_limit > 0.0) {
+                        for (int h = 0; h < H; ++h) {
+                            if (g[h] > swiglu_limit) g[h] = swiglu_limit;
+                            if (u[h] > swiglu_limit) u[h] = swiglu_limit;
+                            if (u[h] < -swiglu_limit) u[h] = -swiglu_limit;
+                        }
                     }
                     for (int h = 0; h < H; ++h) a[h] = silu(g[h]) * u[h];
                     if (act_mode == ORACLE_ACT_BF16) {

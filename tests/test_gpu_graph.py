@@ -13,9 +13,10 @@ from helpers import assert_close, to_dev
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("T", [300, 2500])  # single-block routing; one cooperative routing launch
 @pytest.mark.parametrize("pipeline", [moe.MOE_SPLIT, moe.MOE_FUSED])
-def test_graph_replay_matches_oracle(pipeline):
-    inp = wl.make_custom(300, 512, 256, 16, 4, seed=21)
+def test_graph_replay_matches_oracle(pipeline, T):
+    inp = wl.make_custom(T, 512, 256, 16, 4, seed=21)
     w = inp["workload"]
     dev = to_dev(inp)
     out = torch.empty(w.T, w.D, dtype=torch.bfloat16, device="cuda")
@@ -41,7 +42,7 @@ def test_graph_replay_matches_oracle(pipeline):
         assert moe.moe_ffn_sync_status(ws) == 0
         assert_close(out, ref, label="graph replay")
     # new routing written into the same input buffers is picked up by the replay
-    inp2 = wl.make_custom(300, 512, 256, 16, 4, seed=22)
+    inp2 = wl.make_custom(T, 512, 256, 16, 4, seed=22)
     dev["topk_ids"].copy_(torch.from_numpy(inp2["topk_ids"]))
     dev["topk_w"].copy_(torch.from_numpy(inp2["topk_w"]))
     g.replay()

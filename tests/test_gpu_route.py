@@ -1,6 +1,8 @@
 """Routing permutation on the GPU is bit-exact against the oracle's counting
 sort ("Prime Flash MoE" sec. 3 and 6: tokens processed in per-expert sorted
-order), including empty experts, one hot expert, repeats and T = 1."""
+order), including empty experts, one hot expert, repeats and T = 1.  Problems
+too large for the single-block kernel run both through the one-launch
+cooperative routing (default) and the three-launch path."""
 import numpy as np
 import pytest
 import torch
@@ -10,6 +12,13 @@ import oracle
 from grouped_gemm_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True, params=[1, 0], ids=["coop", "three_launches"])
+def route_mode(request):
+    moe.moe_ffn_set_option(moe.MOE_OPT_ROUTE_COOP, request.param)
+    yield request.param
+    moe.moe_ffn_set_option(moe.MOE_OPT_ROUTE_COOP, 1)
 
 
 def gpu_route(ids, E):
@@ -49,7 +58,8 @@ def test_route_large_skewed():
     check(ids, w.E)
 
 
-@pytest.mark.parametrize("T,E,k", [(1, 1, 1), (1, 8, 8), (3, 1024, 4), (777, 5, 3), (513, 300, 2)])
+@pytest.mark.parametrize("T,E,k", [(1, 1, 1), (1, 8, 8), (3, 1024, 4), (777, 5, 3), (513, 300, 2), (9000, 1, 1),
+                                   (20000, 1024, 8), (65536, 7, 1), (4097, 128, 8)])
 def test_route_shapes(T, E, k):
     ids, _ = wl.draw_routing(np.random.default_rng(T), T, E, k, "uniform") if k <= E else (None, None)
     check(ids, E)
@@ -67,3 +77,14 @@ def test_route_bad_id_reported():
     st, c, _, s = gpu_route(ids, 8)
     assert st == 4  # MOE_ERR_BAD_ROUTING
     assert c.sum() == 19 and s[9] == -1
+
+
+def test_route_bad_id_reported_multi_block():
+    rng = np.random.default_rng(9)
+    ids = rng.integers(0, 16, size=(6000, 2)).astype(np.int32)
+    ids[4321, 0] = -3
+    st, c, _, s = gpu_route(ids, 16)
+    assert st == 4  # MOE_ERR_BAD_ROUTING
+    assert c.sum() == 6000 * 2 - 1 and s[4321 * 2] == -1
+    ref = oracle.route(np.where(ids < 0, 0, ids), 16)
+    assert c[0] == ref["counts"][0] - 1
