@@ -14,7 +14,8 @@ import threading
 
 __all__ = [
     "MOE_BF16", "MOE_MXFP8", "MOE_FUSED", "MOE_SPLIT", "MoeFFNError", "library_path", "lib",
-    "moe_ffn_workspace_size", "moe_ffn_workspace_init", "moe_ffn_forward", "moe_ffn_forward_logits", "moe_ffn_router_topk", "moe_ffn_route", "moe_ffn_route_noalloc",
+    "moe_ffn_workspace_size", "moe_ffn_workspace_init", "moe_ffn_forward", "moe_ffn_forward_logits", "moe_ffn_forward_ex", "MoeFFNExtras",
+    "moe_ffn_workspace_size_ex", "moe_ffn_router_topk", "moe_ffn_route", "moe_ffn_route_noalloc",
     "moe_ffn_sync_status", "moe_ffn_set_wait_limit_ns", "moe_ffn_profile_enable", "moe_ffn_profile_read", "moe_ffn_profile_stage_kernel", "moe_ffn_set_option", "MOE_OPT_GATHER", "moe_ffn_prepare_mxfp8_weights", "moe_ffn_debug_mx_quantize", "moe_ffn_status_string", "alloc_workspace",
 ]
 
@@ -26,6 +27,11 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
 
 _lock = threading.Lock()
 _lib = None
+
+
+class MoeFFNExtras(ctypes.Structure):
+    """moe_ffn_extras_t: clamped SwiGLU limit, shared experts, router logits."""
+    _fields_ = [("swiglu_limit", ctypes.c_float), ("n_shared", ctypes.c_int), ("router_logits", ctypes.c_void_p)]
 
 
 class MoeFFNError(RuntimeError):
@@ -59,6 +65,10 @@ def lib() -> ctypes.CDLL:
             L.moe_ffn_router_topk.restype = i
             L.moe_ffn_forward_logits.argtypes = [vp] * 10 + [i] * 7 + [vp, sz, vp]
             L.moe_ffn_forward_logits.restype = i
+            L.moe_ffn_workspace_size_ex.argtypes = [i] * 8
+            L.moe_ffn_workspace_size_ex.restype = sz
+            L.moe_ffn_forward_ex.argtypes = [vp] * 9 + [i] * 7 + [c.POINTER(MoeFFNExtras), vp, sz, vp]
+            L.moe_ffn_forward_ex.restype = i
             L.moe_ffn_route.argtypes = [vp, vp, i, i, i, vp, vp, vp, vp, sz, vp]
             L.moe_ffn_route.restype = i
             L.moe_ffn_route_noalloc.argtypes = [vp, vp, i, i, i, vp, vp, vp, vp, vp]
@@ -122,10 +132,15 @@ def moe_ffn_workspace_init(workspace, stream=None) -> int:
                                                _stream(stream)), "moe_ffn_workspace_init")
 
 
-def alloc_workspace(T, E, D, H, k, dtype=MOE_BF16, pipeline=MOE_SPLIT, device="cuda"):
-    """A caller-owned workspace tensor of the right size, status words zeroed."""
+def moe_ffn_workspace_size_ex(T, E, D, H, k, n_shared, dtype=MOE_BF16, pipeline=MOE_SPLIT) -> int:
+    return lib().moe_ffn_workspace_size_ex(T, E, D, H, k, n_shared, dtype, pipeline)
+
+
+def alloc_workspace(T, E, D, H, k, dtype=MOE_BF16, pipeline=MOE_SPLIT, device="cuda", n_shared=0):
+    """A caller-owned workspace tensor of the right size, status words zeroed
+    (sized for moe_ffn_forward_ex with n_shared shared experts)."""
     import torch
-    n = moe_ffn_workspace_size(T, E, D, H, k, dtype, pipeline)
+    n = moe_ffn_workspace_size_ex(T, E, D, H, k, n_shared, dtype, pipeline)
     if n == 0:
         raise MoeFFNError(1, "moe_ffn_workspace_size")
     ws = torch.empty(n, dtype=torch.uint8, device=device)
@@ -153,6 +168,19 @@ def moe_ffn_forward_logits(x, w1, w2, router_logits, topk_ids, topk_w, out, *, E
                                       _p(topk_ids), _p(topk_w), _p(out), T, E, D, H, k, dtype, pipeline,
                                       _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     return _check(st, "moe_ffn_forward_logits") if check else st
+
+
+def moe_ffn_forward_ex(x, w1, w2, topk_ids, topk_w, out, *, E, D, H, k, workspace, dtype=MOE_BF16,
+                       pipeline=MOE_SPLIT, x_sf=None, w1_sf=None, w2_sf=None, T=None, swiglu_limit=0.0, n_shared=0,
+                       router_logits=None, stream=None, check=True) -> int:
+    """moe_ffn_forward with a clamped SwiGLU (swiglu_limit > 0), n_shared shared
+    experts stored after the E routed ones, and/or router logits [T, E]."""
+    T = x.shape[0] if T is None else T
+    ex = MoeFFNExtras(float(swiglu_limit), int(n_shared), _p(router_logits))
+    st = lib().moe_ffn_forward_ex(_p(x), _p(x_sf), _p(w1), _p(w1_sf), _p(w2), _p(w2_sf), _p(topk_ids), _p(topk_w),
+                                  _p(out), T, E, D, H, k, dtype, pipeline, ctypes.byref(ex), _p(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream))
+    return _check(st, "moe_ffn_forward_ex") if check else st
 
 
 def moe_ffn_router_topk(logits, k, topk_ids, topk_w, T=None, E=None, stream=None, check=True) -> int:

@@ -27,7 +27,7 @@ std::atomic<int> g_fused_cluster{1};  // MOE_OPT_FUSED_CLUSTER: 0 off, 1 automat
 std::atomic<int> g_pair_mma{2};       // MOE_OPT_PAIR_MMA: 0 off, 1 on, 2 automatic (not for small problems)
 std::atomic<int> g_swap_ab{0};        // MOE_OPT_SWAP_AB: swap-AB tail tiles (measured slower on GB300: off)
 std::atomic<int> g_out_hint{0};       // MOE_OPT_OUT_L2_HINT: 0 off (measured no gain), 1 automatic, 2 always
-std::atomic<int> g_gather_blocks{4};  // MOE_OPT_GATHER_BLOCKS: gather blocks per SM
+std::atomic<int> g_gather_blocks{8};  // MOE_OPT_GATHER_BLOCKS: gather blocks per SM
 std::atomic<int> g_pair_swap{0};      // MOE_OPT_PAIR_SWAP: max routed rows of a swap-AB pair tile (measured slower: off)
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -261,6 +261,7 @@ moe_status_t forward_fused_cluster_bf16(const Workspace& ws, const void* x, cons
   fa.s1 = H / C / h1;
   fa.s2 = D / C / kFusedClusterN;
   fa.stall_test = g_stall_test.load();
+  fa.swiglu_limit = ws.swiglu_limit;
   prof_front(false);
   prof_kernel(2, "fused_cluster_bf16");
   prof_kernel(3, "none");
@@ -306,6 +307,7 @@ moe_status_t forward_fused_bf16(const Workspace& ws, const void* x, const void* 
   fa.H = H;
   fa.n_slices = H / 128;
   fa.stall_test = g_stall_test.load();
+  fa.swiglu_limit = ws.swiglu_limit;
   const int grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * fa.n_slices);
   prof_front(false);
   prof_kernel(2, "fused_moe_bf16");
@@ -351,6 +353,7 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
   ma.D = D;
   ma.H = H;
   ma.stall_test = g_stall_test.load();
+  ma.swiglu_limit = ws.swiglu_limit;
   ma.out_hint = out_hint_for((int64_t)T * D * 2);
   MxArgs up = ma;
   up.sf_a = ws.xg_sf;
@@ -437,6 +440,7 @@ moe_status_t forward_fused_cluster_mxfp8(const Workspace& ws, const void* x, con
   fa.s1 = H / C / 128;
   fa.s2 = D / C / 256;
   fa.stall_test = g_stall_test.load();
+  fa.swiglu_limit = ws.swiglu_limit;
   prof_front(true);
   prof_kernel(2, "fused_cluster_mxfp8");
   prof_kernel(3, "none");
@@ -489,6 +493,7 @@ moe_status_t forward_fused_mxfp8(const Workspace& ws, const void* x, const void*
   fa.D = D;
   fa.H = H;
   fa.stall_test = g_stall_test.load();
+  fa.swiglu_limit = ws.swiglu_limit;
   const int grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * (H / 128));
   prof_front(true);
   prof_kernel(2, "fused_moe_mxfp8");
@@ -609,7 +614,8 @@ moe_status_t moe_ffn_route(const int32_t* topk_ids, const float* topk_w, int T, 
 static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w1, const void* w1_sf, const void* w2,
                                   const void* w2_sf, const int32_t* topk_ids, const float* topk_w, void* out, int T,
                                   int E, int D, int H, int k, int dtype, int pipeline, void* workspace,
-                                  size_t workspace_bytes, void* stream, const float* router_logits) {
+                                  size_t workspace_bytes, void* stream, const float* router_logits,
+                                  float swiglu_limit = 0.f) {
   if (!shape_ok(T, E, D, H, k)) return MOE_ERR_INVALID_ARG;
   if (dtype != MOE_BF16 && dtype != MOE_MXFP8) return MOE_ERR_INVALID_ARG;
   if (pipeline != MOE_FUSED && pipeline != MOE_SPLIT) return MOE_ERR_INVALID_ARG;
@@ -628,6 +634,7 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
   Workspace ws = plan_workspace(workspace, T, E, D, H, k, pipeline, dtype);
   if (workspace_bytes < ws.bytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
   ws.router_logits = router_logits;
+  ws.swiglu_limit = swiglu_limit;
   const int sms = num_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -693,6 +700,7 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
   ga.H = H;
   ga.prefetch = g_prefetch.load();
   ga.stall_test = g_stall_test.load();
+  ga.swiglu_limit = ws.swiglu_limit;
   ga.counts = ws.counts;
   ga.pad_offsets = ws.pad_offsets;
   ga.swap_ab = g_swap_ab.load();
@@ -791,6 +799,59 @@ moe_status_t moe_ffn_profile_read(float* ms, int capacity, int* n_stages) {
     if (cudaEventElapsedTime(&ms[n], g_prof.ev[i], g_prof.ev[i + 1]) != cudaSuccess) return MOE_ERR_CUDA;
   *n_stages = n;
   return MOE_OK;
+}
+
+// Workspace of a call with shared experts: the plan of the extended problem
+// (E + n_shared experts, k + n_shared pairs per token) followed by the
+// extended ids and weights [T, k + n_shared].
+static size_t ex_workspace_bytes(int T, int E, int D, int H, int k, int n_shared, int dtype, int pipeline,
+                                 size_t* ext_offset) {
+  const size_t base = plan_workspace(nullptr, T, E + n_shared, D, H, k + n_shared, pipeline, dtype).bytes;
+  if (ext_offset) *ext_offset = base;
+  if (n_shared == 0) return base;
+  const size_t one = align_up(sizeof(int32_t) * (size_t)T * (k + n_shared), 256);
+  return base + 2 * one;
+}
+
+size_t moe_ffn_workspace_size_ex(int T, int E, int D, int H, int k, int n_shared, int dtype, int pipeline) {
+  if (n_shared < 0 || E + n_shared > kMaxExperts || !shape_ok(T, E + n_shared, D, H, k + n_shared) ||
+      (dtype != MOE_BF16 && dtype != MOE_MXFP8) || (pipeline != MOE_FUSED && pipeline != MOE_SPLIT))
+    return 0;
+  return ex_workspace_bytes(T, E, D, H, k, n_shared, dtype, pipeline, nullptr);
+}
+
+moe_status_t moe_ffn_forward_ex(const void* x, const void* x_sf, const void* w1, const void* w1_sf, const void* w2,
+                                const void* w2_sf, int32_t* topk_ids, float* topk_w, void* out, int T, int E, int D,
+                                int H, int k, int dtype, int pipeline, const moe_ffn_extras_t* extras,
+                                void* workspace, size_t workspace_bytes, void* stream) {
+  const float limit = extras ? extras->swiglu_limit : 0.f;
+  const int ns = extras ? extras->n_shared : 0;
+  const float* logits = extras ? extras->router_logits : nullptr;
+  if (!(limit >= 0.f) || ns < 0 || E + ns > kMaxExperts) return MOE_ERR_INVALID_ARG;
+  if (logits && (k > E || (reinterpret_cast<uintptr_t>(logits) & 3u))) return MOE_ERR_INVALID_ARG;
+  if (ns == 0)
+    return forward_entry(x, x_sf, w1, w1_sf, w2, w2_sf, topk_ids, topk_w, out, T, E, D, H, k, dtype, pipeline,
+                         workspace, workspace_bytes, stream, logits, limit);
+  if (!shape_ok(T, E + ns, D, H, k + ns)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!topk_ids || !topk_w || !workspace) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(topk_ids) & 3u) || (reinterpret_cast<uintptr_t>(topk_w) & 3u))
+    return MOE_ERR_MISALIGNED;
+  size_t ext_off = 0;
+  if (workspace_bytes < ex_workspace_bytes(T, E, D, H, k, ns, dtype, pipeline, &ext_off))
+    return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // routed ids and weights first (the router, when the call starts from
+  // logits), then [T, k + n_shared] with every shared expert at weight 1
+  int32_t* ids_ext = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + ext_off);
+  float* w_ext = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ids_ext) +
+                                          align_up(sizeof(int32_t) * (size_t)T * (k + ns), 256));
+  cudaError_t e = cudaSuccess;
+  if (logits) e = launch_router_topk(logits, T, E, k, topk_ids, topk_w, st);
+  if (e == cudaSuccess) e = launch_extend_routing(topk_ids, topk_w, T, E, k, ns, ids_ext, w_ext, st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return forward_entry(x, x_sf, w1, w1_sf, w2, w2_sf, ids_ext, w_ext, out, T, E + ns, D, H, k + ns, dtype, pipeline,
+                       workspace, ext_off, stream, nullptr, limit);
 }
 
 const char* moe_ffn_profile_stage_kernel(int stage) {

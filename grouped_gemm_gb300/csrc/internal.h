@@ -47,6 +47,7 @@ struct Workspace {
   // the call starts from them (moe_ffn_forward_logits), else nullptr.
   const float* router_logits;
   unsigned long long wait_limit_ns;  // bound of every device wait of the call
+  float swiglu_limit;                // > 0: clamped SwiGLU (moe_ffn_forward_ex), else plain
 };
 
 // MOE_OPT_ROUTE_COOP: 1 (default) routes problems too large for the
@@ -97,6 +98,10 @@ cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const flo
 // softmax of the selected logits, for each of T tokens of logits [T, E].
 cudaError_t launch_router_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
                                cudaStream_t stream);
+// ids_ext / w_ext [T, k + n_shared]: the routed ids and weights of each token,
+// then the shared experts E .. E + n_shared - 1 at weight 1.
+cudaError_t launch_extend_routing(const int32_t* ids, const float* w, int T, int E, int k, int n_shared,
+                                  int32_t* ids_ext, float* w_ext, cudaStream_t stream);
 // xg[padded slot of pair p] = x[p / k] for every routed pair, and (when
 // out != nullptr) out[0 .. out_bytes) = 0, out_bytes a multiple of 16 * T.
 // pdl: launched as a programmatic dependent of the routing launch.

@@ -15,6 +15,7 @@
 //   3. per-block stable scatter using warp match + per-warp prefix counts.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <map>
@@ -930,6 +931,29 @@ cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const flo
   return cudaLaunchKernelEx(&cfg, route_scatter_kernel, static_cast<const int32_t*>(topk_ids), topk_w, P, E, k,
                             static_cast<const int*>(ws.blk_base), static_cast<const int*>(ws.offsets),
                             static_cast<const int*>(ws.pad_offsets), ws.row_tok, ws.slot_w, ws.slot_of_pair);
+}
+
+namespace {
+__global__ void __launch_bounds__(256) extend_routing_kernel(const int32_t* __restrict__ ids,
+                                                             const float* __restrict__ w, int64_t T, int E, int k,
+                                                             int n_shared, int32_t* __restrict__ ids_ext,
+                                                             float* __restrict__ w_ext) {
+  const int kx = k + n_shared;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < T * kx; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / kx;
+    const int j = (int)(i % kx);
+    ids_ext[i] = j < k ? ids[t * k + j] : E + (j - k);
+    w_ext[i] = j < k ? w[t * k + j] : 1.f;
+  }
+}
+}  // namespace
+
+cudaError_t launch_extend_routing(const int32_t* ids, const float* w, int T, int E, int k, int n_shared,
+                                  int32_t* ids_ext, float* w_ext, cudaStream_t stream) {
+  const int64_t n = (int64_t)T * (k + n_shared);
+  const int grid = (int)std::min<int64_t>((n + 255) / 256, 4096);
+  extend_routing_kernel<<<grid > 0 ? grid : 1, 256, 0, stream>>>(ids, w, T, E, k, n_shared, ids_ext, w_ext);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_router_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,

@@ -110,6 +110,42 @@ moe_status_t moe_ffn_forward_logits(const void* x, const void* x_sf, const void*
                                     int32_t* topk_ids, float* topk_w, void* out, int T, int E, int D, int H, int k,
                                     int dtype, int pipeline, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Optional extras of a forward call (moe_ffn_forward_ex); zero-initialize
+ * and set what is needed.
+ *   swiglu_limit   > 0: the clamped SwiGLU of the gpt-oss-style expert
+ *                  ("Porting Block-Scaled GEMM Kernels from Blackwell to
+ *                  Rubin" sec. 5.3): gate = min(gate, limit),
+ *                  up = min(max(up, -limit), limit), then silu(gate) * up.
+ *                  0: the plain SwiGLU.
+ *   n_shared       >= 0 shared experts ("GC-MoE on SM120" sec. 4.7: a shared
+ *                  expert runs on every token): experts E .. E + n_shared - 1
+ *                  of w1 / w2 (and of their MXFP8 scales), stored after the E
+ *                  routed ones, are added for every token with weight 1, in
+ *                  the same launches as the routed experts (each token gets
+ *                  k + n_shared pairs).  Requires E + n_shared <= 1024.
+ *   router_logits  optional [T, E] float32: the call starts from router
+ *                  logits as moe_ffn_forward_logits does; topk_ids / topk_w
+ *                  are then outputs. */
+typedef struct {
+  float swiglu_limit;
+  int n_shared;
+  const float* router_logits;
+} moe_ffn_extras_t;
+
+/* Workspace bytes of moe_ffn_forward_ex with n_shared shared experts (equal
+ * to moe_ffn_workspace_size when n_shared == 0); 0 for an invalid shape. */
+size_t moe_ffn_workspace_size_ex(int T, int E, int D, int H, int k, int n_shared, int dtype, int pipeline);
+
+/* moe_ffn_forward with the extras above (extras may be NULL: then it is
+ * moe_ffn_forward).  topk_ids / topk_w [T, k] hold the routed experts (or
+ * receive them, with router_logits); the workspace must hold
+ * moe_ffn_workspace_size_ex bytes.  Same requirements, layouts and errors as
+ * moe_ffn_forward; MOE_ERR_INVALID_ARG for a negative limit or n_shared. */
+moe_status_t moe_ffn_forward_ex(const void* x, const void* x_sf, const void* w1, const void* w1_sf, const void* w2,
+                                const void* w2_sf, int32_t* topk_ids, float* topk_w, void* out, int T, int E, int D,
+                                int H, int k, int dtype, int pipeline, const moe_ffn_extras_t* extras,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
 /* One-time repacking of MXFP8 weight scales into the 512-byte tile layout the
  * kernels copy into tensor memory ("Prime Flash MoE" sec. 7 "Scales are
  * piped through tensor memory"; 128 rows x 4 K-scales per tile).
@@ -263,8 +299,9 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   most 160 MiB, 2 always, 0 never.  Measured on GB300 at
  *                   mxfp8 (out 134 MB): split 2.12 -> 2.10 ms, fused 2.28 ->
  *                   2.34 ms; large_skewed unchanged.
- *   MOE_OPT_GATHER_BLOCKS  1..16 (default 4): blocks per SM of the row-gather
- *                   kernels (bytes in flight against HBM latency). */
+ *   MOE_OPT_GATHER_BLOCKS  1..16 (default 8): blocks per SM of the row-gather
+ *                   kernels (bytes in flight against HBM latency).  Measured
+ *                   on GB300 at large_skewed: 4 -> 0.94 ms, 8 -> 0.87 ms. */
 typedef enum {
   MOE_OPT_GATHER = 0,
   MOE_OPT_L2_PREFETCH = 1,
