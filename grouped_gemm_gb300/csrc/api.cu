@@ -131,6 +131,7 @@ std::atomic<int> g_route_coop{1};
 Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipeline, int dtype) {
   Workspace w{};
   w.wait_limit_ns = g_wait_limit_ns.load();
+  w.route_stall_test = g_stall_test.load() == 2 ? 1 : 0;
   const int64_t P = (int64_t)T * k;
   const int64_t live_experts = P < E ? P : E;
   w.S_max = (int64_t)align_up((size_t)(P + live_experts * (kRowPad - 1)), kRowPad);
@@ -260,7 +261,7 @@ moe_status_t forward_fused_cluster_bf16(const Workspace& ws, const void* x, cons
   fa.h1 = h1;
   fa.s1 = H / C / h1;
   fa.s2 = D / C / kFusedClusterN;
-  fa.stall_test = g_stall_test.load();
+  fa.stall_test = g_stall_test.load() == 1 ? 1 : 0;
   fa.swiglu_limit = ws.swiglu_limit;
   prof_front(false);
   prof_kernel(2, "fused_cluster_bf16");
@@ -306,7 +307,7 @@ moe_status_t forward_fused_bf16(const Workspace& ws, const void* x, const void* 
   fa.D = D;
   fa.H = H;
   fa.n_slices = H / 128;
-  fa.stall_test = g_stall_test.load();
+  fa.stall_test = g_stall_test.load() == 1 ? 1 : 0;
   fa.swiglu_limit = ws.swiglu_limit;
   const int grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * fa.n_slices);
   prof_front(false);
@@ -352,7 +353,7 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
   ma.wait_limit_ns = g_wait_limit_ns.load();
   ma.D = D;
   ma.H = H;
-  ma.stall_test = g_stall_test.load();
+  ma.stall_test = g_stall_test.load() == 1 ? 1 : 0;
   ma.swiglu_limit = ws.swiglu_limit;
   ma.out_hint = out_hint_for((int64_t)T * D * 2);
   MxArgs up = ma;
@@ -439,7 +440,7 @@ moe_status_t forward_fused_cluster_mxfp8(const Workspace& ws, const void* x, con
   fa.out_hint = out_hint_for((int64_t)T * D * 2);
   fa.s1 = H / C / 128;
   fa.s2 = D / C / 256;
-  fa.stall_test = g_stall_test.load();
+  fa.stall_test = g_stall_test.load() == 1 ? 1 : 0;
   fa.swiglu_limit = ws.swiglu_limit;
   prof_front(true);
   prof_kernel(2, "fused_cluster_mxfp8");
@@ -492,7 +493,7 @@ moe_status_t forward_fused_mxfp8(const Workspace& ws, const void* x, const void*
   fa.wait_limit_ns = g_wait_limit_ns.load();
   fa.D = D;
   fa.H = H;
-  fa.stall_test = g_stall_test.load();
+  fa.stall_test = g_stall_test.load() == 1 ? 1 : 0;
   fa.swiglu_limit = ws.swiglu_limit;
   const int grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * (H / 128));
   prof_front(true);
@@ -534,7 +535,7 @@ moe_status_t moe_ffn_set_option(int option, long long value) {
       g_gather_mode.store((int)value);
       return MOE_OK;
     case MOE_OPT_TEST_STALL:
-      if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
+      if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
       g_stall_test.store((int)value);
       return MOE_OK;
     case MOE_OPT_FUSED_CLUSTER:
@@ -699,7 +700,7 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
   ga.D = D;
   ga.H = H;
   ga.prefetch = g_prefetch.load();
-  ga.stall_test = g_stall_test.load();
+  ga.stall_test = g_stall_test.load() == 1 ? 1 : 0;
   ga.swiglu_limit = ws.swiglu_limit;
   ga.counts = ws.counts;
   ga.pad_offsets = ws.pad_offsets;

@@ -48,6 +48,7 @@ struct Workspace {
   const float* router_logits;
   unsigned long long wait_limit_ns;  // bound of every device wait of the call
   float swiglu_limit;                // > 0: clamped SwiGLU (moe_ffn_forward_ex), else plain
+  int route_stall_test;              // test hook: one routing block never reaches the grid barrier
 };
 
 // MOE_OPT_ROUTE_COOP: 1 (default) routes problems too large for the

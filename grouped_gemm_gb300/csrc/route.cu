@@ -535,6 +535,7 @@ struct CoopRouteArgs {
   float* slot_w;
   int* slot_of_pair;
   int64_t S_max;
+  int stall_test;  // test hook: block 0 leaves before the first barrier
 };
 
 __device__ bool coop_grid_sync(const CoopRouteArgs& a, int site) {
@@ -611,6 +612,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32) route_coop_kernel(const CoopR
     for (int w = 0; w < kCoopWarps; ++w) t += wcnt[w * E + e];
     a.blk[(int64_t)b * E + e] = t;
   }
+  if (a.stall_test && b == 0) return;  // the others' first barrier wait runs out
   if (!coop_grid_sync(a, 80)) return;
 
   // ---- B: exclusive prefix over blocks of each expert's column: one warp per
@@ -892,6 +894,7 @@ cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const flo
     ca.slot_w = ws.slot_w;
     ca.slot_of_pair = ws.slot_of_pair;
     ca.S_max = ws.S_max;
+    ca.stall_test = ws.route_stall_test;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(NB);
     cfg.blockDim = dim3(kCoopWarps * 32);

@@ -219,12 +219,19 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   shared-memory ring the GEMM producers prefetch operand
  *                   tiles into L2 (cp.async.bulk.prefetch.tensor); 0 = off.
  *                   Measured on GB300, prefetching slowed every workload.
- *   MOE_OPT_TEST_STALL  0 (default) or 1: test hook for failure detection.
- *                   With 1, each GEMM kernel's MMA issuer first waits on a
- *                   barrier that nothing ever arrives on; the wait runs out
- *                   after the wait limit, the kernel records
+ *   MOE_OPT_TEST_STALL  0 (default), 1 or 2: test hooks for failure
+ *                   detection.  With 1, each GEMM kernel's MMA issuer first
+ *                   waits on a barrier that nothing ever arrives on; the wait
+ *                   runs out after the wait limit, the kernel records
  *                   MOE_ERR_DEVICE_TIMEOUT and exits cleanly (no fault, no
- *                   hang), so the status path can be tested on a GPU.
+ *                   hang), so the status path can be tested on a GPU.  With 2,
+ *                   one block of the one-launch routing leaves before its
+ *                   first grid barrier; the other blocks' waits run out, the
+ *                   routing records MOE_ERR_DEVICE_TIMEOUT and leaves tables
+ *                   with no row blocks, so the GEMMs that follow do nothing.
+ *                   After a timeout, moe_ffn_sync_status (which clears the
+ *                   status words, including the routing barrier's state) must
+ *                   be called before the workspace is used again.
  *   MOE_OPT_UP_PAIRS  0 (default) or 1: with 1 (and MOE_OPT_GATHER 0) each
  *                   tile of the bf16 up-projection takes two row blocks of
  *                   one expert against one weight tile ("Prime Flash MoE"

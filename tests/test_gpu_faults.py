@@ -60,3 +60,24 @@ def test_bad_expert_id_is_reported():
     tw[7, 1] = 0.0
     ref = oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], ids, tw, act=oracle.ACT_BF16)
     assert_close(out, ref, label="bad id dropped")
+
+
+@pytest.mark.parametrize("pipeline", [moe.MOE_SPLIT, moe.MOE_FUSED])
+def test_routing_barrier_timeout_is_reported_and_context_survives(pipeline):
+    # 4000 tokens x 4 = 16000 pairs: the one-launch cooperative routing, whose
+    # block 0 leaves before the first grid barrier (MOE_OPT_TEST_STALL 2)
+    inp = wl.make_custom(4000, 256, 128, 16, 4, seed=8)
+    dev = to_dev(inp)
+    moe.moe_ffn_set_wait_limit_ns(1_000_000)
+    moe.moe_ffn_set_option(moe.MOE_OPT_TEST_STALL, 2)
+    try:
+        out, ws = run_forward(inp, dev, pipeline=pipeline, check_status=False)
+        st = moe.moe_ffn_sync_status(ws)
+    finally:
+        moe.moe_ffn_set_option(moe.MOE_OPT_TEST_STALL, 0)
+        moe.moe_ffn_set_wait_limit_ns(2_000_000_000)
+    assert st == 6, moe.moe_ffn_status_string(st)
+    assert torch.isfinite(out.float()).all()        # zero-filled, no stale rows
+    assert moe.moe_ffn_sync_status(ws) == 0
+    out, _ = run_forward(inp, dev, pipeline=pipeline, workspace=ws)
+    assert_close(out, oracle_out(inp), label="after routing timeout")
