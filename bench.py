@@ -109,6 +109,8 @@ KERNEL_SOURCES = {
     "fused_moe_bf16": ["grouped_gemm_gb300/csrc/gemm_fused.cu"] + _PTX,
     "fused_cluster_mxfp8": ["grouped_gemm_gb300/csrc/gemm_fused_cluster_mx.cu"] + _MXH + _PTX,
     "fused_moe_mxfp8": ["grouped_gemm_gb300/csrc/gemm_fused_mx.cu"] + _MXH + _PTX,
+    "route": ["grouped_gemm_gb300/csrc/route.cu"] + _PTX,
+    "gather_tokens": ["grouped_gemm_gb300/csrc/route.cu"] + _PTX,
 }
 
 
