@@ -28,6 +28,7 @@ std::atomic<int> g_pair_mma{2};       // MOE_OPT_PAIR_MMA: 0 off, 1 on, 2 automa
 std::atomic<int> g_swap_ab{0};        // MOE_OPT_SWAP_AB: swap-AB tail tiles (measured slower on GB300: off)
 std::atomic<int> g_out_hint{0};       // MOE_OPT_OUT_L2_HINT: 0 off (measured no gain), 1 automatic, 2 always
 std::atomic<int> g_gather_blocks{8};  // MOE_OPT_GATHER_BLOCKS: gather blocks per SM
+std::atomic<int> g_l2_policy{0};      // MOE_OPT_L2_POLICY: bit 0 weights evict_first, bit 1 xg evict_last
 std::atomic<int> g_pair_swap{0};      // MOE_OPT_PAIR_SWAP: max routed rows of a swap-AB pair tile (measured slower: off)
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -127,11 +128,13 @@ void prof_front(bool mx) {
 }  // namespace
 
 std::atomic<int> g_route_coop{1};
+std::atomic<int> g_router_fused{0};
 
 Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipeline, int dtype) {
   Workspace w{};
   w.wait_limit_ns = g_wait_limit_ns.load();
   w.route_stall_test = g_stall_test.load() == 2 ? 1 : 0;
+  w.l2_policy = g_l2_policy.load();
   const int64_t P = (int64_t)T * k;
   const int64_t live_experts = P < E ? P : E;
   w.S_max = (int64_t)align_up((size_t)(P + live_experts * (kRowPad - 1)), kRowPad);
@@ -562,6 +565,14 @@ moe_status_t moe_ffn_set_option(int option, long long value) {
       if (value < 1 || value > 16) return MOE_ERR_INVALID_ARG;
       g_gather_blocks.store((int)value);
       return MOE_OK;
+    case MOE_OPT_L2_POLICY:
+      if (value < 0 || value > 3) return MOE_ERR_INVALID_ARG;
+      g_l2_policy.store((int)value);
+      return MOE_OK;
+    case MOE_OPT_ROUTER_FUSED:
+      if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
+      g_router_fused.store((int)value);
+      return MOE_OK;
     case MOE_OPT_PAIR_SWAP:
       if (value < 0 || value > 256) return MOE_ERR_INVALID_ARG;
       g_pair_swap.store((int)value);
@@ -707,6 +718,7 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
   ga.swap_ab = g_swap_ab.load();
   ga.pair_swap_max = g_pair_swap.load();
   ga.out_hint = out_hint_for((int64_t)T * D * 2);
+  ga.l2_policy = ws.l2_policy;
 
   const int dyn_opt = g_dynamic_tiles.load();
   const bool small_problem = (int64_t)ws.max_rb * (H / kUpFold) < 8LL * sms;

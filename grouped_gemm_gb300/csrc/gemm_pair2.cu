@@ -167,7 +167,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
         if (leader) mbar_arrive_expect_tx(&full[s], 2 * kQStage);
         const uint32_t fb = mapa_shared(smem_addr(&full[s]), 0);
         tma_load_2d_pair(sA + s * kQA, &map_a, fb, kb * kBK, arow);
-        tma_load_2d_pair(sB + s * kQB, &map_b, fb, kb * kBK, brow);
+        if (args.l2_policy & 1)  // weight tiles are read by one pair: evict them first
+          tma_load_2d_pair_hint(sB + s * kQB, &map_b, fb, kb * kBK, brow, l2_policy_evict_first());
+        else
+          tma_load_2d_pair(sB + s * kQB, &map_b, fb, kb * kBK, brow);
         issued_phase[s] = (int)ph;
         if (++s == kQStages) {
           s = 0;

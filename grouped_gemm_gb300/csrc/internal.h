@@ -49,11 +49,15 @@ struct Workspace {
   unsigned long long wait_limit_ns;  // bound of every device wait of the call
   float swiglu_limit;                // > 0: clamped SwiGLU (moe_ffn_forward_ex), else plain
   int route_stall_test;              // test hook: one routing block never reaches the grid barrier
+  int l2_policy;                     // MOE_OPT_L2_POLICY bits (see api.cu)
 };
 
 // MOE_OPT_ROUTE_COOP: 1 (default) routes problems too large for the
 // single-block kernel in one cooperative launch; 0 uses three launches.
 extern std::atomic<int> g_route_coop;
+// MOE_OPT_ROUTER_FUSED: 1 runs the router inside single-block routing
+// launches; 0 (default) always launches it separately.
+extern std::atomic<int> g_router_fused;
 
 // pipeline = kRouteOnly plans only the routing regions (the common prefix of
 // every layout).
@@ -85,6 +89,7 @@ struct GemmArgs {
                             //   run as swap-AB tiles (0 = never)
   int out_hint;             // 1: reductions into out carry an L2 evict_last hint
   float swiglu_limit;       // > 0: gate clamped to <= limit, up to [-limit, limit] before SwiGLU
+  int l2_policy;            // bit 0: weight tiles loaded with an L2 evict_first policy
 };
 
 // Routing; when zero_out != nullptr the first launch also zero-fills

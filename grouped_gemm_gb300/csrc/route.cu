@@ -144,14 +144,9 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
   router_tokens_any(logits, E, k, t0, min(T, t0 + per_block), ids, w, nullptr);
 }
 
-// Per-block histograms of the routed pairs.  With logits != nullptr the block
-// first runs the router over its tokens, writing ids_out / w_out, and counts
-// the selected experts as it goes (ids is then unused).
 __global__ void __launch_bounds__(256) route_count_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int k,
                                                           int NB, int* __restrict__ blk_counts, int* __restrict__ err,
-                                                          uint4* __restrict__ zero_out, int64_t zero_vecs,
-                                                          const float* __restrict__ logits, int32_t* ids_out,
-                                                          float* w_out) {
+                                                          uint4* __restrict__ zero_out, int64_t zero_vecs) {
   extern __shared__ int hist[];
   if (zero_out) {  // every block of the (possibly wider) grid helps zero-fill the reduction target
     const uint4 z = make_uint4(0, 0, 0, 0);
@@ -162,20 +157,15 @@ __global__ void __launch_bounds__(256) route_count_kernel(const int32_t* __restr
   if ((int)blockIdx.x >= NB) return;
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
-  if (logits) {
-    const int T = (int)(P / k), t0 = (int)blockIdx.x * kRouteTokPerBlock;
-    router_tokens_any(logits, E, k, t0, min(T, t0 + kRouteTokPerBlock), ids_out, w_out, hist);
-  } else {
-    const int64_t p0 = (int64_t)blockIdx.x * kRouteTokPerBlock * k;
-    const int64_t p1 = min(P, p0 + (int64_t)kRouteTokPerBlock * k);
-    bool bad = false;
-    for (int64_t p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
-      const int e = ids[p];
-      if ((unsigned)e < (unsigned)E) atomicAdd(&hist[e], 1);
-      else bad = true;
-    }
-    if (bad) atomicOr(err, kErrBadRouting);
+  const int64_t p0 = (int64_t)blockIdx.x * kRouteTokPerBlock * k;
+  const int64_t p1 = min(P, p0 + (int64_t)kRouteTokPerBlock * k);
+  bool bad = false;
+  for (int64_t p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
+    const int e = ids[p];
+    if ((unsigned)e < (unsigned)E) atomicAdd(&hist[e], 1);
+    else bad = true;
   }
+  if (bad) atomicOr(err, kErrBadRouting);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) blk_counts[(int64_t)blockIdx.x * E + e] = hist[e];
 }
@@ -498,8 +488,8 @@ __global__ void __launch_bounds__(1024)
 // blocks (all co-resident), for problems too large for the single-block
 // kernel: the three phases of the three-kernel path separated by two grid
 // barriers instead of two kernel boundaries.
-//   A. per-warp histograms of contiguous pair ranges (the router first, when
-//      logits are given); block totals to blk[b][e].  Block 0 sets meta to
+//   A. per-warp histograms of contiguous pair ranges; block totals to
+//      blk[b][e].  Block 0 sets meta to
 //      "no row blocks" and every block marks its pairs' slots and its share
 //      of the padded slots -1, so that if a barrier ever runs out the GEMMs
 //      that follow find nothing to do rather than stale tables.
@@ -517,9 +507,6 @@ constexpr int kCoopWarps = 8;
 struct CoopRouteArgs {
   const int32_t* ids;
   const float* topk_w;
-  const float* logits;   // router mode when set: ids / topk_w are written first
-  int32_t* ids_out;
-  float* w_out;
   int64_t P;
   int E, k, NB;
   int* err;
@@ -565,7 +552,6 @@ __device__ bool coop_grid_sync(const CoopRouteArgs& a, int site) {
   return __syncthreads_and(ok) != 0;
 }
 
-template <bool kRouter>
 __global__ void __launch_bounds__(kCoopWarps * 32) route_coop_kernel(const CoopRouteArgs a) {
   extern __shared__ int sm[];
   int* wcnt = sm;                       // [kCoopWarps][E] per-warp counts, then bases
@@ -592,16 +578,10 @@ __global__ void __launch_bounds__(kCoopWarps * 32) route_coop_kernel(const CoopR
   for (int64_t r = (int64_t)b * blockDim.x + threadIdx.x; r < a.S_max; r += (int64_t)a.NB * blockDim.x)
     a.row_tok[r] = -1;
   for (int i = threadIdx.x; i < kCoopWarps * E; i += blockDim.x) wcnt[i] = 0;
-  if constexpr (kRouter) {
-    const int t0 = b * kRouteTokPerBlock;
-    router_tokens_any(a.logits, E, k, t0, t0 + (int)((p1 - p0) / k), a.ids_out, a.w_out, nullptr);
-    ids = a.ids_out;
-    tw = a.w_out;
-  }
   __syncthreads();
   bool bad = false;
   for (int64_t p = q0 + lane; p < q1; p += 32) {
-    const int e = load_i32<kRouter>(ids + p);
+    const int e = ids[p];
     if ((unsigned)e < (unsigned)E) atomicAdd(&wcnt[warp * E + e], 1);
     else bad = true;
   }
@@ -615,58 +595,89 @@ __global__ void __launch_bounds__(kCoopWarps * 32) route_coop_kernel(const CoopR
   if (a.stall_test && b == 0) return;  // the others' first barrier wait runs out
   if (!coop_grid_sync(a, 80)) return;
 
-  // ---- B: exclusive prefix over blocks of each expert's column: one warp per
-  // expert (warps of all blocks share the experts) when the column is short,
-  // else one block per expert, 256 blocks per step
-  if (a.NB <= 64) {
-    for (int e = b * kCoopWarps + warp; e < E; e += a.NB * kCoopWarps) {
-      int carry = 0;
-      for (int c0 = 0; c0 < a.NB; c0 += 32) {
-        const int bb = c0 + lane;
-        const int v = bb < a.NB ? a.blk[(int64_t)bb * E + e] : 0;
-        int x = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, x, o);
-          if (lane >= o) x += y;
+  // With few blocks (NB <= 64) every block reads the whole [NB, E] table of
+  // block counts after the first barrier and derives the totals and its own
+  // prefix itself (one barrier); otherwise phase B scans the columns first.
+  const bool one_barrier = a.NB <= 64;
+  if (!one_barrier) {
+    // ---- B: exclusive prefix over blocks of each expert's column: one warp per
+    // expert (warps of all blocks share the experts) when the column is short,
+    // else one block per expert, 256 blocks per step
+    if (a.NB <= 64) {
+      for (int e = b * kCoopWarps + warp; e < E; e += a.NB * kCoopWarps) {
+        int carry = 0;
+        for (int c0 = 0; c0 < a.NB; c0 += 32) {
+          const int bb = c0 + lane;
+          const int v = bb < a.NB ? a.blk[(int64_t)bb * E + e] : 0;
+          int x = v;
+  #pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+          }
+          if (bb < a.NB) a.blk[(int64_t)bb * E + e] = carry + x - v;
+          carry += __shfl_sync(0xffffffffu, x, 31);
         }
-        if (bb < a.NB) a.blk[(int64_t)bb * E + e] = carry + x - v;
-        carry += __shfl_sync(0xffffffffu, x, 31);
+        if (lane == 0) a.counts[e] = carry;
       }
-      if (lane == 0) a.counts[e] = carry;
-    }
-  } else {
-    for (int e = b; e < E; e += a.NB) {
-      int carry = 0;
-      for (int c0 = 0; c0 < a.NB; c0 += blockDim.x) {
-        const int bb = c0 + threadIdx.x;
-        const int v = bb < a.NB ? a.blk[(int64_t)bb * E + e] : 0;
-        int x = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, x, o);
-          if (lane >= o) x += y;
+    } else {
+      for (int e = b; e < E; e += a.NB) {
+        int carry = 0;
+        for (int c0 = 0; c0 < a.NB; c0 += blockDim.x) {
+          const int bb = c0 + threadIdx.x;
+          const int v = bb < a.NB ? a.blk[(int64_t)bb * E + e] : 0;
+          int x = v;
+  #pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+          }
+          if (lane == 31) warp_sums[warp] = x;
+          __syncthreads();
+          int wbase = 0, tot = 0;
+          for (int w = 0; w < kCoopWarps; ++w) {
+            const int sw = warp_sums[w];
+            if (w < warp) wbase += sw;
+            tot += sw;
+          }
+          if (bb < a.NB) a.blk[(int64_t)bb * E + e] = carry + wbase + x - v;
+          carry += tot;
+          __syncthreads();
         }
-        if (lane == 31) warp_sums[warp] = x;
-        __syncthreads();
-        int wbase = 0, tot = 0;
-        for (int w = 0; w < kCoopWarps; ++w) {
-          const int sw = warp_sums[w];
-          if (w < warp) wbase += sw;
-          tot += sw;
-        }
-        if (bb < a.NB) a.blk[(int64_t)bb * E + e] = carry + wbase + x - v;
-        carry += tot;
-        __syncthreads();
+        if (threadIdx.x == 0) a.counts[e] = carry;
       }
-      if (threadIdx.x == 0) a.counts[e] = carry;
     }
+    if (!coop_grid_sync(a, 81)) return;
   }
-  if (!coop_grid_sync(a, 81)) return;
 
   // ---- C: scans over experts (every block), tables (block 0), scatter (all)
   int warp_tot[3];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = a.counts[e];
+  if (one_barrier) {
+    // totals and this block's prefix over blocks, straight from blk; the
+    // prefix waits in s_qoff until the per-warp bases are formed below
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int tot = 0, mine = 0;
+      for (int bb = 0; bb < a.NB; ++bb) {
+        const int c = a.blk[(int64_t)bb * E + e];
+        mine += bb < b ? c : 0;
+        tot += c;
+      }
+      s_cnt[e] = tot;
+      s_qoff[e] = mine;
+      if (b == 0) a.counts[e] = tot;
+    }
+  } else {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_cnt[e] = a.counts[e];
+  }
+  __syncthreads();
+  // one_barrier: this block's prefix of expert e, held by the thread that
+  // forms e's per-warp bases below (s_qoff is reused for the pair offsets)
+  int my_prefix[(kMaxExperts + kCoopWarps * 32 - 1) / (kCoopWarps * 32)];
+#pragma unroll
+  for (int q = 0; q < (kMaxExperts + kCoopWarps * 32 - 1) / (kCoopWarps * 32); ++q) {
+    const int e = threadIdx.x + q * kCoopWarps * 32;
+    my_prefix[q] = (one_barrier && e < E) ? s_qoff[e] : 0;
+  }
   __syncthreads();
   // serial-in-thread chunks: thread i owns experts [i*per, (i+1)*per)
   const int per = (E + blockDim.x - 1) / blockDim.x;
@@ -736,9 +747,12 @@ __global__ void __launch_bounds__(kCoopWarps * 32) route_coop_kernel(const CoopR
       a.meta[0] = warp_tot[1] / kRowPad;
     }
   }
-  // this block's per-warp bases: blk[b][e] (prefix over blocks) + earlier warps
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int acc = a.blk[(int64_t)b * E + e];
+  // this block's per-warp bases: its prefix over blocks + earlier warps
+#pragma unroll
+  for (int q = 0; q < (kMaxExperts + kCoopWarps * 32 - 1) / (kCoopWarps * 32); ++q) {
+    const int e = threadIdx.x + q * kCoopWarps * 32;
+    if (e >= E) break;
+    int acc = one_barrier ? my_prefix[q] : a.blk[(int64_t)b * E + e];
     for (int w = 0; w < kCoopWarps; ++w) {
       const int c = wcnt[w * E + e];
       wcnt[w * E + e] = acc;
@@ -746,8 +760,7 @@ __global__ void __launch_bounds__(kCoopWarps * 32) route_coop_kernel(const CoopR
     }
   }
   __syncthreads();
-  scatter_range<kRouter>(ids, tw, q0, q1, E, k, wcnt + warp * E, s_off, s_poff, a.row_tok, a.slot_w,
-                         a.slot_of_pair);
+  scatter_range(ids, tw, q0, q1, E, k, wcnt + warp * E, s_off, s_poff, a.row_tok, a.slot_w, a.slot_of_pair);
 }
 
 // Token-major gather: xg[padded slot of pair p, :] = x[t, :] for the k pairs
@@ -766,7 +779,10 @@ __global__ void __launch_bounds__(256)
     gather_tokens_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ ids,
                          const int* __restrict__ slot_of_pair, const int* __restrict__ offsets,
                          const int* __restrict__ pad_offsets, int T, int E, int k, int vec_per_row,
-                         uint4* __restrict__ xg, uint4* __restrict__ out, int out_vecs_per_row) {
+                         uint4* __restrict__ xg, uint4* __restrict__ out, int out_vecs_per_row, int keep_xg) {
+  // keep_xg: the gathered rows are stored with an L2 evict_last policy, so
+  // that more of them are still in L2 when the up projection reads them
+  const uint64_t pol = l2_policy_evict_last();
   griddep_wait();
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -795,9 +811,15 @@ __global__ void __launch_bounds__(256)
         const int slot = __shfl_sync(0xffffffffu, ps, jj);
         if (slot < 0) continue;
         uint4* dst = xg + (int64_t)slot * vec_per_row + v0;
+        if (keep_xg) {
 #pragma unroll
-        for (int i = 0; i < kGatherChunkVecs / 32; ++i)
-          if (v0 + i * 32 + lane < vec_per_row) dst[i * 32 + lane] = v[i];
+          for (int i = 0; i < kGatherChunkVecs / 32; ++i)
+            if (v0 + i * 32 + lane < vec_per_row) st_global_v4_hint(dst + i * 32 + lane, v[i], pol);
+        } else {
+#pragma unroll
+          for (int i = 0; i < kGatherChunkVecs / 32; ++i)
+            if (v0 + i * 32 + lane < vec_per_row) dst[i * 32 + lane] = v[i];
+        }
       }
     }
     if (out) {
@@ -830,14 +852,12 @@ bool route_coop_fits(int NB, int E) {
     int per_sm = 0, sms = 0, coop = 0;
     const size_t smem = route_coop_smem(E);
     if (smem > 48 * 1024 &&
-        cudaFuncSetAttribute(route_coop_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+        cudaFuncSetAttribute(route_coop_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess) {
       cudaGetLastError();
       return false;
     }
-    if (smem > 48 * 1024)
-      cudaFuncSetAttribute(route_coop_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_coop_kernel<true>, kCoopWarps * 32, smem) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, route_coop_kernel, kCoopWarps * 32, smem) !=
             cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess) {
@@ -858,7 +878,15 @@ cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const flo
   // with the router, topk_ids / topk_w are the caller's output arrays
   int32_t* ids_out = logits ? const_cast<int32_t*>(topk_ids) : nullptr;
   float* w_out = logits ? const_cast<float*>(topk_w) : nullptr;
-  if (!zero_out && P <= kRouteSmallMaxPairs && E <= kRouteSmallMaxExperts) {
+  const bool small = !zero_out && P <= kRouteSmallMaxPairs && E <= kRouteSmallMaxExperts;
+  if (logits && (!small || !g_router_fused.load())) {
+    // the router as its own wide launch (one warp per token): inside a
+    // routing launch of a few blocks it would run on a small share of the GPU
+    cudaError_t e = launch_router_topk(logits, T, E, k, ids_out, w_out, stream);
+    if (e != cudaSuccess) return e;
+    logits = nullptr;
+  }
+  if (small) {
     if (logits)
       route_small_kernel<true><<<1, 1024, 0, stream>>>(
           topk_ids, topk_w, (int)P, E, k, ws.err, ws.counts, ws.offsets, ws.pad_offsets, ws.meta, ws.expert_of_rb,
@@ -874,9 +902,6 @@ cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const flo
     CoopRouteArgs ca{};
     ca.ids = topk_ids;
     ca.topk_w = topk_w;
-    ca.logits = logits;
-    ca.ids_out = ids_out;
-    ca.w_out = w_out;
     ca.P = P;
     ca.E = E;
     ca.k = k;
@@ -905,13 +930,11 @@ cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const flo
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return logits ? cudaLaunchKernelEx(&cfg, route_coop_kernel<true>, ca)
-                  : cudaLaunchKernelEx(&cfg, route_coop_kernel<false>, ca);
+    return cudaLaunchKernelEx(&cfg, route_coop_kernel, ca);
   }
   const int grid = zero_out ? (NB > zero_grid ? NB : zero_grid) : NB;
   route_count_kernel<<<grid, 256, E * sizeof(int), stream>>>(topk_ids, P, E, k, NB, ws.blk_base, ws.err,
-                                                             static_cast<uint4*>(zero_out), zero_bytes / 16, logits,
-                                                             ids_out, w_out);
+                                                             static_cast<uint4*>(zero_out), zero_bytes / 16);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // the scan and the scatter start as programmatic dependents (their launch
@@ -982,7 +1005,8 @@ cudaError_t launch_gather_zero(const Workspace& ws, const void* x, const int32_t
   return cudaLaunchKernelEx(&cfg, gather_tokens_kernel, static_cast<const uint4*>(x), topk_ids,
                             static_cast<const int*>(ws.slot_of_pair), static_cast<const int*>(ws.offsets),
                             static_cast<const int*>(ws.pad_offsets), T, E, k, D / 8, static_cast<uint4*>(ws.xg),
-                            static_cast<uint4*>(out), out ? (int)(out_bytes / 16 / T) : 0);
+                            static_cast<uint4*>(out), out ? (int)(out_bytes / 16 / T) : 0,
+                            (ws.l2_policy & 2) ? 1 : 0);
 }
 
 }  // namespace moe

@@ -98,11 +98,12 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
 moe_status_t moe_ffn_router_topk(const float* logits, int T, int E, int k, int32_t* topk_ids, float* topk_w,
                                  void* stream);
 
-/* moe_ffn_forward starting from router logits: the routing launch runs the
- * router of moe_ffn_router_topk over each token first (fused with the
- * per-expert histogram, no extra launch), writes topk_ids / topk_w (caller
- * arrays [T, k], outputs here), then the forward pass proceeds exactly as
- * moe_ffn_forward with those ids and weights.  Same workspace, requirements
+/* moe_ffn_forward starting from router logits: the router of
+ * moe_ffn_router_topk runs over each token first (a launch of one warp per
+ * token, right before the routing launch; see MOE_OPT_ROUTER_FUSED) and
+ * writes topk_ids / topk_w (caller arrays [T, k], outputs here); then the
+ * forward pass proceeds exactly as moe_ffn_forward with those ids and
+ * weights.  Same workspace, requirements
  * and errors as moe_ffn_forward, plus k <= E and router_logits [T, E] float32
  * (4-byte aligned). */
 moe_status_t moe_ffn_forward_logits(const void* x, const void* x_sf, const void* w1, const void* w1_sf,
@@ -308,7 +309,21 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   2.34 ms; large_skewed unchanged.
  *   MOE_OPT_GATHER_BLOCKS  1..16 (default 8): blocks per SM of the row-gather
  *                   kernels (bytes in flight against HBM latency).  Measured
- *                   on GB300 at large_skewed: 4 -> 0.94 ms, 8 -> 0.87 ms. */
+ *                   on GB300 at large_skewed: 4 -> 0.94 ms, 8 -> 0.87 ms.
+ *   MOE_OPT_L2_POLICY  0 (default) .. 3, bits: 1 = the CTA-pair GEMMs load
+ *                   weight tiles (read by one pair each) with an L2
+ *                   evict_first policy; 2 = the row gather stores the
+ *                   gathered rows (read right after by the up projection)
+ *                   with evict_last.
+ *   MOE_OPT_ROUTER_FUSED  0 (default) or 1: with router logits, 1 runs the
+ *                   router inside the routing launch when that launch is a
+ *                   single block (small problems), else as its own launch of
+ *                   one warp per token; 0 always launches it separately.
+ *                   Measured on GB300 at decode from logits: 0.422 ms fused,
+ *                   0.413 ms separate (one block has too few warps for the
+ *                   tokens' logits).
+ *   (MOE_OPT_L2_POLICY measured at prefill: 0.343 ms with 0, 0.349 with 1,
+ *                   0.342 with 2, 0.348 with 3: no gain, off.) */
 typedef enum {
   MOE_OPT_GATHER = 0,
   MOE_OPT_L2_PREFETCH = 1,
@@ -322,7 +337,9 @@ typedef enum {
   MOE_OPT_PAIR_SWAP = 9,
   MOE_OPT_ROUTE_COOP = 10,
   MOE_OPT_OUT_L2_HINT = 11,
-  MOE_OPT_GATHER_BLOCKS = 12
+  MOE_OPT_GATHER_BLOCKS = 12,
+  MOE_OPT_L2_POLICY = 13,
+  MOE_OPT_ROUTER_FUSED = 14
 } moe_option_t;
 moe_status_t moe_ffn_set_option(int option, long long value);
 

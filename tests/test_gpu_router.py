@@ -71,6 +71,7 @@ def test_router_rejects_bad_k():
 PIPES = {"split": moe.MOE_SPLIT, "fused": moe.MOE_FUSED}
 
 
+@pytest.mark.parametrize("fused_router", [0, 1])  # router launch of its own / inside single-block routing
 @pytest.mark.parametrize("pipe", list(PIPES))
 @pytest.mark.parametrize("T,D,H,E,k", [
     (64, 256, 128, 8, 2),       # the tiny workload's shape: single-block routing
@@ -78,7 +79,15 @@ PIPES = {"split": moe.MOE_SPLIT, "fused": moe.MOE_FUSED}
     (2048, 2048, 768, 128, 8),  # prefill dims: multi-block routing, every expert live
     (150, 256, 128, 300, 2),    # E > 256: multi-block routing, most experts empty
 ])
-def test_forward_from_logits(T, D, H, E, k, pipe):
+def test_forward_from_logits(T, D, H, E, k, pipe, fused_router):
+    moe.moe_ffn_set_option(moe.MOE_OPT_ROUTER_FUSED, fused_router)
+    try:
+        _forward_from_logits(T, D, H, E, k, pipe)
+    finally:
+        moe.moe_ffn_set_option(moe.MOE_OPT_ROUTER_FUSED, 0)
+
+
+def _forward_from_logits(T, D, H, E, k, pipe):
     inp = wl.make_custom(T, D, H, E, k, seed=T + E, routing="uniform")
     lg = wl.router_logits(T, E, seed=T * 3 + k)
     rids, rw = oracle.router_topk(lg, k)
