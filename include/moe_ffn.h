@@ -23,7 +23,9 @@
  * pipeline and MXFP8 also need D % 256 == 0 (else MOE_ERR_UNSUPPORTED).
  *
  * Ownership: the caller owns every buffer, including the workspace; the
- * library allocates no device memory.  Calls are asynchronous on `stream` (a
+ * library allocates no device memory.  A workspace serves one call at a time:
+ * calls that may run concurrently on the device (different streams) need
+ * workspaces of their own.  Calls are asynchronous on `stream` (a
  * cudaStream_t passed as void*, NULL = legacy default stream) and may be
  * captured in CUDA graphs.  Host-detectable errors are returned immediately;
  * errors found on the device (an expert id out of range, a bounded wait that
