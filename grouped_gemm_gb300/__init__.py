@@ -238,6 +238,7 @@ MOE_OPT_OUT_L2_HINT = 11
 MOE_OPT_GATHER_BLOCKS = 12
 MOE_OPT_L2_POLICY = 13
 MOE_OPT_ROUTER_FUSED = 14
+MOE_OPT_PREFETCH_MB = 15
 
 
 def moe_ffn_set_option(option: int, value: int) -> int:

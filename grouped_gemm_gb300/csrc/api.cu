@@ -29,6 +29,7 @@ std::atomic<int> g_swap_ab{0};        // MOE_OPT_SWAP_AB: swap-AB tail tiles (me
 std::atomic<int> g_out_hint{0};       // MOE_OPT_OUT_L2_HINT: 0 off (measured no gain), 1 automatic, 2 always
 std::atomic<int> g_gather_blocks{8};  // MOE_OPT_GATHER_BLOCKS: gather blocks per SM
 std::atomic<int> g_l2_policy{0};      // MOE_OPT_L2_POLICY: bit 0 weights evict_first, bit 1 xg evict_last
+std::atomic<int> g_prefetch_mb{0};    // MOE_OPT_PREFETCH_MB: weights prefetched into L2 during routing
 std::atomic<int> g_pair_swap{0};      // MOE_OPT_PAIR_SWAP: max routed rows of a swap-AB pair tile (measured slower: off)
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -573,6 +574,10 @@ moe_status_t moe_ffn_set_option(int option, long long value) {
       if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
       g_router_fused.store((int)value);
       return MOE_OK;
+    case MOE_OPT_PREFETCH_MB:
+      if (value < 0 || value > 1024) return MOE_ERR_INVALID_ARG;
+      g_prefetch_mb.store((int)value);
+      return MOE_OK;
     case MOE_OPT_PAIR_SWAP:
       if (value < 0 || value > 256) return MOE_ERR_INVALID_ARG;
       g_pair_swap.store((int)value);
@@ -647,6 +652,10 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
   if (workspace_bytes < ws.bytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
   ws.router_logits = router_logits;
   ws.swiglu_limit = swiglu_limit;
+  // the up projection's weights, from the first expert on (its first tiles)
+  ws.prefetch_base = w1;
+  ws.prefetch_bytes = std::min<int64_t>((int64_t)g_prefetch_mb.load() << 20,
+                                        (int64_t)E * 2 * H * D * (dtype == MOE_MXFP8 ? 1 : 2)) & ~(int64_t)15;
   const int sms = num_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -50,6 +50,8 @@ struct Workspace {
   float swiglu_limit;                // > 0: clamped SwiGLU (moe_ffn_forward_ex), else plain
   int route_stall_test;              // test hook: one routing block never reaches the grid barrier
   int l2_policy;                     // MOE_OPT_L2_POLICY bits (see api.cu)
+  const void* prefetch_base;         // the gather prefetches [base, base + bytes) into L2
+  int64_t prefetch_bytes;            //   while the routing finishes (0 = off)
 };
 
 // MOE_OPT_ROUTE_COOP: 1 (default) routes problems too large for the

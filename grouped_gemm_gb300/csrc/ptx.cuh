@@ -179,6 +179,12 @@ __device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, 
                : "memory");
 }
 
+// Prefetch `bytes` (a multiple of 16, 16-byte aligned address) of global
+// memory into L2 (no completion tracking).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* gptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gptr), "r"(bytes) : "memory");
+}
+
 // Four rows of a rank-2 tensor map (box one row high) into four consecutive
 // box-sized rows of shared memory ("Prime Flash MoE" sec. 3: the token tile is
 // a gather, row r of the tile comes from an arbitrary row of x).

@@ -407,6 +407,9 @@ __global__ void __launch_bounds__(1024)
   __shared__ int s_off[kRouteSmallMaxExperts], s_poff[kRouteSmallMaxExperts], s_cnt[kRouteSmallMaxExperts];
   __shared__ int s_qoff[kRouteSmallMaxExperts];
   __shared__ int warp_sums[32];
+  // the gather that follows may start now: it waits for this grid before
+  // reading the routing tables, and meanwhile prefetches weights into L2
+  if (threadIdx.x == 0) griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int sub = (P + kRouteSmallWarps - 1) / kRouteSmallWarps;
   const int q0 = min(P, warp * sub), q1 = min(P, q0 + sub);
@@ -553,6 +556,7 @@ __device__ bool coop_grid_sync(const CoopRouteArgs& a, int site) {
 }
 
 __global__ void __launch_bounds__(kCoopWarps * 32) route_coop_kernel(const CoopRouteArgs a) {
+  if (threadIdx.x == 0) griddep_launch_dependents();  // see route_small_kernel
   extern __shared__ int sm[];
   int* wcnt = sm;                       // [kCoopWarps][E] per-warp counts, then bases
   int* s_off = wcnt + kCoopWarps * a.E;  // [E]
@@ -779,10 +783,20 @@ __global__ void __launch_bounds__(256)
     gather_tokens_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ ids,
                          const int* __restrict__ slot_of_pair, const int* __restrict__ offsets,
                          const int* __restrict__ pad_offsets, int T, int E, int k, int vec_per_row,
-                         uint4* __restrict__ xg, uint4* __restrict__ out, int out_vecs_per_row, int keep_xg) {
+                         uint4* __restrict__ xg, uint4* __restrict__ out, int out_vecs_per_row, int keep_xg,
+                         const uint8_t* __restrict__ pf_base, int64_t pf_bytes) {
   // keep_xg: the gathered rows are stored with an L2 evict_last policy, so
   // that more of them are still in L2 when the up projection reads them
   const uint64_t pol = l2_policy_evict_last();
+  // While the routing finishes (latency-bound, HBM idle), each block asks L2
+  // for its share of the first pf_bytes of the up projection's weights: the
+  // first tiles of the up kernel then find them in L2.
+  if (pf_bytes > 0 && threadIdx.x == 0) {
+    const int64_t chunk = ((pf_bytes + gridDim.x - 1) / gridDim.x + 15) & ~(int64_t)15;
+    const int64_t b0 = (int64_t)blockIdx.x * chunk;
+    const int64_t n = min(chunk, pf_bytes - b0);
+    if (n > 0) bulk_prefetch_l2(pf_base + b0, (uint32_t)n);
+  }
   griddep_wait();
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1006,7 +1020,8 @@ cudaError_t launch_gather_zero(const Workspace& ws, const void* x, const int32_t
                             static_cast<const int*>(ws.slot_of_pair), static_cast<const int*>(ws.offsets),
                             static_cast<const int*>(ws.pad_offsets), T, E, k, D / 8, static_cast<uint4*>(ws.xg),
                             static_cast<uint4*>(out), out ? (int)(out_bytes / 16 / T) : 0,
-                            (ws.l2_policy & 2) ? 1 : 0);
+                            (ws.l2_policy & 2) ? 1 : 0, static_cast<const uint8_t*>(ws.prefetch_base),
+                            ws.prefetch_bytes);
 }
 
 }  // namespace moe

@@ -324,6 +324,12 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   Measured on GB300 at decode from logits: 0.422 ms fused,
  *                   0.413 ms separate (one block has too few warps for the
  *                   tokens' logits).
+ *   MOE_OPT_PREFETCH_MB  0 (default) .. 1024: while the routing launch runs
+ *                   (its latency leaves HBM idle), the bf16 row-gather's
+ *                   blocks ask L2 for the first this-many MiB of w1, the
+ *                   weights of the up projection's first tiles.  Measured on
+ *                   GB300: decode 0.410 ms with 0, 0.408 with 32, 0.409 with
+ *                   64; prefill 0.345 with 0, 0.348 with 96 (no gain, off).
  *   (MOE_OPT_L2_POLICY measured at prefill: 0.343 ms with 0, 0.349 with 1,
  *                   0.342 with 2, 0.348 with 3: no gain, off.) */
 typedef enum {
@@ -341,7 +347,8 @@ typedef enum {
   MOE_OPT_OUT_L2_HINT = 11,
   MOE_OPT_GATHER_BLOCKS = 12,
   MOE_OPT_L2_POLICY = 13,
-  MOE_OPT_ROUTER_FUSED = 14
+  MOE_OPT_ROUTER_FUSED = 14,
+  MOE_OPT_PREFETCH_MB = 15
 } moe_option_t;
 moe_status_t moe_ffn_set_option(int option, long long value);
 
