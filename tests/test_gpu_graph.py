@@ -49,3 +49,52 @@ def test_graph_replay_matches_oracle(pipeline, T):
     torch.cuda.synchronize()
     ref2 = oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], inp2["topk_ids"], inp2["topk_w"], act=oracle.ACT_BF16)
     assert_close(out, ref2, label="graph replay, new routing")
+
+
+@pytest.mark.parametrize("name,pipeline,n_sample", [
+    ("decode", moe.MOE_SPLIT, None), ("decode", moe.MOE_FUSED, None),
+    ("prefill", moe.MOE_SPLIT, 64), ("prefill", moe.MOE_FUSED, 64),
+    ("mxfp8", moe.MOE_SPLIT, 24), ("mxfp8", moe.MOE_FUSED, 24),
+])
+def test_graph_replay_full_workload_sampled(name, pipeline, n_sample):
+    """The benchmark's configuration: the full-size workload, one step
+    captured in a CUDA graph and replayed; outputs checked on a seeded sample
+    of tokens (each token's output depends only on its own row)."""
+    inp = wl.make_inputs(name, seed=0)
+    w = inp["workload"]
+    mx = w.dtype == "mxfp8"
+    dev = to_dev(inp)
+    dtype = moe.MOE_MXFP8 if mx else moe.MOE_BF16
+    if mx:
+        w1p = torch.empty(inp["w1_sf"].size, dtype=torch.uint8, device="cuda")
+        w2p = torch.empty(inp["w2_sf"].size, dtype=torch.uint8, device="cuda")
+        moe.moe_ffn_prepare_mxfp8_weights(dev["w1_sf"], dev["w2_sf"], w1p, w2p, w.E, w.D, w.H)
+    out = torch.empty(w.T, w.D, dtype=torch.bfloat16, device="cuda")
+    ws = moe.alloc_workspace(w.T, w.E, w.D, w.H, w.k, dtype, pipeline)
+
+    def step():
+        moe.moe_ffn_forward(dev["x"], dev["w1"], dev["w2"], dev["topk_ids"], dev["topk_w"], out, E=w.E, D=w.D,
+                            H=w.H, k=w.k, workspace=ws, dtype=dtype, pipeline=pipeline, x_sf=dev.get("x_sf"),
+                            w1_sf=w1p if mx else None, w2_sf=w2p if mx else None)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    out.fill_(float("nan"))
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert moe.moe_ffn_sync_status(ws) == 0
+    tokens = None if n_sample is None else np.sort(np.random.default_rng(5).choice(w.T, n_sample, replace=False))
+    ref = oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], inp["topk_ids"], inp["topk_w"],
+                         act=oracle.ACT_MXFP8 if mx else oracle.ACT_BF16, x_sf=inp.get("x_sf"),
+                         w1_sf=inp.get("w1_sf"), w2_sf=inp.get("w2_sf"),
+                         tokens=None if tokens is None else tokens.astype(np.int32))
+    got = out if tokens is None else out[torch.from_numpy(tokens).cuda()]
+    assert_close(got, ref, dtype="mxfp8" if mx else "bf16", label=f"graph {name} pipeline={pipeline}")
+    assert torch.isfinite(out.float()).all()
