@@ -496,9 +496,10 @@ __global__ void __launch_bounds__(1024)
 //      "no row blocks" and every block marks its pairs' slots and its share
 //      of the padded slots -1, so that if a barrier ever runs out the GEMMs
 //      that follow find nothing to do rather than stale tables.
-//   B. each expert's column is scanned (by one warp when NB <= 64, else by
-//      one block): blk[.][e] becomes the exclusive prefix over blocks,
-//      counts[e] the total.
+//   B. (more than 64 blocks only) one block per expert scans its column:
+//      blk[.][e] becomes the exclusive prefix over blocks, counts[e] the
+//      total.  With at most 64 blocks phase C reads the whole table instead,
+//      and the second barrier is skipped.
 //   C. every block scans counts over experts (offsets, padded offsets);
 //      block 0 writes the expert tables (offsets, pad_offsets, expert_of_rb,
 //      pair_info, padding rows, meta); every block scatters its own pairs with
@@ -604,52 +605,32 @@ __global__ void __launch_bounds__(kCoopWarps * 32) route_coop_kernel(const CoopR
   // prefix itself (one barrier); otherwise phase B scans the columns first.
   const bool one_barrier = a.NB <= 64;
   if (!one_barrier) {
-    // ---- B: exclusive prefix over blocks of each expert's column: one warp per
-    // expert (warps of all blocks share the experts) when the column is short,
-    // else one block per expert, 256 blocks per step
-    if (a.NB <= 64) {
-      for (int e = b * kCoopWarps + warp; e < E; e += a.NB * kCoopWarps) {
-        int carry = 0;
-        for (int c0 = 0; c0 < a.NB; c0 += 32) {
-          const int bb = c0 + lane;
-          const int v = bb < a.NB ? a.blk[(int64_t)bb * E + e] : 0;
-          int x = v;
-  #pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
-          }
-          if (bb < a.NB) a.blk[(int64_t)bb * E + e] = carry + x - v;
-          carry += __shfl_sync(0xffffffffu, x, 31);
+    // ---- B: exclusive prefix over blocks of each expert's column, one block
+    // per expert, 256 blocks per step
+    for (int e = b; e < E; e += a.NB) {
+      int carry = 0;
+      for (int c0 = 0; c0 < a.NB; c0 += blockDim.x) {
+        const int bb = c0 + threadIdx.x;
+        const int v = bb < a.NB ? a.blk[(int64_t)bb * E + e] : 0;
+        int x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
         }
-        if (lane == 0) a.counts[e] = carry;
-      }
-    } else {
-      for (int e = b; e < E; e += a.NB) {
-        int carry = 0;
-        for (int c0 = 0; c0 < a.NB; c0 += blockDim.x) {
-          const int bb = c0 + threadIdx.x;
-          const int v = bb < a.NB ? a.blk[(int64_t)bb * E + e] : 0;
-          int x = v;
-  #pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
-          }
-          if (lane == 31) warp_sums[warp] = x;
-          __syncthreads();
-          int wbase = 0, tot = 0;
-          for (int w = 0; w < kCoopWarps; ++w) {
-            const int sw = warp_sums[w];
-            if (w < warp) wbase += sw;
-            tot += sw;
-          }
-          if (bb < a.NB) a.blk[(int64_t)bb * E + e] = carry + wbase + x - v;
-          carry += tot;
-          __syncthreads();
+        if (lane == 31) warp_sums[warp] = x;
+        __syncthreads();
+        int wbase = 0, tot = 0;
+        for (int w = 0; w < kCoopWarps; ++w) {
+          const int sw = warp_sums[w];
+          if (w < warp) wbase += sw;
+          tot += sw;
         }
-        if (threadIdx.x == 0) a.counts[e] = carry;
+        if (bb < a.NB) a.blk[(int64_t)bb * E + e] = carry + wbase + x - v;
+        carry += tot;
+        __syncthreads();
       }
+      if (threadIdx.x == 0) a.counts[e] = carry;
     }
     if (!coop_grid_sync(a, 81)) return;
   }
