@@ -31,10 +31,10 @@ constexpr int kScatterWarps = 8;
 
 // ---------------------------------------------------------------- router
 // Top-k of one token's router logits by one warp, and the softmax of the
-// selected logits (the step that produces the path's inputs: "Prime Flash
-// MoE" sec. 1, a router selects the top-k experts of each token together with
-// normalized routing weights; the workloads take the top k of per-(token,
-// expert) logits and renormalize a softmax over the selected k).
+// selected logits.  This is the step upstream of the path: "Prime Flash MoE"
+// sec. 1 takes each token's k experts and their weights (which sum to one) as
+// given, and the workloads produce them from per-(token, expert) logits, the
+// k largest with a softmax over just those k.
 //   order: decreasing logit, ties to the lower expert id, NaN read as -inf;
 //   w[j] = exp(l_j - l_0) / sum_i exp(l_i - l_0) in fp32 (l_0 the largest);
 //   every weight is 1/k when l_0 is -inf.

@@ -85,10 +85,10 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
                              int D, int H, int k, int dtype, int pipeline, void* workspace, size_t workspace_bytes,
                              void* stream);
 
-/* The router step that produces the path's inputs ("Prime Flash MoE" sec. 1:
- * a router selects the top-k experts of each token together with normalized
- * routing weights; the workloads' routers take the top k of per-(token,
- * expert) logits and renormalize a softmax over the selected k).
+/* The router step upstream of the path ("Prime Flash MoE" sec. 1 takes each
+ * token's k experts and their weights, which sum to one, as given; the
+ * workloads produce them from per-(token, expert) logits: the k largest, with
+ * a softmax over just those k).
  *   logits    [T, E] float32 (4-byte aligned; a NaN logit is read as -inf)
  *   topk_ids  [T, k] int32 output: the k experts with the largest logits, in
  *             order of decreasing logit, ties going to the lower expert id
@@ -120,8 +120,8 @@ moe_status_t moe_ffn_forward_logits(const void* x, const void* x_sf, const void*
  *                  Rubin" sec. 5.3): gate = min(gate, limit),
  *                  up = min(max(up, -limit), limit), then silu(gate) * up.
  *                  0: the plain SwiGLU.
- *   n_shared       >= 0 shared experts ("GC-MoE on SM120" sec. 4.7: a shared
- *                  expert runs on every token): experts E .. E + n_shared - 1
+ *   n_shared       >= 0 shared experts ("GC-MoE on SM120" sec. 4.7: every
+ *                  token uses a shared expert): experts E .. E + n_shared - 1
  *                  of w1 / w2 (and of their MXFP8 scales), stored after the E
  *                  routed ones, are added for every token with weight 1, in
  *                  the same launches as the routed experts (each token gets

@@ -184,11 +184,10 @@ int oracle_route(int T, int E, int k, const int32_t* ids, int pad,
 /* ------------------------------------------------------------------------ */
 
 /*
- * Top-k selection with normalized weights, the step that produces the path's
- * inputs ("Prime Flash MoE" sec. 1: "a router has already selected the top-k
- * experts for each token, together with normalized routing weights"; the
- * workloads' routers take the top k of per-(token, expert) logits and a
- * softmax renormalized over the selected k).
+ * Top-k selection with normalized weights, the step upstream of the path
+ * ("Prime Flash MoE" sec. 1 starts from each token's k experts and weights
+ * summing to one, produced beforehand; the workloads produce them from
+ * per-(token, expert) logits: the k largest, with a softmax over those k).
  *
  * For each token t, with l[e] = logits[t][e] (a NaN logit is read as -inf):
  *   ids[t][0..k-1]: the k experts with the largest l[e], in order of
@@ -261,9 +260,10 @@ static double silu(double g) { return g / (1.0 + exp(-g)); }
  *     g[h] = sum_d W1[e][h][d]   x[t][d]        h < H   (gate rows 0..H-1)
  *     u[h] = sum_d W1[e][H+h][d] x[t][d]                (up rows H..2H-1)
  *     (clamped variant, swiglu_limit L > 0: g[h] = min(g[h], L),
- *      u[h] = min(max(u[h], -L), L) first -- the gate from above only, the up
- *      projection on both sides, as "Porting Block-Scaled GEMM Kernels from
- *      Blackwell to Rubin" sec. 5.3 describes the gpt-oss-style activation)
+ *      u[h] = min(max(u[h], -L), L) first -- an upper bound on the gate, a
+ *      bound on both sides of the up projection: the gpt-oss-style
+ *      activation of "Porting Block-Scaled GEMM Kernels from Blackwell to
+ *      Rubin" sec. 5.3)
  *     a[h] = silu(g[h]) * u[h]
  *     a    = act_round(a)                               (see below)
  *     y[d] = sum_h W2[e][d][h] a[h]

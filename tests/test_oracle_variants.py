@@ -1,8 +1,8 @@
 """Pins for the oracle's activation and shared-expert variants (CPU only).
 
 Clamped SwiGLU ("Porting Block-Scaled GEMM Kernels from Blackwell to Rubin"
-sec. 5.3: gate clamped from above only, up symmetrically, then
-silu(gate) * up): the one-expert, weight-1 case is the dense clamped FFN
+sec. 5.3: an upper bound on the gate, a two-sided bound on the up projection,
+then silu(gate) * up): the one-expert, weight-1 case is the dense clamped FFN
 written with torch's clamp and silu in fp64; a limit above every |gate| and
 |up| leaves the plain SwiGLU; the clamp bounds |act| by 0.2785 * limit for a
 small limit.  Shared experts (GC-MoE on SM120 sec. 4.7: a shared expert runs
