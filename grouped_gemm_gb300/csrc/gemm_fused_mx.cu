@@ -1,6 +1,7 @@
 // gemm_fused_mx.cu -- the fused pipeline in MXFP8 ("Prime Flash MoE" sec. 7:
-// the pipeline, the split-K and the shared ring carry over from bf16; the
-// epilogue also quantizes; the MXFP8 down loop is strictly serialized).
+// the pipeline, the split-K and the shared ring carry over from bf16, the
+// epilogue requantizes act, and the down loop runs its jobs one after another
+// on a single accumulator).
 //
 // Per tile (128-row block rb, 128-wide slice j of H):
 //   GEMM1  acc[128 x 256] = (xg * s_x) . ([W1 gate j | up j] * s_w1)^T over K=D,
