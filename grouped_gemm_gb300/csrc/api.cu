@@ -907,9 +907,11 @@ moe_status_t moe_ffn_sync_status(void* workspace, void* stream) {
   if (!workspace) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int words[2] = {0, 0};
+  // read and clear on the call's own stream (no legacy-default-stream sync)
   if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cudaMemcpy(words, workspace, sizeof words, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cudaMemset(workspace, 0, 64) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpyAsync(words, workspace, sizeof words, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemsetAsync(workspace, 0, 64, st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+    return MOE_ERR_CUDA;
   if (words[0] & kErrLaunch) return MOE_ERR_CUDA;
   if (words[0] & kErrTimeout) return MOE_ERR_DEVICE_TIMEOUT;
   if (words[0] & kErrBadRouting) return MOE_ERR_BAD_ROUTING;

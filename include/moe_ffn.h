@@ -353,7 +353,7 @@ typedef enum {
 moe_status_t moe_ffn_set_option(int option, long long value);
 
 /* Per-stage timing of later moe_ffn_forward calls (a benchmarking aid, off by
- * default).  While enabled, each call records CUDA events on its stream
+ * default; process-wide state, for single-threaded use).  While enabled, each call records CUDA events on its stream
  * between its stages; the split pipeline's stages are
  *   0 routing (three kernels), 1 gather + zero-fill of out,
  *   2 up-projection + SwiGLU, 3 down-projection + weighted reduction.
