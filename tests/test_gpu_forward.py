@@ -68,6 +68,8 @@ def oracle_out(inp, tokens=None):
     (512, 2048, 768, 128, 8, "topk_logits"),  # prefill dims, 512 tokens
     (96, 384, 128, 6, 3, "uniform"),          # D % 256 != 0 (split only: 128-column down tiles)
     (200, 256, 128, 1024, 4, "uniform"),      # the largest expert count
+    (130, 256, 128, 1, 1, "uniform"),         # one expert, top-1: a dense SwiGLU FFN scaled by w
+    (100, 256, 128, 64, 32, "uniform"),       # k = 32 distinct experts per token
 ])
 def test_forward_small(T, D, H, E, k, routing, pipeline):
     if D % 256 and MODES[pipeline][0] != moe.MOE_SPLIT:
