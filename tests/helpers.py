@@ -53,9 +53,9 @@ def compare(gpu, ref, dtype="bf16"):
     return max_rel, mean_rel, cos
 
 
-def assert_close(gpu, ref, dtype="bf16", label=""):
+def assert_close(gpu, ref, dtype="bf16", label="", tol=None):
     max_rel, mean_rel, cos = compare(gpu, ref, dtype)
-    tmax, tmean = TOL[dtype]
+    tmax, tmean = TOL[dtype] if tol is None else tol
     msg = f"{label}: max_rel={max_rel:.3e} (<= {tmax}) mean_rel={mean_rel:.3e} (<= {tmean}) cos={cos:.6f}"
     assert max_rel <= tmax and mean_rel <= tmean, msg
     return max_rel, mean_rel, cos
