@@ -14,6 +14,12 @@
 #include "ptx.cuh"
 
 namespace moe {
+// The routing kernels the last launch_route call of this host thread launched
+// ('+' between them; route.cu).
+const char* last_route_kernels();
+}  // namespace moe
+
+namespace moe {
 namespace {
 
 std::atomic<unsigned long long> g_wait_limit_ns{2000ull * 1000 * 1000};
@@ -122,7 +128,7 @@ void prof_kernel(int stage, const char* name) {
 
 // The routing and gather stages, common to every pipeline.
 void prof_front(bool mx) {
-  prof_kernel(0, "route");
+  prof_kernel(0, last_route_kernels());  // called after the routing launch
   prof_kernel(1, mx ? "gather_rows_mx" : "gather_tokens");
 }
 
@@ -741,6 +747,7 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
   const int pair_slots = pair_mma ? pair_cluster_slots() : 0;
   if (pair_mma && pair_slots <= 0) return MOE_ERR_CUDA;
   prof_front(false);
+  if (in_gemm_gather) prof_kernel(1, "none");  // rows gathered by the up kernel
   prof_kernel(2, pair_mma ? "up_swiglu_pair2" : (gather == 0 && g_up_pairs.load()) ? "up_pair_bf16" : "up_swiglu_bf16");
   prof_kernel(3, pair_down ? "down_reduce_pair2" : "down_reduce_bf16");
   if (pair_mma)

@@ -830,6 +830,8 @@ __global__ void __launch_bounds__(256)
 
 namespace {
 
+thread_local const char* t_route_kernels = "none";
+
 size_t route_coop_smem(int E) { return sizeof(int) * (size_t)(kCoopWarps + 4) * E; }
 
 // Whether NB routing blocks can all be resident at once (checked once per
@@ -866,6 +868,8 @@ bool route_coop_fits(int NB, int E) {
 
 }  // namespace
 
+const char* last_route_kernels() { return t_route_kernels; }
+
 cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const float* topk_w, int T, int E, int k,
                          cudaStream_t stream, void* zero_out, int64_t zero_bytes, int zero_grid, bool pdl) {
   const int64_t P = (int64_t)T * k;
@@ -881,7 +885,9 @@ cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const flo
     if (e != cudaSuccess) return e;
     logits = nullptr;
   }
+  const bool router_first = ws.router_logits && !logits;
   if (small) {
+    t_route_kernels = router_first ? "router_topk+route_small" : "route_small";
     if (logits)
       route_small_kernel<true><<<1, 1024, 0, stream>>>(
           topk_ids, topk_w, (int)P, E, k, ws.err, ws.counts, ws.offsets, ws.pad_offsets, ws.meta, ws.expert_of_rb,
@@ -894,6 +900,7 @@ cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const flo
   }
   const int NB = ws.route_blocks;
   if (!zero_out && route_coop_fits(NB, E)) {
+    t_route_kernels = router_first ? "router_topk+route_coop" : "route_coop";
     CoopRouteArgs ca{};
     ca.ids = topk_ids;
     ca.topk_w = topk_w;
@@ -928,6 +935,8 @@ cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const flo
     return cudaLaunchKernelEx(&cfg, route_coop_kernel, ca);
   }
   const int grid = zero_out ? (NB > zero_grid ? NB : zero_grid) : NB;
+  t_route_kernels = router_first ? "router_topk+route_count+route_scan+route_scatter"
+                                 : "route_count+route_scan+route_scatter";
   route_count_kernel<<<grid, 256, E * sizeof(int), stream>>>(topk_ids, P, E, k, NB, ws.blk_base, ws.err,
                                                              static_cast<uint4*>(zero_out), zero_bytes / 16);
   cudaError_t e = cudaGetLastError();
