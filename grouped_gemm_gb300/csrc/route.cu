@@ -39,11 +39,10 @@ constexpr int kScatterWarps = 8;
 //   w[j] = exp(l_j - l_0) / sum_i exp(l_i - l_0) in fp32 (l_0 the largest);
 //   every weight is 1/k when l_0 is -inf.
 // Lane l holds experts l, l + 32, ... (EPL of them); the expert selected
-// j-th is kept by lane j % 32 in slot j / 32.  `count(e)` is called once per
-// selected expert by the lane that keeps it.
-template <int EPL, typename Count>
+// j-th is kept by lane j % 32 in slot j / 32.
+template <int EPL>
 __device__ __forceinline__ void router_warp_topk(const float* __restrict__ lrow, int E, int k, int32_t* ids,
-                                                 float* w, Count count) {
+                                                 float* w) {
   const int lane = threadIdx.x & 31;
   float v[EPL];
   uint32_t avail = 0;  // bit i: expert lane + 32 i exists and is not taken yet
@@ -103,7 +102,6 @@ __device__ __forceinline__ void router_warp_topk(const float* __restrict__ lrow,
     if (j < k) {
       ids[j] = seli[q];
       w[j] = (flat ? 1.f : expf(selv[q] - m)) / s;
-      count(seli[q]);
     }
   }
 }
@@ -114,25 +112,24 @@ __host__ __device__ constexpr int router_epl(int E) {
 }
 
 // Tokens [t0, t1) by the block's warps: top-k ids and weights written to
-// ids/w [T, k], each selected expert counted in the shared histogram.
+// ids / w [T, k].
 template <int EPL>
 __device__ void router_tokens(const float* __restrict__ logits, int E, int k, int t0, int t1, int32_t* ids,
-                              float* w, int* hist) {
+                              float* w) {
   const int warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   for (int t = t0 + warp; t < t1; t += nw)
-    router_warp_topk<EPL>(logits + (int64_t)t * E, E, k, ids + (int64_t)t * k, w + (int64_t)t * k,
-                          [&](int e) { if (hist) atomicAdd(&hist[e], 1); });
+    router_warp_topk<EPL>(logits + (int64_t)t * E, E, k, ids + (int64_t)t * k, w + (int64_t)t * k);
 }
 
 __device__ void router_tokens_any(const float* __restrict__ logits, int E, int k, int t0, int t1, int32_t* ids,
-                                  float* w, int* hist) {
+                                  float* w) {
   switch (router_epl(E)) {
-    case 1: router_tokens<1>(logits, E, k, t0, t1, ids, w, hist); break;
-    case 2: router_tokens<2>(logits, E, k, t0, t1, ids, w, hist); break;
-    case 4: router_tokens<4>(logits, E, k, t0, t1, ids, w, hist); break;
-    case 8: router_tokens<8>(logits, E, k, t0, t1, ids, w, hist); break;
-    case 16: router_tokens<16>(logits, E, k, t0, t1, ids, w, hist); break;
-    default: router_tokens<32>(logits, E, k, t0, t1, ids, w, hist); break;
+    case 1: router_tokens<1>(logits, E, k, t0, t1, ids, w); break;
+    case 2: router_tokens<2>(logits, E, k, t0, t1, ids, w); break;
+    case 4: router_tokens<4>(logits, E, k, t0, t1, ids, w); break;
+    case 8: router_tokens<8>(logits, E, k, t0, t1, ids, w); break;
+    case 16: router_tokens<16>(logits, E, k, t0, t1, ids, w); break;
+    default: router_tokens<32>(logits, E, k, t0, t1, ids, w); break;
   }
 }
 
@@ -141,7 +138,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
                                                           int32_t* __restrict__ ids, float* __restrict__ w) {
   const int per_block = blockDim.x >> 5;
   const int t0 = blockIdx.x * per_block;
-  router_tokens_any(logits, E, k, t0, min(T, t0 + per_block), ids, w, nullptr);
+  router_tokens_any(logits, E, k, t0, min(T, t0 + per_block), ids, w);
 }
 
 __global__ void __launch_bounds__(256) route_count_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int k,
@@ -415,7 +412,7 @@ __global__ void __launch_bounds__(1024)
   const int q0 = min(P, warp * sub), q1 = min(P, q0 + sub);
   for (int i = threadIdx.x; i < kRouteSmallWarps * E; i += blockDim.x) wcnt[i] = 0;
   if constexpr (kRouter) {
-    router_tokens_any(logits, E, k, 0, P / k, ids_out, w_out, nullptr);
+    router_tokens_any(logits, E, k, 0, P / k, ids_out, w_out);
     ids = ids_out;
     topk_w = w_out;
   }

@@ -93,3 +93,23 @@ def test_noalloc_route_size_limits_on_host():
     assert L.moe_ffn_route_noalloc(A, A, 131072, 1024, 1, A, A, A, None, None) == 7
     assert L.moe_ffn_route_noalloc(A, A, 16384, 1024, 8, A, A, A, None, None) == 7
     assert L.moe_ffn_route_noalloc(A, A, 16385, 1024, 8, A, A, A, None, None) == 5
+
+
+def test_extras_and_router_reject_bad_arguments_on_host():
+    L = moe.lib()
+    A = 1 << 20  # a fake, 16-byte aligned address: never dereferenced
+    ws = 10 ** 9
+    base = [A, None, A, None, A, None, A, A, A, 64, 8, 256, 128, 2, 0, 1]
+    for limit, ns in ((-1.0, 0), (float("nan"), 0), (0.0, -1), (0.0, 1017)):
+        ex = moe.MoeFFNExtras(limit, ns, None)
+        assert L.moe_ffn_forward_ex(*base, ctypes.byref(ex), A, ws, None) == 1
+    ex = moe.MoeFFNExtras(0.0, 0, A)                        # router logits with k > E
+    b2 = list(base); b2[13] = 9
+    assert L.moe_ffn_forward_ex(*b2, ctypes.byref(ex), A, ws, None) == 1
+    assert L.moe_ffn_router_topk(A, 16, 8, 9, A, A, None) == 1     # k > E
+    assert L.moe_ffn_router_topk(A, 16, 8, 0, A, A, None) == 1     # k < 1
+    assert L.moe_ffn_router_topk(A + 2, 16, 8, 2, A, A, None) == 3  # misaligned logits
+    assert L.moe_ffn_router_topk(A, 0, 8, 2, A, A, None) == 0      # T == 0: no-op
+    assert moe.moe_ffn_workspace_size_ex(64, 8, 256, 128, 2, 0) == moe.moe_ffn_workspace_size(64, 8, 256, 128, 2)
+    assert moe.moe_ffn_workspace_size_ex(64, 8, 256, 128, 2, 2) > moe.moe_ffn_workspace_size(64, 10, 256, 128, 4)
+    assert moe.moe_ffn_workspace_size_ex(64, 1020, 256, 128, 2, 5) == 0  # E + n_shared > 1024
