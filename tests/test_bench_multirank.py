@@ -55,3 +55,32 @@ def test_reference_arm_only_on_rank0():
     class A:
         workload, steps, warmup, gpus, pipeline = "tiny", 1, 0, 2, "split"
     assert bench.run_reference(A(), rank=1) is None
+
+
+def test_reference_arm_line_contract():
+    # the CPU oracle as the reference arm: one JSON line with the same metric,
+    # its own cpu_baseline and an e2e with no host-device traffic
+    class A:
+        workload, steps, warmup, gpus, pipeline = "tiny", 1, 0, 1, "split"
+    line = bench.run_reference(A(), rank=0)
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["value"] > 0 and line["unit"] == "TFLOP/s" and line["higher_is_better"] is True
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    e2e = line["e2e"]
+    assert e2e["value"] == line["value"] and e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+    assert line["config"]["workload"] == "tiny"
+
+
+def test_algorithmic_counts():
+    import numpy as np
+    from grouped_gemm_gb300 import workloads as wl
+    w = wl.WORKLOADS["tiny"]
+    ids = np.array([[0, 1]] * w.T, np.int32)          # two live experts
+    alg = bench.algorithmic(w, ids)
+    P = w.T * w.k
+    assert alg["step_flops"] == 6.0 * P * w.D * w.H
+    assert alg["up_swiglu"]["flops"] + alg["down_reduce"]["flops"] == alg["step_flops"]
+    # compulsory bytes: x, the live experts' weights, ids and weights, out
+    assert alg["step_bytes"] == w.T * w.D * 2 + 2 * 3 * w.H * w.D * 2 + P * 8 + w.T * w.D * 2
+    assert alg["live_experts"] == 2
