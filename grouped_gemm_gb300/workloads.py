@@ -34,7 +34,7 @@ class Workload:
     E: int
     k: int
     routing: str          # "topk_logits" | "uniform" | "zipf"
-    dtype: str = "bf16"   # "bf16" | "mxfp8"
+    dtype: str = "bf16"   # "bf16" | "mxfp8" | "mxfp4w" (MXFP8 activations, MXFP4 weights)
 
     @property
     def pairs(self) -> int:
@@ -137,6 +137,40 @@ def mx_encode_rows(a: np.ndarray):
     return q.reshape(shp), sf.reshape(shp[:-1] + (shp[-1] // 32,))
 
 
+_E2M1_GRID = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def mx4_encode_rows(a: np.ndarray):
+    """Encode float32 rows (last dim a multiple of 32) as MXFP4: E2M1 codes
+    packed two to a byte (element 2j in the low four bits of byte j) + e8m0
+    scales, one per 32 elements.
+
+    Input preparation only: each block's scale 2^e is the smallest power of two
+    with max|a|/2^e <= 6; each scaled value goes to the nearest grid point of
+    |E2M1| (ties to the even code), with its sign.
+    """
+    a = np.ascontiguousarray(a, np.float32)
+    shp = a.shape
+    blk = a.reshape(-1, 32).astype(np.float64)
+    amax = np.abs(blk).max(axis=1)
+    f, ex = np.frexp(amax)
+    e = (ex - 1) - 2 + ((2.0 * f) > 1.5)
+    e = np.where(amax == 0, 0, e).astype(np.int64)
+    scaled = blk * np.ldexp(1.0, -e)[:, None]
+    mag = np.minimum(np.abs(scaled), 6.0)
+    dist = np.abs(mag[..., None] - _E2M1_GRID)                   # distance to each grid point
+    best = dist.min(axis=-1, keepdims=True)
+    tied = np.isclose(dist, best, rtol=0, atol=0)
+    # among the nearest points prefer the even code (codes 0, 2, 4, 6 = grid points 0, 1, 2, 4)
+    even = (np.arange(8) % 2 == 0)
+    code = np.where((tied & even).any(axis=-1), np.argmax(tied & even, axis=-1), np.argmax(tied, axis=-1))
+    code = code.astype(np.uint8) | np.where(scaled < 0, 8, 0).astype(np.uint8)
+    code = code.reshape(shp)
+    packed = (code[..., 0::2] | (code[..., 1::2] << 4)).astype(np.uint8)
+    sf = (e + 127).astype(np.uint8).reshape(shp[:-1] + (shp[-1] // 32,))
+    return packed, sf
+
+
 def make_inputs(w: Workload | str, seed: int = 0, T: int | None = None):
     """Draw one workload's inputs.  Order of draws: x, W1, W2, routing.
 
@@ -158,6 +192,17 @@ def make_inputs(w: Workload | str, seed: int = 0, T: int | None = None):
         for e in range(w.E):
             w2[e] = _bf16_bits(_normal(rng, (w.D, w.H), 0.02))
         out["w1"], out["w2"] = w1, w2
+    elif w.dtype == "mxfp4w":  # MXFP8 activations, MXFP4 weights
+        out["x"], out["x_sf"] = mx_encode_rows(_normal(rng, (w.T, w.D), 1.0))
+        w1 = np.empty((w.E, 2 * w.H, w.D // 2), np.uint8)
+        w1_sf = np.empty((w.E, 2 * w.H, w.D // 32), np.uint8)
+        for e in range(w.E):
+            w1[e], w1_sf[e] = mx4_encode_rows(_normal(rng, (2 * w.H, w.D), 0.02))
+        w2 = np.empty((w.E, w.D, w.H // 2), np.uint8)
+        w2_sf = np.empty((w.E, w.D, w.H // 32), np.uint8)
+        for e in range(w.E):
+            w2[e], w2_sf[e] = mx4_encode_rows(_normal(rng, (w.D, w.H), 0.02))
+        out.update(w1=w1, w1_sf=w1_sf, w2=w2, w2_sf=w2_sf)
     else:
         out["x"], out["x_sf"] = mx_encode_rows(_normal(rng, (w.T, w.D), 1.0))
         w1 = np.empty((w.E, 2 * w.H, w.D), np.uint8)

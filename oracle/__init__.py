@@ -25,7 +25,7 @@ _LIB = os.path.join(_HERE, "_build", "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-IN_BF16, IN_MXFP8 = 0, 1
+IN_BF16, IN_MXFP8, IN_MXFP4W = 0, 1, 2
 ACT_EXACT, ACT_BF16, ACT_MXFP8 = 0, 1, 2
 
 
@@ -59,6 +59,12 @@ def _load():
             lib.oracle_e8m0_to_f64.restype = c.c_double
             lib.oracle_mx_scale_exponent.argtypes = [c.c_double]
             lib.oracle_mx_scale_exponent.restype = c.c_int
+            lib.oracle_e2m1_to_f64.argtypes = [c.c_uint8]
+            lib.oracle_e2m1_to_f64.restype = c.c_double
+            lib.oracle_f64_to_e2m1.argtypes = [c.c_double]
+            lib.oracle_f64_to_e2m1.restype = c.c_uint8
+            lib.oracle_mx4_scale_exponent.argtypes = [c.c_double]
+            lib.oracle_mx4_scale_exponent.restype = c.c_int
             lib.oracle_mx_quantize.argtypes = [c.c_void_p, c.c_int, c.c_void_p, c.c_void_p, c.c_void_p]
             lib.oracle_mx_quantize.restype = None
             lib.oracle_route.argtypes = [c.c_int, c.c_int, c.c_int, c.c_void_p, c.c_int,
@@ -102,6 +108,22 @@ def f64_to_e4m3(vals) -> np.ndarray:
     lib = _load()
     v = np.asarray(vals, np.float64)
     return np.array([lib.oracle_f64_to_e4m3(float(x)) for x in v.ravel()], np.uint8).reshape(v.shape)
+
+
+def e2m1_to_f64(codes) -> np.ndarray:
+    lib = _load()
+    c = np.asarray(codes, np.uint8)
+    return np.array([lib.oracle_e2m1_to_f64(int(q)) for q in c.ravel()]).reshape(c.shape)
+
+
+def f64_to_e2m1(vals) -> np.ndarray:
+    lib = _load()
+    v = np.asarray(vals, np.float64)
+    return np.array([lib.oracle_f64_to_e2m1(float(x)) for x in v.ravel()], np.uint8).reshape(v.shape)
+
+
+def mx4_scale_exponent(amax: float) -> int:
+    return _load().oracle_mx4_scale_exponent(float(amax))
 
 
 def mx_scale_exponent(amax: float) -> int:
@@ -152,13 +174,16 @@ def router_topk(logits: np.ndarray, k: int):
 
 # ---------------------------------------------------------------- forward
 def moe_ffn(x, w1, w2, topk_ids, topk_w, *, act=ACT_BF16, x_sf=None, w1_sf=None, w2_sf=None,
-            tokens=None, threads: int = 0, swiglu_limit: float = 0.0) -> np.ndarray:
+            tokens=None, threads: int = 0, swiglu_limit: float = 0.0, fp4_weights: bool = False) -> np.ndarray:
     """fp64 forward pass.
 
     bf16 inputs are uint16 bit patterns; MXFP8 inputs are uint8 e4m3 codes with
     uint8 e8m0 scale arrays (one per 32 along the last dimension).  Returns
     float64 out[n_tokens, D] for ``tokens`` (or all T tokens).  ``swiglu_limit``
     > 0 selects the clamped SwiGLU (gate <= limit, |up| <= limit).
+    ``fp4_weights``: W1 [E, 2H, D/2] and W2 [E, D, H/2] hold MXFP4 weights
+    (E2M1 codes packed two to a byte, low four bits first, one e8m0 scale per
+    32 elements), x stays MXFP8.
     """
     mx = x_sf is not None
     x = np.ascontiguousarray(x)
@@ -170,7 +195,10 @@ def moe_ffn(x, w1, w2, topk_ids, topk_w, *, act=ACT_BF16, x_sf=None, w1_sf=None,
     E, H2, D1 = w1.shape
     H = H2 // 2
     k = ids.shape[1]
-    assert D1 == D and w2.shape == (E, D, H) and tw.shape == ids.shape == (T, k)
+    if fp4_weights:
+        assert mx and D1 * 2 == D and w2.shape == (E, D, H // 2) and tw.shape == ids.shape == (T, k)
+    else:
+        assert D1 == D and w2.shape == (E, D, H) and tw.shape == ids.shape == (T, k)
     if mx:
         x_sf, w1_sf, w2_sf = (np.ascontiguousarray(a, np.uint8) for a in (x_sf, w1_sf, w2_sf))
         assert x.dtype == np.uint8 and w1.dtype == np.uint8 and w2.dtype == np.uint8
@@ -179,7 +207,7 @@ def moe_ffn(x, w1, w2, topk_ids, topk_w, *, act=ACT_BF16, x_sf=None, w1_sf=None,
     tok = None if tokens is None else np.ascontiguousarray(tokens, np.int32)
     n = T if tok is None else tok.size
     out = np.zeros((n, D), np.float64)
-    rc = _load().oracle_moe_ffn(T, E, D, H, k, IN_MXFP8 if mx else IN_BF16,
+    rc = _load().oracle_moe_ffn(T, E, D, H, k, IN_MXFP4W if fp4_weights else (IN_MXFP8 if mx else IN_BF16),
                                 _ptr(x), _ptr(x_sf), _ptr(w1), _ptr(w1_sf), _ptr(w2), _ptr(w2_sf),
                                 _ptr(ids), _ptr(tw), act, _ptr(tok), n, _ptr(out), int(threads),
                                 float(swiglu_limit))

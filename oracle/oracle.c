@@ -138,6 +138,53 @@ void oracle_mx_quantize(const double* a, int n, uint8_t* q, uint8_t* sf, double*
     }
 }
 
+/*
+ * OCP E2M1 (the MXFP4 element; routed expert weights in "GC-MoE on SM120"
+ * sec. 2.2, scale formats, one UE8M0 scale per 32 elements): s.ee.m in the
+ * low four bits of a byte, bias 1, exponent field 0 = subnormal (0 or 0.5),
+ * no infinities or NaN; the magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4 and 6.
+ */
+double oracle_e2m1_to_f64(uint8_t code) {
+    int s = (code >> 3) & 1, ef = (code >> 1) & 3, m = code & 1;
+    double v = ef == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, ef - 1);
+    return s ? -v : v;
+}
+
+/* Real number -> E2M1 (low four bits), round to nearest with ties to the even
+ * code (mantissa bit 0), saturating to +-6.  (NaN is not representable; it
+ * maps to the largest magnitude.) */
+uint8_t oracle_f64_to_e2m1(double v) {
+    uint8_t sign = (v < 0 || (v == 0 && signbit(v))) ? 0x8 : 0x0;
+    double a = fabs(v);
+    if (isnan(v) || a >= 6.0) return sign | 0x7;
+    if (a < 1.0) {
+        /* subnormal grid: multiples of 0.5 (1.0 is the smallest normal, code 2) */
+        double n = nearbyint(a * 2.0);
+        return sign | (uint8_t)n;
+    }
+    int ex;
+    double f = frexp(a, &ex);                           /* a = f 2^ex, f in [0.5,1) */
+    int e = ex - 1;                                     /* a = (2f) 2^e, 2f in [1,2) */
+    double mant = nearbyint((2.0 * f - 1.0) * 2.0);     /* 1 fraction bit, RNE */
+    if (mant == 2.0) { mant = 0.0; e += 1; }
+    if (e > 2) return sign | 0x7;
+    return sign | (uint8_t)(((e + 1) << 1) | (int)mant);
+}
+
+/*
+ * Scale exponent for one MXFP4 block: the smallest integer e with
+ * amax * 2^-e <= 6, i.e. ceil(log2(amax / 6)).  With amax = m 2^p, m in
+ * [1,2), and 6 = 1.5 2^2:  e = p - 2 + (m > 1.5).  amax == 0 yields 0.
+ */
+int oracle_mx4_scale_exponent(double amax) {
+    if (amax == 0.0) return 0;
+    int ex;
+    double f = frexp(amax, &ex);
+    double m = 2.0 * f;
+    int p = ex - 1;
+    return p - 2 + (m > 1.5 ? 1 : 0);
+}
+
 /* ------------------------------------------------------------------------ */
 /* Routing permutation                                                      */
 /* ------------------------------------------------------------------------ */
@@ -237,7 +284,7 @@ int oracle_router_topk(int T, int E, int k, const float* logits, int32_t* ids, d
 /* The forward pass                                                         */
 /* ------------------------------------------------------------------------ */
 
-enum { ORACLE_IN_BF16 = 0, ORACLE_IN_MXFP8 = 1 };
+enum { ORACLE_IN_BF16 = 0, ORACLE_IN_MXFP8 = 1, ORACLE_IN_MXFP4W = 2 };
 enum { ORACLE_ACT_EXACT = 0, ORACLE_ACT_BF16 = 1, ORACLE_ACT_MXFP8 = 2 };
 
 /* Element i of a row-major operand, dequantized exactly to double.
@@ -246,6 +293,17 @@ enum { ORACLE_ACT_EXACT = 0, ORACLE_ACT_BF16 = 1, ORACLE_ACT_MXFP8 = 2 };
 static double elem(int in_mode, const void* v, const uint8_t* sf, int64_t i) {
     if (in_mode == ORACLE_IN_BF16) return oracle_bf16_to_f64(((const uint16_t*)v)[i]);
     return oracle_e4m3_to_f64(((const uint8_t*)v)[i]) * oracle_e8m0_to_f64(sf[i / 32]);
+}
+
+/* Element i of a weight operand.  MXFP4 weights: E2M1 codes packed two to a
+ * byte along the last dimension (element 2j in the low four bits of byte j,
+ * element 2j + 1 in the high four), scaled by 2^(sf[i/32] - 127); the
+ * activations stay MXFP8 in that mode. */
+static double welem(int in_mode, const void* v, const uint8_t* sf, int64_t i) {
+    if (in_mode != ORACLE_IN_MXFP4W) return elem(in_mode, v, sf, i);
+    uint8_t byte = ((const uint8_t*)v)[i / 2];
+    uint8_t code = (i & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xf);
+    return oracle_e2m1_to_f64(code) * oracle_e8m0_to_f64(sf[i / 32]);
 }
 
 static double silu(double g) { return g / (1.0 + exp(-g)); }
@@ -273,7 +331,8 @@ static double silu(double g) { return g / (1.0 + exp(-g)); }
  * act_round: EXACT keeps fp64; BF16 rounds each a[h] to binary32 then to bf16
  * (RNE); MXFP8 requantizes a to e4m3 with one scale per 32 consecutive h.
  * Shapes: x[T][D], W1[E][2H][D], W2[E][D][H], ids/topk_w[T][k]; MXFP8 scale
- * arrays have one byte per 32 elements of the last dimension.
+ * arrays have one byte per 32 elements of the last dimension.  in_mode
+ * MXFP4W: x as MXFP8, W1 / W2 as MXFP4 (see welem; D and H multiples of 32).
  * Returns 0, or -1 for an expert id outside [0, E) or a bad argument.
  */
 int oracle_moe_ffn(int T, int E, int D, int H, int k, int in_mode,
@@ -285,7 +344,7 @@ int oracle_moe_ffn(int T, int E, int D, int H, int k, int in_mode,
                    double* out, int n_threads, double swiglu_limit) {
     if (T < 0 || E < 1 || D < 1 || H < 1 || k < 1) return -1;
     if (act_mode == ORACLE_ACT_MXFP8 && H % 32) return -1;
-    if (in_mode == ORACLE_IN_MXFP8 && (D % 32 || H % 32)) return -1;
+    if ((in_mode == ORACLE_IN_MXFP8 || in_mode == ORACLE_IN_MXFP4W) && (D % 32 || H % 32)) return -1;
     int n = tokens ? n_tokens : T;
     for (int i = 0; i < n; ++i) {
         int t = tokens ? tokens[i] : i;
@@ -317,7 +376,8 @@ int oracle_moe_ffn(int T, int E, int D, int H, int k, int in_mode,
                 double* acc = out + (int64_t)i * D;
                 for (int d = 0; d < D; ++d) {
                     acc[d] = 0.0;
-                    xd[d] = elem(in_mode, x, x_sf, (int64_t)t * D + d);
+                    xd[d] = elem(in_mode == ORACLE_IN_MXFP4W ? ORACLE_IN_MXFP8 : in_mode, x, x_sf,
+                                 (int64_t)t * D + d);
                 }
                 for (int j = 0; j < k; ++j) {
                     int e = ids[(int64_t)t * k + j];
@@ -327,8 +387,8 @@ int oracle_moe_ffn(int T, int E, int D, int H, int k, int in_mode,
                         double sg = 0.0, su = 0.0;
                         int64_t rg = w1e + (int64_t)h * D, ru = w1e + (int64_t)(H + h) * D;
                         for (int d = 0; d < D; ++d) {
-                            sg += elem(in_mode, w1, w1_sf, rg + d) * xd[d];
-                            su += elem(in_mode, w1, w1_sf, ru + d) * xd[d];
+                            sg += welem(in_mode, w1, w1_sf, rg + d) * xd[d];
+                            su += welem(in_mode, w1, w1_sf, ru + d) * xd[d];
                         }
                         g[h] = sg;
                         u[h] = su;
@@ -350,7 +410,7 @@ int oracle_moe_ffn(int T, int E, int D, int H, int k, int in_mode,
                     for (int d = 0; d < D; ++d) {
                         double y = 0.0;
                         int64_t r = w2e + (int64_t)d * H;
-                        for (int h = 0; h < H; ++h) y += elem(in_mode, w2, w2_sf, r + h) * a[h];
+                        for (int h = 0; h < H; ++h) y += welem(in_mode, w2, w2_sf, r + h) * a[h];
                         acc[d] += w * y;
                     }
                 }
