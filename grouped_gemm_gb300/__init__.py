@@ -16,7 +16,7 @@ __all__ = [
     "MOE_BF16", "MOE_MXFP8", "MOE_FUSED", "MOE_SPLIT", "MoeFFNError", "library_path", "lib",
     "moe_ffn_workspace_size", "moe_ffn_workspace_init", "moe_ffn_forward", "moe_ffn_forward_logits", "moe_ffn_forward_ex", "MoeFFNExtras",
     "moe_ffn_workspace_size_ex", "moe_ffn_router_topk", "moe_ffn_route", "moe_ffn_route_noalloc",
-    "moe_ffn_sync_status", "moe_ffn_set_wait_limit_ns", "moe_ffn_profile_enable", "moe_ffn_profile_read", "moe_ffn_profile_stage_kernel", "moe_ffn_set_option", "MOE_OPT_GATHER", "moe_ffn_prepare_mxfp8_weights", "moe_ffn_debug_mx_quantize", "moe_ffn_status_string", "alloc_workspace",
+    "moe_ffn_sync_status", "moe_ffn_set_wait_limit_ns", "moe_ffn_profile_enable", "moe_ffn_profile_read", "moe_ffn_profile_stage_kernel", "moe_ffn_set_option", "MOE_OPT_GATHER", "moe_ffn_prepare_mxfp8_weights", "moe_ffn_widen_mxfp4_weights", "moe_ffn_debug_mx_quantize", "moe_ffn_status_string", "alloc_workspace",
 ]
 
 MOE_BF16, MOE_MXFP8 = 0, 1
@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
             L.moe_ffn_route_noalloc.restype = i
             L.moe_ffn_prepare_mxfp8_weights.argtypes = [vp, vp, vp, vp, i, i, i, vp]
             L.moe_ffn_prepare_mxfp8_weights.restype = i
+            L.moe_ffn_widen_mxfp4_weights.argtypes = [vp, c.c_int64, vp, vp]
+            L.moe_ffn_widen_mxfp4_weights.restype = i
             L.moe_ffn_debug_mx_quantize.argtypes = [vp, c.c_int64, vp, vp, vp]
             L.moe_ffn_debug_mx_quantize.restype = i
             L.moe_ffn_sync_status.argtypes = [vp, vp]
@@ -211,6 +213,14 @@ def moe_ffn_route_noalloc(topk_ids, topk_w, T, E, k, counts, offsets, slot_of_pa
 def moe_ffn_prepare_mxfp8_weights(w1_sf, w2_sf, w1_sf_packed, w2_sf_packed, E, D, H, stream=None) -> int:
     return _check(lib().moe_ffn_prepare_mxfp8_weights(_p(w1_sf), _p(w2_sf), _p(w1_sf_packed), _p(w2_sf_packed), E, D,
                                                        H, _stream(stream)), "moe_ffn_prepare_mxfp8_weights")
+
+
+def moe_ffn_widen_mxfp4_weights(w_fp4, w_e4m3, stream=None) -> int:
+    """MXFP4 weight codes (uint8, two per byte) -> e4m3 codes (uint8, one per byte)."""
+    if w_fp4.numel() * 2 != w_e4m3.numel():
+        raise ValueError(f"w_fp4 holds {w_fp4.numel() * 2} codes, w_e4m3 {w_e4m3.numel()}")
+    return _check(lib().moe_ffn_widen_mxfp4_weights(_p(w_fp4), w_e4m3.numel(), _p(w_e4m3), _stream(stream)),
+                  "moe_ffn_widen_mxfp4_weights")
 
 
 def moe_ffn_debug_mx_quantize(x, q, sf, stream=None) -> int:

@@ -17,6 +17,8 @@ namespace moe {
 // The routing kernels the last launch_route call of this host thread launched
 // ('+' between them; route.cu).
 const char* last_route_kernels();
+// MXFP4 weight codes widened to e4m3 codes (mx4.cu)
+cudaError_t launch_widen_e2m1(const void* in, int64_t n_bytes, void* out, int grid, cudaStream_t stream);
 }  // namespace moe
 
 namespace moe {
@@ -902,6 +904,16 @@ moe_status_t moe_ffn_prepare_mxfp8_weights(const void* w1_sf, const void* w2_sf,
   cudaError_t e = launch_pack_sf(w1_sf, w1_sf_packed, (int64_t)E * 2 * H, D, sms * 4, st);
   if (e == cudaSuccess) e = launch_pack_sf(w2_sf, w2_sf_packed, (int64_t)E * D, H, sms * 4, st);
   return cuda_status(e);
+}
+
+moe_status_t moe_ffn_widen_mxfp4_weights(const void* w_fp4, int64_t n_elems, void* w_e4m3, void* stream) {
+  if (n_elems < 0 || n_elems % 32) return MOE_ERR_INVALID_ARG;
+  if (n_elems == 0) return MOE_OK;
+  if (!w_fp4 || !w_e4m3) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w_fp4) || !aligned16(w_e4m3)) return MOE_ERR_MISALIGNED;
+  const int sms = num_sms();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  return cuda_status(launch_widen_e2m1(w_fp4, n_elems / 2, w_e4m3, sms * 8, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_ffn_debug_mx_quantize(const float* in, int64_t n, uint8_t* q, uint8_t* sf, void* stream) {

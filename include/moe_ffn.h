@@ -158,6 +158,26 @@ moe_status_t moe_ffn_forward_ex(const void* x, const void* x_sf, const void* w1,
 moe_status_t moe_ffn_prepare_mxfp8_weights(const void* w1_sf, const void* w2_sf, void* w1_sf_packed,
                                            void* w2_sf_packed, int E, int D, int H, void* stream);
 
+/* MXFP4 expert weights for the MXFP8 path.  An MXFP4 weight is an E2M1 code
+ * (1 sign, 2 exponent bits with bias 1, 1 mantissa bit: magnitudes 0, 0.5, 1,
+ * 1.5, 2, 3, 4, 6) with one ue8m0 scale per 32 consecutive elements along the
+ * reduction dimension, the routed-weight format of "GC-MoE on SM120" sec. 2.2
+ * (scale formats).  This call widens the codes once, at weight-load time, to
+ * e4m3 codes of the same values (exact: every E2M1 value is an e4m3 value);
+ * the scale arrays stay as they are and go through
+ * moe_ffn_prepare_mxfp8_weights, and moe_ffn_forward then runs with
+ * MOE_MXFP8.  The weights then occupy one byte per element in HBM, not half.
+ *   w_fp4   n_elems/2 bytes, two codes per byte along the contiguous dimension:
+ *           element 2j in bits 0..3 of byte j, element 2j+1 in bits 4..7;
+ *           16-byte aligned (W1 [E, 2H, D/2] and W2 [E, D, H/2] row-major)
+ *   w_e4m3  n_elems bytes output, element i in byte i, 16-byte aligned
+ *           (W1 [E, 2H, D], W2 [E, D, H])
+ * n_elems a multiple of 32 (0 does nothing).  Device pointers, asynchronous
+ * on stream; the input is only read.  Errors: MOE_ERR_INVALID_ARG (n_elems
+ * negative or not a multiple of 32, NULL pointer), MOE_ERR_MISALIGNED,
+ * MOE_ERR_CUDA (launch failure). */
+moe_status_t moe_ffn_widen_mxfp4_weights(const void* w_fp4, int64_t n_elems, void* w_e4m3, void* stream);
+
 /* Test hook: the MXFP8 requantization the up-projection epilogue applies to
  * act, run on n fp32 values (n % 32 == 0): per 32 values, scale exponent
  * e = ceil(log2(amax/448)) (0 for amax == 0, at least -127), scale byte

@@ -113,3 +113,14 @@ def test_extras_and_router_reject_bad_arguments_on_host():
     assert moe.moe_ffn_workspace_size_ex(64, 8, 256, 128, 2, 0) == moe.moe_ffn_workspace_size(64, 8, 256, 128, 2)
     assert moe.moe_ffn_workspace_size_ex(64, 8, 256, 128, 2, 2) > moe.moe_ffn_workspace_size(64, 10, 256, 128, 4)
     assert moe.moe_ffn_workspace_size_ex(64, 1020, 256, 128, 2, 5) == 0  # E + n_shared > 1024
+
+
+def test_widen_mxfp4_rejects_bad_arguments_on_host():
+    L = moe.lib()
+    A = 1 << 20  # a fake, 16-byte aligned address: never dereferenced
+    assert L.moe_ffn_widen_mxfp4_weights(A, 48, A, None) == 1        # not a multiple of 32
+    assert L.moe_ffn_widen_mxfp4_weights(A, -32, A, None) == 1
+    assert L.moe_ffn_widen_mxfp4_weights(None, 64, A, None) == 1
+    assert L.moe_ffn_widen_mxfp4_weights(A + 8, 64, A, None) == 3     # misaligned input
+    assert L.moe_ffn_widen_mxfp4_weights(A, 64, A + 4, None) == 3     # misaligned output
+    assert L.moe_ffn_widen_mxfp4_weights(None, 0, None, None) == 0    # nothing to do
