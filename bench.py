@@ -51,7 +51,7 @@ def parse_args():
                          "fused into the routing launch) instead of given top-k ids and weights")
     ap.add_argument("--no-graph", action="store_true", help="launch each step eagerly instead of replaying a CUDA graph")
     ap.add_argument("--option", action="append", default=[], metavar="NAME=VALUE",
-                    help="library tuning option, e.g. PAIR_TAILS=0 (moe_ffn_set_option; repeatable)")
+                    help="library tuning option, e.g. PAIR_MMA=0 (moe_ffn_set_option; repeatable)")
     return ap.parse_args()
 
 

@@ -620,9 +620,10 @@ moe_status_t moe_ffn_route(const int32_t* topk_ids, const float* topk_w, int T, 
   if (workspace_bytes < ws.bytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (T == 0) {
-    if (counts) cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, st);
-    if (offsets) cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), st);
-    return cuda_status(cudaGetLastError());
+    cudaError_t z = cudaSuccess;
+    if (counts) z = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, st);
+    if (z == cudaSuccess && offsets) z = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (E + 1), st);
+    return cuda_status(z);
   }
   cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
