@@ -85,6 +85,19 @@ def algorithmic(w, ids):
     }
 
 
+def gemm_only(stage_ms, pipeline, step_flops):
+    """The GEMM stages alone (routing and gather excluded, as in the pages'
+    timed region): their summed per-stage durations and the step's FLOPs over
+    that time.  None when a stage is missing."""
+    names = ["up_swiglu", "down_reduce"] if pipeline == "split" else ["fused_gemm", "to_bf16"]
+    if any(n not in stage_ms for n in names):
+        return None
+    ms = sum(stage_ms[n] for n in names)
+    if ms <= 0:
+        return None
+    return {"ms": round(ms, 5), "tflops": round(step_flops / (ms * 1e-3) / 1e12, 3), "stages": names}
+
+
 def source_digest(files):
     h = hashlib.sha256()
     for f in files:
@@ -400,6 +413,7 @@ def run_ours(args, rank, world, local_rank):
                    "l2": (f"inputs larger than L2: {alg['step_bytes'] / 1e9:.2f} GB compulsory per step "
                           f"(129 MB L2), no flush needed")},
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gemm_only": gemm_only(stage_ms, args.pipeline, alg["step_flops"]),
         "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
     }
 

@@ -84,3 +84,12 @@ def test_algorithmic_counts():
     # compulsory bytes: x, the live experts' weights, ids and weights, out
     assert alg["step_bytes"] == w.T * w.D * 2 + 2 * 3 * w.H * w.D * 2 + P * 8 + w.T * w.D * 2
     assert alg["live_experts"] == 2
+
+
+def test_gemm_only_figure():
+    # split: up + down; fused: the fused GEMM and its rounding pass
+    g = bench.gemm_only({"route": 0.02, "gather_zero": 0.03, "up_swiglu": 0.2, "down_reduce": 0.1}, "split", 3e11)
+    assert g["ms"] == pytest.approx(0.3) and g["tflops"] == pytest.approx(3e11 / 0.3e-3 / 1e12)
+    g = bench.gemm_only({"route": 0.02, "gather_zero": 0.03, "fused_gemm": 0.4, "to_bf16": 0.0}, "fused", 4e11)
+    assert g["ms"] == pytest.approx(0.4) and g["stages"] == ["fused_gemm", "to_bf16"]
+    assert bench.gemm_only({"route": 0.02}, "split", 1e9) is None
