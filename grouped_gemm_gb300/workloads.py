@@ -34,7 +34,7 @@ class Workload:
     E: int
     k: int
     routing: str          # "topk_logits" | "uniform" | "zipf"
-    dtype: str = "bf16"   # "bf16" | "mxfp8" | "mxfp4w" (MXFP8 activations, MXFP4 weights)
+    dtype: str = "bf16"   # "bf16" | "mxfp8" | "mxfp4w" (MXFP8 activations, MXFP4 weights) | "nvfp4"
 
     @property
     def pairs(self) -> int:
@@ -171,6 +171,50 @@ def mx4_encode_rows(a: np.ndarray):
     return packed, sf
 
 
+E4M3_MAX = 448.0
+E2M1_MAX = 6.0
+
+
+def nv4_global_scale(a: np.ndarray) -> np.float32:
+    """Global scale of an NVFP4 tensor: amax / (448 * 6), so that the largest
+    block scale is the largest e4m3 value (1.0 for an all-zero tensor)."""
+    amax = float(np.abs(a).max()) if a.size else 0.0
+    return np.float32(amax / (E4M3_MAX * E2M1_MAX) if amax > 0 else 1.0)
+
+
+def nv4_encode_rows(a: np.ndarray, gs: float):
+    """Encode float32 rows (last dim a multiple of 16) as NVFP4 with global
+    scale gs: E2M1 codes packed two to a byte (element 2j in the low four
+    bits) + e4m3 scale bytes, one per 16 elements.
+
+    Input preparation only: each block's scale is torch's float8_e4m3fn cast
+    of amax / (6 gs), clamped to 448 first; each element goes to the nearest E2M1 value of
+    a / (scale gs) (ties to the even code, saturating at 6).
+    """
+    a = np.ascontiguousarray(a, np.float32)
+    shp = a.shape
+    blk = a.reshape(-1, 16).astype(np.float64)
+    amax = np.abs(blk).max(axis=1)
+    # torch's cast does not saturate (above 464 it gives NaN): clamp to 448 first
+    ratio = np.minimum(amax / (E2M1_MAX * float(gs)), E4M3_MAX)
+    sfc = torch.from_numpy(ratio.astype(np.float32)).to(torch.float8_e4m3fn)
+    sval = sfc.double().numpy()
+    sf = sfc.view(torch.uint8).numpy()
+    denom = sval * float(gs)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        scaled = np.where(denom[:, None] > 0, blk / denom[:, None], 0.0)
+    mag = np.minimum(np.abs(scaled), E2M1_MAX)
+    dist = np.abs(mag[..., None] - _E2M1_GRID)
+    best = dist.min(axis=-1, keepdims=True)
+    tied = dist == best
+    even = (np.arange(8) % 2 == 0)
+    code = np.where((tied & even).any(axis=-1), np.argmax(tied & even, axis=-1), np.argmax(tied, axis=-1))
+    code = code.astype(np.uint8) | np.where(scaled < 0, 8, 0).astype(np.uint8)
+    code = code.reshape(shp)
+    packed = (code[..., 0::2] | (code[..., 1::2] << 4)).astype(np.uint8)
+    return packed, sf.reshape(shp[:-1] + (shp[-1] // 16,))
+
+
 def make_inputs(w: Workload | str, seed: int = 0, T: int | None = None):
     """Draw one workload's inputs.  Order of draws: x, W1, W2, routing.
 
@@ -192,6 +236,19 @@ def make_inputs(w: Workload | str, seed: int = 0, T: int | None = None):
         for e in range(w.E):
             w2[e] = _bf16_bits(_normal(rng, (w.D, w.H), 0.02))
         out["w1"], out["w2"] = w1, w2
+    elif w.dtype == "nvfp4":  # NVFP4 activations and weights, global scales per tensor / per expert
+        xa = _normal(rng, (w.T, w.D), 1.0)
+        out["x_gs"] = nv4_global_scale(xa)
+        out["x"], out["x_sf"] = nv4_encode_rows(xa, out["x_gs"])
+        for name, rows, cols in (("w1", 2 * w.H, w.D), ("w2", w.D, w.H)):
+            q = np.empty((w.E, rows, cols // 2), np.uint8)
+            sf = np.empty((w.E, rows, cols // 16), np.uint8)
+            gs = np.empty(w.E, np.float32)
+            for e in range(w.E):
+                a = _normal(rng, (rows, cols), 0.02)
+                gs[e] = nv4_global_scale(a)
+                q[e], sf[e] = nv4_encode_rows(a, gs[e])
+            out[name], out[name + "_sf"], out[name + "_gs"] = q, sf, gs
     elif w.dtype == "mxfp4w":  # MXFP8 activations, MXFP4 weights
         out["x"], out["x_sf"] = mx_encode_rows(_normal(rng, (w.T, w.D), 1.0))
         w1 = np.empty((w.E, 2 * w.H, w.D // 2), np.uint8)

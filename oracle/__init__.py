@@ -26,7 +26,7 @@ _lock = threading.Lock()
 _lib = None
 
 IN_BF16, IN_MXFP8, IN_MXFP4W = 0, 1, 2
-ACT_EXACT, ACT_BF16, ACT_MXFP8 = 0, 1, 2
+ACT_EXACT, ACT_BF16, ACT_MXFP8, ACT_NVFP4 = 0, 1, 2, 3
 
 
 def build(force: bool = False) -> str:
@@ -75,6 +75,12 @@ def _load():
             lib.oracle_moe_ffn.argtypes = [c.c_int] * 6 + [c.c_void_p] * 8 + [c.c_int, c.c_void_p, c.c_int,
                                                                                c.c_void_p, c.c_int, c.c_double]
             lib.oracle_moe_ffn.restype = c.c_int
+            vp, i_, d_ = c.c_void_p, c.c_int, c.c_double
+            lib.oracle_nv4_quantize.argtypes = [vp, i_, d_, vp, vp, vp]
+            lib.oracle_nv4_quantize.restype = None
+            lib.oracle_moe_ffn_nvfp4.argtypes = ([i_] * 5 + [vp, vp, d_, vp, vp, vp, vp, vp, vp, vp, vp, i_, d_, vp, i_,
+                                                              vp, i_, d_])
+            lib.oracle_moe_ffn_nvfp4.restype = c.c_int
             lib.oracle_max_threads.argtypes = []
             lib.oracle_max_threads.restype = c.c_int
             _lib = lib
@@ -138,6 +144,18 @@ def mx_quantize(a: np.ndarray):
     sf = np.empty(a.size // 32, np.uint8)
     deq = np.empty(a.size, np.float64)
     _load().oracle_mx_quantize(_ptr(a), a.size, _ptr(q), _ptr(sf), _ptr(deq))
+    return q, sf, deq
+
+
+def nv4_quantize(a: np.ndarray, gs: float):
+    """Per-16 NVFP4 quantization of a 1-D array with global scale gs; returns
+    (packed codes, e4m3 scale bytes, dequantized)."""
+    a = np.ascontiguousarray(a, np.float64).ravel()
+    assert a.size % 16 == 0
+    q = np.zeros(a.size // 2, np.uint8)
+    sf = np.empty(a.size // 16, np.uint8)
+    deq = np.empty(a.size, np.float64)
+    _load().oracle_nv4_quantize(_ptr(a), a.size, float(gs), _ptr(q), _ptr(sf), _ptr(deq))
     return q, sf, deq
 
 
@@ -213,6 +231,36 @@ def moe_ffn(x, w1, w2, topk_ids, topk_w, *, act=ACT_BF16, x_sf=None, w1_sf=None,
                                 float(swiglu_limit))
     if rc != 0:
         raise ValueError(f"oracle_moe_ffn failed ({rc})")
+    return out
+
+
+def moe_ffn_nvfp4(x, x_sf, x_gs, w1, w1_sf, w1_gs, w2, w2_sf, w2_gs, topk_ids, topk_w, *, act=ACT_EXACT,
+                  act_gs: float = 0.0, tokens=None, threads: int = 0, swiglu_limit: float = 0.0) -> np.ndarray:
+    """fp64 forward pass with NVFP4 operands: packed E2M1 codes (two per byte,
+    low four bits first), e4m3 scale bytes per 16 along the last dimension, a
+    global scale for x and one per expert for W1 and W2.  ``act`` is
+    ACT_EXACT, ACT_BF16 or ACT_NVFP4 (requantized with global scale
+    ``act_gs``)."""
+    x, x_sf, w1, w1_sf, w2, w2_sf = (np.ascontiguousarray(a, np.uint8) for a in (x, x_sf, w1, w1_sf, w2, w2_sf))
+    w1_gs = np.ascontiguousarray(w1_gs, np.float32)
+    w2_gs = np.ascontiguousarray(w2_gs, np.float32)
+    ids = np.ascontiguousarray(topk_ids, np.int32)
+    tw = np.ascontiguousarray(topk_w, np.float32)
+    T, D = x.shape[0], x.shape[1] * 2
+    E, H2 = w1.shape[0], w1.shape[1]
+    H = H2 // 2
+    k = ids.shape[1]
+    assert w1.shape == (E, 2 * H, D // 2) and w2.shape == (E, D, H // 2)
+    assert x_sf.shape == (T, D // 16) and w1_sf.shape == (E, 2 * H, D // 16) and w2_sf.shape == (E, D, H // 16)
+    assert w1_gs.shape == (E,) and w2_gs.shape == (E,) and tw.shape == ids.shape == (T, k)
+    tok = None if tokens is None else np.ascontiguousarray(tokens, np.int32)
+    n = T if tok is None else tok.size
+    out = np.zeros((n, D), np.float64)
+    rc = _load().oracle_moe_ffn_nvfp4(T, E, D, H, k, _ptr(x), _ptr(x_sf), float(x_gs), _ptr(w1), _ptr(w1_sf),
+                                      _ptr(w1_gs), _ptr(w2), _ptr(w2_sf), _ptr(w2_gs), _ptr(ids), _ptr(tw), act,
+                                      float(act_gs), _ptr(tok), n, _ptr(out), int(threads), float(swiglu_limit))
+    if rc != 0:
+        raise ValueError(f"oracle_moe_ffn_nvfp4 failed ({rc})")
     return out
 
 

@@ -421,6 +421,158 @@ int oracle_moe_ffn(int T, int E, int D, int H, int k, int in_mode,
     return failed ? -2 : 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* NVFP4                                                                    */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * NVFP4 ("Porting Block-Scaled GEMM Kernels from Blackwell to Rubin": sec. 1.2
+ * counts 16 scales per 256-element row, i.e. one scale per 16 elements along
+ * K; sec. 5.3 dequantizes gate and up by the expert's global scale alpha):
+ * an element is an E2M1 code c, its 16-element block carries an E4M3 scale
+ * s (a non-negative code), and the whole operand (for the weights: each
+ * expert) one fp32 global scale G, so the value is
+ *     e2m1(c) * e4m3(s) * G.
+ * Codes are packed two per byte along K, element 2j in the low four bits.
+ */
+static double nv4_elem(const uint8_t* v, const uint8_t* sf, int64_t i) {
+    uint8_t byte = v[i / 2];
+    uint8_t code = (i & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xf);
+    return oracle_e2m1_to_f64(code) * oracle_e4m3_to_f64(sf[i / 16]);
+}
+
+/*
+ * Quantize n values (n a multiple of 16) to NVFP4 with global scale gs > 0.
+ * Reading (the pages give the format, not the recipe): per block of 16, on
+ * the values rounded to binary32 (the precision of the accumulators the
+ * kernel quantizes from), the block scale is the e4m3 code nearest to
+ * amax / (6 gs) (round to nearest even, saturating at 448), so that the
+ * largest element lands near the top of the E2M1 range; each element is
+ * then the E2M1 code nearest to v / (e4m3(s) gs) (ties to the even code,
+ * saturating at 6).  A block whose scale rounds to 0 is all zeros.
+ * codes: n/2 bytes (packed as above), sf: n/16 bytes, deq (optional): the
+ * dequantized values e2m1 * e4m3(s) * gs.
+ */
+void oracle_nv4_quantize(const double* a, int n, double gs, uint8_t* codes, uint8_t* sf, double* deq) {
+    for (int b = 0; b < n / 16; ++b) {
+        double amax = 0.0;
+        for (int i = 0; i < 16; ++i) {
+            double v = (double)(float)a[b * 16 + i];
+            if (fabs(v) > amax) amax = fabs(v);
+        }
+        uint8_t s = oracle_f64_to_e4m3(amax / (6.0 * gs));
+        double scale = oracle_e4m3_to_f64(s) * gs;
+        sf[b] = s;
+        for (int i = 0; i < 16; ++i) {
+            int idx = b * 16 + i;
+            double v = (double)(float)a[idx];
+            uint8_t c = scale > 0.0 ? oracle_f64_to_e2m1(v / scale) : 0;
+            if (idx & 1) codes[idx / 2] = (uint8_t)((codes[idx / 2] & 0x0f) | (c << 4));
+            else         codes[idx / 2] = (uint8_t)((codes[idx / 2] & 0xf0) | c);
+            if (deq) deq[idx] = oracle_e2m1_to_f64(c) * scale;
+        }
+    }
+}
+
+enum { ORACLE_ACT_NVFP4 = 3 };
+
+/*
+ * The forward pass of oracle_moe_ffn with NVFP4 operands: x [T, D/2] codes,
+ * x_sf [T, D/16], global x_gs; W1 [E, 2H, D/2], w1_sf [E, 2H, D/16], one
+ * global w1_gs[e] per expert; W2 [E, D, H/2], w2_sf [E, D, H/16], w2_gs[e].
+ * Every element is dequantized exactly (nv4_elem times its global scale) and
+ * the arithmetic is that of oracle_moe_ffn in fp64.  act_mode: EXACT keeps
+ * act in fp64; NVFP4 requantizes act per 16 along H with the global scale
+ * act_gs (oracle_nv4_quantize) before the down projection; BF16 rounds act
+ * to bf16 as in oracle_moe_ffn.  D and H multiples of 32.
+ * Returns 0, or -1 for an expert id outside [0, E) or a bad argument.
+ */
+int oracle_moe_ffn_nvfp4(int T, int E, int D, int H, int k,
+                         const uint8_t* x, const uint8_t* x_sf, double x_gs,
+                         const uint8_t* w1, const uint8_t* w1_sf, const float* w1_gs,
+                         const uint8_t* w2, const uint8_t* w2_sf, const float* w2_gs,
+                         const int32_t* ids, const float* topk_w,
+                         int act_mode, double act_gs, const int32_t* tokens, int n_tokens,
+                         double* out, int n_threads, double swiglu_limit) {
+    if (T < 0 || E < 1 || D < 1 || H < 1 || k < 1 || D % 32 || H % 32) return -1;
+    if (act_mode != ORACLE_ACT_EXACT && act_mode != ORACLE_ACT_BF16 && act_mode != ORACLE_ACT_NVFP4) return -1;
+    if (act_mode == ORACLE_ACT_NVFP4 && !(act_gs > 0.0)) return -1;
+    int n = tokens ? n_tokens : T;
+    for (int i = 0; i < n; ++i) {
+        int t = tokens ? tokens[i] : i;
+        if (t < 0 || t >= T) return -1;
+        for (int j = 0; j < k; ++j)
+            if (ids[(int64_t)t * k + j] < 0 || ids[(int64_t)t * k + j] >= E) return -1;
+    }
+#ifdef _OPENMP
+    if (n_threads > 0) omp_set_num_threads(n_threads);
+#else
+    (void)n_threads;
+#endif
+    int failed = 0;
+#pragma omp parallel
+    {
+        double* xd = (double*)malloc(sizeof(double) * (size_t)D);
+        double* g = (double*)malloc(sizeof(double) * (size_t)H);
+        double* u = (double*)malloc(sizeof(double) * (size_t)H);
+        double* a = (double*)malloc(sizeof(double) * (size_t)H);
+        uint8_t* aq = (uint8_t*)calloc((size_t)H / 2 + 1, 1);
+        uint8_t* asf = (uint8_t*)malloc((size_t)H / 16 + 1);
+        if (!xd || !g || !u || !a || !aq || !asf) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int i = 0; i < n; ++i) {
+                int t = tokens ? tokens[i] : i;
+                double* acc = out + (int64_t)i * D;
+                for (int d = 0; d < D; ++d) {
+                    acc[d] = 0.0;
+                    xd[d] = nv4_elem(x, x_sf, (int64_t)t * D + d) * x_gs;
+                }
+                for (int j = 0; j < k; ++j) {
+                    int e = ids[(int64_t)t * k + j];
+                    double w = (double)topk_w[(int64_t)t * k + j];
+                    double g1 = (double)w1_gs[e], g2 = (double)w2_gs[e];
+                    int64_t w1e = (int64_t)e * 2 * H * D;
+                    for (int h = 0; h < H; ++h) {
+                        double sg = 0.0, su = 0.0;
+                        int64_t rg = w1e + (int64_t)h * D, ru = w1e + (int64_t)(H + h) * D;
+                        for (int d = 0; d < D; ++d) {
+                            sg += nv4_elem(w1, w1_sf, rg + d) * g1 * xd[d];
+                            su += nv4_elem(w1, w1_sf, ru + d) * g1 * xd[d];
+                        }
+                        g[h] = sg;
+                        u[h] = su;
+                    }
+                    if (swiglu_limit > 0.0) {
+                        for (int h = 0; h < H; ++h) {
+                            if (g[h] > swiglu_limit) g[h] = swiglu_limit;
+                            if (u[h] > swiglu_limit) u[h] = swiglu_limit;
+                            if (u[h] < -swiglu_limit) u[h] = -swiglu_limit;
+                        }
+                    }
+                    for (int h = 0; h < H; ++h) a[h] = silu(g[h]) * u[h];
+                    if (act_mode == ORACLE_ACT_BF16) {
+                        for (int h = 0; h < H; ++h) a[h] = oracle_bf16_to_f64(oracle_f32_to_bf16((float)a[h]));
+                    } else if (act_mode == ORACLE_ACT_NVFP4) {
+                        oracle_nv4_quantize(a, H, act_gs, aq, asf, a);
+                    }
+                    int64_t w2e = (int64_t)e * D * H;
+                    for (int d = 0; d < D; ++d) {
+                        double y = 0.0;
+                        int64_t r = w2e + (int64_t)d * H;
+                        for (int h = 0; h < H; ++h) y += nv4_elem(w2, w2_sf, r + h) * g2 * a[h];
+                        acc[d] += w * y;
+                    }
+                }
+            }
+        }
+        free(xd); free(g); free(u); free(a); free(aq); free(asf);
+    }
+    return failed ? -2 : 0;
+}
+
 int oracle_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();
