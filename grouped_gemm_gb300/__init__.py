@@ -98,11 +98,18 @@ def lib() -> ctypes.CDLL:
 
 
 def _p(t):
-    """Device (or host) pointer of a tensor, None for None, ints pass through."""
+    """Device pointer of a tensor, None for None, ints pass through.  Every
+    array argument of the C ABI is a dense device array, so a tensor must be
+    a contiguous CUDA tensor: anything else is refused here rather than
+    handed to a kernel."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_cuda:
+        raise ValueError(f"expected a CUDA tensor, got one on {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"expected a contiguous tensor, got strides {tuple(t.stride())}")
     return t.data_ptr()
 
 

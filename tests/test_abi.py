@@ -124,3 +124,15 @@ def test_widen_mxfp4_rejects_bad_arguments_on_host():
     assert L.moe_ffn_widen_mxfp4_weights(A + 8, 64, A, None) == 3     # misaligned input
     assert L.moe_ffn_widen_mxfp4_weights(A, 64, A + 4, None) == 3     # misaligned output
     assert L.moe_ffn_widen_mxfp4_weights(None, 0, None, None) == 0    # nothing to do
+
+
+def test_binding_refuses_host_and_strided_tensors():
+    import torch
+    x = torch.zeros(4, 256, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        moe._p(x)
+    with pytest.raises(ValueError):
+        moe._p(x.t())
+    assert moe._p(None) is None and moe._p(1 << 20) == 1 << 20
+    with pytest.raises(ValueError, match="CUDA"):
+        moe.moe_ffn_router_topk(torch.zeros(4, 8), 2, torch.zeros(4, 2, dtype=torch.int32), torch.zeros(4, 2))
