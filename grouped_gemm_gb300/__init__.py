@@ -113,6 +113,31 @@ def _p(t):
     return t.data_ptr()
 
 
+def _need(t, nbytes, name):
+    """A tensor argument must hold at least nbytes (the kernels read and write
+    exactly the extents the sizes imply; a raw int pointer is the caller's
+    responsibility)."""
+    if t is None or isinstance(t, int):
+        return
+    have = t.numel() * t.element_size()
+    if have < nbytes:
+        raise ValueError(f"{name} holds {have} bytes, the call needs {int(nbytes)}")
+
+
+def _need_forward(x, x_sf, w1, w1_sf, w2, w2_sf, topk_ids, topk_w, out, T, E, D, H, k, dtype):
+    eb = 2 if dtype == MOE_BF16 else 1
+    _need(x, T * D * eb, "x")
+    _need(w1, E * 2 * H * D * eb, "w1")
+    _need(w2, E * D * H * eb, "w2")
+    _need(out, T * D * 2, "out")
+    _need(topk_ids, T * k * 4, "topk_ids")
+    _need(topk_w, T * k * 4, "topk_w")
+    if dtype != MOE_BF16:
+        _need(x_sf, T * D // 32, "x_sf")
+        _need(w1_sf, E * 2 * H * D // 32, "w1_sf")
+        _need(w2_sf, E * D * H // 32, "w2_sf")
+
+
 def _stream(stream):
     if stream is None:
         import torch
@@ -161,6 +186,7 @@ def moe_ffn_forward(x, w1, w2, topk_ids, topk_w, out, *, E, D, H, k, workspace, 
                     pipeline=MOE_SPLIT, x_sf=None, w1_sf=None, w2_sf=None, T=None, stream=None,
                     check=True) -> int:
     T = x.shape[0] if T is None else T
+    _need_forward(x, x_sf, w1, w1_sf, w2, w2_sf, topk_ids, topk_w, out, T, E, D, H, k, dtype)
     st = lib().moe_ffn_forward(_p(x), _p(x_sf), _p(w1), _p(w1_sf), _p(w2), _p(w2_sf), _p(topk_ids), _p(topk_w),
                                _p(out), T, E, D, H, k, dtype, pipeline, _p(workspace),
                                workspace.numel() * workspace.element_size(), _stream(stream))
@@ -173,6 +199,8 @@ def moe_ffn_forward_logits(x, w1, w2, router_logits, topk_ids, topk_w, out, *, E
     """moe_ffn_forward from router logits [T, E] fp32; topk_ids / topk_w [T, k]
     are written by the call."""
     T = x.shape[0] if T is None else T
+    _need_forward(x, x_sf, w1, w1_sf, w2, w2_sf, topk_ids, topk_w, out, T, E, D, H, k, dtype)
+    _need(router_logits, T * E * 4, "router_logits")
     st = lib().moe_ffn_forward_logits(_p(x), _p(x_sf), _p(w1), _p(w1_sf), _p(w2), _p(w2_sf), _p(router_logits),
                                       _p(topk_ids), _p(topk_w), _p(out), T, E, D, H, k, dtype, pipeline,
                                       _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
@@ -185,6 +213,10 @@ def moe_ffn_forward_ex(x, w1, w2, topk_ids, topk_w, out, *, E, D, H, k, workspac
     """moe_ffn_forward with a clamped SwiGLU (swiglu_limit > 0), n_shared shared
     experts stored after the E routed ones, and/or router logits [T, E]."""
     T = x.shape[0] if T is None else T
+    ns = int(n_shared)
+    ns = ns if 0 <= ns <= 1024 - E else 0   # an out-of-range count is the C ABI's to reject
+    _need_forward(x, x_sf, w1, w1_sf, w2, w2_sf, topk_ids, topk_w, out, T, E + ns, D, H, k, dtype)
+    _need(router_logits, T * E * 4, "router_logits")
     ex = MoeFFNExtras(float(swiglu_limit), int(n_shared), _p(router_logits))
     st = lib().moe_ffn_forward_ex(_p(x), _p(x_sf), _p(w1), _p(w1_sf), _p(w2), _p(w2_sf), _p(topk_ids), _p(topk_w),
                                   _p(out), T, E, D, H, k, dtype, pipeline, ctypes.byref(ex), _p(workspace),
@@ -196,12 +228,24 @@ def moe_ffn_router_topk(logits, k, topk_ids, topk_w, T=None, E=None, stream=None
     """Top-k experts and softmax-renormalized weights of router logits [T, E]."""
     T = logits.shape[0] if T is None else T
     E = logits.shape[1] if E is None else E
+    _need(logits, T * E * 4, "logits")
+    _need(topk_ids, T * k * 4, "topk_ids")
+    _need(topk_w, T * k * 4, "topk_w")
     st = lib().moe_ffn_router_topk(_p(logits), T, E, k, _p(topk_ids), _p(topk_w), _stream(stream))
     return _check(st, "moe_ffn_router_topk") if check else st
 
 
+def _need_route(topk_ids, topk_w, T, E, k, counts, offsets, slot_of_pair):
+    _need(topk_ids, T * k * 4, "topk_ids")
+    _need(topk_w, T * k * 4, "topk_w")
+    _need(counts, E * 4, "counts")
+    _need(offsets, (E + 1) * 4, "offsets")
+    _need(slot_of_pair, T * k * 4, "slot_of_pair")
+
+
 def moe_ffn_route(topk_ids, topk_w, T, E, k, counts, offsets, slot_of_pair, workspace, stream=None,
                   check=True) -> int:
+    _need_route(topk_ids, topk_w, T, E, k, counts, offsets, slot_of_pair)
     st = lib().moe_ffn_route(_p(topk_ids), _p(topk_w), T, E, k, _p(counts), _p(offsets), _p(slot_of_pair),
                              _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     return _check(st, "moe_ffn_route") if check else st
@@ -212,12 +256,17 @@ def moe_ffn_route_noalloc(topk_ids, topk_w, T, E, k, counts, offsets, slot_of_pa
     """Routing permutation without a caller workspace, for callers that
     cannot allocate device memory (scratch is a fixed array inside the
     library; T*k <= 131072).  Calls on one device must not overlap."""
+    _need_route(topk_ids, topk_w, T, E, k, counts, offsets, slot_of_pair)
+    _need(status_bits, 4, "status_bits")
     st = lib().moe_ffn_route_noalloc(_p(topk_ids), _p(topk_w), T, E, k, _p(counts), _p(offsets),
                                      _p(slot_of_pair), _p(status_bits), _stream(stream))
     return _check(st, "moe_ffn_route_noalloc") if check else st
 
 
 def moe_ffn_prepare_mxfp8_weights(w1_sf, w2_sf, w1_sf_packed, w2_sf_packed, E, D, H, stream=None) -> int:
+    for t, n, name in ((w1_sf, E * 2 * H * D // 32, "w1_sf"), (w1_sf_packed, E * 2 * H * D // 32, "w1_sf_packed"),
+                       (w2_sf, E * D * H // 32, "w2_sf"), (w2_sf_packed, E * D * H // 32, "w2_sf_packed")):
+        _need(t, n, name)
     return _check(lib().moe_ffn_prepare_mxfp8_weights(_p(w1_sf), _p(w2_sf), _p(w1_sf_packed), _p(w2_sf_packed), E, D,
                                                        H, _stream(stream)), "moe_ffn_prepare_mxfp8_weights")
 
@@ -231,6 +280,8 @@ def moe_ffn_widen_mxfp4_weights(w_fp4, w_e4m3, stream=None) -> int:
 
 
 def moe_ffn_debug_mx_quantize(x, q, sf, stream=None) -> int:
+    _need(q, x.numel(), "q")
+    _need(sf, x.numel() // 32, "sf")
     return _check(lib().moe_ffn_debug_mx_quantize(_p(x), x.numel(), _p(q), _p(sf), _stream(stream)),
                   "moe_ffn_debug_mx_quantize")
 

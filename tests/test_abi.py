@@ -136,3 +136,35 @@ def test_binding_refuses_host_and_strided_tensors():
     assert moe._p(None) is None and moe._p(1 << 20) == 1 << 20
     with pytest.raises(ValueError, match="CUDA"):
         moe.moe_ffn_router_topk(torch.zeros(4, 8), 2, torch.zeros(4, 2, dtype=torch.int32), torch.zeros(4, 2))
+
+
+def test_binding_checks_buffer_sizes():
+    # sizes are checked before any pointer is taken, so CPU tensors show it here
+    import torch
+    T, E, D, H, k = 4, 2, 256, 128, 2
+    x = torch.zeros(T, D, dtype=torch.bfloat16)
+    w1 = torch.zeros(E, 2 * H, D, dtype=torch.bfloat16)
+    w2 = torch.zeros(E, D, H - 1, dtype=torch.bfloat16)            # one column short
+    ids = torch.zeros(T, k, dtype=torch.int32)
+    tw = torch.zeros(T, k)
+    out = torch.zeros(T, D, dtype=torch.bfloat16)
+    ws = torch.zeros(1 << 20, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="w2"):
+        moe.moe_ffn_forward(x, w1, w2, ids, tw, out, E=E, D=D, H=H, k=k, workspace=ws)
+    with pytest.raises(ValueError, match="slot_of_pair"):
+        moe.moe_ffn_route(ids, tw, T, E, k, torch.zeros(E, dtype=torch.int32), torch.zeros(E + 1, dtype=torch.int32),
+                          torch.zeros(T * k - 1, dtype=torch.int32), ws)
+    with pytest.raises(ValueError, match="logits"):
+        moe.moe_ffn_router_topk(torch.zeros(T, E - 1), k, ids, tw, E=E)
+
+
+def test_binding_leaves_out_of_range_shared_counts_to_the_c_abi():
+    import torch
+    T, E, D, H, k = 4, 4, 256, 128, 2
+    t = lambda *s, dt=torch.bfloat16: torch.zeros(*s, dtype=dt)
+    args = (t(T, D), t(E, 2 * H, D), t(E, D, H), t(T, k, dt=torch.int32), t(T, k, dt=torch.float32), t(T, D))
+    # the size check must not turn an invalid count into a size error (the host
+    # tensors then fail the device check, after the size check passed)
+    for ns in (-1, 1021):
+        with pytest.raises(ValueError, match="CUDA"):
+            moe.moe_ffn_forward_ex(*args, E=E, D=D, H=H, k=k, workspace=t(1 << 20, dt=torch.uint8), n_shared=ns)
