@@ -170,3 +170,24 @@ def test_bad_arguments_rejected():
         raise AssertionError("a zero act global scale was accepted")
     except ValueError:
         pass
+
+
+def test_clamp_and_bf16_act_on_decoded_operands():
+    """The clamped SwiGLU and the bf16-rounded act of the NVFP4 mode against a
+    dense computation on operands decoded here (one expert, top-1)."""
+    T, D, H = 6, 64, 64
+    inp = wl.make_custom(T=T, D=D, H=H, E=1, k=1, seed=56, routing="uniform", dtype="nvfp4")
+    inp["topk_w"] = np.ones((T, 1), np.float32)
+    x = decode_nv4(inp["x"], inp["x_sf"], inp["x_gs"])
+    w1 = decode_nv4(inp["w1"][0], inp["w1_sf"][0], inp["w1_gs"][0])
+    w2 = decode_nv4(inp["w2"][0], inp["w2_sf"][0], inp["w2_gs"][0])
+    g, u = x @ w1[:H].T, x @ w1[H:].T
+    lim = float(np.quantile(np.abs(np.concatenate([g.ravel(), u.ravel()])), 0.5))
+    gc, uc = np.minimum(g, lim), np.clip(u, -lim, lim)
+    ref = (gc / (1.0 + np.exp(-gc)) * uc) @ w2.T
+    got = run(inp, act=oracle.ACT_EXACT, swiglu_limit=lim)
+    assert rel_err(got, ref) < 1e-12
+    assert rel_err(run(inp, act=oracle.ACT_EXACT), ref) > 1e-3          # the clamp was active
+    a = (g / (1.0 + np.exp(-g)) * u).astype(np.float32)
+    a_bf16 = torch.from_numpy(a).to(torch.bfloat16).double().numpy()
+    assert rel_err(run(inp, act=oracle.ACT_BF16), a_bf16 @ w2.T) < 1e-12
