@@ -5,7 +5,7 @@ import torch
 
 import grouped_gemm_gb300 as moe
 
-# spec tolerances: max|gpu - ref| <= TOL_MAX * max|ref| and
+# parity tolerances of the path: max|gpu - ref| <= TOL_MAX * max|ref| and
 # sum|gpu - ref| / sum|ref| <= TOL_MEAN (ratio of L1 norms)
 TOL = {"bf16": (2e-2, 5e-3), "mxfp8": (4e-2, 1e-2)}
 

@@ -1,7 +1,7 @@
 """The library driven from a plain C program through include/moe_ffn.h alone
 (no Python binding, no PyTorch on the call path): the program is compiled and
 linked against libmoe_ffn.so on the CPU (not gpu-marked), and on a GPU its
-output is compared with the oracle at the spec bf16 tolerances."""
+output is compared with the oracle at the bf16 parity tolerances."""
 import os
 import shutil
 import subprocess

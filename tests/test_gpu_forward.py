@@ -1,6 +1,6 @@
 """End-to-end parity of the CUDA forward pass against the fp64 CPU oracle.
 
-Tolerances (the benchmark spec): max|gpu - oracle| <= 2e-2 * max|oracle| and
+Tolerances: max|gpu - oracle| <= 2e-2 * max|oracle| and
 sum|gpu - oracle| / sum|oracle| <= 5e-3 for bf16.  The oracle rounds act to
 bf16 as the method does ("Prime Flash MoE" sec. 5, "SwiGLU - which never
 leaves the SM").  Small cases are compared element by element over every
@@ -79,7 +79,7 @@ def test_forward_small(T, D, H, E, k, routing, pipeline):
     inp = wl.make_custom(T, D, H, E, k, seed=T + D, routing=routing)
     out, _ = run_mode(inp, to_dev(inp), pipeline)
     # out collects its k rows with bf16 reductions, each rounding the running
-    # sum; the benchmark spec's bound (5e-3 mean) is set for k <= 8, and the rounding
+    # sum; the parity bound (5e-3 mean) is set for k <= 8, and the rounding
     # errors of more adds grow like a random walk, so larger k get
     # 5e-3 * sqrt(k / 8) (the max bound is unchanged)
     tol = (2e-2, 5e-3 * max(1.0, math.sqrt(k / 8)))

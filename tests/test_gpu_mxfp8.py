@@ -1,7 +1,7 @@
 """MXFP8 path ("Prime Flash MoE" sec. 7): the device requantizer against the
 oracle's codec (bit-exact: both decide in fp32), the weight-scale repacking
 against its documented tile layout, and the forward pass against the fp64
-oracle (act requantized per 32 along H on both sides) at the north-star
+oracle (act requantized per 32 along H on both sides) at the parity
 MXFP8 tolerances (max 4e-2, mean 1e-2)."""
 import numpy as np
 import pytest

@@ -6,7 +6,7 @@ both sides, so they must match bit for bit.  Weights: the kernel computes the
 softmax of the selected logits in fp32 (expf within 2 ulp, a sum of at most
 1024 terms in at most 42 roundings, one division), so each weight is within
 about 3e-6 relative of the fp64 oracle; the test allows 1e-5 relative.
-Forward outputs use the spec bf16 tolerances against the oracle's
+Forward outputs use the bf16 parity tolerances against the oracle's
 forward pass on the oracle's own ids and weights."""
 import numpy as np
 import pytest

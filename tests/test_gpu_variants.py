@@ -4,7 +4,7 @@ Rubin" sec. 5.3: gate clamped from above, up on both sides), shared experts
 run on every token ("GC-MoE on SM120" sec. 4.7), and both together with the
 router.  Every kernel family's SwiGLU epilogue is covered: single-CTA and
 CTA-pair split GEMMs, the fused pipeline on clusters and with split-K, and
-both MXFP8 pipelines.  Spec tolerances (bf16 2e-2 / 5e-3, MXFP8 4e-2 /
+both MXFP8 pipelines.  Parity tolerances (bf16 2e-2 / 5e-3, MXFP8 4e-2 /
 1e-2); the oracle gets the same extended ids and weights, built here with
 numpy (routed ids, then E .. E + n_shared - 1 at weight 1)."""
 import numpy as np

@@ -1,7 +1,7 @@
 """Pins for the CPU oracle: each test checks it against something other than
 itself -- a library routine, a closed form, brute force or an invariant of the
 method ("Prime Flash MoE - Faster MoE Kernels optimized for Blackwell", sec. 1
-"The computation"; spec invariants: top-1 with weight 1 is the dense
+"The computation"; invariants of the method: top-1 with weight 1 is the dense
 SwiGLU FFN of that expert, identical experts scale by the weight sum, token
 order does not matter).  CPU only."""
 import math
