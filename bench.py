@@ -426,6 +426,22 @@ def oracle_call(inp, tokens):
                           x_sf=inp.get("x_sf"), w1_sf=inp.get("w1_sf"), w2_sf=inp.get("w2_sf"))
 
 
+def host_cpu():
+    """The host's CPU model (lscpu), its logical CPU count and the oracle's
+    OpenMP threads, for the CPU baseline's record."""
+    import oracle
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return {"model": model or os.uname().machine, "nproc": os.cpu_count(), "omp_threads": oracle.max_threads()}
+
+
 def cpu_baseline(inp, w, budget_s=12.0):
     """The oracle, as it stands, on the host cores over a bounded token sample."""
     import numpy as np
@@ -445,7 +461,7 @@ def cpu_baseline(inp, w, budget_s=12.0):
     dt = time.time() - t0
     return {"value": round(per_tok * n / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": f"{n} of {w.T} tokens of the {w.name} workload (all k={w.k} experts each), {dt:.1f} s",
-            "tokens_per_s": round(n / dt, 3)}
+            "tokens_per_s": round(n / dt, 3), "host": host_cpu()}
 
 
 # ---------------------------------------------------------------- reference arm
@@ -486,7 +502,8 @@ def run_reference(args, rank):
         "config": {"workload": w.name, "T": w.T, "D": w.D, "H": w.H, "E": w.E, "k": w.k, "routing": w.routing,
                    "pipeline": args.pipeline, "seed": 0, "parallelism": "host cores"},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{n} tokens of the {w.name} workload per step (all k={w.k} experts each)"},
+                         "sample": f"{n} tokens of the {w.name} workload per step (all k={w.k} experts each)",
+                         "host": host_cpu()},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     return line

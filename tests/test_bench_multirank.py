@@ -93,3 +93,8 @@ def test_gemm_only_figure():
     g = bench.gemm_only({"route": 0.02, "gather_zero": 0.03, "fused_gemm": 0.4, "to_bf16": 0.0}, "fused", 4e11)
     assert g["ms"] == pytest.approx(0.4) and g["stages"] == ["fused_gemm", "to_bf16"]
     assert bench.gemm_only({"route": 0.02}, "split", 1e9) is None
+
+
+def test_host_cpu_record():
+    h = bench.host_cpu()
+    assert h["model"] and h["nproc"] >= 1 and h["omp_threads"] >= 1
