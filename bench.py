@@ -1,13 +1,17 @@
 #!/usr/bin/env python
 """Benchmark of the routed MoE SwiGLU FFN forward pass on GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload decode]
-                    [--pipeline split] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload large_skewed]
+                    [--pipeline split] [--impl ours|reference] [--no-also]
 
 One step = one full forward pass (routing, gather + zero-fill, up-projection
 with SwiGLU, down-projection with the weighted reduction) over one batch of
-seeded synthetic inputs already resident in HBM.  Prints ONE JSON line on
-rank 0.  Under torchrun each rank runs its own token batch against its own
+seeded synthetic inputs already resident in HBM.  The default workload is the
+largest one (T=131072 tokens, D=2048, H=768, E=128, top-8, Zipf-skewed
+routing) on the split pipeline.  Prints ONE JSON line on rank 0; at N=1 it
+also carries, under "other_configs", the same measurement (timed steps,
+per-stage kernel fractions, clocks) of the other workloads and pipelines,
+taken in the same run after the main one.  Under torchrun each rank runs its own token batch against its own
 copy of the weights (the path shards by tokens, no collective on the data
 path): weak scaling, value = all ranks' FLOPs / max-over-ranks time.
 
@@ -32,6 +36,11 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE FFN fwd TFLOP/s & tokens/s on 1×GB300; % of roofline (tensor or HBM)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# GB300 data-sheet figures (dense, no sparsity), reported beside the measured-peak fractions
+NOMINAL_PEAKS = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0, "fp8_tflops": 4500.0}
+# measured after the main workload in the same run (N=1): workload, pipeline
+ALSO = [("large_skewed", "split"), ("large_skewed", "fused"), ("prefill", "split"), ("prefill", "fused"),
+        ("mxfp8", "split"), ("mxfp8", "fused"), ("decode", "split"), ("decode", "fused")]
 STAGES = {"split": ["route", "gather_zero", "up_swiglu", "down_reduce"],
           "fused": ["route", "gather_zero", "fused_gemm", "to_bf16"]}
 
@@ -42,7 +51,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="decode")
+    ap.add_argument("--workload", default="large_skewed")
     ap.add_argument("--pipeline", choices=["split", "fused"], default="split")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -50,6 +59,8 @@ def parse_args():
                     help="start each step from router logits [T, E] (moe_ffn_forward_logits: top-k and softmax "
                          "fused into the routing launch) instead of given top-k ids and weights")
     ap.add_argument("--no-graph", action="store_true", help="launch each step eagerly instead of replaying a CUDA graph")
+    ap.add_argument("--no-also", action="store_true",
+                    help="skip the other workloads and pipelines measured after the main one (N=1 only)")
     ap.add_argument("--option", action="append", default=[], metavar="NAME=VALUE",
                     help="library tuning option, e.g. PAIR_MMA=0 (moe_ffn_set_option; repeatable)")
     return ap.parse_args()
@@ -142,34 +153,87 @@ def traffic_from_profiles(kernel, workload):
 
 
 class ClockSampler:
+    """SM clock and clock-event reasons sampled every few milliseconds by a
+    background thread through NVML (libnvidia-ml, read-only queries), so that
+    even a timed region of a fraction of a second holds samples; nvidia-smi
+    at 100 ms when NVML cannot be loaded."""
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    # NVML clock-event reason bits of those four
+    BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40}
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
-    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, gpu_index):
-        self.samples = []
+    def __init__(self, device_index, period_s=0.005):
+        self.samples = []        # (time, sm_mhz, sm_max_mhz, [reason names])
         self.proc = None
+        self._stop = threading.Event()
+        self.source = None
+        if self._start_nvml(device_index, period_s):
+            self.source = f"nvml every {period_s * 1e3:.0f} ms"
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
-                 "-i", str(gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-i", str(device_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             return
-        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.source = "nvidia-smi every 100 ms"
+        self.thread = threading.Thread(target=self._read_smi, daemon=True)
         self.thread.start()
 
-    def _read(self):
+    def _start_nvml(self, device_index, period_s):
+        import ctypes
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return False
+            handle = ctypes.c_void_p()
+            uuid = None
+            try:
+                import torch
+                u = getattr(torch.cuda.get_device_properties(device_index), "uuid", None)
+                uuid = f"GPU-{u}" if u is not None else None
+            except Exception:
+                uuid = None
+            if not uuid or nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(handle)) != 0:
+                if nv.nvmlDeviceGetHandleByIndex_v2(int(device_index), ctypes.byref(handle)) != 0:
+                    return False
+            clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+            reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            if nv.nvmlDeviceGetClockInfo(handle, 1, ctypes.byref(clk)) != 0:   # NVML_CLOCK_SM
+                return False
+        except (OSError, AttributeError):
+            return False
+
+        def loop():
+            while not self._stop.is_set():
+                ok = nv.nvmlDeviceGetClockInfo(handle, 1, ctypes.byref(clk)) == 0
+                ok = ok and nv.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) == 0
+                ok = ok and reasons_fn(handle, ctypes.byref(rs)) == 0
+                if ok:
+                    names = [n for n, b in self.BITS.items() if rs.value & b]
+                    self.samples.append((time.time(), float(clk.value), float(mx.value), names))
+                time.sleep(period_s)
+
+        self.thread = threading.Thread(target=loop, daemon=True)
+        self.thread.start()
+        return True
+
+    def _read_smi(self):
         for line in self.proc.stdout:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                self.samples.append((time.time(), float(parts[1]), float(parts[2]), parts[5:9]))
+                names = [self.NAMES[i] for i, v in enumerate(parts[5:9]) if v.lower() == "active"]
+                self.samples.append((time.time(), float(parts[1]), float(parts[2]), names))
             except ValueError:
                 pass
 
     def stop(self):
+        self._stop.set()
         if self.proc:
             self.proc.terminate()
             try:
@@ -178,13 +242,13 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self, t0, t1):
-        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        inside = [s for s in list(self.samples) if t0 <= s[0] <= t1]
         if not inside:
             return None
         sm = [s[1] for s in inside]
-        reasons = sorted({self.NAMES[i] for s in inside for i, v in enumerate(s[3]) if v.lower() == "active"})
+        reasons = sorted({n for s in inside for n in s[3]})
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(s[2] for s in inside), "reasons": reasons,
-                "samples": len(inside)}
+                "samples": len(inside), "source": self.source}
 
 
 def max_over_ranks(x: float, world: int, device=None) -> float:
@@ -203,18 +267,53 @@ def weak_scaling_tflops(flops_per_rank: float, ms_max: float, world: int) -> flo
 
 
 # ---------------------------------------------------------------- our arm
-def run_ours(args, rank, world, local_rank):
+def roofline_fracs(alg, stage_ms, pipeline, mx, peaks, peak_src, stage_kernels, workload):
+    """The dominant kernel's achieved rate against its roofline (measured
+    peak, and the data-sheet peak beside it), and the step's bound."""
+    if mx:  # e4m3 contraction: the measured bf16 peak times the nominal fp8/bf16 ratio (4.5 / 2.25)
+        peaks = dict(peaks)
+        peaks["bf16_tflops"] = peaks["bf16_tflops"] * 2.0
+        peak_src += " bf16 x nominal fp8/bf16 ratio 2"
+    nominal_tf = NOMINAL_PEAKS["fp8_tflops"] if mx else NOMINAL_PEAKS["bf16_tflops"]
+    if pipeline == "split":
+        dom = max(("up_swiglu", "down_reduce"), key=lambda s: stage_ms.get(s, 0.0))
+        kd = alg[dom]
+    else:
+        dom = "fused_gemm"
+        kd = {"flops": alg["up_swiglu"]["flops"] + alg["down_reduce"]["flops"], "bytes": alg["step_bytes"]}
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    tensor_bound = kd["flops"] / kd["bytes"] > ridge
+    t_dom = stage_ms[dom] * 1e-3
+    if tensor_bound:
+        achieved, peak, nominal, unit = kd["flops"] / t_dom / 1e12, peaks["bf16_tflops"], nominal_tf, "TFLOP/s"
+    else:
+        achieved, peak, nominal, unit = kd["bytes"] / t_dom / 1e9, peaks["hbm_gbs"], NOMINAL_PEAKS["hbm_gbs"], "GB/s"
+    kname = stage_kernels[dom]
+    roofline = {"bound": "tensor" if tensor_bound else "hbm", "kernel": kname, "achieved": round(achieved, 1),
+                "peak": peak, "peak_source": peak_src, "unit": unit, "frac": round(achieved / peak, 4),
+                "peak_nominal": nominal, "frac_nominal": round(achieved / nominal, 4),
+                "traffic": traffic_from_profiles(kname, workload),
+                "algorithmic_per_launch": kd["flops"] if tensor_bound else kd["bytes"],
+                "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()}, "stage_kernels": stage_kernels}
+    step_bound = max(alg["step_flops"] / (peaks["bf16_tflops"] * 1e12), alg["step_bytes"] / (peaks["hbm_gbs"] * 1e9))
+    step_bound_nominal = max(alg["step_flops"] / (nominal_tf * 1e12),
+                             alg["step_bytes"] / (NOMINAL_PEAKS["hbm_gbs"] * 1e9))
+    return roofline, step_bound, step_bound_nominal
+
+
+def bench_workload(args, name, pipeline_name, rank, world, sampler, full=True):
+    """Time one workload and pipeline (CUDA-graph replay of one step, inputs
+    resident in HBM).  full: also the median of single replays, the clocks of
+    a sustained run, the end-to-end pass from host buffers and the CPU
+    baseline (the main line); otherwise the timed steps and the per-stage
+    kernel fractions only (the other configurations of the same run)."""
     import numpy as np
     import torch
 
     import grouped_gemm_gb300 as moe
     from grouped_gemm_gb300 import workloads as wl
 
-    torch.cuda.set_device(local_rank)
-    for opt in args.option:
-        name, val = opt.split("=")
-        moe.moe_ffn_set_option(getattr(moe, "MOE_OPT_" + name.upper()), int(val))
-    inp = wl.make_inputs(args.workload, seed=rank)
+    inp = wl.make_inputs(name, seed=rank)
     w = inp["workload"]
     mx = w.dtype == "mxfp8"
     dtype = moe.MOE_MXFP8 if mx else moe.MOE_BF16
@@ -232,7 +331,7 @@ def run_ours(args, rank, world, local_rank):
         logits_np = wl.router_logits(w.T, w.E, seed=1000 + rank)
         logits = torch.from_numpy(logits_np).cuda()
     out = torch.empty(w.T, w.D, dtype=torch.bfloat16, device="cuda")
-    pipeline = moe.MOE_SPLIT if args.pipeline == "split" else moe.MOE_FUSED
+    pipeline = moe.MOE_SPLIT if pipeline_name == "split" else moe.MOE_FUSED
     ws = moe.alloc_workspace(w.T, w.E, w.D, w.H, w.k, dtype, pipeline)
     stream = torch.cuda.current_stream()
 
@@ -273,8 +372,7 @@ def run_ours(args, rank, world, local_rank):
     if logits is not None:  # the experts the router picked set the algorithmic bytes
         inp["topk_ids"] = ids.cpu().numpy()
 
-    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
-    time.sleep(0.3)
+    time.sleep(0.05)
     barrier()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -289,27 +387,28 @@ def run_ours(args, rank, world, local_rank):
     barrier()
     ms_total = max_over_ranks(ev0.elapsed_time(ev1), world, device="cuda")
     ms = ms_total / args.steps
-    # keep the same step running so the clock sampler sees load for >= 1.5 s
-    t_sus0 = time.time()
-    while time.time() - t_sus0 < 1.5:
-        for _ in range(20):
+    t_sus0 = t_sus1 = None
+    ms_median = None
+    if full:
+        # keep the same step running for 1.5 s: clocks under sustained load
+        t_sus0 = time.time()
+        while time.time() - t_sus0 < 1.5:
+            for _ in range(20):
+                timed_step()
+            torch.cuda.synchronize()
+        t_sus1 = time.time()
+        # the pages' statistic beside the contract's mean: the median of single
+        # replays, each between its own pair of events (a separate pass)
+        n_med = max(1, min(args.steps, 50))
+        med_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_med)]
+        for i in range(n_med):
+            med_ev[2 * i].record(stream)
             timed_step()
+            med_ev[2 * i + 1].record(stream)
         torch.cuda.synchronize()
-    t_sus1 = time.time()
-    # the pages' statistic beside the contract's mean: the median of single
-    # replays, each between its own pair of events (a separate pass)
-    n_med = max(1, min(args.steps, 50))
-    med_ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_med)]
-    for i in range(n_med):
-        med_ev[2 * i].record(stream)
-        timed_step()
-        med_ev[2 * i + 1].record(stream)
-    torch.cuda.synchronize()
-    ms_median = max_over_ranks(statistics.median(med_ev[2 * i].elapsed_time(med_ev[2 * i + 1]) for i in range(n_med)),
-                               world, device="cuda")
-    if sampler:
-        time.sleep(0.2)
-        sampler.stop()
+        ms_median = max_over_ranks(
+            statistics.median(med_ev[2 * i].elapsed_time(med_ev[2 * i + 1]) for i in range(n_med)), world,
+            device="cuda")
     st = moe.moe_ffn_sync_status(ws)
     if st != 0:
         raise SystemExit(f"device status after timing: {moe.moe_ffn_status_string(st)}")
@@ -325,39 +424,41 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(min(args.steps, 30)):
         step()
         per.append(moe.moe_ffn_profile_read())
-    names = STAGES[args.pipeline]
-    stage_kernels = {name: moe.moe_ffn_profile_stage_kernel(i) for i, name in enumerate(names)}
+    names = STAGES[pipeline_name]
+    stage_kernels = {nm: moe.moe_ffn_profile_stage_kernel(i) for i, nm in enumerate(names)}
     moe.moe_ffn_profile_enable(False)
-    stage_ms = {name: statistics.median(p[i] for p in per) for i, name in enumerate(names) if len(per[0]) > i}
+    stage_ms = {nm: statistics.median(p[i] for p in per) for i, nm in enumerate(names) if len(per[0]) > i}
     # our kernels per step, from the kernels each stage launched ("a+b" = two)
     launches_per_step = sum(len(n.split("+")) for n in stage_kernels.values() if n and n != "none")
 
     peaks, peak_src = load_peaks()
-    if mx:  # e4m3 contraction: the measured bf16 peak times the nominal fp8/bf16 ratio (4.5 / 2.25)
-        peaks = dict(peaks)
-        peaks["bf16_tflops"] = peaks["bf16_tflops"] * 2.0
-        peak_src += " bf16 x nominal fp8/bf16 ratio 2"
-    if args.pipeline == "split":
-        dom = max(("up_swiglu", "down_reduce"), key=lambda s: stage_ms.get(s, 0.0))
-        kd = alg[dom]
-    else:
-        dom = "fused_gemm"
-        kd = {"flops": alg["up_swiglu"]["flops"] + alg["down_reduce"]["flops"],
-              "bytes": alg["step_bytes"]}
-    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    tensor_bound = kd["flops"] / kd["bytes"] > ridge
-    t_dom = stage_ms[dom] * 1e-3
-    if tensor_bound:
-        achieved, peak, unit = kd["flops"] / t_dom / 1e12, peaks["bf16_tflops"], "TFLOP/s"
-    else:
-        achieved, peak, unit = kd["bytes"] / t_dom / 1e9, peaks["hbm_gbs"], "GB/s"
-    kname = stage_kernels[dom]
-    roofline = {"bound": "tensor" if tensor_bound else "hbm", "kernel": kname, "achieved": round(achieved, 1),
-                "peak": peak, "peak_source": peak_src, "unit": unit, "frac": round(achieved / peak, 4),
-                "traffic": traffic_from_profiles(kname, args.workload),
-                "algorithmic_per_launch": kd["flops"] if tensor_bound else kd["bytes"],
-                "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()}, "stage_kernels": stage_kernels}
-    step_bound = max(alg["step_flops"] / (peaks["bf16_tflops"] * 1e12), alg["step_bytes"] / (peaks["hbm_gbs"] * 1e9))
+    roofline, step_bound, step_bound_nominal = roofline_fracs(alg, stage_ms, pipeline_name, mx, peaks, peak_src,
+                                                              stage_kernels, name)
+    clocks = sampler.summary(t_host0, t_host1) if sampler else None
+    config = {"workload": w.name, "T": w.T, "D": w.D, "H": w.H, "E": w.E, "k": w.k, "routing": w.routing,
+              "pipeline": pipeline_name, "seed": "rank", "parallelism": f"token-sharded x{world}",
+              "options": args.option,
+              "routing_input": "router logits [T, E] fp32" if args.from_logits else "top-k ids and weights",
+              "launch": "eager" if graph is None else "CUDA graph replay of one step",
+              "l2": (f"inputs larger than L2: {alg['step_bytes'] / 1e9:.2f} GB compulsory per step "
+                     f"(129 MB L2), no flush needed")}
+    line = {
+        "value": round(value, 3), "unit": "TFLOP/s", "ms_per_step": round(ms, 5),
+        "dtype": "e4m3 (MXFP8)" if mx else "bf16", "tokens_per_s": round(tokens_per_s, 1),
+        "roofline_step_frac": round(step_bound / (ms * 1e-3), 4),
+        "roofline_step_frac_nominal": round(step_bound_nominal / (ms * 1e-3), 4),
+        "config": config, "roofline": roofline,
+        "gemm_only": gemm_only(stage_ms, pipeline_name, alg["step_flops"]),
+        "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+    }
+    if not full:
+        return line
+    line["ms_per_step_median"] = round(ms_median, 5)
+    if sampler:
+        sus = sampler.summary(t_sus0, t_sus1)
+        if sus is not None:
+            sus["window"] = "the same step run for 1.5 s right after the timed region"
+        line["clocks_sustained"] = sus
 
     # end to end: host buffers, copies inside the timed region
     e2e = None
@@ -398,36 +499,51 @@ def run_ours(args, rank, world, local_rank):
                                          (lgh.numel() * 4 if logits is not None else idh.numel() * 4 + twh.numel() * 4)),
                "d2h_bytes_per_step": int(outh.numel() * 2), "ms_per_step": round(e_ms, 4),
                "resident": "expert weights stay in HBM (model parameters)"}
-
-    cpu = None
+    line["e2e"] = e2e
+    line["cpu_baseline"] = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(inp, w, budget_s=12.0)
+        line["cpu_baseline"] = cpu_baseline(inp, w, budget_s=12.0)
+    return line
 
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import grouped_gemm_gb300 as moe
+
+    torch.cuda.set_device(local_rank)
+    for opt in args.option:
+        nm, val = opt.split("=")
+        moe.moe_ffn_set_option(getattr(moe, "MOE_OPT_" + nm.upper()), int(val))
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    try:
+        main = bench_workload(args, args.workload, args.pipeline, rank, world, sampler, full=True)
+        torch.cuda.empty_cache()
+        others = []
+        if world == 1 and not args.no_also and not args.from_logits and not args.option:
+            for name, pipe in ALSO:
+                if (name, pipe) == (args.workload, args.pipeline):
+                    continue
+                try:
+                    others.append(bench_workload(args, name, pipe, rank, world, sampler, full=False))
+                except (RuntimeError, SystemExit, ValueError) as exc:   # one failing config does not lose the line
+                    others.append({"config": {"workload": name, "pipeline": pipe}, "error": str(exc)[:300]})
+                torch.cuda.empty_cache()
+    finally:
+        if sampler:
+            sampler.stop()
     if rank != 0:
         return None
-    clocks = sampler.summary(t_host0, t_host1) if sampler else None
-    if clocks is None and sampler:
-        clocks = sampler.summary(t_sus0, t_sus1)
-        if clocks is not None:
-            clocks["window"] = "the same step run for 1.5 s right after the timed region"
-    return {
-        "metric": METRIC, "value": round(value, 3), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms, 5), "ms_per_step_median": round(ms_median, 5),
-        "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3 (MXFP8)" if mx else "bf16", "data": "synthetic",
-        "tokens_per_s": round(tokens_per_s, 1),
-        "roofline_step_frac": round(step_bound / (ms * 1e-3), 4),
-        "config": {"workload": w.name, "T": w.T, "D": w.D, "H": w.H, "E": w.E, "k": w.k, "routing": w.routing,
-                   "pipeline": args.pipeline, "seed": "rank", "parallelism": f"token-sharded x{world}",
-                   "options": args.option,
-                   "routing_input": "router logits [T, E] fp32" if args.from_logits else "top-k ids and weights",
-                   "launch": "eager" if graph is None else "CUDA graph replay of one step",
-                   "l2": (f"inputs larger than L2: {alg['step_bytes'] / 1e9:.2f} GB compulsory per step "
-                          f"(129 MB L2), no flush needed")},
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gemm_only": gemm_only(stage_ms, args.pipeline, alg["step_flops"]),
-        "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
-    }
+    line = {"metric": METRIC, "value": main["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": main["ms_per_step"], "ms_per_step_median": main["ms_per_step_median"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": main["dtype"],
+            "data": "synthetic"}
+    for key in ("tokens_per_s", "roofline_step_frac", "roofline_step_frac_nominal", "config", "roofline",
+                "cpu_baseline", "e2e", "gemm_only", "gpu_launches", "clocks", "clocks_sustained"):
+        line[key] = main.get(key)
+    if others:
+        line["other_configs"] = others
+    return line
 
 
 def oracle_call(inp, tokens):

@@ -73,6 +73,10 @@ def lib() -> ctypes.CDLL:
             L.moe_ffn_route.restype = i
             L.moe_ffn_route_noalloc.argtypes = [vp, vp, i, i, i, vp, vp, vp, vp, vp]
             L.moe_ffn_route_noalloc.restype = i
+            L.moe_ffn_route_padded_slots.argtypes = [i, i, i]
+            L.moe_ffn_route_padded_slots.restype = c.c_int64
+            L.moe_ffn_route_padded.argtypes = [vp, vp, i, i, i, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+            L.moe_ffn_route_padded.restype = i
             L.moe_ffn_prepare_mxfp8_weights.argtypes = [vp, vp, vp, vp, i, i, i, vp]
             L.moe_ffn_prepare_mxfp8_weights.restype = i
             L.moe_ffn_widen_mxfp4_weights.argtypes = [vp, c.c_int64, vp, vp]
@@ -249,6 +253,31 @@ def moe_ffn_route(topk_ids, topk_w, T, E, k, counts, offsets, slot_of_pair, work
     st = lib().moe_ffn_route(_p(topk_ids), _p(topk_w), T, E, k, _p(counts), _p(offsets), _p(slot_of_pair),
                              _p(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
     return _check(st, "moe_ffn_route") if check else st
+
+
+def moe_ffn_route_padded_slots(T, E, k) -> int:
+    """Capacity S_max of the padded routing tables (0 for an invalid shape)."""
+    return int(lib().moe_ffn_route_padded_slots(T, E, k))
+
+
+def moe_ffn_route_padded(topk_ids, topk_w, T, E, k, pad_offsets, expert_of_rb, pair_info, row_tok, slot_w, n_blocks,
+                         workspace, stream=None, check=True) -> int:
+    """The padded routing tables the grouped GEMMs consume (pad_offsets [E+1],
+    expert_of_rb and pair_info [S_max/128], row_tok and slot_w [S_max],
+    n_blocks [2] = row blocks and pairs), S_max = moe_ffn_route_padded_slots."""
+    smax = moe_ffn_route_padded_slots(T, E, k)
+    _need(topk_ids, T * k * 4, "topk_ids")
+    _need(topk_w, T * k * 4, "topk_w")
+    _need(pad_offsets, (E + 1) * 4, "pad_offsets")
+    _need(expert_of_rb, smax // 128 * 4, "expert_of_rb")
+    _need(pair_info, smax // 128 * 4, "pair_info")
+    _need(row_tok, smax * 4, "row_tok")
+    _need(slot_w, smax * 4, "slot_w")
+    _need(n_blocks, 8, "n_blocks")
+    st = lib().moe_ffn_route_padded(_p(topk_ids), _p(topk_w), T, E, k, _p(pad_offsets), _p(expert_of_rb),
+                                    _p(pair_info), _p(row_tok), _p(slot_w), _p(n_blocks), _p(workspace),
+                                    workspace.numel() * workspace.element_size(), _stream(stream))
+    return _check(st, "moe_ffn_route_padded") if check else st
 
 
 def moe_ffn_route_noalloc(topk_ids, topk_w, T, E, k, counts, offsets, slot_of_pair, status_bits=None, stream=None,

@@ -177,6 +177,7 @@ Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipe
     if (pipeline == MOE_SPLIT) {
       w.act = take((size_t)w.S_max * H);
       w.act_sf = take((size_t)w.S_max * H / 32);
+      if (f32_accum(k)) w.acc_f32 = take((size_t)T * D * 4);
     } else {
       w.acc_f32 = take((size_t)T * D * 4);
       int cmin = 0;  // ring capacity for the smallest cluster size that applies
@@ -191,6 +192,7 @@ Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipe
   } else if (pipeline == MOE_SPLIT) {
     w.xg = take((size_t)w.S_max * D * 2);
     w.act = take((size_t)w.S_max * H * 2);
+    if (f32_accum(k)) w.acc_f32 = take((size_t)T * D * 4);
   } else {
     w.xg = take((size_t)w.S_max * D * 2);
     w.acc_f32 = take((size_t)T * D * 4);
@@ -291,7 +293,9 @@ moe_status_t forward_fused_bf16(const Workspace& ws, const void* x, const void* 
                                 const int32_t* topk_ids, const float* topk_w, void* out, int T, int E, int D, int H,
                                 int k, int sms, cudaStream_t st) {
   const int opt = g_fused_cluster.load();
-  if (opt && fused_cluster_ok(D, H)) {
+  // the cluster kernel reduces finished rows into out in bf16; for large k
+  // the split-K kernel's fp32 accumulator is taken instead
+  if (opt && fused_cluster_ok(D, H) && !f32_accum(k)) {
     int C = (opt > 1 && fused_cluster_h1(D, H, opt)) ? opt : 0;
     if (!C) C = choose_cluster_size(D, H, (int64_t)T * k, E, ws.max_rb);
     if (C) return forward_fused_cluster_bf16(ws, x, w1, w2, topk_ids, topk_w, out, T, E, D, H, k, sms, C, st);
@@ -350,7 +354,12 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
   cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st, nullptr, 0, 0, !g_prof.on);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 1);
-  e = launch_gather_mx(ws, x, x_sf, topk_ids, T, E, k, D, out, (int64_t)T * D * 2, sms * g_gather_blocks.load(), st, !g_prof.on);
+  // large k: the rows of a token are summed in the fp32 accumulator
+  float* acc = f32_accum(k) ? static_cast<float*>(ws.acc_f32) : nullptr;
+  e = acc ? launch_gather_mx(ws, x, x_sf, topk_ids, T, E, k, D, acc, (int64_t)T * D * 4, sms * g_gather_blocks.load(),
+                             st, !g_prof.on)
+          : launch_gather_mx(ws, x, x_sf, topk_ids, T, E, k, D, out, (int64_t)T * D * 2, sms * g_gather_blocks.load(),
+                             st, !g_prof.on);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 2);
   MxArgs ma{};
@@ -361,6 +370,7 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
   ma.act = ws.act;
   ma.act_sf = ws.act_sf;
   ma.out = out;
+  ma.out_f32 = acc;
   ma.err = ws.err;
   ma.wait_limit_ns = g_wait_limit_ns.load();
   ma.D = D;
@@ -375,7 +385,7 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
   up.k_blocks = D / 128;
   prof_front(true);
   prof_kernel(2, "up_swiglu_mxfp8");
-  prof_kernel(3, "down_reduce_mxfp8");
+  prof_kernel(3, acc ? "down_reduce_mxfp8+f32_to_bf16" : "down_reduce_mxfp8");
   e = launch_up_mxfp8(map_xg, map_w1, up, (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * up.n_col_tiles), st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 3);
@@ -386,6 +396,7 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
   dn.k_blocks = H / 128;
   e = launch_down_mxfp8(map_act, map_w2, dn, (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * dn.n_col_tiles), st,
                         !g_prof.on);
+  if (e == cudaSuccess && acc) e = launch_f32_to_bf16(acc, out, (int64_t)T * D, sms * 4, st);
   prof_mark(st, 4);
   return cuda_status(e);
 }
@@ -472,7 +483,7 @@ moe_status_t forward_fused_mxfp8(const Workspace& ws, const void* x, const void*
                                  const float* topk_w, void* out, int T, int E, int D, int H, int k, int sms,
                                  cudaStream_t st) {
   const int opt = g_fused_cluster.load();
-  if (opt && ws.ring) {
+  if (opt && ws.ring && !f32_accum(k)) {
     int C = (opt > 1 && fused_cluster_mx_fits(D, H, opt)) ? opt : 0;
     if (!C) C = choose_cluster_size_mx(D, H, (int64_t)T * k, E, ws.max_rb);
     if (C)
@@ -635,6 +646,35 @@ moe_status_t moe_ffn_route(const int32_t* topk_ids, const float* topk_w, int T, 
   return cuda_status(e);
 }
 
+int64_t moe_ffn_route_padded_slots(int T, int E, int k) {
+  if (T < 0 || E < 1 || E > kMaxExperts || k < 1 || (int64_t)T * k >= ((int64_t)1 << 30)) return 0;
+  return plan_workspace(nullptr, T, E, 128, 128, k, kRouteOnly).S_max;
+}
+
+moe_status_t moe_ffn_route_padded(const int32_t* topk_ids, const float* topk_w, int T, int E, int k,
+                                  int32_t* pad_offsets, int32_t* expert_of_rb, int32_t* pair_info, int32_t* row_tok,
+                                  float* slot_w, int32_t* n_blocks, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  if (T < 1 || E < 1 || E > kMaxExperts || k < 1 || (int64_t)T * k >= ((int64_t)1 << 30)) return MOE_ERR_INVALID_ARG;
+  if (!workspace || !topk_ids || !topk_w || !pad_offsets || !expert_of_rb || !pair_info || !row_tok || !slot_w ||
+      !n_blocks)
+    return MOE_ERR_INVALID_ARG;
+  Workspace ws = plan_workspace(workspace, T, E, 128, 128, k, kRouteOnly);
+  if (workspace_bytes < ws.bytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st);
+  auto copy = [&](void* dst, const void* src, size_t bytes) {
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, st);
+  };
+  copy(pad_offsets, ws.pad_offsets, sizeof(int32_t) * (E + 1));
+  copy(expert_of_rb, ws.expert_of_rb, sizeof(int32_t) * ws.max_rb);
+  copy(pair_info, ws.pair_info, sizeof(int32_t) * ws.max_rb);
+  copy(row_tok, ws.row_tok, sizeof(int32_t) * ws.S_max);
+  copy(slot_w, ws.slot_w, sizeof(float) * ws.S_max);
+  copy(n_blocks, ws.meta, sizeof(int32_t) * 2);
+  return cuda_status(e);
+}
+
 // The forward pass from top-k ids and weights, or (router_logits != nullptr)
 // from router logits, the routing launch writing topk_ids / topk_w first.
 static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w1, const void* w1_sf, const void* w2,
@@ -703,15 +743,21 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
     return MOE_ERR_CUDA;
 
   prof_mark(st, 0);
-  // With the in-GEMM gather the routing launch also zero-fills out;
+  // Large k: the rows of a token are summed in the fp32 accumulator, which is
+  // zero-filled instead of out and rounded into out after the down kernel.
+  float* acc = f32_accum(k) ? static_cast<float*>(ws.acc_f32) : nullptr;
+  void* zero_target = acc ? static_cast<void*>(acc) : out;
+  const int64_t zero_bytes = (int64_t)T * D * (acc ? 4 : 2);
+  // With the in-GEMM gather the routing launch also zero-fills the target;
   // otherwise the gather kernel does.
   cudaError_t e = in_gemm_gather
-                      ? launch_route(ws, topk_ids, topk_w, T, E, k, st, out, (int64_t)T * D * 2, sms * 2, !g_prof.on)
+                      ? launch_route(ws, topk_ids, topk_w, T, E, k, st, zero_target, zero_bytes, sms * 2, !g_prof.on)
                       : launch_route(ws, topk_ids, topk_w, T, E, k, st, nullptr, 0, 0, !g_prof.on);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 1);
   if (!in_gemm_gather) {
-    e = launch_gather_zero(ws, x, topk_ids, T, E, k, D, out, (int64_t)T * D * 2, sms * g_gather_blocks.load(), st, !g_prof.on);
+    e = launch_gather_zero(ws, x, topk_ids, T, E, k, D, zero_target, zero_bytes, sms * g_gather_blocks.load(), st,
+                           !g_prof.on);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   prof_mark(st, 2);
@@ -724,6 +770,7 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
   ga.slot_w = ws.slot_w;
   ga.act = ws.act;
   ga.out = out;
+  ga.out_f32 = acc;
   ga.err = ws.err;
   ga.wait_limit_ns = g_wait_limit_ns.load();
   ga.D = D;
@@ -733,8 +780,9 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
   ga.swiglu_limit = ws.swiglu_limit;
   ga.counts = ws.counts;
   ga.pad_offsets = ws.pad_offsets;
-  ga.swap_ab = g_swap_ab.load();
-  ga.pair_swap_max = g_pair_swap.load();
+  // swap-AB tiles reduce bf16 rows only
+  ga.swap_ab = acc ? 0 : g_swap_ab.load();
+  ga.pair_swap_max = acc ? 0 : g_pair_swap.load();
   ga.out_hint = out_hint_for((int64_t)T * D * 2);
   ga.l2_policy = ws.l2_policy;
 
@@ -752,7 +800,8 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
   prof_front(false);
   if (in_gemm_gather) prof_kernel(1, "none");  // rows gathered by the up kernel
   prof_kernel(2, pair_mma ? "up_swiglu_pair2" : (gather == 0 && g_up_pairs.load()) ? "up_pair_bf16" : "up_swiglu_bf16");
-  prof_kernel(3, pair_down ? "down_reduce_pair2" : "down_reduce_bf16");
+  prof_kernel(3, pair_down ? (acc ? "down_reduce_pair2+f32_to_bf16" : "down_reduce_pair2")
+                           : (acc ? "down_reduce_bf16+f32_to_bf16" : "down_reduce_bf16"));
   if (pair_mma)
     e = launch_up_pair2_bf16(map_xg, map_w1, up,
                              (int)std::min<int64_t>(pair_slots, (int64_t)ws.max_rb * up.n_col_tiles), st, !g_prof.on);
@@ -774,6 +823,7 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
                                !g_prof.on);
   else
     e = launch_down_bf16(map_act, map_w2, dn, dn_grid, st, !g_prof.on, down_n);
+  if (e == cudaSuccess && acc) e = launch_f32_to_bf16(acc, out, (int64_t)T * D, sms * 4, st);
   prof_mark(st, 4);
   return cuda_status(e);
 }

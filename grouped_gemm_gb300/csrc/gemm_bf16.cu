@@ -531,6 +531,26 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
           bulk_store(static_cast<__nv_bfloat16*>(args.act) + slot * args.H + j * G, my_stage, G * 2);
           bulk_commit();
         }
+      } else if (args.out_f32) {
+        // fp32 reduction target: four chunks of N/4 columns (N bytes staged each)
+        constexpr int CW = N / 4;
+        const float w = args.slot_w[slot];
+        float* frow = args.out_f32 + (int64_t)(tok < 0 ? 0 : tok) * args.D + j * N;
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+          bulk_wait_read_all();          // the previous reduction has left the staging row
+#pragma unroll 1
+          for (int c = 0; c < CW / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld_x32(tacc + q * CW + c * 32, v);
+            if (tok >= 0) stage_scaled_f32x32(my_stage + c * 128, w, v);
+          }
+          if (tok >= 0) {
+            fence_proxy_async_smem();
+            bulk_reduce_add_f32(frow + q * CW, my_stage, CW * 4);
+            bulk_commit();
+          }
+        }
       } else {
         const float w = args.slot_w[slot];
         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(args.out) + (int64_t)(tok < 0 ? 0 : tok) * args.D + j * N;

@@ -239,6 +239,27 @@ __global__ void __launch_bounds__(kMxThreads, 1)
                            half * 2;
           *reinterpret_cast<uint16_t*>(sfdst) = (uint16_t)sfw;
         }
+      } else if (args.out_f32) {
+        // fp32 reduction target: this thread's 128 columns read at once (the
+        // accumulator is then free), staged and reduced as two 256-byte chunks
+        const float w = args.slot_w[slot];
+        uint32_t v[4][32];
+        tmem_ld_x32_pair(lane_base + half * 128, lane_base + half * 128 + 32, v[0], v[1]);
+        tmem_ld_x32_pair(lane_base + half * 128 + 64, lane_base + half * 128 + 96, v[2], v[3]);
+        tc_fence_before();
+        mbar_arrive(tempty);
+        if (tok >= 0) {
+          float* frow = args.out_f32 + (int64_t)tok * args.D + j * kMxN + half * 128;
+#pragma unroll
+          for (int c = 0; c < 4; c += 2) {
+            bulk_wait_read_all();
+            stage_scaled_f32x32(my_stage, w, v[c]);
+            stage_scaled_f32x32(my_stage + 128, w, v[c + 1]);
+            fence_proxy_async_smem();
+            bulk_reduce_add_f32(frow + c * 32, my_stage, 256);
+            bulk_commit();
+          }
+        }
       } else {
         const float w = args.slot_w[slot];
         bulk_wait_read_all();

@@ -322,6 +322,23 @@ __global__ void __launch_bounds__(kQThreads, 1)
           bulk_store(static_cast<__nv_bfloat16*>(args.act) + slot * args.H + j * 128, my_stage, 256);
           bulk_commit();
         }
+      } else if (args.out_f32) {
+        // fp32 reduction target: four quarter rows of 64 columns (256 bytes staged each)
+        const float w = valid ? args.slot_w[slot] : 0.f;
+        float* frow = args.out_f32 + (int64_t)(tok < 0 ? 0 : tok) * args.D + j * 256;
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+          bulk_wait_read_all();        // the previous reduction has left the staging row
+          uint32_t v0[32], v1[32];
+          tmem_ld_x32_pair(tacc + q * 64, tacc + q * 64 + 32, v0, v1);
+          if (tok >= 0) {
+            stage_scaled_f32x32(my_stage, w, v0);
+            stage_scaled_f32x32(my_stage + 128, w, v1);
+            fence_proxy_async_smem();
+            bulk_reduce_add_f32(frow + q * 64, my_stage, 256);
+            bulk_commit();
+          }
+        }
       } else {
         const float w = valid ? args.slot_w[slot] : 0.f;
         __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(args.out) + (int64_t)(tok < 0 ? 0 : tok) * args.D + j * 256;

@@ -16,6 +16,12 @@ constexpr int kBK = 64;           // K elements per pipeline stage (128 B of bf1
 constexpr int kRowPad = 128;      // per-expert row segments are padded to this
 constexpr int kMaxExperts = 1024;
 constexpr int kRouteTokPerBlock = 256;  // tokens per routing block
+// From this many routed pairs per token on, the rows of a token are summed in
+// fp32 (a [T, D] workspace accumulator, rounded to bf16 once at the end)
+// instead of by bf16 reductions into out: each bf16 reduction rounds the
+// running sum, and the rounding errors of k adds grow with k.
+constexpr int kF32AccumMinK = 9;
+inline bool f32_accum(int k) { return k >= kF32AccumMinK; }
 
 // Device-side view of the caller's workspace.  Every region starts on a
 // 256-byte boundary; sizes depend only on (T, E, D, H, k, pipeline).
@@ -75,6 +81,7 @@ struct GemmArgs {
   const float* slot_w;
   void* act;                // up: bf16 [S_max, H] output
   void* out;                // down: bf16 [T, D] reduction target
+  float* out_f32;           // down: non-null = fp32 [T, D] reduction target instead of out
   int* err;
   unsigned long long wait_limit_ns;
   int D, H;
@@ -241,6 +248,7 @@ struct MxArgs {
   void* act;                // up: e4m3 [S_max, H] output
   void* act_sf;             // up: blocked scale tiles of act
   void* out;                // down: bf16 [T, D] reduction target
+  float* out_f32;           // down: non-null = fp32 [T, D] reduction target instead of out
   const void* sf_a;         // blocked scale tiles of the A operand
   const void* sf_b;         // blocked scale tiles of the weights
   int* err;

@@ -421,6 +421,33 @@ __device__ __forceinline__ void tmem_ld_x32_pair(uint32_t ta, uint32_t tb, uint3
       : "memory");
 }
 
+// One 32-column load of 32-bit accumulator words for the calling warp's 32
+// TMEM lanes, then wait for it.
+__device__ __forceinline__ void tmem_ld_x32(uint32_t ta, uint32_t (&a)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
+        "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]),
+        "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]),
+        "=r"(a[24]), "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31])
+      : "r"(ta)
+      : "memory");
+}
+
+// Stage 32 fp32 values w * acc[i] (acc: raw accumulator words) as 128
+// contiguous bytes of shared memory (eight 16-byte stores).
+__device__ __forceinline__ void stage_scaled_f32x32(uint8_t* sdst, float w, const uint32_t (&acc)[32]) {
+#pragma unroll
+  for (int q = 0; q < 8; ++q)
+    st_shared_v4(sdst + q * 16, __float_as_uint(w * __uint_as_float(acc[4 * q])),
+                 __float_as_uint(w * __uint_as_float(acc[4 * q + 1])),
+                 __float_as_uint(w * __uint_as_float(acc[4 * q + 2])),
+                 __float_as_uint(w * __uint_as_float(acc[4 * q + 3])));
+}
+
 // ----------------------------------------------------------------- reductions
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

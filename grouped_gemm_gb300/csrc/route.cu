@@ -969,7 +969,15 @@ __global__ void __launch_bounds__(256) extend_routing_kernel(const int32_t* __re
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < T * kx; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t t = i / kx;
     const int j = (int)(i % kx);
-    ids_ext[i] = j < k ? ids[t * k + j] : E + (j - k);
+    // a routed id outside [0, E) would name a shared expert (ids E ..
+    // E + n_shared - 1 of the extended problem): -1 keeps it out of range so
+    // the routing reports it as a bad id
+    int id = E + (j - k);
+    if (j < k) {
+      id = ids[t * k + j];
+      if (id < 0 || id >= E) id = -1;
+    }
+    ids_ext[i] = id;
     w_ext[i] = j < k ? w[t * k + j] : 1.f;
   }
 }

@@ -196,6 +196,38 @@ moe_status_t moe_ffn_route(const int32_t* topk_ids, const float* topk_w, int T, 
                            int32_t* offsets, int32_t* slot_of_pair, void* workspace, size_t workspace_bytes,
                            void* stream);
 
+/* Capacity, in padded slots, of the padded routing tables of a problem:
+ * S_max = T*k + min(E, T*k)*127 rounded up to a multiple of 128 (every
+ * expert's segment padded to whole 128-row blocks fits in it).  0 for an
+ * invalid shape. */
+int64_t moe_ffn_route_padded_slots(int T, int E, int k);
+
+/* The padded routing tables the grouped GEMMs consume, written to caller
+ * arrays for bit-exact checks.  "Prime Flash MoE" sec. 3 and sec. 6: the
+ * routed rows are sorted by expert and every expert's segment is padded to
+ * whole 128-row blocks, so a row block never straddles two experts; the
+ * padding rows are dropped in the epilogues.
+ *   pad_offsets  [E+1]  exclusive scan of counts[e] rounded up to 128
+ *   expert_of_rb [S_max/128]  expert of row block rb, for rb < n_blocks[0]
+ *   pair_info    [S_max/128]  the CTA-pair kernels' schedule, for i < n_blocks[1]:
+ *                       (first row block << 1) | (1 if the next row block
+ *                       belongs to the same expert); pairs cover each expert's
+ *                       blocks in order, two at a time
+ *   row_tok      [S_max]  token t of padded slot s (its pair t*k+j sits at
+ *                       pad_offsets[e] + its rank within expert e), -1 for
+ *                       padding; entries from pad_offsets[E] on are unspecified
+ *   slot_w       [S_max]  topk_w[t, j] of that pair, 0 for padding
+ *   n_blocks     [2]   number of row blocks (pad_offsets[E] / 128), number of pairs
+ * S_max = moe_ffn_route_padded_slots(T, E, k).  All arrays are device memory
+ * owned by the caller; the workspace is sized as for moe_ffn_route.  Requires
+ * T >= 1.  Errors: MOE_ERR_INVALID_ARG (shape or a null pointer),
+ * MOE_ERR_WORKSPACE_TOO_SMALL, MOE_ERR_CUDA; a bad id is reported through
+ * moe_ffn_sync_status. */
+moe_status_t moe_ffn_route_padded(const int32_t* topk_ids, const float* topk_w, int T, int E, int k,
+                                  int32_t* pad_offsets, int32_t* expert_of_rb, int32_t* pair_info, int32_t* row_tok,
+                                  float* slot_w, int32_t* n_blocks, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
 /* The routing permutation, for callers that cannot allocate device memory.
  * The paper has no counterpart to this entry point.
  *
@@ -207,7 +239,11 @@ moe_status_t moe_ffn_route(const int32_t* topk_ids, const float* topk_w, int T, 
  * still the caller's.  Limits: T*k <= 131072 pairs and E <= 1024; larger
  * problems return MOE_ERR_WORKSPACE_TOO_SMALL without launching anything.
  * status_bits (optional, device int32) receives the call's device error bits:
- * 0, or bit 0 set when an expert id was outside [0, E).
+ * 0 when the call succeeded; bit 0 (value 1) when an expert id was outside
+ * [0, E) (those pairs are dropped); bit 1 (value 2) when a bounded device wait
+ * ran out (problems of more than 8192 pairs route in one cooperative launch
+ * whose blocks meet at a grid barrier): counts, offsets and slot_of_pair are
+ * then invalid.
  * The first call on each device looks up the array's device address (setup
  * done once per device, with that device current); make that first call
  * before any stream capture.  The call allocates nothing.  All calls on a

@@ -59,3 +59,38 @@ def assert_close(gpu, ref, dtype="bf16", label="", tol=None):
     msg = f"{label}: max_rel={max_rel:.3e} (<= {tmax}) mean_rel={mean_rel:.3e} (<= {tmean}) cos={cos:.6f}"
     assert max_rel <= tmax and mean_rel <= tmean, msg
     return max_rel, mean_rel, cos
+
+
+def coverage_tokens(topk_ids, n_random=1000, seed=1, pad=128):
+    """A deterministic sample of tokens for checking a full-size output on the
+    oracle: for every expert with routed pairs, the tokens of its first and
+    last routed row and of the first row of its last 128-row block (the tail
+    block, which in the CTA-pair kernels may be the odd half pair), plus
+    n_random tokens drawn with a seeded generator.  Sorted, distinct, int32.
+    Row order within an expert follows the flat pair index t*k + j."""
+    ids = np.asarray(topk_ids)
+    T, k = ids.shape
+    flat = ids.ravel()
+    order = np.argsort(flat, kind="stable")          # pairs grouped by expert, flat order within
+    experts, starts, counts = np.unique(flat[order], return_index=True, return_counts=True)
+    picks = []
+    for s, n in zip(starts, counts):
+        ranks = {0, n - 1, (n - 1) // pad * pad}
+        picks.extend(order[s + r] // k for r in ranks)
+    rnd = np.random.default_rng(seed).choice(T, min(T, n_random), replace=False)
+    return np.unique(np.concatenate([np.asarray(picks, np.int64), rnd])).astype(np.int32)
+
+
+_INPUT_CACHE = {}
+
+
+def cached_inputs(name, seed=0):
+    """wl.make_inputs(name, seed), kept for the next test that asks (the large
+    workloads take seconds to draw).  Callers must not modify the arrays."""
+    from grouped_gemm_gb300 import workloads as wl
+    key = (name, seed)
+    if key not in _INPUT_CACHE:
+        if len(_INPUT_CACHE) >= 2:
+            _INPUT_CACHE.pop(next(iter(_INPUT_CACHE)))
+        _INPUT_CACHE[key] = wl.make_inputs(name, seed=seed)
+    return _INPUT_CACHE[key]

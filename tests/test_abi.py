@@ -25,7 +25,7 @@ def test_header_declares_entry_points():
 
 
 def test_library_exports_every_declared_symbol():
-    lib = ctypes.CDLL(moe.library_path() if os.path.exists(moe.library_path()) else moe.lib()._name)
+    lib = ctypes.CDLL(moe.lib()._name)  # rebuilt first if a source is newer
     missing = [n for n in declared_functions() if not hasattr(lib, n)]
     assert not missing, missing
 
@@ -168,3 +168,29 @@ def test_binding_leaves_out_of_range_shared_counts_to_the_c_abi():
     for ns in (-1, 1021):
         with pytest.raises(ValueError, match="CUDA"):
             moe.moe_ffn_forward_ex(*args, E=E, D=D, H=H, k=k, workspace=t(1 << 20, dt=torch.uint8), n_shared=ns)
+
+
+def test_route_padded_capacity_and_host_checks():
+    def s_max(T, E, k):
+        P = T * k
+        return max(128, (P + min(E, P) * 127 + 127) // 128 * 128)
+    for T, E, k in ((4096, 128, 8), (3, 1024, 4), (64, 8, 2), (1, 1, 1), (131072, 128, 8)):
+        assert moe.moe_ffn_route_padded_slots(T, E, k) == s_max(T, E, k)
+    assert moe.moe_ffn_route_padded_slots(4, 0, 2) == 0
+    assert moe.moe_ffn_route_padded_slots(-1, 8, 2) == 0
+    L = moe.lib()
+    ws = ctypes.create_string_buffer(1 << 16)
+    nul = [None] * 6
+    # T = 0, null arrays and a missing workspace are refused before any launch
+    assert L.moe_ffn_route_padded(None, None, 0, 8, 2, *nul, ctypes.addressof(ws), 1 << 16, None) == 1
+    assert L.moe_ffn_route_padded(None, None, 4, 8, 2, *nul, ctypes.addressof(ws), 1 << 16, None) == 1
+    assert L.moe_ffn_route_padded(1, 1, 4, 8, 2, 1, 1, 1, 1, 1, 1, None, 0, None) == 1
+
+
+def test_workspace_holds_fp32_row_sums_for_large_k():
+    # from k = 9 on the split pipeline sums each token's rows in an fp32 [T, D] accumulator
+    T, E, D, H = 1000, 64, 512, 256
+    for dtype in (moe.MOE_BF16, moe.MOE_MXFP8):
+        k8 = moe.moe_ffn_workspace_size(T, E, D, H, 8, dtype, moe.MOE_SPLIT)
+        k9 = moe.moe_ffn_workspace_size(T, E, D, H, 9, dtype, moe.MOE_SPLIT)
+        assert k9 >= k8 + T * D * 4

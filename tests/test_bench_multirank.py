@@ -98,3 +98,37 @@ def test_gemm_only_figure():
 def test_host_cpu_record():
     h = bench.host_cpu()
     assert h["model"] and h["nproc"] >= 1 and h["omp_threads"] >= 1
+
+
+def test_roofline_fractions_measured_and_nominal():
+    import numpy as np
+    from grouped_gemm_gb300 import workloads as wl
+    w = wl.WORKLOADS["large_skewed"]
+    ids = np.tile(np.arange(8, dtype=np.int32), (w.T, 1))
+    alg = bench.algorithmic(w, ids)
+    peaks = {"hbm_gbs": 6000.0, "bf16_tflops": 1800.0}
+    stage_ms = {"route": 0.03, "gather_zero": 0.5, "up_swiglu": 4.0, "down_reduce": 2.0}
+    kern = {"route": "route_coop", "gather_zero": "gather_tokens", "up_swiglu": "up_swiglu_pair2",
+            "down_reduce": "down_reduce_pair2"}
+    roof, step_bound, step_nom = bench.roofline_fracs(alg, stage_ms, "split", False, peaks, "measured", kern,
+                                                      "large_skewed")
+    # the up projection (the longer stage) is tensor-bound: FLOPs over its time
+    achieved = alg["up_swiglu"]["flops"] / 4e-3 / 1e12
+    assert roof["bound"] == "tensor" and roof["kernel"] == "up_swiglu_pair2"
+    assert roof["frac"] == pytest.approx(achieved / 1800.0, rel=1e-3)
+    assert roof["frac_nominal"] == pytest.approx(achieved / bench.NOMINAL_PEAKS["bf16_tflops"], rel=1e-3)
+    assert step_bound == pytest.approx(alg["step_flops"] / 1.8e15)
+    assert step_nom == pytest.approx(alg["step_flops"] / 2.25e15)
+    # MXFP8: the fp8 peaks (twice the measured bf16 one; the data-sheet fp8 figure)
+    roof8, sb8, sn8 = bench.roofline_fracs(alg, stage_ms, "split", True, peaks, "measured", kern, "mxfp8")
+    assert roof8["peak"] == 3600.0 and roof8["peak_nominal"] == bench.NOMINAL_PEAKS["fp8_tflops"]
+
+
+def test_clock_summary_keeps_samples_inside_the_window():
+    s = bench.ClockSampler.__new__(bench.ClockSampler)
+    s.source = "test"
+    s.samples = [(1.0, 1500.0, 2070.0, []), (2.0, 2000.0, 2070.0, ["sw_power_cap"]), (2.5, 2070.0, 2070.0, []),
+                 (4.0, 900.0, 2070.0, ["hw_slowdown"])]
+    c = s.summary(1.5, 3.0)
+    assert c["samples"] == 2 and c["sm_mhz"] == pytest.approx(2035.0) and c["reasons"] == ["sw_power_cap"]
+    assert s.summary(5.0, 6.0) is None

@@ -11,7 +11,7 @@ import grouped_gemm_gb300 as moe
 import oracle
 from grouped_gemm_gb300 import workloads as wl
 
-from helpers import assert_close
+from helpers import assert_close, cached_inputs, coverage_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -117,6 +117,8 @@ PIPES = {"split": (moe.MOE_SPLIT, 1), "fused": (moe.MOE_FUSED, 1), "fused_splitk
     (1, 256, 384, 4, 4, "uniform"),
     (129, 768, 256, 40, 8, "zipf"),
     (512, 1024, 512, 16, 8, "uniform"),
+    (100, 256, 256, 64, 32, "uniform"),     # k = 32: rows of a token summed in fp32
+    (300, 512, 256, 32, 12, "zipf"),        # k = 12 with empty experts
 ])
 def test_mxfp8_forward_small(T, D, H, E, k, routing, pipe):
     inp = wl.make_custom(T, D, H, E, k, seed=T + H, routing=routing, dtype="mxfp8")
@@ -127,12 +129,13 @@ def test_mxfp8_forward_small(T, D, H, E, k, routing, pipe):
 
 @pytest.mark.parametrize("pipe", list(PIPES))
 def test_mxfp8_full_workload_sampled(pipe):
-    inp = wl.make_inputs("mxfp8", seed=0)
+    # every expert's first, last and tail-block rows plus 1000 seeded random tokens
+    inp = cached_inputs("mxfp8")
     out = run_mx(inp, *PIPES[pipe])
-    tokens = np.sort(np.random.default_rng(2).choice(inp["workload"].T, 48, replace=False)).astype(np.int32)
+    tokens = coverage_tokens(inp["topk_ids"], seed=2)
     r = assert_close(out[torch.from_numpy(tokens.astype(np.int64)).cuda()], oracle_mx(inp, tokens), dtype="mxfp8",
                      label="mxfp8 workload")
-    print(f"mxfp8 workload: max_rel={r[0]:.2e} mean_rel={r[1]:.2e} cos={r[2]:.6f}")
+    print(f"mxfp8 workload {pipe}: {tokens.size} tokens, max_rel={r[0]:.2e} mean_rel={r[1]:.2e} cos={r[2]:.6f}")
     assert torch.isfinite(out.float()).all()
 
 

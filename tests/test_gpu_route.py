@@ -34,6 +34,54 @@ def gpu_route(ids, E):
     return st, counts.cpu().numpy(), offsets.cpu().numpy(), slot.cpu().numpy()[:T * k]
 
 
+def expected_padded(ref, ids, w, E):
+    """The padded tables the GEMMs read, from the oracle's padded offsets and
+    padded slot of every pair: row_tok / slot_w of each padded slot, the expert
+    of each 128-row block, and pairs of consecutive blocks of one expert."""
+    T, k = ids.shape
+    po = ref["pad_offsets"]
+    s_pad = int(po[E])
+    row_tok = np.full(s_pad, -1, np.int64)
+    slot_w = np.zeros(s_pad, np.float32)
+    ps = ref["pad_slot_of_pair"]
+    row_tok[ps] = np.arange(T * k) // k
+    slot_w[ps] = w.ravel()
+    nrb = (po[1:] - po[:-1]) // 128
+    expert_of_rb = np.repeat(np.arange(E), nrb)
+    pairs = []
+    for e in range(E):
+        rb0 = int(po[e]) // 128
+        for q in range(0, int(nrb[e]), 2):
+            pairs.append(((rb0 + q) << 1) | (1 if q + 1 < nrb[e] else 0))
+    return dict(row_tok=row_tok, slot_w=slot_w, expert_of_rb=expert_of_rb, pair_info=np.array(pairs, np.int64),
+                n_blocks=s_pad // 128)
+
+
+def check_padded(ids, E, ref):
+    """moe_ffn_route_padded against the oracle, bit for bit (slot_w compared as
+    float32 bit patterns: each is a copied routing weight)."""
+    T, k = ids.shape
+    rng = np.random.default_rng(T * 7 + E)
+    w = rng.random((T, k), dtype=np.float32)
+    smax = moe.moe_ffn_route_padded_slots(T, E, k)
+    dev_ids = torch.from_numpy(np.ascontiguousarray(ids, np.int32)).cuda()
+    ws = moe.alloc_workspace(T, E, 128, 128, k, moe.MOE_BF16, moe.MOE_FUSED)
+    fill = lambda n, dt=torch.int32: torch.full((n,), -7, dtype=dt, device="cuda")
+    po, erb, pinfo = fill(E + 1), fill(smax // 128), fill(smax // 128)
+    rtok, sw, nb = fill(smax), torch.full((smax,), -7.0, device="cuda"), fill(2)
+    moe.moe_ffn_route_padded(dev_ids, torch.from_numpy(w).cuda(), T, E, k, po, erb, pinfo, rtok, sw, nb, ws)
+    assert moe.moe_ffn_sync_status(ws) == 0
+    exp = expected_padded(ref, ids, w, E)
+    n_rb, n_pairs = (int(v) for v in nb.cpu().numpy())
+    assert np.array_equal(po.cpu().numpy(), ref["pad_offsets"])
+    assert n_rb == exp["n_blocks"] and n_pairs == exp["pair_info"].size
+    assert np.array_equal(erb.cpu().numpy()[:n_rb], exp["expert_of_rb"])
+    assert np.array_equal(pinfo.cpu().numpy()[:n_pairs], exp["pair_info"])
+    s_pad = n_rb * 128
+    assert np.array_equal(rtok.cpu().numpy()[:s_pad], exp["row_tok"])
+    assert np.array_equal(sw.cpu().numpy()[:s_pad].view(np.uint32), exp["slot_w"].view(np.uint32))
+
+
 def check(ids, E):
     st, c, o, s = gpu_route(ids, E)
     assert st == 0
@@ -41,9 +89,11 @@ def check(ids, E):
     assert np.array_equal(c, ref["counts"])
     assert np.array_equal(o, ref["offsets"])
     assert np.array_equal(s, ref["slot_of_pair"])
+    if ids.shape[0] > 0:
+        check_padded(ids, E, ref)
 
 
-@pytest.mark.parametrize("name", ["tiny", "decode", "prefill"])
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "mxfp8"])
 def test_route_workloads(name):
     w = wl.WORKLOADS[name]
     ids, _ = wl.draw_routing(np.random.default_rng(0), w.T, w.E, w.k, w.routing)

@@ -16,7 +16,7 @@ import grouped_gemm_gb300 as moe
 import oracle
 from grouped_gemm_gb300 import workloads as wl
 
-from helpers import assert_close, to_dev
+from helpers import assert_close, cached_inputs, coverage_tokens, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -128,3 +128,30 @@ def test_forward_from_logits_mxfp8():
         ref = oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], rids, rw.astype(np.float32), act=oracle.ACT_MXFP8,
                              x_sf=inp["x_sf"], w1_sf=inp["w1_sf"], w2_sf=inp["w2_sf"])
         assert_close(out, ref, dtype="mxfp8", label=f"mxfp8 from logits pipeline={pipe}")
+
+
+@pytest.mark.parametrize("pipe", list(PIPES))
+def test_forward_from_logits_full_prefill(pipe):
+    """The prefill workload (T=4096, D=2048, H=768, E=128, k=8) started from
+    router logits: ids bit-exact and weights within W_RTOL of the oracle's
+    router; the output on every expert's first, last and tail-block rows plus
+    1000 seeded random tokens."""
+    inp = cached_inputs("prefill")
+    w = inp["workload"]
+    T, D, H, E, k = w.T, w.D, w.H, w.E, w.k
+    lg = wl.router_logits(T, E, seed=1000)
+    rids, rw = oracle.router_topk(lg, k)
+    dev = to_dev(inp)
+    ids = torch.full((T, k), -1, dtype=torch.int32, device="cuda")
+    tw = torch.zeros((T, k), dtype=torch.float32, device="cuda")
+    out = torch.full((T, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = moe.alloc_workspace(T, E, D, H, k, moe.MOE_BF16, PIPES[pipe])
+    moe.moe_ffn_forward_logits(dev["x"], dev["w1"], dev["w2"], torch.from_numpy(lg).cuda(), ids, tw, out, E=E, D=D,
+                               H=H, k=k, workspace=ws, pipeline=PIPES[pipe])
+    assert moe.moe_ffn_sync_status(ws) == 0
+    assert np.array_equal(ids.cpu().numpy(), rids)
+    np.testing.assert_allclose(tw.cpu().numpy().astype(np.float64), rw, rtol=W_RTOL, atol=0)
+    tokens = coverage_tokens(rids, seed=3)
+    ref = oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], rids, tw.cpu().numpy(), act=oracle.ACT_BF16, tokens=tokens)
+    assert_close(out[torch.from_numpy(tokens.astype(np.int64)).cuda()], ref, label=f"prefill from logits {pipe}")
+    assert torch.isfinite(out.float()).all()

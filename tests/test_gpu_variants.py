@@ -119,3 +119,28 @@ def test_forward_ex_rejects_bad_extras():
     # a workspace sized without the shared expert is too small for one
     assert moe.moe_ffn_forward_ex(dev["x"], dev["w1"], dev["w2"], dev["topk_ids"], dev["topk_w"], out, E=3, D=256,
                                   H=128, k=2, workspace=ws, n_shared=1, check=False) == 5
+
+
+@pytest.mark.parametrize("pipeline", [moe.MOE_SPLIT, moe.MOE_FUSED])
+def test_forward_ex_routed_id_of_a_shared_expert_is_bad_routing(pipeline):
+    # With one shared expert the extended problem has E + 1 experts, but a
+    # routed id must still lie in [0, E): id E names the shared expert and is
+    # reported as a bad id (the pair dropped), not run as that expert.
+    T, D, H, E, k, ns = 64, 256, 128, 4, 2, 1
+    inp = wl.make_custom(T, D, H, E + ns, k, seed=17, routing="uniform")
+    ids = inp["topk_ids"] % E
+    ids[9, 1] = E
+    inp["topk_ids"] = ids
+    dev = to_dev(inp)
+    out = torch.full((T, D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = moe.alloc_workspace(T, E, D, H, k, moe.MOE_BF16, pipeline, n_shared=ns)
+    moe.moe_ffn_forward_ex(dev["x"], dev["w1"], dev["w2"], dev["topk_ids"], dev["topk_w"], out, E=E, D=D, H=H, k=k,
+                           workspace=ws, pipeline=pipeline, n_shared=ns)
+    assert moe.moe_ffn_sync_status(ws) == 4          # MOE_ERR_BAD_ROUTING
+    kept = ids.copy()
+    tw = inp["topk_w"].copy()
+    kept[9, 1] = 0
+    tw[9, 1] = 0.0
+    ide, twe = extended(kept, tw, E, ns)
+    ref = oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], ide, twe, act=oracle.ACT_BF16)
+    assert_close(out, ref, label="routed id E dropped")
