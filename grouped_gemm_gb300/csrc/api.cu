@@ -39,6 +39,7 @@ std::atomic<int> g_gather_blocks{8};  // MOE_OPT_GATHER_BLOCKS: gather blocks pe
 std::atomic<int> g_l2_policy{0};      // MOE_OPT_L2_POLICY: bit 0 weights evict_first, bit 1 xg evict_last
 std::atomic<int> g_prefetch_mb{0};    // MOE_OPT_PREFETCH_MB: weights prefetched into L2 during routing
 std::atomic<int> g_pair_swap{0};      // MOE_OPT_PAIR_SWAP: max routed rows of a swap-AB pair tile (measured slower: off)
+std::atomic<int> g_wide_up{0};        // MOE_OPT_WIDE_UP: 512-column up tiles on CTA pairs
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -601,6 +602,10 @@ moe_status_t moe_ffn_set_option(int option, long long value) {
       if (value < 0 || value > 256) return MOE_ERR_INVALID_ARG;
       g_pair_swap.store((int)value);
       return MOE_OK;
+    case MOE_OPT_WIDE_UP:
+      if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
+      g_wide_up.store((int)value);
+      return MOE_OK;
 
     case MOE_OPT_TILE_COLS:
       if (value != 0 && value != 128 && value != 256) return MOE_ERR_INVALID_ARG;
@@ -799,10 +804,19 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
   if (pair_mma && pair_slots <= 0) return MOE_ERR_CUDA;
   prof_front(false);
   if (in_gemm_gather) prof_kernel(1, "none");  // rows gathered by the up kernel
-  prof_kernel(2, pair_mma ? "up_swiglu_pair2" : (gather == 0 && g_up_pairs.load()) ? "up_pair_bf16" : "up_swiglu_bf16");
+  const bool wide_up = pair_mma && g_wide_up.load() == 1;
+  const int wide_slots = wide_up ? pair_wide_cluster_slots() : 0;
+  if (wide_up && wide_slots <= 0) return MOE_ERR_CUDA;
+  prof_kernel(2, wide_up ? "up_swiglu_pair2_wide"
+                         : pair_mma ? "up_swiglu_pair2"
+                                    : (gather == 0 && g_up_pairs.load()) ? "up_pair_bf16" : "up_swiglu_bf16");
   prof_kernel(3, pair_down ? (acc ? "down_reduce_pair2+f32_to_bf16" : "down_reduce_pair2")
                            : (acc ? "down_reduce_bf16+f32_to_bf16" : "down_reduce_bf16"));
-  if (pair_mma)
+  if (wide_up)
+    e = launch_up_pair2_wide_bf16(map_xg, map_w1, up,
+                                  (int)std::min<int64_t>(wide_slots, (int64_t)ws.max_rb * ((up.n_col_tiles + 1) / 2)),
+                                  st, !g_prof.on);
+  else if (pair_mma)
     e = launch_up_pair2_bf16(map_xg, map_w1, up,
                              (int)std::min<int64_t>(pair_slots, (int64_t)ws.max_rb * up.n_col_tiles), st, !g_prof.on);
   else if (gather == 0 && g_up_pairs.load())

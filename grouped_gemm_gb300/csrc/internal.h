@@ -143,6 +143,11 @@ cudaError_t launch_down_pair2_bf16(const CUtensorMap& map_act, const CUtensorMap
                                    int n_pairs, cudaStream_t stream, bool pdl);
 // Co-resident two-CTA clusters of the pair kernels on the current device.
 int pair_cluster_slots();
+// The up projection on CTA pairs in 512-column tiles (act tiles 2g and 2g+1
+// of one block pair; args.n_col_tiles = H / 128), map_w1 boxes of 128 rows.
+cudaError_t launch_up_pair2_wide_bf16(const CUtensorMap& map_xg, const CUtensorMap& map_w1, const GemmArgs& args,
+                                      int n_pairs, cudaStream_t stream, bool pdl);
+int pair_wide_cluster_slots();
 // n = output columns per tile: kDownN, or kDownNNarrow when D % 256 != 0;
 // map_w2's boxes must be n rows.
 cudaError_t launch_down_bf16(const CUtensorMap& map_act, const CUtensorMap& map_w2, const GemmArgs& args, int grid,

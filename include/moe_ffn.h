@@ -386,6 +386,14 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   weights of the up projection's first tiles.  Measured on
  *                   GB300: decode 0.410 ms with 0, 0.408 with 32, 0.409 with
  *                   64; prefill 0.345 with 0, 0.348 with 96 (no gain, off).
+ *   MOE_OPT_WIDE_UP  0 (default) or 1: with CTA pairs, 1 runs the up
+ *                   projection in 512-column tiles (two 256-column halves of
+ *                   the pair's accumulator, the act tiles j and j+1 of one
+ *                   block pair) whose halves the epilogue frees one after the
+ *                   other, so the next tile's MMAs start on half 0 while half
+ *                   1 is still being read: a quarter fewer operand bytes per
+ *                   FLOP than 256-column tiles, four 48 KB stages instead of
+ *                   six 32 KB ones.
  *   (MOE_OPT_L2_POLICY measured at prefill: 0.343 ms with 0, 0.349 with 1,
  *                   0.342 with 2, 0.348 with 3: no gain, off.) */
 typedef enum {
@@ -404,7 +412,8 @@ typedef enum {
   MOE_OPT_GATHER_BLOCKS = 12,
   MOE_OPT_L2_POLICY = 13,
   MOE_OPT_ROUTER_FUSED = 14,
-  MOE_OPT_PREFETCH_MB = 15
+  MOE_OPT_PREFETCH_MB = 15,
+  MOE_OPT_WIDE_UP = 16
 } moe_option_t;
 moe_status_t moe_ffn_set_option(int option, long long value);
 

@@ -23,7 +23,7 @@ pytestmark = pytest.mark.gpu
 # materializing gather kernel (default), with in-kernel gathers, with two row
 # blocks per up tile, with the tail row blocks run as swap-AB tiles and with
 # both GEMMs on CTA pairs (down tiles never swap-AB by default, or swap-AB for
-# small pairs, or always); the
+# small pairs, or always; the up projection in 512-column tiles); the
 # fused pipeline on clusters (default where the shape allows) and with the
 # H-split fp32 partial sums.
 MODES = {
@@ -35,11 +35,12 @@ MODES = {
     "split_pair2": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 1}),
     "split_pair2_swap": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 1, moe.MOE_OPT_PAIR_SWAP: 128}),
     "split_pair2_allswap": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 1, moe.MOE_OPT_PAIR_SWAP: 256}),
+    "split_wide": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 1, moe.MOE_OPT_WIDE_UP: 1}),
     "fused": (moe.MOE_FUSED, {}),
     "fused_splitk": (moe.MOE_FUSED, {moe.MOE_OPT_FUSED_CLUSTER: 0}),
 }
 DEFAULTS = {moe.MOE_OPT_UP_PAIRS: 0, moe.MOE_OPT_GATHER: 0, moe.MOE_OPT_SWAP_AB: 0, moe.MOE_OPT_FUSED_CLUSTER: 1,
-            moe.MOE_OPT_PAIR_MMA: 2, moe.MOE_OPT_PAIR_SWAP: 0}
+            moe.MOE_OPT_PAIR_MMA: 2, moe.MOE_OPT_PAIR_SWAP: 0, moe.MOE_OPT_WIDE_UP: 0}
 PIPELINES = list(MODES)
 
 
@@ -156,7 +157,7 @@ def test_forward_full_workload_sampled(name, pipeline):
     """Full-size workloads: decode on every token; prefill and large_skewed on
     the first and last routed token of every expert, the first token of every
     expert's last row block, and 1000 seeded random tokens."""
-    if name == "large_skewed" and pipeline not in ("split", "fused", "fused_splitk", "split_pair2"):
+    if name == "large_skewed" and pipeline not in ("split", "fused", "fused_splitk", "split_pair2", "split_wide"):
         pytest.skip("option variants are covered at the smaller sizes")
     inp = cached_inputs(name)
     out, _ = run_mode(inp, to_dev(inp), pipeline)
