@@ -126,6 +126,8 @@ KERNEL_SOURCES = {
     "up_swiglu_pair2": ["grouped_gemm_gb300/csrc/gemm_pair2.cu"] + _PTX,
     "down_reduce_pair2": ["grouped_gemm_gb300/csrc/gemm_pair2.cu"] + _PTX,
     "up_swiglu_pair2_wide": ["grouped_gemm_gb300/csrc/gemm_pair2_wide.cu"] + _PTX,
+    "up_swiglu_bf16_m64": ["grouped_gemm_gb300/csrc/gemm_bf16.cu"] + _PTX,
+    "down_reduce_bf16_m64": ["grouped_gemm_gb300/csrc/gemm_bf16.cu"] + _PTX,
     "up_pair_bf16": ["grouped_gemm_gb300/csrc/gemm_pair.cu"] + _PTX,
     "up_swiglu_mxfp8": ["grouped_gemm_gb300/csrc/gemm_mxfp8.cu"] + _MXH + _PTX,
     "down_reduce_mxfp8": ["grouped_gemm_gb300/csrc/gemm_mxfp8.cu"] + _MXH + _PTX,

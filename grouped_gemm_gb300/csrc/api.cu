@@ -40,6 +40,7 @@ std::atomic<int> g_l2_policy{0};      // MOE_OPT_L2_POLICY: bit 0 weights evict_
 std::atomic<int> g_prefetch_mb{0};    // MOE_OPT_PREFETCH_MB: weights prefetched into L2 during routing
 std::atomic<int> g_pair_swap{0};      // MOE_OPT_PAIR_SWAP: max routed rows of a swap-AB pair tile (measured slower: off)
 std::atomic<int> g_wide_up{0};        // MOE_OPT_WIDE_UP: 512-column up tiles on CTA pairs
+std::atomic<int> g_tile_m{0};         // MOE_OPT_TILE_M: rows per tile of the single-CTA split GEMMs (0 automatic)
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -602,6 +603,10 @@ moe_status_t moe_ffn_set_option(int option, long long value) {
       if (value < 0 || value > 256) return MOE_ERR_INVALID_ARG;
       g_pair_swap.store((int)value);
       return MOE_OK;
+    case MOE_OPT_TILE_M:
+      if (value != 0 && value != 64 && value != 128) return MOE_ERR_INVALID_ARG;
+      g_tile_m.store((int)value);
+      return MOE_OK;
     case MOE_OPT_WIDE_UP:
       if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
       g_wide_up.store((int)value);
@@ -738,12 +743,19 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
           ? kUpFoldNarrow
           : kUpFold;  // auto: narrow when the wide tiles make fewer than ~8 waves
   const bool pair_down = pair_mma && down_n == kDownN;
+  // 64-row tiles for the single-CTA GEMMs: by option, or automatically when
+  // an expert gets at most 64 routed rows on average
+  const int tile_m_opt = g_tile_m.load();
+  const int64_t P = (int64_t)T * k;
+  const bool m64 = !pair_mma && !in_gemm_gather && !g_up_pairs.load() &&
+                   (tile_m_opt == 64 || (tile_m_opt == 0 && P <= 64 * std::min<int64_t>(P, E)));
+  const int bm = m64 ? 64 : kBM;
   CUtensorMap map_xg, map_w1, map_act, map_w2;
   const bool map_a_ok = in_gemm_gather ? make_map_bf16(&map_xg, x, (uint64_t)T, (uint64_t)D, 1)
-                                       : make_map_bf16(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, kBM);
+                                       : make_map_bf16(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, bm);
   if (!map_a_ok ||
       !make_map_bf16(&map_w1, w1, (uint64_t)E * 2 * H, (uint64_t)D, fold) ||
-      !make_map_bf16(&map_act, ws.act, (uint64_t)ws.S_max, (uint64_t)H, kBM) ||
+      !make_map_bf16(&map_act, ws.act, (uint64_t)ws.S_max, (uint64_t)H, bm) ||
       !make_map_bf16(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, pair_down ? 128 : down_n))
     return MOE_ERR_CUDA;
 
@@ -798,7 +810,7 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
   up.tile_counter = dyn ? ws.meta + 2 : nullptr;
   up.n_col_tiles = H / fold;
   up.k_blocks = D / kBK;
-  const int up_grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * up.n_col_tiles);
+  const int up_grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * up.n_col_tiles * (kBM / bm));
   up.x = x;
   const int pair_slots = pair_mma ? pair_cluster_slots() : 0;
   if (pair_mma && pair_slots <= 0) return MOE_ERR_CUDA;
@@ -807,11 +819,14 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
   const bool wide_up = pair_mma && g_wide_up.load() == 1;
   const int wide_slots = wide_up ? pair_wide_cluster_slots() : 0;
   if (wide_up && wide_slots <= 0) return MOE_ERR_CUDA;
-  prof_kernel(2, wide_up ? "up_swiglu_pair2_wide"
-                         : pair_mma ? "up_swiglu_pair2"
-                                    : (gather == 0 && g_up_pairs.load()) ? "up_pair_bf16" : "up_swiglu_bf16");
+  prof_kernel(2, wide_up    ? "up_swiglu_pair2_wide"
+                 : pair_mma ? "up_swiglu_pair2"
+                 : (gather == 0 && g_up_pairs.load()) ? "up_pair_bf16"
+                 : m64      ? "up_swiglu_bf16_m64"
+                            : "up_swiglu_bf16");
   prof_kernel(3, pair_down ? (acc ? "down_reduce_pair2+f32_to_bf16" : "down_reduce_pair2")
-                           : (acc ? "down_reduce_bf16+f32_to_bf16" : "down_reduce_bf16"));
+                           : m64 ? (acc ? "down_reduce_bf16_m64+f32_to_bf16" : "down_reduce_bf16_m64")
+                                 : (acc ? "down_reduce_bf16+f32_to_bf16" : "down_reduce_bf16"));
   if (wide_up)
     e = launch_up_pair2_wide_bf16(map_xg, map_w1, up,
                                   (int)std::min<int64_t>(wide_slots, (int64_t)ws.max_rb * ((up.n_col_tiles + 1) / 2)),
@@ -822,7 +837,7 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
   else if (gather == 0 && g_up_pairs.load())
     e = launch_up_pair_bf16(map_xg, map_w1, up, up_grid, st);
   else
-    e = launch_up_bf16(map_xg, map_w1, up, up_grid, st, gather, fold, !g_prof.on);
+    e = launch_up_bf16(map_xg, map_w1, up, up_grid, st, gather, fold, !g_prof.on, bm);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 3);
 
@@ -830,13 +845,13 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
   dn.tile_counter = dyn ? ws.meta + 3 : nullptr;
   dn.n_col_tiles = D / down_n;
   dn.k_blocks = H / kBK;
-  const int dn_grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * dn.n_col_tiles);
+  const int dn_grid = (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * dn.n_col_tiles * (kBM / bm));
   if (pair_down)
     e = launch_down_pair2_bf16(map_act, map_w2, dn,
                                (int)std::min<int64_t>(pair_slots, (int64_t)ws.max_rb * dn.n_col_tiles), st,
                                !g_prof.on);
   else
-    e = launch_down_bf16(map_act, map_w2, dn, dn_grid, st, !g_prof.on, down_n);
+    e = launch_down_bf16(map_act, map_w2, dn, dn_grid, st, !g_prof.on, down_n, bm);
   if (e == cudaSuccess && acc) e = launch_f32_to_bf16(acc, out, (int64_t)T * D, sms * 4, st);
   prof_mark(st, 4);
   return cuda_status(e);

@@ -38,9 +38,9 @@ namespace {
 enum { kModeUp = 0, kModeDown = 1 };
 constexpr int kTileSlots = 4;   // depth of the producer -> consumers tile-index ring
 
-template <int MODE, int N, int STAGES>
+template <int MODE, int N, int STAGES, int BM = kBM>
 struct GemmCfg {
-  static constexpr int kABytes = kBM * kBK * 2;             // 16 KB
+  static constexpr int kABytes = BM * kBK * 2;              // 16 KB (8 KB for 64-row tiles)
   static constexpr int kBBytes = N * kBK * 2;               // N rows of 128 B
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * N;                   // double-buffered accumulator
@@ -50,8 +50,8 @@ struct GemmCfg {
   // UP stages its row of N/2 act values the same way and writes it with one
   // bulk copy.
   static constexpr int kStageRowBytes = N + 16;
-  static constexpr int kStagingBytes = kBM * kStageRowBytes;
-  static constexpr int kBarrierBytes = 256;
+  static constexpr int kStagingBytes = BM * kStageRowBytes;
+  static constexpr int kBarrierBytes = STAGES > 6 ? 512 : 256;
   // No alignment slack: dynamic shared memory starts 1024-byte aligned (the
   // kernel checks and reports an error otherwise).
   static constexpr int kSmemBytes = STAGES * kStageBytes + kStagingBytes + kBarrierBytes;
@@ -97,11 +97,19 @@ __device__ __forceinline__ float swiglu(float g, float u, float lim) {
   return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-template <int MODE, int N, int STAGES, int GATHER>
+// BM = 64: 64-row tiles (tcgen05.mma M = 64), for problems with few routed
+// rows per expert (Pearl "Optimizing Grouped GEMM for MoE on Blackwell":
+// tile_m = 64 in 1-CTA mode halves the token stage, so more weight stages fit).
+// Each 128-row block is two 64-row halves; tiles are ordered all first halves,
+// then all second halves, and a second half without routed rows is skipped.
+// The M = 64 accumulator sits in TMEM lanes 0..15 of each 32-lane quadrant
+// (row r in lane 32 * (r / 16) + r % 16), so epilogue lanes 16..31 idle.
+template <int MODE, int N, int STAGES, int GATHER, int BM = kBM>
 __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
     grouped_gemm_bf16_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                              const GemmArgs args) {
-  using Cfg = GemmCfg<MODE, N, STAGES>;
+  static_assert(BM == kBM || (BM == 64 && GATHER == kGatherTile), "64-row tiles read the pre-gathered rows");
+  using Cfg = GemmCfg<MODE, N, STAGES, BM>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_addr(smem_raw) & 1023u) {  // SW128 tiles need 1024-byte alignment
     if (threadIdx.x == 0) atomicOr(args.err, kErrLaunch);
@@ -172,8 +180,18 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
   if (threadIdx.x == 0) griddep_launch_dependents();
 
   const int num_rb = args.meta[0];
-  const int n_tiles = num_rb * args.n_col_tiles;
+  constexpr int kHalves = kBM / BM;  // row tiles per 128-row block
+  const int n_tiles = num_rb * kHalves * args.n_col_tiles;
   const int KB = args.k_blocks;
+  // the 128-row block of a tile and the first padded slot of its rows
+  auto tile_rb = [&](int tile) {
+    const int rbh = tile / args.n_col_tiles;
+    return kHalves == 1 ? rbh : (rbh >= num_rb ? rbh - num_rb : rbh);
+  };
+  auto tile_row0 = [&](int tile) -> int64_t {
+    const int rbh = tile / args.n_col_tiles;
+    return kHalves == 1 ? (int64_t)rbh * kBM : (int64_t)tile_rb(tile) * kBM + (rbh >= num_rb ? BM : 0);
+  };
 
   // consumer side of the tile ring: the next tile index, or -1 if aborting;
   // t_ns gets the tile's swap-AB width (0 = normal tile)
@@ -205,7 +223,7 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
     // them -- more bytes in flight than the shared-memory ring can hold.
     int pf_tile = blockIdx.x, pf_kb = 0, pf_e = pf_tile < n_tiles ? args.expert_of_rb[pf_tile / args.n_col_tiles] : 0;
     auto prefetch_one = [&]() {
-      if (pf_tile >= n_tiles) return;
+      if (BM != kBM || pf_tile >= n_tiles) return;
       const int prb = pf_tile / args.n_col_tiles, pj = pf_tile % args.n_col_tiles;
       if (GATHER == kGatherTile) tma_prefetch_2d(&map_a, pf_kb * kBK, prb * kBM);
       if (MODE == kModeUp) {
@@ -234,8 +252,14 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
         } else {
           next = args.tile_counter ? atomicAdd(args.tile_counter, 1)
                                    : (tile < 0 ? (int)blockIdx.x : tile + (int)gridDim.x);
+          // 64-row tiles: skip a second half that holds no routed rows
+          while (BM != kBM && next < n_tiles && next >= num_rb * args.n_col_tiles) {
+            const int nrb = tile_rb(next);
+            if (rb_rows(args, nrb, args.expert_of_rb[nrb]) > BM) break;
+            next = args.tile_counter ? atomicAdd(args.tile_counter, 1) : next + (int)gridDim.x;
+          }
           int ns = 0;
-          if (N == 256 && args.swap_ab && next < n_tiles) {
+          if (BM == kBM && N == 256 && args.swap_ab && next < n_tiles) {
             const int nrb = next / args.n_col_tiles;
             const int v = rb_rows(args, nrb, args.expert_of_rb[nrb]);
             if (v < kBM && ((v + 15) & ~15) <= kSwapMaxN) ns = (v + 15) & ~15;
@@ -256,8 +280,9 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
       }
       if (next >= n_tiles) break;
       tile = next;
-      const int rb = tile / args.n_col_tiles, j = tile % args.n_col_tiles;
+      const int rb = tile_rb(tile), j = tile % args.n_col_tiles;
       const int e = args.expert_of_rb[rb];
+      const int a_row0 = (int)tile_row0(tile);
       int g0 = 0, g1 = 0, g2 = 0, g3 = 0;
       if (GATHER == kGatherTma4) {  // lane l fetches tile rows 4l..4l+3; padding rows read row 0
         const int* rt = args.row_tok + (int64_t)rb * kBM + lane * 4;
@@ -281,7 +306,7 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
         if (GATHER == kGatherTma4) {
           tma_gather4(sA + s * Cfg::kABytes + lane * 4 * kBK * 2, &map_a, &full[s], kb * kBK, g0, g1, g2, g3);
         } else if (GATHER == kGatherTile && lane == 0) {
-          tma_load_2d(sA + s * Cfg::kABytes, &map_a, &full[s], kb * kBK, rb * kBM);
+          tma_load_2d(sA + s * Cfg::kABytes, &map_a, &full[s], kb * kBK, a_row0);
         }
         if (lane == 0) {
           if (args.prefetch > 0) prefetch_one();
@@ -307,7 +332,7 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = idesc_bf16_f32(kBM, N);
+    constexpr uint32_t idesc = idesc_bf16_f32(BM, N);
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
@@ -338,7 +363,7 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
         tc_fence_after();
         const uint64_t adesc = sdesc_sw128(smem_addr(sA + s * Cfg::kABytes));
         const uint64_t bdesc = sdesc_sw128(smem_addr(sB + s * Cfg::kBBytes));
-        if (N == 256 && ns > 0) {
+        if (BM == kBM && N == 256 && ns > 0) {
           // swap-AB: weight rows are M, the tile's routed rows are N
           const uint64_t bdesc_hi = sdesc_sw128(smem_addr(sB + s * Cfg::kBBytes + kBM * kBK * 2));
 #pragma unroll
@@ -423,7 +448,9 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
   } else if (warp >= 2 && warp < 6) {
     // ------------------------------------------------------------ epilogue
     const int quad = warp & 3;  // TMEM lanes this warp may access
-    const int row = quad * 32 + lane;
+    // the tile row this thread's TMEM lane holds (64-row tiles: lanes 0..15 only)
+    const bool row_lane = BM == kBM || lane < 16;
+    const int row = BM == kBM ? quad * 32 + lane : quad * 16 + (lane & 15);
     const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
     uint8_t* my_stage = sStage + row * Cfg::kStageRowBytes;
     // barrier of the 128 epilogue threads (bounded, unlike bar.sync)
@@ -442,12 +469,12 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
       const uint32_t aph = (uint32_t)(it >> 1) & 1u;
       if (!mbar_wait(&tfull[acc], aph, wc, 4)) break;
       tc_fence_after();
-      const int rb = tile / args.n_col_tiles, j = tile % args.n_col_tiles;
-      const int64_t slot = (int64_t)rb * kBM + row;
-      const int tok = args.row_tok[slot];
+      const int rb = tile_rb(tile), j = tile % args.n_col_tiles;
+      const int64_t slot = tile_row0(tile) + row;
+      const int tok = row_lane ? args.row_tok[slot] : -1;
       const uint32_t tacc = lane_base + acc * N;
       const int ns = t_ns;
-      if (N == 256 && ns > 0) {
+      if (BM == kBM && N == 256 && ns > 0) {
         // Swap-AB tile: this thread's TMEM lane is weight row `row` of each
         // 128-row half and the columns are the tile's rows c < ns.  The values
         // go transposed into the staging tile (staging row c = tile row c),
@@ -600,11 +627,11 @@ __global__ void __launch_bounds__(threads_for<GATHER>(), 1)
   }
 }
 
-template <int MODE, int N, int STAGES, int GATHER>
+template <int MODE, int N, int STAGES, int GATHER, int BM = kBM>
 cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args, int grid,
                         cudaStream_t stream, bool pdl) {
-  using Cfg = GemmCfg<MODE, N, STAGES>;
-  auto kern = grouped_gemm_bf16_kernel<MODE, N, STAGES, GATHER>;
+  using Cfg = GemmCfg<MODE, N, STAGES, BM>;
+  auto kern = grouped_gemm_bf16_kernel<MODE, N, STAGES, GATHER, BM>;
   // once per device: not a stream operation, so it stays out of graph capture
   static bool smem_set[64] = {};
   int dev = 0;
@@ -630,7 +657,13 @@ cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmAr
 }  // namespace
 
 cudaError_t launch_up_bf16(const CUtensorMap& map_a, const CUtensorMap& map_w1, const GemmArgs& args, int grid,
-                           cudaStream_t stream, int gather, int fold, bool pdl) {
+                           cudaStream_t stream, int gather, int fold, bool pdl, int bm) {
+  if (bm == 64) {  // 64-row tiles (map_a boxes of 64 rows), pre-gathered rows
+    if (fold == kUpFoldNarrow)
+      return launch_gemm<kModeUp, 2 * kUpFoldNarrow, kUpStagesM64Narrow, kGatherTile, 64>(map_a, map_w1, args, grid,
+                                                                                        stream, pdl);
+    return launch_gemm<kModeUp, 2 * kUpFold, kUpStagesM64, kGatherTile, 64>(map_a, map_w1, args, grid, stream, pdl);
+  }
   if (fold == kUpFoldNarrow)  // 64 gate + 64 up rows per tile, 6-stage ring
     return launch_gemm<kModeUp, 2 * kUpFoldNarrow, kUpStagesNarrow, kGatherTile>(map_a, map_w1, args, grid, stream,
                                                                                 pdl);
@@ -642,7 +675,13 @@ cudaError_t launch_up_bf16(const CUtensorMap& map_a, const CUtensorMap& map_w1, 
 }
 
 cudaError_t launch_down_bf16(const CUtensorMap& map_act, const CUtensorMap& map_w2, const GemmArgs& args, int grid,
-                             cudaStream_t stream, bool pdl, int n) {
+                             cudaStream_t stream, bool pdl, int n, int bm) {
+  if (bm == 64) {  // 64-row tiles (map_act boxes of 64 rows)
+    if (n == kDownNNarrow)
+      return launch_gemm<kModeDown, kDownNNarrow, kDownStagesM64Narrow, kGatherTile, 64>(map_act, map_w2, args, grid,
+                                                                                        stream, pdl);
+    return launch_gemm<kModeDown, kDownN, kDownStagesM64, kGatherTile, 64>(map_act, map_w2, args, grid, stream, pdl);
+  }
   if (n == kDownNNarrow)  // D % 256 != 0: 128-column output tiles
     return launch_gemm<kModeDown, kDownNNarrow, kDownStagesNarrow, kGatherTile>(map_act, map_w2, args, grid, stream,
                                                                               pdl);

@@ -127,8 +127,9 @@ cudaError_t launch_gather_zero(const Workspace& ws, const void* x, const int32_t
 // cp.async warps gather rows of args.x (map_a unused).
 // fold = gate (and up) rows per tile: kUpFold (N = 256) or kUpFoldNarrow (N =
 // 128, gather 0 only); map_w1's boxes must be `fold` rows.
+// bm = 64: 64-row tiles (gather 0 only; map_a boxes of 64 rows).
 cudaError_t launch_up_bf16(const CUtensorMap& map_a, const CUtensorMap& map_w1, const GemmArgs& args, int grid,
-                           cudaStream_t stream, int gather, int fold, bool pdl);
+                           cudaStream_t stream, int gather, int fold, bool pdl, int bm = kBM);
 // Up-projection with two row blocks of one expert per tile sharing each W1
 // tile (tiles = block pairs x column tiles).
 cudaError_t launch_up_pair_bf16(const CUtensorMap& map_a, const CUtensorMap& map_w1, const GemmArgs& args, int grid,
@@ -150,8 +151,9 @@ cudaError_t launch_up_pair2_wide_bf16(const CUtensorMap& map_xg, const CUtensorM
 int pair_wide_cluster_slots();
 // n = output columns per tile: kDownN, or kDownNNarrow when D % 256 != 0;
 // map_w2's boxes must be n rows.
+// bm = 64: 64-row tiles (map_act boxes of 64 rows).
 cudaError_t launch_down_bf16(const CUtensorMap& map_act, const CUtensorMap& map_w2, const GemmArgs& args, int grid,
-                             cudaStream_t stream, bool pdl, int n);
+                             cudaStream_t stream, bool pdl, int n, int bm = kBM);
 
 struct FusedArgs {
   const int* meta;
@@ -303,5 +305,10 @@ constexpr int kDownN = 256;
 constexpr int kDownStages = 4;
 constexpr int kDownNNarrow = 128;
 constexpr int kDownStagesNarrow = 6;
+// 64-row tiles: the token stage is 8 KB, so more weight stages fit
+constexpr int kUpStagesM64 = 5;          // 8 + 32 KB
+constexpr int kUpStagesM64Narrow = 8;    // 8 + 16 KB
+constexpr int kDownStagesM64 = 5;        // 8 + 32 KB
+constexpr int kDownStagesM64Narrow = 8;  // 8 + 16 KB
 
 }  // namespace moe

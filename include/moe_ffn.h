@@ -394,6 +394,16 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   1 is still being read: a quarter fewer operand bytes per
  *                   FLOP than 256-column tiles, four 48 KB stages instead of
  *                   six 32 KB ones.
+ *   MOE_OPT_TILE_M  0 (default: automatic, 64 when the routed pairs are at
+ *                   most 64 per expert on average), 64 or 128: rows per tile
+ *                   of the single-CTA split GEMMs (the CTA-pair kernels always
+ *                   take 128 per CTA).  64-row tiles (tcgen05.mma M = 64)
+ *                   halve the token stage so that more weight stages fit in
+ *                   shared memory; a 128-row block's second half is skipped
+ *                   when it holds no routed rows.  Measured on GB300 at
+ *                   decode (16 rows per expert): step 0.410 ms with 128,
+ *                   0.387 with 64 (up kernel 0.266 -> 0.250 ms, 0.97 of the
+ *                   measured HBM copy rate).
  *   (MOE_OPT_L2_POLICY measured at prefill: 0.343 ms with 0, 0.349 with 1,
  *                   0.342 with 2, 0.348 with 3: no gain, off.) */
 typedef enum {
@@ -413,7 +423,8 @@ typedef enum {
   MOE_OPT_L2_POLICY = 13,
   MOE_OPT_ROUTER_FUSED = 14,
   MOE_OPT_PREFETCH_MB = 15,
-  MOE_OPT_WIDE_UP = 16
+  MOE_OPT_WIDE_UP = 16,
+  MOE_OPT_TILE_M = 17
 } moe_option_t;
 moe_status_t moe_ffn_set_option(int option, long long value);
 

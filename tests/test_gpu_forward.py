@@ -24,10 +24,11 @@ pytestmark = pytest.mark.gpu
 # blocks per up tile, with the tail row blocks run as swap-AB tiles and with
 # both GEMMs on CTA pairs (down tiles never swap-AB by default, or swap-AB for
 # small pairs, or always; the up projection in 512-column tiles); the
+# single-CTA GEMMs with 64-row tiles; the
 # fused pipeline on clusters (default where the shape allows) and with the
 # H-split fp32 partial sums.
 MODES = {
-    "split": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 0}),
+    "split": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 0, moe.MOE_OPT_TILE_M: 128}),
     "split_pairs": (moe.MOE_SPLIT, {moe.MOE_OPT_UP_PAIRS: 1}),
     "split_gather4": (moe.MOE_SPLIT, {moe.MOE_OPT_GATHER: 1}),
     "split_cpasync": (moe.MOE_SPLIT, {moe.MOE_OPT_GATHER: 2}),
@@ -36,11 +37,12 @@ MODES = {
     "split_pair2_swap": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 1, moe.MOE_OPT_PAIR_SWAP: 128}),
     "split_pair2_allswap": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 1, moe.MOE_OPT_PAIR_SWAP: 256}),
     "split_wide": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 1, moe.MOE_OPT_WIDE_UP: 1}),
+    "split_m64": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 0, moe.MOE_OPT_TILE_M: 64}),
     "fused": (moe.MOE_FUSED, {}),
     "fused_splitk": (moe.MOE_FUSED, {moe.MOE_OPT_FUSED_CLUSTER: 0}),
 }
 DEFAULTS = {moe.MOE_OPT_UP_PAIRS: 0, moe.MOE_OPT_GATHER: 0, moe.MOE_OPT_SWAP_AB: 0, moe.MOE_OPT_FUSED_CLUSTER: 1,
-            moe.MOE_OPT_PAIR_MMA: 2, moe.MOE_OPT_PAIR_SWAP: 0, moe.MOE_OPT_WIDE_UP: 0}
+            moe.MOE_OPT_PAIR_MMA: 2, moe.MOE_OPT_PAIR_SWAP: 0, moe.MOE_OPT_WIDE_UP: 0, moe.MOE_OPT_TILE_M: 0}
 PIPELINES = list(MODES)
 
 
@@ -157,7 +159,8 @@ def test_forward_full_workload_sampled(name, pipeline):
     """Full-size workloads: decode on every token; prefill and large_skewed on
     the first and last routed token of every expert, the first token of every
     expert's last row block, and 1000 seeded random tokens."""
-    if name == "large_skewed" and pipeline not in ("split", "fused", "fused_splitk", "split_pair2", "split_wide"):
+    if name == "large_skewed" and pipeline not in ("split", "fused", "fused_splitk", "split_pair2", "split_wide",
+                                                   "split_m64"):
         pytest.skip("option variants are covered at the smaller sizes")
     inp = cached_inputs(name)
     out, _ = run_mode(inp, to_dev(inp), pipeline)
