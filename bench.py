@@ -84,10 +84,11 @@ def algorithmic(w, ids):
     live = int(np.unique(ids).size)
     eb = 2 if w.dtype == "bf16" else 1
     sfb = 0 if w.dtype == "bf16" else 1.0 / 32
-    elem = eb + sfb
-    step_bytes = (w.T * w.D * elem + live * 3 * w.H * w.D * elem + P * 8 + w.T * w.D * 2)
-    up_bytes = live * 2 * w.H * w.D * elem + P * w.D * elem + P * w.H * elem
-    down_bytes = live * w.D * w.H * elem + P * w.H * elem + w.T * w.D * 2
+    elem = eb + sfb                                              # activations (x, act)
+    welem = (0.5 + sfb) if w.dtype == "mxfp4w" else elem         # expert weights
+    step_bytes = (w.T * w.D * elem + live * 3 * w.H * w.D * welem + P * 8 + w.T * w.D * 2)
+    up_bytes = live * 2 * w.H * w.D * welem + P * w.D * elem + P * w.H * elem
+    down_bytes = live * w.D * w.H * welem + P * w.H * elem + w.T * w.D * 2
     return {
         "step_flops": 6.0 * P * w.D * w.H, "step_bytes": float(step_bytes),
         "up_swiglu": {"flops": 4.0 * P * w.D * w.H, "bytes": float(up_bytes)},
@@ -131,6 +132,8 @@ KERNEL_SOURCES = {
     "up_pair_bf16": ["grouped_gemm_gb300/csrc/gemm_pair.cu"] + _PTX,
     "up_swiglu_mxfp8": ["grouped_gemm_gb300/csrc/gemm_mxfp8.cu"] + _MXH + _PTX,
     "down_reduce_mxfp8": ["grouped_gemm_gb300/csrc/gemm_mxfp8.cu"] + _MXH + _PTX,
+    "up_swiglu_mxfp4w": ["grouped_gemm_gb300/csrc/gemm_mxfp8.cu"] + _MXH + _PTX,
+    "down_reduce_mxfp4w": ["grouped_gemm_gb300/csrc/gemm_mxfp8.cu"] + _MXH + _PTX,
     "fused_cluster_bf16": ["grouped_gemm_gb300/csrc/gemm_fused_cluster.cu"] + _PTX,
     "fused_moe_bf16": ["grouped_gemm_gb300/csrc/gemm_fused.cu"] + _PTX,
     "fused_cluster_mxfp8": ["grouped_gemm_gb300/csrc/gemm_fused_cluster_mx.cu"] + _MXH + _PTX,
@@ -318,8 +321,8 @@ def bench_workload(args, name, pipeline_name, rank, world, sampler, full=True):
 
     inp = wl.make_inputs(name, seed=rank)
     w = inp["workload"]
-    mx = w.dtype == "mxfp8"
-    dtype = moe.MOE_MXFP8 if mx else moe.MOE_BF16
+    mx = w.dtype in ("mxfp8", "mxfp4w")      # MXFP8 activations (e4m3 or packed E2M1 weights)
+    dtype = {"bf16": moe.MOE_BF16, "mxfp8": moe.MOE_MXFP8, "mxfp4w": moe.MOE_MXFP4W}[w.dtype]
     dev = {k: torch.from_numpy(inp[k] if mx else inp[k].view(np.int16)).cuda() for k in ("x", "w1", "w2")}
     if mx:  # weight scales are repacked once, like the weights themselves
         dev["x_sf"] = torch.from_numpy(inp["x_sf"]).cuda()
@@ -447,7 +450,8 @@ def bench_workload(args, name, pipeline_name, rank, world, sampler, full=True):
                      f"(129 MB L2), no flush needed")}
     line = {
         "value": round(value, 3), "unit": "TFLOP/s", "ms_per_step": round(ms, 5),
-        "dtype": "e4m3 (MXFP8)" if mx else "bf16", "tokens_per_s": round(tokens_per_s, 1),
+        "dtype": {"bf16": "bf16", "mxfp8": "e4m3 (MXFP8)", "mxfp4w": "e4m3 x e2m1 (MXFP8 x MXFP4)"}[w.dtype],
+        "tokens_per_s": round(tokens_per_s, 1),
         "roofline_step_frac": round(step_bound / (ms * 1e-3), 4),
         "roofline_step_frac_nominal": round(step_bound_nominal / (ms * 1e-3), 4),
         "config": config, "roofline": roofline,
@@ -551,10 +555,11 @@ def run_ours(args, rank, world, local_rank):
 
 def oracle_call(inp, tokens):
     import oracle
-    mx = inp["workload"].dtype == "mxfp8"
+    dt = inp["workload"].dtype
     return oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], inp["topk_ids"], inp["topk_w"],
-                          act=oracle.ACT_MXFP8 if mx else oracle.ACT_BF16, tokens=tokens,
-                          x_sf=inp.get("x_sf"), w1_sf=inp.get("w1_sf"), w2_sf=inp.get("w2_sf"))
+                          act=oracle.ACT_BF16 if dt == "bf16" else oracle.ACT_MXFP8, tokens=tokens,
+                          x_sf=inp.get("x_sf"), w1_sf=inp.get("w1_sf"), w2_sf=inp.get("w2_sf"),
+                          fp4_weights=dt == "mxfp4w")
 
 
 def host_cpu():

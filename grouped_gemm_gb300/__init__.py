@@ -13,13 +13,13 @@ import os
 import threading
 
 __all__ = [
-    "MOE_BF16", "MOE_MXFP8", "MOE_FUSED", "MOE_SPLIT", "MoeFFNError", "library_path", "lib",
+    "MOE_BF16", "MOE_MXFP8", "MOE_MXFP4W", "MOE_FUSED", "MOE_SPLIT", "MoeFFNError", "library_path", "lib",
     "moe_ffn_workspace_size", "moe_ffn_workspace_init", "moe_ffn_forward", "moe_ffn_forward_logits", "moe_ffn_forward_ex", "MoeFFNExtras",
     "moe_ffn_workspace_size_ex", "moe_ffn_router_topk", "moe_ffn_route", "moe_ffn_route_noalloc",
     "moe_ffn_sync_status", "moe_ffn_set_wait_limit_ns", "moe_ffn_profile_enable", "moe_ffn_profile_read", "moe_ffn_profile_stage_kernel", "moe_ffn_set_option", "MOE_OPT_GATHER", "moe_ffn_prepare_mxfp8_weights", "moe_ffn_widen_mxfp4_weights", "moe_ffn_debug_mx_quantize", "moe_ffn_status_string", "alloc_workspace",
 ]
 
-MOE_BF16, MOE_MXFP8 = 0, 1
+MOE_BF16, MOE_MXFP8, MOE_MXFP4W = 0, 1, 2
 MOE_FUSED, MOE_SPLIT = 0, 1
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_MISALIGNED",
                 4: "MOE_ERR_BAD_ROUTING", 5: "MOE_ERR_WORKSPACE_TOO_SMALL", 6: "MOE_ERR_DEVICE_TIMEOUT",
@@ -130,9 +130,10 @@ def _need(t, nbytes, name):
 
 def _need_forward(x, x_sf, w1, w1_sf, w2, w2_sf, topk_ids, topk_w, out, T, E, D, H, k, dtype):
     eb = 2 if dtype == MOE_BF16 else 1
+    wb = 0.5 if dtype == MOE_MXFP4W else eb    # packed E2M1 weights: two codes per byte
     _need(x, T * D * eb, "x")
-    _need(w1, E * 2 * H * D * eb, "w1")
-    _need(w2, E * D * H * eb, "w2")
+    _need(w1, E * 2 * H * D * wb, "w1")
+    _need(w2, E * D * H * wb, "w2")
     _need(out, T * D * 2, "out")
     _need(topk_ids, T * k * 4, "topk_ids")
     _need(topk_w, T * k * 4, "topk_w")

@@ -96,6 +96,22 @@ bool make_map_bf16(CUtensorMap* m, const void* base, uint64_t rows, uint64_t col
 bool make_map_fp8(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   return make_map_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, rows, cols, box_rows);
 }
+// E2M1 codes [rows, cols], two per byte (element 2j in the low four bits of
+// byte j), loaded in boxes of [box_rows, 128 codes] into 128-byte swizzled
+// shared-memory rows, every 16 codes (8 bytes) in a 16-byte slot
+// (16U4_ALIGN16B: base 32-byte aligned, cols a multiple of 128).
+bool make_map_fp4(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols / 2};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 
 int num_sms() {
   int dev = 0, n = 0;
@@ -173,7 +189,7 @@ Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipe
   w.blk_base = reinterpret_cast<int*>(take(sizeof(int) * (size_t)w.route_blocks * E));
   if (pipeline == kRouteOnly) {
     // routing regions only
-  } else if (dtype == MOE_MXFP8) {
+  } else if (dtype != MOE_BF16) {  // MXFP8 activations (e4m3 weights, or MXFP4 weights)
     w.xg = take((size_t)w.S_max * D);
     w.xg_sf = take((size_t)w.S_max * D / 32);
     if (pipeline == MOE_SPLIT) {
@@ -345,12 +361,13 @@ moe_status_t forward_fused_bf16(const Workspace& ws, const void* x, const void* 
 moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void* x_sf, const void* w1,
                                  const void* w1_sf, const void* w2, const void* w2_sf, const int32_t* topk_ids,
                                  const float* topk_w, void* out, int T, int E, int D, int H, int k, int sms,
-                                 cudaStream_t st) {
+                                 cudaStream_t st, bool fp4w) {
   CUtensorMap map_xg, map_w1, map_act, map_w2;
+  auto make_w = fp4w ? make_map_fp4 : make_map_fp8;
   if (!make_map_fp8(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, kBM) ||
-      !make_map_fp8(&map_w1, w1, (uint64_t)E * 2 * H, (uint64_t)D, 128) ||
+      !make_w(&map_w1, w1, (uint64_t)E * 2 * H, (uint64_t)D, 128) ||
       !make_map_fp8(&map_act, ws.act, (uint64_t)ws.S_max, (uint64_t)H, kBM) ||
-      !make_map_fp8(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, 256))
+      !make_w(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, 256))
     return MOE_ERR_CUDA;
   prof_mark(st, 0);
   cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st, nullptr, 0, 0, !g_prof.on);
@@ -386,9 +403,11 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
   up.n_col_tiles = H / 128;
   up.k_blocks = D / 128;
   prof_front(true);
-  prof_kernel(2, "up_swiglu_mxfp8");
-  prof_kernel(3, acc ? "down_reduce_mxfp8+f32_to_bf16" : "down_reduce_mxfp8");
-  e = launch_up_mxfp8(map_xg, map_w1, up, (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * up.n_col_tiles), st);
+  prof_kernel(2, fp4w ? "up_swiglu_mxfp4w" : "up_swiglu_mxfp8");
+  prof_kernel(3, fp4w ? (acc ? "down_reduce_mxfp4w+f32_to_bf16" : "down_reduce_mxfp4w")
+                      : (acc ? "down_reduce_mxfp8+f32_to_bf16" : "down_reduce_mxfp8"));
+  e = launch_up_mxfp8(map_xg, map_w1, up, (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * up.n_col_tiles), st,
+                      fp4w);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 3);
   MxArgs dn = ma;
@@ -397,7 +416,7 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
   dn.n_col_tiles = D / 256;
   dn.k_blocks = H / 128;
   e = launch_down_mxfp8(map_act, map_w2, dn, (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * dn.n_col_tiles), st,
-                        !g_prof.on);
+                        !g_prof.on, fp4w);
   if (e == cudaSuccess && acc) e = launch_f32_to_bf16(acc, out, (int64_t)T * D, sms * 4, st);
   prof_mark(st, 4);
   return cuda_status(e);
@@ -540,7 +559,7 @@ using namespace moe;
 extern "C" {
 
 size_t moe_ffn_workspace_size(int T, int E, int D, int H, int k, int dtype, int pipeline) {
-  if (!shape_ok(T, E, D, H, k) || (dtype != MOE_BF16 && dtype != MOE_MXFP8) ||
+  if (!shape_ok(T, E, D, H, k) || (dtype != MOE_BF16 && dtype != MOE_MXFP8 && dtype != MOE_MXFP4W) ||
       (pipeline != MOE_FUSED && pipeline != MOE_SPLIT))
     return 0;
   return plan_workspace(nullptr, T, E, D, H, k, pipeline, dtype).bytes;
@@ -693,13 +712,17 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
                                   size_t workspace_bytes, void* stream, const float* router_logits,
                                   float swiglu_limit = 0.f) {
   if (!shape_ok(T, E, D, H, k)) return MOE_ERR_INVALID_ARG;
-  if (dtype != MOE_BF16 && dtype != MOE_MXFP8) return MOE_ERR_INVALID_ARG;
+  if (dtype != MOE_BF16 && dtype != MOE_MXFP8 && dtype != MOE_MXFP4W) return MOE_ERR_INVALID_ARG;
   if (pipeline != MOE_FUSED && pipeline != MOE_SPLIT) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!x || !w1 || !w2 || !topk_ids || !topk_w || !out || !workspace) return MOE_ERR_INVALID_ARG;
   if (dtype == MOE_BF16 && (x_sf || w1_sf || w2_sf)) return MOE_ERR_INVALID_ARG;
-  if (dtype == MOE_MXFP8 && (!x_sf || !w1_sf || !w2_sf)) return MOE_ERR_INVALID_ARG;
-  if (dtype == MOE_MXFP8 && ((reinterpret_cast<uintptr_t>(x_sf) & 3u) || !aligned16(w1_sf) || !aligned16(w2_sf)))
+  if (dtype != MOE_BF16 && (!x_sf || !w1_sf || !w2_sf)) return MOE_ERR_INVALID_ARG;
+  if (dtype != MOE_BF16 && ((reinterpret_cast<uintptr_t>(x_sf) & 3u) || !aligned16(w1_sf) || !aligned16(w2_sf)))
+    return MOE_ERR_MISALIGNED;
+  // packed 4-bit weights: split pipeline only; their tensor maps want 32-byte aligned bases
+  if (dtype == MOE_MXFP4W && pipeline != MOE_SPLIT) return MOE_ERR_UNSUPPORTED;
+  if (dtype == MOE_MXFP4W && (((reinterpret_cast<uintptr_t>(w1) | reinterpret_cast<uintptr_t>(w2)) & 31u) != 0))
     return MOE_ERR_MISALIGNED;
   if (!aligned16(x) || !aligned16(w1) || !aligned16(w2) || !aligned16(out) || !aligned16(workspace) ||
       (reinterpret_cast<uintptr_t>(topk_ids) & 3u) || (reinterpret_cast<uintptr_t>(topk_w) & 3u))
@@ -714,14 +737,15 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
   // the up projection's weights, from the first expert on (its first tiles)
   ws.prefetch_base = w1;
   ws.prefetch_bytes = std::min<int64_t>((int64_t)g_prefetch_mb.load() << 20,
-                                        (int64_t)E * 2 * H * D * (dtype == MOE_MXFP8 ? 1 : 2)) & ~(int64_t)15;
+                                        (int64_t)E * 2 * H * D * (dtype == MOE_BF16 ? 2 : 1)) & ~(int64_t)15;
   const int sms = num_sms();
   if (sms <= 0) return MOE_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dtype == MOE_MXFP8 && pipeline == MOE_FUSED)
     return forward_fused_mxfp8(ws, x, x_sf, w1, w1_sf, w2, w2_sf, topk_ids, topk_w, out, T, E, D, H, k, sms, st);
-  if (dtype == MOE_MXFP8)
-    return forward_split_mxfp8(ws, x, x_sf, w1, w1_sf, w2, w2_sf, topk_ids, topk_w, out, T, E, D, H, k, sms, st);
+  if (dtype != MOE_BF16)
+    return forward_split_mxfp8(ws, x, x_sf, w1, w1_sf, w2, w2_sf, topk_ids, topk_w, out, T, E, D, H, k, sms, st,
+                               dtype == MOE_MXFP4W);
   if (pipeline == MOE_FUSED) return forward_fused_bf16(ws, x, w1, w2, topk_ids, topk_w, out, T, E, D, H, k, sms, st);
 
   const int gather = g_gather_mode.load();
@@ -926,7 +950,7 @@ static size_t ex_workspace_bytes(int T, int E, int D, int H, int k, int n_shared
 
 size_t moe_ffn_workspace_size_ex(int T, int E, int D, int H, int k, int n_shared, int dtype, int pipeline) {
   if (n_shared < 0 || E + n_shared > kMaxExperts || !shape_ok(T, E + n_shared, D, H, k + n_shared) ||
-      (dtype != MOE_BF16 && dtype != MOE_MXFP8) || (pipeline != MOE_FUSED && pipeline != MOE_SPLIT))
+      (dtype != MOE_BF16 && dtype != MOE_MXFP8 && dtype != MOE_MXFP4W) || (pipeline != MOE_FUSED && pipeline != MOE_SPLIT))
     return 0;
   return ex_workspace_bytes(T, E, D, H, k, n_shared, dtype, pipeline, nullptr);
 }

@@ -35,12 +35,21 @@ constexpr int kMxThreads = 64 + 256;   // producer warp, MMA warp, 8 epilogue wa
 constexpr int kMxEpi = 256;            // two warps per TMEM lane quadrant, one per column half
 constexpr uint64_t kMxDrainNs = 200ull * 1000 * 1000;
 
-template <int MODE, int STAGES>
+// FP4W: the weights (B operand) are MXFP4, E2M1 codes packed two per byte in
+// global memory.  Their tensor map (16U4_ALIGN16B) spreads each 16 codes (8
+// bytes) over a 16-byte slot of shared memory, so a B tile keeps the e4m3
+// tile's geometry (128 K elements per 128-byte swizzled row, "Porting
+// Block-Scaled GEMM Kernels" sec. 2.1: on sm_103a kind::mxf8f6f4 reads a 4-bit
+// operand next to an 8-bit one from such 1-byte-per-element containers),
+// while only the packed bytes cross from global memory: they are what the
+// stage's transaction count expects.  The instruction descriptor gives B the
+// E2M1 code of kind::mxf8f6f4, 5 (sec. 2.3).
+template <int MODE, int STAGES, int FP4W = 0>
 struct MxCfg {
   static constexpr int kA = kBM * kMxBK;          // 16 KB
-  static constexpr int kB = kMxN * kMxBK;         // 32 KB
+  static constexpr int kB = kMxN * kMxBK;         // 32 KB of shared memory
   static constexpr int kSF = 512 * 3;             // SFA tile + two SFB tiles
-  static constexpr int kTx = kA + kB + kSF;
+  static constexpr int kTx = kA + (FP4W ? kB / 2 : kB) + kSF;
   // DOWN: each epilogue thread stages half an output row (128 bf16, +16 B so
   // a warp's rows fall on distinct banks) for its bulk reduction.
   static constexpr int kStageRowBytes = kMxN + 16;
@@ -60,11 +69,11 @@ __device__ __forceinline__ float mx_swiglu(float g, float u, float lim) {
   return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
-template <int MODE, int STAGES>
+template <int MODE, int STAGES, int FP4W = 0>
 __global__ void __launch_bounds__(kMxThreads, 1)
     grouped_gemm_mxfp8_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                               const MxArgs args) {
-  using Cfg = MxCfg<MODE, STAGES>;
+  using Cfg = MxCfg<MODE, STAGES, FP4W>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -160,7 +169,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = idesc_mxf8(kBM, kMxN);
+    constexpr uint32_t idesc = idesc_mxf8(kBM, kMxN) | (FP4W ? kFmtE2M1 << 10 : 0u);
     int s = 0;
     uint32_t ph = 0;
     bool ok = true;
@@ -306,11 +315,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   }
 }
 
-template <int MODE, int STAGES>
+template <int MODE, int STAGES, int FP4W = 0>
 cudaError_t launch_mx(const CUtensorMap& a, const CUtensorMap& b, const MxArgs& args, int grid, cudaStream_t stream,
                       bool pdl) {
-  using Cfg = MxCfg<MODE, STAGES>;
-  auto kern = grouped_gemm_mxfp8_kernel<MODE, STAGES>;
+  using Cfg = MxCfg<MODE, STAGES, FP4W>;
+  auto kern = grouped_gemm_mxfp8_kernel<MODE, STAGES, FP4W>;
   // once per device: not a stream operation, so it stays out of graph capture
   static bool smem_set[64] = {};
   int dev = 0;
@@ -439,11 +448,13 @@ __global__ void mx_quantize_kernel(const float* __restrict__ in, int64_t n_block
 }  // namespace
 
 cudaError_t launch_up_mxfp8(const CUtensorMap& a, const CUtensorMap& w1, const MxArgs& args, int grid,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, bool fp4w) {
+  if (fp4w) return launch_mx<kMxUp, 4, 1>(a, w1, args, grid, stream, false);
   return launch_mx<kMxUp, 4>(a, w1, args, grid, stream, false);
 }
 cudaError_t launch_down_mxfp8(const CUtensorMap& act, const CUtensorMap& w2, const MxArgs& args, int grid,
-                              cudaStream_t stream, bool pdl) {
+                              cudaStream_t stream, bool pdl, bool fp4w) {
+  if (fp4w) return launch_mx<kMxDown, 3, 1>(act, w2, args, grid, stream, pdl);
   return launch_mx<kMxDown, 3>(act, w2, args, grid, stream, pdl);
 }
 cudaError_t launch_gather_mx(const Workspace& ws, const void* x, const void* x_sf, const int32_t* topk_ids, int T,

@@ -268,10 +268,11 @@ struct MxArgs {
   float swiglu_limit;       // > 0: gate clamped to <= limit, up to [-limit, limit] before SwiGLU
 };
 
+// fp4w: the weight maps are MXFP4 (16U4_ALIGN16B tensor maps of packed E2M1 codes).
 cudaError_t launch_up_mxfp8(const CUtensorMap& a, const CUtensorMap& w1, const MxArgs& args, int grid,
-                            cudaStream_t stream);
+                            cudaStream_t stream, bool fp4w = false);
 cudaError_t launch_down_mxfp8(const CUtensorMap& act, const CUtensorMap& w2, const MxArgs& args, int grid,
-                              cudaStream_t stream, bool pdl);
+                              cudaStream_t stream, bool pdl, bool fp4w = false);
 cudaError_t launch_gather_mx(const Workspace& ws, const void* x, const void* x_sf, const int32_t* topk_ids, int T,
                              int E, int k, int D, void* out, int64_t out_bytes, int grid, cudaStream_t stream,
                              bool pdl);

@@ -93,6 +93,10 @@ __device__ __forceinline__ void umma_mxf8(uint32_t d_tmem, uint64_t a_desc, uint
 __host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N) {
   return ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 7) << 27);
 }
+// Format code of E2M1 (FP4) for an operand of kind::mxf8f6f4 (bits 7-9 for A,
+// 10-12 for B; "Porting Block-Scaled GEMM Kernels" sec. 2.3: 5 under this
+// kind, while 1 would read as E5M2).
+constexpr uint32_t kFmtE2M1 = 5;
 __device__ __forceinline__ uint32_t idesc_with_sf_id(uint32_t idesc, uint32_t k_group) {
   return idesc | (k_group << 29) | (k_group << 4);
 }

@@ -52,6 +52,8 @@ WORKLOADS = {
     "prefill": Workload("prefill", 4096, 2048, 768, 128, 8, "topk_logits"),
     "large_skewed": Workload("large_skewed", 131072, 2048, 768, 128, 8, "zipf"),
     "mxfp8": Workload("mxfp8", 16384, 4096, 1536, 64, 8, "uniform", "mxfp8"),
+    # the decode shape with MXFP4 expert weights (MXFP8 activations)
+    "decode_mxfp4w": Workload("decode_mxfp4w", 64, 6144, 2048, 32, 8, "uniform", "mxfp4w"),
 }
 
 ZIPF_S = 1.1

@@ -54,7 +54,7 @@ typedef enum {
   MOE_ERR_CUDA = 7                 /* a CUDA runtime call failed */
 } moe_status_t;
 
-typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1 } moe_dtype_t;
+typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1, MOE_MXFP4W = 2 } moe_dtype_t;
 
 /* MOE_FUSED: one GEMM kernel per call, the activation never leaves the SM
  *            ("Prime Flash MoE" sec. 2 "Trick 2", sec. 4).
@@ -79,7 +79,18 @@ moe_status_t moe_ffn_workspace_init(void* workspace, size_t workspace_bytes, voi
  * ue8m0 scale byte s (value 2^(s-127)).  x_sf is row-major [T, D/32] (4-byte
  * aligned); w1_sf and w2_sf are the weight scales already repacked by
  * moe_ffn_prepare_mxfp8_weights.  The activation is requantized to MXFP8
- * (per 32 along H) between the two GEMMs; out stays bf16. */
+ * (per 32 along H) between the two GEMMs; out stays bf16.
+ *
+ * MOE_MXFP4W (split pipeline only; MOE_ERR_UNSUPPORTED for MOE_FUSED): x and
+ * its scales as for MOE_MXFP8; w1 [E, 2H, D/2] and w2 [E, D, H/2] hold MXFP4
+ * weights, E2M1 codes packed two per byte along the reduction dimension
+ * (element 2j in bits 0..3 of byte j), one ue8m0 scale per 32 elements
+ * (the routed-weight format of "GC-MoE on SM120" sec. 2.2), scales repacked by
+ * moe_ffn_prepare_mxfp8_weights as for MOE_MXFP8.  The codes stay 4-bit in
+ * HBM: the GEMMs read them with 4-bit tensor maps and multiply them as the
+ * E2M1 operand of kind::mxf8f6f4 ("Porting Block-Scaled GEMM Kernels from
+ * Blackwell to Rubin" sec. 2.1, 2.3).  w1 and w2 must be 32-byte aligned
+ * (MOE_ERR_MISALIGNED otherwise). */
 moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, const void* w1_sf, const void* w2,
                              const void* w2_sf, const int32_t* topk_ids, const float* topk_w, void* out, int T, int E,
                              int D, int H, int k, int dtype, int pipeline, void* workspace, size_t workspace_bytes,
@@ -166,7 +177,8 @@ moe_status_t moe_ffn_prepare_mxfp8_weights(const void* w1_sf, const void* w2_sf,
  * e4m3 codes of the same values (exact: every E2M1 value is an e4m3 value);
  * the scale arrays stay as they are and go through
  * moe_ffn_prepare_mxfp8_weights, and moe_ffn_forward then runs with
- * MOE_MXFP8.  The weights then occupy one byte per element in HBM, not half.
+ * MOE_MXFP8.  The weights then occupy one byte per element in HBM, not half;
+ * MOE_MXFP4W runs the packed codes as they are, at half a byte per element.
  *   w_fp4   n_elems/2 bytes, two codes per byte along the contiguous dimension:
  *           element 2j in bits 0..3 of byte j, element 2j+1 in bits 4..7;
  *           16-byte aligned (W1 [E, 2H, D/2] and W2 [E, D, H/2] row-major)

@@ -71,6 +71,16 @@ def test_forward_rejects_bad_arguments_on_host():
     assert call(*a) == 0                                   # T == 0: no-op
     a = list(base); a[17] = 16
     assert call(*a) in (5, 7)                              # workspace too small (or no device here)
+    # MXFP4 weights: scales required, split pipeline only, weights 32-byte aligned
+    mx4 = list(base); mx4[14] = 2; mx4[15] = 1; mx4[1] = mx4[3] = mx4[5] = A
+    a = list(mx4); a[3] = None
+    assert call(*a) == 1                                   # missing weight scales
+    a = list(mx4); a[15] = 0
+    assert call(*a) == 2                                   # fused pipeline: unsupported
+    a = list(mx4); a[2] = A + 16
+    assert call(*a) == 3                                   # w1 16- but not 32-byte aligned
+    assert moe.moe_ffn_workspace_size(64, 8, 256, 128, 2, moe.MOE_MXFP4W, moe.MOE_SPLIT) == \
+        moe.moe_ffn_workspace_size(64, 8, 256, 128, 2, moe.MOE_MXFP8, moe.MOE_SPLIT)
 
 
 def test_header_compiles_as_c_and_cpp():

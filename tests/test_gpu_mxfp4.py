@@ -1,8 +1,10 @@
 """MXFP4 expert weights ("GC-MoE on SM120" sec. 2.2: E2M1 codes with one
 UE8M0 scale per 32 elements) on the MXFP8 path: the device widening of the
-codes against e4m3 codes of the format's 16 values (bit-exact), and the
-forward pass on widened weights against the oracle's MXFP4 weight mode (act
-requantized per 32 along H on both sides) at the MXFP8 tolerances."""
+codes against e4m3 codes of the format's 16 values (bit-exact), the forward
+pass on widened weights, and the forward pass on the packed 4-bit codes
+themselves (MOE_MXFP4W: 4-bit tensor maps, E2M1 as the B operand of
+kind::mxf8f6f4), each against the oracle's MXFP4 weight mode (act requantized
+per 32 along H on both sides) at the MXFP8 tolerances."""
 import numpy as np
 import pytest
 import torch
@@ -58,3 +60,49 @@ def test_mxfp4_weights_forward(T, D, H, E, k, routing, pipeline):
                          x_sf=inp["x_sf"], w1_sf=inp["w1_sf"], w2_sf=inp["w2_sf"], fp4_weights=True)
     r = assert_close(out, ref, dtype="mxfp8", label=f"mxfp4 weights T={T} D={D} H={H}")
     print(f"mxfp4 weights pipeline={pipeline} T={T} D={D} H={H} E={E} k={k}: max_rel={r[0]:.2e} mean_rel={r[1]:.2e}")
+
+
+def run_mx4(inp):
+    """moe_ffn_forward with MOE_MXFP4W: the packed codes as they are."""
+    w = inp["workload"]
+    dev = {k: torch.from_numpy(np.ascontiguousarray(inp[k])).cuda() for k in ("x", "x_sf", "w1", "w2")}
+    w1p = torch.empty(inp["w1_sf"].size, dtype=torch.uint8, device="cuda")
+    w2p = torch.empty(inp["w2_sf"].size, dtype=torch.uint8, device="cuda")
+    moe.moe_ffn_prepare_mxfp8_weights(torch.from_numpy(inp["w1_sf"]).cuda(), torch.from_numpy(inp["w2_sf"]).cuda(),
+                                      w1p, w2p, w.E, w.D, w.H)
+    ids = torch.from_numpy(inp["topk_ids"]).cuda()
+    tw = torch.from_numpy(inp["topk_w"]).cuda()
+    out = torch.full((w.T, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = moe.alloc_workspace(w.T, w.E, w.D, w.H, w.k, moe.MOE_MXFP4W, moe.MOE_SPLIT)
+    moe.moe_ffn_forward(dev["x"], dev["w1"], dev["w2"], ids, tw, out, E=w.E, D=w.D, H=w.H, k=w.k, workspace=ws,
+                        dtype=moe.MOE_MXFP4W, pipeline=moe.MOE_SPLIT, x_sf=dev["x_sf"], w1_sf=w1p, w2_sf=w2p)
+    st = moe.moe_ffn_sync_status(ws)
+    assert st == 0, moe.moe_ffn_status_string(st)
+    return out
+
+
+@pytest.mark.parametrize("T,D,H,E,k,routing", [
+    (64, 256, 128, 8, 2, "topk_logits"),
+    (300, 512, 256, 16, 4, "uniform"),
+    (1, 256, 384, 4, 4, "uniform"),
+    (129, 768, 256, 40, 8, "zipf"),          # several experts empty
+    (100, 256, 256, 64, 32, "uniform"),      # k = 32: rows of a token summed in fp32
+])
+def test_mxfp4_packed_weights_forward(T, D, H, E, k, routing):
+    inp = wl.make_custom(T, D, H, E, k, seed=T + H, routing=routing, dtype="mxfp4w")
+    out = run_mx4(inp)
+    ref = oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], inp["topk_ids"], inp["topk_w"], act=oracle.ACT_MXFP8,
+                         x_sf=inp["x_sf"], w1_sf=inp["w1_sf"], w2_sf=inp["w2_sf"], fp4_weights=True)
+    r = assert_close(out, ref, dtype="mxfp8", label=f"packed mxfp4 weights T={T} D={D} H={H} E={E} k={k}")
+    print(f"packed mxfp4 T={T} D={D} H={H} E={E} k={k}: max_rel={r[0]:.2e} mean_rel={r[1]:.2e} cos={r[2]:.6f}")
+
+
+def test_mxfp4_packed_weights_decode_workload():
+    """The decode workload's shape (T=64, D=6144, H=2048, E=32, k=8) with MXFP4
+    weights, every token checked: the weight stream that 4-bit codes halve."""
+    inp = wl.make_inputs("decode_mxfp4w", seed=0)
+    out = run_mx4(inp)
+    ref = oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], inp["topk_ids"], inp["topk_w"], act=oracle.ACT_MXFP8,
+                         x_sf=inp["x_sf"], w1_sf=inp["w1_sf"], w2_sf=inp["w2_sf"], fp4_weights=True)
+    r = assert_close(out, ref, dtype="mxfp8", label="packed mxfp4 weights, decode workload")
+    print(f"packed mxfp4 decode: max_rel={r[0]:.2e} mean_rel={r[1]:.2e} cos={r[2]:.6f}")
