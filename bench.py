@@ -135,6 +135,7 @@ KERNEL_SOURCES = {
     "up_swiglu_mxfp4w": ["grouped_gemm_gb300/csrc/gemm_mxfp8.cu"] + _MXH + _PTX,
     "down_reduce_mxfp4w": ["grouped_gemm_gb300/csrc/gemm_mxfp8.cu"] + _MXH + _PTX,
     "fused_cluster_bf16": ["grouped_gemm_gb300/csrc/gemm_fused_cluster.cu"] + _PTX,
+    "fused_dsmem_bf16": ["grouped_gemm_gb300/csrc/gemm_fused_dsmem.cu"] + _PTX,
     "fused_moe_bf16": ["grouped_gemm_gb300/csrc/gemm_fused.cu"] + _PTX,
     "fused_cluster_mxfp8": ["grouped_gemm_gb300/csrc/gemm_fused_cluster_mx.cu"] + _MXH + _PTX,
     "fused_moe_mxfp8": ["grouped_gemm_gb300/csrc/gemm_fused_mx.cu"] + _MXH + _PTX,

@@ -339,6 +339,7 @@ MOE_OPT_ROUTER_FUSED = 14
 MOE_OPT_PREFETCH_MB = 15
 MOE_OPT_WIDE_UP = 16
 MOE_OPT_TILE_M = 17
+MOE_OPT_FUSED_DSMEM = 18
 
 
 def moe_ffn_set_option(option: int, value: int) -> int:

@@ -40,6 +40,7 @@ std::atomic<int> g_l2_policy{0};      // MOE_OPT_L2_POLICY: bit 0 weights evict_
 std::atomic<int> g_prefetch_mb{0};    // MOE_OPT_PREFETCH_MB: weights prefetched into L2 during routing
 std::atomic<int> g_pair_swap{0};      // MOE_OPT_PAIR_SWAP: max routed rows of a swap-AB pair tile (measured slower: off)
 std::atomic<int> g_wide_up{0};        // MOE_OPT_WIDE_UP: 512-column up tiles on CTA pairs
+std::atomic<int> g_fused_dsmem{0};    // MOE_OPT_FUSED_DSMEM: act kept in shared memory in the cluster kernel (measured slower: off)
 std::atomic<int> g_tile_m{0};         // MOE_OPT_TILE_M: rows per tile of the single-CTA split GEMMs (0 automatic)
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -233,15 +234,16 @@ namespace {
 // act columns, i.e. more operand bytes per FLOP, and for single-CTA clusters,
 // which measured slower on GB300 than their share).  The row-block count is
 // estimated from the routed pairs (half a padded block per live expert).
-int choose_cluster_size(int D, int H, int64_t pairs, int E, int max_rb) {
+int choose_cluster_size(int D, int H, int64_t pairs, int E, int max_rb, bool dsmem) {
   const int64_t live = std::min<int64_t>(pairs, E);
   const int64_t est_rb = std::min<int64_t>(max_rb, std::max<int64_t>(live, (pairs + kBM - 1) / kBM + live / 2));
   int best = 0;
   double best_cost = 0;
   for (int C : {1, 2, 4, 8}) {
     const int h1 = fused_cluster_h1(D, H, C);
-    if (!h1) continue;
-    const int ncl = std::min(fused_cluster_max_clusters(C), kFusedClusterMaxCtas / C);
+    if (!h1 || (dsmem && !fused_dsmem_fits(D, H, C))) continue;
+    const int ncl = std::min(dsmem ? fused_dsmem_max_clusters(C) : fused_cluster_max_clusters(C),
+                             kFusedClusterMaxCtas / C);
     if (ncl <= 0) continue;
     const double waves = (double)((est_rb + ncl - 1) / ncl);
     const double narrow = h1 == 128 ? 1.0 : h1 == 96 ? 1.1 : h1 == 64 ? 1.25 : 1.6;
@@ -259,16 +261,17 @@ int choose_cluster_size(int D, int H, int64_t pairs, int E, int max_rb) {
 // ring and reduce finished rows into out.
 moe_status_t forward_fused_cluster_bf16(const Workspace& ws, const void* x, const void* w1, const void* w2,
                                         const int32_t* topk_ids, const float* topk_w, void* out, int T, int E, int D,
-                                        int H, int k, int sms, int C, cudaStream_t st) {
+                                        int H, int k, int sms, int C, bool dsmem, cudaStream_t st) {
   const int h1 = fused_cluster_h1(D, H, C);
   const int ncl_cap = kFusedClusterMaxCtas / C;
-  const int ncl = std::min(std::min(fused_cluster_max_clusters(C), ncl_cap), ws.max_rb);
+  const int ncl = std::min(std::min(dsmem ? fused_dsmem_max_clusters(C) : fused_cluster_max_clusters(C), ncl_cap),
+                           ws.max_rb);
   if (ncl <= 0 || !h1) return MOE_ERR_CUDA;
   CUtensorMap map_xg, map_w1, map_w2, map_ring;
   if (!make_map_bf16(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, kBM) ||
       !make_map_bf16(&map_w1, w1, (uint64_t)E * 2 * H, (uint64_t)D, (uint32_t)h1) ||
       !make_map_bf16(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, kFusedClusterN) ||
-      !make_map_bf16(&map_ring, ws.ring, (uint64_t)ncl_cap * 2 * kBM, (uint64_t)H, kBM))
+      (!dsmem && !make_map_bf16(&map_ring, ws.ring, (uint64_t)ncl_cap * 2 * kBM, (uint64_t)H, kBM)))
     return MOE_ERR_CUDA;
   prof_mark(st, 0);
   cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st, nullptr, 0, 0, !g_prof.on);
@@ -296,9 +299,10 @@ moe_status_t forward_fused_cluster_bf16(const Workspace& ws, const void* x, cons
   fa.stall_test = g_stall_test.load() == 1 ? 1 : 0;
   fa.swiglu_limit = ws.swiglu_limit;
   prof_front(false);
-  prof_kernel(2, "fused_cluster_bf16");
+  prof_kernel(2, dsmem ? "fused_dsmem_bf16" : "fused_cluster_bf16");
   prof_kernel(3, "none");
-  e = launch_fused_cluster_bf16(map_xg, map_w1, map_w2, map_ring, fa, ncl, st);
+  e = dsmem ? launch_fused_dsmem_bf16(map_xg, map_w1, map_w2, fa, ncl, st)
+            : launch_fused_cluster_bf16(map_xg, map_w1, map_w2, map_ring, fa, ncl, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 3);
   prof_mark(st, 4);  // no rounding pass: out is reduced in bf16 directly
@@ -314,9 +318,17 @@ moe_status_t forward_fused_bf16(const Workspace& ws, const void* x, const void* 
   // the cluster kernel reduces finished rows into out in bf16; for large k
   // the split-K kernel's fp32 accumulator is taken instead
   if (opt && fused_cluster_ok(D, H) && !f32_accum(k)) {
-    int C = (opt > 1 && fused_cluster_h1(D, H, opt)) ? opt : 0;
-    if (!C) C = choose_cluster_size(D, H, (int64_t)T * k, E, ws.max_rb);
-    if (C) return forward_fused_cluster_bf16(ws, x, w1, w2, topk_ids, topk_w, out, T, E, D, H, k, sms, C, st);
+    // act kept in shared memory where a cluster size allows it, else the L2 ring
+    bool dsmem = false;
+    int C = 0;
+    if (g_fused_dsmem.load()) {
+      C = (opt > 1 && fused_dsmem_fits(D, H, opt)) ? opt : 0;
+      if (!C && opt == 1) C = choose_cluster_size(D, H, (int64_t)T * k, E, ws.max_rb, true);
+      dsmem = C != 0;
+    }
+    if (!C) C = (opt > 1 && fused_cluster_h1(D, H, opt)) ? opt : 0;
+    if (!C) C = choose_cluster_size(D, H, (int64_t)T * k, E, ws.max_rb, false);
+    if (C) return forward_fused_cluster_bf16(ws, x, w1, w2, topk_ids, topk_w, out, T, E, D, H, k, sms, C, dsmem, st);
   }
   CUtensorMap map_xg, map_w1, map_w2;
   if (!make_map_bf16(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, kBM) ||
@@ -621,6 +633,10 @@ moe_status_t moe_ffn_set_option(int option, long long value) {
     case MOE_OPT_PAIR_SWAP:
       if (value < 0 || value > 256) return MOE_ERR_INVALID_ARG;
       g_pair_swap.store((int)value);
+      return MOE_OK;
+    case MOE_OPT_FUSED_DSMEM:
+      if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
+      g_fused_dsmem.store((int)value);
       return MOE_OK;
     case MOE_OPT_TILE_M:
       if (value != 0 && value != 64 && value != 128) return MOE_ERR_INVALID_ARG;

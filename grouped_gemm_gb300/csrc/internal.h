@@ -241,6 +241,18 @@ cudaError_t launch_fused_cluster_mxfp8(const CUtensorMap& map_xg, const CUtensor
                                        const CUtensorMap& map_w2, const CUtensorMap& map_ring,
                                        const FusedClusterMxArgs& args, int n_clusters, cudaStream_t stream);
 
+// The fused pipeline on clusters with act kept in shared memory: each CTA's
+// act slice (h = H / C columns, a multiple of 64, at most 256) stays in its own
+// shared memory and GEMM2's K tiles move between the cluster's CTAs by
+// shared-to-shared bulk copies.  h1 / s1 / s2 as for the ring kernel.
+inline bool fused_dsmem_fits(int D, int H, int C) {
+  if (!fused_cluster_h1(D, H, C)) return false;
+  const int h = H / C;
+  return h % 64 == 0 && h <= 256;
+}
+int fused_dsmem_max_clusters(int csize);
+cudaError_t launch_fused_dsmem_bf16(const CUtensorMap& map_xg, const CUtensorMap& map_w1, const CUtensorMap& map_w2,
+                                    const FusedClusterArgs& args, int n_clusters, cudaStream_t stream);
 // Co-resident clusters of size csize on the current device (0 on failure).
 int fused_cluster_max_clusters(int csize);
 cudaError_t launch_fused_cluster_bf16(const CUtensorMap& map_xg, const CUtensorMap& map_w1, const CUtensorMap& map_w2,

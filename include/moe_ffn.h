@@ -416,6 +416,22 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   decode (16 rows per expert): step 0.410 ms with 128,
  *                   0.387 with 64 (up kernel 0.266 -> 0.250 ms, 0.97 of the
  *                   measured HBM copy rate).
+ *   MOE_OPT_FUSED_DSMEM  0 (default) or 1: with 1 the bf16 fused pipeline on
+ *                   clusters keeps act in shared memory (each CTA's slice of
+ *                   H / C columns; the producer warp of every CTA copies the
+ *                   other CTAs' K tiles of GEMM2's A operand from their shared
+ *                   memory into its own pipeline stages) whenever a cluster
+ *                   size gives slices of 64 to 256 columns in steps of 64;
+ *                   0, or any other shape, exchanges act through an
+ *                   L2-resident ring in global memory instead.  Measured on
+ *                   GB300 (fused GEMM kernel): decode 1.19 against 0.41 ms,
+ *                   prefill 0.85 against 0.37 ms, large_skewed 19.4 against
+ *                   7.1 ms (three pipeline stages where the ring kernel has
+ *                   four, and every CTA copies (C - 1) / C of the act K tiles
+ *                   once per 256 output columns); a first form in which each
+ *                   owner pushed its tiles into the other CTAs' stages by
+ *                   shared-to-shared bulk copies, with a handshake per tile,
+ *                   measured 1.26 / 0.66 / 15.9 ms.
  *   (MOE_OPT_L2_POLICY measured at prefill: 0.343 ms with 0, 0.349 with 1,
  *                   0.342 with 2, 0.348 with 3: no gain, off.) */
 typedef enum {
@@ -436,7 +452,8 @@ typedef enum {
   MOE_OPT_ROUTER_FUSED = 14,
   MOE_OPT_PREFETCH_MB = 15,
   MOE_OPT_WIDE_UP = 16,
-  MOE_OPT_TILE_M = 17
+  MOE_OPT_TILE_M = 17,
+  MOE_OPT_FUSED_DSMEM = 18
 } moe_option_t;
 moe_status_t moe_ffn_set_option(int option, long long value);
 

@@ -25,8 +25,8 @@ pytestmark = pytest.mark.gpu
 # both GEMMs on CTA pairs (down tiles never swap-AB by default, or swap-AB for
 # small pairs, or always; the up projection in 512-column tiles); the
 # single-CTA GEMMs with 64-row tiles; the
-# fused pipeline on clusters (default where the shape allows) and with the
-# H-split fp32 partial sums.
+# fused pipeline on clusters (default where the shape allows; act through the
+# L2 ring, or kept in shared memory) and with the H-split fp32 partial sums.
 MODES = {
     "split": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 0, moe.MOE_OPT_TILE_M: 128}),
     "split_pairs": (moe.MOE_SPLIT, {moe.MOE_OPT_UP_PAIRS: 1}),
@@ -39,10 +39,12 @@ MODES = {
     "split_wide": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 1, moe.MOE_OPT_WIDE_UP: 1}),
     "split_m64": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 0, moe.MOE_OPT_TILE_M: 64}),
     "fused": (moe.MOE_FUSED, {}),
+    "fused_dsmem": (moe.MOE_FUSED, {moe.MOE_OPT_FUSED_DSMEM: 1}),
     "fused_splitk": (moe.MOE_FUSED, {moe.MOE_OPT_FUSED_CLUSTER: 0}),
 }
 DEFAULTS = {moe.MOE_OPT_UP_PAIRS: 0, moe.MOE_OPT_GATHER: 0, moe.MOE_OPT_SWAP_AB: 0, moe.MOE_OPT_FUSED_CLUSTER: 1,
-            moe.MOE_OPT_PAIR_MMA: 2, moe.MOE_OPT_PAIR_SWAP: 0, moe.MOE_OPT_WIDE_UP: 0, moe.MOE_OPT_TILE_M: 0}
+            moe.MOE_OPT_PAIR_MMA: 2, moe.MOE_OPT_PAIR_SWAP: 0, moe.MOE_OPT_WIDE_UP: 0, moe.MOE_OPT_TILE_M: 0,
+            moe.MOE_OPT_FUSED_DSMEM: 0}
 PIPELINES = list(MODES)
 
 
@@ -86,6 +88,7 @@ def test_forward_small(T, D, H, E, k, routing, pipeline):
     print(f"{pipeline} T={T} D={D} H={H} E={E} k={k}: max_rel={r[0]:.2e} mean_rel={r[1]:.2e} cos={r[2]:.6f}")
 
 
+@pytest.mark.parametrize("dsmem", [1, 0])          # act in shared memory where the slice fits; the L2 ring
 @pytest.mark.parametrize("csize", [1, 2, 4, 8])   # 1: automatic
 @pytest.mark.parametrize("T,D,H,E,k", [
     (150, 512, 128, 8, 2),      # 64 or 128 act columns per CTA
@@ -93,17 +96,20 @@ def test_forward_small(T, D, H, E, k, routing, pipeline):
     (200, 2048, 256, 32, 8),    # 32 act columns per CTA with clusters of 8
     (1000, 2048, 768, 8, 8),    # prefill dims, ~8 row blocks per expert: each ring buffer reused
 ])
-def test_fused_cluster_shapes(T, D, H, E, k, csize):
+def test_fused_cluster_shapes(T, D, H, E, k, csize, dsmem):
     if csize > 1 and (D % (256 * csize) or (H // csize) % 32):
         pytest.skip("cluster size does not apply to this shape")
     inp = wl.make_custom(T, D, H, E, k, seed=T + H, routing="uniform")
     moe.moe_ffn_set_option(moe.MOE_OPT_FUSED_CLUSTER, csize)
+    moe.moe_ffn_set_option(moe.MOE_OPT_FUSED_DSMEM, dsmem)
     try:
         out, _ = run_forward(inp, to_dev(inp), pipeline=moe.MOE_FUSED)
     finally:
         moe.moe_ffn_set_option(moe.MOE_OPT_FUSED_CLUSTER, 1)
-    r = assert_close(out, oracle_out(inp), label=f"fused C={csize} T={T} D={D} H={H} E={E} k={k}")
-    print(f"fused C={csize} T={T} D={D} H={H} E={E} k={k}: max_rel={r[0]:.2e} mean_rel={r[1]:.2e} cos={r[2]:.6f}")
+        moe.moe_ffn_set_option(moe.MOE_OPT_FUSED_DSMEM, 0)
+    r = assert_close(out, oracle_out(inp), label=f"fused C={csize} dsmem={dsmem} T={T} D={D} H={H} E={E} k={k}")
+    print(f"fused C={csize} dsmem={dsmem} T={T} D={D} H={H} E={E} k={k}: max_rel={r[0]:.2e} mean_rel={r[1]:.2e} "
+          f"cos={r[2]:.6f}")
 
 
 @pytest.mark.parametrize("pipeline", PIPELINES)
@@ -159,8 +165,8 @@ def test_forward_full_workload_sampled(name, pipeline):
     """Full-size workloads: decode on every token; prefill and large_skewed on
     the first and last routed token of every expert, the first token of every
     expert's last row block, and 1000 seeded random tokens."""
-    if name == "large_skewed" and pipeline not in ("split", "fused", "fused_splitk", "split_pair2", "split_wide",
-                                                   "split_m64"):
+    if name == "large_skewed" and pipeline not in ("split", "fused", "fused_dsmem", "fused_splitk", "split_pair2",
+                                                   "split_wide", "split_m64"):
         pytest.skip("option variants are covered at the smaller sizes")
     inp = cached_inputs(name)
     out, _ = run_mode(inp, to_dev(inp), pipeline)

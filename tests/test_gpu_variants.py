@@ -25,9 +25,10 @@ MODES = {  # name: (pipeline, options)
     "split_wide": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 1, moe.MOE_OPT_WIDE_UP: 1}),
     "split_m64": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 0, moe.MOE_OPT_TILE_M: 64}),
     "fused": (moe.MOE_FUSED, {}),
+    "fused_dsmem": (moe.MOE_FUSED, {moe.MOE_OPT_FUSED_DSMEM: 1}),
     "fused_splitk": (moe.MOE_FUSED, {moe.MOE_OPT_FUSED_CLUSTER: 0}),
 }
-DEFAULTS = {moe.MOE_OPT_PAIR_MMA: 2, moe.MOE_OPT_FUSED_CLUSTER: 1, moe.MOE_OPT_WIDE_UP: 0, moe.MOE_OPT_TILE_M: 0}
+DEFAULTS = {moe.MOE_OPT_PAIR_MMA: 2, moe.MOE_OPT_FUSED_CLUSTER: 1, moe.MOE_OPT_WIDE_UP: 0, moe.MOE_OPT_TILE_M: 0, moe.MOE_OPT_FUSED_DSMEM: 0}
 
 
 def extended(ids, tw, E, ns):
