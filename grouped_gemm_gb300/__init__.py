@@ -340,6 +340,8 @@ MOE_OPT_PREFETCH_MB = 15
 MOE_OPT_WIDE_UP = 16
 MOE_OPT_TILE_M = 17
 MOE_OPT_FUSED_DSMEM = 18
+MOE_OPT_HALF_PAIR_M128 = 19
+MOE_OPT_ROUTE_SMALL_PAIRS = 20
 
 
 def moe_ffn_set_option(option: int, value: int) -> int:

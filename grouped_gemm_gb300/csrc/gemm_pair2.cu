@@ -17,9 +17,16 @@
 // DOWN (GEMM2 + weighted reduce): B = W2[e] rows j*256 + 128 * rank .. +128;
 //     the epilogue scales by the routing weight and reduces half rows into out
 //     with bulk .add.bf16.
-// Tiles are (block pair, column tile j); a pair whose second block does not
-// exist (an expert with an odd number of row blocks) still runs both CTAs: the
-// odd CTA loads the first block's rows again and stores nothing.
+// Tiles are (block pair, column tile j).  A pair whose second block does not
+// exist (an expert with an odd number of row blocks: a half pair) still runs
+// both CTAs.  UP: the odd CTA loads the first block's rows again and stores
+// nothing.  DOWN (args.half_m128): it runs as one M = 128 pair MMA, 64 rows of
+// the block in each CTA, so no tensor-core work goes to a missing block.
+// Measured layout of that shape: each CTA's 64 accumulator rows take all 128
+// TMEM lanes, lanes 0..63 holding columns [0, N/2) of rows 0..63 and lanes
+// 64..127 columns [N/2, N) of the same rows, so each lane reduces a half row.
+// (The same for UP, with [gate 64 | up 64] B tiles per CTA, measured the up
+// kernel 3-12% slower over all tiles and is not built.)
 //
 // Swap-AB pair tiles (DOWN, args.pair_swap_max > 0): a pair whose blocks hold
 // at most pair_swap_max routed rows -- typically a half pair, an expert's odd
@@ -154,14 +161,18 @@ __global__ void __launch_bounds__(kQThreads, 1)
     for (int tile = pair_slot; ok && tile < n_tiles; tile += n_pair_slots) {
       const int info = args.pair_info[tile / NJ], j = tile % NJ;
       const int rb0 = info >> 1, two = info & 1;
-      const int my_rb = rb0 + (int)(rank & (uint32_t)two);  // the odd CTA of a half pair reloads rb0
       const int e = args.expert_of_rb[rb0];
       const int brow = MODE == kPairUp ? e * 2 * args.H + (int)rank * args.H + j * 128
                                        : e * args.D + j * 256 + (int)rank * 128;
       // swap-AB: this CTA's half of the ns routed rows (the TMA box still moves
       // 128 rows; the MMA reads the first ns / 2)
       const int ns = MODE == kPairDown ? pair_swap_ns(args, info) : 0;
-      const int arow = ns ? rb0 * kBM + (int)rank * (ns >> 1) : my_rb * kBM;
+      // DOWN half pair (M = 128): this CTA's 64 rows of the block (the box
+      // moves 128 rows; the MMA reads the first 64)
+      const bool m128 = MODE == kPairDown && !two && !ns && args.half_m128;
+      const int arow = ns     ? rb0 * kBM + (int)rank * (ns >> 1)
+                       : m128 ? rb0 * kBM + (int)rank * 64
+                              : (rb0 + (int)(rank & (uint32_t)two)) * kBM;  // the odd CTA of a half pair reloads rb0
       for (int kb = 0; kb < KB; ++kb) {
         if (!(ok = mbar_wait(&empty[s], ph ^ 1u, wc, 61))) break;
         if (leader) mbar_arrive_expect_tx(&full[s], 2 * kQStage);
@@ -201,6 +212,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
       const uint32_t d_tmem = tmem_base + acc * 256;
       const int ns = MODE == kPairDown ? pair_swap_ns(args, args.pair_info[tile / NJ]) : 0;
       const uint32_t idesc_swap = idesc_bf16_f32(2 * kBM, ns ? ns : 16);
+      // DOWN: a half pair runs as one M = 128 pair MMA (64 rows in each CTA)
+      const bool m128_t = MODE == kPairDown && !ns && args.half_m128 && !(args.pair_info[tile / NJ] & 1);
       for (int kb = 0; kb < KB; ++kb) {
         if (!(ok = mbar_wait(&full[s], ph, wc, 63))) break;
         tc_fence_after();
@@ -210,6 +223,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             umma_bf16_pair(d_tmem, bdesc + 2 * kk, adesc + 2 * kk, idesc_swap, (kb | kk) != 0);
+        } else if (m128_t) {
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_bf16_pair(d_tmem, adesc + 2 * kk, bdesc + 2 * kk, idesc_bf16_f32(kBM, 256), (kb | kk) != 0);
         } else {
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
@@ -249,12 +266,53 @@ __global__ void __launch_bounds__(kQThreads, 1)
       if (!mbar_wait(&tfull[acc], (uint32_t)(it >> 1) & 1u, wc, 64)) break;
       tc_fence_after();
       const int info = args.pair_info[tile / NJ], j = tile % NJ;
-      const bool valid = rank == 0 || (info & 1);
-      const int64_t slot = (int64_t)((info >> 1) + (int)rank) * kBM + row;
-      const int tok = valid ? args.row_tok[slot] : -1;
       const uint32_t tacc = lane_base + acc * 256;
       const int ns = MODE == kPairDown ? pair_swap_ns(args, info) : 0;
-      if (MODE == kPairDown && ns > 0) {
+      const bool m128 = MODE == kPairDown && !(info & 1) && !ns && args.half_m128;
+      // m128: TMEM lane row (0..127) holds columns [128 * half, +128) of tile row
+      // (row & 63), the block's row rank * 64 + (row & 63)
+      const int half = row >> 6;
+      const int64_t slot = m128 ? (int64_t)(info >> 1) * kBM + (int)rank * 64 + (row & 63)
+                                : (int64_t)((info >> 1) + (int)rank) * kBM + row;
+      const int tok = (m128 || rank == 0 || (info & 1)) ? args.row_tok[slot] : -1;
+      const bool valid = tok >= 0;
+      if (MODE == kPairDown && m128) {
+        // output columns j*256 + 128*half .. +128 of the row
+        {
+          const float w = valid ? args.slot_w[slot] : 0.f;
+          uint32_t v[4][32];
+          tmem_ld_x32_pair(tacc, tacc + 32, v[0], v[1]);
+          tmem_ld_x32_pair(tacc + 64, tacc + 96, v[2], v[3]);
+          if (tok >= 0) {
+            const int64_t col0 = (int64_t)tok * args.D + j * 256 + half * 128;
+            if (args.out_f32) {
+#pragma unroll
+              for (int c = 0; c < 4; c += 2) {
+                bulk_wait_read_all();
+                stage_scaled_f32x32(my_stage, w, v[c]);
+                stage_scaled_f32x32(my_stage + 128, w, v[c + 1]);
+                fence_proxy_async_smem();
+                bulk_reduce_add_f32(args.out_f32 + col0 + c * 32, my_stage, 256);
+                bulk_commit();
+              }
+            } else {
+              bulk_wait_read_all();
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  st_shared_v4(my_stage + c * 64 + q * 16, pack_bf16x2(w * q_u2f(v[c][8 * q + 0]), w * q_u2f(v[c][8 * q + 1])),
+                               pack_bf16x2(w * q_u2f(v[c][8 * q + 2]), w * q_u2f(v[c][8 * q + 3])),
+                               pack_bf16x2(w * q_u2f(v[c][8 * q + 4]), w * q_u2f(v[c][8 * q + 5])),
+                               pack_bf16x2(w * q_u2f(v[c][8 * q + 6]), w * q_u2f(v[c][8 * q + 7])));
+              fence_proxy_async_smem();
+              bulk_reduce_add_bf16_hint(static_cast<__nv_bfloat16*>(args.out) + col0, my_stage, 256,
+                                        args.out_hint != 0, l2_policy_evict_last());
+              bulk_commit();
+            }
+          }
+        }
+      } else if (MODE == kPairDown && ns > 0) {
         // Swap-AB tile: TMEM lane `row` is output column j*256 + 128*rank + row,
         // column c is routed row c of the pair (slot (info >> 1) * 128 + c).
         // 128 routed rows at a time go transposed into the staging tile (staging

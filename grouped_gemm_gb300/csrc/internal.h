@@ -66,6 +66,9 @@ extern std::atomic<int> g_route_coop;
 // MOE_OPT_ROUTER_FUSED: 1 runs the router inside single-block routing
 // launches; 0 (default) always launches it separately.
 extern std::atomic<int> g_router_fused;
+// MOE_OPT_ROUTE_SMALL_PAIRS: problems of at most this many pairs (and at most
+// 256 experts) route in one single-block launch.
+extern std::atomic<int64_t> g_route_small_pairs;
 
 // pipeline = kRouteOnly plans only the routing regions (the common prefix of
 // every layout).
@@ -99,6 +102,8 @@ struct GemmArgs {
   int out_hint;             // 1: reductions into out carry an L2 evict_last hint
   float swiglu_limit;       // > 0: gate clamped to <= limit, up to [-limit, limit] before SwiGLU
   int l2_policy;            // bit 0: weight tiles loaded with an L2 evict_first policy
+  int half_m128;            // CTA-pair down kernel: a half pair runs as one M = 128 pair MMA (else M = 256,
+                            //   the odd CTA recomputing the first block and storing nothing)
 };
 
 // Routing; when zero_out != nullptr the first launch also zero-fills

@@ -383,12 +383,11 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
 }
 
 // The whole routing permutation in one 1024-thread block, for small problems
-// (P <= kRouteSmallMaxPairs, E <= kRouteSmallMaxExperts): per-warp histograms
+// (P <= g_route_small_pairs, E <= kRouteSmallMaxExperts): per-warp histograms
 // of 32 contiguous pair ranges, scans over warps and experts, padding and
 // block->expert tables, then the same stable warp-match scatter as above.
 constexpr int kRouteSmallWarps = 32;
 constexpr int kRouteSmallMaxExperts = 256;
-constexpr int64_t kRouteSmallMaxPairs = 8192;
 
 // kRouter: the block first runs the router over all T tokens (logits [T, E]),
 // writing ids / topk_w, and then routes what it wrote.
@@ -874,7 +873,7 @@ cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const flo
   // with the router, topk_ids / topk_w are the caller's output arrays
   int32_t* ids_out = logits ? const_cast<int32_t*>(topk_ids) : nullptr;
   float* w_out = logits ? const_cast<float*>(topk_w) : nullptr;
-  const bool small = !zero_out && P <= kRouteSmallMaxPairs && E <= kRouteSmallMaxExperts;
+  const bool small = !zero_out && P <= g_route_small_pairs.load() && E <= kRouteSmallMaxExperts;
   if (logits && (!small || !g_router_fused.load())) {
     // the router as its own wide launch (one warp per token): inside a
     // routing launch of a few blocks it would run on a small share of the GPU

@@ -432,6 +432,18 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   owner pushed its tiles into the other CTAs' stages by
  *                   shared-to-shared bulk copies, with a handshake per tile,
  *                   measured 1.26 / 0.66 / 15.9 ms.
+ *   MOE_OPT_HALF_PAIR_M128  0 (default) or 1: with 1, in the CTA-pair down
+ *                   projection, an expert's odd last row block (a pair
+ *                   without its second block) runs as one M = 128 pair MMA
+ *                   with 64 of its rows in each CTA; 0 runs it at M = 256 with
+ *                   the odd CTA repeating the first block and storing nothing.
+ *                   Measured on GB300, same box: prefill down kernel 0.117 /
+ *                   0.123 ms with 1 against 0.115 / 0.121 with 0, large_skewed
+ *                   2.78 against 2.73 ms (the kernel is not bound by MMA work).
+ *   MOE_OPT_ROUTE_SMALL_PAIRS  0 .. 1048576 (default 8192): problems of at
+ *                   most this many routed pairs (and at most 256 experts)
+ *                   route in one single-block launch instead of the
+ *                   cooperative one.
  *   (MOE_OPT_L2_POLICY measured at prefill: 0.343 ms with 0, 0.349 with 1,
  *                   0.342 with 2, 0.348 with 3: no gain, off.) */
 typedef enum {
@@ -453,7 +465,9 @@ typedef enum {
   MOE_OPT_PREFETCH_MB = 15,
   MOE_OPT_WIDE_UP = 16,
   MOE_OPT_TILE_M = 17,
-  MOE_OPT_FUSED_DSMEM = 18
+  MOE_OPT_FUSED_DSMEM = 18,
+  MOE_OPT_HALF_PAIR_M128 = 19,
+  MOE_OPT_ROUTE_SMALL_PAIRS = 20
 } moe_option_t;
 moe_status_t moe_ffn_set_option(int option, long long value);
 

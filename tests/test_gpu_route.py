@@ -2,7 +2,9 @@
 sort ("Prime Flash MoE" sec. 3 and 6: tokens processed in per-expert sorted
 order), including empty experts, one hot expert, repeats and T = 1.  Problems
 too large for the single-block kernel run both through the one-launch
-cooperative routing (default) and the three-launch path."""
+cooperative routing (default) and the three-launch path; the single-block
+kernel is also run on every problem it can take (at most 256 experts) with
+its size limit raised."""
 import numpy as np
 import pytest
 import torch
@@ -14,11 +16,15 @@ from grouped_gemm_gb300 import workloads as wl
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(autouse=True, params=[1, 0], ids=["coop", "three_launches"])
+@pytest.fixture(autouse=True, params=[(1, 8192), (0, 8192), (1, 1 << 20)],
+                ids=["coop", "three_launches", "single_block"])
 def route_mode(request):
-    moe.moe_ffn_set_option(moe.MOE_OPT_ROUTE_COOP, request.param)
+    coop, small_pairs = request.param
+    moe.moe_ffn_set_option(moe.MOE_OPT_ROUTE_COOP, coop)
+    moe.moe_ffn_set_option(moe.MOE_OPT_ROUTE_SMALL_PAIRS, small_pairs)
     yield request.param
     moe.moe_ffn_set_option(moe.MOE_OPT_ROUTE_COOP, 1)
+    moe.moe_ffn_set_option(moe.MOE_OPT_ROUTE_SMALL_PAIRS, 8192)
 
 
 def gpu_route(ids, E):
