@@ -59,6 +59,8 @@ def parse_args():
                     help="start each step from router logits [T, E] (moe_ffn_forward_logits: top-k and softmax "
                          "fused into the routing launch) instead of given top-k ids and weights")
     ap.add_argument("--no-graph", action="store_true", help="launch each step eagerly instead of replaying a CUDA graph")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the workload's token count T (a smaller case of the same kernels, for profiling)")
     ap.add_argument("--no-also", action="store_true",
                     help="skip the other workloads and pipelines measured after the main one (N=1 only)")
     ap.add_argument("--option", action="append", default=[], metavar="NAME=VALUE",
@@ -320,7 +322,7 @@ def bench_workload(args, name, pipeline_name, rank, world, sampler, full=True):
     import grouped_gemm_gb300 as moe
     from grouped_gemm_gb300 import workloads as wl
 
-    inp = wl.make_inputs(name, seed=rank)
+    inp = wl.make_inputs(name, seed=rank, T=args.tokens if name == args.workload else None)
     w = inp["workload"]
     mx = w.dtype in ("mxfp8", "mxfp4w")      # MXFP8 activations (e4m3 or packed E2M1 weights)
     dtype = {"bf16": moe.MOE_BF16, "mxfp8": moe.MOE_MXFP8, "mxfp4w": moe.MOE_MXFP4W}[w.dtype]
@@ -528,7 +530,7 @@ def run_ours(args, rank, world, local_rank):
         main = bench_workload(args, args.workload, args.pipeline, rank, world, sampler, full=True)
         torch.cuda.empty_cache()
         others = []
-        if world == 1 and not args.no_also and not args.from_logits and not args.option:
+        if world == 1 and not args.no_also and not args.from_logits and not args.option and args.tokens is None:
             for name, pipe in ALSO:
                 if (name, pipe) == (args.workload, args.pipeline):
                     continue

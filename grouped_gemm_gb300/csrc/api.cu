@@ -40,6 +40,7 @@ std::atomic<int> g_l2_policy{0};      // MOE_OPT_L2_POLICY: bit 0 weights evict_
 std::atomic<int> g_prefetch_mb{0};    // MOE_OPT_PREFETCH_MB: weights prefetched into L2 during routing
 std::atomic<int> g_pair_swap{0};      // MOE_OPT_PAIR_SWAP: max routed rows of a swap-AB pair tile (measured slower: off)
 std::atomic<int> g_wide_up{0};        // MOE_OPT_WIDE_UP: 512-column up tiles on CTA pairs
+std::atomic<int> g_down_bands{1};     // MOE_OPT_DOWN_BANDS: token bands of the down tiles' order (0 automatic, 1 off)
 std::atomic<int> g_half_m128{0};      // MOE_OPT_HALF_PAIR_M128: half pairs as M = 128 pair MMAs (measured no gain: off)
 std::atomic<int> g_fused_dsmem{0};    // MOE_OPT_FUSED_DSMEM: act kept in shared memory in the cluster kernel (measured slower: off)
 std::atomic<int> g_tile_m{0};         // MOE_OPT_TILE_M: rows per tile of the single-CTA split GEMMs (0 automatic)
@@ -53,6 +54,19 @@ constexpr int64_t kOutHintMaxBytes = 160ll << 20;
 int out_hint_for(int64_t out_bytes) {
   const int opt = g_out_hint.load();
   return opt == 2 || (opt == 1 && out_bytes <= kOutHintMaxBytes) ? 1 : 0;
+}
+
+// Token bands of the down projection's tile order: the reductions into out
+// then stay within the rows of one band at a time, which L2 holds while the
+// weights stream past.  Automatic: bands of at most 48 MiB of out, when out
+// is larger than 64 MiB.
+int down_bands(int T, int D) {
+  const int opt = g_down_bands.load();
+  if (opt >= 1) return T >= opt ? opt : 1;
+  const int64_t out_bytes = (int64_t)T * D * 2;
+  if (out_bytes <= (64ll << 20)) return 1;
+  const int64_t n = (out_bytes + (48ll << 20) - 1) / (48ll << 20);
+  return (int)std::min<int64_t>(std::min<int64_t>(n, 64), T);
 }
 
 bool shape_ok(int T, int E, int D, int H, int k) {
@@ -190,6 +204,8 @@ Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipe
   w.slot_w = reinterpret_cast<float*>(take(sizeof(float) * w.S_max));
   w.slot_of_pair = reinterpret_cast<int*>(take(sizeof(int) * (P ? P : 1)));
   w.blk_base = reinterpret_cast<int*>(take(sizeof(int) * (size_t)w.route_blocks * E));
+  w.rb_order = reinterpret_cast<int*>(take(sizeof(int) * w.max_rb));
+  w.pair_order = reinterpret_cast<int*>(take(sizeof(int) * w.max_rb));
   if (pipeline == kRouteOnly) {
     // routing regions only
   } else if (dtype != MOE_BF16) {  // MXFP8 activations (e4m3 weights, or MXFP4 weights)
@@ -394,6 +410,8 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
           : launch_gather_mx(ws, x, x_sf, topk_ids, T, E, k, D, out, (int64_t)T * D * 2, sms * g_gather_blocks.load(),
                              st, !g_prof.on);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
+  const int bands = down_bands(T, D);
+  if (bands > 1 && launch_band_order(ws, T, bands, st) != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 2);
   MxArgs ma{};
   ma.meta = ws.meta;
@@ -417,6 +435,7 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
   up.n_col_tiles = H / 128;
   up.k_blocks = D / 128;
   prof_front(true);
+  if (bands > 1) prof_kernel(1, "gather_rows_mx+band_order");
   prof_kernel(2, fp4w ? "up_swiglu_mxfp4w" : "up_swiglu_mxfp8");
   prof_kernel(3, fp4w ? (acc ? "down_reduce_mxfp4w+f32_to_bf16" : "down_reduce_mxfp4w")
                       : (acc ? "down_reduce_mxfp8+f32_to_bf16" : "down_reduce_mxfp8"));
@@ -425,6 +444,7 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 3);
   MxArgs dn = ma;
+  dn.rb_order = bands > 1 ? ws.rb_order : nullptr;
   dn.sf_a = ws.act_sf;
   dn.sf_b = w2_sf;
   dn.n_col_tiles = D / 256;
@@ -644,6 +664,10 @@ moe_status_t moe_ffn_set_option(int option, long long value) {
       if (value != 0 && value != 64 && value != 128) return MOE_ERR_INVALID_ARG;
       g_tile_m.store((int)value);
       return MOE_OK;
+    case MOE_OPT_DOWN_BANDS:
+      if (value < 0 || value > 64) return MOE_ERR_INVALID_ARG;
+      g_down_bands.store((int)value);
+      return MOE_OK;
     case MOE_OPT_ROUTE_SMALL_PAIRS:
       if (value < 0 || value > (1 << 20)) return MOE_ERR_INVALID_ARG;
       g_route_small_pairs.store(value);
@@ -827,6 +851,9 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
                            !g_prof.on);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
+  // the CTA-pair down kernel walks its block pairs in token-band order
+  const int bands = pair_down ? down_bands(T, D) : 1;
+  if (bands > 1 && launch_band_order(ws, T, bands, st) != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 2);
 
   GemmArgs ga{};
@@ -866,7 +893,8 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
   const int pair_slots = pair_mma ? pair_cluster_slots() : 0;
   if (pair_mma && pair_slots <= 0) return MOE_ERR_CUDA;
   prof_front(false);
-  if (in_gemm_gather) prof_kernel(1, "none");  // rows gathered by the up kernel
+  if (in_gemm_gather) prof_kernel(1, bands > 1 ? "band_order" : "none");  // rows gathered by the up kernel
+  else if (bands > 1) prof_kernel(1, "gather_tokens+band_order");
   const bool wide_up = pair_mma && g_wide_up.load() == 1;
   const int wide_slots = wide_up ? pair_wide_cluster_slots() : 0;
   if (wide_up && wide_slots <= 0) return MOE_ERR_CUDA;
@@ -893,6 +921,7 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
   prof_mark(st, 3);
 
   GemmArgs dn = ga;
+  dn.pair_order = bands > 1 ? ws.pair_order : nullptr;
   dn.tile_counter = dyn ? ws.meta + 3 : nullptr;
   dn.n_col_tiles = D / down_n;
   dn.k_blocks = H / kBK;

@@ -120,6 +120,11 @@ __global__ void __launch_bounds__(kMxThreads, 1)
   const int num_rb = args.meta[0];
   const int n_tiles = num_rb * args.n_col_tiles;
   const int KB = args.k_blocks;             // K / 128
+  // row block of a tile: in token-band order for DOWN when an order is given
+  auto tile_rb = [&](int tile) {
+    const int i = tile / args.n_col_tiles;
+    return (MODE == kMxDown && args.rb_order) ? args.rb_order[i] : i;
+  };
   const uint8_t* sf_a = static_cast<const uint8_t*>(args.sf_a);
   const uint8_t* sf_b = static_cast<const uint8_t*>(args.sf_b);
 
@@ -133,7 +138,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     for (int i = 0; i < STAGES; ++i) issued_phase[i] = -1;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
-      const int rb = tile / args.n_col_tiles, j = tile % args.n_col_tiles;
+      const int rb = tile_rb(tile), j = tile % args.n_col_tiles;
       const int e = args.expert_of_rb[rb];
       for (int kb = 0; kb < KB; ++kb) {
         if (!(ok = mbar_wait(&empty[s], ph ^ 1u, wc, 21))) break;
@@ -217,7 +222,7 @@ __global__ void __launch_bounds__(kMxThreads, 1)
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++it) {
       if (!mbar_wait(tfull, (uint32_t)it & 1u, wc, 24)) break;
       tc_fence_after();
-      const int rb = tile / args.n_col_tiles, j = tile % args.n_col_tiles;
+      const int rb = tile_rb(tile), j = tile % args.n_col_tiles;
       const int64_t slot = (int64_t)rb * kBM + row;
       const int tok = args.row_tok[slot];
       if (MODE == kMxUp) {

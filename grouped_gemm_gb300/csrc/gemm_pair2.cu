@@ -149,6 +149,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
   const int NJ = args.n_col_tiles;
   const int n_tiles = args.meta[1] * NJ;  // (block pair, column tile)
   const int KB = args.k_blocks;
+  // pair_info of the i-th block pair processed: in token-band order for DOWN
+  // when an order is given (the reductions then stay within one band of out)
+  auto tile_pair = [&](int i) {
+    return args.pair_info[(MODE == kPairDown && args.pair_order) ? args.pair_order[i] : i];
+  };
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
@@ -159,7 +164,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     for (int i = 0; i < kQStages; ++i) issued_phase[i] = -1;
     bool ok = true;
     for (int tile = pair_slot; ok && tile < n_tiles; tile += n_pair_slots) {
-      const int info = args.pair_info[tile / NJ], j = tile % NJ;
+      const int info = tile_pair(tile / NJ), j = tile % NJ;
       const int rb0 = info >> 1, two = info & 1;
       const int e = args.expert_of_rb[rb0];
       const int brow = MODE == kPairUp ? e * 2 * args.H + (int)rank * args.H + j * 128
@@ -210,10 +215,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
       if (!(ok = mbar_wait_cluster(&tempty[acc], ((uint32_t)(it >> 1) & 1u) ^ 1u, wc, 62))) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * 256;
-      const int ns = MODE == kPairDown ? pair_swap_ns(args, args.pair_info[tile / NJ]) : 0;
+      const int ns = MODE == kPairDown ? pair_swap_ns(args, tile_pair(tile / NJ)) : 0;
       const uint32_t idesc_swap = idesc_bf16_f32(2 * kBM, ns ? ns : 16);
       // DOWN: a half pair runs as one M = 128 pair MMA (64 rows in each CTA)
-      const bool m128_t = MODE == kPairDown && !ns && args.half_m128 && !(args.pair_info[tile / NJ] & 1);
+      const bool m128_t = MODE == kPairDown && !ns && args.half_m128 && !(tile_pair(tile / NJ) & 1);
       for (int kb = 0; kb < KB; ++kb) {
         if (!(ok = mbar_wait(&full[s], ph, wc, 63))) break;
         tc_fence_after();
@@ -265,7 +270,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       const int acc = it & 1;
       if (!mbar_wait(&tfull[acc], (uint32_t)(it >> 1) & 1u, wc, 64)) break;
       tc_fence_after();
-      const int info = args.pair_info[tile / NJ], j = tile % NJ;
+      const int info = tile_pair(tile / NJ), j = tile % NJ;
       const uint32_t tacc = lane_base + acc * 256;
       const int ns = MODE == kPairDown ? pair_swap_ns(args, info) : 0;
       const bool m128 = MODE == kPairDown && !(info & 1) && !ns && args.half_m128;

@@ -38,6 +38,8 @@ struct Workspace {
   float* slot_w;       // [S_max] routing weight of each padded slot, 0 for padding
   int* slot_of_pair;   // [P]   unpadded slot of pair p = t*k + j
   int* blk_base;       // [NB*E] per routing block: rank base within each expert
+  int* rb_order;       // [max_rb] row blocks ordered by the token band of their first row (down kernels)
+  int* pair_order;     // [max_rb] block pairs in the same order
   void* xg;            // [S_max, D] bf16 gathered rows (split pipeline)
   void* act;           // [S_max, H] bf16 activation (split pipeline)
   void* acc_f32;       // [T, D] fp32 reduction target (fused pipeline)
@@ -102,6 +104,7 @@ struct GemmArgs {
   int out_hint;             // 1: reductions into out carry an L2 evict_last hint
   float swiglu_limit;       // > 0: gate clamped to <= limit, up to [-limit, limit] before SwiGLU
   int l2_policy;            // bit 0: weight tiles loaded with an L2 evict_first policy
+  const int* pair_order;    // down: nullptr, or the order in which the block pairs are processed
   int half_m128;            // CTA-pair down kernel: a half pair runs as one M = 128 pair MMA (else M = 256,
                             //   the odd CTA recomputing the first block and storing nothing)
 };
@@ -114,6 +117,12 @@ struct GemmArgs {
 cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const float* topk_w, int T, int E, int k,
                          cudaStream_t stream, void* zero_out = nullptr, int64_t zero_bytes = 0, int zero_grid = 0,
                          bool pdl = false);
+// Orders of the down projection's tiles by token band (reductions into a
+// reduction target larger than L2 then find the rows of one band of tokens
+// there): rb_order = the row blocks, pair_order = the block pairs, each sorted
+// stably by band(token of its first row) = tok * n_bands / T.  One block,
+// launched after the routing.
+cudaError_t launch_band_order(const Workspace& ws, int T, int n_bands, cudaStream_t stream);
 // The router alone: top-k ids (decreasing logit, ties to the lower id) and the
 // softmax of the selected logits, for each of T tokens of logits [T, E].
 cudaError_t launch_router_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
@@ -273,6 +282,7 @@ struct MxArgs {
   void* act_sf;             // up: blocked scale tiles of act
   void* out;                // down: bf16 [T, D] reduction target
   float* out_f32;           // down: non-null = fp32 [T, D] reduction target instead of out
+  const int* rb_order;      // down: nullptr, or the order in which the row blocks are processed
   const void* sf_a;         // blocked scale tiles of the A operand
   const void* sf_b;         // blocked scale tiles of the weights
   int* err;

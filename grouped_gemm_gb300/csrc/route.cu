@@ -990,6 +990,48 @@ cudaError_t launch_extend_routing(const int32_t* ids, const float* w, int T, int
   return cudaGetLastError();
 }
 
+namespace {
+// Band of a row block: that of the token of its first row (always a routed
+// row: padding rows sit at the end of each expert's segment).
+__device__ __forceinline__ int block_band(const int* row_tok, int rb, int T, int n_bands) {
+  const int tok = row_tok[(int64_t)rb * kRowPad];
+  return (int)((int64_t)(tok < 0 ? 0 : tok) * n_bands / T);
+}
+
+__global__ void __launch_bounds__(1024) band_order_kernel(const int* __restrict__ meta, const int* __restrict__ row_tok,
+                                                          const int* __restrict__ pair_info, int T, int n_bands,
+                                                          int* __restrict__ rb_order, int* __restrict__ pair_order) {
+  __shared__ int warp_sums[32];
+  griddep_wait();
+  const int n_rb = meta[0], n_pq = meta[1];
+  for (int which = 0; which < 2; ++which) {
+    const int n = which ? n_pq : n_rb;
+    int* out = which ? pair_order : rb_order;
+    // thread t owns the contiguous items [i0, i1): a stable counting sort by band
+    const int per = (n + (int)blockDim.x - 1) / (int)blockDim.x;
+    const int i0 = min(n, (int)threadIdx.x * per), i1 = min(n, i0 + per);
+    auto band = [&](int i) { return block_band(row_tok, which ? pair_info[i] >> 1 : i, T, n_bands); };
+    int base = 0;  // items of the lower bands
+    for (int b = 0; b < n_bands; ++b) {
+      int c = 0;
+      for (int i = i0; i < i1; ++i) c += band(i) == b;
+      int tot;
+      int pos = base + block_exclusive_scan(c, warp_sums, &tot);
+      for (int i = i0; i < i1; ++i)
+        if (band(i) == b) out[pos++] = i;
+      base += tot;
+    }
+  }
+}
+}  // namespace
+
+cudaError_t launch_band_order(const Workspace& ws, int T, int n_bands, cudaStream_t stream) {
+  if (T <= 0 || n_bands < 1) return cudaSuccess;
+  band_order_kernel<<<1, 1024, 0, stream>>>(ws.meta, ws.row_tok, ws.pair_info, T, n_bands, ws.rb_order,
+                                           ws.pair_order);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_router_topk(const float* logits, int T, int E, int k, int32_t* ids, float* w,
                                cudaStream_t stream) {
   if (T == 0) return cudaSuccess;

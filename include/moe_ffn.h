@@ -444,6 +444,14 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   most this many routed pairs (and at most 256 experts)
  *                   route in one single-block launch instead of the
  *                   cooperative one.
+ *   MOE_OPT_DOWN_BANDS  1 (default: off), 0 (automatic: bands of at most
+ *                   48 MiB of out when out exceeds 64 MiB) or 2 .. 64: the
+ *                   split pipeline's down projection (CTA-pair bf16 kernel,
+ *                   MXFP8 kernel) processes its tiles ordered by the token band
+ *                   of their first row (band = token * bands / T; stable, so
+ *                   expert order within a band), so that its reductions into
+ *                   an out larger than L2 meet the rows of one band at a time
+ *                   in L2; the weights are then read once per band.
  *   (MOE_OPT_L2_POLICY measured at prefill: 0.343 ms with 0, 0.349 with 1,
  *                   0.342 with 2, 0.348 with 3: no gain, off.) */
 typedef enum {
@@ -467,7 +475,8 @@ typedef enum {
   MOE_OPT_TILE_M = 17,
   MOE_OPT_FUSED_DSMEM = 18,
   MOE_OPT_HALF_PAIR_M128 = 19,
-  MOE_OPT_ROUTE_SMALL_PAIRS = 20
+  MOE_OPT_ROUTE_SMALL_PAIRS = 20,
+  MOE_OPT_DOWN_BANDS = 21
 } moe_option_t;
 moe_status_t moe_ffn_set_option(int option, long long value);
 

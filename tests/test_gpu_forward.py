@@ -37,6 +37,7 @@ MODES = {
     "split_pair2_swap": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 1, moe.MOE_OPT_PAIR_SWAP: 128}),
     "split_pair2_allswap": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 1, moe.MOE_OPT_PAIR_SWAP: 256}),
     "split_pair2_half128": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 1, moe.MOE_OPT_HALF_PAIR_M128: 1}),
+    "split_pair2_bands": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 1, moe.MOE_OPT_DOWN_BANDS: 3}),
     "split_wide": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 1, moe.MOE_OPT_WIDE_UP: 1}),
     "split_m64": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 0, moe.MOE_OPT_TILE_M: 64}),
     "fused": (moe.MOE_FUSED, {}),
@@ -45,7 +46,7 @@ MODES = {
 }
 DEFAULTS = {moe.MOE_OPT_UP_PAIRS: 0, moe.MOE_OPT_GATHER: 0, moe.MOE_OPT_SWAP_AB: 0, moe.MOE_OPT_FUSED_CLUSTER: 1,
             moe.MOE_OPT_PAIR_MMA: 2, moe.MOE_OPT_PAIR_SWAP: 0, moe.MOE_OPT_WIDE_UP: 0, moe.MOE_OPT_TILE_M: 0,
-            moe.MOE_OPT_FUSED_DSMEM: 0, moe.MOE_OPT_HALF_PAIR_M128: 0}
+            moe.MOE_OPT_FUSED_DSMEM: 0, moe.MOE_OPT_HALF_PAIR_M128: 0, moe.MOE_OPT_DOWN_BANDS: 1}
 PIPELINES = list(MODES)
 
 
@@ -167,7 +168,7 @@ def test_forward_full_workload_sampled(name, pipeline):
     the first and last routed token of every expert, the first token of every
     expert's last row block, and 1000 seeded random tokens."""
     if name == "large_skewed" and pipeline not in ("split", "fused", "fused_dsmem", "fused_splitk", "split_pair2",
-                                                   "split_wide", "split_m64"):
+                                                   "split_wide", "split_m64", "split_pair2_bands"):
         pytest.skip("option variants are covered at the smaller sizes")
     inp = cached_inputs(name)
     out, _ = run_mode(inp, to_dev(inp), pipeline)

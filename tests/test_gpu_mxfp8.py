@@ -77,9 +77,10 @@ def test_weight_scale_repacking_layout():
     assert np.array_equal(p2.cpu().numpy(), expected(w2_sf))
 
 
-def run_mx(inp, pipeline=moe.MOE_SPLIT, cluster=1):
+def run_mx(inp, pipeline=moe.MOE_SPLIT, cluster=1, bands=1):
     """cluster: MOE_OPT_FUSED_CLUSTER for the call (1 automatic, 2/4/8 that
-    size, 0 the fused kernel with fp32 partial sums)."""
+    size, 0 the fused kernel with fp32 partial sums); bands:
+    MOE_OPT_DOWN_BANDS (token-band order of the split down kernel's tiles)."""
     w = inp["workload"]
     dev = {k: torch.from_numpy(inp[k]).cuda() for k in ("x", "x_sf", "w1", "w2")}
     w1p = torch.empty(inp["w1_sf"].size, dtype=torch.uint8, device="cuda")
@@ -91,11 +92,13 @@ def run_mx(inp, pipeline=moe.MOE_SPLIT, cluster=1):
     out = torch.full((w.T, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
     ws = moe.alloc_workspace(w.T, w.E, w.D, w.H, w.k, moe.MOE_MXFP8, pipeline)
     moe.moe_ffn_set_option(moe.MOE_OPT_FUSED_CLUSTER, cluster)
+    moe.moe_ffn_set_option(moe.MOE_OPT_DOWN_BANDS, bands)
     try:
         moe.moe_ffn_forward(dev["x"], dev["w1"], dev["w2"], ids, tw, out, E=w.E, D=w.D, H=w.H, k=w.k, workspace=ws,
                             dtype=moe.MOE_MXFP8, pipeline=pipeline, x_sf=dev["x_sf"], w1_sf=w1p, w2_sf=w2p)
     finally:
         moe.moe_ffn_set_option(moe.MOE_OPT_FUSED_CLUSTER, 1)
+        moe.moe_ffn_set_option(moe.MOE_OPT_DOWN_BANDS, 1)
     st = moe.moe_ffn_sync_status(ws)
     assert st == 0, moe.moe_ffn_status_string(st)
     return out
@@ -106,8 +109,10 @@ def oracle_mx(inp, tokens=None):
                           x_sf=inp["x_sf"], w1_sf=inp["w1_sf"], w2_sf=inp["w2_sf"], tokens=tokens)
 
 
-# fused: on clusters (automatic size); fused_splitk: H split over CTAs with fp32 partial sums
-PIPES = {"split": (moe.MOE_SPLIT, 1), "fused": (moe.MOE_FUSED, 1), "fused_splitk": (moe.MOE_FUSED, 0)}
+# fused: on clusters (automatic size); fused_splitk: H split over CTAs with fp32 partial sums;
+# split_bands: the down kernel's tiles in the order of three token bands
+PIPES = {"split": (moe.MOE_SPLIT, 1), "fused": (moe.MOE_FUSED, 1), "fused_splitk": (moe.MOE_FUSED, 0),
+         "split_bands": (moe.MOE_SPLIT, 1, 3)}
 
 
 @pytest.mark.parametrize("pipe", list(PIPES))
