@@ -37,7 +37,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE FFN fwd TFLOP/s & tokens/s on 1×GB300; % of roofline (tensor or HBM)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # GB300 data-sheet figures (dense, no sparsity), reported beside the measured-peak fractions
-NOMINAL_PEAKS = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0, "fp8_tflops": 4500.0}
+NOMINAL_PEAKS = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0, "fp8_tflops": 4500.0, "fp4_tflops": 13500.0}
 # measured after the main workload in the same run (N=1): workload, pipeline
 ALSO = [("large_skewed", "split"), ("large_skewed", "fused"), ("prefill", "split"), ("prefill", "fused"),
         ("mxfp8", "split"), ("mxfp8", "fused"), ("decode", "split"), ("decode", "fused")]
@@ -84,8 +84,8 @@ def algorithmic(w, ids):
     import numpy as np
     P = w.T * w.k
     live = int(np.unique(ids).size)
-    eb = 2 if w.dtype == "bf16" else 1
-    sfb = 0 if w.dtype == "bf16" else 1.0 / 32
+    eb = 2 if w.dtype == "bf16" else 0.5 if w.dtype == "nvfp4" else 1
+    sfb = 0 if w.dtype == "bf16" else 1.0 / 16 if w.dtype == "nvfp4" else 1.0 / 32
     elem = eb + sfb                                              # activations (x, act)
     welem = (0.5 + sfb) if w.dtype == "mxfp4w" else elem         # expert weights
     step_bytes = (w.T * w.D * elem + live * 3 * w.H * w.D * welem + P * 8 + w.T * w.D * 2)
@@ -135,6 +135,8 @@ KERNEL_SOURCES = {
     "up_swiglu_mxfp8": ["grouped_gemm_gb300/csrc/gemm_mxfp8.cu"] + _MXH + _PTX,
     "down_reduce_mxfp8": ["grouped_gemm_gb300/csrc/gemm_mxfp8.cu"] + _MXH + _PTX,
     "up_swiglu_mxfp4w": ["grouped_gemm_gb300/csrc/gemm_mxfp8.cu"] + _MXH + _PTX,
+    "up_swiglu_nvfp4": ["grouped_gemm_gb300/csrc/gemm_nvfp4.cu"] + _MXH + _PTX,
+    "down_reduce_nvfp4": ["grouped_gemm_gb300/csrc/gemm_nvfp4.cu"] + _MXH + _PTX,
     "down_reduce_mxfp4w": ["grouped_gemm_gb300/csrc/gemm_mxfp8.cu"] + _MXH + _PTX,
     "fused_cluster_bf16": ["grouped_gemm_gb300/csrc/gemm_fused_cluster.cu"] + _PTX,
     "fused_dsmem_bf16": ["grouped_gemm_gb300/csrc/gemm_fused_dsmem.cu"] + _PTX,
@@ -276,14 +278,19 @@ def weak_scaling_tflops(flops_per_rank: float, ms_max: float, world: int) -> flo
 
 
 # ---------------------------------------------------------------- our arm
-def roofline_fracs(alg, stage_ms, pipeline, mx, peaks, peak_src, stage_kernels, workload):
+def roofline_fracs(alg, stage_ms, pipeline, mx, peaks, peak_src, stage_kernels, workload, fp4=False):
     """The dominant kernel's achieved rate against its roofline (measured
     peak, and the data-sheet peak beside it), and the step's bound."""
-    if mx:  # e4m3 contraction: the measured bf16 peak times the nominal fp8/bf16 ratio (4.5 / 2.25)
+    if fp4:  # e2m1 x e2m1 contraction: the measured bf16 peak times the nominal fp4/bf16 ratio (13.5 / 2.25)
+        peaks = dict(peaks)
+        peaks["bf16_tflops"] = peaks["bf16_tflops"] * 6.0
+        peak_src += " bf16 x nominal fp4/bf16 ratio 6"
+    elif mx:  # e4m3 contraction: the measured bf16 peak times the nominal fp8/bf16 ratio (4.5 / 2.25)
         peaks = dict(peaks)
         peaks["bf16_tflops"] = peaks["bf16_tflops"] * 2.0
         peak_src += " bf16 x nominal fp8/bf16 ratio 2"
-    nominal_tf = NOMINAL_PEAKS["fp8_tflops"] if mx else NOMINAL_PEAKS["bf16_tflops"]
+    nominal_tf = (NOMINAL_PEAKS["fp4_tflops"] if fp4 else NOMINAL_PEAKS["fp8_tflops"] if mx
+                  else NOMINAL_PEAKS["bf16_tflops"])
     if pipeline == "split":
         dom = max(("up_swiglu", "down_reduce"), key=lambda s: stage_ms.get(s, 0.0))
         kd = alg[dom]
@@ -324,10 +331,20 @@ def bench_workload(args, name, pipeline_name, rank, world, sampler, full=True):
 
     inp = wl.make_inputs(name, seed=rank, T=args.tokens if name == args.workload else None)
     w = inp["workload"]
-    mx = w.dtype in ("mxfp8", "mxfp4w")      # MXFP8 activations (e4m3 or packed E2M1 weights)
-    dtype = {"bf16": moe.MOE_BF16, "mxfp8": moe.MOE_MXFP8, "mxfp4w": moe.MOE_MXFP4W}[w.dtype]
+    nv = w.dtype == "nvfp4"                  # NVFP4 activations and weights, global scales
+    mx = w.dtype in ("mxfp8", "mxfp4w", "nvfp4")  # block-scaled (one-byte or packed four-bit codes)
+    dtype = {"bf16": moe.MOE_BF16, "mxfp8": moe.MOE_MXFP8, "mxfp4w": moe.MOE_MXFP4W, "nvfp4": moe.MOE_NVFP4}[w.dtype]
     dev = {k: torch.from_numpy(inp[k] if mx else inp[k].view(np.int16)).cuda() for k in ("x", "w1", "w2")}
-    if mx:  # weight scales are repacked once, like the weights themselves
+    if nv:  # weight scales repacked once; the global scales as device scalars and vectors
+        dev["x_sf"] = torch.from_numpy(inp["x_sf"]).cuda()
+        dev["w1_sf"] = torch.empty(inp["w1_sf"].size, dtype=torch.uint8, device="cuda")
+        dev["w2_sf"] = torch.empty(inp["w2_sf"].size, dtype=torch.uint8, device="cuda")
+        moe.moe_ffn_prepare_nvfp4_weights(torch.from_numpy(inp["w1_sf"]).cuda(), torch.from_numpy(inp["w2_sf"]).cuda(),
+                                          dev["w1_sf"], dev["w2_sf"], w.E, w.D, w.H)
+        gs = {"x_gs": torch.tensor([float(inp["x_gs"])], dtype=torch.float32, device="cuda"),
+              "w1_gs": torch.from_numpy(inp["w1_gs"]).cuda(), "w2_gs": torch.from_numpy(inp["w2_gs"]).cuda(),
+              "act_gs": torch.tensor([float(inp["act_gs"])], dtype=torch.float32, device="cuda")}
+    elif mx:  # weight scales are repacked once, like the weights themselves
         dev["x_sf"] = torch.from_numpy(inp["x_sf"]).cuda()
         dev["w1_sf"] = torch.empty(inp["w1_sf"].size, dtype=torch.uint8, device="cuda")
         dev["w2_sf"] = torch.empty(inp["w2_sf"].size, dtype=torch.uint8, device="cuda")
@@ -345,6 +362,11 @@ def bench_workload(args, name, pipeline_name, rank, world, sampler, full=True):
     stream = torch.cuda.current_stream()
 
     def step():  # one forward pass on the current stream
+        if nv:
+            moe.moe_ffn_forward_nvfp4(dev["x"], dev["x_sf"], dev["w1"], dev["w1_sf"], dev["w2"], dev["w2_sf"],
+                                      gs["x_gs"], gs["w1_gs"], gs["w2_gs"], gs["act_gs"], ids, tw, out, E=w.E, D=w.D,
+                                      H=w.H, k=w.k, workspace=ws)
+            return
         if logits is not None:
             moe.moe_ffn_forward_logits(dev["x"], dev["w1"], dev["w2"], logits, ids, tw, out, E=w.E, D=w.D, H=w.H,
                                        k=w.k, workspace=ws, dtype=dtype, pipeline=pipeline, x_sf=dev.get("x_sf"),
@@ -442,7 +464,7 @@ def bench_workload(args, name, pipeline_name, rank, world, sampler, full=True):
 
     peaks, peak_src = load_peaks()
     roofline, step_bound, step_bound_nominal = roofline_fracs(alg, stage_ms, pipeline_name, mx, peaks, peak_src,
-                                                              stage_kernels, name)
+                                                              stage_kernels, name, fp4=nv)
     clocks = sampler.summary(t_host0, t_host1) if sampler else None
     config = {"workload": w.name, "T": w.T, "D": w.D, "H": w.H, "E": w.E, "k": w.k, "routing": w.routing,
               "pipeline": pipeline_name, "seed": "rank", "parallelism": f"token-sharded x{world}",
@@ -453,7 +475,8 @@ def bench_workload(args, name, pipeline_name, rank, world, sampler, full=True):
                      f"(129 MB L2), no flush needed")}
     line = {
         "value": round(value, 3), "unit": "TFLOP/s", "ms_per_step": round(ms, 5),
-        "dtype": {"bf16": "bf16", "mxfp8": "e4m3 (MXFP8)", "mxfp4w": "e4m3 x e2m1 (MXFP8 x MXFP4)"}[w.dtype],
+        "dtype": {"bf16": "bf16", "mxfp8": "e4m3 (MXFP8)", "mxfp4w": "e4m3 x e2m1 (MXFP8 x MXFP4)",
+                  "nvfp4": "e2m1 (NVFP4)"}[w.dtype],
         "tokens_per_s": round(tokens_per_s, 1),
         "roofline_step_frac": round(step_bound / (ms * 1e-3), 4),
         "roofline_step_frac_nominal": round(step_bound_nominal / (ms * 1e-3), 4),
@@ -559,6 +582,10 @@ def run_ours(args, rank, world, local_rank):
 def oracle_call(inp, tokens):
     import oracle
     dt = inp["workload"].dtype
+    if dt == "nvfp4":
+        return oracle.moe_ffn_nvfp4(inp["x"], inp["x_sf"], float(inp["x_gs"]), inp["w1"], inp["w1_sf"], inp["w1_gs"],
+                                    inp["w2"], inp["w2_sf"], inp["w2_gs"], inp["topk_ids"], inp["topk_w"],
+                                    act=oracle.ACT_NVFP4, act_gs=float(inp["act_gs"]), tokens=tokens)
     return oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], inp["topk_ids"], inp["topk_w"],
                           act=oracle.ACT_BF16 if dt == "bf16" else oracle.ACT_MXFP8, tokens=tokens,
                           x_sf=inp.get("x_sf"), w1_sf=inp.get("w1_sf"), w2_sf=inp.get("w2_sf"),

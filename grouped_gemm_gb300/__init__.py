@@ -13,13 +13,13 @@ import os
 import threading
 
 __all__ = [
-    "MOE_BF16", "MOE_MXFP8", "MOE_MXFP4W", "MOE_FUSED", "MOE_SPLIT", "MoeFFNError", "library_path", "lib",
+    "MOE_BF16", "MOE_MXFP8", "MOE_MXFP4W", "MOE_NVFP4", "MOE_FUSED", "MOE_SPLIT", "MoeFFNError", "library_path", "lib",
     "moe_ffn_workspace_size", "moe_ffn_workspace_init", "moe_ffn_forward", "moe_ffn_forward_logits", "moe_ffn_forward_ex", "MoeFFNExtras",
     "moe_ffn_workspace_size_ex", "moe_ffn_router_topk", "moe_ffn_route", "moe_ffn_route_noalloc",
     "moe_ffn_sync_status", "moe_ffn_set_wait_limit_ns", "moe_ffn_profile_enable", "moe_ffn_profile_read", "moe_ffn_profile_stage_kernel", "moe_ffn_set_option", "MOE_OPT_GATHER", "moe_ffn_prepare_mxfp8_weights", "moe_ffn_widen_mxfp4_weights", "moe_ffn_debug_mx_quantize", "moe_ffn_status_string", "alloc_workspace",
 ]
 
-MOE_BF16, MOE_MXFP8, MOE_MXFP4W = 0, 1, 2
+MOE_BF16, MOE_MXFP8, MOE_MXFP4W, MOE_NVFP4 = 0, 1, 2, 3
 MOE_FUSED, MOE_SPLIT = 0, 1
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_MISALIGNED",
                 4: "MOE_ERR_BAD_ROUTING", 5: "MOE_ERR_WORKSPACE_TOO_SMALL", 6: "MOE_ERR_DEVICE_TIMEOUT",
@@ -32,6 +32,12 @@ _lib = None
 class MoeFFNExtras(ctypes.Structure):
     """moe_ffn_extras_t: clamped SwiGLU limit, shared experts, router logits."""
     _fields_ = [("swiglu_limit", ctypes.c_float), ("n_shared", ctypes.c_int), ("router_logits", ctypes.c_void_p)]
+
+
+class NvFp4Scales(ctypes.Structure):
+    """moe_ffn_nvfp4_scales_t: device pointers to the fp32 global scales."""
+    _fields_ = [("x_gs", ctypes.c_void_p), ("w1_gs", ctypes.c_void_p), ("w2_gs", ctypes.c_void_p),
+                ("act_gs", ctypes.c_void_p)]
 
 
 class MoeFFNError(RuntimeError):
@@ -79,6 +85,10 @@ def lib() -> ctypes.CDLL:
             L.moe_ffn_route_padded.restype = i
             L.moe_ffn_prepare_mxfp8_weights.argtypes = [vp, vp, vp, vp, i, i, i, vp]
             L.moe_ffn_prepare_mxfp8_weights.restype = i
+            L.moe_ffn_prepare_nvfp4_weights.argtypes = [vp, vp, vp, vp, i, i, i, vp]
+            L.moe_ffn_prepare_nvfp4_weights.restype = i
+            L.moe_ffn_forward_nvfp4.argtypes = [vp] * 6 + [c.POINTER(NvFp4Scales)] + [vp] * 3 + [i] * 5 + [vp, sz, vp]
+            L.moe_ffn_forward_nvfp4.restype = i
             L.moe_ffn_widen_mxfp4_weights.argtypes = [vp, c.c_int64, vp, vp]
             L.moe_ffn_widen_mxfp4_weights.restype = i
             L.moe_ffn_debug_mx_quantize.argtypes = [vp, c.c_int64, vp, vp, vp]
@@ -299,6 +309,35 @@ def moe_ffn_prepare_mxfp8_weights(w1_sf, w2_sf, w1_sf_packed, w2_sf_packed, E, D
         _need(t, n, name)
     return _check(lib().moe_ffn_prepare_mxfp8_weights(_p(w1_sf), _p(w2_sf), _p(w1_sf_packed), _p(w2_sf_packed), E, D,
                                                        H, _stream(stream)), "moe_ffn_prepare_mxfp8_weights")
+
+
+def moe_ffn_prepare_nvfp4_weights(w1_sf, w2_sf, w1_sf_packed, w2_sf_packed, E, D, H, stream=None) -> int:
+    """Repack NVFP4 weight scales (e4m3 bytes, one per 16 elements) into the
+    kernels' 512-byte tiles."""
+    for t, n, name in ((w1_sf, E * 2 * H * D // 16, "w1_sf"), (w1_sf_packed, E * 2 * H * D // 16, "w1_sf_packed"),
+                       (w2_sf, E * D * H // 16, "w2_sf"), (w2_sf_packed, E * D * H // 16, "w2_sf_packed")):
+        _need(t, n, name)
+    return _check(lib().moe_ffn_prepare_nvfp4_weights(_p(w1_sf), _p(w2_sf), _p(w1_sf_packed), _p(w2_sf_packed), E, D,
+                                                       H, _stream(stream)), "moe_ffn_prepare_nvfp4_weights")
+
+
+def moe_ffn_forward_nvfp4(x, x_sf, w1, w1_sf, w2, w2_sf, x_gs, w1_gs, w2_gs, act_gs, topk_ids, topk_w, out, *, E, D,
+                          H, k, workspace, T=None, stream=None, check=True) -> int:
+    """Forward pass with NVFP4 operands (split pipeline): packed E2M1 codes
+    (uint8), e4m3 scales per 16 (x_sf row-major, w*_sf repacked), fp32 global
+    scales as device tensors x_gs [1], w1_gs [E], w2_gs [E], act_gs [1]."""
+    T = x.shape[0] if T is None else T
+    for t, n, name in ((x, T * D // 2, "x"), (x_sf, T * D // 16, "x_sf"), (w1, E * 2 * H * D // 2, "w1"),
+                       (w1_sf, E * 2 * H * D // 16, "w1_sf"), (w2, E * D * H // 2, "w2"),
+                       (w2_sf, E * D * H // 16, "w2_sf"), (x_gs, 4, "x_gs"), (w1_gs, 4 * E, "w1_gs"),
+                       (w2_gs, 4 * E, "w2_gs"), (act_gs, 4, "act_gs"), (topk_ids, T * k * 4, "topk_ids"),
+                       (topk_w, T * k * 4, "topk_w"), (out, T * D * 2, "out")):
+        _need(t, n, name)
+    gs = NvFp4Scales(_p(x_gs), _p(w1_gs), _p(w2_gs), _p(act_gs))
+    st = lib().moe_ffn_forward_nvfp4(_p(x), _p(x_sf), _p(w1), _p(w1_sf), _p(w2), _p(w2_sf), ctypes.byref(gs),
+                                     _p(topk_ids), _p(topk_w), _p(out), T, E, D, H, k, _p(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(stream))
+    return _check(st, "moe_ffn_forward_nvfp4") if check else st
 
 
 def moe_ffn_widen_mxfp4_weights(w_fp4, w_e4m3, stream=None) -> int:

@@ -208,6 +208,12 @@ Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipe
   w.pair_order = reinterpret_cast<int*>(take(sizeof(int) * w.max_rb));
   if (pipeline == kRouteOnly) {
     // routing regions only
+  } else if (dtype == MOE_NVFP4) {  // split only: packed codes and e4m3 scales per 16
+    w.xg = take((size_t)w.S_max * D / 2);
+    w.xg_sf = take((size_t)w.S_max * D / 16);
+    w.act = take((size_t)w.S_max * H / 2);
+    w.act_sf = take((size_t)w.S_max * H / 16);
+    if (f32_accum(k)) w.acc_f32 = take((size_t)T * D * 4);
   } else if (dtype != MOE_BF16) {  // MXFP8 activations (e4m3 weights, or MXFP4 weights)
     w.xg = take((size_t)w.S_max * D);
     w.xg_sf = take((size_t)w.S_max * D / 32);
@@ -456,6 +462,73 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
   return cuda_status(e);
 }
 
+// NVFP4 split pipeline: routing, gather of packed rows and their scale tiles
+// (+ zero of out), block-scaled up projection with SwiGLU and NVFP4
+// requantization of act, block-scaled down projection with the reduction.
+moe_status_t forward_split_nvfp4(const Workspace& ws, const void* x, const void* x_sf, const void* w1,
+                                 const void* w1_sf, const void* w2, const void* w2_sf, const moe_ffn_nvfp4_scales_t& gs,
+                                 const int32_t* topk_ids, const float* topk_w, void* out, int T, int E, int D, int H,
+                                 int k, int sms, cudaStream_t st) {
+  CUtensorMap map_xg, map_w1, map_act, map_w2;  // packed codes read as bytes, 256 codes per 128-byte box row
+  if (!make_map_fp8(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D / 2, kBM) ||
+      !make_map_fp8(&map_w1, w1, (uint64_t)E * 2 * H, (uint64_t)D / 2, 128) ||
+      !make_map_fp8(&map_act, ws.act, (uint64_t)ws.S_max, (uint64_t)H / 2, kBM) ||
+      !make_map_fp8(&map_w2, w2, (uint64_t)E * D, (uint64_t)H / 2, 128))  // two 128-row boxes per stage
+    return MOE_ERR_CUDA;
+  prof_mark(st, 0);
+  cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st, nullptr, 0, 0, !g_prof.on);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  prof_mark(st, 1);
+  float* acc = f32_accum(k) ? static_cast<float*>(ws.acc_f32) : nullptr;
+  e = acc ? launch_gather_mx(ws, x, x_sf, topk_ids, T, E, k, D, acc, (int64_t)T * D * 4, sms * g_gather_blocks.load(),
+                             st, !g_prof.on, true)
+          : launch_gather_mx(ws, x, x_sf, topk_ids, T, E, k, D, out, (int64_t)T * D * 2, sms * g_gather_blocks.load(),
+                             st, !g_prof.on, true);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  prof_mark(st, 2);
+  MxArgs ma{};
+  ma.meta = ws.meta;
+  ma.expert_of_rb = ws.expert_of_rb;
+  ma.row_tok = ws.row_tok;
+  ma.slot_w = ws.slot_w;
+  ma.act = ws.act;
+  ma.act_sf = ws.act_sf;
+  ma.out = out;
+  ma.out_f32 = acc;
+  ma.x_gs = gs.x_gs;
+  ma.w1_gs = gs.w1_gs;
+  ma.w2_gs = gs.w2_gs;
+  ma.act_gs = gs.act_gs;
+  ma.err = ws.err;
+  ma.wait_limit_ns = g_wait_limit_ns.load();
+  ma.D = D;
+  ma.H = H;
+  ma.stall_test = g_stall_test.load() == 1 ? 1 : 0;
+  ma.swiglu_limit = ws.swiglu_limit;
+  MxArgs up = ma;
+  up.sf_a = ws.xg_sf;
+  up.sf_b = w1_sf;
+  up.n_col_tiles = H / 128;
+  up.k_blocks = D / 256;
+  prof_front(true);
+  prof_kernel(1, "gather_rows_nv");
+  prof_kernel(2, "up_swiglu_nvfp4");
+  prof_kernel(3, acc ? "down_reduce_nvfp4+f32_to_bf16" : "down_reduce_nvfp4");
+  e = launch_up_nvfp4(map_xg, map_w1, up, (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * up.n_col_tiles), st);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  prof_mark(st, 3);
+  MxArgs dn = ma;
+  dn.sf_a = ws.act_sf;
+  dn.sf_b = w2_sf;
+  dn.n_col_tiles = D / 256;
+  dn.k_blocks = H / 256;
+  e = launch_down_nvfp4(map_act, map_w2, dn, (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * dn.n_col_tiles), st,
+                        !g_prof.on);
+  if (e == cudaSuccess && acc) e = launch_f32_to_bf16(acc, out, (int64_t)T * D, sms * 4, st);
+  prof_mark(st, 4);
+  return cuda_status(e);
+}
+
 // Cluster size for the MXFP8 fused kernel (same estimate as the bf16 one; the
 // act slices are always 128 columns wide).
 int choose_cluster_size_mx(int D, int H, int64_t pairs, int E, int max_rb) {
@@ -593,7 +666,8 @@ using namespace moe;
 extern "C" {
 
 size_t moe_ffn_workspace_size(int T, int E, int D, int H, int k, int dtype, int pipeline) {
-  if (!shape_ok(T, E, D, H, k) || (dtype != MOE_BF16 && dtype != MOE_MXFP8 && dtype != MOE_MXFP4W) ||
+  if (dtype == MOE_NVFP4 && pipeline != MOE_SPLIT) return 0;
+  if (!shape_ok(T, E, D, H, k) || (dtype != MOE_BF16 && dtype != MOE_MXFP8 && dtype != MOE_MXFP4W && dtype != MOE_NVFP4) ||
       (pipeline != MOE_FUSED && pipeline != MOE_SPLIT))
     return 0;
   return plan_workspace(nullptr, T, E, D, H, k, pipeline, dtype).bytes;
@@ -1006,7 +1080,8 @@ static size_t ex_workspace_bytes(int T, int E, int D, int H, int k, int n_shared
 
 size_t moe_ffn_workspace_size_ex(int T, int E, int D, int H, int k, int n_shared, int dtype, int pipeline) {
   if (n_shared < 0 || E + n_shared > kMaxExperts || !shape_ok(T, E + n_shared, D, H, k + n_shared) ||
-      (dtype != MOE_BF16 && dtype != MOE_MXFP8 && dtype != MOE_MXFP4W) || (pipeline != MOE_FUSED && pipeline != MOE_SPLIT))
+      (dtype != MOE_BF16 && dtype != MOE_MXFP8 && dtype != MOE_MXFP4W && dtype != MOE_NVFP4) ||
+      (pipeline != MOE_FUSED && pipeline != MOE_SPLIT) || (dtype == MOE_NVFP4 && pipeline != MOE_SPLIT))
     return 0;
   return ex_workspace_bytes(T, E, D, H, k, n_shared, dtype, pipeline, nullptr);
 }
@@ -1080,6 +1155,46 @@ moe_status_t moe_ffn_debug_mx_quantize(const float* in, int64_t n, uint8_t* q, u
   if (n < 0 || n % 32 || (n > 0 && (!in || !q || !sf))) return MOE_ERR_INVALID_ARG;
   if (n == 0) return MOE_OK;
   return cuda_status(launch_mx_quantize(in, n, q, sf, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_ffn_prepare_nvfp4_weights(const void* w1_sf, const void* w2_sf, void* w1_sf_packed,
+                                           void* w2_sf_packed, int E, int D, int H, void* stream) {
+  if (E < 1 || D < 256 || H < 256 || D % 256 || H % 256) return MOE_ERR_INVALID_ARG;
+  if (!w1_sf || !w2_sf || !w1_sf_packed || !w2_sf_packed) return MOE_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(w1_sf) & 3u) || (reinterpret_cast<uintptr_t>(w2_sf) & 3u) ||
+      !aligned16(w1_sf_packed) || !aligned16(w2_sf_packed))
+    return MOE_ERR_MISALIGNED;
+  const int sms = num_sms();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the packing groups four scale bytes of a row per 512-byte tile: 4 x 32
+  // elements of MXFP8 scales, or 4 x 16 elements of NVFP4 scales (K doubled)
+  cudaError_t e = launch_pack_sf(w1_sf, w1_sf_packed, (int64_t)E * 2 * H, 2 * D, sms * 4, st);
+  if (e == cudaSuccess) e = launch_pack_sf(w2_sf, w2_sf_packed, (int64_t)E * D, 2 * H, sms * 4, st);
+  return cuda_status(e);
+}
+
+moe_status_t moe_ffn_forward_nvfp4(const void* x, const void* x_sf, const void* w1, const void* w1_sf, const void* w2,
+                                   const void* w2_sf, const moe_ffn_nvfp4_scales_t* gs, const int32_t* topk_ids,
+                                   const float* topk_w, void* out, int T, int E, int D, int H, int k,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+  if (!shape_ok(T, E, D, H, k) || D % 256 || H % 256) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !x_sf || !w1 || !w1_sf || !w2 || !w2_sf || !gs || !topk_ids || !topk_w || !out || !workspace)
+    return MOE_ERR_INVALID_ARG;
+  if (!gs->x_gs || !gs->w1_gs || !gs->w2_gs || !gs->act_gs) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w1) || !aligned16(w2) || !aligned16(out) || !aligned16(workspace) ||
+      !aligned16(w1_sf) || !aligned16(w2_sf) || (reinterpret_cast<uintptr_t>(x_sf) & 3u) ||
+      (reinterpret_cast<uintptr_t>(topk_ids) & 3u) || (reinterpret_cast<uintptr_t>(topk_w) & 3u) ||
+      (reinterpret_cast<uintptr_t>(gs->x_gs) & 3u) || (reinterpret_cast<uintptr_t>(gs->w1_gs) & 3u) ||
+      (reinterpret_cast<uintptr_t>(gs->w2_gs) & 3u) || (reinterpret_cast<uintptr_t>(gs->act_gs) & 3u))
+    return MOE_ERR_MISALIGNED;
+  Workspace ws = plan_workspace(workspace, T, E, D, H, k, MOE_SPLIT, MOE_NVFP4);
+  if (workspace_bytes < ws.bytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const int sms = num_sms();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  return forward_split_nvfp4(ws, x, x_sf, w1, w1_sf, w2, w2_sf, *gs, topk_ids, topk_w, out, T, E, D, H, k, sms,
+                             static_cast<cudaStream_t>(stream));
 }
 
 moe_status_t moe_ffn_sync_status(void* workspace, void* stream) {

@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(256)
                             const int* __restrict__ offsets, const int* __restrict__ pad_offsets,
                             const int* __restrict__ row_tok, const int* __restrict__ meta, int T, int E, int k,
                             int vec_per_row, int kt_per_row, uint4* __restrict__ xg, uint8_t* __restrict__ xg_sf,
-                            uint4* __restrict__ out, int out_vecs_per_row) {
+                            uint4* __restrict__ out, int out_vecs_per_row, uint32_t pad_sf) {
   griddep_wait();
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -407,7 +407,8 @@ __global__ void __launch_bounds__(256)
   }
   // scales: one warp per (row block, K tile) writes the blocked 512-byte tile
   // with coalesced 16-byte stores, lane l gathering the 4-byte scale words of
-  // rows l, l + 32, l + 64, l + 96 (padding rows: scale 1.0, e8m0 127)
+  // rows l, l + 32, l + 64, l + 96 (padding rows: pad_sf, an e8m0 scale of 1.0
+  // for MXFP8, a zero e4m3 scale for NVFP4)
   const int64_t n_sf_tiles = (int64_t)meta[0] * kt_per_row;
   for (int64_t q = gwarp; q < n_sf_tiles; q += nwarps) {
     const int64_t rb = q / kt_per_row;
@@ -416,7 +417,7 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       const int tok = row_tok[rb * kRowPad + g * 32 + lane];
-      wv[g] = tok >= 0 ? __ldg(x_sf + (int64_t)tok * kt_per_row + kt) : 0x7f7f7f7fu;
+      wv[g] = tok >= 0 ? __ldg(x_sf + (int64_t)tok * kt_per_row + kt) : pad_sf;
     }
     *reinterpret_cast<uint4*>(xg_sf + sf_tile_offset(rb, kt, kt_per_row) + lane * 16) =
         make_uint4(wv[0], wv[1], wv[2], wv[3]);
@@ -464,7 +465,7 @@ cudaError_t launch_down_mxfp8(const CUtensorMap& act, const CUtensorMap& w2, con
 }
 cudaError_t launch_gather_mx(const Workspace& ws, const void* x, const void* x_sf, const int32_t* topk_ids, int T,
                              int E, int k, int D, void* out, int64_t out_bytes, int grid, cudaStream_t stream,
-                             bool pdl) {
+                             bool pdl, bool nv) {
   if (T == 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -478,9 +479,10 @@ cudaError_t launch_gather_mx(const Workspace& ws, const void* x, const void* x_s
   return cudaLaunchKernelEx(&cfg, gather_tokens_mx_kernel, static_cast<const uint4*>(x),
                             static_cast<const uint32_t*>(x_sf), topk_ids, static_cast<const int*>(ws.slot_of_pair),
                             static_cast<const int*>(ws.offsets), static_cast<const int*>(ws.pad_offsets),
-                            static_cast<const int*>(ws.row_tok), static_cast<const int*>(ws.meta), T, E, k, D / 16,
-                            D / 128, static_cast<uint4*>(ws.xg), static_cast<uint8_t*>(ws.xg_sf),
-                            static_cast<uint4*>(out), out ? (int)(out_bytes / 16 / T) : 0);
+                            static_cast<const int*>(ws.row_tok), static_cast<const int*>(ws.meta), T, E, k,
+                            nv ? D / 32 : D / 16, nv ? D / 64 : D / 128, static_cast<uint4*>(ws.xg),
+                            static_cast<uint8_t*>(ws.xg_sf), static_cast<uint4*>(out),
+                            out ? (int)(out_bytes / 16 / T) : 0, nv ? 0u : 0x7f7f7f7fu);
 }
 cudaError_t launch_pack_sf(const void* sf, void* packed, int64_t rows, int K, int grid, cudaStream_t stream) {
   pack_sf_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint32_t*>(sf), static_cast<uint8_t*>(packed), rows, K);

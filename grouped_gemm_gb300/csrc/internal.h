@@ -283,6 +283,10 @@ struct MxArgs {
   void* out;                // down: bf16 [T, D] reduction target
   float* out_f32;           // down: non-null = fp32 [T, D] reduction target instead of out
   const int* rb_order;      // down: nullptr, or the order in which the row blocks are processed
+  const float* x_gs;        // NVFP4: global scales of x [1], of W1 and W2 per expert [E], of act [1]
+  const float* w1_gs;
+  const float* w2_gs;
+  const float* act_gs;
   const void* sf_a;         // blocked scale tiles of the A operand
   const void* sf_b;         // blocked scale tiles of the weights
   int* err;
@@ -300,9 +304,15 @@ cudaError_t launch_up_mxfp8(const CUtensorMap& a, const CUtensorMap& w1, const M
                             cudaStream_t stream, bool fp4w = false);
 cudaError_t launch_down_mxfp8(const CUtensorMap& act, const CUtensorMap& w2, const MxArgs& args, int grid,
                               cudaStream_t stream, bool pdl, bool fp4w = false);
+// nv: NVFP4 rows (D/2 bytes of packed codes, D/16 e4m3 scales) instead of MXFP8.
 cudaError_t launch_gather_mx(const Workspace& ws, const void* x, const void* x_sf, const int32_t* topk_ids, int T,
                              int E, int k, int D, void* out, int64_t out_bytes, int grid, cudaStream_t stream,
-                             bool pdl);
+                             bool pdl, bool nv = false);
+// NVFP4 split GEMMs (k_blocks = K / 256; the maps read packed codes as bytes).
+cudaError_t launch_up_nvfp4(const CUtensorMap& a, const CUtensorMap& w1, const MxArgs& args, int grid,
+                            cudaStream_t stream);
+cudaError_t launch_down_nvfp4(const CUtensorMap& act, const CUtensorMap& w2, const MxArgs& args, int grid,
+                              cudaStream_t stream, bool pdl);
 cudaError_t launch_pack_sf(const void* sf, void* packed, int64_t rows, int K, int grid, cudaStream_t stream);
 cudaError_t launch_mx_quantize(const float* in, int64_t n, uint8_t* q, uint8_t* sf, cudaStream_t stream);
 

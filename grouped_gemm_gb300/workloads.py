@@ -54,6 +54,8 @@ WORKLOADS = {
     "mxfp8": Workload("mxfp8", 16384, 4096, 1536, 64, 8, "uniform", "mxfp8"),
     # the decode shape with MXFP4 expert weights (MXFP8 activations)
     "decode_mxfp4w": Workload("decode_mxfp4w", 64, 6144, 2048, 32, 8, "uniform", "mxfp4w"),
+    # the decode shape with NVFP4 activations and weights
+    "decode_nvfp4": Workload("decode_nvfp4", 64, 6144, 2048, 32, 8, "uniform", "nvfp4"),
 }
 
 ZIPF_S = 1.1
@@ -251,6 +253,10 @@ def make_inputs(w: Workload | str, seed: int = 0, T: int | None = None):
                 gs[e] = nv4_global_scale(a)
                 q[e], sf[e] = nv4_encode_rows(a, gs[e])
             out[name], out[name + "_sf"], out[name + "_gs"] = q, sf, gs
+        # global scale of act (a calibrated constant of the model, not drawn):
+        # gate and up have standard deviation 0.02 sqrt(D) for these draws, so
+        # act blocks up to 25 (0.02^2 D) keep their e4m3 scale below 448
+        out["act_gs"] = np.float32(25.0 * 0.02 ** 2 * w.D / (6.0 * 448.0))
     elif w.dtype == "mxfp4w":  # MXFP8 activations, MXFP4 weights
         out["x"], out["x_sf"] = mx_encode_rows(_normal(rng, (w.T, w.D), 1.0))
         w1 = np.empty((w.E, 2 * w.H, w.D // 2), np.uint8)

@@ -54,7 +54,7 @@ typedef enum {
   MOE_ERR_CUDA = 7                 /* a CUDA runtime call failed */
 } moe_status_t;
 
-typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1, MOE_MXFP4W = 2 } moe_dtype_t;
+typedef enum { MOE_BF16 = 0, MOE_MXFP8 = 1, MOE_MXFP4W = 2, MOE_NVFP4 = 3 } moe_dtype_t;
 
 /* MOE_FUSED: one GEMM kernel per call, the activation never leaves the SM
  *            ("Prime Flash MoE" sec. 2 "Trick 2", sec. 4).
@@ -95,6 +95,45 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
                              const void* w2_sf, const int32_t* topk_ids, const float* topk_w, void* out, int T, int E,
                              int D, int H, int k, int dtype, int pipeline, void* workspace, size_t workspace_bytes,
                              void* stream);
+
+/* NVFP4 operands ("Porting Block-Scaled GEMM Kernels from Blackwell to
+ * Rubin" sec. 1.2: one scale per 16 elements along K; sec. 6.1: UE4M3 block
+ * scales paired with fp32 global scales, per expert in MoE kernels): every
+ * element is an E2M1 code c (packed two per byte along K, element 2j in bits
+ * 0..3 of byte j), its 16-element block carries a non-negative E4M3 scale s,
+ * and its tensor (each expert, for the weights) an fp32 global scale G: the
+ * value is e2m1(c) * e4m3(s) * G.  act between the GEMMs is requantized the
+ * same way with the global scale act_gs (per 16: s = the E4M3 code nearest to
+ * amax / (6 act_gs), codes = the E2M1 values nearest to v / (e4m3(s) act_gs),
+ * ties to even, saturating at 448 and 6).  All four are device pointers:
+ *   x_gs [1], w1_gs [E], w2_gs [E], act_gs [1]  float32, 4-byte aligned. */
+typedef struct {
+  const float* x_gs;
+  const float* w1_gs;
+  const float* w2_gs;
+  const float* act_gs;
+} moe_ffn_nvfp4_scales_t;
+
+/* One-time repacking of NVFP4 weight scales into the 512-byte tiles the
+ * kernels copy into tensor memory (128 rows x 4 scales, i.e. 64 elements of K
+ * per tile).  w1_sf [E, 2H, D/16] and w2_sf [E, D, H/16] row-major e4m3 bytes
+ * (4-byte aligned); w1_sf_packed (E*2H*D/16 bytes) and w2_sf_packed (E*D*H/16
+ * bytes) 16-byte aligned caller buffers.  D and H multiples of 256. */
+moe_status_t moe_ffn_prepare_nvfp4_weights(const void* w1_sf, const void* w2_sf, void* w1_sf_packed,
+                                           void* w2_sf_packed, int E, int D, int H, void* stream);
+
+/* The forward pass with NVFP4 operands, split pipeline: x [T, D/2] packed
+ * codes with x_sf [T, D/16] e4m3 scales (row-major), W1 [E, 2H, D/2] and
+ * W2 [E, D, H/2] packed codes with scales repacked by
+ * moe_ffn_prepare_nvfp4_weights, the global scales in *gs; out [T, D] bf16,
+ * overwritten.  GEMMs on tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
+ * with both operands packed in shared memory.  Requires D and H multiples of
+ * 256; workspace of moe_ffn_workspace_size(..., MOE_NVFP4, MOE_SPLIT).
+ * Errors as moe_ffn_forward. */
+moe_status_t moe_ffn_forward_nvfp4(const void* x, const void* x_sf, const void* w1, const void* w1_sf, const void* w2,
+                                   const void* w2_sf, const moe_ffn_nvfp4_scales_t* gs, const int32_t* topk_ids,
+                                   const float* topk_w, void* out, int T, int E, int D, int H, int k,
+                                   void* workspace, size_t workspace_bytes, void* stream);
 
 /* The router step upstream of the path ("Prime Flash MoE" sec. 1 takes each
  * token's k experts and their weights, which sum to one, as given; the
