@@ -382,6 +382,7 @@ MOE_OPT_FUSED_DSMEM = 18
 MOE_OPT_HALF_PAIR_M128 = 19
 MOE_OPT_ROUTE_SMALL_PAIRS = 20
 MOE_OPT_DOWN_BANDS = 21
+MOE_OPT_DOWN_EPI8 = 22
 
 
 def moe_ffn_set_option(option: int, value: int) -> int:

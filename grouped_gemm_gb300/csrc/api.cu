@@ -41,6 +41,7 @@ std::atomic<int> g_prefetch_mb{0};    // MOE_OPT_PREFETCH_MB: weights prefetched
 std::atomic<int> g_pair_swap{0};      // MOE_OPT_PAIR_SWAP: max routed rows of a swap-AB pair tile (measured slower: off)
 std::atomic<int> g_wide_up{0};        // MOE_OPT_WIDE_UP: 512-column up tiles on CTA pairs
 std::atomic<int> g_down_bands{1};     // MOE_OPT_DOWN_BANDS: token bands of the down tiles' order (0 automatic, 1 off)
+std::atomic<int> g_down_epi8{1};      // MOE_OPT_DOWN_EPI8: eight epilogue warps in the CTA-pair down kernel
 std::atomic<int> g_half_m128{0};      // MOE_OPT_HALF_PAIR_M128: half pairs as M = 128 pair MMAs (measured no gain: off)
 std::atomic<int> g_fused_dsmem{0};    // MOE_OPT_FUSED_DSMEM: act kept in shared memory in the cluster kernel (measured slower: off)
 std::atomic<int> g_tile_m{0};         // MOE_OPT_TILE_M: rows per tile of the single-CTA split GEMMs (0 automatic)
@@ -746,6 +747,10 @@ moe_status_t moe_ffn_set_option(int option, long long value) {
       if (value < 0 || value > (1 << 20)) return MOE_ERR_INVALID_ARG;
       g_route_small_pairs.store(value);
       return MOE_OK;
+    case MOE_OPT_DOWN_EPI8:
+      if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
+      g_down_epi8.store((int)value);
+      return MOE_OK;
     case MOE_OPT_HALF_PAIR_M128:
       if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
       g_half_m128.store((int)value);
@@ -954,6 +959,7 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
   ga.out_hint = out_hint_for((int64_t)T * D * 2);
   ga.l2_policy = ws.l2_policy;
   ga.half_m128 = g_half_m128.load();
+  ga.down_epi8 = g_down_epi8.load();
 
   const int dyn_opt = g_dynamic_tiles.load();
   const bool small_problem = (int64_t)ws.max_rb * (H / kUpFold) < 8LL * sms;

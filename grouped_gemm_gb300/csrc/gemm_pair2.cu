@@ -54,17 +54,29 @@ namespace moe {
 namespace {
 
 enum { kPairUp = 0, kPairDown = 1 };
-constexpr int kQStages = 6;
-constexpr int kQThreads = 192;
 constexpr int kQA = kBM * kBK * 2;          // 16 KB: this CTA's 128 rows of A
 constexpr int kQB = 128 * kBK * 2;          // 16 KB: this CTA's half of the 256-row B tile
 constexpr int kQStage = kQA + kQB;
-constexpr int kQStageRow = 256 + 16;        // epilogue staging row (+16 B: a warp's rows on distinct banks)
-constexpr int kQStaging = kBM * kQStageRow;
 constexpr int kQBarrierBytes = 256;
-constexpr int kQSmem = kQStages * kQStage + kQStaging + kQBarrierBytes;
-static_assert(kQSmem <= 232448, "shared memory");
-static_assert((2 * kQStages + 7) * 8 + 8 <= kQBarrierBytes, "barrier area");
+// NEPI epilogue warps.  Four: one per TMEM lane quadrant, each thread one
+// accumulator row, staged and reduced as two half rows in turn (staging row of
+// 256 B + 16 B, so a warp's 32 rows fall on distinct banks), six stages.
+// Eight (down projection): two warps per quadrant, one per half row; a warp
+// reads its 128 columns into registers and releases the accumulator before it
+// stages anything, so the MMAs of the next tile but one never wait for the
+// reductions; both half rows of a row share one 528-byte staging row (two
+// 256-byte halves + 16 B), five stages.
+template <int NEPI>
+struct PairCfg {
+  static_assert(NEPI == 4 || NEPI == 8, "epilogue warps");
+  static constexpr int kStages = NEPI == 8 ? 5 : 6;
+  static constexpr int kThreads = 64 + 32 * NEPI;
+  static constexpr int kStageRow = NEPI == 8 ? 2 * 256 + 16 : 256 + 16;
+  static constexpr int kStaging = kBM * kStageRow;
+  static constexpr int kSmem = kStages * kQStage + kStaging + kQBarrierBytes;
+  static_assert(kSmem <= 232448, "shared memory");
+  static_assert((2 * kStages + 7) * 8 + 8 <= kQBarrierBytes, "barrier area");
+};
 constexpr uint64_t kQDrainNs = 200ull * 1000 * 1000;
 constexpr uint64_t kQSettleNs = 2ull * 1000 * 1000;  // abort path: copies in flight land well within this
 
@@ -86,10 +98,14 @@ __device__ __forceinline__ int pair_swap_ns(const GemmArgs& a, int info) {
   return rows <= a.pair_swap_max ? (rows + 15) & ~15 : 0;
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(kQThreads, 1)
+template <int MODE, int NEPI>
+__global__ void __launch_bounds__(PairCfg<NEPI>::kThreads, 1)
     gemm_pair2_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                       const GemmArgs args) {
+  using Cfg = PairCfg<NEPI>;
+  constexpr int kQStages = Cfg::kStages;
+  constexpr int kQStageRow = Cfg::kStageRow;
+  static_assert(MODE == kPairDown || NEPI == 4, "eight epilogue warps: down projection only");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_addr(smem_raw) & 1023u) {  // the same in every CTA: all of them return here
     if (threadIdx.x == 0) atomicOr(args.err, kErrLaunch);
@@ -98,7 +114,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   uint8_t* sA = smem_raw;
   uint8_t* sB = sA + kQStages * kQA;
   uint8_t* sStage = sB + kQStages * kQB;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + kQStaging);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + Cfg::kStaging);
   uint64_t* empty = full + kQStages;
   uint64_t* tfull = empty + kQStages;
   uint64_t* tempty = tfull + 2;
@@ -122,11 +138,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 8);  // even CTA: four epilogue warps of each CTA
+      mbar_init(&tempty[a], 2 * NEPI);  // even CTA: every epilogue warp of each CTA
     }
     mbar_init(drain, 1);
     mbar_init(never, 1);
-    mbar_init(epi_bar, 128);
+    mbar_init(epi_bar, 128);  // the four warps of epilogue half 0
     *abort_flag = 0;
     fence_mbar_init();
     prefetch_tmap(&map_a);
@@ -254,8 +270,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
     // ------------------------------------------------------------ epilogue (both CTAs)
     const int quad = warp & 3;  // TMEM lanes this warp may access
     const int row = quad * 32 + lane;
+    const int ehalf = NEPI == 8 ? (warp - 2) >> 2 : 0;  // eight warps: the half row (128 columns) this warp takes
     const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
-    uint8_t* my_stage = sStage + row * kQStageRow;
+    uint8_t* my_stage = sStage + row * kQStageRow + ehalf * 256;
     const uint32_t tempty_leader0 = mapa_shared(smem_addr(&tempty[0]), 0);
     // barrier of this CTA's 128 epilogue threads (bounded, unlike bar.sync)
     uint32_t epi_ph = 0;
@@ -281,9 +298,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
                                 : (int64_t)((info >> 1) + (int)rank) * kBM + row;
       const int tok = (m128 || rank == 0 || (info & 1)) ? args.row_tok[slot] : -1;
       const bool valid = tok >= 0;
+      bool released = false;  // this warp has already told the MMA issuer it read the accumulator
       if (MODE == kPairDown && m128) {
-        // output columns j*256 + 128*half .. +128 of the row
-        {
+        // output columns j*256 + 128*half .. +128 of the row (the four warps of
+        // epilogue half 0; with eight warps the others have nothing to read)
+        if (ehalf == 0) {
           const float w = valid ? args.slot_w[slot] : 0.f;
           uint32_t v[4][32];
           tmem_ld_x32_pair(tacc, tacc + 32, v[0], v[1]);
@@ -317,6 +336,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
             }
           }
         }
+      } else if (MODE == kPairDown && ns > 0 && ehalf != 0) {
+        // swap-AB tiles are read by the four warps of epilogue half 0
       } else if (MODE == kPairDown && ns > 0) {
         // Swap-AB tile: TMEM lane `row` is output column j*256 + 128*rank + row,
         // column c is routed row c of the pair (slot (info >> 1) * 128 + c).
@@ -386,11 +407,12 @@ __global__ void __launch_bounds__(kQThreads, 1)
           bulk_commit();
         }
       } else if (args.out_f32) {
-        // fp32 reduction target: four quarter rows of 64 columns (256 bytes staged each)
+        // fp32 reduction target: quarter rows of 64 columns (256 bytes staged
+        // each), all four by one warp, or two by each of a quadrant's two warps
         const float w = valid ? args.slot_w[slot] : 0.f;
         float* frow = args.out_f32 + (int64_t)(tok < 0 ? 0 : tok) * args.D + j * 256;
 #pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 4 / (NEPI / 4) * ehalf; q < 4 / (NEPI / 4) * (ehalf + 1); ++q) {
           bulk_wait_read_all();        // the previous reduction has left the staging row
           uint32_t v0[32], v1[32];
           tmem_ld_x32_pair(tacc + q * 64, tacc + q * 64 + 32, v0, v1);
@@ -401,6 +423,33 @@ __global__ void __launch_bounds__(kQThreads, 1)
             bulk_reduce_add_f32(frow + q * 64, my_stage, 256);
             bulk_commit();
           }
+        }
+      } else if (NEPI == 8) {
+        // this warp's half row: 128 columns into registers, the accumulator
+        // released, then staged and reduced while the MMAs go on
+        const float w = valid ? args.slot_w[slot] : 0.f;
+        uint32_t v[4][32];
+        const uint32_t tcol = tacc + ehalf * 128;
+        tmem_ld_x32_pair(tcol, tcol + 32, v[0], v[1]);
+        tmem_ld_x32_pair(tcol + 64, tcol + 96, v[2], v[3]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty_leader0 + acc * 8);
+        released = true;
+        if (tok >= 0) {
+          bulk_wait_read_all();  // the previous tile's reduction has left the staging half row
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              st_shared_v4(my_stage + c * 64 + q * 16, pack_bf16x2(w * q_u2f(v[c][8 * q + 0]), w * q_u2f(v[c][8 * q + 1])),
+                           pack_bf16x2(w * q_u2f(v[c][8 * q + 2]), w * q_u2f(v[c][8 * q + 3])),
+                           pack_bf16x2(w * q_u2f(v[c][8 * q + 4]), w * q_u2f(v[c][8 * q + 5])),
+                           pack_bf16x2(w * q_u2f(v[c][8 * q + 6]), w * q_u2f(v[c][8 * q + 7])));
+          fence_proxy_async_smem();
+          bulk_reduce_add_bf16_hint(static_cast<__nv_bfloat16*>(args.out) + (int64_t)tok * args.D + j * 256 + ehalf * 128,
+                                    my_stage, 256, args.out_hint != 0, l2_policy_evict_last());
+          bulk_commit();
         }
       } else {
         const float w = valid ? args.slot_w[slot] : 0.f;
@@ -436,9 +485,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
         }
       }
       // this warp has read the accumulator: tell the even CTA's MMA issuer
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(tempty_leader0 + acc * 8);
+      if (!released) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty_leader0 + acc * 8);
+      }
     }
     bulk_wait_all();  // bulk stores / reductions complete before the CTA exits
   }
@@ -454,10 +505,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
   }
 }
 
-template <int MODE>
+template <int MODE, int NEPI>
 cudaError_t launch_pair2(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args, int n_pairs,
                          cudaStream_t stream, bool pdl) {
-  auto kern = gemm_pair2_kernel<MODE>;
+  auto kern = gemm_pair2_kernel<MODE, NEPI>;
+  constexpr int kQSmem = PairCfg<NEPI>::kSmem;
   // once per device: not a stream operation, so it stays out of graph capture
   static bool smem_set[64] = {};
   int dev = 0;
@@ -469,7 +521,7 @@ cudaError_t launch_pair2(const CUtensorMap& a, const CUtensorMap& b, const GemmA
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * n_pairs);
-  cfg.blockDim = dim3(kQThreads);
+  cfg.blockDim = dim3(PairCfg<NEPI>::kThreads);
   cfg.dynamicSmemBytes = kQSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
@@ -492,11 +544,12 @@ int pair_cluster_slots() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   if (cache[dev]) return cache[dev];
-  auto kern = gemm_pair2_kernel<kPairUp>;
+  auto kern = gemm_pair2_kernel<kPairUp, 4>;
+  constexpr int kQSmem = PairCfg<4>::kSmem;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2);
-  cfg.blockDim = dim3(kQThreads);
+  cfg.blockDim = dim3(PairCfg<4>::kThreads);
   cfg.dynamicSmemBytes = kQSmem;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -516,12 +569,13 @@ int pair_cluster_slots() {
 
 cudaError_t launch_up_pair2_bf16(const CUtensorMap& map_xg, const CUtensorMap& map_w1, const GemmArgs& args,
                                  int n_pairs, cudaStream_t stream, bool pdl) {
-  return launch_pair2<kPairUp>(map_xg, map_w1, args, n_pairs, stream, pdl);
+  return launch_pair2<kPairUp, 4>(map_xg, map_w1, args, n_pairs, stream, pdl);
 }
 
 cudaError_t launch_down_pair2_bf16(const CUtensorMap& map_act, const CUtensorMap& map_w2, const GemmArgs& args,
                                    int n_pairs, cudaStream_t stream, bool pdl) {
-  return launch_pair2<kPairDown>(map_act, map_w2, args, n_pairs, stream, pdl);
+  return args.down_epi8 ? launch_pair2<kPairDown, 8>(map_act, map_w2, args, n_pairs, stream, pdl)
+                        : launch_pair2<kPairDown, 4>(map_act, map_w2, args, n_pairs, stream, pdl);
 }
 
 }  // namespace moe

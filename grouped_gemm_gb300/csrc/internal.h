@@ -107,6 +107,7 @@ struct GemmArgs {
   const int* pair_order;    // down: nullptr, or the order in which the block pairs are processed
   int half_m128;            // CTA-pair down kernel: a half pair runs as one M = 128 pair MMA (else M = 256,
                             //   the odd CTA recomputing the first block and storing nothing)
+  int down_epi8;            // CTA-pair down kernel: eight epilogue warps (else four)
 };
 
 // Routing; when zero_out != nullptr the first launch also zero-fills

@@ -491,6 +491,13 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   expert order within a band), so that its reductions into
  *                   an out larger than L2 meet the rows of one band at a time
  *                   in L2; the weights are then read once per band.
+ *   MOE_OPT_DOWN_EPI8  1 (default) or 0: eight epilogue warps in the
+ *                   CTA-pair down projection (two per TMEM lane quadrant, one
+ *                   per half row: each reads its 128 accumulator columns into
+ *                   registers and releases the accumulator before it stages
+ *                   and reduces them; five pipeline stages), or four (one per
+ *                   quadrant, each row staged and reduced as two half rows in
+ *                   turn while the accumulator is held; six stages).
  *   (MOE_OPT_L2_POLICY measured at prefill: 0.343 ms with 0, 0.349 with 1,
  *                   0.342 with 2, 0.348 with 3: no gain, off.) */
 typedef enum {
@@ -515,7 +522,8 @@ typedef enum {
   MOE_OPT_FUSED_DSMEM = 18,
   MOE_OPT_HALF_PAIR_M128 = 19,
   MOE_OPT_ROUTE_SMALL_PAIRS = 20,
-  MOE_OPT_DOWN_BANDS = 21
+  MOE_OPT_DOWN_BANDS = 21,
+  MOE_OPT_DOWN_EPI8 = 22
 } moe_option_t;
 moe_status_t moe_ffn_set_option(int option, long long value);
 
