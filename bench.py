@@ -134,6 +134,8 @@ KERNEL_SOURCES = {
     "up_pair_bf16": ["grouped_gemm_gb300/csrc/gemm_pair.cu"] + _PTX,
     "up_swiglu_mxfp8": ["grouped_gemm_gb300/csrc/gemm_mxfp8.cu"] + _MXH + _PTX,
     "down_reduce_mxfp8": ["grouped_gemm_gb300/csrc/gemm_mxfp8.cu"] + _MXH + _PTX,
+    "up_swiglu_mxfp8_pair2": ["grouped_gemm_gb300/csrc/gemm_mxfp8_pair.cu"] + _MXH + _PTX,
+    "down_reduce_mxfp8_pair2": ["grouped_gemm_gb300/csrc/gemm_mxfp8_pair.cu"] + _MXH + _PTX,
     "up_swiglu_mxfp4w": ["grouped_gemm_gb300/csrc/gemm_mxfp8.cu"] + _MXH + _PTX,
     "up_swiglu_nvfp4": ["grouped_gemm_gb300/csrc/gemm_nvfp4.cu"] + _MXH + _PTX,
     "down_reduce_nvfp4": ["grouped_gemm_gb300/csrc/gemm_nvfp4.cu"] + _MXH + _PTX,

@@ -383,6 +383,8 @@ MOE_OPT_HALF_PAIR_M128 = 19
 MOE_OPT_ROUTE_SMALL_PAIRS = 20
 MOE_OPT_DOWN_BANDS = 21
 MOE_OPT_DOWN_EPI8 = 22
+MOE_OPT_MX_PAIRS = 23
+MOE_OPT_UP_SWAP = 24
 
 
 def moe_ffn_set_option(option: int, value: int) -> int:

@@ -41,6 +41,8 @@ std::atomic<int> g_prefetch_mb{0};    // MOE_OPT_PREFETCH_MB: weights prefetched
 std::atomic<int> g_pair_swap{0};      // MOE_OPT_PAIR_SWAP: max routed rows of a swap-AB pair tile (measured slower: off)
 std::atomic<int> g_wide_up{0};        // MOE_OPT_WIDE_UP: 512-column up tiles on CTA pairs
 std::atomic<int> g_down_bands{1};     // MOE_OPT_DOWN_BANDS: token bands of the down tiles' order (0 automatic, 1 off)
+std::atomic<int> g_up_swap{1};        // MOE_OPT_UP_SWAP: swap-AB half pairs in the CTA-pair up kernel
+std::atomic<int> g_mx_pairs{0};       // MOE_OPT_MX_PAIRS: MXFP8 split GEMMs on CTA pairs (0 off: measured slower, 1 on, 2 automatic)
 std::atomic<int> g_down_epi8{1};      // MOE_OPT_DOWN_EPI8: eight epilogue warps in the CTA-pair down kernel
 std::atomic<int> g_half_m128{0};      // MOE_OPT_HALF_PAIR_M128: half pairs as M = 128 pair MMAs (measured no gain: off)
 std::atomic<int> g_fused_dsmem{0};    // MOE_OPT_FUSED_DSMEM: act kept in shared memory in the cluster kernel (measured slower: off)
@@ -126,6 +128,21 @@ bool make_map_fp4(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Blocked scale tiles [tiles x 512 bytes] seen as a [tiles, 128] u32 tensor,
+// one tile per box (no swizzle: a tile lands in shared memory as stored).
+bool make_map_sf(CUtensorMap* m, const void* base, uint64_t tiles) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {128, tiles};
+  cuuint64_t strides[1] = {512};
+  cuuint32_t box[2] = {128, 1};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -399,13 +416,25 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
                                  const void* w1_sf, const void* w2, const void* w2_sf, const int32_t* topk_ids,
                                  const float* topk_w, void* out, int T, int E, int D, int H, int k, int sms,
                                  cudaStream_t st, bool fp4w) {
-  CUtensorMap map_xg, map_w1, map_act, map_w2;
+  // CTA pairs (e4m3 weights) unless the problem is small: decode-sized
+  // problems stream weights, and single CTAs spread over more SMs
+  const int mxp_opt = g_mx_pairs.load();
+  const bool small = (int64_t)ws.max_rb * (H / 128) < 8LL * sms;
+  const bool pairs = !fp4w && (mxp_opt == 1 || (mxp_opt == 2 && !small));
+  CUtensorMap map_xg, map_w1, map_act, map_w2, sf_xg, sf_w1, sf_act, sf_w2;
   auto make_w = fp4w ? make_map_fp4 : make_map_fp8;
   if (!make_map_fp8(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, kBM) ||
       !make_w(&map_w1, w1, (uint64_t)E * 2 * H, (uint64_t)D, 128) ||
       !make_map_fp8(&map_act, ws.act, (uint64_t)ws.S_max, (uint64_t)H, kBM) ||
-      !make_w(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, 256))
+      !make_w(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, pairs ? 128 : 256))
     return MOE_ERR_CUDA;
+  if (pairs && (!make_map_sf(&sf_xg, ws.xg_sf, (uint64_t)(ws.S_max / 128) * (D / 128)) ||
+                !make_map_sf(&sf_w1, w1_sf, (uint64_t)E * (2 * H / 128) * (D / 128)) ||
+                !make_map_sf(&sf_act, ws.act_sf, (uint64_t)(ws.S_max / 128) * (H / 128)) ||
+                !make_map_sf(&sf_w2, w2_sf, (uint64_t)E * (D / 128) * (H / 128))))
+    return MOE_ERR_CUDA;
+  const int mx_slots = pairs ? mx_pair_cluster_slots() : 0;
+  if (pairs && mx_slots <= 0) return MOE_ERR_CUDA;
   prof_mark(st, 0);
   cudaError_t e = launch_route(ws, topk_ids, topk_w, T, E, k, st, nullptr, 0, 0, !g_prof.on);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -423,6 +452,7 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
   MxArgs ma{};
   ma.meta = ws.meta;
   ma.expert_of_rb = ws.expert_of_rb;
+  ma.pair_info = ws.pair_info;
   ma.row_tok = ws.row_tok;
   ma.slot_w = ws.slot_w;
   ma.act = ws.act;
@@ -443,21 +473,31 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
   up.k_blocks = D / 128;
   prof_front(true);
   if (bands > 1) prof_kernel(1, "gather_rows_mx+band_order");
-  prof_kernel(2, fp4w ? "up_swiglu_mxfp4w" : "up_swiglu_mxfp8");
-  prof_kernel(3, fp4w ? (acc ? "down_reduce_mxfp4w+f32_to_bf16" : "down_reduce_mxfp4w")
-                      : (acc ? "down_reduce_mxfp8+f32_to_bf16" : "down_reduce_mxfp8"));
-  e = launch_up_mxfp8(map_xg, map_w1, up, (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * up.n_col_tiles), st,
-                      fp4w);
+  prof_kernel(2, fp4w ? "up_swiglu_mxfp4w" : pairs ? "up_swiglu_mxfp8_pair2" : "up_swiglu_mxfp8");
+  prof_kernel(3, fp4w    ? (acc ? "down_reduce_mxfp4w+f32_to_bf16" : "down_reduce_mxfp4w")
+                 : pairs ? (acc ? "down_reduce_mxfp8_pair2+f32_to_bf16" : "down_reduce_mxfp8_pair2")
+                         : (acc ? "down_reduce_mxfp8+f32_to_bf16" : "down_reduce_mxfp8"));
+  if (pairs)
+    e = launch_up_mxfp8_pair(map_xg, map_w1, sf_xg, sf_w1, up,
+                             (int)std::min<int64_t>(mx_slots, (int64_t)ws.max_rb * up.n_col_tiles), st);
+  else
+    e = launch_up_mxfp8(map_xg, map_w1, up, (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * up.n_col_tiles), st,
+                        fp4w);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_mark(st, 3);
   MxArgs dn = ma;
   dn.rb_order = bands > 1 ? ws.rb_order : nullptr;
+  dn.pair_order = bands > 1 ? ws.pair_order : nullptr;
   dn.sf_a = ws.act_sf;
   dn.sf_b = w2_sf;
   dn.n_col_tiles = D / 256;
   dn.k_blocks = H / 128;
-  e = launch_down_mxfp8(map_act, map_w2, dn, (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * dn.n_col_tiles), st,
-                        !g_prof.on, fp4w);
+  if (pairs)
+    e = launch_down_mxfp8_pair(map_act, map_w2, sf_act, sf_w2, dn,
+                               (int)std::min<int64_t>(mx_slots, (int64_t)ws.max_rb * dn.n_col_tiles), st, !g_prof.on);
+  else
+    e = launch_down_mxfp8(map_act, map_w2, dn, (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * dn.n_col_tiles), st,
+                          !g_prof.on, fp4w);
   if (e == cudaSuccess && acc) e = launch_f32_to_bf16(acc, out, (int64_t)T * D, sms * 4, st);
   prof_mark(st, 4);
   return cuda_status(e);
@@ -747,6 +787,14 @@ moe_status_t moe_ffn_set_option(int option, long long value) {
       if (value < 0 || value > (1 << 20)) return MOE_ERR_INVALID_ARG;
       g_route_small_pairs.store(value);
       return MOE_OK;
+    case MOE_OPT_UP_SWAP:
+      if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
+      g_up_swap.store((int)value);
+      return MOE_OK;
+    case MOE_OPT_MX_PAIRS:
+      if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
+      g_mx_pairs.store((int)value);
+      return MOE_OK;
     case MOE_OPT_DOWN_EPI8:
       if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
       g_down_epi8.store((int)value);
@@ -903,13 +951,14 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
   const bool m64 = !pair_mma && !in_gemm_gather && !g_up_pairs.load() &&
                    (tile_m_opt == 64 || (tile_m_opt == 0 && P <= 64 * std::min<int64_t>(P, E)));
   const int bm = m64 ? 64 : kBM;
-  CUtensorMap map_xg, map_w1, map_act, map_w2;
+  CUtensorMap map_xg, map_w1, map_w1_64, map_act, map_w2;
   const bool map_a_ok = in_gemm_gather ? make_map_bf16(&map_xg, x, (uint64_t)T, (uint64_t)D, 1)
                                        : make_map_bf16(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, bm);
   if (!map_a_ok ||
       !make_map_bf16(&map_w1, w1, (uint64_t)E * 2 * H, (uint64_t)D, fold) ||
       !make_map_bf16(&map_act, ws.act, (uint64_t)ws.S_max, (uint64_t)H, bm) ||
-      !make_map_bf16(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, pair_down ? 128 : down_n))
+      !make_map_bf16(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, pair_down ? 128 : down_n) ||
+      (pair_mma && !make_map_bf16(&map_w1_64, w1, (uint64_t)E * 2 * H, (uint64_t)D, 64)))
     return MOE_ERR_CUDA;
 
   prof_mark(st, 0);
@@ -960,6 +1009,7 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
   ga.l2_policy = ws.l2_policy;
   ga.half_m128 = g_half_m128.load();
   ga.down_epi8 = g_down_epi8.load();
+  ga.up_swap = g_up_swap.load();
 
   const int dyn_opt = g_dynamic_tiles.load();
   const bool small_problem = (int64_t)ws.max_rb * (H / kUpFold) < 8LL * sms;
@@ -991,7 +1041,7 @@ static moe_status_t forward_entry(const void* x, const void* x_sf, const void* w
                                   (int)std::min<int64_t>(wide_slots, (int64_t)ws.max_rb * ((up.n_col_tiles + 1) / 2)),
                                   st, !g_prof.on);
   else if (pair_mma)
-    e = launch_up_pair2_bf16(map_xg, map_w1, up,
+    e = launch_up_pair2_bf16(map_xg, map_w1, map_w1_64, up,
                              (int)std::min<int64_t>(pair_slots, (int64_t)ws.max_rb * up.n_col_tiles), st, !g_prof.on);
   else if (gather == 0 && g_up_pairs.load())
     e = launch_up_pair_bf16(map_xg, map_w1, up, up_grid, st);

@@ -39,6 +39,17 @@
 // transposed accumulator (lane = output column, column = routed row) into the
 // staging tile row by row and reduces each staged row into out as usual.
 //
+// Swap-AB half pairs (UP, args.up_swap): an expert's odd last row block holds
+// at most 128 routed rows, yet a half pair pays for a full 256 x 256 MMA.  With
+// the operands swapped the tensor cores do 256 x ns per K step (ns = the
+// block's routed rows rounded up to 16): the M side is 256 W1 rows, each CTA
+// loading [gate 64 | up 64] rows for its 64 act columns c (two 64-row boxes),
+// and the N side the block's routed rows, ns / 2 in each CTA.  A CTA's
+// accumulator then holds gate column c in lane c and up column c in lane
+// 64 + c, routed row r in TMEM column r: the warps of lane quadrants 2 and 3
+// pass their up values through shared memory (fp32) to the warps of quadrants
+// 0 and 1, which form silu(gate) * up and store act.
+//
 // Synchronization: both CTAs' TMA loads complete on the even CTA's full[]
 // barrier (which expects the pair's bytes); the MMA commits arrive on empty[]
 // and tfull[] of both CTAs (multicast); each CTA's epilogue warps arrive on the
@@ -89,6 +100,15 @@ __device__ __forceinline__ float q_swiglu(float g, float u, float lim) {
   return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
+// N of a swap-AB up tile: a half pair's routed rows rounded up to 16, or 0
+// for a normal tile (every role of both CTAs derives it from the same tables).
+__device__ __forceinline__ int up_swap_ns(const GemmArgs& a, int info) {
+  if (!a.up_swap || (info & 1)) return 0;
+  const int rb0 = info >> 1, e = a.expert_of_rb[rb0];
+  const int rows = min(kBM, a.counts[e] - (rb0 * kBM - a.pad_offsets[e]));
+  return (rows + 15) & ~15;
+}
+
 // N of a swap-AB pair tile (routed rows of the pair rounded up to 16), or 0
 // for a normal tile.  Every role of both CTAs derives it from the same tables.
 __device__ __forceinline__ int pair_swap_ns(const GemmArgs& a, int info) {
@@ -101,7 +121,7 @@ __device__ __forceinline__ int pair_swap_ns(const GemmArgs& a, int info) {
 template <int MODE, int NEPI>
 __global__ void __launch_bounds__(PairCfg<NEPI>::kThreads, 1)
     gemm_pair2_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                      const GemmArgs args) {
+                      const __grid_constant__ CUtensorMap map_b64, const GemmArgs args) {
   using Cfg = PairCfg<NEPI>;
   constexpr int kQStages = Cfg::kStages;
   constexpr int kQStageRow = Cfg::kStageRow;
@@ -147,6 +167,7 @@ __global__ void __launch_bounds__(PairCfg<NEPI>::kThreads, 1)
     fence_mbar_init();
     prefetch_tmap(&map_a);
     prefetch_tmap(&map_b);
+    if (MODE == kPairUp && args.up_swap) prefetch_tmap(&map_b64);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, 512);
@@ -187,7 +208,9 @@ __global__ void __launch_bounds__(PairCfg<NEPI>::kThreads, 1)
                                        : e * args.D + j * 256 + (int)rank * 128;
       // swap-AB: this CTA's half of the ns routed rows (the TMA box still moves
       // 128 rows; the MMA reads the first ns / 2)
-      const int ns = MODE == kPairDown ? pair_swap_ns(args, info) : 0;
+      const int ns = MODE == kPairDown ? pair_swap_ns(args, info) : up_swap_ns(args, info);
+      // swap-AB UP: gate and up rows of this CTA's 64 act columns of tile j
+      const int wrow = e * 2 * args.H + j * 128 + (int)rank * 64;
       // DOWN half pair (M = 128): this CTA's 64 rows of the block (the box
       // moves 128 rows; the MMA reads the first 64)
       const bool m128 = MODE == kPairDown && !two && !ns && args.half_m128;
@@ -199,7 +222,10 @@ __global__ void __launch_bounds__(PairCfg<NEPI>::kThreads, 1)
         if (leader) mbar_arrive_expect_tx(&full[s], 2 * kQStage);
         const uint32_t fb = mapa_shared(smem_addr(&full[s]), 0);
         tma_load_2d_pair(sA + s * kQA, &map_a, fb, kb * kBK, arow);
-        if (args.l2_policy & 1)  // weight tiles are read by one pair: evict them first
+        if (MODE == kPairUp && ns) {
+          tma_load_2d_pair(sB + s * kQB, &map_b64, fb, kb * kBK, wrow);
+          tma_load_2d_pair(sB + s * kQB + kQB / 2, &map_b64, fb, kb * kBK, wrow + args.H);
+        } else if (args.l2_policy & 1)  // weight tiles are read by one pair: evict them first
           tma_load_2d_pair_hint(sB + s * kQB, &map_b, fb, kb * kBK, brow, l2_policy_evict_first());
         else
           tma_load_2d_pair(sB + s * kQB, &map_b, fb, kb * kBK, brow);
@@ -231,7 +257,7 @@ __global__ void __launch_bounds__(PairCfg<NEPI>::kThreads, 1)
       if (!(ok = mbar_wait_cluster(&tempty[acc], ((uint32_t)(it >> 1) & 1u) ^ 1u, wc, 62))) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * 256;
-      const int ns = MODE == kPairDown ? pair_swap_ns(args, tile_pair(tile / NJ)) : 0;
+      const int ns = MODE == kPairDown ? pair_swap_ns(args, tile_pair(tile / NJ)) : up_swap_ns(args, tile_pair(tile / NJ));
       const uint32_t idesc_swap = idesc_bf16_f32(2 * kBM, ns ? ns : 16);
       // DOWN: a half pair runs as one M = 128 pair MMA (64 rows in each CTA)
       const bool m128_t = MODE == kPairDown && !ns && args.half_m128 && !(tile_pair(tile / NJ) & 1);
@@ -289,7 +315,7 @@ __global__ void __launch_bounds__(PairCfg<NEPI>::kThreads, 1)
       tc_fence_after();
       const int info = tile_pair(tile / NJ), j = tile % NJ;
       const uint32_t tacc = lane_base + acc * 256;
-      const int ns = MODE == kPairDown ? pair_swap_ns(args, info) : 0;
+      const int ns = MODE == kPairDown ? pair_swap_ns(args, info) : up_swap_ns(args, info);
       const bool m128 = MODE == kPairDown && !(info & 1) && !ns && args.half_m128;
       // m128: TMEM lane row (0..127) holds columns [128 * half, +128) of tile row
       // (row & 63), the block's row rank * 64 + (row & 63)
@@ -384,6 +410,48 @@ __global__ void __launch_bounds__(PairCfg<NEPI>::kThreads, 1)
           }
         }
         if (failed) break;
+      } else if (MODE == kPairUp && ns > 0) {
+        // Swap-AB half pair: lane c / 64 + c hold gate / up of act column
+        // 64 * rank + c, TMEM column r routed row r of the block.  U[r][c]
+        // (fp32, 256 B a row) stages the up values in the staging area.
+        const int64_t slot0 = (int64_t)(info >> 1) * kBM;
+        float* U = reinterpret_cast<float*>(sStage);
+        bulk_wait_read_all();  // this thread's last store has left its staging row
+        if (!epi_sync(69)) break;  // every staging row free, the previous tile's U reads done
+        if (quad >= 2) {
+#pragma unroll 1
+          for (int r0 = 0; r0 < ns; r0 += 32) {
+            uint32_t a[32];
+            tmem_ld_x32(tacc + r0, a);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) U[(r0 + i) * 64 + (row - 64)] = q_u2f(a[i]);
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(tempty_leader0 + acc * 8);
+          released = true;
+        }
+        if (!epi_sync(70)) break;  // U complete
+        if (quad < 2) {
+          __nv_bfloat16* acol = static_cast<__nv_bfloat16*>(args.act) + j * 128 + (int)rank * 64 + row;
+#pragma unroll 1
+          for (int r0 = 0; r0 < ns; r0 += 32) {
+            uint32_t a[32];
+            tmem_ld_x32(tacc + r0, a);
+            const int tk = r0 + lane < ns ? args.row_tok[slot0 + r0 + lane] : -1;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int tki = __shfl_sync(0xffffffffu, tk, i);
+              if (tki >= 0)
+                acol[(slot0 + r0 + i) * args.H] = __float2bfloat16(q_swiglu(q_u2f(a[i]), U[(r0 + i) * 64 + row], swiglu_lim));
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(tempty_leader0 + acc * 8);
+          released = true;
+        }
+        if (!epi_sync(71)) break;  // U read: the staging area is free for the next tile
       } else if (MODE == kPairUp) {
         if (tok >= 0) bulk_wait_read_all();  // the previous tile's store has left the staging row
 #pragma unroll 1
@@ -506,8 +574,8 @@ __global__ void __launch_bounds__(PairCfg<NEPI>::kThreads, 1)
 }
 
 template <int MODE, int NEPI>
-cudaError_t launch_pair2(const CUtensorMap& a, const CUtensorMap& b, const GemmArgs& args, int n_pairs,
-                         cudaStream_t stream, bool pdl) {
+cudaError_t launch_pair2(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b64, const GemmArgs& args,
+                         int n_pairs, cudaStream_t stream, bool pdl) {
   auto kern = gemm_pair2_kernel<MODE, NEPI>;
   constexpr int kQSmem = PairCfg<NEPI>::kSmem;
   // once per device: not a stream operation, so it stays out of graph capture
@@ -533,7 +601,7 @@ cudaError_t launch_pair2(const CUtensorMap& a, const CUtensorMap& b, const GemmA
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, kern, a, b, args);
+  return cudaLaunchKernelEx(&cfg, kern, a, b, b64, args);
 }
 
 }  // namespace
@@ -567,15 +635,15 @@ int pair_cluster_slots() {
   return n;
 }
 
-cudaError_t launch_up_pair2_bf16(const CUtensorMap& map_xg, const CUtensorMap& map_w1, const GemmArgs& args,
-                                 int n_pairs, cudaStream_t stream, bool pdl) {
-  return launch_pair2<kPairUp, 4>(map_xg, map_w1, args, n_pairs, stream, pdl);
+cudaError_t launch_up_pair2_bf16(const CUtensorMap& map_xg, const CUtensorMap& map_w1, const CUtensorMap& map_w1_64,
+                                 const GemmArgs& args, int n_pairs, cudaStream_t stream, bool pdl) {
+  return launch_pair2<kPairUp, 4>(map_xg, map_w1, map_w1_64, args, n_pairs, stream, pdl);
 }
 
 cudaError_t launch_down_pair2_bf16(const CUtensorMap& map_act, const CUtensorMap& map_w2, const GemmArgs& args,
                                    int n_pairs, cudaStream_t stream, bool pdl) {
-  return args.down_epi8 ? launch_pair2<kPairDown, 8>(map_act, map_w2, args, n_pairs, stream, pdl)
-                        : launch_pair2<kPairDown, 4>(map_act, map_w2, args, n_pairs, stream, pdl);
+  return args.down_epi8 ? launch_pair2<kPairDown, 8>(map_act, map_w2, map_w2, args, n_pairs, stream, pdl)
+                        : launch_pair2<kPairDown, 4>(map_act, map_w2, map_w2, args, n_pairs, stream, pdl);
 }
 
 }  // namespace moe

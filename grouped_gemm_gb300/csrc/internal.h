@@ -108,6 +108,7 @@ struct GemmArgs {
   int half_m128;            // CTA-pair down kernel: a half pair runs as one M = 128 pair MMA (else M = 256,
                             //   the odd CTA recomputing the first block and storing nothing)
   int down_epi8;            // CTA-pair down kernel: eight epilogue warps (else four)
+  int up_swap;              // CTA-pair up kernel: half pairs run as swap-AB tiles
 };
 
 // Routing; when zero_out != nullptr the first launch also zero-fills
@@ -153,8 +154,9 @@ cudaError_t launch_up_pair_bf16(const CUtensorMap& map_a, const CUtensorMap& map
 // tile); n_pairs pairs of CTAs are launched as two-CTA clusters.  Up: fold
 // 128, map_w1 boxes of 128 rows.  Down: 256-column tiles, map_w2 boxes of 128
 // rows.
-cudaError_t launch_up_pair2_bf16(const CUtensorMap& map_xg, const CUtensorMap& map_w1, const GemmArgs& args,
-                                 int n_pairs, cudaStream_t stream, bool pdl);
+// map_w1_64: W1 in boxes of 64 rows (the swap-AB half pairs, args.up_swap)
+cudaError_t launch_up_pair2_bf16(const CUtensorMap& map_xg, const CUtensorMap& map_w1, const CUtensorMap& map_w1_64,
+                                 const GemmArgs& args, int n_pairs, cudaStream_t stream, bool pdl);
 cudaError_t launch_down_pair2_bf16(const CUtensorMap& map_act, const CUtensorMap& map_w2, const GemmArgs& args,
                                    int n_pairs, cudaStream_t stream, bool pdl);
 // Co-resident two-CTA clusters of the pair kernels on the current device.
@@ -284,6 +286,8 @@ struct MxArgs {
   void* out;                // down: bf16 [T, D] reduction target
   float* out_f32;           // down: non-null = fp32 [T, D] reduction target instead of out
   const int* rb_order;      // down: nullptr, or the order in which the row blocks are processed
+  const int* pair_info;     // CTA-pair kernels: pairs of row blocks of one expert (see Workspace)
+  const int* pair_order;    // CTA-pair down kernel: nullptr, or the order of the block pairs
   const float* x_gs;        // NVFP4: global scales of x [1], of W1 and W2 per expert [E], of act [1]
   const float* w1_gs;
   const float* w2_gs;
@@ -314,6 +318,15 @@ cudaError_t launch_up_nvfp4(const CUtensorMap& a, const CUtensorMap& w1, const M
                             cudaStream_t stream);
 cudaError_t launch_down_nvfp4(const CUtensorMap& act, const CUtensorMap& w2, const MxArgs& args, int grid,
                               cudaStream_t stream, bool pdl);
+// MXFP8 GEMMs on CTA pairs (cta_group::2): map_a / map_b in boxes of 128 rows,
+// sfa / sfb the blocked scale tiles as [tiles, 128] u32 maps (make_map_sf).
+cudaError_t launch_up_mxfp8_pair(const CUtensorMap& a, const CUtensorMap& w1, const CUtensorMap& sfa,
+                                 const CUtensorMap& sfb, const MxArgs& args, int n_pairs, cudaStream_t stream);
+cudaError_t launch_down_mxfp8_pair(const CUtensorMap& act, const CUtensorMap& w2, const CUtensorMap& sfa,
+                                   const CUtensorMap& sfb, const MxArgs& args, int n_pairs, cudaStream_t stream,
+                                   bool pdl);
+// co-resident two-CTA clusters of the MXFP8 pair kernels (0 on error)
+int mx_pair_cluster_slots();
 cudaError_t launch_pack_sf(const void* sf, void* packed, int64_t rows, int K, int grid, cudaStream_t stream);
 cudaError_t launch_mx_quantize(const float* in, int64_t n, uint8_t* q, uint8_t* sf, cudaStream_t stream);
 

@@ -498,6 +498,25 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   and reduces them; five pipeline stages), or four (one per
  *                   quadrant, each row staged and reduced as two half rows in
  *                   turn while the accumulator is held; six stages).
+ *   MOE_OPT_MX_PAIRS  0 (default: off), 1 or 2 (automatic): the MXFP8 split
+ *                   pipeline's GEMMs (e4m3 weights) on CTA pairs
+ *                   (tcgen05 cta_group::2, M = 256 rows of two row blocks of
+ *                   one expert, each CTA holding half of the weight tile; the
+ *                   A scales of a CTA's rows and the B scales of all 256
+ *                   columns copied into each CTA's tensor memory); automatic
+ *                   uses them unless the problem is decode-sized (fewer than
+ *                   8 x SMs row-block x column tiles).  Measured on GB300,
+ *                   mxfp8 workload, same box: step 2.20 ms with pairs against
+ *                   2.13 ms without (up kernel 1.30 against 1.22 ms, down
+ *                   0.79-0.81 against 0.78-0.80 ms): off.
+ *   MOE_OPT_UP_SWAP  1 (default) or 0: in the CTA-pair up projection an
+ *                   expert's odd last row block (a half pair) runs with the
+ *                   operands swapped: 256 W1 rows ([gate 64 | up 64] of each
+ *                   CTA's 64 act columns) as the MMA's M side and the block's
+ *                   routed rows, rounded up to 16, as its N side, so the
+ *                   tensor cores do 256 x ns rather than 256 x 256 per K
+ *                   step; 0 runs it as a full pair whose odd CTA repeats the
+ *                   block and stores nothing.
  *   (MOE_OPT_L2_POLICY measured at prefill: 0.343 ms with 0, 0.349 with 1,
  *                   0.342 with 2, 0.348 with 3: no gain, off.) */
 typedef enum {
@@ -523,7 +542,9 @@ typedef enum {
   MOE_OPT_HALF_PAIR_M128 = 19,
   MOE_OPT_ROUTE_SMALL_PAIRS = 20,
   MOE_OPT_DOWN_BANDS = 21,
-  MOE_OPT_DOWN_EPI8 = 22
+  MOE_OPT_DOWN_EPI8 = 22,
+  MOE_OPT_MX_PAIRS = 23,
+  MOE_OPT_UP_SWAP = 24
 } moe_option_t;
 moe_status_t moe_ffn_set_option(int option, long long value);
 

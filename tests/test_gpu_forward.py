@@ -39,6 +39,7 @@ MODES = {
     "split_pair2_half128": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 1, moe.MOE_OPT_HALF_PAIR_M128: 1}),
     "split_pair2_bands": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 1, moe.MOE_OPT_DOWN_BANDS: 3}),
     "split_pair2_epi4": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 1, moe.MOE_OPT_DOWN_EPI8: 0}),
+    "split_pair2_noswap": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 1, moe.MOE_OPT_UP_SWAP: 0}),
     "split_wide": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 1, moe.MOE_OPT_WIDE_UP: 1}),
     "split_m64": (moe.MOE_SPLIT, {moe.MOE_OPT_PAIR_MMA: 0, moe.MOE_OPT_TILE_M: 64}),
     "fused": (moe.MOE_FUSED, {}),
@@ -48,7 +49,7 @@ MODES = {
 DEFAULTS = {moe.MOE_OPT_UP_PAIRS: 0, moe.MOE_OPT_GATHER: 0, moe.MOE_OPT_SWAP_AB: 0, moe.MOE_OPT_FUSED_CLUSTER: 1,
             moe.MOE_OPT_PAIR_MMA: 2, moe.MOE_OPT_PAIR_SWAP: 0, moe.MOE_OPT_WIDE_UP: 0, moe.MOE_OPT_TILE_M: 0,
             moe.MOE_OPT_FUSED_DSMEM: 0, moe.MOE_OPT_HALF_PAIR_M128: 0, moe.MOE_OPT_DOWN_BANDS: 1,
-            moe.MOE_OPT_DOWN_EPI8: 1}
+            moe.MOE_OPT_DOWN_EPI8: 1, moe.MOE_OPT_UP_SWAP: 1}
 PIPELINES = list(MODES)
 
 
