@@ -59,6 +59,8 @@ def parse_args():
                     help="start each step from router logits [T, E] (moe_ffn_forward_logits: top-k and softmax "
                          "fused into the routing launch) instead of given top-k ids and weights")
     ap.add_argument("--no-graph", action="store_true", help="launch each step eagerly instead of replaying a CUDA graph")
+    ap.add_argument("--host-chunk", type=int, default=0,
+                    help="e2e: token chunk of the host-buffer entry point (0: the library's automatic choice)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the workload's token count T (a smaller case of the same kernels, for profiling)")
     ap.add_argument("--no-also", action="store_true",
@@ -504,8 +506,22 @@ def bench_workload(args, name, pipeline_name, rank, world, sampler, full=True):
         twh = torch.from_numpy(inp["topk_w"]).pin_memory()
         lgh = torch.from_numpy(logits_np).pin_memory() if logits is not None else None
         outh = torch.empty(w.T, w.D, dtype=torch.bfloat16).pin_memory()
+        # the host-buffer entry point (copies of one token chunk overlap the
+        # computation of the neighbouring chunks) where it applies; router
+        # logits and NVFP4: copies in, the step, the copy out, one after another
+        host_api = logits is None and not nv
+        if host_api:
+            hws = torch.empty(moe.moe_ffn_host_workspace_size(w.T, w.E, w.D, w.H, w.k, dtype, pipeline,
+                                                              chunk_tokens=args.host_chunk),
+                              dtype=torch.uint8, device="cuda")
+            moe.moe_ffn_workspace_init(hws)
 
         def e2e_step():
+            if host_api:
+                moe.moe_ffn_forward_host(xh, dev["w1"], dev["w2"], idh, twh, outh, E=w.E, D=w.D, H=w.H, k=w.k,
+                                         workspace=hws, dtype=dtype, pipeline=pipeline, x_sf=xsfh,
+                                         w1_sf=dev.get("w1_sf"), w2_sf=dev.get("w2_sf"), chunk_tokens=args.host_chunk)
+                return
             dev["x"].copy_(xh, non_blocking=True)
             if mx:
                 dev["x_sf"].copy_(xsfh, non_blocking=True)
@@ -533,7 +549,14 @@ def bench_workload(args, name, pipeline_name, rank, world, sampler, full=True):
                "h2d_bytes_per_step": int(xh.numel() * xh.element_size() + (xsfh.numel() if mx else 0) +
                                          (lgh.numel() * 4 if logits is not None else idh.numel() * 4 + twh.numel() * 4)),
                "d2h_bytes_per_step": int(outh.numel() * 2), "ms_per_step": round(e_ms, 4),
-               "resident": "expert weights stay in HBM (model parameters)"}
+               "resident": "expert weights stay in HBM (model parameters)",
+               "call": (f"moe_ffn_forward_host (token chunks: {args.host_chunk or 'automatic'}; copies overlap "
+                        "the neighbouring chunks' computation)" if host_api else
+                        "copies in, the forward call, the copy out")}
+        if host_api:
+            st = moe.moe_ffn_sync_status(hws)
+            if st != 0:
+                raise SystemExit(f"device status after the host-buffer calls: {moe.moe_ffn_status_string(st)}")
     line["e2e"] = e2e
     line["cpu_baseline"] = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -15,6 +15,7 @@ import threading
 __all__ = [
     "MOE_BF16", "MOE_MXFP8", "MOE_MXFP4W", "MOE_NVFP4", "MOE_FUSED", "MOE_SPLIT", "MoeFFNError", "library_path", "lib",
     "moe_ffn_workspace_size", "moe_ffn_workspace_init", "moe_ffn_forward", "moe_ffn_forward_logits", "moe_ffn_forward_ex", "MoeFFNExtras",
+    "moe_ffn_host_workspace_size", "moe_ffn_forward_host",
     "moe_ffn_workspace_size_ex", "moe_ffn_router_topk", "moe_ffn_route", "moe_ffn_route_noalloc",
     "moe_ffn_sync_status", "moe_ffn_set_wait_limit_ns", "moe_ffn_profile_enable", "moe_ffn_profile_read", "moe_ffn_profile_stage_kernel", "moe_ffn_set_option", "MOE_OPT_GATHER", "moe_ffn_prepare_mxfp8_weights", "moe_ffn_widen_mxfp4_weights", "moe_ffn_debug_mx_quantize", "moe_ffn_status_string", "alloc_workspace",
 ]
@@ -71,6 +72,10 @@ def lib() -> ctypes.CDLL:
             L.moe_ffn_router_topk.restype = i
             L.moe_ffn_forward_logits.argtypes = [vp] * 10 + [i] * 7 + [vp, sz, vp]
             L.moe_ffn_forward_logits.restype = i
+            L.moe_ffn_host_workspace_size.argtypes = [i] * 8
+            L.moe_ffn_host_workspace_size.restype = sz
+            L.moe_ffn_forward_host.argtypes = [vp] * 9 + [i] * 8 + [vp, sz, vp]
+            L.moe_ffn_forward_host.restype = i
             L.moe_ffn_workspace_size_ex.argtypes = [i] * 8
             L.moe_ffn_workspace_size_ex.restype = sz
             L.moe_ffn_forward_ex.argtypes = [vp] * 9 + [i] * 7 + [c.POINTER(MoeFFNExtras), vp, sz, vp]
@@ -206,6 +211,38 @@ def moe_ffn_forward(x, w1, w2, topk_ids, topk_w, out, *, E, D, H, k, workspace, 
                                _p(out), T, E, D, H, k, dtype, pipeline, _p(workspace),
                                workspace.numel() * workspace.element_size(), _stream(stream))
     return _check(st, "moe_ffn_forward") if check else st
+
+
+def moe_ffn_host_workspace_size(T, E, D, H, k, dtype=MOE_BF16, pipeline=MOE_SPLIT, chunk_tokens=0) -> int:
+    return int(lib().moe_ffn_host_workspace_size(T, chunk_tokens, E, D, H, k, dtype, pipeline))
+
+
+def _host_p(t, nbytes, name):
+    """Address of a host (CPU) tensor argument holding at least nbytes."""
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError(f"{name}: expected a host tensor, got one on {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+    _need(t, nbytes, name)
+    return t.data_ptr()
+
+
+def moe_ffn_forward_host(x, w1, w2, topk_ids, topk_w, out, *, E, D, H, k, workspace, dtype=MOE_BF16,
+                         pipeline=MOE_SPLIT, x_sf=None, w1_sf=None, w2_sf=None, chunk_tokens=0, T=None, stream=None,
+                         check=True) -> int:
+    """moe_ffn_forward_host: x (x_sf), topk_ids, topk_w and out are host tensors
+    (page-locked for overlapped copies), the weights and workspace CUDA tensors."""
+    T = x.shape[0] if T is None else T
+    eb = 2 if dtype == MOE_BF16 else 1
+    _need_forward(None, None, w1, w1_sf, w2, w2_sf, None, None, None, T, E, D, H, k, dtype)
+    st = lib().moe_ffn_forward_host(
+        _host_p(x, T * D * eb, "x"), _host_p(x_sf, T * D // 32, "x_sf"), _p(w1), _p(w1_sf), _p(w2), _p(w2_sf),
+        _host_p(topk_ids, T * k * 4, "topk_ids"), _host_p(topk_w, T * k * 4, "topk_w"),
+        _host_p(out, T * D * 2, "out"), T, E, D, H, k, dtype, pipeline, chunk_tokens, _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    return _check(st, "moe_ffn_forward_host") if check else st
 
 
 def moe_ffn_forward_logits(x, w1, w2, router_logits, topk_ids, topk_w, out, *, E, D, H, k, workspace,
@@ -385,6 +422,7 @@ MOE_OPT_DOWN_BANDS = 21
 MOE_OPT_DOWN_EPI8 = 22
 MOE_OPT_MX_PAIRS = 23
 MOE_OPT_UP_SWAP = 24
+MOE_OPT_ROUTE_TPB = 25
 
 
 def moe_ffn_set_option(option: int, value: int) -> int:

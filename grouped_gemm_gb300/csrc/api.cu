@@ -41,6 +41,7 @@ std::atomic<int> g_prefetch_mb{0};    // MOE_OPT_PREFETCH_MB: weights prefetched
 std::atomic<int> g_pair_swap{0};      // MOE_OPT_PAIR_SWAP: max routed rows of a swap-AB pair tile (measured slower: off)
 std::atomic<int> g_wide_up{0};        // MOE_OPT_WIDE_UP: 512-column up tiles on CTA pairs
 std::atomic<int> g_down_bands{1};     // MOE_OPT_DOWN_BANDS: token bands of the down tiles' order (0 automatic, 1 off)
+constexpr int kHostChunkTokens = 16384;  // moe_ffn_forward_host: automatic chunk size
 std::atomic<int> g_up_swap{1};        // MOE_OPT_UP_SWAP: swap-AB half pairs in the CTA-pair up kernel
 std::atomic<int> g_mx_pairs{0};       // MOE_OPT_MX_PAIRS: MXFP8 split GEMMs on CTA pairs (0 off: measured slower, 1 on, 2 automatic)
 std::atomic<int> g_down_epi8{1};      // MOE_OPT_DOWN_EPI8: eight epilogue warps in the CTA-pair down kernel
@@ -190,6 +191,7 @@ void prof_front(bool mx) {
 
 std::atomic<int> g_route_coop{1};
 std::atomic<int> g_router_fused{0};
+std::atomic<int> g_route_tpb{0};  // MOE_OPT_ROUTE_TPB: tokens per routing block (0: 256)
 std::atomic<int64_t> g_route_small_pairs{8192};
 
 Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipeline, int dtype) {
@@ -202,7 +204,9 @@ Workspace plan_workspace(void* base, int T, int E, int D, int H, int k, int pipe
   w.S_max = (int64_t)align_up((size_t)(P + live_experts * (kRowPad - 1)), kRowPad);
   if (w.S_max == 0) w.S_max = kRowPad;
   w.max_rb = (int)(w.S_max / kRowPad);
-  w.route_blocks = (T + kRouteTokPerBlock - 1) / kRouteTokPerBlock;
+  // tokens per routing block: by option (64, 128 or 256), else the default
+  w.route_tpb = g_route_tpb.load() ? g_route_tpb.load() : kRouteTokPerBlock;
+  w.route_blocks = (T + w.route_tpb - 1) / w.route_tpb;
   if (w.route_blocks == 0) w.route_blocks = 1;
   uint8_t* b = static_cast<uint8_t*>(base);
   size_t off = 0;
@@ -787,6 +791,10 @@ moe_status_t moe_ffn_set_option(int option, long long value) {
       if (value < 0 || value > (1 << 20)) return MOE_ERR_INVALID_ARG;
       g_route_small_pairs.store(value);
       return MOE_OK;
+    case MOE_OPT_ROUTE_TPB:
+      if (value != 0 && value != 64 && value != 128 && value != 256) return MOE_ERR_INVALID_ARG;
+      g_route_tpb.store((int)value);
+      return MOE_OK;
     case MOE_OPT_UP_SWAP:
       if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
       g_up_swap.store((int)value);
@@ -1073,6 +1081,151 @@ moe_status_t moe_ffn_forward(const void* x, const void* x_sf, const void* w1, co
                              void* stream) {
   return forward_entry(x, x_sf, w1, w1_sf, w2, w2_sf, topk_ids, topk_w, out, T, E, D, H, k, dtype, pipeline,
                        workspace, workspace_bytes, stream, nullptr);
+}
+
+// ---------------------------------------------------------------- host buffers
+// Forward pass from host memory, tokens in chunks: the copy in of chunk c + 1
+// (copy stream 1), the forward pass of chunk c (the caller's stream) and the
+// copy out of chunk c - 1 (copy stream 2) run at the same time; two sets of
+// device staging buffers alternate.  The copy streams and events are created
+// once per device; a host mutex keeps one call's enqueue sequence whole.
+namespace {
+struct HostPipe {
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, in_ready[2] = {}, computed[2] = {}, out_done[2] = {};
+  bool ok = false;
+};
+std::mutex g_host_mu;
+HostPipe g_host_pipe[64];
+
+HostPipe* host_pipe() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  HostPipe& p = g_host_pipe[dev];
+  if (p.ok) return &p;
+  bool ok = cudaStreamCreateWithFlags(&p.in, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&p.out, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaEventCreateWithFlags(&p.start, cudaEventDisableTiming) == cudaSuccess;
+  for (int b = 0; ok && b < 2; ++b)
+    ok = cudaEventCreateWithFlags(&p.in_ready[b], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&p.computed[b], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&p.out_done[b], cudaEventDisableTiming) == cudaSuccess;
+  p.ok = ok;
+  return ok ? &p : nullptr;
+}
+
+int host_chunk_tokens(int T, int chunk_tokens) {
+  if (chunk_tokens > 0) return std::min(chunk_tokens, std::max(T, 1));
+  // automatic: whole problems up to 8192 tokens (their copies are short, and
+  // smaller chunks lose GEMM efficiency); above, T / 8 rounded up to 128
+  // tokens, at least 4096 (every chunk streams the weights once more) and at
+  // most 16384
+  if (T <= 8192) return std::max(T, 1);
+  const int c = (int)(((int64_t)T + 8 * 128 - 1) / (8 * 128) * 128);
+  return std::min(kHostChunkTokens, std::max(4096, c));
+}
+
+struct HostLayout {
+  size_t fwd = 0, x = 0, x_sf = 0, ids = 0, tw = 0, out = 0, set = 0, bytes = 0;
+};
+HostLayout host_layout(int Tc, int E, int D, int H, int k, int dtype, int pipeline) {
+  HostLayout l;
+  l.fwd = align_up(plan_workspace(nullptr, Tc, E, D, H, k, pipeline, dtype).bytes, 256);
+  l.x = align_up((size_t)Tc * D * (dtype == MOE_BF16 ? 2 : 1), 256);
+  l.x_sf = dtype == MOE_BF16 ? 0 : align_up((size_t)Tc * D / 32, 256);
+  l.ids = align_up((size_t)Tc * k * 4, 256);
+  l.tw = l.ids;
+  l.out = align_up((size_t)Tc * D * 2, 256);
+  l.set = l.x + l.x_sf + l.ids + l.tw + l.out;
+  l.bytes = l.fwd + 2 * l.set;
+  return l;
+}
+}  // namespace
+
+size_t moe_ffn_host_workspace_size(int T, int chunk_tokens, int E, int D, int H, int k, int dtype, int pipeline) {
+  if (chunk_tokens < 0 || (dtype != MOE_BF16 && dtype != MOE_MXFP8 && dtype != MOE_MXFP4W)) return 0;
+  const int Tc = host_chunk_tokens(T, chunk_tokens);
+  if (moe_ffn_workspace_size(Tc, E, D, H, k, dtype, pipeline) == 0) return 0;
+  return host_layout(Tc, E, D, H, k, dtype, pipeline).bytes;
+}
+
+moe_status_t moe_ffn_forward_host(const void* x_host, const void* x_sf_host, const void* w1, const void* w1_sf,
+                                  const void* w2, const void* w2_sf, const int32_t* topk_ids_host,
+                                  const float* topk_w_host, void* out_host, int T, int E, int D, int H, int k,
+                                  int dtype, int pipeline, int chunk_tokens, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  if (!shape_ok(T, E, D, H, k) || chunk_tokens < 0) return MOE_ERR_INVALID_ARG;
+  if (dtype != MOE_BF16 && dtype != MOE_MXFP8 && dtype != MOE_MXFP4W) return MOE_ERR_INVALID_ARG;
+  if (pipeline != MOE_FUSED && pipeline != MOE_SPLIT) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x_host || !topk_ids_host || !topk_w_host || !out_host || !workspace || (dtype != MOE_BF16 && !x_sf_host))
+    return MOE_ERR_INVALID_ARG;
+  const int Tc = host_chunk_tokens(T, chunk_tokens);
+  const HostLayout l = host_layout(Tc, E, D, H, k, dtype, pipeline);
+  if (workspace_bytes < l.bytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  const size_t row = (size_t)D * (dtype == MOE_BF16 ? 2 : 1), row_sf = (size_t)D / 32;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  struct Set {
+    uint8_t *x, *x_sf, *ids, *tw, *out;
+  } set[2];
+  for (int b = 0; b < 2; ++b) {
+    uint8_t* p = base + l.fwd + b * l.set;
+    set[b].x = p;
+    set[b].x_sf = p + l.x;
+    set[b].ids = p + l.x + l.x_sf;
+    set[b].tw = set[b].ids + l.ids;
+    set[b].out = set[b].tw + l.tw;
+  }
+  std::lock_guard<std::mutex> lock(g_host_mu);
+  HostPipe* hp = host_pipe();
+  if (!hp) return MOE_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const uint8_t* xh = static_cast<const uint8_t*>(x_host);
+  const uint8_t* xsh = static_cast<const uint8_t*>(x_sf_host);
+  uint8_t* oh = static_cast<uint8_t*>(out_host);
+  // both copy streams start behind everything already queued on the caller's stream
+  cudaError_t e = cudaEventRecord(hp->start, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->in, hp->start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->out, hp->start, 0);
+  const int n_chunks = (T + Tc - 1) / Tc;
+  moe_status_t rs = MOE_OK;
+  for (int c = 0; c < n_chunks && e == cudaSuccess && rs == MOE_OK; ++c) {
+    const int b = c & 1, t0 = c * Tc, tn = std::min(Tc, T - t0);
+    Set& sb = set[b];
+    // in: buffers of set b are free once chunk c - 2's forward pass has read them
+    if (c >= 2) e = cudaStreamWaitEvent(hp->in, hp->computed[b], 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(sb.x, xh + (size_t)t0 * row, (size_t)tn * row, cudaMemcpyHostToDevice, hp->in);
+    if (e == cudaSuccess && dtype != MOE_BF16)
+      e = cudaMemcpyAsync(sb.x_sf, xsh + (size_t)t0 * row_sf, (size_t)tn * row_sf, cudaMemcpyHostToDevice, hp->in);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(sb.ids, topk_ids_host + (size_t)t0 * k, (size_t)tn * k * 4, cudaMemcpyHostToDevice, hp->in);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(sb.tw, topk_w_host + (size_t)t0 * k, (size_t)tn * k * 4, cudaMemcpyHostToDevice, hp->in);
+    if (e == cudaSuccess) e = cudaEventRecord(hp->in_ready[b], hp->in);
+    // forward pass of chunk c on the caller's stream, into out set b once
+    // chunk c - 2's copy out has read it
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, hp->in_ready[b], 0);
+    if (e == cudaSuccess && c >= 2) e = cudaStreamWaitEvent(st, hp->out_done[b], 0);
+    if (e != cudaSuccess) break;
+    rs = forward_entry(sb.x, dtype == MOE_BF16 ? nullptr : sb.x_sf, w1, w1_sf, w2, w2_sf,
+                       reinterpret_cast<const int32_t*>(sb.ids), reinterpret_cast<const float*>(sb.tw), sb.out, tn,
+                       E, D, H, k, dtype, pipeline, workspace, l.fwd, stream, nullptr);
+    if (rs != MOE_OK) break;
+    e = cudaEventRecord(hp->computed[b], st);
+    // out
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->out, hp->computed[b], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(oh + (size_t)t0 * D * 2, sb.out, (size_t)tn * D * 2, cudaMemcpyDeviceToHost, hp->out);
+    if (e == cudaSuccess) e = cudaEventRecord(hp->out_done[b], hp->out);
+  }
+  // the caller's stream waits for the last copies out (and the copy streams
+  // are joined back, so the call is one unit of work on the caller's stream)
+  if (e == cudaSuccess) e = cudaEventRecord(hp->start, hp->out);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, hp->start, 0);
+  if (e == cudaSuccess) e = cudaEventRecord(hp->in_ready[0], hp->in);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, hp->in_ready[0], 0);
+  if (rs != MOE_OK) return rs;
+  return cuda_status(e);
 }
 
 moe_status_t moe_ffn_forward_logits(const void* x, const void* x_sf, const void* w1, const void* w1_sf,

@@ -15,7 +15,7 @@ constexpr int kBM = 128;          // rows per tile = tcgen05 MMA M
 constexpr int kBK = 64;           // K elements per pipeline stage (128 B of bf16)
 constexpr int kRowPad = 128;      // per-expert row segments are padded to this
 constexpr int kMaxExperts = 1024;
-constexpr int kRouteTokPerBlock = 256;  // tokens per routing block
+constexpr int kRouteTokPerBlock = 256;  // tokens per routing block (default; Workspace::route_tpb)
 // From this many routed pairs per token on, the rows of a token are summed in
 // fp32 (a [T, D] workspace accumulator, rounded to bf16 once at the end)
 // instead of by bf16 reductions into out: each bf16 reduction rounds the
@@ -50,6 +50,7 @@ struct Workspace {
   size_t bytes;        // total bytes required
   int64_t S_max;       // padded slot capacity (multiple of 128)
   int max_rb;
+  int route_tpb;       // tokens per routing block (MOE_OPT_ROUTE_TPB)
   int route_blocks;
   // Not a region of the workspace: the call's router logits [T, E] fp32 when
   // the call starts from them (moe_ffn_forward_logits), else nullptr.

@@ -142,8 +142,9 @@ __global__ void __launch_bounds__(256) router_topk_kernel(const float* __restric
 }
 
 __global__ void __launch_bounds__(256) route_count_kernel(const int32_t* __restrict__ ids, int64_t P, int E, int k,
-                                                          int NB, int* __restrict__ blk_counts, int* __restrict__ err,
-                                                          uint4* __restrict__ zero_out, int64_t zero_vecs) {
+                                                          int NB, int tpb, int* __restrict__ blk_counts,
+                                                          int* __restrict__ err, uint4* __restrict__ zero_out,
+                                                          int64_t zero_vecs) {
   extern __shared__ int hist[];
   if (zero_out) {  // every block of the (possibly wider) grid helps zero-fill the reduction target
     const uint4 z = make_uint4(0, 0, 0, 0);
@@ -154,8 +155,8 @@ __global__ void __launch_bounds__(256) route_count_kernel(const int32_t* __restr
   if ((int)blockIdx.x >= NB) return;
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
-  const int64_t p0 = (int64_t)blockIdx.x * kRouteTokPerBlock * k;
-  const int64_t p1 = min(P, p0 + (int64_t)kRouteTokPerBlock * k);
+  const int64_t p0 = (int64_t)blockIdx.x * tpb * k;
+  const int64_t p1 = min(P, p0 + (int64_t)tpb * k);
   bool bad = false;
   for (int64_t p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
     const int e = ids[p];
@@ -346,7 +347,7 @@ __device__ __forceinline__ void scatter_range(const int32_t* ids, const float* t
 
 __global__ void __launch_bounds__(kScatterWarps * 32)
     route_scatter_kernel(const int32_t* __restrict__ ids, const float* __restrict__ topk_w, int64_t P, int E, int k,
-                         const int* __restrict__ blk_base, const int* __restrict__ offsets,
+                         int tpb, const int* __restrict__ blk_base, const int* __restrict__ offsets,
                          const int* __restrict__ pad_offsets, int* __restrict__ row_tok, float* __restrict__ slot_w,
                          int* __restrict__ slot_of_pair) {
   extern __shared__ int wcnt[];  // [kScatterWarps][E], then offsets[E], pad_offsets[E]
@@ -355,8 +356,8 @@ __global__ void __launch_bounds__(kScatterWarps * 32)
   griddep_wait();  // programmatic dependent of the scan launch
   griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t p0 = (int64_t)blockIdx.x * kRouteTokPerBlock * k;
-  const int64_t p1 = min(P, p0 + (int64_t)kRouteTokPerBlock * k);
+  const int64_t p0 = (int64_t)blockIdx.x * tpb * k;
+  const int64_t p1 = min(P, p0 + (int64_t)tpb * k);
   const int64_t sub = (p1 - p0 + kScatterWarps - 1) / kScatterWarps;
   const int64_t q0 = min(p1, p0 + warp * sub), q1 = min(p1, q0 + sub);
   for (int i = threadIdx.x; i < kScatterWarps * E; i += blockDim.x) wcnt[i] = 0;
@@ -509,6 +510,7 @@ struct CoopRouteArgs {
   const float* topk_w;
   int64_t P;
   int E, k, NB;
+  int tpb;  // tokens per block
   int* err;
   unsigned long long wait_limit_ns;
   int* blk;
@@ -563,8 +565,8 @@ __global__ void __launch_bounds__(kCoopWarps * 32) route_coop_kernel(const CoopR
   __shared__ int warp_sums[32];
   const int E = a.E, k = a.k, b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t p0 = (int64_t)b * kRouteTokPerBlock * k;
-  const int64_t p1 = min(a.P, p0 + (int64_t)kRouteTokPerBlock * k);
+  const int64_t p0 = (int64_t)b * a.tpb * k;
+  const int64_t p1 = min(a.P, p0 + (int64_t)a.tpb * k);
   const int64_t sub = (p1 - p0 + kCoopWarps - 1) / kCoopWarps;
   const int64_t q0 = min(p1, p0 + warp * sub), q1 = min(p1, q0 + sub);
   const int32_t* ids = a.ids;
@@ -904,6 +906,7 @@ cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const flo
     ca.E = E;
     ca.k = k;
     ca.NB = NB;
+    ca.tpb = ws.route_tpb;
     ca.err = ws.err;
     ca.wait_limit_ns = ws.wait_limit_ns;
     ca.blk = ws.blk_base;
@@ -933,8 +936,8 @@ cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const flo
   const int grid = zero_out ? (NB > zero_grid ? NB : zero_grid) : NB;
   t_route_kernels = router_first ? "router_topk+route_count+route_scan+route_scatter"
                                  : "route_count+route_scan+route_scatter";
-  route_count_kernel<<<grid, 256, E * sizeof(int), stream>>>(topk_ids, P, E, k, NB, ws.blk_base, ws.err,
-                                                             static_cast<uint4*>(zero_out), zero_bytes / 16);
+  route_count_kernel<<<grid, 256, E * sizeof(int), stream>>>(topk_ids, P, E, k, NB, ws.route_tpb, ws.blk_base,
+                                                             ws.err, static_cast<uint4*>(zero_out), zero_bytes / 16);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // the scan and the scatter start as programmatic dependents (their launch
@@ -955,7 +958,7 @@ cudaError_t launch_route(const Workspace& ws, const int32_t* topk_ids, const flo
   cfg.blockDim = dim3(kScatterWarps * 32);
   cfg.dynamicSmemBytes = (kScatterWarps + 2) * E * sizeof(int);
   return cudaLaunchKernelEx(&cfg, route_scatter_kernel, static_cast<const int32_t*>(topk_ids), topk_w, P, E, k,
-                            static_cast<const int*>(ws.blk_base), static_cast<const int*>(ws.offsets),
+                            ws.route_tpb, static_cast<const int*>(ws.blk_base), static_cast<const int*>(ws.offsets),
                             static_cast<const int*>(ws.pad_offsets), ws.row_tok, ws.slot_w, ws.slot_of_pair);
 }
 

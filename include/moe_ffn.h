@@ -135,6 +135,37 @@ moe_status_t moe_ffn_forward_nvfp4(const void* x, const void* x_sf, const void* 
                                    const float* topk_w, void* out, int T, int E, int D, int H, int k,
                                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* The forward pass from and to HOST memory: x (and x_sf), topk_ids and
+ * topk_w are read from host memory, out is written to host memory; the
+ * weights (and their scales) and the workspace are device memory as for
+ * moe_ffn_forward.  The tokens are processed in chunks of chunk_tokens
+ * (0: automatic: the whole problem up to 8192 tokens, else T / 8 rounded up
+ * to a multiple of 128, within [4096, 16384]; the last chunk may be shorter): while chunk c runs on `stream`, chunk c + 1
+ * is copied in and chunk c - 1 copied out on two copy streams of the library,
+ * through two sets of device staging buffers in the workspace.  Each chunk is
+ * one moe_ffn_forward call, so each output row is exactly what
+ * moe_ffn_forward gives for that token.
+ *   Layouts as moe_ffn_forward (dtype MOE_BF16, MOE_MXFP8 or MOE_MXFP4W).
+ *   Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister):
+ *   copies from or to pageable memory are correct but block the calling
+ *   thread and do not overlap the computation.
+ *   workspace: moe_ffn_host_workspace_size(T, chunk_tokens, ...) bytes of
+ *   device memory; its first bytes are the forward workspace of a chunk, so
+ *   moe_ffn_sync_status(workspace) reads the call's status words.
+ * Asynchronous on stream: the work queued on stream before the call comes
+ * first, and everything the call does (copies included) completes before the
+ * work queued on stream after it; the host buffers must stay valid and out
+ * unread until then.  Calls on one device are serialized on the host (one
+ * mutex) while they enqueue; their device work is ordered by `stream`.
+ * Errors as moe_ffn_forward; MOE_ERR_INVALID_ARG for a negative
+ * chunk_tokens or a NULL host pointer. */
+size_t moe_ffn_host_workspace_size(int T, int chunk_tokens, int E, int D, int H, int k, int dtype, int pipeline);
+moe_status_t moe_ffn_forward_host(const void* x_host, const void* x_sf_host, const void* w1, const void* w1_sf,
+                                  const void* w2, const void* w2_sf, const int32_t* topk_ids_host,
+                                  const float* topk_w_host, void* out_host, int T, int E, int D, int H, int k,
+                                  int dtype, int pipeline, int chunk_tokens, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
 /* The router step upstream of the path ("Prime Flash MoE" sec. 1 takes each
  * token's k experts and their weights, which sum to one, as given; the
  * workloads produce them from per-(token, expert) logits: the k largest, with
@@ -517,6 +548,10 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   tensor cores do 256 x ns rather than 256 x 256 per K
  *                   step; 0 runs it as a full pair whose odd CTA repeats the
  *                   block and stores nothing.
+ *   MOE_OPT_ROUTE_TPB  0 (default: 256), 64, 128 or 256: tokens per block of
+ *                   the multi-block routing (the cooperative launch and the
+ *                   three-launch fallback); set before sizing the workspace
+ *                   (the per-block count table takes blocks x E ints).
  *   (MOE_OPT_L2_POLICY measured at prefill: 0.343 ms with 0, 0.349 with 1,
  *                   0.342 with 2, 0.348 with 3: no gain, off.) */
 typedef enum {
@@ -544,7 +579,8 @@ typedef enum {
   MOE_OPT_DOWN_BANDS = 21,
   MOE_OPT_DOWN_EPI8 = 22,
   MOE_OPT_MX_PAIRS = 23,
-  MOE_OPT_UP_SWAP = 24
+  MOE_OPT_UP_SWAP = 24,
+  MOE_OPT_ROUTE_TPB = 25
 } moe_option_t;
 moe_status_t moe_ffn_set_option(int option, long long value);
 

@@ -204,3 +204,36 @@ def test_workspace_holds_fp32_row_sums_for_large_k():
         k8 = moe.moe_ffn_workspace_size(T, E, D, H, 8, dtype, moe.MOE_SPLIT)
         k9 = moe.moe_ffn_workspace_size(T, E, D, H, 9, dtype, moe.MOE_SPLIT)
         assert k9 >= k8 + T * D * 4
+
+
+def test_host_entry_sizes_and_rejects_bad_arguments_on_host():
+    one = moe.moe_ffn_workspace_size(300, 16, 512, 256, 4)
+    h = moe.moe_ffn_host_workspace_size(300, 16, 512, 256, 4)
+    # the forward workspace of a chunk plus two sets of staging buffers
+    assert h >= one + 2 * (300 * 512 * 2 + 2 * 300 * 4 * 4 + 300 * 512 * 2)
+    assert moe.moe_ffn_host_workspace_size(300, 16, 512, 256, 4, chunk_tokens=64) < h
+    # automatic chunks: whole problems up to 8192 tokens, else T / 8 within [4096, 16384]
+    size = lambda T, c=0: moe.moe_ffn_host_workspace_size(T, 16, 512, 256, 4, chunk_tokens=c)
+    assert size(200000) == size(16384, 16384)
+    assert size(16384) == size(16384, 4096)
+    assert size(50000) == size(50000, 6272)
+    assert size(8192) == size(8192, 8192)
+    assert moe.moe_ffn_host_workspace_size(300, 16, 512, 256, 4, dtype=moe.MOE_NVFP4) == 0
+    assert moe.moe_ffn_host_workspace_size(300, 16, 512, 256, 4, chunk_tokens=-1) == 0
+    L = moe.lib()
+    A = 1 << 20  # fake addresses: never dereferenced
+    base = [A, None, A, None, A, None, A, A, A, 300, 16, 512, 256, 4, 0, 1, 0, A, 10 ** 9, None]
+    a = list(base); a[0] = None
+    assert L.moe_ffn_forward_host(*a) == 1                  # null x
+    a = list(base); a[8] = None
+    assert L.moe_ffn_forward_host(*a) == 1                  # null out
+    a = list(base); a[16] = -5
+    assert L.moe_ffn_forward_host(*a) == 1                  # negative chunk size
+    a = list(base); a[14] = 3
+    assert L.moe_ffn_forward_host(*a) == 1                  # NVFP4 has its own entry point
+    a = list(base); a[14] = 1
+    assert L.moe_ffn_forward_host(*a) == 1                  # MXFP8 without x scales
+    a = list(base); a[9] = 0
+    assert L.moe_ffn_forward_host(*a) == 0                  # T == 0: no-op
+    a = list(base); a[18] = 1024
+    assert L.moe_ffn_forward_host(*a) == 5                  # workspace too small

@@ -2,7 +2,8 @@
 sort ("Prime Flash MoE" sec. 3 and 6: tokens processed in per-expert sorted
 order), including empty experts, one hot expert, repeats and T = 1.  Problems
 too large for the single-block kernel run both through the one-launch
-cooperative routing (default) and the three-launch path; the single-block
+cooperative routing (default) and the three-launch path, with 256 tokens per
+routing block and with fewer (64, 128); the single-block
 kernel is also run on every problem it can take (at most 256 experts) with
 its size limit raised."""
 import numpy as np
@@ -16,15 +17,17 @@ from grouped_gemm_gb300 import workloads as wl
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(autouse=True, params=[(1, 8192), (0, 8192), (1, 1 << 20)],
-                ids=["coop", "three_launches", "single_block"])
+@pytest.fixture(autouse=True, params=[(1, 8192, 0), (0, 8192, 0), (1, 1 << 20, 0), (1, 8192, 64), (0, 8192, 128)],
+                ids=["coop", "three_launches", "single_block", "coop_tpb64", "three_launches_tpb128"])
 def route_mode(request):
-    coop, small_pairs = request.param
+    coop, small_pairs, tpb = request.param
     moe.moe_ffn_set_option(moe.MOE_OPT_ROUTE_COOP, coop)
     moe.moe_ffn_set_option(moe.MOE_OPT_ROUTE_SMALL_PAIRS, small_pairs)
+    moe.moe_ffn_set_option(moe.MOE_OPT_ROUTE_TPB, tpb)  # tokens per routing block (0: 256)
     yield request.param
     moe.moe_ffn_set_option(moe.MOE_OPT_ROUTE_COOP, 1)
     moe.moe_ffn_set_option(moe.MOE_OPT_ROUTE_SMALL_PAIRS, 8192)
+    moe.moe_ffn_set_option(moe.MOE_OPT_ROUTE_TPB, 0)
 
 
 def gpu_route(ids, E):
