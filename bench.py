@@ -40,7 +40,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NOMINAL_PEAKS = {"hbm_gbs": 7900.0, "bf16_tflops": 2250.0, "fp8_tflops": 4500.0, "fp4_tflops": 13500.0}
 # measured after the main workload in the same run (N=1): workload, pipeline
 ALSO = [("large_skewed", "split"), ("large_skewed", "fused"), ("prefill", "split"), ("prefill", "fused"),
-        ("mxfp8", "split"), ("mxfp8", "fused"), ("decode", "split"), ("decode", "fused")]
+        ("mxfp8", "split"), ("mxfp8", "fused"), ("decode", "split"), ("decode", "fused"),
+        ("decode_mxfp4w", "split"), ("decode_nvfp4", "split")]
 STAGES = {"split": ["route", "gather_zero", "up_swiglu", "down_reduce"],
           "fused": ["route", "gather_zero", "fused_gemm", "to_bf16"]}
 
