@@ -1187,10 +1187,13 @@ moe_status_t moe_ffn_forward_host(const void* x_host, const void* x_sf_host, con
   cudaError_t e = cudaEventRecord(hp->start, st);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->in, hp->start, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->out, hp->start, 0);
-  const int n_chunks = (T + Tc - 1) / Tc;
+  // chunk c covers tokens [t0, t0 + tn): a quarter chunk first when there
+  // are several (the copy in that nothing overlaps is short), then full ones
+  const int first = T > Tc ? std::max(std::min(Tc, 128), Tc / 4) : T;
   moe_status_t rs = MOE_OK;
-  for (int c = 0; c < n_chunks && e == cudaSuccess && rs == MOE_OK; ++c) {
-    const int b = c & 1, t0 = c * Tc, tn = std::min(Tc, T - t0);
+  int t0 = 0;
+  for (int c = 0; t0 < T && e == cudaSuccess && rs == MOE_OK; ++c) {
+    const int b = c & 1, tn = std::min(c == 0 ? first : Tc, T - t0);
     Set& sb = set[b];
     // in: buffers of set b are free once chunk c - 2's forward pass has read them
     if (c >= 2) e = cudaStreamWaitEvent(hp->in, hp->computed[b], 0);
@@ -1217,6 +1220,7 @@ moe_status_t moe_ffn_forward_host(const void* x_host, const void* x_sf_host, con
     if (e == cudaSuccess)
       e = cudaMemcpyAsync(oh + (size_t)t0 * D * 2, sb.out, (size_t)tn * D * 2, cudaMemcpyDeviceToHost, hp->out);
     if (e == cudaSuccess) e = cudaEventRecord(hp->out_done[b], hp->out);
+    t0 += tn;
   }
   // the caller's stream waits for the last copies out (and the copy streams
   // are joined back, so the call is one unit of work on the caller's stream)

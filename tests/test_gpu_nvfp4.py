@@ -4,8 +4,8 @@ Blackwell to Rubin" sec. 1.2, 6.1; GEMMs on kind::mxf4nvf4.block_scale
 .scale_vec::4X) against the oracle's NVFP4 mode with act requantized to NVFP4
 by the same rule and global scale on both sides.
 
-Tolerance: the bf16 parity bounds (max 2e-2, mean 5e-3).  North star states
-none for NVFP4; the GPU and the oracle quantize from the same decoded
+Tolerance: the bf16 parity bounds (max 2e-2, mean 5e-3).  No bound is stated
+for NVFP4; the GPU and the oracle quantize from the same decoded
 operands, so they differ only by fp32 against fp64 accumulation, the rare act
 code that the two precisions round to opposite sides of a decision boundary,
 and the bf16 output and its reductions -- the bf16 bounds' own sources."""
