@@ -1187,13 +1187,22 @@ moe_status_t moe_ffn_forward_host(const void* x_host, const void* x_sf_host, con
   cudaError_t e = cudaEventRecord(hp->start, st);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->in, hp->start, 0);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->out, hp->start, 0);
-  // chunk c covers tokens [t0, t0 + tn): a quarter chunk first when there
-  // are several (the copy in that nothing overlaps is short), then full ones
-  const int first = T > Tc ? std::max(std::min(Tc, 128), Tc / 4) : T;
+  // chunk c covers tokens [t0, t0 + tn).  With eight or more chunks the
+  // first and the last are a quarter chunk: the copy in that nothing overlaps
+  // and the copy out that nothing overlaps are then short (measured: with
+  // fewer chunks the extra chunk costs more than it saves).
+  const int q = T >= 8 * Tc && Tc >= 512 ? Tc / 4 : 0;
+  auto chunk_at = [&](int t0) {
+    const int rem = T - t0;
+    if (!q) return std::min(Tc, rem);
+    if (t0 == 0) return q;
+    if (rem > Tc + q) return Tc;
+    return rem > 2 * q ? rem - q : rem;  // the tail: [rem - q, q], or rem whole
+  };
   moe_status_t rs = MOE_OK;
   int t0 = 0;
   for (int c = 0; t0 < T && e == cudaSuccess && rs == MOE_OK; ++c) {
-    const int b = c & 1, tn = std::min(c == 0 ? first : Tc, T - t0);
+    const int b = c & 1, tn = chunk_at(t0);
     Set& sb = set[b];
     // in: buffers of set b are free once chunk c - 2's forward pass has read them
     if (c >= 2) e = cudaStreamWaitEvent(hp->in, hp->computed[b], 0);

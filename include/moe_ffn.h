@@ -140,9 +140,9 @@ moe_status_t moe_ffn_forward_nvfp4(const void* x, const void* x_sf, const void* 
  * weights (and their scales) and the workspace are device memory as for
  * moe_ffn_forward.  The tokens are processed in chunks of chunk_tokens
  * (0: automatic: the whole problem up to 8192 tokens, else T / 8 rounded up
- * to a multiple of 128, within [4096, 16384]; with several chunks the first
- * is a quarter of that, the copy in that nothing overlaps; the last may be
- * shorter): while chunk c runs on `stream`, chunk c + 1
+ * to a multiple of 128, within [4096, 16384]; the last chunk may be shorter;
+ * with eight chunks or more the first and the last are a quarter chunk, so
+ * the copy in and the copy out that nothing overlaps are short): while chunk c runs on `stream`, chunk c + 1
  * is copied in and chunk c - 1 copied out on two copy streams of the library,
  * through two sets of device staging buffers in the workspace.  Each chunk is
  * one moe_ffn_forward call, so each output row is exactly what

@@ -71,6 +71,13 @@ def test_host_forward_chunks(chunk, pipeline):
     assert_close(out, oracle_out(inp), label=f"host chunk={chunk}")
 
 
+def test_host_forward_ramped_chunks():
+    # eight chunks or more: a quarter chunk first and last ([128, 512 x 8, 256, 128] here)
+    inp = wl.make_custom(4608, 256, 128, 8, 2, seed=35, routing="uniform")
+    out, _ = run_host(inp, 512)
+    assert_close(out, oracle_out(inp), label="host ramped chunks")
+
+
 def test_host_forward_pageable_memory():
     inp = wl.make_custom(200, 256, 128, 8, 2, seed=32, routing="topk_logits")
     out, _ = run_host(inp, 48, pinned=False)
