@@ -158,7 +158,9 @@ moe_status_t moe_ffn_forward_nvfp4(const void* x, const void* x_sf, const void* 
  * first, and everything the call does (copies included) completes before the
  * work queued on stream after it; the host buffers must stay valid and out
  * unread until then.  Calls on one device are serialized on the host (one
- * mutex) while they enqueue; their device work is ordered by `stream`.
+ * mutex) while they enqueue; their device work is ordered by `stream`.  Not
+ * for stream capture: the library's copy streams are not part of a graph
+ * (capture moe_ffn_forward with the caller's own copies instead).
  * Errors as moe_ffn_forward; MOE_ERR_INVALID_ARG for a negative
  * chunk_tokens or a NULL host pointer. */
 size_t moe_ffn_host_workspace_size(int T, int chunk_tokens, int E, int D, int H, int k, int dtype, int pipeline);
