@@ -138,6 +138,10 @@ KERNEL_SOURCES = {
     "up_swiglu_mxfp8": ["grouped_gemm_gb300/csrc/gemm_mxfp8.cu"] + _MXH + _PTX,
     "down_reduce_mxfp8": ["grouped_gemm_gb300/csrc/gemm_mxfp8.cu"] + _MXH + _PTX,
     "up_swiglu_mxfp8_pair2": ["grouped_gemm_gb300/csrc/gemm_mxfp8_pair.cu"] + _MXH + _PTX,
+    "up_swiglu_mxfp8_swap": ["grouped_gemm_gb300/csrc/gemm_mx_swap.cu", "grouped_gemm_gb300/csrc/mx_swap.h"] + _MXH + _PTX,
+    "down_reduce_mxfp8_swap": ["grouped_gemm_gb300/csrc/gemm_mx_swap.cu", "grouped_gemm_gb300/csrc/mx_swap.h"] + _MXH + _PTX,
+    "up_swiglu_mxfp4w_swap": ["grouped_gemm_gb300/csrc/gemm_mx_swap.cu", "grouped_gemm_gb300/csrc/mx_swap.h"] + _MXH + _PTX,
+    "down_reduce_mxfp4w_swap": ["grouped_gemm_gb300/csrc/gemm_mx_swap.cu", "grouped_gemm_gb300/csrc/mx_swap.h"] + _MXH + _PTX,
     "down_reduce_mxfp8_pair2": ["grouped_gemm_gb300/csrc/gemm_mxfp8_pair.cu"] + _MXH + _PTX,
     "up_swiglu_mxfp4w": ["grouped_gemm_gb300/csrc/gemm_mxfp8.cu"] + _MXH + _PTX,
     "up_swiglu_nvfp4": ["grouped_gemm_gb300/csrc/gemm_nvfp4.cu"] + _MXH + _PTX,

@@ -423,6 +423,7 @@ MOE_OPT_DOWN_EPI8 = 22
 MOE_OPT_MX_PAIRS = 23
 MOE_OPT_UP_SWAP = 24
 MOE_OPT_ROUTE_TPB = 25
+MOE_OPT_MX_SWAP = 26
 
 
 def moe_ffn_set_option(option: int, value: int) -> int:

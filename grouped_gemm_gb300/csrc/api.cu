@@ -11,6 +11,7 @@
 
 #include "../../include/moe_ffn.h"
 #include "internal.h"
+#include "mx_swap.h"
 #include "ptx.cuh"
 
 namespace moe {
@@ -42,6 +43,7 @@ std::atomic<int> g_pair_swap{0};      // MOE_OPT_PAIR_SWAP: max routed rows of a
 std::atomic<int> g_wide_up{0};        // MOE_OPT_WIDE_UP: 512-column up tiles on CTA pairs
 std::atomic<int> g_down_bands{1};     // MOE_OPT_DOWN_BANDS: token bands of the down tiles' order (0 automatic, 1 off)
 constexpr int kHostChunkTokens = 16384;  // moe_ffn_forward_host: automatic chunk size
+std::atomic<int> g_mx_swap{0};        // MOE_OPT_MX_SWAP: swap-AB MXFP8 split GEMMs (0 off: measured slower, 1 on, 2 decode-sized problems)
 std::atomic<int> g_up_swap{1};        // MOE_OPT_UP_SWAP: swap-AB half pairs in the CTA-pair up kernel
 std::atomic<int> g_mx_pairs{0};       // MOE_OPT_MX_PAIRS: MXFP8 split GEMMs on CTA pairs (0 off: measured slower, 1 on, 2 automatic)
 std::atomic<int> g_down_epi8{1};      // MOE_OPT_DOWN_EPI8: eight epilogue warps in the CTA-pair down kernel
@@ -425,12 +427,22 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
   const int mxp_opt = g_mx_pairs.load();
   const bool small = (int64_t)ws.max_rb * (H / 128) < 8LL * sms;
   const bool pairs = !fp4w && (mxp_opt == 1 || (mxp_opt == 2 && !small));
-  CUtensorMap map_xg, map_w1, map_act, map_w2, sf_xg, sf_w1, sf_act, sf_w2;
+  // swapped operands (weights on the MMA's M side) when an expert holds few
+  // rows: by option, or automatically at <= 64 routed rows per live expert on
+  // average; bf16 row sums only (k <= 8)
+  const int swap_opt = g_mx_swap.load();
+  const int64_t P = (int64_t)T * k;
+  const bool swap = !pairs && !f32_accum(k) &&
+                    (swap_opt == 1 || (swap_opt == 2 && P <= 64 * std::min<int64_t>(P, E)));
+  CUtensorMap map_xg, map_w1, map_act, map_w2, sf_xg, sf_w1, sf_act, sf_w2, map_xg32, map_act32;
   auto make_w = fp4w ? make_map_fp4 : make_map_fp8;
   if (!make_map_fp8(&map_xg, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, kBM) ||
       !make_w(&map_w1, w1, (uint64_t)E * 2 * H, (uint64_t)D, 128) ||
       !make_map_fp8(&map_act, ws.act, (uint64_t)ws.S_max, (uint64_t)H, kBM) ||
-      !make_w(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, pairs ? 128 : 256))
+      !make_w(&map_w2, w2, (uint64_t)E * D, (uint64_t)H, (pairs || swap) ? 128 : 256))
+    return MOE_ERR_CUDA;
+  if (swap && (!make_map_fp8(&map_xg32, ws.xg, (uint64_t)ws.S_max, (uint64_t)D, 32) ||
+               !make_map_fp8(&map_act32, ws.act, (uint64_t)ws.S_max, (uint64_t)H, 32)))
     return MOE_ERR_CUDA;
   if (pairs && (!make_map_sf(&sf_xg, ws.xg_sf, (uint64_t)(ws.S_max / 128) * (D / 128)) ||
                 !make_map_sf(&sf_w1, w1_sf, (uint64_t)E * (2 * H / 128) * (D / 128)) ||
@@ -477,11 +489,40 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
   up.k_blocks = D / 128;
   prof_front(true);
   if (bands > 1) prof_kernel(1, "gather_rows_mx+band_order");
-  prof_kernel(2, fp4w ? "up_swiglu_mxfp4w" : pairs ? "up_swiglu_mxfp8_pair2" : "up_swiglu_mxfp8");
-  prof_kernel(3, fp4w    ? (acc ? "down_reduce_mxfp4w+f32_to_bf16" : "down_reduce_mxfp4w")
+  prof_kernel(2, swap    ? (fp4w ? "up_swiglu_mxfp4w_swap" : "up_swiglu_mxfp8_swap")
+                 : fp4w  ? "up_swiglu_mxfp4w"
+                 : pairs ? "up_swiglu_mxfp8_pair2"
+                         : "up_swiglu_mxfp8");
+  prof_kernel(3, swap    ? (fp4w ? "down_reduce_mxfp4w_swap" : "down_reduce_mxfp8_swap")
+                 : fp4w  ? (acc ? "down_reduce_mxfp4w+f32_to_bf16" : "down_reduce_mxfp4w")
                  : pairs ? (acc ? "down_reduce_mxfp8_pair2+f32_to_bf16" : "down_reduce_mxfp8_pair2")
                          : (acc ? "down_reduce_mxfp8+f32_to_bf16" : "down_reduce_mxfp8"));
-  if (pairs)
+  MxSwapArgs sw{};
+  if (swap) {
+    sw.meta = ws.meta;
+    sw.expert_of_rb = ws.expert_of_rb;
+    sw.counts = ws.counts;
+    sw.pad_offsets = ws.pad_offsets;
+    sw.row_tok = ws.row_tok;
+    sw.slot_w = ws.slot_w;
+    sw.act = ws.act;
+    sw.act_sf = ws.act_sf;
+    sw.out = out;
+    sw.err = ws.err;
+    sw.wait_limit_ns = ma.wait_limit_ns;
+    sw.D = D;
+    sw.H = H;
+    sw.stall_test = ma.stall_test;
+    sw.out_hint = ma.out_hint;
+    sw.swiglu_limit = ma.swiglu_limit;
+    MxSwapArgs su = sw;
+    su.sf_x = ws.xg_sf;
+    su.sf_w = w1_sf;
+    su.n_col_tiles = H / 128;
+    su.k_blocks = D / 128;
+    e = launch_up_mx_swap(map_w1, map_xg32, su, (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * su.n_col_tiles), st,
+                          fp4w);
+  } else if (pairs)
     e = launch_up_mxfp8_pair(map_xg, map_w1, sf_xg, sf_w1, up,
                              (int)std::min<int64_t>(mx_slots, (int64_t)ws.max_rb * up.n_col_tiles), st);
   else
@@ -496,7 +537,15 @@ moe_status_t forward_split_mxfp8(const Workspace& ws, const void* x, const void*
   dn.sf_b = w2_sf;
   dn.n_col_tiles = D / 256;
   dn.k_blocks = H / 128;
-  if (pairs)
+  if (swap) {
+    MxSwapArgs sd = sw;
+    sd.sf_x = ws.act_sf;
+    sd.sf_w = w2_sf;
+    sd.n_col_tiles = D / 128;
+    sd.k_blocks = H / 128;
+    e = launch_down_mx_swap(map_w2, map_act32, sd, (int)std::min<int64_t>(sms, (int64_t)ws.max_rb * sd.n_col_tiles), st,
+                            !g_prof.on, fp4w);
+  } else if (pairs)
     e = launch_down_mxfp8_pair(map_act, map_w2, sf_act, sf_w2, dn,
                                (int)std::min<int64_t>(mx_slots, (int64_t)ws.max_rb * dn.n_col_tiles), st, !g_prof.on);
   else
@@ -790,6 +839,10 @@ moe_status_t moe_ffn_set_option(int option, long long value) {
     case MOE_OPT_ROUTE_SMALL_PAIRS:
       if (value < 0 || value > (1 << 20)) return MOE_ERR_INVALID_ARG;
       g_route_small_pairs.store(value);
+      return MOE_OK;
+    case MOE_OPT_MX_SWAP:
+      if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
+      g_mx_swap.store((int)value);
       return MOE_OK;
     case MOE_OPT_ROUTE_TPB:
       if (value != 0 && value != 64 && value != 128 && value != 256) return MOE_ERR_INVALID_ARG;

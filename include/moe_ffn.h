@@ -556,6 +556,16 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   the multi-block routing (the cooperative launch and the
  *                   three-launch fallback); set before sizing the workspace
  *                   (the per-block count table takes blocks x E ints).
+ *   MOE_OPT_MX_SWAP  0 (default: off), 1 or 2 (automatic): the MXFP8 split
+ *                   pipeline's GEMMs (e4m3 or MXFP4 weights) with the operands
+ *                   swapped: 128 weight rows as the MMA's M side and a row
+ *                   block's routed rows, rounded up to 16, as its N side (up:
+ *                   gate and up in two accumulators, so each act column's pair
+ *                   shares a TMEM lane).  Automatic: at most 64 routed rows
+ *                   per live expert on average and k <= 8.  Measured on GB300,
+ *                   decode shape with MXFP4 weights: step 0.195 ms against
+ *                   0.174 (up kernel 0.113 against 0.102, down 0.074 against
+ *                   0.065): off.
  *   (MOE_OPT_L2_POLICY measured at prefill: 0.343 ms with 0, 0.349 with 1,
  *                   0.342 with 2, 0.348 with 3: no gain, off.) */
 typedef enum {
@@ -584,7 +594,8 @@ typedef enum {
   MOE_OPT_DOWN_EPI8 = 22,
   MOE_OPT_MX_PAIRS = 23,
   MOE_OPT_UP_SWAP = 24,
-  MOE_OPT_ROUTE_TPB = 25
+  MOE_OPT_ROUTE_TPB = 25,
+  MOE_OPT_MX_SWAP = 26
 } moe_option_t;
 moe_status_t moe_ffn_set_option(int option, long long value);
 

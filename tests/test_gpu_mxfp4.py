@@ -62,8 +62,9 @@ def test_mxfp4_weights_forward(T, D, H, E, k, routing, pipeline):
     print(f"mxfp4 weights pipeline={pipeline} T={T} D={D} H={H} E={E} k={k}: max_rel={r[0]:.2e} mean_rel={r[1]:.2e}")
 
 
-def run_mx4(inp):
-    """moe_ffn_forward with MOE_MXFP4W: the packed codes as they are."""
+def run_mx4(inp, swap=2):
+    """moe_ffn_forward with MOE_MXFP4W: the packed codes as they are.  swap:
+    MOE_OPT_MX_SWAP (0 the default kernels, 1 the swap-AB ones, 2 automatic)."""
     w = inp["workload"]
     dev = {k: torch.from_numpy(np.ascontiguousarray(inp[k])).cuda() for k in ("x", "x_sf", "w1", "w2")}
     w1p = torch.empty(inp["w1_sf"].size, dtype=torch.uint8, device="cuda")
@@ -74,34 +75,42 @@ def run_mx4(inp):
     tw = torch.from_numpy(inp["topk_w"]).cuda()
     out = torch.full((w.T, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
     ws = moe.alloc_workspace(w.T, w.E, w.D, w.H, w.k, moe.MOE_MXFP4W, moe.MOE_SPLIT)
-    moe.moe_ffn_forward(dev["x"], dev["w1"], dev["w2"], ids, tw, out, E=w.E, D=w.D, H=w.H, k=w.k, workspace=ws,
-                        dtype=moe.MOE_MXFP4W, pipeline=moe.MOE_SPLIT, x_sf=dev["x_sf"], w1_sf=w1p, w2_sf=w2p)
+    moe.moe_ffn_set_option(moe.MOE_OPT_MX_SWAP, swap)
+    try:
+        moe.moe_ffn_forward(dev["x"], dev["w1"], dev["w2"], ids, tw, out, E=w.E, D=w.D, H=w.H, k=w.k, workspace=ws,
+                            dtype=moe.MOE_MXFP4W, pipeline=moe.MOE_SPLIT, x_sf=dev["x_sf"], w1_sf=w1p, w2_sf=w2p)
+    finally:
+        moe.moe_ffn_set_option(moe.MOE_OPT_MX_SWAP, 0)
     st = moe.moe_ffn_sync_status(ws)
     assert st == 0, moe.moe_ffn_status_string(st)
     return out
 
 
+@pytest.mark.parametrize("swap", [0, 1])       # the swap-AB kernels (weights on the M side), or not
 @pytest.mark.parametrize("T,D,H,E,k,routing", [
     (64, 256, 128, 8, 2, "topk_logits"),
     (300, 512, 256, 16, 4, "uniform"),
     (1, 256, 384, 4, 4, "uniform"),
     (129, 768, 256, 40, 8, "zipf"),          # several experts empty
-    (100, 256, 256, 64, 32, "uniform"),      # k = 32: rows of a token summed in fp32
+    (100, 256, 256, 64, 32, "uniform"),      # k = 32: rows of a token summed in fp32 (never swapped)
+    (700, 512, 256, 4, 2, "uniform"),        # ~350 rows per expert: full 128-row blocks and a ragged one
 ])
-def test_mxfp4_packed_weights_forward(T, D, H, E, k, routing):
+def test_mxfp4_packed_weights_forward(T, D, H, E, k, routing, swap):
     inp = wl.make_custom(T, D, H, E, k, seed=T + H, routing=routing, dtype="mxfp4w")
-    out = run_mx4(inp)
+    out = run_mx4(inp, swap)
     ref = oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], inp["topk_ids"], inp["topk_w"], act=oracle.ACT_MXFP8,
                          x_sf=inp["x_sf"], w1_sf=inp["w1_sf"], w2_sf=inp["w2_sf"], fp4_weights=True)
-    r = assert_close(out, ref, dtype="mxfp8", label=f"packed mxfp4 weights T={T} D={D} H={H} E={E} k={k}")
-    print(f"packed mxfp4 T={T} D={D} H={H} E={E} k={k}: max_rel={r[0]:.2e} mean_rel={r[1]:.2e} cos={r[2]:.6f}")
+    r = assert_close(out, ref, dtype="mxfp8", label=f"packed mxfp4 weights swap={swap} T={T} D={D} H={H} E={E} k={k}")
+    print(f"packed mxfp4 swap={swap} T={T} D={D} H={H} E={E} k={k}: max_rel={r[0]:.2e} mean_rel={r[1]:.2e} "
+          f"cos={r[2]:.6f}")
 
 
-def test_mxfp4_packed_weights_decode_workload():
+@pytest.mark.parametrize("swap", [0, 2])       # the default kernels; automatic (the swap-AB ones here)
+def test_mxfp4_packed_weights_decode_workload(swap):
     """The decode workload's shape (T=64, D=6144, H=2048, E=32, k=8) with MXFP4
     weights, every token checked: the weight stream that 4-bit codes halve."""
     inp = wl.make_inputs("decode_mxfp4w", seed=0)
-    out = run_mx4(inp)
+    out = run_mx4(inp, swap)
     ref = oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], inp["topk_ids"], inp["topk_w"], act=oracle.ACT_MXFP8,
                          x_sf=inp["x_sf"], w1_sf=inp["w1_sf"], w2_sf=inp["w2_sf"], fp4_weights=True)
     r = assert_close(out, ref, dtype="mxfp8", label="packed mxfp4 weights, decode workload")

@@ -77,11 +77,12 @@ def test_weight_scale_repacking_layout():
     assert np.array_equal(p2.cpu().numpy(), expected(w2_sf))
 
 
-def run_mx(inp, pipeline=moe.MOE_SPLIT, cluster=1, bands=1, pairs=0, check=True):
+def run_mx(inp, pipeline=moe.MOE_SPLIT, cluster=1, bands=1, pairs=0, swap=0, check=True):
     """cluster: MOE_OPT_FUSED_CLUSTER for the call (1 automatic, 2/4/8 that
     size, 0 the fused kernel with fp32 partial sums); bands:
     MOE_OPT_DOWN_BANDS (token-band order of the split down kernel's tiles);
-    pairs: MOE_OPT_MX_PAIRS (split GEMMs on CTA pairs: 0 off, 1 on, 2 automatic).
+    pairs: MOE_OPT_MX_PAIRS (split GEMMs on CTA pairs: 0 off, 1 on, 2 automatic);
+    swap: MOE_OPT_MX_SWAP (swap-AB split GEMMs: 0 off, 1 on, 2 automatic).
     check=False returns (out, status) instead of asserting a clean status."""
     w = inp["workload"]
     dev = {k: torch.from_numpy(inp[k]).cuda() for k in ("x", "x_sf", "w1", "w2")}
@@ -96,6 +97,7 @@ def run_mx(inp, pipeline=moe.MOE_SPLIT, cluster=1, bands=1, pairs=0, check=True)
     moe.moe_ffn_set_option(moe.MOE_OPT_FUSED_CLUSTER, cluster)
     moe.moe_ffn_set_option(moe.MOE_OPT_DOWN_BANDS, bands)
     moe.moe_ffn_set_option(moe.MOE_OPT_MX_PAIRS, pairs)
+    moe.moe_ffn_set_option(moe.MOE_OPT_MX_SWAP, swap)
     try:
         moe.moe_ffn_forward(dev["x"], dev["w1"], dev["w2"], ids, tw, out, E=w.E, D=w.D, H=w.H, k=w.k, workspace=ws,
                             dtype=moe.MOE_MXFP8, pipeline=pipeline, x_sf=dev["x_sf"], w1_sf=w1p, w2_sf=w2p)
@@ -103,6 +105,7 @@ def run_mx(inp, pipeline=moe.MOE_SPLIT, cluster=1, bands=1, pairs=0, check=True)
         moe.moe_ffn_set_option(moe.MOE_OPT_FUSED_CLUSTER, 1)
         moe.moe_ffn_set_option(moe.MOE_OPT_DOWN_BANDS, 1)
         moe.moe_ffn_set_option(moe.MOE_OPT_MX_PAIRS, 0)
+        moe.moe_ffn_set_option(moe.MOE_OPT_MX_SWAP, 0)
     st = moe.moe_ffn_sync_status(ws)
     if not check:
         return out, st
@@ -115,12 +118,16 @@ def oracle_mx(inp, tokens=None):
                           x_sf=inp["x_sf"], w1_sf=inp["w1_sf"], w2_sf=inp["w2_sf"], tokens=tokens)
 
 
-# split: the default (single-CTA kernels); split_pairs: the CTA-pair kernels;
+# split: the default (single-CTA kernels); split_swap: the swap-AB kernels;
+# split_swap_auto: the automatic swap choice (swap-AB where an expert holds at
+# most 64 rows on average);
+# split_pairs: the CTA-pair kernels;
 # split_auto: pairs chosen automatically (single CTAs at the small shapes, pairs
 # at full size); fused: on clusters
 # (automatic size); fused_splitk: H split over CTAs with fp32 partial sums;
 # split_bands: the down kernel's tiles in the order of three token bands
-PIPES = {"split": (moe.MOE_SPLIT, 1), "split_pairs": (moe.MOE_SPLIT, 1, 1, 1),
+PIPES = {"split": (moe.MOE_SPLIT, 1), "split_swap": (moe.MOE_SPLIT, 1, 1, 0, 1),
+         "split_swap_auto": (moe.MOE_SPLIT, 1, 1, 0, 2), "split_pairs": (moe.MOE_SPLIT, 1, 1, 1),
          "split_auto": (moe.MOE_SPLIT, 1, 1, 2), "fused": (moe.MOE_FUSED, 1), "fused_splitk": (moe.MOE_FUSED, 0),
          "split_bands": (moe.MOE_SPLIT, 1, 3), "split_pairs_bands": (moe.MOE_SPLIT, 1, 3, 1)}
 
@@ -145,8 +152,8 @@ def test_mxfp8_forward_small(T, D, H, E, k, routing, pipe):
 @pytest.mark.parametrize("pipe", list(PIPES))
 def test_mxfp8_full_workload_sampled(pipe):
     # every expert's first, last and tail-block rows plus 1000 seeded random tokens
-    if pipe == "split_auto":
-        pytest.skip("at full size the automatic choice is the CTA pairs: covered by split_pairs")
+    if pipe in ("split_auto", "split_swap", "split_swap_auto"):
+        pytest.skip("at full size: the CTA pairs (split_pairs) or the single-CTA kernels (split)")
     inp = cached_inputs("mxfp8")
     out = run_mx(inp, *PIPES[pipe])
     tokens = coverage_tokens(inp["topk_ids"], seed=2)
@@ -170,8 +177,8 @@ def test_mxfp8_fused_cluster_sizes(T, D, H, E, k, csize):
     print(f"mxfp8 fused C={csize} T={T} D={D} H={H} E={E} k={k}: max_rel={r[0]:.2e} mean_rel={r[1]:.2e}")
 
 
-@pytest.mark.parametrize("pairs", [0, 1])
-def test_mxfp8_wait_timeout_is_reported_and_context_survives(pairs):
+@pytest.mark.parametrize("pairs,swap", [(0, 0), (1, 0), (0, 1)])
+def test_mxfp8_wait_timeout_is_reported_and_context_survives(pairs, swap):
     # the MMA issuer of the single-CTA (pairs 0) or CTA-pair (pairs 1) MXFP8
     # kernels first waits on a barrier nothing arrives on (MOE_OPT_TEST_STALL
     # 1); with a 1 ms bound the wait runs out, the status reads
@@ -180,10 +187,10 @@ def test_mxfp8_wait_timeout_is_reported_and_context_survives(pairs):
     moe.moe_ffn_set_wait_limit_ns(1_000_000)
     moe.moe_ffn_set_option(moe.MOE_OPT_TEST_STALL, 1)
     try:
-        _, st = run_mx(inp, pairs=pairs, check=False)
+        _, st = run_mx(inp, pairs=pairs, swap=swap, check=False)
     finally:
         moe.moe_ffn_set_option(moe.MOE_OPT_TEST_STALL, 0)
         moe.moe_ffn_set_wait_limit_ns(2_000_000_000)
     assert st == 6, moe.moe_ffn_status_string(st)
-    out = run_mx(inp, pairs=pairs)
-    assert_close(out, oracle_mx(inp), dtype="mxfp8", label=f"mxfp8 after timeout pairs={pairs}")
+    out = run_mx(inp, pairs=pairs, swap=swap)
+    assert_close(out, oracle_mx(inp), dtype="mxfp8", label=f"mxfp8 after timeout pairs={pairs} swap={swap}")
