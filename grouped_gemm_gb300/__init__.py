@@ -424,6 +424,7 @@ MOE_OPT_MX_PAIRS = 23
 MOE_OPT_UP_SWAP = 24
 MOE_OPT_ROUTE_TPB = 25
 MOE_OPT_MX_SWAP = 26
+MOE_OPT_HOST_RAMP = 27
 
 
 def moe_ffn_set_option(option: int, value: int) -> int:

@@ -43,6 +43,7 @@ std::atomic<int> g_pair_swap{0};      // MOE_OPT_PAIR_SWAP: max routed rows of a
 std::atomic<int> g_wide_up{0};        // MOE_OPT_WIDE_UP: 512-column up tiles on CTA pairs
 std::atomic<int> g_down_bands{1};     // MOE_OPT_DOWN_BANDS: token bands of the down tiles' order (0 automatic, 1 off)
 constexpr int kHostChunkTokens = 16384;  // moe_ffn_forward_host: automatic chunk size
+std::atomic<int> g_host_ramp{1};      // MOE_OPT_HOST_RAMP: quarter chunks at both ends of a long host pipeline
 std::atomic<int> g_mx_swap{0};        // MOE_OPT_MX_SWAP: swap-AB MXFP8 split GEMMs (0 off: measured slower, 1 on, 2 decode-sized problems)
 std::atomic<int> g_up_swap{1};        // MOE_OPT_UP_SWAP: swap-AB half pairs in the CTA-pair up kernel
 std::atomic<int> g_mx_pairs{0};       // MOE_OPT_MX_PAIRS: MXFP8 split GEMMs on CTA pairs (0 off: measured slower, 1 on, 2 automatic)
@@ -840,6 +841,10 @@ moe_status_t moe_ffn_set_option(int option, long long value) {
       if (value < 0 || value > (1 << 20)) return MOE_ERR_INVALID_ARG;
       g_route_small_pairs.store(value);
       return MOE_OK;
+    case MOE_OPT_HOST_RAMP:
+      if (value != 0 && value != 1) return MOE_ERR_INVALID_ARG;
+      g_host_ramp.store((int)value);
+      return MOE_OK;
     case MOE_OPT_MX_SWAP:
       if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
       g_mx_swap.store((int)value);
@@ -1244,7 +1249,7 @@ moe_status_t moe_ffn_forward_host(const void* x_host, const void* x_sf_host, con
   // first and the last are a quarter chunk: the copy in that nothing overlaps
   // and the copy out that nothing overlaps are then short (measured: with
   // fewer chunks the extra chunk costs more than it saves).
-  const int q = T >= 8 * Tc && Tc >= 512 ? Tc / 4 : 0;
+  const int q = g_host_ramp.load() && T >= 8 * Tc && Tc >= 512 ? Tc / 4 : 0;
   auto chunk_at = [&](int t0) {
     const int rem = T - t0;
     if (!q) return std::min(Tc, rem);

@@ -566,6 +566,9 @@ void moe_ffn_set_wait_limit_ns(uint64_t ns);
  *                   decode shape with MXFP4 weights: step 0.195 ms against
  *                   0.174 (up kernel 0.113 against 0.102, down 0.074 against
  *                   0.065): off.
+ *   MOE_OPT_HOST_RAMP  1 (default) or 0: moe_ffn_forward_host with eight
+ *                   chunks or more makes its first and last chunks a quarter
+ *                   chunk; 0 keeps every chunk full (the last one ragged).
  *   (MOE_OPT_L2_POLICY measured at prefill: 0.343 ms with 0, 0.349 with 1,
  *                   0.342 with 2, 0.348 with 3: no gain, off.) */
 typedef enum {
@@ -595,7 +598,8 @@ typedef enum {
   MOE_OPT_MX_PAIRS = 23,
   MOE_OPT_UP_SWAP = 24,
   MOE_OPT_ROUTE_TPB = 25,
-  MOE_OPT_MX_SWAP = 26
+  MOE_OPT_MX_SWAP = 26,
+  MOE_OPT_HOST_RAMP = 27
 } moe_option_t;
 moe_status_t moe_ffn_set_option(int option, long long value);
 
