@@ -237,3 +237,39 @@ def test_host_entry_sizes_and_rejects_bad_arguments_on_host():
     assert L.moe_ffn_forward_host(*a) == 0                  # T == 0: no-op
     a = list(base); a[18] = 1024
     assert L.moe_ffn_forward_host(*a) == 5                  # workspace too small
+
+
+def test_option_values_are_checked_on_host():
+    # each option takes its documented values; anything else is refused and
+    # leaves the option as it was
+    cases = {
+        moe.MOE_OPT_DOWN_EPI8: ([0, 1], [2, -1]),
+        moe.MOE_OPT_MX_PAIRS: ([0, 1, 2], [3]),
+        moe.MOE_OPT_UP_SWAP: ([0, 1], [2]),
+        moe.MOE_OPT_ROUTE_TPB: ([0, 64, 128, 256], [32, 100, 512]),
+        moe.MOE_OPT_MX_SWAP: ([0, 1, 2], [3]),
+        moe.MOE_OPT_HOST_RAMP: ([0, 1], [2]),
+    }
+    defaults = {moe.MOE_OPT_DOWN_EPI8: 1, moe.MOE_OPT_MX_PAIRS: 0, moe.MOE_OPT_UP_SWAP: 1,
+                moe.MOE_OPT_ROUTE_TPB: 0, moe.MOE_OPT_MX_SWAP: 0, moe.MOE_OPT_HOST_RAMP: 1}
+    try:
+        for opt, (good, bad) in cases.items():
+            for v in good:
+                assert moe.moe_ffn_set_option(opt, v) == 0, (opt, v)
+            for v in bad:
+                assert moe.lib().moe_ffn_set_option(opt, v) == 1, (opt, v)
+        assert moe.lib().moe_ffn_set_option(999, 0) == 1          # unknown option
+    finally:
+        for opt, v in defaults.items():
+            moe.moe_ffn_set_option(opt, v)
+
+
+def test_routing_block_size_option_sizes_the_workspace():
+    # fewer tokens per routing block -> more blocks -> a larger per-block count table
+    base = moe.moe_ffn_workspace_size(4096, 128, 2048, 768, 8)
+    moe.moe_ffn_set_option(moe.MOE_OPT_ROUTE_TPB, 64)
+    try:
+        small_blocks = moe.moe_ffn_workspace_size(4096, 128, 2048, 768, 8)
+    finally:
+        moe.moe_ffn_set_option(moe.MOE_OPT_ROUTE_TPB, 0)
+    assert small_blocks >= base + (4096 // 64 - 4096 // 256) * 128 * 4 - 256
