@@ -1,7 +1,8 @@
 """The library driven from a plain C program through include/moe_ffn.h alone
 (no Python binding, no PyTorch on the call path): the program is compiled and
 linked against libmoe_ffn.so on the CPU (not gpu-marked), and on a GPU its
-output is compared with the oracle at the bf16 parity tolerances."""
+output is compared with the oracle at the bf16 parity tolerances, through
+device buffers and through the host-buffer entry point."""
 import os
 import shutil
 import subprocess
@@ -36,8 +37,9 @@ def test_c_program_compiles_and_links(tmp_path):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("host_chunk", [None, 64])   # device buffers; host buffers in chunks of 64 tokens
 @pytest.mark.parametrize("pipeline", [0, 1])
-def test_c_program_matches_oracle(tmp_path, pipeline):
+def test_c_program_matches_oracle(tmp_path, pipeline, host_chunk):
     import oracle
     from helpers import assert_close
     import torch
@@ -49,10 +51,12 @@ def test_c_program_matches_oracle(tmp_path, pipeline):
                       ("ids", np.ascontiguousarray(inp["topk_ids"], np.int32)),
                       ("w", np.ascontiguousarray(inp["topk_w"], np.float32))):
         arr.tofile(str(tmp_path / f"{name}.bin"))
-    r = subprocess.run([exe, str(tmp_path), str(T), str(E), str(D), str(H), str(k), str(pipeline)],
-                       capture_output=True, text=True, timeout=120)
+    argv = [exe, str(tmp_path), str(T), str(E), str(D), str(H), str(k), str(pipeline)]
+    if host_chunk is not None:
+        argv.append(str(host_chunk))
+    r = subprocess.run(argv, capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stderr
     out_bits = np.fromfile(str(tmp_path / "out.bin"), dtype=np.uint16).reshape(T, D)
     out = torch.from_numpy(out_bits.view(np.int16)).view(torch.bfloat16)
     ref = oracle.moe_ffn(inp["x"], inp["w1"], inp["w2"], inp["topk_ids"], inp["topk_w"], act=oracle.ACT_BF16)
-    assert_close(out, ref, label=f"C program pipeline={pipeline}")
+    assert_close(out, ref, label=f"C program pipeline={pipeline} host_chunk={host_chunk}")
