@@ -135,7 +135,10 @@ moe_status_t moe_ffn_forward_nvfp4(const void* x, const void* x_sf, const void* 
                                    const float* topk_w, void* out, int T, int E, int D, int H, int k,
                                    void* workspace, size_t workspace_bytes, void* stream);
 
-/* The forward pass from and to HOST memory: x (and x_sf), topk_ids and
+/* The forward pass from and to HOST memory (the library's own entry point:
+ * "Prime Flash MoE" sec. 8 times the kernels with inputs resident on the GPU
+ * and defines no host-buffer call; each chunk computes what moe_ffn_forward
+ * does, the operation of sec. 1).  x (and x_sf), topk_ids and
  * topk_w are read from host memory, out is written to host memory; the
  * weights (and their scales) and the workspace are device memory as for
  * moe_ffn_forward.  The tokens are processed in chunks of chunk_tokens
