@@ -218,9 +218,12 @@ def moe_ffn_host_workspace_size(T, E, D, H, k, dtype=MOE_BF16, pipeline=MOE_SPLI
 
 
 def _host_p(t, nbytes, name):
-    """Address of a host (CPU) tensor argument holding at least nbytes."""
+    """Address of a host (CPU) tensor argument holding at least nbytes (a raw
+    int address is passed through: its extent is the caller's responsibility)."""
     if t is None:
         return None
+    if isinstance(t, int):
+        return t
     if t.is_cuda:
         raise ValueError(f"{name}: expected a host tensor, got one on {t.device}")
     if not t.is_contiguous():
@@ -234,7 +237,10 @@ def moe_ffn_forward_host(x, w1, w2, topk_ids, topk_w, out, *, E, D, H, k, worksp
                          check=True) -> int:
     """moe_ffn_forward_host: x (x_sf), topk_ids, topk_w and out are host tensors
     (page-locked for overlapped copies), the weights and workspace CUDA tensors."""
-    T = x.shape[0] if T is None else T
+    if T is None:
+        if isinstance(x, int):
+            raise ValueError("T is required when x is a raw address")
+        T = x.shape[0]
     eb = 2 if dtype == MOE_BF16 else 1
     _need_forward(None, None, w1, w1_sf, w2, w2_sf, None, None, None, T, E, D, H, k, dtype)
     st = lib().moe_ffn_forward_host(

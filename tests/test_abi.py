@@ -273,3 +273,30 @@ def test_routing_block_size_option_sizes_the_workspace():
     finally:
         moe.moe_ffn_set_option(moe.MOE_OPT_ROUTE_TPB, 0)
     assert small_blocks >= base + (4096 // 64 - 4096 // 256) * 128 * 4 - 256
+
+
+def test_host_entry_binding_checks_its_host_tensors():
+    # sizes and the host side are checked before any pointer reaches the C ABI
+    import torch
+    T, E, D, H, k = 4, 2, 256, 128, 2
+    x = torch.zeros(T, D, dtype=torch.bfloat16)
+    w1 = torch.zeros(E, 2 * H, D, dtype=torch.bfloat16)
+    w2 = torch.zeros(E, D, H, dtype=torch.bfloat16)
+    ids = torch.zeros(T, k, dtype=torch.int32)
+    tw = torch.zeros(T, k)
+    out = torch.zeros(T, D, dtype=torch.bfloat16)
+    ws = torch.zeros(1 << 20, dtype=torch.uint8)
+    A = 1 << 20  # device weights as raw addresses (no GPU here); never reached: a host check fails first
+    call = lambda **kw: moe.moe_ffn_forward_host(kw.get("x", x), A, A, kw.get("ids", ids), kw.get("tw", tw),
+                                                 kw.get("out", out), E=E, D=D, H=H, k=k, workspace=A)
+    with pytest.raises(ValueError, match="out"):
+        call(out=torch.zeros(T, D - 1, dtype=torch.bfloat16))      # short output
+    with pytest.raises(ValueError, match="topk_ids"):
+        call(ids=torch.zeros(T, k - 1, dtype=torch.int32))
+    with pytest.raises(ValueError, match="contiguous"):
+        call(x=torch.zeros(D, T, dtype=torch.bfloat16).t())
+    with pytest.raises(ValueError, match="T is required"):
+        call(x=1 << 20)                                             # a raw address carries no shape
+    with pytest.raises(ValueError, match="w2"):                     # weight sizes are checked like moe_ffn_forward's
+        moe.moe_ffn_forward_host(x, w1, torch.zeros(E, D, H - 1, dtype=torch.bfloat16), ids, tw, out,
+                                 E=E, D=D, H=H, k=k, workspace=ws)
